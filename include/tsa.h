@@ -1,0 +1,207 @@
+/*
+ * tsa.h -- C ABI of libtsa: decode-step top-K sparse attention on one GB300.
+ *
+ * One decode step of one attention layer: for every query head, score the
+ * query against every key of the cache, keep the exact top-K keys outside a
+ * static window of initial + recent tokens, attend over those K rows and over
+ * the window separately, and merge the two partial results with the
+ * log-sum-exp rescale.  A second entry point runs ReTopK's reuse path, which
+ * recalls candidate keys from a per-head cache of past queries instead of
+ * scanning every key on most steps.
+ *
+ * Sources (page title, section / equation):
+ *   [RA]  "RetrievalAttention: Accelerating Long-Context LLM Inference via
+ *         Vector Retrieval": Eq. 1, Eq. 2, Eq. 3, Eq. 4-5, the "Flat"
+ *         exact-KNN baseline, "CPU-GPU Co-Execution" (static pattern W),
+ *         Appendix B.2 Algorithm 1 (per-step window update).
+ *   [RTK] "Recall Before You Rank: Similarity-Guided Top-K Reuse for
+ *         Efficient Long-Context Attention" (ReTopK): sections 1-5 of the
+ *         method (query-support cache, similar-query recall, candidate set,
+ *         exact re-ranking, fallback and refresh) and "GPU Kernel".
+ *
+ * Conventions shared by every entry point
+ *   - Element types: q, K, V are bf16 (IEEE binary16-brain, 2 bytes);
+ *     outputs are fp32; indices are int32 token positions (0-based).
+ *   - Head dimension d must be 128 (the only compiled size).
+ *   - GQA: query head h reads KV head h / (Hq / Hkv); Hq % Hkv == 0 and
+ *     Hq / Hkv <= 8.
+ *   - Ownership: the caller allocates every buffer (device memory unless
+ *     stated) and the workspace, and owns the stream.  No entry point
+ *     allocates, frees, synchronises or prints; launches are asynchronous
+ *     on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *   - Errors: every call returns a tsa_status.  Arguments are validated on
+ *     the host before any launch; on an error nothing is launched and
+ *     tsa_last_error() describes the problem (thread-local).  Launch
+ *     failures are reported as TSA_ERR_CUDA.  Faults inside a kernel surface
+ *     through the stream as usual CUDA errors.
+ *   - Concurrency: calls that share a workspace or a ReTopK state must be
+ *     ordered on one stream.
+ */
+#ifndef TSA_H
+#define TSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum tsa_status {
+  TSA_OK = 0,
+  TSA_ERR_INVALID_ARG = -1, /* a size, pointer or layout argument is invalid */
+  TSA_ERR_WORKSPACE = -2,   /* workspace pointer NULL/misaligned or too small */
+  TSA_ERR_CUDA = -3,        /* a CUDA runtime call or launch failed           */
+  TSA_ERR_STATE = -4,       /* ReTopK state handle invalid or not initialised */
+  TSA_ERR_DEVICE_CHECK = -5,/* a device-side check flagged bad input          */
+  TSA_ERR_TIMEOUT = -6      /* reserved: a bounded device wait expired        */
+} tsa_status;
+
+/* KV cache of one layer.
+ *
+ * Contiguous layout (page_table == NULL):
+ *   k, v: bf16 [B][Hkv][l_cap][128]; sequence b, KV head g, position i at
+ *   element ((b*Hkv + g)*l_cap + i)*128.
+ * Paged layout (page_table != NULL):
+ *   k, v: bf16 [num_pages][Hkv][page_size][128]; page_table: int32
+ *   [B][max_pages] (device); position i of sequence b lives in page
+ *   page_table[b*max_pages + i/page_size] at row i % page_size.
+ *   page_size is a power of two in [16, 256]; l_cap = max_pages*page_size.
+ * Base pointers must be 16-byte aligned.  Positions >= the sequence length
+ * are never read. */
+typedef struct tsa_kv {
+  const void* k;
+  const void* v;
+  const int32_t* page_table;
+  int32_t page_size;
+  int32_t max_pages;
+  int64_t l_cap;
+} tsa_kv;
+
+/* Human-readable description of the last error on this thread ("" if none). */
+const char* tsa_last_error(void);
+
+/* Version string of the library build. */
+const char* tsa_version(void);
+
+/* ------------------------------------------------------------------ */
+/* sparse_attn_decode -- [RA] Eq. 1-5 with an exact ("Flat") top-K Omega.
+ *
+ * For each sequence b (length L_b = lens[b], the newest token included)
+ * and query head h:
+ *   z_i   = scale * q_h . k_i                       for i < L_b   (Eq. 1)
+ *   W     = [0, n_init) u [L_b - n_recent, L_b), clipped        (static W)
+ *   Omega = the K positions of [0, L_b) \ W with the largest z,
+ *           ties to the smaller position; all of it if smaller than K
+ *   o_W, o_Omega: softmax-weighted V over W and Omega (Eq. 3)
+ *   out   = g1 o_W + g2 o_Omega, lse = log sum_{W u Omega} e^z  (Eq. 4-5)
+ *
+ * q:          bf16 [B][Hq][128] (device)
+ * kv:         the cache (see tsa_kv); read only
+ * lens:       int32 [B] (device), 0 <= lens[b] <= kv->l_cap
+ * K:          top-K budget (>= 0); n_init, n_recent >= 0
+ * scale:      logit scale (1/sqrt(128) for standard attention)
+ * out:        fp32 [B][Hq][128] (device)
+ * lse_out:    fp32 [B][Hq] or NULL; -inf when W u Omega is empty
+ * topk_idx:   int32 [B][Hq][K] or NULL: Omega in unspecified order, padded
+ *             with -1 when fewer than K positions exist
+ * topk_score: fp32 [B][Hq][K] or NULL: z of topk_idx (padding: -inf)
+ * workspace:  device scratch of at least tsa_decode_workspace_size() bytes,
+ *             256-byte aligned; its contents need no initialisation and are
+ *             overwritten by every call
+ * Returns TSA_OK or an error; see the conventions above. */
+size_t tsa_decode_workspace_size(int B, int Hq, int Hkv, int d, int64_t l_cap,
+                                 int K, int n_init, int n_recent);
+
+int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens,
+                       int B, int Hq, int Hkv, int d, int K, int n_init,
+                       int n_recent, float scale, float* out, float* lse_out,
+                       int32_t* topk_idx, float* topk_score, void* workspace,
+                       size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------ */
+/* lse_merge -- [RA] Eq. 4-5 on precomputed partials.
+ *
+ * For each row r < rows, merges two attention partials over disjoint key
+ * sets, each given as (o, lse) with lse = log sum e^z over its set:
+ *   lse = log(e^lse_a + e^lse_b)
+ *   o   = e^(lse_a - lse) o_a + e^(lse_b - lse) o_b
+ * A partial with lse = -inf is empty and gets weight 0; if both are empty
+ * the row's o is 0 and lse is -inf.
+ * o_a, o_b, o_out: fp32 [rows][d]; lse_a, lse_b, lse_out: fp32 [rows]
+ * (device).  o_out may alias o_a or o_b; lse_out may alias lse_a or lse_b.
+ * d: 1 .. 1024. */
+int lse_merge(const float* o_a, const float* lse_a, const float* o_b,
+              const float* lse_b, float* o_out, float* lse_out, int rows,
+              int d, void* stream);
+
+/* ------------------------------------------------------------------ */
+/* ReTopK -- [RTK] per-head query-support reuse for one sequence.
+ *
+ * State (per layer): for every query head a FIFO of C entries (qbar, S):
+ * qbar a normalised past query (fp32 [128]), S its final top-K positions.
+ * Step t (counted from 0 by the state) with query q and cache length L_t:
+ *   qbar_t = q / |q|;  rho_c = qbar_t . qbar_c  for the C entries
+ *   exact path if max rho < tau  or  t % T_r == 0:
+ *       S_t = exact top-K of all L_t keys (no window)
+ *   reuse path otherwise:
+ *       R_t = the R entries of largest rho (ties: older entry first)
+ *       A_t = Unique(U_{c in R_t} S_c  u  [L_t - W, L_t))      (ascending)
+ *       S_t = top-K of A_t by e_i = scale * q . k_i (ties: smaller
+ *             position); all of A_t when |A_t| <= K
+ *   out = softmax(e_{S_t}) . V_{S_t}   (no window merge)
+ *   push (qbar_t, S_t) into the FIFO, evicting the oldest entry.
+ *
+ * The state lives in caller-owned device memory of retopk_state_size()
+ * bytes (256-byte aligned); the opaque host handle holds sizes, pointers,
+ * the step counter and the FIFO head. */
+typedef struct tsa_retopk tsa_retopk;
+
+size_t retopk_state_size(int Hq, int d, int K, int C);
+
+/* Create a handle over `state_mem`.  Hyper-parameters: 1 <= R <= C <= 64,
+ * K >= 1, W >= 0, T_r >= 1, tau any float (tau > 1: always exact;
+ * tau <= -1 with a large T_r: reuse after step 0).  max_len bounds every
+ * later L_t (it sizes the candidate bitmap, <= 1<<21).  Nothing is launched. */
+int retopk_create(tsa_retopk** st, int Hq, int Hkv, int d, int K, int C,
+                  int R, int W, float tau, int T_r, int64_t max_len,
+                  void* state_mem, size_t state_bytes);
+
+/* Fill the FIFO from the last C prefill queries: prefill_q bf16 [C][Hq][128]
+ * (row c is the query of prefill position L0-C+c; c = 0 is the oldest
+ * entry) and their supports prefill_supports int32 [C][Hq][K] with sizes
+ * prefill_counts int32 [C][Hq] (entries past a count are ignored).  All
+ * device pointers.  Resets the step counter to 0. */
+int retopk_init(tsa_retopk* st, const void* prefill_q,
+                const int32_t* prefill_supports, const int32_t* prefill_counts,
+                void* stream);
+
+/* Workspace needed by retopk_step for caches up to max_len keys. */
+size_t retopk_workspace_size(const tsa_retopk* st);
+
+/* One decode step (see above).  q: bf16 [Hq][128]; kv: this layer's cache
+ * with B = 1 (lens are the host value `len`, 1 <= len <= min(kv->l_cap,
+ * max_len)); out: fp32 [Hq][128].  Optional outputs (NULL to skip):
+ *   support_out int32 [Hq][K] (S_t, unspecified order, -1 padded),
+ *   path_out int32 [Hq] (1 exact, 0 reuse),
+ *   mcand_out int32 [Hq] (|A_t| on the reuse path, len on the exact path),
+ *   cand_out int32 [Hq][R*K+W] (A_t ascending, -1 padded; reuse heads only),
+ *   lse_out fp32 [Hq].
+ * Advances the step counter and the FIFO head. */
+int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len,
+                float scale, float* out, int32_t* support_out,
+                int32_t* path_out, int32_t* mcand_out, int32_t* cand_out,
+                float* lse_out, void* workspace, size_t ws_bytes,
+                void* stream);
+
+/* Host-side counters of the handle (for checkpointing). */
+int retopk_get_counters(const tsa_retopk* st, int64_t* t, int32_t* fifo_head);
+int retopk_set_counters(tsa_retopk* st, int64_t t, int32_t fifo_head);
+
+/* Free the host handle only; the state memory belongs to the caller. */
+int retopk_destroy(tsa_retopk* st);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
