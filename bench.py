@@ -1,0 +1,396 @@
+"""Benchmark: microseconds per decode layer-step (and the scan's HBM roofline).
+
+One step = one decode layer-step of the whole hot path (key scan, exact top-K,
+split-K softmax.V over the selected rows and the window, gamma merge) through
+the C ABI, on seeded synthetic data shaped like the pages' workloads.  The
+default workload is the Llama-3-8B layer at 128K context (32 query / 8 KV
+heads, K = 2048, window 128 + 512); --workload picks another one.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the test oracle, as it stands) on
+a bounded sample of the same workload, on the host cores.
+
+Under torchrun (N > 1) every rank runs its own replica of the layer-step
+(independent problems, no data-path collective): scaling is weak and the
+value is the aggregate microseconds per layer-step over all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "us per decode layer-step (scan + top-K + gather + merge)"
+UNIT = "us/layer-step"
+L2_BYTES = 126 * 1024 * 1024
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, ws: int, device=None) -> float:
+    """Maximum of a per-rank scalar (timing plumbing only)."""
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, ws: int, device=None) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j.get("hbm_gbs", 6800.0)), "measured"
+    return 6800.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workloads
+def algorithmic_bytes(wl) -> dict:
+    """Bytes the method must move per layer-step: every K row of the cache once
+    per KV head, the V rows of the selected set per query head and of the window
+    per query head, q in and the fp32 output out."""
+    d = wl.d
+    lens = wl.lens(0)
+    k_bytes = sum(lens) * wl.Hkv * d * 2
+    win = sum(min(wl.n_init + wl.n_recent, L) for L in lens)
+    pool = [L - min(wl.n_init + wl.n_recent, L) for L in lens]
+    sel = sum(min(wl.K, p) for p in pool)
+    v_bytes = (sel + win) * wl.Hq * d * 2
+    io = wl.B * wl.Hq * d * (2 + 4)
+    return {"scan": k_bytes, "gather": v_bytes, "io": io, "total": k_bytes + v_bytes + io}
+
+
+def run_ours(args, ws, rank, local):
+    import torch
+    import top_retrieval_sparse_gb300 as tsa
+    from workloads.gen import make_decode
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    name = args.workload
+    wl = make_decode(name, device=dev, seed=rank)  # each rank: its own replica
+    paged = wl.page_table is not None
+    kv = (tsa.kv_paged(wl.k_pages, wl.v_pages, wl.page_table) if paged
+          else tsa.kv_contiguous(wl.k, wl.v))
+    if paged:  # the contiguous copy is not needed on the device
+        wl.k = wl.k.cpu() if args.cpu_baseline else None
+        wl.v = wl.v.cpu() if args.cpu_baseline else None
+        torch.cuda.empty_cache()
+    B, Hq, d, K = wl.B, wl.Hq, wl.d, wl.K
+    nb = tsa.decode_workspace_size(B, Hq, wl.Hkv, d, kv.l_cap, K, wl.n_init, wl.n_recent)
+    work = torch.empty(nb, dtype=torch.uint8, device=dev)
+    out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    lens_all = torch.tensor([wl.lens(t) for t in range(wl.steps)], dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        t = i % wl.steps
+        tsa.sparse_attn_decode(wl.q_all[t], kv, lens_all[t], K, wl.n_init, wl.n_recent,
+                               wl.scale, out=out, lse_out=lse, workspace=work, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    # ---- device-timed region (per-stage events on the launching stream) ----
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = Clocks(torch.cuda.current_device() if ws == 1 else local)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        tsa.set_stage_events(ev[i])
+        step(args.warmup + i)
+    tsa.set_stage_events(None)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    total_ms = t0.elapsed_time(t1)
+    total_ms = max_over_ranks(total_ms, ws, dev)
+    scan_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    sel_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    att_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    ms_per_step = total_ms / args.steps
+    us_per_layer_step = 1000.0 * ms_per_step / ws  # aggregate over all replicas
+
+    ab = algorithmic_bytes(wl)
+    hbm, peak_kind = peaks()
+    scan_avg = statistics.mean(scan_ms)
+    achieved = ab["scan"] / (scan_avg * 1e-3) / 1e9
+    path_gbs = ab["total"] / (ms_per_step * 1e-3) / 1e9
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = run_e2e(args, wl, kv, work, tsa, torch, dev)
+
+    res = {
+        "metric": METRIC, "value": round(us_per_layer_step, 3), "unit": UNIT,
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 in, fp32 accumulate/out", "data": "synthetic",
+        "config": {
+            "workload": name, "B": B, "Hq": Hq, "Hkv": wl.Hkv, "d": d,
+            "context": wl.L0 if B > 1 else wl.L0[0], "K": K,
+            "window": [wl.n_init, wl.n_recent], "layout": "paged16" if paged else "contiguous",
+            "decode_steps_cycled": wl.steps,
+            "l2": f"inputs larger than L2 (K cache {ab['scan'] / 2**20:.0f} MiB > 126 MiB); no flush",
+            "parallelism": f"replicas{ws}" if ws > 1 else "single",
+        },
+        "stages_ms": {"scan": round(scan_avg, 5), "select": round(statistics.mean(sel_ms), 5),
+                      "attend+merge": round(statistics.mean(att_ms), 5)},
+        "path_algorithmic_gbs": round(path_gbs, 1),
+        "roofline": {"kernel": "scan_kernel (GQA key scan + pass-1 histogram)",
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "frac_of_8tbs": round(achieved / 8000.0, 4),
+                     "traffic": None, "algorithmic_bytes_per_launch": ab["scan"]},
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    if args.cpu_baseline and rank == 0:
+        res["cpu_baseline"] = oracle_baseline(wl, budget_s=args.cpu_budget)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return res if rank == 0 else None
+
+
+def run_e2e(args, wl, kv, work, tsa, torch, dev):
+    """Per step: pinned host -> device copy of the step's query, its appended
+    K/V token rows and the lengths; the decode call; device -> host read of the
+    output and lse.  Wall-clock per step, synchronised."""
+    B, Hq, d, G = wl.B, wl.Hq, wl.d, wl.Hq // wl.Hkv
+    q_host = wl.q_all.cpu().pin_memory()
+    lens_host = torch.tensor([wl.lens(t) for t in range(wl.steps)], dtype=torch.int32).pin_memory()
+    paged = wl.page_table is not None
+    # the token appended at step t sits at row L0+t; keep host copies of those rows
+    if paged:
+        tok_k = torch.zeros((wl.steps, B, wl.Hkv, d), dtype=torch.bfloat16)
+        tok_v = torch.zeros_like(tok_k)
+        pt = wl.page_table.cpu()
+        for t in range(wl.steps):
+            for b in range(B):
+                pos = wl.L0[b] + t
+                page = int(pt[b, pos // wl.page_size])
+                tok_k[t, b] = wl.k_pages[page, :, pos % wl.page_size].cpu()
+                tok_v[t, b] = wl.v_pages[page, :, pos % wl.page_size].cpu()
+    else:
+        idx = torch.tensor([[l0 + t for l0 in wl.L0] for t in range(wl.steps)])
+        tok_k = torch.stack([torch.stack([wl.k[b, :, int(idx[t, b])].cpu() for b in range(B)])
+                             for t in range(wl.steps)])
+        tok_v = torch.stack([torch.stack([wl.v[b, :, int(idx[t, b])].cpu() for b in range(B)])
+                             for t in range(wl.steps)])
+    tok_k, tok_v = tok_k.pin_memory(), tok_v.pin_memory()
+    q_dev = torch.empty((B, Hq, d), dtype=torch.bfloat16, device=dev)
+    lens_dev = torch.empty((B,), dtype=torch.int32, device=dev)
+    out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    out_host = torch.empty((B, Hq, d), dtype=torch.float32).pin_memory()
+    lse_host = torch.empty((B, Hq), dtype=torch.float32).pin_memory()
+    pt_host = wl.page_table.cpu() if paged else None
+
+    def one(i):
+        t = i % wl.steps
+        q_dev.copy_(q_host[t], non_blocking=True)
+        lens_dev.copy_(lens_host[t], non_blocking=True)
+        for b in range(B):  # append this step's token rows
+            pos = wl.L0[b] + t
+            if paged:
+                page = int(pt_host[b, pos // wl.page_size])
+                wl.k_pages[page, :, pos % wl.page_size].copy_(tok_k[t, b], non_blocking=True)
+                wl.v_pages[page, :, pos % wl.page_size].copy_(tok_v[t, b], non_blocking=True)
+            else:
+                wl.k[b, :, pos].copy_(tok_k[t, b], non_blocking=True)
+                wl.v[b, :, pos].copy_(tok_v[t, b], non_blocking=True)
+        tsa.sparse_attn_decode(q_dev, kv, lens_dev, wl.K, wl.n_init, wl.n_recent, wl.scale,
+                               out=out, lse_out=lse, workspace=work)
+        out_host.copy_(out, non_blocking=True)
+        lse_host.copy_(lse, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for i in range(args.warmup):
+        one(i)
+    n = args.steps
+    t0 = time.perf_counter()
+    for i in range(n):
+        one(args.warmup + i)
+    dt = time.perf_counter() - t0
+    h2d = q_host[0].numel() * 2 + B * 4 + 2 * B * wl.Hkv * d * 2
+    d2h = out_host.numel() * 4 + lse_host.numel() * 4
+    return {"value": round(1e6 * dt / n, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+def oracle_baseline(wl, budget_s=12.0, steps=1):
+    """fp64 single-threaded oracle on a bounded sample: whole query heads of
+    decode step 0, as many as fit the time budget, scaled to one layer-step."""
+    import oracle as orc
+    from workloads.gen import bits
+    G = wl.Hq // wl.Hkv
+    done, t_used = 0, 0.0
+    L = wl.lens(0)
+    order = [(b, h) for b in range(wl.B) for h in range(wl.Hq)]
+    kcache = {}
+    for b, h in order:
+        key = (b, h // G)
+        if key not in kcache:
+            kcache.clear()
+            src_k = wl.k if wl.k is not None else None
+            kcache[key] = (bits(src_k[b, h // G, :L[b]]), bits(wl.v[b, h // G, :L[b]]))
+        kb, vb = kcache[key]
+        qb = bits(wl.q(0)[b, h])
+        t0 = time.perf_counter()
+        orc.decode_head(qb, kb, vb, wl.K, wl.n_init, wl.n_recent, wl.scale)
+        t_used += time.perf_counter() - t0
+        done += 1
+        if t_used >= budget_s:
+            break
+    per_head = t_used / done
+    return {"value": round(1e6 * per_head * wl.B * wl.Hq, 1), "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": f"{done} of {wl.B * wl.Hq} (sequence, query head) pairs of decode step 0, "
+                      f"{t_used:.1f} s, scaled to a whole layer-step"}
+
+
+def run_reference(args, ws, rank):
+    """The reference arm: the fp64 oracle on the host cores, bounded sample."""
+    if rank != 0:
+        return None
+    import torch
+    from workloads.gen import make_decode
+    wl = make_decode(args.workload, device="cpu")
+    per_step_budget = max(0.5, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_baseline(wl, budget_s=per_step_budget * 0.25)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(oracle_baseline(wl, budget_s=per_step_budget))
+    dt = time.perf_counter() - t0
+    v = statistics.mean(x["value"] for x in vals)
+    del torch
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": UNIT,
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1000 * dt / args.steps, 3), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload},
+        "cpu_baseline": {"value": round(v, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": vals[-1]["sample"]},
+        "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="llama128k",
+                    choices=["tiny", "llama128k", "llama1m", "yi_paged"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, ws, rank)
+    else:
+        res = run_ours(args, ws, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

@@ -43,6 +43,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define TSA_API __attribute__((visibility("default")))
+#else
+#define TSA_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -79,10 +85,20 @@ typedef struct tsa_kv {
 } tsa_kv;
 
 /* Human-readable description of the last error on this thread ("" if none). */
-const char* tsa_last_error(void);
+TSA_API const char* tsa_last_error(void);
 
 /* Version string of the library build. */
-const char* tsa_version(void);
+TSA_API const char* tsa_version(void);
+
+/* Per-stage timing (optional, thread-local).  With n >= 4 cudaEvent_t
+ * handles (cast to void*), every later sparse_attn_decode / retopk_step call
+ * on this thread records events[0] after zeroing its workspace counters
+ * (just before the first kernel), events[1] after
+ * the key scan, events[2] after the top-K selection (retopk_step: after the
+ * rescoring) and events[3] after the attention/merge kernel, on the call's
+ * stream.  events == NULL (or n == 0) turns it off.  The events stay owned by
+ * the caller. */
+TSA_API int tsa_set_stage_events(void* const* events, int n);
 
 /* ------------------------------------------------------------------ */
 /* sparse_attn_decode -- [RA] Eq. 1-5 with an exact ("Flat") top-K Omega.
@@ -110,10 +126,10 @@ const char* tsa_version(void);
  *             256-byte aligned; its contents need no initialisation and are
  *             overwritten by every call
  * Returns TSA_OK or an error; see the conventions above. */
-size_t tsa_decode_workspace_size(int B, int Hq, int Hkv, int d, int64_t l_cap,
+TSA_API size_t tsa_decode_workspace_size(int B, int Hq, int Hkv, int d, int64_t l_cap,
                                  int K, int n_init, int n_recent);
 
-int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens,
+TSA_API int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens,
                        int B, int Hq, int Hkv, int d, int K, int n_init,
                        int n_recent, float scale, float* out, float* lse_out,
                        int32_t* topk_idx, float* topk_score, void* workspace,
@@ -131,7 +147,7 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens,
  * o_a, o_b, o_out: fp32 [rows][d]; lse_a, lse_b, lse_out: fp32 [rows]
  * (device).  o_out may alias o_a or o_b; lse_out may alias lse_a or lse_b.
  * d: 1 .. 1024. */
-int lse_merge(const float* o_a, const float* lse_a, const float* o_b,
+TSA_API int lse_merge(const float* o_a, const float* lse_a, const float* o_b,
               const float* lse_b, float* o_out, float* lse_out, int rows,
               int d, void* stream);
 
@@ -157,13 +173,13 @@ int lse_merge(const float* o_a, const float* lse_a, const float* o_b,
  * the step counter and the FIFO head. */
 typedef struct tsa_retopk tsa_retopk;
 
-size_t retopk_state_size(int Hq, int d, int K, int C);
+TSA_API size_t retopk_state_size(int Hq, int d, int K, int C);
 
 /* Create a handle over `state_mem`.  Hyper-parameters: 1 <= R <= C <= 64,
  * K >= 1, W >= 0, T_r >= 1, tau any float (tau > 1: always exact;
  * tau <= -1 with a large T_r: reuse after step 0).  max_len bounds every
  * later L_t (it sizes the candidate bitmap, <= 1<<21).  Nothing is launched. */
-int retopk_create(tsa_retopk** st, int Hq, int Hkv, int d, int K, int C,
+TSA_API int retopk_create(tsa_retopk** st, int Hq, int Hkv, int d, int K, int C,
                   int R, int W, float tau, int T_r, int64_t max_len,
                   void* state_mem, size_t state_bytes);
 
@@ -172,12 +188,12 @@ int retopk_create(tsa_retopk** st, int Hq, int Hkv, int d, int K, int C,
  * entry) and their supports prefill_supports int32 [C][Hq][K] with sizes
  * prefill_counts int32 [C][Hq] (entries past a count are ignored).  All
  * device pointers.  Resets the step counter to 0. */
-int retopk_init(tsa_retopk* st, const void* prefill_q,
+TSA_API int retopk_init(tsa_retopk* st, const void* prefill_q,
                 const int32_t* prefill_supports, const int32_t* prefill_counts,
                 void* stream);
 
 /* Workspace needed by retopk_step for caches up to max_len keys. */
-size_t retopk_workspace_size(const tsa_retopk* st);
+TSA_API size_t retopk_workspace_size(const tsa_retopk* st);
 
 /* One decode step (see above).  q: bf16 [Hq][128]; kv: this layer's cache
  * with B = 1 (lens are the host value `len`, 1 <= len <= min(kv->l_cap,
@@ -188,18 +204,18 @@ size_t retopk_workspace_size(const tsa_retopk* st);
  *   cand_out int32 [Hq][R*K+W] (A_t ascending, -1 padded; reuse heads only),
  *   lse_out fp32 [Hq].
  * Advances the step counter and the FIFO head. */
-int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len,
+TSA_API int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len,
                 float scale, float* out, int32_t* support_out,
                 int32_t* path_out, int32_t* mcand_out, int32_t* cand_out,
                 float* lse_out, void* workspace, size_t ws_bytes,
                 void* stream);
 
 /* Host-side counters of the handle (for checkpointing). */
-int retopk_get_counters(const tsa_retopk* st, int64_t* t, int32_t* fifo_head);
-int retopk_set_counters(tsa_retopk* st, int64_t t, int32_t fifo_head);
+TSA_API int retopk_get_counters(const tsa_retopk* st, int64_t* t, int32_t* fifo_head);
+TSA_API int retopk_set_counters(tsa_retopk* st, int64_t t, int32_t fifo_head);
 
 /* Free the host handle only; the state memory belongs to the caller. */
-int retopk_destroy(tsa_retopk* st);
+TSA_API int retopk_destroy(tsa_retopk* st);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,133 @@
+"""The C-ABI library builds, loads and exports every symbol include/tsa.h
+declares; host-side validation rejects bad arguments without touching a device
+(these checks never launch, so they run without a GPU)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "tsa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "sizeof")))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import top_retrieval_sparse_gb300 as tsa
+    return tsa.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"sparse_attn_decode", "lse_merge", "retopk_step", "retopk_create",
+            "retopk_init", "tsa_decode_workspace_size"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"libtsa.so does not export {n}"
+
+
+def test_library_is_in_tree(lib):
+    import top_retrieval_sparse_gb300 as tsa
+    assert tsa.library_path().startswith(ROOT)
+    assert lib.tsa_version().decode().startswith("tsa")
+
+
+FAKE = C.c_void_p(1 << 20)  # aligned, never dereferenced: validation fails first
+
+
+def _kv(tsa, l_cap=1024, page_table=None, page_size=0, max_pages=0):
+    return tsa._KvStruct(1 << 20, 1 << 21, page_table, page_size, max_pages, l_cap)
+
+
+def _decode(lib, tsa, **kw):
+    a = dict(q=FAKE, kv=_kv(tsa), lens=FAKE, B=1, Hq=8, Hkv=2, d=128, K=16, n_init=4,
+             n_recent=8, scale=0.1, out=FAKE, lse=None, idx=None, sc=None, ws=FAKE,
+             ws_bytes=1 << 40, stream=None)
+    a.update(kw)
+    return lib.sparse_attn_decode(a["q"], C.byref(a["kv"]), a["lens"], a["B"], a["Hq"],
+                                  a["Hkv"], a["d"], a["K"], a["n_init"], a["n_recent"],
+                                  a["scale"], a["out"], a["lse"], a["idx"], a["sc"], a["ws"],
+                                  a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=64), -1),                        # only d = 128 is compiled
+    (dict(Hq=6, Hkv=4), -1),                 # Hq % Hkv
+    (dict(Hq=18, Hkv=2), -1),                # group size 9 > 8
+    (dict(K=-1), -1),
+    (dict(n_init=-2), -1),
+    (dict(q=None), -1),
+    (dict(q=C.c_void_p((1 << 20) + 4)), -1),  # q not 16-byte aligned
+    (dict(scale=float("nan")), -1),
+    (dict(ws=None), -2),
+    (dict(ws=C.c_void_p((1 << 20) + 64)), -2),  # workspace not 256-byte aligned
+    (dict(ws_bytes=100), -2),                   # workspace too small
+])
+def test_decode_validation(lib, kw, code):
+    import top_retrieval_sparse_gb300 as tsa
+    assert _decode(lib, tsa, **kw) == code
+    assert lib.tsa_last_error().decode() != ""
+
+
+def test_decode_validation_paged(lib):
+    import top_retrieval_sparse_gb300 as tsa
+    assert _decode(lib, tsa, kv=_kv(tsa, 1024, 1 << 22, 24, 64)) == -1    # page size 24
+    assert _decode(lib, tsa, kv=_kv(tsa, 1000, 1 << 22, 16, 64)) == -1    # l_cap mismatch
+    assert _decode(lib, tsa, kv=_kv(tsa, 1024, 1 << 22, 16, 0)) == -1
+    k = tsa._KvStruct(None, 1 << 21, None, 0, 0, 1024)
+    assert _decode(lib, tsa, kv=k) == -1
+
+
+def test_workspace_sizes(lib):
+    small = lib.tsa_decode_workspace_size(1, 32, 8, 128, 131136, 2048, 128, 512)
+    big = lib.tsa_decode_workspace_size(1, 32, 8, 128, 1 << 20, 4096, 128, 1024)
+    assert 0 < small < big
+    # scores + candidate positions dominate: 2 x 4 bytes per (head, position)
+    assert big >= 32 * (1 << 20) * 8
+    assert lib.tsa_decode_workspace_size(1, 32, 8, 128, 1000, -1, 0, 0) == 0
+
+
+def test_lse_merge_validation(lib):
+    assert lib.lse_merge(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 0, None) == -1
+    assert lib.lse_merge(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2048, None) == -1
+    assert lib.lse_merge(None, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 16, None) == -1
+    assert lib.lse_merge(None, None, None, None, None, None, 0, 16, None) == 0
+
+
+def test_retopk_host_state_machine(lib):
+    """create / counters / destroy are host-only; step refuses before init."""
+    n = lib.retopk_state_size(28, 128, 512, 32)
+    assert n >= 28 * 32 * (128 + 512 + 1) * 4
+    h = C.c_void_p()
+    assert lib.retopk_create(C.byref(h), 28, 4, 128, 512, 32, 4, 32, 0.85, 128, 70000,
+                             FAKE, n) == 0
+    assert lib.retopk_workspace_size(h) > 28 * 70000 * 8
+    t, head = C.c_int64(), C.c_int32()
+    assert lib.retopk_get_counters(h, C.byref(t), C.byref(head)) == 0
+    assert (t.value, head.value) == (0, 0)
+    import top_retrieval_sparse_gb300 as tsa
+    kv = _kv(tsa, 70000)
+    rc = lib.retopk_step(h, FAKE, C.byref(kv), 100, 0.1, FAKE, None, None, None, None, None,
+                         FAKE, 1 << 40, None)
+    assert rc == -4  # not initialised
+    assert lib.retopk_set_counters(h, 5, 40) == -1   # head outside [0, C)
+    assert lib.retopk_set_counters(h, 5, 3) == 0
+    rc = lib.retopk_step(h, FAKE, C.byref(kv), 70001, 0.1, FAKE, None, None, None, None, None,
+                         FAKE, 1 << 40, None)
+    assert rc == -1  # len beyond max_len
+    rc = lib.retopk_step(h, FAKE, C.byref(kv), 100, 0.1, FAKE, None, None, None, None, None,
+                         FAKE, 10, None)
+    assert rc == -2  # workspace too small
+    assert lib.retopk_destroy(h) == 0
+    bad = C.c_void_p()
+    assert lib.retopk_create(C.byref(bad), 28, 4, 128, 512, 32, 40, 32, 0.85, 128, 70000,
+                             FAKE, n) == -1  # R > C
+    assert lib.retopk_create(C.byref(bad), 28, 4, 128, 512, 32, 4, 32, 0.85, 0, 70000,
+                             FAKE, n) == -1  # T_r < 1
+    assert lib.retopk_create(C.byref(bad), 28, 4, 128, 512, 32, 4, 32, 0.85, 128, 70000,
+                             FAKE, n - 1) == -1  # state too small

@@ -1,0 +1,189 @@
+"""GPU parity of sparse_attn_decode against the fp64 oracle (element by element).
+
+Sizes span several 64-row scan tiles, several 16K-position selection chunks
+and ragged tails; full-size configurations are checked on sampled heads.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import check_head, gpu_decode
+from workloads.gen import make_decode
+
+pytestmark = pytest.mark.gpu
+
+
+def run_and_check(wl, steps, heads=None, K=None):
+    stats = []
+    for t in steps:
+        out, lse, idx, sc = gpu_decode(wl, t, K=K)
+        for b in range(wl.B):
+            for h in (range(wl.Hq) if heads is None else heads):
+                stats.append(check_head(wl, t, b, h, out[b, h], lse[b, h], idx[b, h],
+                                        sc[b, h] if sc.size else None, K=K))
+    return stats
+
+
+def test_tiny_config_all_steps():
+    wl = make_decode("tiny")
+    st = run_and_check(wl, range(wl.steps))
+    assert max(s["zrel"] for s in st) < 1e-5
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 4), (12, 4), (10, 2), (28, 4), (32, 4)])
+def test_group_sizes(Hq, Hkv):
+    wl = make_decode("llama128k", L0=5000 + 3 * Hq, steps=2, B=1, K=100, Hq=Hq, Hkv=Hkv,
+                     n_init=16, n_recent=40, plant_frac=0.01)
+    run_and_check(wl, range(2))
+
+
+def test_llama_geometry_downsized_ragged():
+    wl = make_decode("llama128k", L0=40_001, steps=3)  # K=2048, window 128+512
+    run_and_check(wl, range(3))
+
+
+def test_paged_batched_downsized():
+    wl = make_decode("yi_paged", L0=6000, steps=2, B=5, K=300)
+    assert wl.page_table is not None
+    run_and_check(wl, range(2))
+
+
+def test_paged_matches_contiguous():
+    wl = make_decode("yi_paged", L0=3000, steps=1, B=3, K=200)
+    a = gpu_decode(wl, 0, paged=True)
+    c = gpu_decode(wl, 0, paged=False)
+    for b in range(wl.B):
+        for h in range(wl.Hq):
+            assert set(a[2][b, h].tolist()) == set(c[2][b, h].tolist())
+    np.testing.assert_allclose(a[0], c[0], atol=1e-5, rtol=0)
+
+
+@pytest.mark.parametrize("K", [0, 1, 64, 5000, 100000])
+def test_K_edge_cases(K):
+    """K = 0 (window only), K = 1, K >= |P| (every pool position: full softmax)."""
+    wl = make_decode("tiny", L0=4500, steps=1)
+    run_and_check(wl, [0], K=K)
+
+
+def test_window_covers_cache_and_tiny_lengths():
+    for L0 in (0, 1, 3, 60, 67, 130):
+        wl = make_decode("tiny", L0=L0, steps=1, K=16)
+        run_and_check(wl, [0])
+
+
+def test_zero_length_sequence_in_batch():
+    wl = make_decode("yi_paged", L0=2000, steps=1, B=3, K=50, paged=False)
+    import top_retrieval_sparse_gb300 as tsa
+    dev = "cuda"
+    kv = tsa.kv_contiguous(wl.k.to(dev), wl.v.to(dev))
+    q = wl.q(0).to(dev).contiguous()
+    lens = torch.tensor([0] + wl.lens(0)[1:], dtype=torch.int32, device=dev)
+    lse = torch.empty((wl.B, wl.Hq), device=dev)
+    idx = torch.empty((wl.B, wl.Hq, wl.K), dtype=torch.int32, device=dev)
+    out, _, _, _ = tsa.sparse_attn_decode(q, kv, lens, wl.K, wl.n_init, wl.n_recent,
+                                          wl.scale, lse_out=lse, topk_idx=idx)
+    torch.cuda.synchronize()
+    assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))
+    assert torch.all(idx[0] == -1)
+    o, l, i = out.cpu().numpy(), lse.cpu().numpy(), idx.cpu().numpy()
+    for b in (1, 2):
+        for h in range(0, wl.Hq, 7):
+            check_head(wl, 0, b, h, o[b, h], l[b, h], i[b, h])
+
+
+def test_all_equal_keys_take_lowest_positions():
+    """Every logit ties: the selected set is the K lowest pool positions."""
+    wl = make_decode("tiny", L0=3000, steps=1, K=100)
+    wl.k[:] = wl.k[:, :, :1, :]  # every key equals key 0
+    out, lse, idx, sc = gpu_decode(wl, 0)
+    L = wl.lens(0)[0]
+    pool = [i for i in range(L) if not (i < wl.n_init or i >= L - wl.n_recent)]
+    for h in range(wl.Hq):
+        assert sorted(idx[0, h].tolist()) == pool[: wl.K]
+        check_head(wl, 0, 0, h, out[0, h], lse[0, h], idx[0, h])
+
+
+def test_many_ties_at_threshold():
+    """Keys quantised so that many logits tie exactly around the K-th."""
+    wl = make_decode("tiny", L0=20_000, steps=1, K=500)
+    kf = wl.k.float()
+    wl.k[:] = (torch.round(kf * 2) / 2).to(torch.bfloat16)
+    wl.q_all[:] = (torch.round(wl.q_all.float())).to(torch.bfloat16)
+    run_and_check(wl, [0])
+
+
+def test_repeated_calls_reuse_workspace():
+    """A workspace needs no initialisation: garbage-filled and reused twice."""
+    import top_retrieval_sparse_gb300 as tsa
+    wl = make_decode("tiny", L0=9000, steps=2)
+    dev = "cuda"
+    kv = tsa.kv_contiguous(wl.k.to(dev), wl.v.to(dev))
+    n = tsa.decode_workspace_size(1, wl.Hq, wl.Hkv, 128, wl.lcap, wl.K, wl.n_init, wl.n_recent)
+    ws = torch.full((n,), 0xAB, dtype=torch.uint8, device=dev)
+    for t in (0, 1, 0):
+        q = wl.q(t).to(dev).contiguous()
+        lens = torch.tensor(wl.lens(t), dtype=torch.int32, device=dev)
+        lse = torch.empty((1, wl.Hq), device=dev)
+        idx = torch.empty((1, wl.Hq, wl.K), dtype=torch.int32, device=dev)
+        out, _, _, _ = tsa.sparse_attn_decode(q, kv, lens, wl.K, wl.n_init, wl.n_recent,
+                                              wl.scale, lse_out=lse, topk_idx=idx, workspace=ws)
+        torch.cuda.synchronize()
+        o, l, i = out.cpu().numpy(), lse.cpu().numpy(), idx.cpu().numpy()
+        for h in range(wl.Hq):
+            check_head(wl, t, 0, h, o[0, h], l[0, h], i[0, h])
+
+
+def test_lse_merge_matches_oracle():
+    import oracle as orc
+    import top_retrieval_sparse_gb300 as tsa
+    rng = np.random.default_rng(5)
+    rows, d = 300, 128
+    oa = rng.standard_normal((rows, d)).astype(np.float32)
+    ob = rng.standard_normal((rows, d)).astype(np.float32)
+    la = (5 * rng.standard_normal(rows)).astype(np.float32)
+    lb = (5 * rng.standard_normal(rows)).astype(np.float32)
+    la[::7] = -np.inf
+    lb[::11] = -np.inf
+    dev = "cuda"
+    t = [torch.from_numpy(x).to(dev) for x in (oa, la, ob, lb)]
+    o, l = tsa.lse_merge(*t)
+    # aliasing: write into the first operand
+    o2, l2 = tsa.lse_merge(t[0].clone(), t[1].clone(), t[2], t[3])
+    a0, a1 = t[0].clone(), t[1].clone()
+    tsa.lse_merge(a0, a1, t[2], t[3], o_out=a0, lse_out=a1)
+    torch.cuda.synchronize()
+    o, l = o.cpu().numpy(), l.cpu().numpy()
+    for r in range(rows):
+        # (o, lse) partials as (o, m=lse, l=1) in the oracle's Eq. 4-5 merge
+        ma, ea = (la[r], 1.0) if np.isfinite(la[r]) else (-np.inf, 0.0)
+        mb, eb = (lb[r], 1.0) if np.isfinite(lb[r]) else (-np.inf, 0.0)
+        ro, rl = orc.merge(oa[r].astype(np.float64), ma, ea, ob[r].astype(np.float64), mb, eb)
+        assert np.max(np.abs(o[r] - ro)) < 1e-5
+        assert (np.isneginf(l[r]) and np.isneginf(rl)) or abs(l[r] - rl) < 1e-5
+    np.testing.assert_array_equal(a0.cpu().numpy(), o)
+    np.testing.assert_array_equal(a1.cpu().numpy(), l)
+
+
+# ------------------------------------------------------------ full sizes
+@pytest.mark.slow
+def test_full_llama128k_all_heads():
+    wl = make_decode("llama128k", steps=64)
+    st = run_and_check(wl, [63])
+    print("llama128k: tie-adopted heads", sum(s["verdict"] == 2 for s in st),
+          "max err", max(s["err"] for s in st))
+
+
+@pytest.mark.slow
+def test_full_llama1m_sampled_heads():
+    wl = make_decode("llama1m", steps=16)
+    run_and_check(wl, [15], heads=[0, 9, 22, 31])
+
+
+@pytest.mark.slow
+def test_full_yi_paged_sampled():
+    wl = make_decode("yi_paged")
+    out, lse, idx, sc = gpu_decode(wl, 31)
+    for b, h in [(0, 0), (3, 17), (7, 31), (12, 5), (15, 30)]:
+        check_head(wl, 31, b, h, out[b, h], lse[b, h], idx[b, h])

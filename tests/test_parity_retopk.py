@@ -1,0 +1,150 @@
+"""GPU parity of retopk_step against the ReTopK oracle, run in lockstep.
+
+Per step and head: the path decision, the candidate set A_t (bit-exact) and
+the support S_t (bit-exact up to the near-tie rule) must match the oracle;
+the output must be within 2e-3 max-abs of the oracle evaluated on the support.
+Where the oracle's own decision lies within a rounding margin (|max rho - tau|,
+rho_(R) vs rho_(R+1), the top-K near-tie) it adopts the GPU's choice, so one
+rounding-level tie does not diverge the two caches.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from helpers import OUT_TOL, TIE_REL
+from workloads.gen import bits, make_retopk
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_prefill_supports(tsa, wl, kv, dev):
+    """Exact top-K of each prefill query over its causal prefix (no window),
+    computed with sparse_attn_decode."""
+    Cn, Hq, K = wl.C, wl.Hq, wl.K
+    sup = torch.full((Cn, Hq, K), -1, dtype=torch.int32, device=dev)
+    for c in range(Cn):
+        p = wl.L0 - Cn + c
+        q = wl.q_prefill[c].to(dev)[None].contiguous()
+        lens = torch.tensor([p + 1], dtype=torch.int32, device=dev)
+        idx = torch.empty((1, Hq, K), dtype=torch.int32, device=dev)
+        tsa.sparse_attn_decode(q, kv, lens, K, 0, 0, wl.scale, topk_idx=idx)
+        sup[c] = idx[0]
+    cnt = (sup >= 0).sum(-1).to(torch.int32)
+    return sup, cnt
+
+
+def run_lockstep(wl, steps, check_out=True):
+    import top_retrieval_sparse_gb300 as tsa
+    dev = "cuda"
+    G = wl.Hq // wl.Hkv
+    kv = tsa.kv_contiguous(wl.k.to(dev), wl.v.to(dev))
+    g = tsa.ReTopK(wl.Hq, wl.Hkv, 128, wl.K, wl.C, wl.R, wl.W, wl.tau, wl.T_r, wl.lcap)
+    sup, cnt = gpu_prefill_supports(tsa, wl, kv, dev)
+    g.init(wl.q_prefill.to(dev).contiguous(), sup, cnt)
+
+    kb = [bits(wl.k[0, i]) for i in range(wl.Hkv)]
+    vb = [bits(wl.v[0, i]) for i in range(wl.Hkv)]
+    qpre = bits(wl.q_prefill)
+    o = orc.ReTopK(wl.Hq, 128, wl.K, wl.C, wl.R, wl.W, wl.tau, wl.T_r,
+                   path_abs=1e-5, rho_abs=1e-5, topk_rel=TIE_REL)
+    sup_h, cnt_h = sup.cpu().numpy(), cnt.cpu().numpy()
+    for c in range(wl.C):
+        p = wl.L0 - wl.C + c
+        for h in range(wl.Hq):
+            z = orc.scores(qpre[c, h], kb[h // G][: p + 1], wl.scale)
+            got = sup_h[c, h, : cnt_h[c, h]]
+            verdict = orc.topk_check(z, np.arange(p + 1), wl.K, got, TIE_REL)
+            assert verdict in (1, 2), f"prefill support c={c} h={h} rejected"
+            o.set_slot(h, c, qpre[c, h], got)
+
+    cap = wl.R * wl.K + wl.W
+    so = torch.empty((wl.Hq, wl.K), dtype=torch.int32, device=dev)
+    po = torch.empty((wl.Hq,), dtype=torch.int32, device=dev)
+    mo = torch.empty((wl.Hq,), dtype=torch.int32, device=dev)
+    co = torch.empty((wl.Hq, cap), dtype=torch.int32, device=dev)
+    lo = torch.empty((wl.Hq,), dtype=torch.float32, device=dev)
+    stats = {"exact": 0, "reuse": 0, "adopt_path": 0, "adopt_cand": 0, "tie_sup": 0,
+             "max_err": 0.0, "mcand": []}
+    for t in range(steps):
+        L = wl.length(t)
+        q = wl.q_all[t].to(dev).contiguous()
+        out = g.step(q, kv, L, wl.scale, support_out=so, path_out=po, mcand_out=mo,
+                     cand_out=co, lse_out=lo)
+        torch.cuda.synchronize()
+        out_h, sup_g, path_g = out.cpu().numpy(), so.cpu().numpy(), po.cpu().numpy()
+        m_g, cand_g = mo.cpu().numpy(), co.cpu().numpy()
+        qb = bits(wl.q_all[t])
+        for h in range(wl.Hq):
+            sg = sup_g[h][sup_g[h] >= 0]
+            cg = cand_g[h][: m_g[h]] if path_g[h] == 0 else None
+            if path_g[h] == 0:
+                assert np.all(cand_g[h][m_g[h]:] == -1)
+            r = o.step_head(h, qb[h], kb[h // G][:L], vb[h // G][:L], wl.scale,
+                            other_path=int(path_g[h]), other_cand=cg, other_sup=sg)
+            assert r["path"] == path_g[h], f"t={t} h={h}: path {path_g[h]} vs {r['path']}"
+            if r["path"] == 0:
+                assert r["cand_ok"] in (1, 2), f"t={t} h={h}: candidate set differs"
+                assert m_g[h] == len(r["cand"])
+                assert m_g[h] <= cap
+                stats["mcand"].append(int(m_g[h]))
+            else:
+                assert m_g[h] == L
+            assert r["sup_ok"] in (1, 2), f"t={t} h={h}: support rejected"
+            err = float(np.max(np.abs(out_h[h] - r["out"])))
+            if check_out:
+                assert err <= OUT_TOL, f"t={t} h={h}: out err {err}"
+            stats["max_err"] = max(stats["max_err"], err)
+            stats["exact" if r["path"] else "reuse"] += 1
+            stats["adopt_path"] += r["adopt_path"]
+            stats["adopt_cand"] += r["adopt_cand"]
+            stats["tie_sup"] += r["sup_ok"] == 2
+        o.advance()
+    assert g.counters() == (steps, steps % wl.C)
+    return stats
+
+
+def test_retopk_downsized_lockstep():
+    wl = make_retopk(L0=6000, steps=40, K=64, C=8, R=2, W=8, T_r=16)
+    st = run_lockstep(wl, 40)
+    assert st["reuse"] > 0 and st["exact"] > 0
+    print("retopk downsized:", {k: v for k, v in st.items() if k != "mcand"},
+          "mean M_t", np.mean(st["mcand"]))
+
+
+def test_retopk_fallback_mix():
+    """A slow-moving walk with tau high enough that the fallback fires."""
+    wl = make_retopk(L0=5000, steps=30, K=48, C=6, R=3, W=5, T_r=1000, tau=0.97)
+    st = run_lockstep(wl, 30)
+    assert st["exact"] > wl.Hq  # more than the step-0 refresh
+
+
+def test_retopk_always_exact_matches_decode():
+    """tau > 1: every step takes the exact path == sparse_attn_decode, no window."""
+    import top_retrieval_sparse_gb300 as tsa
+    wl = make_retopk(L0=3000, steps=4, K=40, C=4, R=2, W=4, tau=1.5)
+    dev = "cuda"
+    kv = tsa.kv_contiguous(wl.k.to(dev), wl.v.to(dev))
+    g = tsa.ReTopK(wl.Hq, wl.Hkv, 128, wl.K, wl.C, wl.R, wl.W, wl.tau, wl.T_r, wl.lcap)
+    sup, cnt = gpu_prefill_supports(tsa, wl, kv, dev)
+    g.init(wl.q_prefill.to(dev).contiguous(), sup, cnt)
+    for t in range(wl.steps):
+        L = wl.length(t)
+        q = wl.q_all[t].to(dev).contiguous()
+        so = torch.empty((wl.Hq, wl.K), dtype=torch.int32, device=dev)
+        out = g.step(q, kv, L, wl.scale, support_out=so)
+        idx = torch.empty((1, wl.Hq, wl.K), dtype=torch.int32, device=dev)
+        ref, _, _, _ = tsa.sparse_attn_decode(q[None], kv, torch.tensor([L], dtype=torch.int32,
+                                              device=dev), wl.K, 0, 0, wl.scale, topk_idx=idx)
+        torch.cuda.synchronize()
+        for h in range(wl.Hq):
+            assert set(so[h].tolist()) == set(idx[0, h].tolist())
+        assert torch.max(torch.abs(out - ref[0])).item() < 1e-5
+
+
+@pytest.mark.slow
+def test_retopk_full_config_lockstep():
+    wl = make_retopk()  # Qwen2.5-7B geometry, 64K, C=32 R=4 K=512 W=32 tau=0.85 T_r=128
+    st = run_lockstep(wl, wl.steps)
+    print("retopk64k:", {k: v for k, v in st.items() if k != "mcand"},
+          "mean M_t", float(np.mean(st["mcand"])), "max M_t", max(st["mcand"]))

@@ -1,0 +1,246 @@
+"""Decode-step top-K sparse attention on GB300 (sm_103a).
+
+Thin ctypes binding over ``libtsa.so`` (C ABI in ``include/tsa.h``).  The
+functions keep the library's names (``sparse_attn_decode``, ``lse_merge``,
+``retopk_*``) and only marshal arguments: every step of the computation runs
+in the library's CUDA kernels.  PyTorch supplies device memory and streams.
+
+Importing this package loads the library; if it is missing it is built with
+nvcc, and if that fails the import raises -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import math
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "TsaError", "lib", "KV", "kv_contiguous", "kv_paged", "decode_workspace_size",
+    "sparse_attn_decode", "lse_merge", "ReTopK", "library_path", "set_stage_events",
+]
+
+TSA_OK = 0
+_ERRORS = {-1: "TSA_ERR_INVALID_ARG", -2: "TSA_ERR_WORKSPACE", -3: "TSA_ERR_CUDA",
+           -4: "TSA_ERR_STATE", -5: "TSA_ERR_DEVICE_CHECK", -6: "TSA_ERR_TIMEOUT"}
+
+
+class TsaError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{_ERRORS.get(code, code)}: {msg}")
+        self.code = code
+
+
+class _KvStruct(C.Structure):
+    _fields_ = [("k", C.c_void_p), ("v", C.c_void_p), ("page_table", C.c_void_p),
+                ("page_size", C.c_int32), ("max_pages", C.c_int32), ("l_cap", C.c_int64)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load libtsa.so (building it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            L = C.CDLL(path)
+            P, i32, i64, f32, sz = C.c_void_p, C.c_int, C.c_int64, C.c_float, C.c_size_t
+            L.tsa_last_error.restype = C.c_char_p
+            L.tsa_version.restype = C.c_char_p
+            L.tsa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i64, i32, i32, i32]
+            L.tsa_decode_workspace_size.restype = sz
+            L.sparse_attn_decode.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32, f32,
+                                             P, P, P, P, P, sz, P]
+            L.lse_merge.argtypes = [P, P, P, P, P, P, i32, i32, P]
+            L.retopk_state_size.argtypes = [i32, i32, i32, i32]
+            L.retopk_state_size.restype = sz
+            L.retopk_create.argtypes = [C.POINTER(P), i32, i32, i32, i32, i32, i32, i32, f32,
+                                        i32, i64, P, sz]
+            L.retopk_init.argtypes = [P, P, P, P, P]
+            L.retopk_workspace_size.argtypes = [P]
+            L.retopk_workspace_size.restype = sz
+            L.retopk_step.argtypes = [P, P, P, i64, f32, P, P, P, P, P, P, P, sz, P]
+            L.retopk_get_counters.argtypes = [P, C.POINTER(i64), C.POINTER(C.c_int32)]
+            L.retopk_set_counters.argtypes = [P, i64, C.c_int32]
+            L.retopk_destroy.argtypes = [P]
+            L.tsa_set_stage_events.argtypes = [C.POINTER(P), i32]
+            _lib = L
+    return _lib
+
+
+def _check(rc: int) -> None:
+    if rc != TSA_OK:
+        raise TsaError(rc, lib().tsa_last_error().decode())
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> C.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _want(t: torch.Tensor, dtype, name: str):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def set_stage_events(events) -> None:
+    """Per-stage timing: a list of 4 torch.cuda.Event(enable_timing=True) (or None).
+
+    Later calls on this thread record them before the first launch and after
+    the scan, the selection and the attention kernel, on the call's stream."""
+    if not events:
+        _check(lib().tsa_set_stage_events(None, 0))
+        return
+    arr = (C.c_void_p * len(events))(*[C.c_void_p(e.cuda_event) for e in events])
+    _check(lib().tsa_set_stage_events(arr, len(events)))
+
+
+class KV:
+    """A layer's KV cache as the library sees it (keeps the tensors alive)."""
+
+    def __init__(self, k, v, page_table=None, page_size=0):
+        _want(k, torch.bfloat16, "k")
+        _want(v, torch.bfloat16, "v")
+        self.k, self.v, self.page_table = k, v, page_table
+        if page_table is None:
+            if k.dim() != 4:
+                raise ValueError("contiguous k must be [B][Hkv][l_cap][d]")
+            self.B, self.Hkv, self.l_cap, self.d = k.shape
+            self.struct = _KvStruct(k.data_ptr(), v.data_ptr(), None, 0, 0, self.l_cap)
+        else:
+            _want(page_table, torch.int32, "page_table")
+            if k.dim() != 4:
+                raise ValueError("paged k must be [pages][Hkv][page_size][d]")
+            _, self.Hkv, ps, self.d = k.shape
+            self.B, max_pages = page_table.shape
+            self.l_cap = max_pages * ps
+            self.struct = _KvStruct(k.data_ptr(), v.data_ptr(), page_table.data_ptr(), ps,
+                                    max_pages, self.l_cap)
+
+
+def kv_contiguous(k: torch.Tensor, v: torch.Tensor) -> KV:
+    return KV(k, v)
+
+
+def kv_paged(k_pages: torch.Tensor, v_pages: torch.Tensor, page_table: torch.Tensor) -> KV:
+    return KV(k_pages, v_pages, page_table)
+
+
+def decode_workspace_size(B, Hq, Hkv, d, l_cap, K, n_init, n_recent) -> int:
+    return int(lib().tsa_decode_workspace_size(B, Hq, Hkv, d, l_cap, K, n_init, n_recent))
+
+
+def sparse_attn_decode(q: torch.Tensor, kv: KV, lens: torch.Tensor, K: int, n_init: int,
+                       n_recent: int, scale: Optional[float] = None,
+                       out: Optional[torch.Tensor] = None,
+                       lse_out: Optional[torch.Tensor] = None,
+                       topk_idx: Optional[torch.Tensor] = None,
+                       topk_score: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None, stream=None):
+    """One decode step over every sequence and query head (see include/tsa.h).
+
+    q: bf16 [B][Hq][d] on the device; lens: int32 [B] on the device.
+    Returns (out, lse_out, topk_idx, topk_score) (the optional ones may be None).
+    """
+    _want(q, torch.bfloat16, "q")
+    _want(lens, torch.int32, "lens")
+    B, Hq, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        nb = decode_workspace_size(B, Hq, kv.Hkv, d, kv.l_cap, K, n_init, n_recent)
+        workspace = torch.empty(max(nb, 256), dtype=torch.uint8, device=q.device)
+    _check(lib().sparse_attn_decode(
+        _p(q), C.byref(kv.struct), _p(lens), B, Hq, kv.Hkv, d, K, n_init, n_recent,
+        float(scale), _p(out), _p(lse_out), _p(topk_idx), _p(topk_score), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out, lse_out, topk_idx, topk_score
+
+
+def lse_merge(o_a, lse_a, o_b, lse_b, o_out=None, lse_out=None, stream=None):
+    """Eq. 4-5 merge of two (o, lse) partials: o fp32 [rows][d], lse fp32 [rows]."""
+    rows, d = o_a.shape
+    if o_out is None:
+        o_out = torch.empty_like(o_a)
+    if lse_out is None:
+        lse_out = torch.empty_like(lse_a)
+    for t, n in ((o_a, "o_a"), (o_b, "o_b"), (o_out, "o_out"), (lse_a, "lse_a"),
+                 (lse_b, "lse_b"), (lse_out, "lse_out")):
+        _want(t, torch.float32, n)
+    _check(lib().lse_merge(_p(o_a), _p(lse_a), _p(o_b), _p(lse_b), _p(o_out), _p(lse_out),
+                           rows, d, _stream(stream)))
+    return o_out, lse_out
+
+
+class ReTopK:
+    """ReTopK per-layer state (query-support FIFO per head) on the device."""
+
+    def __init__(self, Hq, Hkv, d, K, C_, R, W, tau, T_r, max_len, device="cuda"):
+        n = int(lib().retopk_state_size(Hq, d, K, C_))
+        if n == 0:
+            raise TsaError(-1, "invalid ReTopK sizes")
+        self.state = torch.zeros(n, dtype=torch.uint8, device=device)
+        self.handle = C.c_void_p()
+        _check(lib().retopk_create(C.byref(self.handle), Hq, Hkv, d, K, C_, R, W, float(tau),
+                                   T_r, max_len, _p(self.state), n))
+        self.Hq, self.Hkv, self.d, self.K, self.C, self.R, self.W = Hq, Hkv, d, K, C_, R, W
+        self.cand_cap = R * K + W
+        self.workspace = torch.empty(int(lib().retopk_workspace_size(self.handle)),
+                                     dtype=torch.uint8, device=device)
+
+    def __del__(self):
+        try:
+            if self.handle:
+                lib().retopk_destroy(self.handle)
+                self.handle = C.c_void_p()
+        except Exception:
+            pass
+
+    def init(self, prefill_q, prefill_supports, prefill_counts, stream=None):
+        _want(prefill_q, torch.bfloat16, "prefill_q")
+        _want(prefill_supports, torch.int32, "prefill_supports")
+        _want(prefill_counts, torch.int32, "prefill_counts")
+        _check(lib().retopk_init(self.handle, _p(prefill_q), _p(prefill_supports),
+                                 _p(prefill_counts), _stream(stream)))
+
+    def step(self, q, kv: KV, length: int, scale=None, out=None, support_out=None,
+             path_out=None, mcand_out=None, cand_out=None, lse_out=None, stream=None):
+        _want(q, torch.bfloat16, "q")
+        if scale is None:
+            scale = 1.0 / math.sqrt(self.d)
+        if out is None:
+            out = torch.empty((self.Hq, self.d), dtype=torch.float32, device=q.device)
+        _check(lib().retopk_step(self.handle, _p(q), C.byref(kv.struct), int(length),
+                                 float(scale), _p(out), _p(support_out), _p(path_out),
+                                 _p(mcand_out), _p(cand_out), _p(lse_out), _p(self.workspace),
+                                 self.workspace.numel(), _stream(stream)))
+        return out
+
+    def counters(self):
+        t, h = C.c_int64(), C.c_int32()
+        _check(lib().retopk_get_counters(self.handle, C.byref(t), C.byref(h)))
+        return t.value, h.value
+
+    def set_counters(self, t: int, fifo_head: int) -> None:
+        _check(lib().retopk_set_counters(self.handle, t, fifo_head))

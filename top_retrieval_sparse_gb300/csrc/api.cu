@@ -1,0 +1,653 @@
+// api.cu -- C ABI of libtsa (declared in include/tsa.h).
+//
+// Host-side validation, workspace layout and the launch sequence of each
+// entry point.  Nothing here allocates device memory, synchronises or prints.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "../../include/tsa.h"
+#include "tsa_internal.cuh"
+#include "tsa_kernels.h"
+
+namespace tsa {
+int attend_split_rows();
+int attend_max_splits();
+}  // namespace tsa
+
+using namespace tsa;
+
+namespace {
+
+thread_local std::string g_err;
+thread_local cudaEvent_t g_stage[4] = {nullptr, nullptr, nullptr, nullptr};
+
+// Record stage event i on stream st when stage timing is on.
+cudaError_t stage_mark(int i, cudaStream_t st) {
+  if (!g_stage[i]) return cudaSuccess;
+  return cudaEventRecord(g_stage[i], st);
+}
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+int ok() {
+  g_err.clear();
+  return TSA_OK;
+}
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(TSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr size_t kAlign = 256;
+size_t up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+
+int num_sms() {
+  static int sms[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!sms[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    sms[dev] = v > 0 ? v : 148;
+  }
+  return sms[dev];
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Positions per CTA of the selection kernel (multiple of its 16-byte loop).
+constexpr int kSelectChunk = 16384;
+
+// Workspace of one decode call (offsets from the base).
+struct DecodeLayout {
+  size_t zero_begin, status, hist, sel_n, cand_n, tick_sel, tick_att, zero_end;
+  size_t scores, cand, sel_idx, sel_z, part, total;
+  int64_t stride;  // score row stride (positions)
+  int n_wsplit, n_ssplit;
+};
+
+DecodeLayout decode_layout(int B, int Hq, int64_t l_cap, int K, int n_init, int n_recent) {
+  DecodeLayout L{};
+  const size_t rows = (size_t)B * Hq;
+  const int sr = attend_split_rows();
+  L.stride = (int64_t)up((size_t)(l_cap > 0 ? l_cap : 1), 2048);
+  int64_t win = (int64_t)n_init + n_recent;
+  if (win > l_cap) win = l_cap;
+  L.n_wsplit = (int)((win + sr - 1) / sr);
+  L.n_ssplit = K > 0 ? (K + sr - 1) / sr : (L.n_wsplit == 0 ? 1 : 0);
+  size_t o = 0;
+  L.zero_begin = o;
+  L.status = o; o = up(o + 4);
+  L.hist = o; o = up(o + rows * kHistBins * 4);
+  L.sel_n = o; o = up(o + rows * 4);
+  L.cand_n = o; o = up(o + rows * 4);
+  L.tick_sel = o; o = up(o + rows * 4);
+  L.tick_att = o; o = up(o + rows * 4);
+  L.zero_end = o;
+  L.scores = o; o = up(o + rows * (size_t)L.stride * 4);
+  L.cand = o; o = up(o + rows * (size_t)L.stride * 4);
+  const size_t kk = (size_t)(K > 0 ? K : 1);
+  L.sel_idx = o; o = up(o + rows * kk * 4);
+  L.sel_z = o; o = up(o + rows * kk * 4);
+  L.part = o; o = up(o + rows * (size_t)(L.n_wsplit + L.n_ssplit) * (kD + 2) * 4);
+  L.total = o;
+  return L;
+}
+
+int check_kv(const tsa_kv* kv, int B, int Hkv) {
+  if (!kv) return fail(TSA_ERR_INVALID_ARG, "kv is NULL");
+  if (!kv->k || !kv->v) return fail(TSA_ERR_INVALID_ARG, "kv->k / kv->v is NULL");
+  if (!aligned(kv->k, 16) || !aligned(kv->v, 16))
+    return fail(TSA_ERR_INVALID_ARG, "kv->k / kv->v must be 16-byte aligned");
+  if (kv->l_cap < 0) return fail(TSA_ERR_INVALID_ARG, "kv->l_cap < 0");
+  if (kv->l_cap >= (int64_t)1 << 31) return fail(TSA_ERR_INVALID_ARG, "kv->l_cap >= 2^31");
+  if (kv->page_table) {
+    const int ps = kv->page_size;
+    if (ps < 16 || ps > 256 || (ps & (ps - 1)))
+      return fail(TSA_ERR_INVALID_ARG, "page_size %d: must be a power of two in [16, 256]", ps);
+    if (kv->max_pages <= 0) return fail(TSA_ERR_INVALID_ARG, "max_pages must be > 0");
+    if ((int64_t)kv->max_pages * ps != kv->l_cap)
+      return fail(TSA_ERR_INVALID_ARG, "paged cache: l_cap must equal max_pages*page_size");
+  }
+  (void)B;
+  (void)Hkv;
+  return TSA_OK;
+}
+
+KvView make_view(const tsa_kv* kv, int Hkv) {
+  KvView v{};
+  v.k = static_cast<const uint16_t*>(kv->k);
+  v.v = static_cast<const uint16_t*>(kv->v);
+  v.page_table = kv->page_table;
+  v.page_shift = 0;
+  if (kv->page_table)
+    while ((1 << v.page_shift) < kv->page_size) ++v.page_shift;
+  v.max_pages = kv->max_pages;
+  v.l_cap = kv->l_cap;
+  v.Hkv = Hkv;
+  return v;
+}
+
+int check_heads(int B, int Hq, int Hkv, int d) {
+  if (d != kD) return fail(TSA_ERR_INVALID_ARG, "d = %d: only d = 128 is compiled", d);
+  if (B < 0 || Hq <= 0 || Hkv <= 0) return fail(TSA_ERR_INVALID_ARG, "B/Hq/Hkv out of range");
+  if (Hq % Hkv) return fail(TSA_ERR_INVALID_ARG, "Hq %% Hkv != 0 (Hq=%d Hkv=%d)", Hq, Hkv);
+  if (Hq / Hkv > kMaxGroup)
+    return fail(TSA_ERR_INVALID_ARG, "group size %d > %d", Hq / Hkv, kMaxGroup);
+  if ((int64_t)B * Hkv > kMaxUnits)
+    return fail(TSA_ERR_INVALID_ARG, "B*Hkv = %lld > %d", (long long)B * Hkv, kMaxUnits);
+  if ((int64_t)B * Hq > 65535)
+    return fail(TSA_ERR_INVALID_ARG, "B*Hq = %lld > 65535", (long long)B * Hq);
+  return TSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tsa_last_error(void) { return g_err.c_str(); }
+
+const char* tsa_version(void) { return "tsa 0.1 (sm_103a)"; }
+
+int tsa_set_stage_events(void* const* events, int n) {
+  if (events && n > 0 && n < 4)
+    return fail(TSA_ERR_INVALID_ARG, "tsa_set_stage_events needs 4 events");
+  for (int i = 0; i < 4; ++i)
+    g_stage[i] = (events && n >= 4) ? static_cast<cudaEvent_t>(events[i]) : nullptr;
+  return ok();
+}
+
+size_t tsa_decode_workspace_size(int B, int Hq, int Hkv, int d, int64_t l_cap, int K,
+                                 int n_init, int n_recent) {
+  (void)Hkv;
+  (void)d;
+  if (B <= 0 || Hq <= 0 || l_cap < 0 || K < 0 || n_init < 0 || n_recent < 0) return 0;
+  return decode_layout(B, Hq, l_cap, K, n_init, n_recent).total;
+}
+
+int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int B, int Hq,
+                       int Hkv, int d, int K, int n_init, int n_recent, float scale, float* out,
+                       float* lse_out, int32_t* topk_idx, float* topk_score, void* workspace,
+                       size_t ws_bytes, void* stream) {
+  int rc = check_heads(B, Hq, Hkv, d);
+  if (rc) return rc;
+  if ((rc = check_kv(kv, B, Hkv))) return rc;
+  if (B == 0) return ok();
+  if (!q || !out || !lens) return fail(TSA_ERR_INVALID_ARG, "q, out and lens must be non-NULL");
+  if (!aligned(q, 16)) return fail(TSA_ERR_INVALID_ARG, "q must be 16-byte aligned");
+  if (!aligned(out, 16)) return fail(TSA_ERR_INVALID_ARG, "out must be 16-byte aligned");
+  if (K < 0 || n_init < 0 || n_recent < 0)
+    return fail(TSA_ERR_INVALID_ARG, "K, n_init, n_recent must be >= 0");
+  if (!std::isfinite(scale)) return fail(TSA_ERR_INVALID_ARG, "scale must be finite");
+  const DecodeLayout Lw = decode_layout(B, Hq, kv->l_cap, K, n_init, n_recent);
+  if (Lw.n_wsplit + Lw.n_ssplit > attend_max_splits())
+    return fail(TSA_ERR_INVALID_ARG, "K + window too large (%d splits > %d)",
+                Lw.n_wsplit + Lw.n_ssplit, attend_max_splits());
+  if (!workspace || !aligned(workspace, kAlign))
+    return fail(TSA_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
+  if (ws_bytes < Lw.total)
+    return fail(TSA_ERR_WORKSPACE, "workspace %zu bytes < required %zu", ws_bytes, Lw.total);
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t e = cudaMemsetAsync(ws + Lw.zero_begin, 0, Lw.zero_end - Lw.zero_begin, st);
+  if (e != cudaSuccess) return cuda_fail(e, "memset");
+  if ((e = stage_mark(0, st)) != cudaSuccess) return cuda_fail(e, "event record");
+
+  const KvView view = make_view(kv, Hkv);
+  const int G = Hq / Hkv;
+  float* scores = reinterpret_cast<float*>(ws + Lw.scores);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(ws + Lw.hist);
+  int* status = reinterpret_cast<int*>(ws + Lw.status);
+  int32_t* sel_idx = topk_idx ? topk_idx : reinterpret_cast<int32_t*>(ws + Lw.sel_idx);
+  float* sel_z = topk_score ? topk_score : reinterpret_cast<float*>(ws + Lw.sel_z);
+  int32_t* sel_n = reinterpret_cast<int32_t*>(ws + Lw.sel_n);
+
+  // 1. key scan + pass-1 histogram
+  if (kv->l_cap > 0) {
+    ScanArgs s{};
+    s.q = static_cast<const uint16_t*>(q);
+    s.kv = view;
+    s.lens = lens;
+    s.B = B;
+    s.Hq = Hq;
+    s.scale = scale;
+    s.n_init = n_init;
+    s.n_recent = n_recent;
+    s.scores = scores;
+    s.score_stride = Lw.stride;
+    s.hist = hist;
+    s.status = status;
+    const int64_t max_tiles = (int64_t)B * Hkv * ((kv->l_cap + 63) / 64);
+    int64_t grid = (int64_t)num_sms() * scan_ctas_per_sm(G);
+    if (grid > max_tiles) grid = max_tiles;
+    if (grid < 1) grid = 1;
+    if ((e = launch_scan(s, (int)grid, st)) != cudaSuccess) return cuda_fail(e, "scan launch");
+  }
+  if ((e = stage_mark(1, st)) != cudaSuccess) return cuda_fail(e, "event record");
+  // 2. exact top-K outside the window
+  if (K > 0) {
+    SelectArgs s{};
+    s.scores = scores;
+    s.score_stride = Lw.stride;
+    s.hist = hist;
+    s.lens = lens;
+    s.l_cap = kv->l_cap;
+    s.B = B;
+    s.Hq = Hq;
+    s.K = K;
+    s.n_init = n_init;
+    s.n_recent = n_recent;
+    s.chunk = kSelectChunk;
+    s.sel_idx = sel_idx;
+    s.sel_z = sel_z;
+    s.sel_n = sel_n;
+    s.cand_n = reinterpret_cast<int32_t*>(ws + Lw.cand_n);
+    s.cand = reinterpret_cast<uint32_t*>(ws + Lw.cand);
+    s.ticket = reinterpret_cast<uint32_t*>(ws + Lw.tick_sel);
+    int chunks = (int)((kv->l_cap + kSelectChunk - 1) / kSelectChunk);
+    if (chunks < 1) chunks = 1;
+    if ((e = launch_select(s, chunks, st)) != cudaSuccess) return cuda_fail(e, "select launch");
+  }
+  if ((e = stage_mark(2, st)) != cudaSuccess) return cuda_fail(e, "event record");
+  // 3. window + selected partials and the gamma merge
+  {
+    AttendArgs a{};
+    a.kv = view;
+    a.lens = lens;
+    a.B = B;
+    a.Hq = Hq;
+    a.scores = scores;
+    a.score_stride = Lw.stride;
+    a.n_init = n_init;
+    a.n_recent = n_recent;
+    a.n_wsplit = Lw.n_wsplit;
+    a.n_ssplit = Lw.n_ssplit;
+    a.sel_idx = sel_idx;
+    a.sel_z = sel_z;
+    a.sel_n = sel_n;
+    a.K = K;
+    a.part = reinterpret_cast<float*>(ws + Lw.part);
+    a.ticket = reinterpret_cast<uint32_t*>(ws + Lw.tick_att);
+    a.out = out;
+    a.lse_out = lse_out;
+    if ((e = launch_attend(a, st)) != cudaSuccess) return cuda_fail(e, "attend launch");
+  }
+  if ((e = stage_mark(3, st)) != cudaSuccess) return cuda_fail(e, "event record");
+  (void)G;
+  return ok();
+}
+
+int lse_merge(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b,
+              float* o_out, float* lse_out, int rows, int d, void* stream) {
+  if (rows < 0 || d < 1 || d > 1024) return fail(TSA_ERR_INVALID_ARG, "rows/d out of range");
+  if (rows == 0) return ok();
+  if (!o_a || !lse_a || !o_b || !lse_b || !o_out || !lse_out)
+    return fail(TSA_ERR_INVALID_ARG, "NULL pointer");
+  cudaError_t e = launch_lse_merge(o_a, lse_a, o_b, lse_b, o_out, lse_out, rows, d,
+                                   static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "lse_merge launch");
+  return ok();
+}
+
+}  // extern "C"
+
+// ===================================================================== ReTopK
+struct tsa_retopk {
+  uint32_t magic;
+  int Hq, Hkv, K, C, R, W, T_r;
+  float tau;
+  int64_t max_len;
+  float* qbar;       // [Hq][C][128]
+  int32_t* sup;      // [Hq][C][K]
+  int32_t* sup_n;    // [Hq][C]
+  int64_t t;
+  int fifo_head;
+  bool initialised;
+};
+
+namespace {
+constexpr uint32_t kMagic = 0x52544b31u;  // "RTK1"
+
+struct RetopkLayout {
+  size_t zero_begin, status, hist, sel_n, cand_n, tick_sel, tick_att, tick_rs, zero_end;
+  size_t scores, cand_exact, qbar_new, path, cand, mcand, ehat, sel_idx, sel_z, part, total;
+  int64_t stride;
+  int cand_cap, n_ssplit;
+};
+
+RetopkLayout retopk_layout(const tsa_retopk* s) {
+  RetopkLayout L{};
+  const size_t H = (size_t)s->Hq;
+  const int sr = attend_split_rows();
+  L.stride = (int64_t)up((size_t)s->max_len, 2048);
+  L.cand_cap = s->R * s->K + s->W;
+  L.n_ssplit = (s->K + sr - 1) / sr;
+  size_t o = 0;
+  L.zero_begin = o;
+  L.status = o; o = up(o + 4);
+  L.hist = o; o = up(o + H * kHistBins * 4);
+  L.sel_n = o; o = up(o + H * 4);
+  L.cand_n = o; o = up(o + H * 4);
+  L.tick_sel = o; o = up(o + H * 4);
+  L.tick_att = o; o = up(o + H * 4);
+  L.tick_rs = o; o = up(o + H * 4);
+  L.zero_end = o;
+  L.scores = o; o = up(o + H * (size_t)L.stride * 4);
+  L.cand_exact = o; o = up(o + H * (size_t)L.stride * 4);
+  L.qbar_new = o; o = up(o + H * kD * 4);
+  L.path = o; o = up(o + H * 4);
+  L.cand = o; o = up(o + H * (size_t)L.cand_cap * 4);
+  L.mcand = o; o = up(o + H * 4);
+  L.ehat = o; o = up(o + H * (size_t)L.cand_cap * 4);
+  L.sel_idx = o; o = up(o + H * (size_t)s->K * 4);
+  L.sel_z = o; o = up(o + H * (size_t)s->K * 4);
+  L.part = o; o = up(o + H * (size_t)L.n_ssplit * (kD + 2) * 4);
+  L.total = o;
+  return L;
+}
+
+size_t state_bytes(int Hq, int K, int C) {
+  return up((size_t)Hq * C * kD * 4) + up((size_t)Hq * C * K * 4) + up((size_t)Hq * C * 4);
+}
+
+int check_state(const tsa_retopk* s) {
+  if (!s || s->magic != kMagic) return fail(TSA_ERR_STATE, "invalid ReTopK handle");
+  return TSA_OK;
+}
+
+constexpr int64_t kMaxBitmapLen = (int64_t)192 * 1024 * 8;  // positions in 192 KiB of bits
+}  // namespace
+
+extern "C" {
+
+size_t retopk_state_size(int Hq, int d, int K, int C) {
+  if (Hq <= 0 || d != kD || K <= 0 || C <= 0) return 0;
+  return state_bytes(Hq, K, C);
+}
+
+int retopk_create(tsa_retopk** st, int Hq, int Hkv, int d, int K, int C, int R, int W, float tau,
+                  int T_r, int64_t max_len, void* state_mem, size_t state_bytes_) {
+  if (!st) return fail(TSA_ERR_INVALID_ARG, "st is NULL");
+  *st = nullptr;
+  int rc = check_heads(1, Hq, Hkv, d);
+  if (rc) return rc;
+  if (K < 1) return fail(TSA_ERR_INVALID_ARG, "K must be >= 1");
+  if (C < 1 || C > 64) return fail(TSA_ERR_INVALID_ARG, "C must be in [1, 64]");
+  if (R < 1 || R > C) return fail(TSA_ERR_INVALID_ARG, "R must be in [1, C]");
+  if (W < 0) return fail(TSA_ERR_INVALID_ARG, "W must be >= 0");
+  if (T_r < 1) return fail(TSA_ERR_INVALID_ARG, "T_r must be >= 1");
+  if (std::isnan(tau)) return fail(TSA_ERR_INVALID_ARG, "tau is NaN");
+  if (max_len < 1 || max_len > kMaxBitmapLen)
+    return fail(TSA_ERR_INVALID_ARG, "max_len must be in [1, %lld]", (long long)kMaxBitmapLen);
+  if ((int64_t)R * K + W > 8192)
+    return fail(TSA_ERR_INVALID_ARG, "R*K + W = %lld > 8192", (long long)R * K + W);
+  if ((K + attend_split_rows() - 1) / attend_split_rows() > attend_max_splits())
+    return fail(TSA_ERR_INVALID_ARG, "K too large");
+  if (!state_mem || !aligned(state_mem, kAlign))
+    return fail(TSA_ERR_INVALID_ARG, "state_mem NULL or not 256-byte aligned");
+  if (state_bytes_ < state_bytes(Hq, K, C))
+    return fail(TSA_ERR_INVALID_ARG, "state_mem too small (%zu < %zu)", state_bytes_,
+                state_bytes(Hq, K, C));
+  tsa_retopk* s = new (std::nothrow) tsa_retopk();
+  if (!s) return fail(TSA_ERR_INVALID_ARG, "out of host memory");
+  s->magic = kMagic;
+  s->Hq = Hq;
+  s->Hkv = Hkv;
+  s->K = K;
+  s->C = C;
+  s->R = R;
+  s->W = W;
+  s->T_r = T_r;
+  s->tau = tau;
+  s->max_len = max_len;
+  uint8_t* m = static_cast<uint8_t*>(state_mem);
+  s->qbar = reinterpret_cast<float*>(m);
+  s->sup = reinterpret_cast<int32_t*>(m + up((size_t)Hq * C * kD * 4));
+  s->sup_n = reinterpret_cast<int32_t*>(m + up((size_t)Hq * C * kD * 4) + up((size_t)Hq * C * K * 4));
+  s->t = 0;
+  s->fifo_head = 0;
+  s->initialised = false;
+  *st = s;
+  return ok();
+}
+
+int retopk_init(tsa_retopk* st, const void* prefill_q, const int32_t* prefill_supports,
+                const int32_t* prefill_counts, void* stream) {
+  int rc = check_state(st);
+  if (rc) return rc;
+  if (!prefill_q || !prefill_supports || !prefill_counts)
+    return fail(TSA_ERR_INVALID_ARG, "NULL prefill pointer");
+  RetopkInitArgs a{};
+  a.prefill_q = static_cast<const uint16_t*>(prefill_q);
+  a.prefill_sup = prefill_supports;
+  a.prefill_n = prefill_counts;
+  a.Hq = st->Hq;
+  a.C = st->C;
+  a.K = st->K;
+  a.cache_qbar = st->qbar;
+  a.cache_sup = st->sup;
+  a.cache_sup_n = st->sup_n;
+  cudaError_t e = launch_retopk_init(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "retopk init launch");
+  st->t = 0;
+  st->fifo_head = 0;
+  st->initialised = true;
+  return ok();
+}
+
+size_t retopk_workspace_size(const tsa_retopk* st) {
+  if (!st || st->magic != kMagic) return 0;
+  return retopk_layout(st).total;
+}
+
+int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, float scale,
+                float* out, int32_t* support_out, int32_t* path_out, int32_t* mcand_out,
+                int32_t* cand_out, float* lse_out, void* workspace, size_t ws_bytes,
+                void* stream) {
+  int rc = check_state(st);
+  if (rc) return rc;
+  if (!st->initialised) return fail(TSA_ERR_STATE, "retopk_init has not been called");
+  if ((rc = check_kv(kv, 1, st->Hkv))) return rc;
+  if (!q || !out) return fail(TSA_ERR_INVALID_ARG, "q and out must be non-NULL");
+  if (!aligned(q, 16) || !aligned(out, 16))
+    return fail(TSA_ERR_INVALID_ARG, "q/out must be 16-byte aligned");
+  if (len < 1 || len > kv->l_cap || len > st->max_len)
+    return fail(TSA_ERR_INVALID_ARG, "len %lld outside [1, min(l_cap, max_len)]", (long long)len);
+  if (!std::isfinite(scale)) return fail(TSA_ERR_INVALID_ARG, "scale must be finite");
+  const RetopkLayout Lw = retopk_layout(st);
+  if (!workspace || !aligned(workspace, kAlign))
+    return fail(TSA_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
+  if (ws_bytes < Lw.total)
+    return fail(TSA_ERR_WORKSPACE, "workspace %zu bytes < required %zu", ws_bytes, Lw.total);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t e = cudaMemsetAsync(ws + Lw.zero_begin, 0, Lw.zero_end - Lw.zero_begin, s);
+  if (e != cudaSuccess) return cuda_fail(e, "memset");
+  if ((e = stage_mark(0, s)) != cudaSuccess) return cuda_fail(e, "event record");
+  const KvView view = make_view(kv, st->Hkv);
+  const int Hq = st->Hq;
+  int32_t* path = reinterpret_cast<int32_t*>(ws + Lw.path);
+  float* qbar_new = reinterpret_cast<float*>(ws + Lw.qbar_new);
+  int32_t* sel_idx = support_out ? support_out : reinterpret_cast<int32_t*>(ws + Lw.sel_idx);
+  float* sel_z = reinterpret_cast<float*>(ws + Lw.sel_z);
+  int32_t* sel_n = reinterpret_cast<int32_t*>(ws + Lw.sel_n);
+  float* scores = reinterpret_cast<float*>(ws + Lw.scores);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(ws + Lw.hist);
+
+  // 1. selector: cosine recall, path decision, candidate union
+  {
+    RetopkSelArgs a{};
+    a.q = static_cast<const uint16_t*>(q);
+    a.cache_qbar = st->qbar;
+    a.cache_sup = st->sup;
+    a.cache_sup_n = st->sup_n;
+    a.Hq = Hq;
+    a.C = st->C;
+    a.R = st->R;
+    a.K = st->K;
+    a.W = st->W;
+    a.fifo_head = st->fifo_head;
+    a.refresh = (st->t % st->T_r) == 0;
+    a.tau = st->tau;
+    a.L = len;
+    a.bitmap_words = (int)((len + 31) / 32);
+    a.qbar_new = qbar_new;
+    a.path = path;
+    a.cand = reinterpret_cast<uint32_t*>(ws + Lw.cand);
+    a.mcand = reinterpret_cast<int32_t*>(ws + Lw.mcand);
+    a.cand_cap = Lw.cand_cap;
+    a.path_out = path_out;
+    a.mcand_out = mcand_out;
+    a.cand_out = cand_out;
+    const size_t smem = up((size_t)a.bitmap_words * 4, 16);
+    if ((e = launch_retopk_selector(a, smem, s)) != cudaSuccess)
+      return cuda_fail(e, "retopk selector launch");
+  }
+  // 2. exact path heads: key scan + exact top-K over all keys (no window)
+  {
+    ScanArgs a{};
+    a.q = static_cast<const uint16_t*>(q);
+    a.kv = view;
+    a.lens = nullptr;
+    a.len_host = len;
+    a.B = 1;
+    a.Hq = Hq;
+    a.scale = scale;
+    a.n_init = 0;
+    a.n_recent = 0;
+    a.head_active = path;
+    a.active_value = 1;
+    a.scores = scores;
+    a.score_stride = Lw.stride;
+    a.hist = hist;
+    a.status = reinterpret_cast<int*>(ws + Lw.status);
+    const int G = Hq / st->Hkv;
+    const int64_t max_tiles = (int64_t)st->Hkv * ((len + 63) / 64);
+    int64_t grid = (int64_t)num_sms() * scan_ctas_per_sm(G);
+    if (grid > max_tiles) grid = max_tiles;
+    if ((e = launch_scan(a, (int)grid, s)) != cudaSuccess) return cuda_fail(e, "scan launch");
+    if ((e = stage_mark(1, s)) != cudaSuccess) return cuda_fail(e, "event record");
+
+    SelectArgs b{};
+    b.scores = scores;
+    b.score_stride = Lw.stride;
+    b.hist = hist;
+    b.lens = nullptr;
+    b.len_host = len;
+    b.l_cap = kv->l_cap;
+    b.B = 1;
+    b.Hq = Hq;
+    b.K = st->K;
+    b.n_init = 0;
+    b.n_recent = 0;
+    b.head_active = path;
+    b.active_value = 1;
+    b.chunk = kSelectChunk;
+    b.sel_idx = sel_idx;
+    b.sel_z = sel_z;
+    b.sel_n = sel_n;
+    b.cand_n = reinterpret_cast<int32_t*>(ws + Lw.cand_n);
+    b.cand = reinterpret_cast<uint32_t*>(ws + Lw.cand_exact);
+    b.ticket = reinterpret_cast<uint32_t*>(ws + Lw.tick_sel);
+    const int chunks = (int)((len + kSelectChunk - 1) / kSelectChunk);
+    if ((e = launch_select(b, chunks, s)) != cudaSuccess) return cuda_fail(e, "select launch");
+  }
+  // 3. reuse path heads: indexed rescoring + re-top-K over A_t
+  {
+    RetopkRescoreArgs a{};
+    a.q = static_cast<const uint16_t*>(q);
+    a.kv = view;
+    a.Hq = Hq;
+    a.scale = scale;
+    a.path = path;
+    a.cand = reinterpret_cast<const uint32_t*>(ws + Lw.cand);
+    a.mcand = reinterpret_cast<const int32_t*>(ws + Lw.mcand);
+    a.cand_cap = Lw.cand_cap;
+    a.K = st->K;
+    a.chunk = 256;
+    a.ehat = reinterpret_cast<float*>(ws + Lw.ehat);
+    a.ticket = reinterpret_cast<uint32_t*>(ws + Lw.tick_rs);
+    a.sel_idx = sel_idx;
+    a.sel_z = sel_z;
+    a.sel_n = sel_n;
+    const int chunks = (Lw.cand_cap + a.chunk - 1) / a.chunk;
+    if ((e = launch_retopk_rescore(a, chunks, s)) != cudaSuccess)
+      return cuda_fail(e, "retopk rescore launch");
+  }
+  if ((e = stage_mark(2, s)) != cudaSuccess) return cuda_fail(e, "event record");
+  // 4. sparse softmax.V over S_t (no window) and the FIFO push
+  {
+    AttendArgs a{};
+    a.kv = view;
+    a.lens = nullptr;
+    a.len_host = len;
+    a.B = 1;
+    a.Hq = Hq;
+    a.scores = scores;
+    a.score_stride = Lw.stride;
+    a.n_init = 0;
+    a.n_recent = 0;
+    a.n_wsplit = 0;
+    a.n_ssplit = Lw.n_ssplit;
+    a.sel_idx = sel_idx;
+    a.sel_z = sel_z;
+    a.sel_n = sel_n;
+    a.K = st->K;
+    a.part = reinterpret_cast<float*>(ws + Lw.part);
+    a.ticket = reinterpret_cast<uint32_t*>(ws + Lw.tick_att);
+    a.out = out;
+    a.lse_out = lse_out;
+    a.push_qbar = qbar_new;
+    a.cache_qbar = st->qbar;
+    a.cache_sup = st->sup;
+    a.cache_sup_n = st->sup_n;
+    a.C = st->C;
+    a.slot = st->fifo_head;
+    if ((e = launch_attend(a, s)) != cudaSuccess) return cuda_fail(e, "attend launch");
+  }
+  if ((e = stage_mark(3, s)) != cudaSuccess) return cuda_fail(e, "event record");
+  st->t += 1;
+  st->fifo_head = (st->fifo_head + 1) % st->C;
+  return ok();
+}
+
+int retopk_get_counters(const tsa_retopk* st, int64_t* t, int32_t* fifo_head) {
+  int rc = check_state(st);
+  if (rc) return rc;
+  if (t) *t = st->t;
+  if (fifo_head) *fifo_head = st->fifo_head;
+  return ok();
+}
+
+int retopk_set_counters(tsa_retopk* st, int64_t t, int32_t fifo_head) {
+  int rc = check_state(st);
+  if (rc) return rc;
+  if (t < 0 || fifo_head < 0 || fifo_head >= st->C)
+    return fail(TSA_ERR_INVALID_ARG, "counters out of range");
+  st->t = t;
+  st->fifo_head = fifo_head;
+  st->initialised = true;
+  return ok();
+}
+
+int retopk_destroy(tsa_retopk* st) {
+  if (!st) return ok();
+  if (st->magic != kMagic) return fail(TSA_ERR_STATE, "invalid ReTopK handle");
+  st->magic = 0;
+  delete st;
+  return ok();
+}
+
+}  // extern "C"

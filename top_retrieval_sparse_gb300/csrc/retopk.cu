@@ -1,0 +1,317 @@
+// retopk.cu -- ReTopK reuse path ("Recall Before You Rank: Similarity-Guided
+// Top-K Reuse for Efficient Long-Context Attention", method sections 1-5 and
+// "GPU Kernel": fused selector, indexed QK, candidate top-K).
+//
+// selector  (one CTA per query head): qbar = q/|q|; rho_c = qbar . qbar_c over
+//           the C cached queries; exact path iff max rho < tau or a refresh
+//           step; otherwise the R most similar entries (ties: older entry
+//           first), the union of their supports and the last W positions as a
+//           shared-memory bitmap, compacted in ascending order -> A_t, M_t.
+// rescore   (CTAs per reuse head): e_i = scale * q . k_i for i in A_t, reading
+//           K rows straight from the candidate positions (no gathered copy);
+//           the last CTA of the head (ticket) keeps the top-K of A_t by
+//           (e desc, position asc) with a CTA radix select.
+// init      fills the FIFO from the last C prefill queries and their supports.
+#include "tsa_internal.cuh"
+#include "tsa_kernels.h"
+
+namespace tsa {
+
+constexpr int kSelectorThreads = 256;
+constexpr int kRescoreThreads = 256;
+constexpr int kRescoreCache = 8192;  // candidates held in shared memory
+constexpr int kMaxC = 64;
+
+__global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(RetopkSelArgs a) {
+  extern __shared__ __align__(16) uint32_t bitmap[];
+  __shared__ float qs[kD];
+  __shared__ float rho[kMaxC];
+  __shared__ float red[kSelectorThreads / 32];
+  __shared__ int chosen[kMaxC];
+  __shared__ int s_path;
+  __shared__ uint32_t wtot[kSelectorThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int h = blockIdx.x;
+
+  // 1. normalise the query
+  float x = 0.f;
+  if (tid < kD) {
+    x = __uint_as_float((uint32_t)a.q[(int64_t)h * kD + tid] << 16);
+    qs[tid] = x;
+  }
+  float ss = warp_sum(x * x);
+  if (lane == 0) red[wid] = ss;
+  __syncthreads();
+  if (tid == 0) {
+    float t = 0.f;
+    for (int w = 0; w < kSelectorThreads / 32; ++w) t += red[w];
+    red[0] = t;
+  }
+  __syncthreads();
+  const float nrm = sqrtf(red[0]);
+  if (tid < kD) {
+    const float qb = nrm > 0.f ? qs[tid] / nrm : 0.f;
+    qs[tid] = qb;
+    a.qbar_new[(int64_t)h * kD + tid] = qb;
+  }
+  __syncthreads();
+
+  // 2. cosine against the cached queries (one warp per entry)
+  for (int c = wid; c < a.C; c += kSelectorThreads / 32) {
+    const float* qc = a.cache_qbar + ((int64_t)h * a.C + c) * kD;
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc = fmaf(qs[lane * 4 + e], qc[lane * 4 + e], acc);
+    acc = warp_sum(acc);
+    if (lane == 0) rho[c] = acc;
+  }
+  __syncthreads();
+
+  // 3. fallback / refresh decision and top-R recall
+  if (tid == 0) {
+    float mx = -INFINITY;
+    for (int c = 0; c < a.C; ++c) mx = fmaxf(mx, rho[c]);
+    const int path = (mx < a.tau || a.refresh) ? 1 : 0;
+    s_path = path;
+    a.path[h] = path;
+    if (a.path_out) a.path_out[h] = path;
+    if (!path) {
+      unsigned used = 0u;  // C <= 64 entries, two words
+      unsigned used_hi = 0u;
+      for (int r = 0; r < a.R; ++r) {
+        int best = -1;
+        float bv = -INFINITY;
+        int bage = 1 << 30;
+        for (int c = 0; c < a.C; ++c) {
+          const bool u = c < 32 ? ((used >> c) & 1u) : ((used_hi >> (c - 32)) & 1u);
+          if (u) continue;
+          const int age = (c - a.fifo_head + a.C) % a.C;  // 0 = oldest
+          if (best < 0 || rho[c] > bv || (rho[c] == bv && age < bage)) {
+            best = c;
+            bv = rho[c];
+            bage = age;
+          }
+        }
+        chosen[r] = best;
+        if (best < 32) used |= 1u << best;
+        else used_hi |= 1u << (best - 32);
+      }
+    }
+  }
+  __syncthreads();
+  uint32_t* crow = a.cand + (int64_t)h * a.cand_cap;
+  if (s_path) {
+    if (tid == 0) {
+      a.mcand[h] = 0;
+      if (a.mcand_out) a.mcand_out[h] = (int32_t)a.L;
+    }
+    if (a.cand_out)
+      for (int j = tid; j < a.cand_cap; j += kSelectorThreads)
+        a.cand_out[(int64_t)h * a.cand_cap + j] = -1;
+    return;
+  }
+
+  // 4. bitmap union of the recalled supports and the recent window
+  const int nwords = (int)((a.L + 31) >> 5);
+  for (int w = tid; w < nwords; w += kSelectorThreads) bitmap[w] = 0u;
+  __syncthreads();
+  for (int r = 0; r < a.R; ++r) {
+    const int64_t hc = (int64_t)h * a.C + chosen[r];
+    const int n = a.cache_sup_n[hc];
+    for (int j = tid; j < n; j += kSelectorThreads) {
+      const int32_t p = a.cache_sup[hc * a.K + j];
+      if (p >= 0 && p < a.L) atomicOr(&bitmap[p >> 5], 1u << (p & 31));
+    }
+  }
+  const int64_t lo = a.L - a.W > 0 ? a.L - a.W : 0;
+  for (int64_t p = lo + tid; p < a.L; p += kSelectorThreads)
+    atomicOr(&bitmap[p >> 5], 1u << (p & 31));
+  __syncthreads();
+
+  // 5. ascending compaction: contiguous word ranges per thread + block scan
+  const int per = (nwords + kSelectorThreads - 1) / kSelectorThreads;
+  const int w0 = tid * per;
+  const int w1 = w0 + per < nwords ? w0 + per : nwords;
+  uint32_t cnt = 0;
+  for (int w = w0; w < w1; ++w) cnt += __popc(bitmap[w]);
+  uint32_t incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wtot[wid] = incl;
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t run = 0;
+    for (int w = 0; w < kSelectorThreads / 32; ++w) {
+      const uint32_t t = wtot[w];
+      wtot[w] = run;
+      run += t;
+    }
+    a.mcand[h] = (int32_t)run;
+    if (a.mcand_out) a.mcand_out[h] = (int32_t)run;
+  }
+  __syncthreads();
+  uint32_t pos = incl - cnt + wtot[wid];
+  for (int w = w0; w < w1; ++w) {
+    uint32_t bits = bitmap[w];
+    while (bits) {
+      const int bit = __ffs(bits) - 1;
+      bits &= bits - 1;
+      if (pos < (uint32_t)a.cand_cap) crow[pos] = ((uint32_t)w << 5) + bit;
+      ++pos;
+    }
+  }
+  if (a.cand_out) {
+    __syncthreads();
+    const int m = a.mcand[h];
+    for (int j = tid; j < a.cand_cap; j += kSelectorThreads)
+      a.cand_out[(int64_t)h * a.cand_cap + j] = j < m ? (int32_t)crow[j] : -1;
+  }
+}
+
+cudaError_t launch_retopk_selector(const RetopkSelArgs& a, size_t smem, cudaStream_t st) {
+  static size_t configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (smem > 48 * 1024 && dev < 64 && configured[dev] < smem) {
+    cudaError_t e = cudaFuncSetAttribute(retopk_selector_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = smem;
+  }
+  retopk_selector_kernel<<<a.Hq, kSelectorThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+// --------------------------------------------------------------- rescore
+struct RescoreShared {
+  RadixScratch rs;
+  int last;
+  int slot;
+};
+
+__global__ void __launch_bounds__(kRescoreThreads) retopk_rescore_kernel(RetopkRescoreArgs a) {
+  extern __shared__ __align__(16) uint64_t cache[];
+  __shared__ RescoreShared sh;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int h = blockIdx.y;
+  if (a.path[h] != 0) return;
+  const int G = a.Hq / a.kv.Hkv;
+  const int g = h / G;
+  const int M = a.mcand[h] < a.cand_cap ? a.mcand[h] : a.cand_cap;
+  const uint32_t* crow = a.cand + (int64_t)h * a.cand_cap;
+  float* erow = a.ehat + (int64_t)h * a.cand_cap;
+
+  // query slice: 4 elements per lane
+  const uint2 qw = *reinterpret_cast<const uint2*>(a.q + (int64_t)h * kD + lane * 4);
+  const float q0 = bf_lo(qw.x), q1 = bf_hi(qw.x), q2 = bf_lo(qw.y), q3 = bf_hi(qw.y);
+
+  const int c0 = blockIdx.x * a.chunk;
+  const int c1 = c0 + a.chunk < M ? c0 + a.chunk : M;
+  constexpr int U = 4;  // rows in flight per warp
+  for (int base = c0 + wid * U; base < c1; base += (kRescoreThreads / 32) * U) {
+    uint2 kw[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int j = base + u;
+      kw[u] = j < c1 ? *reinterpret_cast<const uint2*>(a.kv.k + kv_row(a.kv, 0, g, crow[j]) +
+                                                       lane * 4)
+                     : make_uint2(0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float acc = q0 * bf_lo(kw[u].x);
+      acc = fmaf(q1, bf_hi(kw[u].x), acc);
+      acc = fmaf(q2, bf_lo(kw[u].y), acc);
+      acc = fmaf(q3, bf_hi(kw[u].y), acc);
+      acc = warp_sum(acc);
+      const int j = base + u;
+      if (lane == 0 && j < c1) erow[j] = acc * a.scale;
+    }
+  }
+
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const uint32_t t = atomicAdd(&a.ticket[h], 1u);
+    sh.last = (t == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!sh.last) return;
+  __threadfence();
+
+  const int need = a.K < M ? a.K : M;
+  int32_t* sidx = a.sel_idx + (int64_t)h * a.K;
+  float* sz = a.sel_z + (int64_t)h * a.K;
+  if (tid == 0) sh.slot = 0;
+  const bool in_smem = M <= kRescoreCache;
+  if (in_smem)
+    for (int j = tid; j < M; j += kRescoreThreads)
+      cache[j] = rank_key(((volatile float*)erow)[j], crow[j]);
+  __syncthreads();
+  auto val = [&](int j) -> uint64_t {
+    if (in_smem) return cache[j];
+    return rank_key(((volatile float*)erow)[j], crow[j]);
+  };
+  auto emit = [&](uint64_t v) {
+    const int s = atomicAdd(&sh.slot, 1);
+    if (s < need) {
+      sidx[s] = (int32_t)rank_pos(v);
+      sz[s] = key2f((uint32_t)(v >> 32));
+    }
+  };
+  cta_radix_select(M, need, 0ull, 0ull, 64, val, emit, sh.rs);
+  for (int j = need + tid; j < a.K; j += kRescoreThreads) {
+    sidx[j] = -1;
+    sz[j] = -INFINITY;
+  }
+  if (tid == 0) {
+    a.sel_n[h] = need;
+    a.ticket[h] = 0;
+  }
+}
+
+cudaError_t launch_retopk_rescore(const RetopkRescoreArgs& a, int chunks, cudaStream_t st) {
+  const size_t smem = (size_t)kRescoreCache * sizeof(uint64_t);
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(retopk_rescore_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  dim3 grid(chunks, a.Hq);
+  retopk_rescore_kernel<<<grid, kRescoreThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ init
+__global__ void retopk_init_kernel(RetopkInitArgs a) {
+  __shared__ float red[kD / 32];
+  const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const int64_t src = (int64_t)c * a.Hq + h;
+  const float x = __uint_as_float((uint32_t)a.prefill_q[src * kD + tid] << 16);
+  const float ss = warp_sum(x * x);
+  if ((tid & 31) == 0) red[tid >> 5] = ss;
+  __syncthreads();
+  const float nrm = sqrtf(red[0] + red[1] + red[2] + red[3]);
+  const int64_t hc = (int64_t)h * a.C + c;
+  a.cache_qbar[hc * kD + tid] = nrm > 0.f ? x / nrm : 0.f;
+  int n = a.prefill_n[src];
+  n = n < 0 ? 0 : (n > a.K ? a.K : n);
+  for (int j = tid; j < a.K; j += kD)
+    a.cache_sup[hc * a.K + j] = j < n ? a.prefill_sup[src * a.K + j] : -1;
+  if (tid == 0) a.cache_sup_n[hc] = n;
+}
+
+cudaError_t launch_retopk_init(const RetopkInitArgs& a, cudaStream_t st) {
+  dim3 grid(a.C, a.Hq);
+  retopk_init_kernel<<<grid, kD, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace tsa

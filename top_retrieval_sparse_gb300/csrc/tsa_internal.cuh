@@ -1,0 +1,303 @@
+// tsa_internal.cuh -- device helpers shared by the libtsa kernels.
+//
+// Decode-step top-K sparse attention ("RetrievalAttention: Accelerating
+// Long-Context LLM Inference via Vector Retrieval", Eq. 1-5, Flat exact
+// top-k) and ReTopK reuse ("Recall Before You Rank", method sections 1-5).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tsa {
+
+constexpr int kD = 128;                         // head dimension (only size compiled)
+constexpr int kRowBytes = kD * 2;               // one bf16 K or V row
+constexpr int kHistBits = 11;                   // pass-1 radix digit
+constexpr int kHistBins = 1 << kHistBits;
+constexpr int kHistShift = 32 - kHistBits;
+constexpr int kMaxGroup = 8;                    // query heads per KV head
+constexpr int kMaxUnits = 1024;                 // B * Hkv limit of one call
+constexpr long long kWaitLimitNs = 1000000000;  // bounded waits: 1 s
+
+// Status word codes written by kernels into the workspace (host maps them).
+constexpr int kStatusTimeout = 1;
+
+// ---------------------------------------------------------------- encoding
+// Order-preserving key of an fp32 value: a > b  <=>  key(a) > key(b).
+// -0 is folded into +0 first, so equal logits have equal keys.
+__device__ __forceinline__ uint32_t f2key(float f) {
+  f = f + 0.0f;
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key2f(uint32_t k) {
+  uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+  return __uint_as_float(u);
+}
+// Rank key of (logit, position): larger logit first, then smaller position.
+__device__ __forceinline__ uint64_t rank_key(float z, uint32_t pos) {
+  return ((uint64_t)f2key(z) << 32) | (uint64_t)(0xffffffffu - pos);
+}
+__device__ __forceinline__ uint32_t rank_pos(uint64_t v) {
+  return 0xffffffffu - (uint32_t)(v & 0xffffffffu);
+}
+
+// bf16x2 word -> (low element, high element) as fp32 (exact).
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Packed fp32x2 FMA (sm_100+): d = a * b + c on both halves.
+__device__ __forceinline__ void ffma2(float2& d, float2 a, float2 b) {
+  uint64_t ar, br, dr;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(ar) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1,%2};" : "=l"(br) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1,%2};" : "=l"(dr) : "f"(d.x), "f"(d.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(dr) : "l"(ar), "l"(br));
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(dr));
+}
+
+// ------------------------------------------------------------- KV address
+struct KvView {
+  const uint16_t* k;          // bf16 bits
+  const uint16_t* v;
+  const int32_t* page_table;  // nullptr: contiguous
+  int page_shift;             // log2(page_size) (paged)
+  int max_pages;
+  int64_t l_cap;
+  int Hkv;
+};
+
+// Element offset of row i of KV head g of sequence b.
+__device__ __forceinline__ int64_t kv_row(const KvView& kv, int b, int g, int64_t i) {
+  if (kv.page_table) {
+    int64_t page = kv.page_table[(int64_t)b * kv.max_pages + (i >> kv.page_shift)];
+    int64_t r = i & ((1 << kv.page_shift) - 1);
+    return (((page * kv.Hkv + g) << kv.page_shift) + r) * kD;
+  }
+  return (((int64_t)b * kv.Hkv + g) * kv.l_cap + i) * kD;
+}
+
+// Sequence length, clamped to [0, cap] so that no position past the cache is
+// ever addressed.
+__device__ __forceinline__ int64_t seq_len(const int32_t* lens, int64_t len_host, int b,
+                                           int64_t cap) {
+  int64_t L = lens ? (int64_t)lens[b] : len_host;
+  return L < 0 ? 0 : (L > cap ? cap : L);
+}
+
+// Window W_t = [0, n_init) u [L - n_recent, L), clipped (static pattern W).
+__device__ __forceinline__ bool in_window(int64_t i, int64_t L, int n_init, int n_recent) {
+  return i < n_init || i >= L - n_recent;
+}
+__device__ __forceinline__ int64_t window_count(int64_t L, int n_init, int n_recent) {
+  int64_t a = n_init < L ? n_init : L;
+  int64_t lo = L - n_recent > a ? L - n_recent : a;
+  return a + (L - lo);
+}
+// j-th window position in ascending order (j < window_count).
+__device__ __forceinline__ int64_t window_pos(int64_t j, int64_t L, int n_init, int n_recent) {
+  int64_t a = n_init < L ? n_init : L;
+  if (j < a) return j;
+  int64_t lo = L - n_recent > a ? L - n_recent : a;
+  return lo + (j - a);
+}
+
+// -------------------------------------------------------------- PTX: TMA
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait on an mbarrier phase: false after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if ((long long)(globaltimer_ns() - t0) > kWaitLimitNs) return false;
+  }
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0,
+// both addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// ------------------------------------------------------ warp/block utils
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Warp-aggregated slot reservation: every lane with `pred` gets a distinct
+// index from *counter (one atomic per warp).
+__device__ __forceinline__ int warp_reserve(bool pred, int* counter) {
+  unsigned m = __ballot_sync(0xffffffffu, pred);
+  if (!m) return -1;
+  int lane = threadIdx.x & 31;
+  int leader = __ffs(m) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(counter, __popc(m));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  return pred ? base + __popc(m & ((1u << lane) - 1)) : -1;
+}
+
+// ------------------------------------------------------ CTA radix select
+// Selects the `need` largest of n distinct 64-bit values val(j), j < n, all
+// of which share the bits `prefix` under `mask` (the known high bits), and
+// calls emit(v) once for each selected value (in no particular order).
+// Digit of 11 bits per round, scanned from the top; every round either
+// emits the elements above the threshold digit or finishes.  smem_hist
+// needs kHistBins uint32; uses __syncthreads (all threads must call).
+struct RadixScratch {
+  uint32_t hist[kHistBins];
+  uint32_t warp_tot[32];
+  int digit;
+  int above;
+  int match;
+};
+
+template <class ValFn, class EmitFn>
+__device__ void cta_radix_select(int n, int need, uint64_t prefix, uint64_t mask, int shift,
+                                 ValFn val, EmitFn emit, RadixScratch& s) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  int match = n;  // elements currently matching prefix/mask
+  while (need > 0) {
+    if (match <= need) {  // everything still matching is selected
+      for (int j = tid; j < n; j += nt) {
+        uint64_t v = val(j);
+        if ((v & mask) == prefix) emit(v);
+      }
+      break;
+    }
+    int db = shift < kHistBits ? shift : kHistBits;
+    shift -= db;
+    const uint32_t dmask = (1u << db) - 1u;
+    for (int i = tid; i < kHistBins; i += nt) s.hist[i] = 0;
+    __syncthreads();
+    for (int j = tid; j < n; j += nt) {
+      uint64_t v = val(j);
+      if ((v & mask) == prefix) atomicAdd(&s.hist[(uint32_t)(v >> shift) & dmask], 1u);
+    }
+    __syncthreads();
+    // threshold digit: largest d with sum_{e >= d} hist[e] >= need.
+    // Thread t owns bins scanned from the top in blocks of `per`.
+    const int nb = 1 << db;
+    const int per = (nb + nt - 1) / nt;
+    uint32_t mine = 0;
+    for (int r = 0; r < per; ++r) {
+      int idx = tid * per + r;  // position from the top
+      if (idx < nb) mine += s.hist[nb - 1 - idx];
+    }
+    // inclusive scan of `mine` over threads (top-down order)
+    uint32_t incl = mine;
+    const int lane = tid & 31, wid = tid >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s.warp_tot[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+      int nw = (nt + 31) >> 5;
+      uint32_t w = lane < nw ? s.warp_tot[lane] : 0;
+      uint32_t wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        uint32_t y = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += y;
+      }
+      if (lane < nw) s.warp_tot[lane] = wi - w;  // exclusive warp offsets
+    }
+    __syncthreads();
+    uint32_t excl = incl - mine + s.warp_tot[wid];
+    if (excl < (uint32_t)need && excl + mine >= (uint32_t)need) {
+      uint32_t acc = excl;
+      for (int r = 0; r < per; ++r) {
+        int idx = tid * per + r;
+        if (idx >= nb) break;
+        uint32_t c = s.hist[nb - 1 - idx];
+        if (acc + c >= (uint32_t)need) {
+          s.digit = nb - 1 - idx;
+          s.above = (int)acc;
+          s.match = (int)c;
+          break;
+        }
+        acc += c;
+      }
+    }
+    __syncthreads();
+    const uint32_t dstar = (uint32_t)s.digit;
+    const int above = s.above;
+    const int cnt = s.match;
+    __syncthreads();
+    if (above > 0) {
+      for (int j = tid; j < n; j += nt) {
+        uint64_t v = val(j);
+        if ((v & mask) == prefix && ((uint32_t)(v >> shift) & dmask) > dstar) emit(v);
+      }
+    }
+    need -= above;
+    prefix |= (uint64_t)dstar << shift;
+    mask |= (uint64_t)dmask << shift;
+    match = cnt;
+    if (shift == 0) {  // fully determined: `match` (= 1) element equals prefix
+      if (need > 0)
+        for (int j = tid; j < n; j += nt) {
+          uint64_t v = val(j);
+          if (v == prefix) emit(v);
+        }
+      break;
+    }
+  }
+  __syncthreads();
+}
+
+}  // namespace tsa

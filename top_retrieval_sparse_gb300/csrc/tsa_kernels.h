@@ -1,0 +1,134 @@
+// tsa_kernels.h -- argument blocks and launchers of the libtsa kernels
+// (host <-> device contract inside the library; not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tsa_internal.cuh"
+
+namespace tsa {
+
+// Per-head activity filter: a head takes part iff
+// head_active == nullptr || head_active[b*Hq + h] == active_value.
+struct ScanArgs {
+  const uint16_t* q;         // bf16 [B][Hq][128]
+  KvView kv;
+  const int32_t* lens;       // [B] device, or nullptr -> len_host
+  int64_t len_host;
+  int B, Hq;
+  float scale;
+  int n_init, n_recent;      // window excluded from the histogram
+  const int32_t* head_active;
+  int active_value;
+  float* scores;             // [B][Hq][score_stride]
+  int64_t score_stride;
+  uint32_t* hist;            // [B][Hq][kHistBins], zeroed before the launch
+  int* status;
+};
+cudaError_t launch_scan(const ScanArgs& a, int grid, cudaStream_t st);
+int scan_ctas_per_sm(int G);
+
+struct SelectArgs {
+  const float* scores;       // [B][Hq][score_stride]
+  int64_t score_stride;
+  const uint32_t* hist;      // [B][Hq][kHistBins]
+  const int32_t* lens;
+  int64_t len_host;
+  int64_t l_cap;             // lengths are clamped to it
+  int B, Hq, K;
+  int n_init, n_recent;
+  const int32_t* head_active;
+  int active_value;
+  int chunk;                 // positions per CTA
+  int32_t* sel_idx;          // [B][Hq][K]
+  float* sel_z;              // [B][Hq][K]
+  int32_t* sel_n;            // [B][Hq] counters (zeroed), final |Omega|
+  int32_t* cand_n;           // [B][Hq] counters (zeroed)
+  uint32_t* cand;            // [B][Hq][score_stride] candidate positions
+  uint32_t* ticket;          // [B][Hq] (zeroed)
+};
+cudaError_t launch_select(const SelectArgs& a, int chunks, cudaStream_t st);
+
+struct AttendArgs {
+  KvView kv;
+  const int32_t* lens;
+  int64_t len_host;
+  int B, Hq;
+  const float* scores;       // window logits, [B][Hq][score_stride]
+  int64_t score_stride;
+  int n_init, n_recent;
+  int n_wsplit, n_ssplit;    // splits per head (window, selected)
+  const int32_t* sel_idx;    // [B][Hq][K]
+  const float* sel_z;
+  const int32_t* sel_n;      // [B][Hq]
+  int K;
+  float* part;               // [B][Hq][n_wsplit+n_ssplit][kD + 2]
+  uint32_t* ticket;          // [B][Hq] (zeroed)
+  float* out;                // [B][Hq][128]
+  float* lse_out;            // [B][Hq] or nullptr
+  // ReTopK cache push (push_qbar == nullptr: none)
+  const float* push_qbar;    // [Hq][128] normalised queries of this step
+  float* cache_qbar;         // [Hq][C][128]
+  int32_t* cache_sup;        // [Hq][C][K]
+  int32_t* cache_sup_n;      // [Hq][C]
+  int C, slot;
+};
+cudaError_t launch_attend(const AttendArgs& a, cudaStream_t st);
+
+cudaError_t launch_lse_merge(const float* oa, const float* la, const float* ob,
+                             const float* lb, float* oo, float* lo, int rows, int d,
+                             cudaStream_t st);
+
+// ReTopK ------------------------------------------------------------------
+struct RetopkSelArgs {
+  const uint16_t* q;         // bf16 [Hq][128]
+  const float* cache_qbar;   // [Hq][C][128]
+  const int32_t* cache_sup;  // [Hq][C][K]
+  const int32_t* cache_sup_n;// [Hq][C]
+  int Hq, C, R, K, W;
+  int fifo_head;             // slot of the oldest entry
+  int refresh;               // t % T_r == 0
+  float tau;
+  int64_t L;
+  int bitmap_words;
+  float* qbar_new;           // [Hq][128]
+  int32_t* path;             // [Hq] 1 exact, 0 reuse
+  uint32_t* cand;            // [Hq][cand_cap] ascending
+  int32_t* mcand;            // [Hq]
+  int cand_cap;              // R*K + W
+  int32_t* path_out;         // optional copies
+  int32_t* mcand_out;
+  int32_t* cand_out;         // [Hq][cand_cap], -1 padded
+};
+cudaError_t launch_retopk_selector(const RetopkSelArgs& a, size_t smem, cudaStream_t st);
+
+struct RetopkRescoreArgs {
+  const uint16_t* q;
+  KvView kv;
+  int Hq;
+  float scale;
+  const int32_t* path;       // reuse heads are path == 0
+  const uint32_t* cand;
+  const int32_t* mcand;
+  int cand_cap, K, chunk;
+  float* ehat;               // [Hq][cand_cap]
+  uint32_t* ticket;          // [Hq] (zeroed)
+  int32_t* sel_idx;          // [Hq][K]
+  float* sel_z;
+  int32_t* sel_n;            // [Hq]
+};
+cudaError_t launch_retopk_rescore(const RetopkRescoreArgs& a, int chunks, cudaStream_t st);
+
+struct RetopkInitArgs {
+  const uint16_t* prefill_q;     // [C][Hq][128]
+  const int32_t* prefill_sup;    // [C][Hq][K]
+  const int32_t* prefill_n;      // [C][Hq]
+  int Hq, C, K;
+  float* cache_qbar;
+  int32_t* cache_sup;
+  int32_t* cache_sup_n;
+};
+cudaError_t launch_retopk_init(const RetopkInitArgs& a, cudaStream_t st);
+
+}  // namespace tsa
