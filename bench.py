@@ -88,24 +88,27 @@ class Clocks:
     def start(self):
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
+            if os.path.exists(self.path):
+                os.remove(self.path)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=self.f, stderr=subprocess.DEVNULL)
+                 "--format=csv,noheader,nounits", "-lms", "50", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
     def stop(self):
         if not self.proc:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.12)  # one more sample after the timed region
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        self.f.close()
         sm, smax, reasons = [], None, set()
+        if not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
@@ -171,17 +174,21 @@ def run_ours(args, ws, rank, local):
         tsa.sparse_attn_decode(wl.q_all[t], kv, lens_all[t], K, wl.n_init, wl.n_recent,
                                wl.scale, out=out, lse_out=lse, workspace=work, stream=stream)
 
+    clocks = Clocks(torch.cuda.current_device() if ws == 1 else local)
+    if not args.device_only:
+        clocks.start()  # sampling spans the warm-up and the timed region
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
 
     # ---- device-timed region (per-stage events on the launching stream) ----
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    clocks = Clocks(torch.cuda.current_device() if ws == 1 else local)
+    for e4 in ev:  # torch tracks recording itself; the library re-records these
+        for e in e4:
+            e.record(stream)
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    clocks.start()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -193,7 +200,7 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
-    clk = clocks.stop()
+    clk = clocks.stop() if not args.device_only else None
     total_ms = t0.elapsed_time(t1)
     total_ms = max_over_ranks(total_ms, ws, dev)
     scan_ms = [e[0].elapsed_time(e[1]) for e in ev]
@@ -208,6 +215,16 @@ def run_ours(args, ws, rank, local):
     achieved = ab["scan"] / (scan_avg * 1e-3) / 1e9
     path_gbs = ab["total"] / (ms_per_step * 1e-3) / 1e9
 
+    if args.trace:  # per-CTA timeline of a few more steps (after the timed region)
+        trace_summary = run_trace(args, step, tsa, torch, dev)
+    else:
+        trace_summary = None
+    if args.device_only:  # profiling mode: the device path only
+        return {"workload": name, "us_per_layer_step": round(us_per_layer_step, 3),
+                "stages_ms": {"scan": round(scan_avg, 5),
+                              "select": round(statistics.mean(sel_ms), 5),
+                              "attend+merge": round(statistics.mean(att_ms), 5)},
+                "scan_gbs": round(achieved, 1), "trace": trace_summary} if rank == 0 else None
     # ---- end to end through the public API with host buffers ----
     e2e = run_e2e(args, wl, kv, work, tsa, torch, dev)
 
@@ -241,6 +258,48 @@ def run_ours(args, ws, rank, local):
     if ws > 1:
         torch.distributed.destroy_process_group()
     return res if rank == 0 else None
+
+
+def run_trace(args, step, tsa, torch, dev, nsteps=3):
+    """Run a few steps with the per-CTA trace on and summarise each kernel:
+    span (first CTA start -> last CTA exit), gap from the previous kernel,
+    CTA count and mean per-phase durations (us)."""
+    cap = 1 << 16
+    buf = torch.zeros(64 + 48 * cap, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    tsa.set_trace(buf)
+    for i in range(nsteps):
+        step(10_000 + i)
+    torch.cuda.synchronize()
+    tsa.set_trace(None)
+    recs = tsa.read_trace(buf)
+    names = {1: "scan", 2: "select", 3: "attend", 4: "retopk_selector", 5: "retopk_rescore"}
+    # split records into steps by kernel launch order (records of one launch share the kernel id
+    # and are contiguous in time); group by kernel id and step via start-time clustering
+    recs.sort(key=lambda r: r["t"][0])
+    launches, cur = [], None
+    for r in recs:
+        if cur is None or r["kernel"] != cur["kernel"] or r["t"][0] > cur["end"] + 50_000:
+            cur = {"kernel": r["kernel"], "recs": [], "end": 0}
+            launches.append(cur)
+        cur["recs"].append(r)
+        cur["end"] = max(cur["end"], r["t"][3])
+    out, prev_end = [], None
+    for ln in launches:
+        rs = ln["recs"]
+        t0 = min(r["t"][0] for r in rs)
+        t3 = max(r["t"][3] for r in rs)
+        ph = []
+        for a_, b_ in ((0, 1), (1, 2), (2, 3)):
+            v = [(r["t"][b_] - r["t"][a_]) / 1e3 for r in rs if r["t"][a_] and r["t"][b_]]
+            ph.append(round(sum(v) / len(v), 3) if v else None)
+        out.append({"kernel": names.get(ln["kernel"], ln["kernel"]), "ctas": len(rs),
+                     "span_us": round((t3 - t0) / 1e3, 3),
+                     "gap_us": round((t0 - prev_end) / 1e3, 3) if prev_end else None,
+                     "cta_us_mean": round(sum((r["t"][3] - r["t"][0]) for r in rs) / len(rs) / 1e3, 3),
+                     "phase_us_mean": ph})
+        prev_end = t3
+    return out
 
 
 def run_e2e(args, wl, kv, work, tsa, torch, dev):
@@ -380,6 +439,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--trace", action="store_true",
+                    help="also record a per-CTA kernel timeline of 3 extra steps")
+    ap.add_argument("--device-only", action="store_true",
+                    help="profiling mode: time only the device path (no e2e, no baseline)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

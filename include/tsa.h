@@ -23,8 +23,8 @@
  *   - Element types: q, K, V are bf16 (IEEE binary16-brain, 2 bytes);
  *     outputs are fp32; indices are int32 token positions (0-based).
  *   - Head dimension d must be 128 (the only compiled size).
- *   - GQA: query head h reads KV head h / (Hq / Hkv); Hq % Hkv == 0 and
- *     Hq / Hkv <= 8.
+ *   - GQA: query head h reads KV head h / (Hq / Hkv); Hq % Hkv == 0,
+ *     Hq / Hkv <= 8, B * Hkv <= 512 and B * Hq <= 65535.
  *   - Ownership: the caller allocates every buffer (device memory unless
  *     stated) and the workspace, and owns the stream.  No entry point
  *     allocates, frees, synchronises or prints; launches are asynchronous
@@ -99,6 +99,17 @@ TSA_API const char* tsa_version(void);
  * stream.  events == NULL (or n == 0) turns it off.  The events stay owned by
  * the caller. */
 TSA_API int tsa_set_stage_events(void* const* events, int n);
+
+/* Per-CTA kernel timeline (optional, thread-local).  `buf` is device memory
+ * (64-byte aligned) holding a uint32 record count at offset 0, which the
+ * caller zeroes, followed from offset 64 by records of 48 bytes:
+ *   uint32 kernel (1 scan, 2 select, 3 attend, 4 ReTopK selector,
+ *   5 ReTopK rescore), uint32 CTA (linear block index), uint32 SM id,
+ *   uint32 pad, uint64 t[4] (%globaltimer ns: start, two kernel-specific
+ *   phase marks or 0, exit).
+ * Later calls on this thread append one record per CTA while it fits.
+ * buf == NULL (or too small) turns tracing off. */
+TSA_API int tsa_set_trace(void* buf, size_t bytes);
 
 /* ------------------------------------------------------------------ */
 /* sparse_attn_decode -- [RA] Eq. 1-5 with an exact ("Flat") top-K Omega.

@@ -59,6 +59,7 @@ def _decode(lib, tsa, **kw):
     (dict(d=64), -1),                        # only d = 128 is compiled
     (dict(Hq=6, Hkv=4), -1),                 # Hq % Hkv
     (dict(Hq=18, Hkv=2), -1),                # group size 9 > 8
+    (dict(B=129, Hq=32, Hkv=4), -1),         # B * Hkv > 512
     (dict(K=-1), -1),
     (dict(n_init=-2), -1),
     (dict(q=None), -1),

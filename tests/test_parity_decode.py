@@ -60,7 +60,7 @@ def test_paged_matches_contiguous():
     np.testing.assert_allclose(a[0], c[0], atol=1e-5, rtol=0)
 
 
-@pytest.mark.parametrize("K", [0, 1, 64, 5000, 100000])
+@pytest.mark.parametrize("K", [0, 1, 64, 5000, 50000])
 def test_K_edge_cases(K):
     """K = 0 (window only), K = 1, K >= |P| (every pool position: full softmax)."""
     wl = make_decode("tiny", L0=4500, steps=1)

@@ -23,6 +23,7 @@ from . import build as _build
 __all__ = [
     "TsaError", "lib", "KV", "kv_contiguous", "kv_paged", "decode_workspace_size",
     "sparse_attn_decode", "lse_merge", "ReTopK", "library_path", "set_stage_events",
+    "set_trace", "read_trace",
 ]
 
 TSA_OK = 0
@@ -76,6 +77,7 @@ def lib():
             L.retopk_set_counters.argtypes = [P, i64, C.c_int32]
             L.retopk_destroy.argtypes = [P]
             L.tsa_set_stage_events.argtypes = [C.POINTER(P), i32]
+            L.tsa_set_trace.argtypes = [P, sz]
             _lib = L
     return _lib
 
@@ -112,6 +114,30 @@ def set_stage_events(events) -> None:
         return
     arr = (C.c_void_p * len(events))(*[C.c_void_p(e.cuda_event) for e in events])
     _check(lib().tsa_set_stage_events(arr, len(events)))
+
+
+def set_trace(buf: Optional[torch.Tensor]) -> None:
+    """Per-CTA kernel timeline into a uint8 device tensor (see include/tsa.h);
+    the first 4 bytes count records and must be zeroed by the caller."""
+    if buf is None:
+        _check(lib().tsa_set_trace(None, 0))
+    else:
+        _check(lib().tsa_set_trace(_p(buf), buf.numel()))
+
+
+def read_trace(buf: torch.Tensor):
+    """Decode a trace buffer into a list of dicts (kernel, cta, sm, t0..t3)."""
+    import numpy as np
+    raw = buf.cpu().numpy()
+    n = int(raw[:4].view(np.uint32)[0])
+    cap = (raw.size - 64) // 48
+    rec = raw[64:64 + 48 * min(n, cap)].view(np.uint32).reshape(-1, 12)
+    out = []
+    for r in rec:
+        t = r[4:12].view(np.uint64)
+        out.append({"kernel": int(r[0]), "cta": int(r[1]), "sm": int(r[2]),
+                    "t": [int(x) for x in t]})
+    return out
 
 
 class KV:

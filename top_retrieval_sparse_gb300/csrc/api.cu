@@ -16,6 +16,8 @@
 namespace tsa {
 int attend_split_rows();
 int attend_max_splits();
+int scan_tile_rows();
+int select_chunk();
 }  // namespace tsa
 
 using namespace tsa;
@@ -24,6 +26,7 @@ namespace {
 
 thread_local std::string g_err;
 thread_local cudaEvent_t g_stage[4] = {nullptr, nullptr, nullptr, nullptr};
+thread_local TraceBuf g_trace = {nullptr, nullptr, 0};
 
 // Record stage event i on stream st when stage timing is on.
 cudaError_t stage_mark(int i, cudaStream_t st) {
@@ -65,20 +68,20 @@ int num_sms() {
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
-// Positions per CTA of the selection kernel (multiple of its 16-byte loop).
-constexpr int kSelectChunk = 16384;
 
 // Workspace of one decode call (offsets from the base).
 struct DecodeLayout {
-  size_t zero_begin, status, hist, sel_n, cand_n, tick_sel, tick_att, zero_end;
-  size_t scores, cand, sel_idx, sel_z, part, total;
+  size_t zero_begin, status, hist, sel_n, cand_n, tick_sel, tick_att, tick_unit, zero_end;
+  size_t bstar, scores, cand, sel_idx, sel_z, part, total;
   int64_t stride;  // score row stride (positions)
   int n_wsplit, n_ssplit;
 };
 
-DecodeLayout decode_layout(int B, int Hq, int64_t l_cap, int K, int n_init, int n_recent) {
+DecodeLayout decode_layout(int B, int Hq, int Hkv, int64_t l_cap, int K, int n_init,
+                           int n_recent) {
   DecodeLayout L{};
   const size_t rows = (size_t)B * Hq;
+  const size_t units = (size_t)B * (Hkv > 0 ? Hkv : 1);
   const int sr = attend_split_rows();
   L.stride = (int64_t)up((size_t)(l_cap > 0 ? l_cap : 1), 2048);
   int64_t win = (int64_t)n_init + n_recent;
@@ -93,7 +96,9 @@ DecodeLayout decode_layout(int B, int Hq, int64_t l_cap, int K, int n_init, int 
   L.cand_n = o; o = up(o + rows * 4);
   L.tick_sel = o; o = up(o + rows * 4);
   L.tick_att = o; o = up(o + rows * 4);
+  L.tick_unit = o; o = up(o + units * 4);
   L.zero_end = o;
+  L.bstar = o; o = up(o + rows * 4);
   L.scores = o; o = up(o + rows * (size_t)L.stride * 4);
   L.cand = o; o = up(o + rows * (size_t)L.stride * 4);
   const size_t kk = (size_t)(K > 0 ? K : 1);
@@ -167,12 +172,24 @@ int tsa_set_stage_events(void* const* events, int n) {
   return ok();
 }
 
+int tsa_set_trace(void* buf, size_t bytes) {
+  if (!buf || bytes < 64 + sizeof(TraceRec)) {
+    g_trace = {nullptr, nullptr, 0};
+    return ok();
+  }
+  if (!aligned(buf, 64)) return fail(TSA_ERR_INVALID_ARG, "trace buffer must be 64-byte aligned");
+  g_trace.count = static_cast<uint32_t*>(buf);
+  g_trace.rec = reinterpret_cast<TraceRec*>(static_cast<uint8_t*>(buf) + 64);
+  g_trace.cap = (uint32_t)((bytes - 64) / sizeof(TraceRec));
+  return ok();
+}
+
 size_t tsa_decode_workspace_size(int B, int Hq, int Hkv, int d, int64_t l_cap, int K,
                                  int n_init, int n_recent) {
-  (void)Hkv;
   (void)d;
-  if (B <= 0 || Hq <= 0 || l_cap < 0 || K < 0 || n_init < 0 || n_recent < 0) return 0;
-  return decode_layout(B, Hq, l_cap, K, n_init, n_recent).total;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || l_cap < 0 || K < 0 || n_init < 0 || n_recent < 0)
+    return 0;
+  return decode_layout(B, Hq, Hkv, l_cap, K, n_init, n_recent).total;
 }
 
 int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int B, int Hq,
@@ -189,7 +206,7 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
   if (K < 0 || n_init < 0 || n_recent < 0)
     return fail(TSA_ERR_INVALID_ARG, "K, n_init, n_recent must be >= 0");
   if (!std::isfinite(scale)) return fail(TSA_ERR_INVALID_ARG, "scale must be finite");
-  const DecodeLayout Lw = decode_layout(B, Hq, kv->l_cap, K, n_init, n_recent);
+  const DecodeLayout Lw = decode_layout(B, Hq, Hkv, kv->l_cap, K, n_init, n_recent);
   if (Lw.n_wsplit + Lw.n_ssplit > attend_max_splits())
     return fail(TSA_ERR_INVALID_ARG, "K + window too large (%d splits > %d)",
                 Lw.n_wsplit + Lw.n_ssplit, attend_max_splits());
@@ -228,7 +245,11 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
     s.score_stride = Lw.stride;
     s.hist = hist;
     s.status = status;
-    const int64_t max_tiles = (int64_t)B * Hkv * ((kv->l_cap + 63) / 64);
+    s.K = K;
+    s.unit_ticket = reinterpret_cast<uint32_t*>(ws + Lw.tick_unit);
+    s.bstar = reinterpret_cast<int32_t*>(ws + Lw.bstar);
+    s.trace = g_trace;
+    const int64_t max_tiles = (int64_t)B * Hkv * ((kv->l_cap + scan_tile_rows() - 1) / scan_tile_rows());
     int64_t grid = (int64_t)num_sms() * scan_ctas_per_sm(G);
     if (grid > max_tiles) grid = max_tiles;
     if (grid < 1) grid = 1;
@@ -240,7 +261,8 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
     SelectArgs s{};
     s.scores = scores;
     s.score_stride = Lw.stride;
-    s.hist = hist;
+    s.bstar = reinterpret_cast<const int32_t*>(ws + Lw.bstar);
+    s.trace = g_trace;
     s.lens = lens;
     s.l_cap = kv->l_cap;
     s.B = B;
@@ -248,14 +270,13 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
     s.K = K;
     s.n_init = n_init;
     s.n_recent = n_recent;
-    s.chunk = kSelectChunk;
     s.sel_idx = sel_idx;
     s.sel_z = sel_z;
     s.sel_n = sel_n;
     s.cand_n = reinterpret_cast<int32_t*>(ws + Lw.cand_n);
     s.cand = reinterpret_cast<uint32_t*>(ws + Lw.cand);
     s.ticket = reinterpret_cast<uint32_t*>(ws + Lw.tick_sel);
-    int chunks = (int)((kv->l_cap + kSelectChunk - 1) / kSelectChunk);
+    int chunks = (int)((kv->l_cap + select_chunk() - 1) / select_chunk());
     if (chunks < 1) chunks = 1;
     if ((e = launch_select(s, chunks, st)) != cudaSuccess) return cuda_fail(e, "select launch");
   }
@@ -281,6 +302,8 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
     a.ticket = reinterpret_cast<uint32_t*>(ws + Lw.tick_att);
     a.out = out;
     a.lse_out = lse_out;
+    a.early_window = K > 0;
+    a.trace = g_trace;
     if ((e = launch_attend(a, st)) != cudaSuccess) return cuda_fail(e, "attend launch");
   }
   if ((e = stage_mark(3, st)) != cudaSuccess) return cuda_fail(e, "event record");
@@ -320,8 +343,8 @@ namespace {
 constexpr uint32_t kMagic = 0x52544b31u;  // "RTK1"
 
 struct RetopkLayout {
-  size_t zero_begin, status, hist, sel_n, cand_n, tick_sel, tick_att, tick_rs, zero_end;
-  size_t scores, cand_exact, qbar_new, path, cand, mcand, ehat, sel_idx, sel_z, part, total;
+  size_t zero_begin, status, hist, sel_n, cand_n, tick_sel, tick_att, tick_rs, tick_unit, zero_end;
+  size_t bstar, scores, cand_exact, qbar_new, path, cand, mcand, ehat, sel_idx, sel_z, part, total;
   int64_t stride;
   int cand_cap, n_ssplit;
 };
@@ -342,7 +365,9 @@ RetopkLayout retopk_layout(const tsa_retopk* s) {
   L.tick_sel = o; o = up(o + H * 4);
   L.tick_att = o; o = up(o + H * 4);
   L.tick_rs = o; o = up(o + H * 4);
+  L.tick_unit = o; o = up(o + (size_t)s->Hkv * 4);
   L.zero_end = o;
+  L.bstar = o; o = up(o + H * 4);
   L.scores = o; o = up(o + H * (size_t)L.stride * 4);
   L.cand_exact = o; o = up(o + H * (size_t)L.stride * 4);
   L.qbar_new = o; o = up(o + H * kD * 4);
@@ -511,6 +536,7 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
     a.path_out = path_out;
     a.mcand_out = mcand_out;
     a.cand_out = cand_out;
+    a.trace = g_trace;
     const size_t smem = up((size_t)a.bitmap_words * 4, 16);
     if ((e = launch_retopk_selector(a, smem, s)) != cudaSuccess)
       return cuda_fail(e, "retopk selector launch");
@@ -533,8 +559,12 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
     a.score_stride = Lw.stride;
     a.hist = hist;
     a.status = reinterpret_cast<int*>(ws + Lw.status);
+    a.K = st->K;
+    a.unit_ticket = reinterpret_cast<uint32_t*>(ws + Lw.tick_unit);
+    a.bstar = reinterpret_cast<int32_t*>(ws + Lw.bstar);
+    a.trace = g_trace;
     const int G = Hq / st->Hkv;
-    const int64_t max_tiles = (int64_t)st->Hkv * ((len + 63) / 64);
+    const int64_t max_tiles = (int64_t)st->Hkv * ((len + scan_tile_rows() - 1) / scan_tile_rows());
     int64_t grid = (int64_t)num_sms() * scan_ctas_per_sm(G);
     if (grid > max_tiles) grid = max_tiles;
     if ((e = launch_scan(a, (int)grid, s)) != cudaSuccess) return cuda_fail(e, "scan launch");
@@ -543,7 +573,8 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
     SelectArgs b{};
     b.scores = scores;
     b.score_stride = Lw.stride;
-    b.hist = hist;
+    b.bstar = reinterpret_cast<const int32_t*>(ws + Lw.bstar);
+    b.trace = g_trace;
     b.lens = nullptr;
     b.len_host = len;
     b.l_cap = kv->l_cap;
@@ -554,14 +585,13 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
     b.n_recent = 0;
     b.head_active = path;
     b.active_value = 1;
-    b.chunk = kSelectChunk;
     b.sel_idx = sel_idx;
     b.sel_z = sel_z;
     b.sel_n = sel_n;
     b.cand_n = reinterpret_cast<int32_t*>(ws + Lw.cand_n);
     b.cand = reinterpret_cast<uint32_t*>(ws + Lw.cand_exact);
     b.ticket = reinterpret_cast<uint32_t*>(ws + Lw.tick_sel);
-    const int chunks = (int)((len + kSelectChunk - 1) / kSelectChunk);
+    const int chunks = (int)((len + select_chunk() - 1) / select_chunk());
     if ((e = launch_select(b, chunks, s)) != cudaSuccess) return cuda_fail(e, "select launch");
   }
   // 3. reuse path heads: indexed rescoring + re-top-K over A_t
@@ -582,6 +612,7 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
     a.sel_idx = sel_idx;
     a.sel_z = sel_z;
     a.sel_n = sel_n;
+    a.trace = g_trace;
     const int chunks = (Lw.cand_cap + a.chunk - 1) / a.chunk;
     if ((e = launch_retopk_rescore(a, chunks, s)) != cudaSuccess)
       return cuda_fail(e, "retopk rescore launch");
@@ -615,6 +646,8 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
     a.cache_sup_n = st->sup_n;
     a.C = st->C;
     a.slot = st->fifo_head;
+    a.early_window = 0;
+    a.trace = g_trace;
     if ((e = launch_attend(a, s)) != cudaSuccess) return cuda_fail(e, "attend launch");
   }
   if ((e = stage_mark(3, s)) != cudaSuccess) return cuda_fail(e, "event record");

@@ -8,8 +8,8 @@
 // One grid row per (sequence, query head); each CTA owns a split of 64 rows
 // (window splits first, then selected splits).  A warp gathers 16 rows of V
 // (256-byte rows, 8 bytes per lane, all loads issued before use) and keeps
-// (m, l, o) with its own max; the CTA combines its warps and writes the
-// split partial.  The last CTA of the row (ticket) merges the window splits
+// (m, l, o) with its own max, in base 2 (logits times log2 e, weights by
+// exp2); the CTA combines its warps and writes the split partial.  The last CTA of the row (ticket) merges the window splits
 // into (o_W, z~1, l_W), the selected splits into (o_Omega, z~2, l_Omega),
 // applies Eq. 4-5 and, on a ReTopK step, pushes (qbar, S_t) into the FIFO.
 #include "tsa_internal.cuh"
@@ -22,17 +22,22 @@ constexpr int kAttWarps = kAttThreads / 32;
 constexpr int kSplitRows = 64;
 constexpr int kRowsPerWarp = kSplitRows / kAttWarps;  // 16
 constexpr int kPartStride = kD + 2;                   // o[128], m, l
-constexpr int kMaxSplits = 2048;
+constexpr int kMaxSplits = 1024;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
 struct AttShared {
   float wm[kAttWarps];
   float wl[kAttWarps];
   float wo[kAttWarps][kD];
   float sw[kMaxSplits];  // per-split merge weights (last CTA)
+  float sm[kMaxSplits];  // per-split maxima
+  float sl[kMaxSplits];  // per-split sums
   int last;
 };
 
 __global__ void __launch_bounds__(kAttThreads) attend_kernel(AttendArgs a) {
+  TraceScope trace(a.trace, kTrAttend);
   __shared__ AttShared sh;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int bh = blockIdx.y;
@@ -44,6 +49,9 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(AttendArgs a) {
 
   // ---- rows of this split ----
   const bool is_win = s < a.n_wsplit;
+  // window splits read only the scan's logits: with early_window they run
+  // before the selection kernel (the programmatic predecessor) has finished
+  if (!(is_win && a.early_window)) pdl_wait();
   int64_t nrows;
   int64_t j0;
   if (is_win) {
@@ -54,34 +62,38 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(AttendArgs a) {
     j0 = (int64_t)(s - a.n_wsplit) * kSplitRows;
   }
   const int64_t jw = j0 + wid * kRowsPerWarp;  // this warp's first row
+  // logits are carried in base 2 (z * log2 e) so each weight is one exp2
   float z = -INFINITY;
   int64_t pos = 0;
   if (lane < kRowsPerWarp && jw + lane < nrows) {
     const int64_t j = jw + lane;
     if (is_win) {
       pos = window_pos(j, L, a.n_init, a.n_recent);
-      z = a.scores[(int64_t)bh * a.score_stride + pos];
+      z = __ldcg(a.scores + (int64_t)bh * a.score_stride + pos);
     } else {
       pos = a.sel_idx[(int64_t)bh * a.K + j];
       z = a.sel_z[(int64_t)bh * a.K + j];
     }
+    z *= kLog2e;
   }
   const float m = warp_max(z);
   float l = 0.f;
   float o[4] = {0.f, 0.f, 0.f, 0.f};
   if (m != -INFINITY) {
+    const uint16_t* vbase = a.kv.page_table ? a.kv.v : a.kv.v + kv_row(a.kv, b, g, 0);
     uint2 vv[kRowsPerWarp];
 #pragma unroll
     for (int k = 0; k < kRowsPerWarp; ++k) {
-      const int64_t pk = __shfl_sync(0xffffffffu, pos, k);
+      const int pk = __shfl_sync(0xffffffffu, (int)pos, k);
       const bool valid = jw + k < nrows;
-      vv[k] = valid ? *reinterpret_cast<const uint2*>(a.kv.v + kv_row(a.kv, b, g, pk) + lane * 4)
-                    : make_uint2(0u, 0u);
+      const uint16_t* row = a.kv.page_table ? vbase + kv_row(a.kv, b, g, pk)
+                                            : vbase + (int64_t)pk * kD;
+      vv[k] = valid ? __ldg(reinterpret_cast<const uint2*>(row + lane * 4)) : make_uint2(0u, 0u);
     }
 #pragma unroll
     for (int k = 0; k < kRowsPerWarp; ++k) {
       const float zk = __shfl_sync(0xffffffffu, z, k);
-      const float p = (jw + k < nrows) ? expf(zk - m) : 0.f;
+      const float p = (jw + k < nrows) ? exp2f(zk - m) : 0.f;
       l += p;
       o[0] = fmaf(p, bf_lo(vv[k].x), o[0]);
       o[1] = fmaf(p, bf_hi(vv[k].x), o[1]);
@@ -107,7 +119,7 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(AttendArgs a) {
 #pragma unroll
       for (int w = 0; w < kAttWarps; ++w) {
         if (sh.wm[w] == -INFINITY) continue;
-        const float e = expf(sh.wm[w] - M);
+        const float e = exp2f(sh.wm[w] - M);
         acc = fmaf(e, sh.wo[w][tid], acc);
         lsum = fmaf(e, sh.wl[w], lsum);
       }
@@ -121,6 +133,8 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(AttendArgs a) {
   }
 
   // ---- last CTA of the row merges (Eq. 4-5) ----
+  trace.mark(1);
+  if (is_win && a.early_window) pdl_wait();
   __syncthreads();
   if (tid == 0) {
     __threadfence();
@@ -130,47 +144,48 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(AttendArgs a) {
   __syncthreads();
   if (!sh.last) return;
   __threadfence();
+  trace.mark(2);
 
-  const volatile float* part = a.part + (int64_t)bh * nsplit * kPartStride;
+  const float* part = a.part + (int64_t)bh * nsplit * kPartStride;
+  // split maxima and sums, loaded in parallel (L2: written by other CTAs)
+  for (int i = tid; i < nsplit; i += kAttThreads) {
+    sh.sm[i] = __ldcg(part + (int64_t)i * kPartStride + kD);
+    sh.sl[i] = __ldcg(part + (int64_t)i * kPartStride + kD + 1);
+  }
+  __syncthreads();
   // z~1 (window) and z~2 (selected): maxima of the split maxima
   float z1 = -INFINITY, z2 = -INFINITY;
-  for (int i = 0; i < nsplit; ++i) {
-    const float mi = part[i * kPartStride + kD];
-    if (i < a.n_wsplit) z1 = fmaxf(z1, mi);
-    else z2 = fmaxf(z2, mi);
-  }
-  // per-split rescale to its set's max; l_W and l_Omega
+  for (int i = 0; i < a.n_wsplit; ++i) z1 = fmaxf(z1, sh.sm[i]);
+  for (int i = a.n_wsplit; i < nsplit; ++i) z2 = fmaxf(z2, sh.sm[i]);
+  // per-split rescale to its set's max
   for (int i = tid; i < nsplit; i += kAttThreads) {
-    const float mi = part[i * kPartStride + kD];
+    const float mi = sh.sm[i];
     const float zref = i < a.n_wsplit ? z1 : z2;
-    sh.sw[i] = mi == -INFINITY ? 0.f : expf(mi - zref);
+    sh.sw[i] = mi == -INFINITY ? 0.f : exp2f(mi - zref);
   }
   __syncthreads();
   float lW = 0.f, lO = 0.f, oW = 0.f, oO = 0.f;
-  for (int i = 0; i < nsplit; ++i) {
+  for (int i = 0; i < a.n_wsplit; ++i) {
     const float w = sh.sw[i];
-    if (w == 0.f) continue;
-    const float li = part[i * kPartStride + kD + 1];
-    const float oi = part[i * kPartStride + tid];
-    if (i < a.n_wsplit) {
-      lW = fmaf(w, li, lW);
-      oW = fmaf(w, oi, oW);
-    } else {
-      lO = fmaf(w, li, lO);
-      oO = fmaf(w, oi, oO);
-    }
+    lW = fmaf(w, sh.sl[i], lW);
+    oW = fmaf(w, __ldcg(part + (int64_t)i * kPartStride + tid), oW);
+  }
+  for (int i = a.n_wsplit; i < nsplit; ++i) {
+    const float w = sh.sw[i];
+    lO = fmaf(w, sh.sl[i], lO);
+    oO = fmaf(w, __ldcg(part + (int64_t)i * kPartStride + tid), oO);
   }
   // gamma merge: z~ = max(z~1, z~2); den = sum over W u Omega of e^(z - z~)
   float outv = 0.f, lse = -INFINITY;
   const bool eW = !(lW > 0.f), eO = !(lO > 0.f);
   if (!(eW && eO)) {
     const float zt = eW ? z2 : (eO ? z1 : fmaxf(z1, z2));
-    const float aW = eW ? 0.f : expf(z1 - zt);
-    const float aO = eO ? 0.f : expf(z2 - zt);
+    const float aW = eW ? 0.f : exp2f(z1 - zt);
+    const float aO = eO ? 0.f : exp2f(z2 - zt);
     const float den = aW * lW + aO * lO;
     // g1 o_W + g2 o_Omega with o_W = oW / lW, g1 = aW lW / den (same for Omega)
     outv = (aW * oW + aO * oO) / den;
-    lse = zt + logf(den);
+    lse = (zt + log2f(den)) * kLn2;  // back to natural log
   }
   a.out[(int64_t)bh * kD + tid] = outv;
   if (tid == 0 && a.lse_out) a.lse_out[bh] = lse;
@@ -187,9 +202,17 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(AttendArgs a) {
 }
 
 cudaError_t launch_attend(const AttendArgs& a, cudaStream_t st) {
-  dim3 grid(a.n_wsplit + a.n_ssplit, a.B * a.Hq);
-  attend_kernel<<<grid, kAttThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_wsplit + a.n_ssplit, a.B * a.Hq);
+  cfg.blockDim = dim3(kAttThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attend_kernel, a);
 }
 
 int attend_split_rows() { return kSplitRows; }

@@ -249,11 +249,11 @@ __global__ void __launch_bounds__(kRescoreThreads) retopk_rescore_kernel(RetopkR
   const bool in_smem = M <= kRescoreCache;
   if (in_smem)
     for (int j = tid; j < M; j += kRescoreThreads)
-      cache[j] = rank_key(((volatile float*)erow)[j], crow[j]);
+      cache[j] = rank_key(__ldcg(erow + j), crow[j]);
   __syncthreads();
   auto val = [&](int j) -> uint64_t {
     if (in_smem) return cache[j];
-    return rank_key(((volatile float*)erow)[j], crow[j]);
+    return rank_key(__ldcg(erow + j), crow[j]);
   };
   auto emit = [&](uint64_t v) {
     const int s = atomicAdd(&sh.slot, 1);

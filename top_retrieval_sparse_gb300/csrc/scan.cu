@@ -5,84 +5,113 @@
 // once per KV head and used for all query heads of its group.
 //
 // Design (sm_103a):
-//   * persistent CTAs, a contiguous range of 64-row tiles each, balanced over
-//     the (sequence, KV head) units with at least one active query head;
+//   * persistent CTAs (one per SM, 16 warps), each owning a contiguous range
+//     of 256-row tiles, balanced over the (sequence, KV head) units that have
+//     an active query head;
 //   * tiles stream global -> shared by 1-D bulk copies (cp.async.bulk with an
-//     L2 evict-first hint) into a 4-stage ring completed on mbarriers; a paged
-//     cache issues one copy per page segment of a tile;
-//   * 8 lanes cooperate on one 256-byte row (16 elements each, two 16-byte
-//     shared loads at lane*16 and 128+lane*16: conflict-free), packed fp32x2
-//     FMAs against the group's queries held in registers, then a
-//     reduce-scatter over the 8 lanes leaves one (row, head) logit per lane;
+//     L2 evict-first hint) into a 3-stage ring (64 KiB stages) completed on
+//     mbarriers; a paged cache issues one copy per page segment of a tile;
+//   * the contraction [16 keys x 128] . [128 x 8 heads] runs on the tensor
+//     cores (mma.m16n8k16, bf16 in, fp32 accumulate): each warp owns 16 rows
+//     of a tile, keys are the M operand and the (padded) query heads of the
+//     group the N operand.  The reduction index is permuted identically in
+//     both operands so that every lane reads its A fragment of two k-steps
+//     as one contiguous 16-byte shared load (rows are 256 bytes apart, so a
+//     load phase sees a 2-way bank conflict);
 //   * the pass-1 radix histogram (top 11 bits of the order-preserving key) of
-//     every active head is built in shared memory over positions outside the
-//     static window and flushed to global memory with one atomic per
-//     non-empty bin.
+//     every active head is built in shared memory (two 16-bit counters per
+//     word) over positions outside the static window and flushed to global
+//     memory with one atomic per non-empty bin;
+//   * the last CTA to finish a (sequence, KV head) unit (ticket) turns the
+//     unit's histograms into threshold bins for the selection kernel.
 #include "tsa_internal.cuh"
 #include "tsa_kernels.h"
 
 namespace tsa {
 
-constexpr int kScanThreads = 256;
-constexpr int kTileRows = 64;
-constexpr int kStages = 4;
-constexpr int kTileBytes = kTileRows * kRowBytes;  // 16 KiB
+constexpr int kScanWarps = 16;
+constexpr int kScanThreads = 32 * kScanWarps;
+constexpr int kTileRows = 16 * kScanWarps;         // one m16 block per warp
+constexpr int kTileBytes = kTileRows * kRowBytes;  // 64 KiB
+constexpr int kStages = 3;
+constexpr int kHistWords = kHistBins / 2;          // two 16-bit bins per word
+constexpr int kFlushRows = 65535 - kTileRows;      // flush before a 16-bit bin can wrap
 
-template <int GP>
-struct ScanShape {
-  static constexpr int HG = GP > 4 ? 4 : GP;        // heads per head-group
-  static constexpr int NHG = GP / HG;               // head-groups (1 or 2)
-  static constexpr int TPG = kScanThreads / NHG;    // threads per head-group
-  static constexpr int RPP = TPG / 8;               // rows per pass
-  static constexpr int R = kTileRows / RPP;         // rows per thread per tile
-  static constexpr int NV = R * HG;                 // values per lane before reduce
-  static constexpr int NOUT = NV >= 8 ? NV / 8 : 1; // values per lane after reduce
-};
-
-template <int GP>
+// HP: query heads per KV head rounded up to 1, 2, 4 or 8 (histogram slots).
+template <int HP>
 size_t scan_smem_bytes() {
-  return (size_t)kStages * kTileBytes + (size_t)GP * kHistBins * 4 + kStages * 8 +
+  return (size_t)kStages * kTileBytes + (size_t)HP * kHistWords * 4 + kStages * 8 +
          (kMaxUnits + 1) * 4 + 64;
 }
 
-// Reduce NV per-lane partial sums across the 8 lanes of a row group.
-// After the call lane `lr` holds NOUT complete sums in v[0..NOUT); their
-// original indices are base + i, with base returned.
-template <int NV>
-__device__ __forceinline__ int reduce8(float (&v)[NV], int lr) {
-  int base = 0;
-  int cur = NV;
-#pragma unroll
-  for (int mask = 4; mask >= 1; mask >>= 1) {
-    if (cur >= 2) {
-      const int half = cur / 2;
-      const bool bit = (lr & mask) != 0;
-#pragma unroll
-      for (int i = 0; i < NV / 2; ++i) {
-        if (i < half) {
-          float send = bit ? v[i] : v[i + half];
-          float keep = bit ? v[i + half] : v[i];
-          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
-        }
-      }
-      if (bit) base += half;
-      cur = half;
-    } else {
-      v[0] += __shfl_xor_sync(0xffffffffu, v[0], mask);
-    }
-  }
-  return base;
+// D += A * B, m16n8k16, bf16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int GP>
-__global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
-  using S = ScanShape<GP>;
+// Block-wide: the largest histogram bin b whose suffix count reaches `need`
+// (0 < need <= total), read from global memory.  All threads call; thread 0
+// returns the bin.
+__device__ int find_threshold_bin(const uint32_t* hh, uint32_t need, uint32_t* warp_tot,
+                                  int* out) {
+  constexpr int per = kHistBins / kScanThreads;  // 4 bins per thread, from the top
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  uint32_t c[per], mine = 0;
+#pragma unroll
+  for (int r = 0; r < per; ++r) {
+    c[r] = __ldcg(hh + kHistBins - 1 - (tid * per + r));
+    mine += c[r];
+  }
+  uint32_t incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const uint32_t w = lane < kScanWarps ? warp_tot[lane] : 0u;
+    uint32_t wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    if (lane < kScanWarps) warp_tot[lane] = wi - w;
+  }
+  __syncthreads();
+  uint32_t acc = incl - mine + warp_tot[wid];
+  if (acc < need && acc + mine >= need) {
+#pragma unroll
+    for (int r = 0; r < per; ++r) {
+      if (acc < need && acc + c[r] >= need) *out = kHistBins - 1 - (tid * per + r);
+      acc += c[r];
+    }
+  }
+  __syncthreads();
+  const int v = *out;
+  __syncthreads();
+  return v;
+}
+
+template <int HP>
+__global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
+  TraceScope trace(a.trace, kTrScan);
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kStages * kTileBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(hist + GP * kHistBins);
+  uint64_t* full = reinterpret_cast<uint64_t*>(hist + HP * kHistWords);
   int* unit_tiles = reinterpret_cast<int*>(full + kStages);  // prefix over units
+  __shared__ uint32_t warp_tot[kScanWarps];
+  __shared__ int s_flag, s_bin;
 
+  pdl_trigger();  // the selection kernel may be scheduled as CTAs retire
   const int tid = threadIdx.x;
   const int G = a.Hq / a.kv.Hkv;
   const int nunits = a.B * a.kv.Hkv;
@@ -115,7 +144,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
     }
     if (tid == 0) unit_tiles[nunits] = run;
   }
-  for (int i = tid; i < GP * kHistBins; i += kScanThreads) hist[i] = 0;
+  for (int i = tid; i < HP * kHistWords; i += kScanThreads) hist[i] = 0;
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
     fence_mbar_init();
@@ -123,28 +152,28 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   __syncthreads();
 
   const int total = unit_tiles[nunits];
-  const int t_begin = (int)((int64_t)total * blockIdx.x / gridDim.x);
-  const int t_end = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
+  const int grid = gridDim.x;
+  const int t_begin = (int)((int64_t)total * blockIdx.x / grid);
+  const int t_end = (int)((int64_t)total * (blockIdx.x + 1) / grid);
   const int ntile = t_end - t_begin;
   if (ntile <= 0) return;
 
-  // global tile index -> (unit, tile within the unit)
-  auto locate = [&](int t, int& unit, int& tile) {
+  // global tile index -> unit (last unit whose first tile is <= t)
+  auto locate = [&](int t) {
     int lo = 0, hi = nunits - 1;
-    while (lo < hi) {  // last unit whose first tile is <= t
+    while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (unit_tiles[mid] <= t) lo = mid;
       else hi = mid - 1;
     }
-    unit = lo;
-    tile = t - unit_tiles[lo];
+    return lo;
   };
 
   const uint64_t pol = policy_evict_first();
   // producer (thread 0): stream tile t into stage s
   auto issue = [&](int t, int s) {
-    int unit, tile;
-    locate(t, unit, tile);
+    const int unit = locate(t);
+    const int tile = t - unit_tiles[unit];
     const int b = unit / a.kv.Hkv, g = unit % a.kv.Hkv;
     const int64_t L = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
     const int64_t r0 = (int64_t)tile * kTileRows;
@@ -171,26 +200,63 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
     for (int j = 0; j < pre; ++j) issue(t_begin + j, j);
   }
 
-  // thread roles
-  const int hgi = tid / S::TPG;  // head-group index
-  const int t2 = tid % S::TPG;
-  const int lr = t2 & 7;         // lane within the 8-lane row group
-  const int rp = t2 >> 3;        // row within a pass
+  // mma fragment roles: lane = 4*gr + tq
+  const int warp = tid >> 5, lane = tid & 31;
+  const int gr = lane >> 2;  // A rows gr, gr+8 / B column (query head) gr
+  const int tq = lane & 3;   // k-slot group / C columns 2tq, 2tq+1
 
-  float2 qf[S::HG][8];           // this lane's 16 query elements, per head
-  unsigned act_bits = 0;         // heads (of this head-group) that are active
-  int cur_unit = -1, cur_b = 0, cur_g = 0;
+  uint32_t qb[4][4];         // B fragments: head gr, d in [8(4p+tq), +8) for p < 4
+  float* zrow[2] = {nullptr, nullptr};  // score rows of heads 2tq, 2tq+1 (nullptr: skip)
+  int cur_unit = -1, unit_end = 0, cur_b = 0, cur_g = 0;
   int64_t cur_L = 0;
+  int rows_since_flush = 0;
 
+  // flush the shared histogram of `unit` into global memory (all threads)
   auto flush_hist = [&](int unit) {
     const int b = unit / a.kv.Hkv, g = unit % a.kv.Hkv;
-    for (int i = tid; i < GP * kHistBins; i += kScanThreads) {
-      const uint32_t c = hist[i];
-      if (c) {
-        const int hl = i / kHistBins;
-        atomicAdd(&a.hist[(int64_t)(b * a.Hq + g * G + hl) * kHistBins + (i % kHistBins)], c);
-        hist[i] = 0;
+    __syncthreads();
+    for (int w = tid; w < HP * kHistWords; w += kScanThreads) {
+      const uint32_t v = hist[w];
+      if (v) {
+        const int hl = w / kHistWords;
+        uint32_t* gh = a.hist + (int64_t)(b * a.Hq + g * G + hl) * kHistBins +
+                       2 * (w % kHistWords);
+        if (v & 0xffffu) atomicAdd(gh, v & 0xffffu);
+        if (v >> 16) atomicAdd(gh + 1, v >> 16);
+        hist[w] = 0;
       }
+    }
+    rows_since_flush = 0;
+  };
+  // unit finished by this CTA: flush, add its tiles to the unit ticket; the
+  // CTA that completes the unit computes the threshold bins of its heads
+  auto finish_unit = [&](int unit) {
+    flush_hist(unit);
+    __syncthreads();
+    if (tid == 0) {  // the ticket counts tiles: the CTA completing the count is last
+      const int u0 = unit_tiles[unit], u1 = unit_tiles[unit + 1];
+      const uint32_t mine = (uint32_t)((t_end < u1 ? t_end : u1) - (t_begin > u0 ? t_begin : u0));
+      __threadfence();
+      const uint32_t n = atomicAdd(&a.unit_ticket[unit], mine);
+      s_flag = (n + mine == (uint32_t)(u1 - u0));
+    }
+    __syncthreads();
+    if (!s_flag || a.K <= 0) return;
+    __threadfence();
+    const int b = unit / a.kv.Hkv, g = unit % a.kv.Hkv;
+    const int64_t L = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
+    const int64_t P = L - window_count(L, a.n_init, a.n_recent);
+    const int64_t need = a.K < P ? a.K : P;
+    for (int hl = 0; hl < G; ++hl) {
+      const int bh = b * a.Hq + g * G + hl;
+      if (a.head_active && a.head_active[bh] != a.active_value) continue;
+      int bin = -1;
+      if (need > 0 && need < P) {
+        if (tid == 0) s_bin = -1;
+        bin = find_threshold_bin(a.hist + (int64_t)bh * kHistBins, (uint32_t)need, warp_tot,
+                                 &s_bin);
+      }
+      if (tid == 0) a.bstar[bh] = bin;
     }
   };
 
@@ -198,76 +264,64 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   for (; j < ntile; ++j) {
     const int s = j % kStages;
     const int t = t_begin + j;
-    int unit, tile;
-    locate(t, unit, tile);
-    if (unit != cur_unit) {
-      if (cur_unit >= 0) {
-        __syncthreads();
-        flush_hist(cur_unit);
-        __syncthreads();
-      }
+    if (t >= unit_end) {  // entering a new unit
+      const int unit = locate(t);
+      if (cur_unit >= 0) finish_unit(cur_unit);
       cur_unit = unit;
+      unit_end = unit_tiles[unit + 1];
       cur_b = unit / a.kv.Hkv;
       cur_g = unit % a.kv.Hkv;
       cur_L = seq_len(a.lens, a.len_host, cur_b, a.kv.l_cap);
-      act_bits = 0;
 #pragma unroll
-      for (int i = 0; i < S::HG; ++i) {
-        const int hl = hgi * S::HG + i;
-        const int h = cur_g * G + (hl < G ? hl : 0);
-        if (hl < G && (!a.head_active || a.head_active[cur_b * a.Hq + h] == a.active_value))
-          act_bits |= 1u << i;
-        const uint16_t* qp = a.q + ((int64_t)cur_b * a.Hq + h) * kD;
-        const uint4 w0 = *reinterpret_cast<const uint4*>(qp + lr * 8);
-        const uint4 w1 = *reinterpret_cast<const uint4*>(qp + 64 + lr * 8);
-        const uint32_t ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          qf[i][e] = hl < G ? make_float2(bf_lo(ws[e]), bf_hi(ws[e])) : make_float2(0.f, 0.f);
+      for (int e = 0; e < 2; ++e) {
+        const int hl = 2 * tq + e;
+        const int bh = cur_b * a.Hq + cur_g * G + hl;
+        const bool on = hl < G && (!a.head_active || a.head_active[bh] == a.active_value);
+        zrow[e] = on ? a.scores + (int64_t)bh * a.score_stride : nullptr;
       }
+      const uint16_t* qp = a.q + ((int64_t)cur_b * a.Hq + cur_g * G + (gr < G ? gr : 0)) * kD;
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (gr < G) w = *reinterpret_cast<const uint4*>(qp + 8 * (4 * p + tq));
+        qb[p][0] = w.x; qb[p][1] = w.y; qb[p][2] = w.z; qb[p][3] = w.w;
+      }
+    } else if (rows_since_flush > kFlushRows) {
+      flush_hist(cur_unit);
     }
+    const int tile = t - unit_tiles[cur_unit];
     const bool ok = mbar_wait(&full[s], (uint32_t)((j / kStages) & 1));
     if (__syncthreads_or(!ok)) break;  // uniform decision: leave on timeout
+    if (j == 0) trace.mark(1);
 
-    const uint8_t* tileb = ring + s * kTileBytes;
+    // ---- 16 keys x 8 heads on the tensor cores ----
+    const uint8_t* wb = ring + s * kTileBytes + warp * 16 * kRowBytes;
+    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const uint4 W = *reinterpret_cast<const uint4*>(wb + gr * kRowBytes + 16 * (4 * p + tq));
+      const uint4 X = *reinterpret_cast<const uint4*>(wb + (gr + 8) * kRowBytes + 16 * (4 * p + tq));
+      mma_bf16(c0, W.x, X.x, W.y, X.y, qb[p][0], qb[p][1]);
+      mma_bf16(c1, W.z, X.z, W.w, X.w, qb[p][2], qb[p][3]);
+    }
+    // C: (row gr, head 2tq), (row gr, head 2tq+1), (row gr+8, 2tq), (row gr+8, 2tq+1)
     const int64_t r0 = (int64_t)tile * kTileRows;
-    float v[S::NV];
+    const int64_t rowA = r0 + warp * 16 + gr;
+    const bool pool_tile = r0 >= a.n_init && r0 + kTileRows <= cur_L - a.n_recent;
 #pragma unroll
-    for (int k = 0; k < S::R; ++k) {
-      const uint8_t* rb = tileb + (rp + k * S::RPP) * kRowBytes;
-      const uint4 w0 = *reinterpret_cast<const uint4*>(rb + lr * 16);
-      const uint4 w1 = *reinterpret_cast<const uint4*>(rb + 128 + lr * 16);
-      const uint32_t ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-      float2 acc[S::HG];
-#pragma unroll
-      for (int i = 0; i < S::HG; ++i) acc[i] = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float2 kk = make_float2(bf_lo(ws[e]), bf_hi(ws[e]));
-#pragma unroll
-        for (int i = 0; i < S::HG; ++i) ffma2(acc[i], kk, qf[i][e]);
-      }
-#pragma unroll
-      for (int i = 0; i < S::HG; ++i) v[k * S::HG + i] = acc[i].x + acc[i].y;
-    }
-    const int base = reduce8<S::NV>(v, lr);
-    // lanes holding a duplicate of a value (NV < 8) do not write it
-    const bool owner = (S::NV >= 8) || ((lr & (8 / S::NV - 1)) == 0);
-#pragma unroll
-    for (int o = 0; o < S::NOUT; ++o) {
-      const int idx = base + o;
-      const int k = idx / S::HG;
-      const int il = idx % S::HG;
-      const int64_t i = r0 + rp + k * S::RPP;
-      if (owner && ((act_bits >> il) & 1u) && i < cur_L) {
-        const int hl = hgi * S::HG + il;
-        const int h = cur_g * G + hl;
-        const float z = v[o] * a.scale;
-        a.scores[((int64_t)cur_b * a.Hq + h) * a.score_stride + i] = z;
-        if (!in_window(i, cur_L, a.n_init, a.n_recent))
-          atomicAdd(&hist[hl * kHistBins + (f2key(z) >> kHistShift)], 1u);
+    for (int e = 0; e < 4; ++e) {
+      float* zr = zrow[e & 1];
+      const int64_t i = rowA + ((e >> 1) << 3);
+      if (zr && i < cur_L) {
+        const float z = (c0[e] + c1[e]) * a.scale;
+        zr[i] = z;
+        if (pool_tile || !in_window(i, cur_L, a.n_init, a.n_recent)) {
+          const uint32_t bin = f2key(z) >> kHistShift;
+          atomicAdd(&hist[(2 * tq + (e & 1)) * kHistWords + (bin >> 1)], 1u << ((bin & 1) << 4));
+        }
       }
     }
+    rows_since_flush += kTileRows;
     __syncthreads();  // stage s fully consumed
     if (tid == 0 && j + kStages < ntile) {
       fence_proxy_async();
@@ -285,39 +339,38 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
     __syncthreads();
     return;
   }
-  __syncthreads();
-  if (cur_unit >= 0) flush_hist(cur_unit);
+  trace.mark(2);
+  if (cur_unit >= 0) finish_unit(cur_unit);
 }
 
-template <int GP>
+template <int HP>
 static cudaError_t launch_scan_t(const ScanArgs& a, int grid, cudaStream_t st) {
-  const size_t smem = scan_smem_bytes<GP>();
+  const size_t smem = scan_smem_bytes<HP>();
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(scan_kernel<GP>,
+    cudaError_t e = cudaFuncSetAttribute(scan_kernel<HP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  scan_kernel<GP><<<grid, kScanThreads, smem, st>>>(a);
+  scan_kernel<HP><<<grid, kScanThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
-int scan_padded_group(int G) { return G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8; }
+static int hist_heads(int G) { return G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8; }
 
 int scan_ctas_per_sm(int G) {
-  const int GP = scan_padded_group(G);
-  size_t smem = GP == 1 ? scan_smem_bytes<1>() : GP == 2 ? scan_smem_bytes<2>()
-              : GP == 4 ? scan_smem_bytes<4>() : scan_smem_bytes<8>();
-  int per = (int)((227 * 1024 + 1024) / (smem + 1024));
-  return per < 1 ? 1 : per;
+  (void)G;
+  return 1;
 }
+
+int scan_tile_rows() { return kTileRows; }
 
 cudaError_t launch_scan(const ScanArgs& a, int grid, cudaStream_t st) {
   const int G = a.Hq / a.kv.Hkv;
-  switch (scan_padded_group(G)) {
+  switch (hist_heads(G)) {
     case 1: return launch_scan_t<1>(a, grid, st);
     case 2: return launch_scan_t<2>(a, grid, st);
     case 4: return launch_scan_t<4>(a, grid, st);

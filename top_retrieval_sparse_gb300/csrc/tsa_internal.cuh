@@ -17,7 +17,7 @@ constexpr int kHistBits = 11;                   // pass-1 radix digit
 constexpr int kHistBins = 1 << kHistBits;
 constexpr int kHistShift = 32 - kHistBits;
 constexpr int kMaxGroup = 8;                    // query heads per KV head
-constexpr int kMaxUnits = 1024;                 // B * Hkv limit of one call
+constexpr int kMaxUnits = 512;                  // B * Hkv limit of one call
 constexpr long long kWaitLimitNs = 1000000000;  // bounded waits: 1 s
 
 // Status word codes written by kernels into the workspace (host maps them).
@@ -103,6 +103,15 @@ __device__ __forceinline__ int64_t window_pos(int64_t j, int64_t L, int n_init, 
   return lo + (j - a);
 }
 
+// ------------------------------------------------ programmatic launch
+// Dependent-launch control (sm_90+): a kernel launched with programmatic
+// stream serialization may start before its predecessor finishes; it must
+// call pdl_wait() before touching the predecessor's results.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // -------------------------------------------------------------- PTX: TMA
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -162,6 +171,60 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+
+// ------------------------------------------------------------- tracing
+// Optional per-CTA timeline: when a kernel's argument block carries a trace
+// buffer, thread 0 of every CTA appends one record with the kernel id, the
+// CTA, its SM and up to four %globaltimer stamps (start, two phase marks,
+// exit).  Off (nullptr) costs one predicate per CTA.
+struct TraceRec {
+  uint32_t kernel, block, smid, pad;
+  uint64_t t[4];
+};
+struct TraceBuf {
+  uint32_t* count;   // records appended so far
+  TraceRec* rec;
+  uint32_t cap;
+};
+
+__device__ __forceinline__ uint32_t smid_u32() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %smid;" : "=r"(r));
+  return r;
+}
+
+struct TraceScope {
+  TraceBuf tb;
+  bool on;
+  uint32_t kernel;
+  uint64_t t[4];
+  __device__ TraceScope(const TraceBuf& b, uint32_t k) : tb(b), kernel(k) {
+    on = b.rec != nullptr && threadIdx.x == 0;
+    t[0] = t[1] = t[2] = t[3] = 0;
+    if (on) t[0] = globaltimer_ns();
+  }
+  __device__ void mark(int i) {
+    if (on) t[i] = globaltimer_ns();
+  }
+  __device__ ~TraceScope() {
+    if (on) {
+      t[3] = globaltimer_ns();
+      const uint32_t slot = atomicAdd(tb.count, 1u);
+      if (slot < tb.cap) {
+        TraceRec r;
+        r.kernel = kernel;
+        r.block = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+        r.smid = smid_u32();
+        r.pad = 0;
+        for (int i = 0; i < 4; ++i) r.t[i] = t[i];
+        tb.rec[slot] = r;
+      }
+    }
+  }
+};
+enum TraceKernel : uint32_t {
+  kTrScan = 1, kTrSelect = 2, kTrAttend = 3, kTrSelector = 4, kTrRescore = 5
+};
 
 // ------------------------------------------------------ warp/block utils
 __device__ __forceinline__ float warp_max(float v) {

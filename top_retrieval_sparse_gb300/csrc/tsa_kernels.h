@@ -25,6 +25,14 @@ struct ScanArgs {
   int64_t score_stride;
   uint32_t* hist;            // [B][Hq][kHistBins], zeroed before the launch
   int* status;
+  // threshold bins: the last CTA to finish a (sequence, KV head) unit finds,
+  // for each active head of the unit, the largest bin whose suffix count
+  // reaches min(K, |pool|) and writes it to bstar (-1: every pool position
+  // is selected, or nothing is).  K == 0: no thresholds.
+  int K;
+  uint32_t* unit_ticket;     // [B][Hkv] (zeroed)
+  int32_t* bstar;            // [B][Hq]
+  TraceBuf trace;
 };
 cudaError_t launch_scan(const ScanArgs& a, int grid, cudaStream_t st);
 int scan_ctas_per_sm(int G);
@@ -32,7 +40,7 @@ int scan_ctas_per_sm(int G);
 struct SelectArgs {
   const float* scores;       // [B][Hq][score_stride]
   int64_t score_stride;
-  const uint32_t* hist;      // [B][Hq][kHistBins]
+  const int32_t* bstar;      // [B][Hq] threshold bins from the scan
   const int32_t* lens;
   int64_t len_host;
   int64_t l_cap;             // lengths are clamped to it
@@ -40,13 +48,13 @@ struct SelectArgs {
   int n_init, n_recent;
   const int32_t* head_active;
   int active_value;
-  int chunk;                 // positions per CTA
   int32_t* sel_idx;          // [B][Hq][K]
   float* sel_z;              // [B][Hq][K]
   int32_t* sel_n;            // [B][Hq] counters (zeroed), final |Omega|
   int32_t* cand_n;           // [B][Hq] counters (zeroed)
   uint32_t* cand;            // [B][Hq][score_stride] candidate positions
   uint32_t* ticket;          // [B][Hq] (zeroed)
+  TraceBuf trace;
 };
 cudaError_t launch_select(const SelectArgs& a, int chunks, cudaStream_t st);
 
@@ -73,6 +81,11 @@ struct AttendArgs {
   int32_t* cache_sup;        // [Hq][C][K]
   int32_t* cache_sup_n;      // [Hq][C]
   int C, slot;
+  // window splits may start before the predecessor kernel finishes (set only
+  // when that predecessor is the selection kernel, which itself waited for
+  // the key scan)
+  int early_window;
+  TraceBuf trace;
 };
 cudaError_t launch_attend(const AttendArgs& a, cudaStream_t st);
 
@@ -100,6 +113,7 @@ struct RetopkSelArgs {
   int32_t* path_out;         // optional copies
   int32_t* mcand_out;
   int32_t* cand_out;         // [Hq][cand_cap], -1 padded
+  TraceBuf trace;
 };
 cudaError_t launch_retopk_selector(const RetopkSelArgs& a, size_t smem, cudaStream_t st);
 
@@ -117,6 +131,7 @@ struct RetopkRescoreArgs {
   int32_t* sel_idx;          // [Hq][K]
   float* sel_z;
   int32_t* sel_n;            // [Hq]
+  TraceBuf trace;
 };
 cudaError_t launch_retopk_rescore(const RetopkRescoreArgs& a, int chunks, cudaStream_t st);
 
