@@ -135,6 +135,34 @@ def test_repeated_calls_reuse_workspace():
             check_head(wl, t, 0, h, o[0, h], l[0, h], i[0, h])
 
 
+def test_threshold_hint_fallbacks():
+    """The workspace carries a per-head hint bin between calls; exactness must
+    not depend on it.  A zeroed workspace (hint 0: every pool position is
+    emitted, far too many), a hint left by a workload with much larger logits
+    (hint above the new threshold bin) and a hint from a smaller one must all
+    give the oracle's result."""
+    import top_retrieval_sparse_gb300 as tsa
+    dev = "cuda"
+    big = make_decode("tiny", L0=30_000, steps=1, K=300)
+    small = make_decode("tiny", L0=30_000, steps=1, K=300)
+    small.q_all[:] = (small.q_all.float() * 0.05).to(torch.bfloat16)  # logits ~20x smaller
+    n = tsa.decode_workspace_size(1, big.Hq, big.Hkv, 128, big.lcap, big.K, big.n_init,
+                                  big.n_recent)
+    ws = torch.zeros((n,), dtype=torch.uint8, device=dev)
+    for wl in (big, big, small, big, small, small):
+        kv = tsa.kv_contiguous(wl.k.to(dev), wl.v.to(dev))
+        q = wl.q(0).to(dev).contiguous()
+        lens = torch.tensor(wl.lens(0), dtype=torch.int32, device=dev)
+        lse = torch.empty((1, wl.Hq), device=dev)
+        idx = torch.empty((1, wl.Hq, wl.K), dtype=torch.int32, device=dev)
+        out, _, _, _ = tsa.sparse_attn_decode(q, kv, lens, wl.K, wl.n_init, wl.n_recent,
+                                              wl.scale, lse_out=lse, topk_idx=idx, workspace=ws)
+        torch.cuda.synchronize()
+        o, l, i = out.cpu().numpy(), lse.cpu().numpy(), idx.cpu().numpy()
+        for h in range(wl.Hq):
+            check_head(wl, 0, 0, h, o[0, h], l[0, h], i[0, h])
+
+
 def test_lse_merge_matches_oracle():
     import oracle as orc
     import top_retrieval_sparse_gb300 as tsa

@@ -17,7 +17,6 @@ namespace tsa {
 int attend_split_rows();
 int attend_max_splits();
 int scan_tile_rows();
-int select_chunk();
 }  // namespace tsa
 
 using namespace tsa;
@@ -69,11 +68,29 @@ int num_sms() {
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 
-// Workspace of one decode call (offsets from the base).
+// Device pointers of the exact top-K machinery (scan passes + resolve).
+struct SelWs {
+  int* status;
+  uint32_t* hist;        // zeroed per call
+  uint32_t* tick_unit;   // zeroed per call
+  int32_t* emit_n;       // zeroed per call
+  int32_t* rescan;       // zeroed per call
+  int32_t* hint_bin;     // persists between calls (any content is safe)
+  int32_t* rescan_bin;
+  int32_t* bstar;
+  uint2* cand;
+  int64_t cand_stride;
+  float* wz;
+  int wz_stride;
+};
+
+// Workspace of one decode call (offsets from the base).  [zero_begin,
+// zero_end) is cleared by every call; the hint bins after it persist.
 struct DecodeLayout {
-  size_t zero_begin, status, hist, sel_n, cand_n, tick_sel, tick_att, tick_unit, zero_end;
-  size_t bstar, scores, cand, sel_idx, sel_z, part, total;
-  int64_t stride;  // score row stride (positions)
+  size_t zero_begin, status, hist, sel_n, tick_att, tick_unit, emit_n, rescan, zero_end;
+  size_t hint_bin, rescan_bin, bstar, wz, cand, sel_idx, sel_z, part, total;
+  int64_t cand_stride;
+  int wz_stride;
   int n_wsplit, n_ssplit;
 };
 
@@ -83,9 +100,10 @@ DecodeLayout decode_layout(int B, int Hq, int Hkv, int64_t l_cap, int K, int n_i
   const size_t rows = (size_t)B * Hq;
   const size_t units = (size_t)B * (Hkv > 0 ? Hkv : 1);
   const int sr = attend_split_rows();
-  L.stride = (int64_t)up((size_t)(l_cap > 0 ? l_cap : 1), 2048);
+  L.cand_stride = (int64_t)up((size_t)(l_cap > 0 ? l_cap : 1), 64);
   int64_t win = (int64_t)n_init + n_recent;
   if (win > l_cap) win = l_cap;
+  L.wz_stride = (int)(win > 0 ? win : 1);
   L.n_wsplit = (int)((win + sr - 1) / sr);
   L.n_ssplit = K > 0 ? (K + sr - 1) / sr : (L.n_wsplit == 0 ? 1 : 0);
   size_t o = 0;
@@ -93,20 +111,90 @@ DecodeLayout decode_layout(int B, int Hq, int Hkv, int64_t l_cap, int K, int n_i
   L.status = o; o = up(o + 4);
   L.hist = o; o = up(o + rows * kHistBins * 4);
   L.sel_n = o; o = up(o + rows * 4);
-  L.cand_n = o; o = up(o + rows * 4);
-  L.tick_sel = o; o = up(o + rows * 4);
   L.tick_att = o; o = up(o + rows * 4);
   L.tick_unit = o; o = up(o + units * 4);
+  L.emit_n = o; o = up(o + rows * 4);
+  L.rescan = o; o = up(o + rows * 4);
   L.zero_end = o;
+  L.hint_bin = o; o = up(o + rows * 4);
+  L.rescan_bin = o; o = up(o + rows * 4);
   L.bstar = o; o = up(o + rows * 4);
-  L.scores = o; o = up(o + rows * (size_t)L.stride * 4);
-  L.cand = o; o = up(o + rows * (size_t)L.stride * 4);
+  L.wz = o; o = up(o + rows * (size_t)L.wz_stride * 4);
+  L.cand = o; o = up(o + rows * (size_t)L.cand_stride * 8);
   const size_t kk = (size_t)(K > 0 ? K : 1);
   L.sel_idx = o; o = up(o + rows * kk * 4);
   L.sel_z = o; o = up(o + rows * kk * 4);
   L.part = o; o = up(o + rows * (size_t)(L.n_wsplit + L.n_ssplit) * (kD + 2) * 4);
   L.total = o;
   return L;
+}
+
+// Key scan (pass 0), re-emission for heads whose hint failed (pass 1) and
+// the per-head resolve, all on stream st.  Marks stage events 1 and 2.
+cudaError_t launch_exact_topk(const uint16_t* q, const KvView& view, const int32_t* lens,
+                              int64_t len_host, int64_t max_len, int B, int Hq, int K,
+                              int n_init, int n_recent, float scale,
+                              const int32_t* head_active, int active_value, const SelWs& w,
+                              int32_t* sel_idx, float* sel_z, int32_t* sel_n, cudaStream_t st) {
+  ScanArgs s{};
+  s.q = q;
+  s.kv = view;
+  s.lens = lens;
+  s.len_host = len_host;
+  s.B = B;
+  s.Hq = Hq;
+  s.scale = scale;
+  s.n_init = n_init;
+  s.n_recent = n_recent;
+  s.K = K;
+  s.pass = 0;
+  s.head_active = head_active;
+  s.active_value = active_value;
+  s.hist = w.hist;
+  s.unit_ticket = w.tick_unit;
+  s.hint_bin = w.hint_bin;
+  s.rescan = w.rescan;
+  s.rescan_bin = w.rescan_bin;
+  s.bstar = w.bstar;
+  s.emit_n = w.emit_n;
+  s.cand = w.cand;
+  s.cand_stride = w.cand_stride;
+  s.wz = w.wz;
+  s.wz_stride = w.wz_stride;
+  s.status = w.status;
+  s.trace = g_trace;
+  const int64_t tiles = (int64_t)B * view.Hkv * ((max_len + scan_tile_rows() - 1) / scan_tile_rows());
+  int64_t grid = num_sms();
+  if (grid > tiles) grid = tiles;
+  if (grid < 1) grid = 1;
+  cudaError_t e = launch_scan(s, (int)grid, st, false);
+  if (e != cudaSuccess) return e;
+  if ((e = stage_mark(1, st)) != cudaSuccess) return e;
+  if (K <= 0) return stage_mark(2, st);
+  s.pass = 1;  // heads whose hint failed re-emit with their exact bin
+  s.head_active = w.rescan;
+  s.active_value = 1;
+  if ((e = launch_scan(s, (int)grid, st, true)) != cudaSuccess) return e;
+  ResolveArgs r{};
+  r.lens = lens;
+  r.len_host = len_host;
+  r.l_cap = view.l_cap;
+  r.B = B;
+  r.Hq = Hq;
+  r.K = K;
+  r.n_init = n_init;
+  r.n_recent = n_recent;
+  r.head_active = head_active;
+  r.active_value = active_value;
+  r.emit_n = w.emit_n;
+  r.cand = w.cand;
+  r.cand_stride = w.cand_stride;
+  r.sel_idx = sel_idx;
+  r.sel_z = sel_z;
+  r.sel_n = sel_n;
+  r.trace = g_trace;
+  if ((e = launch_resolve(r, st)) != cudaSuccess) return e;
+  return stage_mark(2, st);
 }
 
 int check_kv(const tsa_kv* kv, int B, int Hkv) {
@@ -222,65 +310,30 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
   if ((e = stage_mark(0, st)) != cudaSuccess) return cuda_fail(e, "event record");
 
   const KvView view = make_view(kv, Hkv);
-  const int G = Hq / Hkv;
-  float* scores = reinterpret_cast<float*>(ws + Lw.scores);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(ws + Lw.hist);
-  int* status = reinterpret_cast<int*>(ws + Lw.status);
   int32_t* sel_idx = topk_idx ? topk_idx : reinterpret_cast<int32_t*>(ws + Lw.sel_idx);
   float* sel_z = topk_score ? topk_score : reinterpret_cast<float*>(ws + Lw.sel_z);
   int32_t* sel_n = reinterpret_cast<int32_t*>(ws + Lw.sel_n);
+  SelWs w{};
+  w.status = reinterpret_cast<int*>(ws + Lw.status);
+  w.hist = reinterpret_cast<uint32_t*>(ws + Lw.hist);
+  w.tick_unit = reinterpret_cast<uint32_t*>(ws + Lw.tick_unit);
+  w.emit_n = reinterpret_cast<int32_t*>(ws + Lw.emit_n);
+  w.rescan = reinterpret_cast<int32_t*>(ws + Lw.rescan);
+  w.hint_bin = reinterpret_cast<int32_t*>(ws + Lw.hint_bin);
+  w.rescan_bin = reinterpret_cast<int32_t*>(ws + Lw.rescan_bin);
+  w.bstar = reinterpret_cast<int32_t*>(ws + Lw.bstar);
+  w.cand = reinterpret_cast<uint2*>(ws + Lw.cand);
+  w.cand_stride = Lw.cand_stride;
+  w.wz = reinterpret_cast<float*>(ws + Lw.wz);
+  w.wz_stride = Lw.wz_stride;
 
-  // 1. key scan + pass-1 histogram
+  // 1-2. key scan, exact top-K outside the window
   if (kv->l_cap > 0) {
-    ScanArgs s{};
-    s.q = static_cast<const uint16_t*>(q);
-    s.kv = view;
-    s.lens = lens;
-    s.B = B;
-    s.Hq = Hq;
-    s.scale = scale;
-    s.n_init = n_init;
-    s.n_recent = n_recent;
-    s.scores = scores;
-    s.score_stride = Lw.stride;
-    s.hist = hist;
-    s.status = status;
-    s.K = K;
-    s.unit_ticket = reinterpret_cast<uint32_t*>(ws + Lw.tick_unit);
-    s.bstar = reinterpret_cast<int32_t*>(ws + Lw.bstar);
-    s.trace = g_trace;
-    const int64_t max_tiles = (int64_t)B * Hkv * ((kv->l_cap + scan_tile_rows() - 1) / scan_tile_rows());
-    int64_t grid = (int64_t)num_sms() * scan_ctas_per_sm(G);
-    if (grid > max_tiles) grid = max_tiles;
-    if (grid < 1) grid = 1;
-    if ((e = launch_scan(s, (int)grid, st)) != cudaSuccess) return cuda_fail(e, "scan launch");
+    if ((e = launch_exact_topk(static_cast<const uint16_t*>(q), view, lens, 0, kv->l_cap, B, Hq,
+                               K, n_init, n_recent, scale, nullptr, 0, w, sel_idx, sel_z, sel_n,
+                               st)) != cudaSuccess)
+      return cuda_fail(e, "top-K launch");
   }
-  if ((e = stage_mark(1, st)) != cudaSuccess) return cuda_fail(e, "event record");
-  // 2. exact top-K outside the window
-  if (K > 0) {
-    SelectArgs s{};
-    s.scores = scores;
-    s.score_stride = Lw.stride;
-    s.bstar = reinterpret_cast<const int32_t*>(ws + Lw.bstar);
-    s.trace = g_trace;
-    s.lens = lens;
-    s.l_cap = kv->l_cap;
-    s.B = B;
-    s.Hq = Hq;
-    s.K = K;
-    s.n_init = n_init;
-    s.n_recent = n_recent;
-    s.sel_idx = sel_idx;
-    s.sel_z = sel_z;
-    s.sel_n = sel_n;
-    s.cand_n = reinterpret_cast<int32_t*>(ws + Lw.cand_n);
-    s.cand = reinterpret_cast<uint32_t*>(ws + Lw.cand);
-    s.ticket = reinterpret_cast<uint32_t*>(ws + Lw.tick_sel);
-    int chunks = (int)((kv->l_cap + select_chunk() - 1) / select_chunk());
-    if (chunks < 1) chunks = 1;
-    if ((e = launch_select(s, chunks, st)) != cudaSuccess) return cuda_fail(e, "select launch");
-  }
-  if ((e = stage_mark(2, st)) != cudaSuccess) return cuda_fail(e, "event record");
   // 3. window + selected partials and the gamma merge
   {
     AttendArgs a{};
@@ -288,8 +341,8 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
     a.lens = lens;
     a.B = B;
     a.Hq = Hq;
-    a.scores = scores;
-    a.score_stride = Lw.stride;
+    a.wz = w.wz;
+    a.wz_stride = w.wz_stride;
     a.n_init = n_init;
     a.n_recent = n_recent;
     a.n_wsplit = Lw.n_wsplit;
@@ -302,12 +355,11 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
     a.ticket = reinterpret_cast<uint32_t*>(ws + Lw.tick_att);
     a.out = out;
     a.lse_out = lse_out;
-    a.early_window = K > 0;
+    a.early_window = K > 0 && kv->l_cap > 0;
     a.trace = g_trace;
     if ((e = launch_attend(a, st)) != cudaSuccess) return cuda_fail(e, "attend launch");
   }
   if ((e = stage_mark(3, st)) != cudaSuccess) return cuda_fail(e, "event record");
-  (void)G;
   return ok();
 }
 
@@ -343,9 +395,10 @@ namespace {
 constexpr uint32_t kMagic = 0x52544b31u;  // "RTK1"
 
 struct RetopkLayout {
-  size_t zero_begin, status, hist, sel_n, cand_n, tick_sel, tick_att, tick_rs, tick_unit, zero_end;
-  size_t bstar, scores, cand_exact, qbar_new, path, cand, mcand, ehat, sel_idx, sel_z, part, total;
-  int64_t stride;
+  size_t zero_begin, status, hist, sel_n, tick_att, tick_rs, tick_unit, emit_n, rescan, zero_end;
+  size_t hint_bin, rescan_bin, bstar, wz, cand_exact, qbar_new, path, cand, mcand, ehat, sel_idx,
+      sel_z, part, total;
+  int64_t cand_stride;
   int cand_cap, n_ssplit;
 };
 
@@ -353,7 +406,7 @@ RetopkLayout retopk_layout(const tsa_retopk* s) {
   RetopkLayout L{};
   const size_t H = (size_t)s->Hq;
   const int sr = attend_split_rows();
-  L.stride = (int64_t)up((size_t)s->max_len, 2048);
+  L.cand_stride = (int64_t)up((size_t)s->max_len, 64);
   L.cand_cap = s->R * s->K + s->W;
   L.n_ssplit = (s->K + sr - 1) / sr;
   size_t o = 0;
@@ -361,15 +414,17 @@ RetopkLayout retopk_layout(const tsa_retopk* s) {
   L.status = o; o = up(o + 4);
   L.hist = o; o = up(o + H * kHistBins * 4);
   L.sel_n = o; o = up(o + H * 4);
-  L.cand_n = o; o = up(o + H * 4);
-  L.tick_sel = o; o = up(o + H * 4);
   L.tick_att = o; o = up(o + H * 4);
   L.tick_rs = o; o = up(o + H * 4);
   L.tick_unit = o; o = up(o + (size_t)s->Hkv * 4);
+  L.emit_n = o; o = up(o + H * 4);
+  L.rescan = o; o = up(o + H * 4);
   L.zero_end = o;
+  L.hint_bin = o; o = up(o + H * 4);
+  L.rescan_bin = o; o = up(o + H * 4);
   L.bstar = o; o = up(o + H * 4);
-  L.scores = o; o = up(o + H * (size_t)L.stride * 4);
-  L.cand_exact = o; o = up(o + H * (size_t)L.stride * 4);
+  L.wz = o; o = up(o + 64);  // no window on this path
+  L.cand_exact = o; o = up(o + H * (size_t)L.cand_stride * 8);
   L.qbar_new = o; o = up(o + H * kD * 4);
   L.path = o; o = up(o + H * 4);
   L.cand = o; o = up(o + H * (size_t)L.cand_cap * 4);
@@ -508,8 +563,19 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
   int32_t* sel_idx = support_out ? support_out : reinterpret_cast<int32_t*>(ws + Lw.sel_idx);
   float* sel_z = reinterpret_cast<float*>(ws + Lw.sel_z);
   int32_t* sel_n = reinterpret_cast<int32_t*>(ws + Lw.sel_n);
-  float* scores = reinterpret_cast<float*>(ws + Lw.scores);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(ws + Lw.hist);
+  SelWs w{};
+  w.status = reinterpret_cast<int*>(ws + Lw.status);
+  w.hist = reinterpret_cast<uint32_t*>(ws + Lw.hist);
+  w.tick_unit = reinterpret_cast<uint32_t*>(ws + Lw.tick_unit);
+  w.emit_n = reinterpret_cast<int32_t*>(ws + Lw.emit_n);
+  w.rescan = reinterpret_cast<int32_t*>(ws + Lw.rescan);
+  w.hint_bin = reinterpret_cast<int32_t*>(ws + Lw.hint_bin);
+  w.rescan_bin = reinterpret_cast<int32_t*>(ws + Lw.rescan_bin);
+  w.bstar = reinterpret_cast<int32_t*>(ws + Lw.bstar);
+  w.cand = reinterpret_cast<uint2*>(ws + Lw.cand_exact);
+  w.cand_stride = Lw.cand_stride;
+  w.wz = reinterpret_cast<float*>(ws + Lw.wz);
+  w.wz_stride = 1;
 
   // 1. selector: cosine recall, path decision, candidate union
   {
@@ -542,58 +608,10 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
       return cuda_fail(e, "retopk selector launch");
   }
   // 2. exact path heads: key scan + exact top-K over all keys (no window)
-  {
-    ScanArgs a{};
-    a.q = static_cast<const uint16_t*>(q);
-    a.kv = view;
-    a.lens = nullptr;
-    a.len_host = len;
-    a.B = 1;
-    a.Hq = Hq;
-    a.scale = scale;
-    a.n_init = 0;
-    a.n_recent = 0;
-    a.head_active = path;
-    a.active_value = 1;
-    a.scores = scores;
-    a.score_stride = Lw.stride;
-    a.hist = hist;
-    a.status = reinterpret_cast<int*>(ws + Lw.status);
-    a.K = st->K;
-    a.unit_ticket = reinterpret_cast<uint32_t*>(ws + Lw.tick_unit);
-    a.bstar = reinterpret_cast<int32_t*>(ws + Lw.bstar);
-    a.trace = g_trace;
-    const int G = Hq / st->Hkv;
-    const int64_t max_tiles = (int64_t)st->Hkv * ((len + scan_tile_rows() - 1) / scan_tile_rows());
-    int64_t grid = (int64_t)num_sms() * scan_ctas_per_sm(G);
-    if (grid > max_tiles) grid = max_tiles;
-    if ((e = launch_scan(a, (int)grid, s)) != cudaSuccess) return cuda_fail(e, "scan launch");
-    if ((e = stage_mark(1, s)) != cudaSuccess) return cuda_fail(e, "event record");
-
-    SelectArgs b{};
-    b.scores = scores;
-    b.score_stride = Lw.stride;
-    b.bstar = reinterpret_cast<const int32_t*>(ws + Lw.bstar);
-    b.trace = g_trace;
-    b.lens = nullptr;
-    b.len_host = len;
-    b.l_cap = kv->l_cap;
-    b.B = 1;
-    b.Hq = Hq;
-    b.K = st->K;
-    b.n_init = 0;
-    b.n_recent = 0;
-    b.head_active = path;
-    b.active_value = 1;
-    b.sel_idx = sel_idx;
-    b.sel_z = sel_z;
-    b.sel_n = sel_n;
-    b.cand_n = reinterpret_cast<int32_t*>(ws + Lw.cand_n);
-    b.cand = reinterpret_cast<uint32_t*>(ws + Lw.cand_exact);
-    b.ticket = reinterpret_cast<uint32_t*>(ws + Lw.tick_sel);
-    const int chunks = (int)((len + select_chunk() - 1) / select_chunk());
-    if ((e = launch_select(b, chunks, s)) != cudaSuccess) return cuda_fail(e, "select launch");
-  }
+  if ((e = launch_exact_topk(static_cast<const uint16_t*>(q), view, nullptr, len, len, 1, Hq,
+                             st->K, 0, 0, scale, path, 1, w, sel_idx, sel_z, sel_n, s)) !=
+      cudaSuccess)
+    return cuda_fail(e, "top-K launch");
   // 3. reuse path heads: indexed rescoring + re-top-K over A_t
   {
     RetopkRescoreArgs a{};
@@ -617,7 +635,6 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
     if ((e = launch_retopk_rescore(a, chunks, s)) != cudaSuccess)
       return cuda_fail(e, "retopk rescore launch");
   }
-  if ((e = stage_mark(2, s)) != cudaSuccess) return cuda_fail(e, "event record");
   // 4. sparse softmax.V over S_t (no window) and the FIFO push
   {
     AttendArgs a{};
@@ -626,8 +643,8 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
     a.len_host = len;
     a.B = 1;
     a.Hq = Hq;
-    a.scores = scores;
-    a.score_stride = Lw.stride;
+    a.wz = w.wz;
+    a.wz_stride = 1;
     a.n_init = 0;
     a.n_recent = 0;
     a.n_wsplit = 0;

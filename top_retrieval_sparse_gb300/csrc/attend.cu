@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(kAttThreads) attend_kernel(AttendArgs a) {
     const int64_t j = jw + lane;
     if (is_win) {
       pos = window_pos(j, L, a.n_init, a.n_recent);
-      z = __ldcg(a.scores + (int64_t)bh * a.score_stride + pos);
+      z = __ldcg(a.wz + (int64_t)bh * a.wz_stride + j);
     } else {
       pos = a.sel_idx[(int64_t)bh * a.K + j];
       z = a.sel_z[(int64_t)bh * a.K + j];

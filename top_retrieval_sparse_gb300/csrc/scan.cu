@@ -18,12 +18,18 @@
 //     both operands so that every lane reads its A fragment of two k-steps
 //     as one contiguous 16-byte shared load (rows are 256 bytes apart, so a
 //     load phase sees a 2-way bank conflict);
-//   * the pass-1 radix histogram (top 11 bits of the order-preserving key) of
-//     every active head is built in shared memory (two 16-bit counters per
-//     word) over positions outside the static window and flushed to global
-//     memory with one atomic per non-empty bin;
-//   * the last CTA to finish a (sequence, KV head) unit (ticket) turns the
-//     unit's histograms into threshold bins for the selection kernel.
+//   * the radix histogram (top 11 bits of the order-preserving key) of every
+//     active head is built in shared memory (two 16-bit counters per word)
+//     over positions outside the static window and flushed to global memory
+//     with one atomic per non-empty bin; window logits are written out;
+//   * pool positions whose bin is >= the head's hint bin are emitted as
+//     (position, logit) pairs (warp-aggregated slot reservation) -- no
+//     logit array is written or re-read;
+//   * the CTA that completes a (sequence, KV head) unit (ticket) finds the
+//     threshold bin b* of each head and checks that the emitted pairs hold
+//     every position of bins >= b*; heads that fail (hint above b*, or far
+//     too many pairs) are re-emitted by a second pass with the exact bin.
+//     Exactness never depends on the hint, only the cost does.
 #include "tsa_internal.cuh"
 #include "tsa_kernels.h"
 
@@ -111,10 +117,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
   __shared__ uint32_t warp_tot[kScanWarps];
   __shared__ int s_flag, s_bin;
 
-  pdl_trigger();  // the selection kernel may be scheduled as CTAs retire
+  if (a.pass == 1) pdl_wait();  // rescan flags come from pass 0
+  pdl_trigger();
   const int tid = threadIdx.x;
   const int G = a.Hq / a.kv.Hkv;
   const int nunits = a.B * a.kv.Hkv;
+  const bool p0 = a.pass == 0;
 
   // ---- prefix of tiles over (sequence, KV head) units with an active head ----
   if (tid < 32) {
@@ -144,7 +152,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
     }
     if (tid == 0) unit_tiles[nunits] = run;
   }
-  for (int i = tid; i < HP * kHistWords; i += kScanThreads) hist[i] = 0;
+  if (p0)
+    for (int i = tid; i < HP * kHistWords; i += kScanThreads) hist[i] = 0;
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
     fence_mbar_init();
@@ -206,8 +215,9 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
   const int tq = lane & 3;   // k-slot group / C columns 2tq, 2tq+1
 
   uint32_t qb[4][4];         // B fragments: head gr, d in [8(4p+tq), +8) for p < 4
-  float* zrow[2] = {nullptr, nullptr};  // score rows of heads 2tq, 2tq+1 (nullptr: skip)
-  int cur_unit = -1, unit_end = 0, cur_b = 0, cur_g = 0;
+  bool on[2] = {false, false};  // heads 2tq, 2tq+1 take part in this pass
+  int hint[2] = {0, 0};         // emission bins of heads 2tq, 2tq+1
+  int cur_unit = -1, unit_end = 0, cur_b = 0, cur_g = 0, head0 = 0;
   int64_t cur_L = 0;
   int rows_since_flush = 0;
 
@@ -228,8 +238,9 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
     }
     rows_since_flush = 0;
   };
-  // unit finished by this CTA: flush, add its tiles to the unit ticket; the
-  // CTA that completes the unit computes the threshold bins of its heads
+  // pass 0: unit finished by this CTA -- flush, add its tiles to the unit
+  // ticket; the CTA that completes the unit decides, per head, the threshold
+  // bin, whether pass 1 must re-emit, and the next call's hint
   auto finish_unit = [&](int unit) {
     flush_hist(unit);
     __syncthreads();
@@ -241,7 +252,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
       s_flag = (n + mine == (uint32_t)(u1 - u0));
     }
     __syncthreads();
-    if (!s_flag || a.K <= 0) return;
+    if (!s_flag) return;
     __threadfence();
     const int b = unit / a.kv.Hkv, g = unit % a.kv.Hkv;
     const int64_t L = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
@@ -250,13 +261,26 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
     for (int hl = 0; hl < G; ++hl) {
       const int bh = b * a.Hq + g * G + hl;
       if (a.head_active && a.head_active[bh] != a.active_value) continue;
-      int bin = -1;
+      const int used = min(max(__ldcg(a.hint_bin + bh), 0), kHistBins - 1);
+      int bin = -1, exact_bin = 0, redo = 0;
       if (need > 0 && need < P) {
         if (tid == 0) s_bin = -1;
         bin = find_threshold_bin(a.hist + (int64_t)bh * kHistBins, (uint32_t)need, warp_tot,
                                  &s_bin);
+        exact_bin = bin;
+        const int64_t emitted = __ldcg(a.emit_n + bh);
+        redo = used > bin || emitted > 4 * need + 4096;
+      } else if (need > 0) {  // every pool position is selected
+        exact_bin = 0;
+        redo = used > 0;
       }
-      if (tid == 0) a.bstar[bh] = bin;
+      if (tid == 0) {
+        a.bstar[bh] = bin;
+        a.rescan[bh] = redo;
+        a.rescan_bin[bh] = exact_bin;
+        if (redo) a.emit_n[bh] = 0;
+        if (need > 0) a.hint_bin[bh] = bin > 0 ? bin - 1 : 0;
+      }
     }
   };
 
@@ -266,27 +290,29 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
     const int t = t_begin + j;
     if (t >= unit_end) {  // entering a new unit
       const int unit = locate(t);
-      if (cur_unit >= 0) finish_unit(cur_unit);
+      if (cur_unit >= 0 && p0) finish_unit(cur_unit);
       cur_unit = unit;
       unit_end = unit_tiles[unit + 1];
       cur_b = unit / a.kv.Hkv;
       cur_g = unit % a.kv.Hkv;
+      head0 = cur_b * a.Hq + cur_g * G;
       cur_L = seq_len(a.lens, a.len_host, cur_b, a.kv.l_cap);
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int hl = 2 * tq + e;
-        const int bh = cur_b * a.Hq + cur_g * G + hl;
-        const bool on = hl < G && (!a.head_active || a.head_active[bh] == a.active_value);
-        zrow[e] = on ? a.scores + (int64_t)bh * a.score_stride : nullptr;
+        const int bh = head0 + hl;
+        on[e] = hl < G && (!a.head_active || a.head_active[bh] == a.active_value);
+        hint[e] = 0;
+        if (on[e]) hint[e] = p0 ? min(max(a.hint_bin[bh], 0), kHistBins - 1) : a.rescan_bin[bh];
       }
-      const uint16_t* qp = a.q + ((int64_t)cur_b * a.Hq + cur_g * G + (gr < G ? gr : 0)) * kD;
+      const uint16_t* qp = a.q + ((int64_t)head0 + (gr < G ? gr : 0)) * kD;
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
         uint4 w = make_uint4(0u, 0u, 0u, 0u);
         if (gr < G) w = *reinterpret_cast<const uint4*>(qp + 8 * (4 * p + tq));
         qb[p][0] = w.x; qb[p][1] = w.y; qb[p][2] = w.z; qb[p][3] = w.w;
       }
-    } else if (rows_since_flush > kFlushRows) {
+    } else if (p0 && rows_since_flush > kFlushRows) {
       flush_hist(cur_unit);
     }
     const int tile = t - unit_tiles[cur_unit];
@@ -308,16 +334,48 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
     const int64_t r0 = (int64_t)tile * kTileRows;
     const int64_t rowA = r0 + warp * 16 + gr;
     const bool pool_tile = r0 >= a.n_init && r0 + kTileRows <= cur_L - a.n_recent;
+    float zv[4];
+    unsigned emit = 0u;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      float* zr = zrow[e & 1];
       const int64_t i = rowA + ((e >> 1) << 3);
-      if (zr && i < cur_L) {
-        const float z = (c0[e] + c1[e]) * a.scale;
-        zr[i] = z;
-        if (pool_tile || !in_window(i, cur_L, a.n_init, a.n_recent)) {
-          const uint32_t bin = f2key(z) >> kHistShift;
-          atomicAdd(&hist[(2 * tq + (e & 1)) * kHistWords + (bin >> 1)], 1u << ((bin & 1) << 4));
+      zv[e] = (c0[e] + c1[e]) * a.scale;
+      if (on[e & 1] && i < cur_L) {
+        const uint32_t bin = f2key(zv[e]) >> kHistShift;
+        if (!pool_tile && in_window(i, cur_L, a.n_init, a.n_recent)) {
+          if (p0) {
+            const int64_t wa = a.n_init < cur_L ? a.n_init : cur_L;
+            const int64_t lo = cur_L - a.n_recent > wa ? cur_L - a.n_recent : wa;
+            const int64_t wj = i < wa ? i : wa + (i - lo);
+            a.wz[(int64_t)(head0 + 2 * tq + (e & 1)) * a.wz_stride + wj] = zv[e];
+          }
+        } else {
+          if (p0)
+            atomicAdd(&hist[(2 * tq + (e & 1)) * kHistWords + (bin >> 1)], 1u << ((bin & 1) << 4));
+          if ((int)bin >= hint[e & 1]) emit |= 1u << e;
+        }
+      }
+    }
+    // emission: one slot reservation per (warp, head) with emitting lanes
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const unsigned m = __ballot_sync(0xffffffffu, (emit >> e) & 1u);
+      if (!m) continue;
+      const int64_t i = rowA + ((e >> 1) << 3);
+#pragma unroll
+      for (int g4 = 0; g4 < 4; ++g4) {
+        const unsigned grp = m & (0x11111111u << g4);
+        if (!grp) continue;
+        const int leader = __ffs(grp) - 1;
+        const int bh = head0 + 2 * g4 + (e & 1);
+        int base = 0;
+        if (lane == leader) base = atomicAdd(&a.emit_n[bh], __popc(grp));
+        base = __shfl_sync(0xffffffffu, base, leader);
+        if ((grp >> lane) & 1u) {
+          const int64_t slot = base + __popc(grp & ((1u << lane) - 1u));
+          if (slot < a.cand_stride)
+            a.cand[(int64_t)bh * a.cand_stride + slot] =
+                make_uint2((uint32_t)i, __float_as_uint(zv[e]));
         }
       }
     }
@@ -340,11 +398,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
     return;
   }
   trace.mark(2);
-  if (cur_unit >= 0) finish_unit(cur_unit);
+  if (cur_unit >= 0 && p0) finish_unit(cur_unit);
 }
 
 template <int HP>
-static cudaError_t launch_scan_t(const ScanArgs& a, int grid, cudaStream_t st) {
+static cudaError_t launch_scan_t(const ScanArgs& a, int grid, cudaStream_t st, bool pdl) {
   const size_t smem = scan_smem_bytes<HP>();
   static int configured[64] = {0};
   int dev = 0;
@@ -355,26 +413,30 @@ static cudaError_t launch_scan_t(const ScanArgs& a, int grid, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  scan_kernel<HP><<<grid, kScanThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kScanThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, scan_kernel<HP>, a);
 }
 
 static int hist_heads(int G) { return G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8; }
 
-int scan_ctas_per_sm(int G) {
-  (void)G;
-  return 1;
-}
-
 int scan_tile_rows() { return kTileRows; }
 
-cudaError_t launch_scan(const ScanArgs& a, int grid, cudaStream_t st) {
+cudaError_t launch_scan(const ScanArgs& a, int grid, cudaStream_t st, bool pdl) {
   const int G = a.Hq / a.kv.Hkv;
   switch (hist_heads(G)) {
-    case 1: return launch_scan_t<1>(a, grid, st);
-    case 2: return launch_scan_t<2>(a, grid, st);
-    case 4: return launch_scan_t<4>(a, grid, st);
-    default: return launch_scan_t<8>(a, grid, st);
+    case 1: return launch_scan_t<1>(a, grid, st, pdl);
+    case 2: return launch_scan_t<2>(a, grid, st, pdl);
+    case 4: return launch_scan_t<4>(a, grid, st, pdl);
+    default: return launch_scan_t<8>(a, grid, st, pdl);
   }
 }
 

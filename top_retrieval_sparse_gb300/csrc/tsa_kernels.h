@@ -11,6 +11,15 @@ namespace tsa {
 
 // Per-head activity filter: a head takes part iff
 // head_active == nullptr || head_active[b*Hq + h] == active_value.
+//
+// Key scan, pass 0: logits of every active head; window logits go to wz, pool
+// positions feed the 11-bit histogram and are emitted as (position, logit)
+// pairs when their bin is >= the head's hint bin.  The CTA that completes a
+// (sequence, KV head) unit turns the histograms into the threshold bin b*
+// and decides per head whether the emitted pairs provably contain the top-K
+// (hint <= b* and not too many emitted); if not, the head is flagged for
+// pass 1, which re-emits with the exact bin (b*, or 0 when every pool
+// position is selected).  The hint for the next call is b* - 1.
 struct ScanArgs {
   const uint16_t* q;         // bf16 [B][Hq][128]
   KvView kv;
@@ -18,53 +27,54 @@ struct ScanArgs {
   int64_t len_host;
   int B, Hq;
   float scale;
-  int n_init, n_recent;      // window excluded from the histogram
+  int n_init, n_recent;      // static window (logits to wz, not emitted)
+  int K;                     // top-K budget
+  int pass;                  // 0 or 1
   const int32_t* head_active;
   int active_value;
-  float* scores;             // [B][Hq][score_stride]
-  int64_t score_stride;
-  uint32_t* hist;            // [B][Hq][kHistBins], zeroed before the launch
+  uint32_t* hist;            // [B][Hq][kHistBins] (zeroed), pass 0
+  uint32_t* unit_ticket;     // [B][Hkv] (zeroed), pass 0
+  int32_t* hint_bin;         // [B][Hq] persistent across calls (any value is safe)
+  int32_t* rescan;           // [B][Hq] (zeroed) 1: pass 1 needed; pass 1 reads it
+  int32_t* rescan_bin;       // [B][Hq] exact emission bin for pass 1
+  int32_t* bstar;            // [B][Hq] threshold bin (-1: all pool / none)
+  int32_t* emit_n;           // [B][Hq] (zeroed) emitted pairs
+  uint2* cand;               // [B][Hq][cand_stride] (position, logit bits)
+  int64_t cand_stride;       // >= l_cap
+  float* wz;                 // [B][Hq][wz_stride] window logits, pass 0
+  int wz_stride;
   int* status;
-  // threshold bins: the last CTA to finish a (sequence, KV head) unit finds,
-  // for each active head of the unit, the largest bin whose suffix count
-  // reaches min(K, |pool|) and writes it to bstar (-1: every pool position
-  // is selected, or nothing is).  K == 0: no thresholds.
-  int K;
-  uint32_t* unit_ticket;     // [B][Hkv] (zeroed)
-  int32_t* bstar;            // [B][Hq]
   TraceBuf trace;
 };
-cudaError_t launch_scan(const ScanArgs& a, int grid, cudaStream_t st);
-int scan_ctas_per_sm(int G);
+cudaError_t launch_scan(const ScanArgs& a, int grid, cudaStream_t st, bool pdl);
 
-struct SelectArgs {
-  const float* scores;       // [B][Hq][score_stride]
-  int64_t score_stride;
-  const int32_t* bstar;      // [B][Hq] threshold bins from the scan
+// Resolve: one CTA per head keeps the top min(K, |pool|) of the emitted
+// pairs (ties to the smaller position) and writes the selected set.
+struct ResolveArgs {
   const int32_t* lens;
   int64_t len_host;
-  int64_t l_cap;             // lengths are clamped to it
+  int64_t l_cap;
   int B, Hq, K;
   int n_init, n_recent;
   const int32_t* head_active;
   int active_value;
+  const int32_t* emit_n;
+  const uint2* cand;
+  int64_t cand_stride;
   int32_t* sel_idx;          // [B][Hq][K]
   float* sel_z;              // [B][Hq][K]
-  int32_t* sel_n;            // [B][Hq] counters (zeroed), final |Omega|
-  int32_t* cand_n;           // [B][Hq] counters (zeroed)
-  uint32_t* cand;            // [B][Hq][score_stride] candidate positions
-  uint32_t* ticket;          // [B][Hq] (zeroed)
+  int32_t* sel_n;            // [B][Hq]
   TraceBuf trace;
 };
-cudaError_t launch_select(const SelectArgs& a, int chunks, cudaStream_t st);
+cudaError_t launch_resolve(const ResolveArgs& a, cudaStream_t st);
 
 struct AttendArgs {
   KvView kv;
   const int32_t* lens;
   int64_t len_host;
   int B, Hq;
-  const float* scores;       // window logits, [B][Hq][score_stride]
-  int64_t score_stride;
+  const float* wz;           // window logits, [B][Hq][wz_stride]
+  int wz_stride;
   int n_init, n_recent;
   int n_wsplit, n_ssplit;    // splits per head (window, selected)
   const int32_t* sel_idx;    // [B][Hq][K]
