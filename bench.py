@@ -273,7 +273,8 @@ def run_trace(args, step, tsa, torch, dev, nsteps=3):
     torch.cuda.synchronize()
     tsa.set_trace(None)
     recs = tsa.read_trace(buf)
-    names = {1: "scan", 2: "select", 3: "attend", 4: "retopk_selector", 5: "retopk_rescore"}
+    names = {1: "scan", 2: "resolve", 3: "attend", 4: "retopk_selector", 5: "retopk_rescore",
+             6: "scan_pass1"}
     # split records into steps by kernel launch order (records of one launch share the kernel id
     # and are contiguous in time); group by kernel id and step via start-time clustering
     recs.sort(key=lambda r: r["t"][0])

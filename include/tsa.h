@@ -103,8 +103,9 @@ TSA_API int tsa_set_stage_events(void* const* events, int n);
 /* Per-CTA kernel timeline (optional, thread-local).  `buf` is device memory
  * (64-byte aligned) holding a uint32 record count at offset 0, which the
  * caller zeroes, followed from offset 64 by records of 48 bytes:
- *   uint32 kernel (1 scan, 2 select, 3 attend, 4 ReTopK selector,
- *   5 ReTopK rescore), uint32 CTA (linear block index), uint32 SM id,
+ *   uint32 kernel (1 key scan, 2 top-K resolve, 3 attend, 4 ReTopK
+ *   selector, 5 ReTopK rescore, 6 key scan re-emission pass), uint32 CTA
+ *   (linear block index), uint32 SM id,
  *   uint32 pad, uint64 t[4] (%globaltimer ns: start, two kernel-specific
  *   phase marks or 0, exit).
  * Later calls on this thread append one record per CTA while it fits.

@@ -14,8 +14,6 @@
 #include "tsa_kernels.h"
 
 namespace tsa {
-int attend_split_rows();
-int attend_max_splits();
 int scan_tile_rows();
 }  // namespace tsa
 
@@ -53,6 +51,12 @@ int cuda_fail(cudaError_t e, const char* what) {
 constexpr size_t kAlign = 256;
 size_t up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 
+// Dense pair list capacity per head: every position once plus the sentinel
+// padding of at most 7 slots per (CTA, warp) run.
+int64_t dense_stride_for(int64_t l_cap) {
+  return (int64_t)up((size_t)(l_cap > 0 ? l_cap : 1) + 32768, 64);
+}
+
 int num_sms() {
   static int sms[64] = {0};
   int dev = 0;
@@ -78,8 +82,10 @@ struct SelWs {
   int32_t* hint_bin;     // persists between calls (any content is safe)
   int32_t* rescan_bin;
   int32_t* bstar;
-  uint2* cand;
-  int64_t cand_stride;
+  uint2* dense;
+  int32_t* dense_n;
+  int64_t dense_stride;
+  uint64_t* spill;
   float* wz;
   int wz_stride;
 };
@@ -87,11 +93,10 @@ struct SelWs {
 // Workspace of one decode call (offsets from the base).  [zero_begin,
 // zero_end) is cleared by every call; the hint bins after it persist.
 struct DecodeLayout {
-  size_t zero_begin, status, hist, sel_n, tick_att, tick_unit, emit_n, rescan, zero_end;
-  size_t hint_bin, rescan_bin, bstar, wz, cand, sel_idx, sel_z, part, total;
-  int64_t cand_stride;
+  size_t zero_begin, status, hist, sel_n, tick_unit, emit_n, dense_n, rescan, zero_end;
+  size_t hint_bin, rescan_bin, bstar, wz, dense, spill, sel_idx, sel_z, total;
+  int64_t dense_stride;
   int wz_stride;
-  int n_wsplit, n_ssplit;
 };
 
 DecodeLayout decode_layout(int B, int Hq, int Hkv, int64_t l_cap, int K, int n_init,
@@ -99,32 +104,29 @@ DecodeLayout decode_layout(int B, int Hq, int Hkv, int64_t l_cap, int K, int n_i
   DecodeLayout L{};
   const size_t rows = (size_t)B * Hq;
   const size_t units = (size_t)B * (Hkv > 0 ? Hkv : 1);
-  const int sr = attend_split_rows();
-  L.cand_stride = (int64_t)up((size_t)(l_cap > 0 ? l_cap : 1), 64);
+  L.dense_stride = dense_stride_for(l_cap);
   int64_t win = (int64_t)n_init + n_recent;
   if (win > l_cap) win = l_cap;
   L.wz_stride = (int)(win > 0 ? win : 1);
-  L.n_wsplit = (int)((win + sr - 1) / sr);
-  L.n_ssplit = K > 0 ? (K + sr - 1) / sr : (L.n_wsplit == 0 ? 1 : 0);
   size_t o = 0;
   L.zero_begin = o;
   L.status = o; o = up(o + 4);
   L.hist = o; o = up(o + rows * kHistBins * 4);
   L.sel_n = o; o = up(o + rows * 4);
-  L.tick_att = o; o = up(o + rows * 4);
   L.tick_unit = o; o = up(o + units * 4);
   L.emit_n = o; o = up(o + rows * 4);
+  L.dense_n = o; o = up(o + rows * 4);
   L.rescan = o; o = up(o + rows * 4);
   L.zero_end = o;
   L.hint_bin = o; o = up(o + rows * 4);
   L.rescan_bin = o; o = up(o + rows * 4);
   L.bstar = o; o = up(o + rows * 4);
   L.wz = o; o = up(o + rows * (size_t)L.wz_stride * 4);
-  L.cand = o; o = up(o + rows * (size_t)L.cand_stride * 8);
+  L.dense = o; o = up(o + rows * (size_t)L.dense_stride * 8);
+  L.spill = o; o = up(o + rows * (size_t)L.dense_stride * 8);
   const size_t kk = (size_t)(K > 0 ? K : 1);
   L.sel_idx = o; o = up(o + rows * kk * 4);
   L.sel_z = o; o = up(o + rows * kk * 4);
-  L.part = o; o = up(o + rows * (size_t)(L.n_wsplit + L.n_ssplit) * (kD + 2) * 4);
   L.total = o;
   return L;
 }
@@ -157,8 +159,9 @@ cudaError_t launch_exact_topk(const uint16_t* q, const KvView& view, const int32
   s.rescan_bin = w.rescan_bin;
   s.bstar = w.bstar;
   s.emit_n = w.emit_n;
-  s.cand = w.cand;
-  s.cand_stride = w.cand_stride;
+  s.dense = w.dense;
+  s.dense_n = w.dense_n;
+  s.dense_stride = w.dense_stride;
   s.wz = w.wz;
   s.wz_stride = w.wz_stride;
   s.status = w.status;
@@ -186,9 +189,11 @@ cudaError_t launch_exact_topk(const uint16_t* q, const KvView& view, const int32
   r.n_recent = n_recent;
   r.head_active = head_active;
   r.active_value = active_value;
-  r.emit_n = w.emit_n;
-  r.cand = w.cand;
-  r.cand_stride = w.cand_stride;
+  r.bstar = w.bstar;
+  r.dense = w.dense;
+  r.dense_n = w.dense_n;
+  r.dense_stride = w.dense_stride;
+  r.spill = w.spill;
   r.sel_idx = sel_idx;
   r.sel_z = sel_z;
   r.sel_n = sel_n;
@@ -295,9 +300,6 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
     return fail(TSA_ERR_INVALID_ARG, "K, n_init, n_recent must be >= 0");
   if (!std::isfinite(scale)) return fail(TSA_ERR_INVALID_ARG, "scale must be finite");
   const DecodeLayout Lw = decode_layout(B, Hq, Hkv, kv->l_cap, K, n_init, n_recent);
-  if (Lw.n_wsplit + Lw.n_ssplit > attend_max_splits())
-    return fail(TSA_ERR_INVALID_ARG, "K + window too large (%d splits > %d)",
-                Lw.n_wsplit + Lw.n_ssplit, attend_max_splits());
   if (!workspace || !aligned(workspace, kAlign))
     return fail(TSA_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
   if (ws_bytes < Lw.total)
@@ -322,8 +324,10 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
   w.hint_bin = reinterpret_cast<int32_t*>(ws + Lw.hint_bin);
   w.rescan_bin = reinterpret_cast<int32_t*>(ws + Lw.rescan_bin);
   w.bstar = reinterpret_cast<int32_t*>(ws + Lw.bstar);
-  w.cand = reinterpret_cast<uint2*>(ws + Lw.cand);
-  w.cand_stride = Lw.cand_stride;
+  w.dense = reinterpret_cast<uint2*>(ws + Lw.dense);
+  w.dense_n = reinterpret_cast<int32_t*>(ws + Lw.dense_n);
+  w.dense_stride = Lw.dense_stride;
+  w.spill = reinterpret_cast<uint64_t*>(ws + Lw.spill);
   w.wz = reinterpret_cast<float*>(ws + Lw.wz);
   w.wz_stride = Lw.wz_stride;
 
@@ -345,17 +349,13 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
     a.wz_stride = w.wz_stride;
     a.n_init = n_init;
     a.n_recent = n_recent;
-    a.n_wsplit = Lw.n_wsplit;
-    a.n_ssplit = Lw.n_ssplit;
+    a.window = 1;
     a.sel_idx = sel_idx;
     a.sel_z = sel_z;
     a.sel_n = sel_n;
     a.K = K;
-    a.part = reinterpret_cast<float*>(ws + Lw.part);
-    a.ticket = reinterpret_cast<uint32_t*>(ws + Lw.tick_att);
     a.out = out;
     a.lse_out = lse_out;
-    a.early_window = K > 0 && kv->l_cap > 0;
     a.trace = g_trace;
     if ((e = launch_attend(a, st)) != cudaSuccess) return cuda_fail(e, "attend launch");
   }
@@ -395,36 +395,35 @@ namespace {
 constexpr uint32_t kMagic = 0x52544b31u;  // "RTK1"
 
 struct RetopkLayout {
-  size_t zero_begin, status, hist, sel_n, tick_att, tick_rs, tick_unit, emit_n, rescan, zero_end;
-  size_t hint_bin, rescan_bin, bstar, wz, cand_exact, qbar_new, path, cand, mcand, ehat, sel_idx,
-      sel_z, part, total;
-  int64_t cand_stride;
-  int cand_cap, n_ssplit;
+  size_t zero_begin, status, hist, sel_n, tick_rs, tick_unit, emit_n, dense_n, rescan, zero_end;
+  size_t hint_bin, rescan_bin, bstar, wz, dense, spill, qbar_new, path, cand, mcand, ehat,
+      sel_idx, sel_z, total;
+  int64_t dense_stride;
+  int cand_cap;
 };
 
 RetopkLayout retopk_layout(const tsa_retopk* s) {
   RetopkLayout L{};
   const size_t H = (size_t)s->Hq;
-  const int sr = attend_split_rows();
-  L.cand_stride = (int64_t)up((size_t)s->max_len, 64);
+  L.dense_stride = dense_stride_for(s->max_len);
   L.cand_cap = s->R * s->K + s->W;
-  L.n_ssplit = (s->K + sr - 1) / sr;
   size_t o = 0;
   L.zero_begin = o;
   L.status = o; o = up(o + 4);
   L.hist = o; o = up(o + H * kHistBins * 4);
   L.sel_n = o; o = up(o + H * 4);
-  L.tick_att = o; o = up(o + H * 4);
   L.tick_rs = o; o = up(o + H * 4);
   L.tick_unit = o; o = up(o + (size_t)s->Hkv * 4);
   L.emit_n = o; o = up(o + H * 4);
+  L.dense_n = o; o = up(o + H * 4);
   L.rescan = o; o = up(o + H * 4);
   L.zero_end = o;
   L.hint_bin = o; o = up(o + H * 4);
   L.rescan_bin = o; o = up(o + H * 4);
   L.bstar = o; o = up(o + H * 4);
   L.wz = o; o = up(o + 64);  // no window on this path
-  L.cand_exact = o; o = up(o + H * (size_t)L.cand_stride * 8);
+  L.dense = o; o = up(o + H * (size_t)L.dense_stride * 8);
+  L.spill = o; o = up(o + H * (size_t)L.dense_stride * 8);
   L.qbar_new = o; o = up(o + H * kD * 4);
   L.path = o; o = up(o + H * 4);
   L.cand = o; o = up(o + H * (size_t)L.cand_cap * 4);
@@ -432,7 +431,6 @@ RetopkLayout retopk_layout(const tsa_retopk* s) {
   L.ehat = o; o = up(o + H * (size_t)L.cand_cap * 4);
   L.sel_idx = o; o = up(o + H * (size_t)s->K * 4);
   L.sel_z = o; o = up(o + H * (size_t)s->K * 4);
-  L.part = o; o = up(o + H * (size_t)L.n_ssplit * (kD + 2) * 4);
   L.total = o;
   return L;
 }
@@ -472,8 +470,6 @@ int retopk_create(tsa_retopk** st, int Hq, int Hkv, int d, int K, int C, int R, 
     return fail(TSA_ERR_INVALID_ARG, "max_len must be in [1, %lld]", (long long)kMaxBitmapLen);
   if ((int64_t)R * K + W > 8192)
     return fail(TSA_ERR_INVALID_ARG, "R*K + W = %lld > 8192", (long long)R * K + W);
-  if ((K + attend_split_rows() - 1) / attend_split_rows() > attend_max_splits())
-    return fail(TSA_ERR_INVALID_ARG, "K too large");
   if (!state_mem || !aligned(state_mem, kAlign))
     return fail(TSA_ERR_INVALID_ARG, "state_mem NULL or not 256-byte aligned");
   if (state_bytes_ < state_bytes(Hq, K, C))
@@ -572,8 +568,10 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
   w.hint_bin = reinterpret_cast<int32_t*>(ws + Lw.hint_bin);
   w.rescan_bin = reinterpret_cast<int32_t*>(ws + Lw.rescan_bin);
   w.bstar = reinterpret_cast<int32_t*>(ws + Lw.bstar);
-  w.cand = reinterpret_cast<uint2*>(ws + Lw.cand_exact);
-  w.cand_stride = Lw.cand_stride;
+  w.dense = reinterpret_cast<uint2*>(ws + Lw.dense);
+  w.dense_n = reinterpret_cast<int32_t*>(ws + Lw.dense_n);
+  w.dense_stride = Lw.dense_stride;
+  w.spill = reinterpret_cast<uint64_t*>(ws + Lw.spill);
   w.wz = reinterpret_cast<float*>(ws + Lw.wz);
   w.wz_stride = 1;
 
@@ -647,14 +645,11 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
     a.wz_stride = 1;
     a.n_init = 0;
     a.n_recent = 0;
-    a.n_wsplit = 0;
-    a.n_ssplit = Lw.n_ssplit;
+    a.window = 0;
     a.sel_idx = sel_idx;
     a.sel_z = sel_z;
     a.sel_n = sel_n;
     a.K = st->K;
-    a.part = reinterpret_cast<float*>(ws + Lw.part);
-    a.ticket = reinterpret_cast<uint32_t*>(ws + Lw.tick_att);
     a.out = out;
     a.lse_out = lse_out;
     a.push_qbar = qbar_new;
@@ -663,7 +658,6 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
     a.cache_sup_n = st->sup_n;
     a.C = st->C;
     a.slot = st->fifo_head;
-    a.early_window = 0;
     a.trace = g_trace;
     if ((e = launch_attend(a, s)) != cudaSuccess) return cuda_fail(e, "attend launch");
   }

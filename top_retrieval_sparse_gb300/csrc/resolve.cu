@@ -5,23 +5,26 @@
 // S_t = TopK(e, K).  Ties go to the smaller position.
 //
 // The scan emitted, for every head, the (position, logit) pairs of all pool
-// positions whose radix bin is at least its emission bin, and checked that
-// this bin does not exceed the threshold bin b* -- so the emitted pairs hold
-// the whole top-K.  One CTA per head keeps the min(K, |pool|) largest by the
-// 64-bit value (order-preserving logit key, ~position) with a CTA radix
-// select over the pairs, held in shared memory when they fit.  Launched as a
-// programmatic dependent of the scan.
+// positions whose radix bin is at least its emission bin into the head's
+// dense list (sentinel-padded runs), and checked that this bin does not
+// exceed the threshold bin b* -- so the list holds the whole top-K.  One CTA
+// per head reads the list once, coalesced: pairs above b* are selected
+// outright, pairs in b* are compacted into shared memory (a global spill past
+// its capacity) and the remaining need is met by a CTA radix select on the
+// 64-bit value (order-preserving logit key, ~position) with b*'s 11 bits
+// known.  Launched as a programmatic dependent of the scan.
 #include "tsa_internal.cuh"
 #include "tsa_kernels.h"
 
 namespace tsa {
 
 constexpr int kResThreads = 512;
-constexpr int kResCache = 12288;  // pairs cached in shared memory (96 KiB)
+constexpr int kResCache = 16384;  // threshold-bin candidates in shared memory (128 KiB)
 
 struct ResShared {
   RadixScratch rs;
-  int slot;
+  int slot;   // selected so far
+  int ncand;  // threshold-bin candidates
 };
 
 __global__ void __launch_bounds__(kResThreads) resolve_kernel(ResolveArgs a) {
@@ -31,8 +34,9 @@ __global__ void __launch_bounds__(kResThreads) resolve_kernel(ResolveArgs a) {
   const int tid = threadIdx.x;
   const int bh = blockIdx.x;
   const int b = bh / a.Hq;
-  pdl_wait();     // the emitted pairs and counts come from the scan
-  pdl_trigger();  // let the attention kernel start its window splits
+  pdl_wait();     // the emitted pairs come from the scan
+  pdl_trigger();  // the attention kernel may be scheduled
+  trace.mark(1);
   if (a.head_active && a.head_active[bh] != a.active_value) return;
 
   const int64_t L = seq_len(a.lens, a.len_host, b, a.l_cap);
@@ -41,33 +45,67 @@ __global__ void __launch_bounds__(kResThreads) resolve_kernel(ResolveArgs a) {
   int32_t* sidx = a.sel_idx + (int64_t)bh * a.K;
   float* sz = a.sel_z + (int64_t)bh * a.K;
   if (need > 0) {
-    int64_t n64 = __ldcg(a.emit_n + bh);
-    if (n64 > a.cand_stride) n64 = a.cand_stride;
+    int64_t n64 = __ldcg(a.dense_n + bh);
+    if (n64 > a.dense_stride) n64 = a.dense_stride;
     const int n = (int)n64;
-    const uint2* row = a.cand + (int64_t)bh * a.cand_stride;
-    const bool in_smem = n <= kResCache;
-    if (in_smem)
-      for (int j = tid; j < n; j += kResThreads) {
-        const uint2 p = __ldcg(row + j);
-        cache[j] = rank_key(__uint_as_float(p.y), p.x);
-      }
-    if (tid == 0) sh.slot = 0;
+    const uint2* row = a.dense + (int64_t)bh * a.dense_stride;
+    uint64_t* spill = a.spill + (int64_t)bh * a.dense_stride;
+    const int bstar = __ldcg(a.bstar + bh);  // -1: every emitted pool position is selected
+    if (tid == 0) {
+      sh.slot = 0;
+      sh.ncand = 0;
+    }
     __syncthreads();
-    trace.mark(1);
-    auto val = [&](int j) -> uint64_t {
-      if (in_smem) return cache[j];
-      const uint2 p = __ldcg(row + j);
-      return rank_key(__uint_as_float(p.y), p.x);
-    };
-    auto emit = [&](uint64_t v) {
-      const int s = atomicAdd(&sh.slot, 1);
-      if (s < need) {
-        sidx[s] = (int32_t)rank_pos(v);
-        sz[s] = key2f((uint32_t)(v >> 32));
+    constexpr int kU = 8;  // pairs in flight per thread
+    for (int jb = 0; jb < n; jb += kResThreads * kU) {
+      uint2 pv[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int j = jb + u * kResThreads + tid;
+        pv[u] = j < n ? __ldcg(row + j) : make_uint2(0xffffffffu, 0u);
       }
-    };
-    cta_radix_select(n, need, 0ull, 0ull, 64, val, emit, sh.rs);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        int cls = 0;  // 1: selected, 2: threshold-bin candidate
+        uint64_t v = 0;
+        if (pv[u].x != 0xffffffffu) {
+          v = rank_key(__uint_as_float(pv[u].y), pv[u].x);
+          const int bin = (int)(v >> (64 - kHistBits));
+          cls = (bstar < 0 || bin > bstar) ? 1 : (bin == bstar ? 2 : 0);
+        }
+        const int s1 = warp_reserve(cls == 1, &sh.slot);
+        if (cls == 1 && s1 < need) {
+          sidx[s1] = (int32_t)rank_pos(v);
+          sz[s1] = key2f((uint32_t)(v >> 32));
+        }
+        const int s2 = warp_reserve(cls == 2, &sh.ncand);
+        if (cls == 2) {
+          if (s2 < kResCache) cache[s2] = v;
+          else if (s2 - kResCache < a.dense_stride) spill[s2 - kResCache] = v;
+        }
+      }
+    }
+    __syncthreads();
     trace.mark(2);
+    const int above = sh.slot < need ? sh.slot : need;
+    int nc = sh.ncand;
+    if (nc > kResCache + a.dense_stride) nc = (int)(kResCache + a.dense_stride);
+    __syncthreads();
+    if (bstar >= 0 && above < need) {
+      auto val = [&](int j) -> uint64_t {
+        return j < kResCache ? cache[j] : __ldcg(spill + (j - kResCache));
+      };
+      auto emit = [&](uint64_t v) {
+        const int s = atomicAdd(&sh.slot, 1);
+        if (s < need) {
+          sidx[s] = (int32_t)rank_pos(v);
+          sz[s] = key2f((uint32_t)(v >> 32));
+        }
+      };
+      const uint64_t prefix = (uint64_t)bstar << (64 - kHistBits);
+      const uint64_t mask = (uint64_t)(kHistBins - 1) << (64 - kHistBits);
+      cta_radix_select(nc, need - above, prefix, mask, 64 - kHistBits, val, emit, sh.rs);
+    }
   }
   for (int64_t j = (need > 0 ? need : 0) + tid; j < a.K; j += kResThreads) {
     sidx[j] = -1;

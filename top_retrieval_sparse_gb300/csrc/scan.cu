@@ -5,12 +5,14 @@
 // once per KV head and used for all query heads of its group.
 //
 // Design (sm_103a):
-//   * persistent CTAs (one per SM, 16 warps), each owning a contiguous range
-//     of 256-row tiles, balanced over the (sequence, KV head) units that have
-//     an active query head;
-//   * tiles stream global -> shared by 1-D bulk copies (cp.async.bulk with an
-//     L2 evict-first hint) into a 3-stage ring (64 KiB stages) completed on
-//     mbarriers; a paged cache issues one copy per page segment of a tile;
+//   * persistent CTAs (one per SM), each owning a contiguous range of 256-row
+//     tiles, balanced over the (sequence, KV head) units that have an active
+//     query head;
+//   * warp-specialised: one producer warp streams tiles global -> shared by
+//     1-D bulk copies (cp.async.bulk with an L2 evict-first hint) into a
+//     3-stage ring (64 KiB stages) with full/empty mbarriers; 16 consumer
+//     warps never synchronise per tile (a paged cache issues one copy per
+//     page segment of a tile);
 //   * the contraction [16 keys x 128] . [128 x 8 heads] runs on the tensor
 //     cores (mma.m16n8k16, bf16 in, fp32 accumulate): each warp owns 16 rows
 //     of a tile, keys are the M operand and the (padded) query heads of the
@@ -23,8 +25,10 @@
 //     over positions outside the static window and flushed to global memory
 //     with one atomic per non-empty bin; window logits are written out;
 //   * pool positions whose bin is >= the head's hint bin are emitted as
-//     (position, logit) pairs (warp-aggregated slot reservation) -- no
-//     logit array is written or re-read;
+//     (position, logit) pairs into the head's dense list; each warp
+//     bump-allocates runs of 8 slots (one global atomic per run) and pads the
+//     tail of its last run with sentinels -- no logit array is written or
+//     re-read;
 //   * the CTA that completes a (sequence, KV head) unit (ticket) finds the
 //     threshold bin b* of each head and checks that the emitted pairs hold
 //     every position of bins >= b*; heads that fail (hint above b*, or far
@@ -35,9 +39,10 @@
 
 namespace tsa {
 
-constexpr int kScanWarps = 16;
-constexpr int kScanThreads = 32 * kScanWarps;
-constexpr int kTileRows = 16 * kScanWarps;         // one m16 block per warp
+constexpr int kScanWarps = 16;                     // consumer warps
+constexpr int kConsumers = 32 * kScanWarps;
+constexpr int kScanThreads = kConsumers + 32;      // + one producer warp
+constexpr int kTileRows = 16 * kScanWarps;         // one m16 block per consumer warp
 constexpr int kTileBytes = kTileRows * kRowBytes;  // 64 KiB
 constexpr int kStages = 3;
 constexpr int kHistWords = kHistBins / 2;          // two 16-bit bins per word
@@ -46,7 +51,7 @@ constexpr int kFlushRows = 65535 - kTileRows;      // flush before a 16-bit bin 
 // HP: query heads per KV head rounded up to 1, 2, 4 or 8 (histogram slots).
 template <int HP>
 size_t scan_smem_bytes() {
-  return (size_t)kStages * kTileBytes + (size_t)HP * kHistWords * 4 + kStages * 8 +
+  return (size_t)kStages * kTileBytes + (size_t)HP * kHistWords * 4 + 2 * kStages * 8 +
          (kMaxUnits + 1) * 4 + 64;
 }
 
@@ -60,13 +65,15 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Block-wide: the largest histogram bin b whose suffix count reaches `need`
-// (0 < need <= total), read from global memory.  All threads call; thread 0
-// returns the bin.
-__device__ int find_threshold_bin(const uint32_t* hh, uint32_t need, uint32_t* warp_tot,
-                                  int* out) {
-  constexpr int per = kHistBins / kScanThreads;  // 4 bins per thread, from the top
+// Consumer-wide, on a head's histogram in global memory: out[0] = the
+// largest bin whose suffix count reaches `need` (the threshold bin b*, or -1),
+// out[1] = the largest bin whose suffix count reaches `budget` (or -1).  All
+// consumer threads call; every caller gets both bins.
+__device__ void find_bins(const uint32_t* hh, uint32_t need, uint32_t budget, uint32_t* warp_tot,
+                          int* out, int& bstar, int& bbud) {
+  constexpr int per = kHistBins / kConsumers;  // 4 bins per thread, from the top
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  if (tid == 0) out[0] = out[1] = -1;
   uint32_t c[per], mine = 0;
 #pragma unroll
   for (int r = 0; r < per; ++r) {
@@ -80,7 +87,7 @@ __device__ int find_threshold_bin(const uint32_t* hh, uint32_t need, uint32_t* w
     if (lane >= o) incl += y;
   }
   if (lane == 31) warp_tot[wid] = incl;
-  __syncthreads();
+  named_sync(kConsumers);
   if (wid == 0) {
     const uint32_t w = lane < kScanWarps ? warp_tot[lane] : 0u;
     uint32_t wi = w;
@@ -91,31 +98,38 @@ __device__ int find_threshold_bin(const uint32_t* hh, uint32_t need, uint32_t* w
     }
     if (lane < kScanWarps) warp_tot[lane] = wi - w;
   }
-  __syncthreads();
-  uint32_t acc = incl - mine + warp_tot[wid];
-  if (acc < need && acc + mine >= need) {
+  named_sync(kConsumers);
+  const uint32_t excl = incl - mine + warp_tot[wid];
+  const uint32_t target[2] = {need, budget};
 #pragma unroll
-    for (int r = 0; r < per; ++r) {
-      if (acc < need && acc + c[r] >= need) *out = kHistBins - 1 - (tid * per + r);
-      acc += c[r];
+  for (int k = 0; k < 2; ++k) {
+    uint32_t acc = excl;
+    if (acc < target[k] && acc + mine >= target[k]) {
+#pragma unroll
+      for (int r = 0; r < per; ++r) {
+        if (acc < target[k] && acc + c[r] >= target[k]) out[k] = kHistBins - 1 - (tid * per + r);
+        acc += c[r];
+      }
     }
   }
-  __syncthreads();
-  const int v = *out;
-  __syncthreads();
-  return v;
+  named_sync(kConsumers);
+  bstar = out[0];
+  bbud = out[1];
+  named_sync(kConsumers);
 }
 
 template <int HP>
 __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
-  TraceScope trace(a.trace, kTrScan);
+  TraceScope trace(a.trace, a.pass ? kTrScan1 : kTrScan);
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kStages * kTileBytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(hist + HP * kHistWords);
-  int* unit_tiles = reinterpret_cast<int*>(full + kStages);  // prefix over units
+  uint64_t* empty = full + kStages;
+  int* unit_tiles = reinterpret_cast<int*>(empty + kStages);  // prefix over units
   __shared__ uint32_t warp_tot[kScanWarps];
-  __shared__ int s_flag, s_bin;
+  __shared__ int s_flag, s_bins[2];
+  __shared__ volatile int s_abort;
 
   if (a.pass == 1) pdl_wait();  // rescan flags come from pass 0
   pdl_trigger();
@@ -155,8 +169,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
   if (p0)
     for (int i = tid; i < HP * kHistWords; i += kScanThreads) hist[i] = 0;
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kScanWarps);
+    }
     fence_mbar_init();
+    s_abort = 0;
   }
   __syncthreads();
 
@@ -178,54 +196,73 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
     return lo;
   };
 
-  const uint64_t pol = policy_evict_first();
-  // producer (thread 0): stream tile t into stage s
-  auto issue = [&](int t, int s) {
-    const int unit = locate(t);
-    const int tile = t - unit_tiles[unit];
-    const int b = unit / a.kv.Hkv, g = unit % a.kv.Hkv;
-    const int64_t L = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
-    const int64_t r0 = (int64_t)tile * kTileRows;
-    const int64_t r1 = r0 + kTileRows < L ? r0 + kTileRows : L;
-    const uint32_t bytes = (uint32_t)(r1 - r0) * kRowBytes;
-    mbar_expect_tx(&full[s], bytes);
-    uint8_t* dst = ring + s * kTileBytes;
-    if (!a.kv.page_table) {
-      bulk_g2s(dst, a.kv.k + kv_row(a.kv, b, g, r0), bytes, &full[s], pol);
-    } else {
-      const int64_t ps = (int64_t)1 << a.kv.page_shift;
-      for (int64_t r = r0; r < r1;) {
-        const int64_t pe = ((r >> a.kv.page_shift) + 1) * ps;
-        const int64_t e = pe < r1 ? pe : r1;
-        bulk_g2s(dst + (r - r0) * kRowBytes, a.kv.k + kv_row(a.kv, b, g, r),
-                 (uint32_t)(e - r) * kRowBytes, &full[s], pol);
-        r = e;
-      }
-    }
-  };
+  const int warp = tid >> 5, lane = tid & 31;
 
-  if (tid == 0) {
-    const int pre = ntile < kStages ? ntile : kStages;
-    for (int j = 0; j < pre; ++j) issue(t_begin + j, j);
+  // ======================= producer warp: the bulk-copy ring ==================
+  if (warp == kScanWarps) {
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int j = 0;
+      for (; j < ntile; ++j) {
+        const int s = j % kStages;
+        if (j >= kStages &&
+            !mbar_wait_or_abort(&empty[s], (uint32_t)((j / kStages - 1) & 1), &s_abort)) {
+          s_abort = 1;
+          break;
+        }
+        if (s_abort) break;
+        const int t = t_begin + j;
+        const int unit = locate(t);
+        const int tile = t - unit_tiles[unit];
+        const int b = unit / a.kv.Hkv, g = unit % a.kv.Hkv;
+        const int64_t L = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
+        const int64_t r0 = (int64_t)tile * kTileRows;
+        const int64_t r1 = r0 + kTileRows < L ? r0 + kTileRows : L;
+        const uint32_t bytes = (uint32_t)(r1 - r0) * kRowBytes;
+        fence_proxy_async();
+        mbar_expect_tx(&full[s], bytes);
+        uint8_t* dst = ring + s * kTileBytes;
+        if (!a.kv.page_table) {
+          bulk_g2s(dst, a.kv.k + kv_row(a.kv, b, g, r0), bytes, &full[s], pol);
+        } else {
+          const int64_t ps = (int64_t)1 << a.kv.page_shift;
+          for (int64_t r = r0; r < r1;) {
+            const int64_t pe = ((r >> a.kv.page_shift) + 1) * ps;
+            const int64_t e = pe < r1 ? pe : r1;
+            bulk_g2s(dst + (r - r0) * kRowBytes, a.kv.k + kv_row(a.kv, b, g, r),
+                     (uint32_t)(e - r) * kRowBytes, &full[s], pol);
+            r = e;
+          }
+        }
+      }
+      // copies of the last (up to kStages) issued tiles may still be landing
+      for (int jj = j - kStages > 0 ? j - kStages : 0; jj < j; ++jj)
+        (void)mbar_wait(&full[jj % kStages], (uint32_t)((jj / kStages) & 1));
+    }
+    return;
   }
 
-  // mma fragment roles: lane = 4*gr + tq
-  const int warp = tid >> 5, lane = tid & 31;
+  // ============================ consumer warps ================================
   const int gr = lane >> 2;  // A rows gr, gr+8 / B column (query head) gr
   const int tq = lane & 3;   // k-slot group / C columns 2tq, 2tq+1
 
   uint32_t qb[4][4];         // B fragments: head gr, d in [8(4p+tq), +8) for p < 4
   bool on[2] = {false, false};  // heads 2tq, 2tq+1 take part in this pass
   int hint[2] = {0, 0};         // emission bins of heads 2tq, 2tq+1
+  bool lane_on = false;         // lane h < G: head h takes part (run owner)
+  int wsum = 0;                 // lane h < G: pairs this warp emitted for head h, this unit
+  int64_t run_ptr = 0;          // lane h < G: next free slot of this warp's run for head h
+  int run_left = 0;             //            slots left in that run
   int cur_unit = -1, unit_end = 0, cur_b = 0, cur_g = 0, head0 = 0;
   int64_t cur_L = 0;
   int rows_since_flush = 0;
+  bool dead = false;
 
-  // flush the shared histogram of `unit` into global memory (all threads)
+  // flush the shared histogram of `unit` into global memory (consumers)
   auto flush_hist = [&](int unit) {
     const int b = unit / a.kv.Hkv, g = unit % a.kv.Hkv;
-    __syncthreads();
-    for (int w = tid; w < HP * kHistWords; w += kScanThreads) {
+    named_sync(kConsumers);
+    for (int w = tid; w < HP * kHistWords; w += kConsumers) {
       const uint32_t v = hist[w];
       if (v) {
         const int hl = w / kHistWords;
@@ -236,14 +273,32 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
         hist[w] = 0;
       }
     }
+    __threadfence();
     rows_since_flush = 0;
   };
   // pass 0: unit finished by this CTA -- flush, add its tiles to the unit
   // ticket; the CTA that completes the unit decides, per head, the threshold
   // bin, whether pass 1 must re-emit, and the next call's hint
+  // this warp leaves the current unit: pad the unused tail of its runs with
+  // sentinels (both passes)
+  auto close_runs = [&]() {
+    if (lane < G && run_left > 0) {
+      uint2* drow = a.dense + (int64_t)(head0 + lane) * a.dense_stride;
+      for (int k = 0; k < run_left; ++k)
+        if (run_ptr + k < a.dense_stride) drow[run_ptr + k] = make_uint2(0xffffffffu, 0u);
+    }
+    run_ptr = 0;
+    run_left = 0;
+  };
   auto finish_unit = [&](int unit) {
     flush_hist(unit);
-    __syncthreads();
+    close_runs();
+    if (lane < G) {  // publish this warp's emission count
+      if (wsum) atomicAdd(&a.emit_n[head0 + lane], wsum);
+      __threadfence();
+    }
+    wsum = 0;
+    named_sync(kConsumers);
     if (tid == 0) {  // the ticket counts tiles: the CTA completing the count is last
       const int u0 = unit_tiles[unit], u1 = unit_tiles[unit + 1];
       const uint32_t mine = (uint32_t)((t_end < u1 ? t_end : u1) - (t_begin > u0 ? t_begin : u0));
@@ -251,7 +306,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
       const uint32_t n = atomicAdd(&a.unit_ticket[unit], mine);
       s_flag = (n + mine == (uint32_t)(u1 - u0));
     }
-    __syncthreads();
+    named_sync(kConsumers);
     if (!s_flag) return;
     __threadfence();
     const int b = unit / a.kv.Hkv, g = unit % a.kv.Hkv;
@@ -262,14 +317,18 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
       const int bh = b * a.Hq + g * G + hl;
       if (a.head_active && a.head_active[bh] != a.active_value) continue;
       const int used = min(max(__ldcg(a.hint_bin + bh), 0), kHistBins - 1);
-      int bin = -1, exact_bin = 0, redo = 0;
+      int bin = -1, exact_bin = 0, redo = 0, next_hint = 0;
       if (need > 0 && need < P) {
-        if (tid == 0) s_bin = -1;
-        bin = find_threshold_bin(a.hist + (int64_t)bh * kHistBins, (uint32_t)need, warp_tot,
-                                 &s_bin);
+        // next call's hint: the lowest bin whose suffix stays within the
+        // emission budget, never above b*
+        const int64_t budget = 3 * need + 4096;
+        int bbud;
+        find_bins(a.hist + (int64_t)bh * kHistBins, (uint32_t)need,
+                  (uint32_t)(budget + 1 < P ? budget + 1 : P + 1), warp_tot, s_bins, bin, bbud);
         exact_bin = bin;
+        next_hint = bbud < 0 ? 0 : (bbud + 1 < bin ? bbud + 1 : bin);
         const int64_t emitted = __ldcg(a.emit_n + bh);
-        redo = used > bin || emitted > 4 * need + 4096;
+        redo = used > bin || emitted > 4 * need + 8192;
       } else if (need > 0) {  // every pool position is selected
         exact_bin = 0;
         redo = used > 0;
@@ -278,19 +337,24 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
         a.bstar[bh] = bin;
         a.rescan[bh] = redo;
         a.rescan_bin[bh] = exact_bin;
-        if (redo) a.emit_n[bh] = 0;
-        if (need > 0) a.hint_bin[bh] = bin > 0 ? bin - 1 : 0;
+        if (redo) {
+          a.emit_n[bh] = 0;
+          a.dense_n[bh] = 0;
+        }
+        if (need > 0) a.hint_bin[bh] = next_hint;
       }
     }
   };
 
-  int j = 0;
-  for (; j < ntile; ++j) {
+  for (int j = 0; j < ntile; ++j) {
     const int s = j % kStages;
     const int t = t_begin + j;
-    if (t >= unit_end) {  // entering a new unit
+    if (t >= unit_end) {  // entering a new unit (all consumers at the same tile)
       const int unit = locate(t);
-      if (cur_unit >= 0 && p0) finish_unit(cur_unit);
+      if (cur_unit >= 0) {
+        if (p0) finish_unit(cur_unit);
+        else close_runs();
+      }
       cur_unit = unit;
       unit_end = unit_tiles[unit + 1];
       cur_b = unit / a.kv.Hkv;
@@ -303,8 +367,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
         const int bh = head0 + hl;
         on[e] = hl < G && (!a.head_active || a.head_active[bh] == a.active_value);
         hint[e] = 0;
-        if (on[e]) hint[e] = p0 ? min(max(a.hint_bin[bh], 0), kHistBins - 1) : a.rescan_bin[bh];
+        if (on[e])
+          hint[e] = p0 ? min(max(__ldcg(a.hint_bin + bh), 0), kHistBins - 1)
+                       : __ldcg(a.rescan_bin + bh);
       }
+      lane_on = lane < G && (!a.head_active || a.head_active[head0 + lane] == a.active_value);
       const uint16_t* qp = a.q + ((int64_t)head0 + (gr < G ? gr : 0)) * kD;
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
@@ -315,90 +382,123 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
     } else if (p0 && rows_since_flush > kFlushRows) {
       flush_hist(cur_unit);
     }
-    const int tile = t - unit_tiles[cur_unit];
-    const bool ok = mbar_wait(&full[s], (uint32_t)((j / kStages) & 1));
-    if (__syncthreads_or(!ok)) break;  // uniform decision: leave on timeout
-    if (j == 0) trace.mark(1);
-
-    // ---- 16 keys x 8 heads on the tensor cores ----
-    const uint8_t* wb = ring + s * kTileBytes + warp * 16 * kRowBytes;
-    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      const uint4 W = *reinterpret_cast<const uint4*>(wb + gr * kRowBytes + 16 * (4 * p + tq));
-      const uint4 X = *reinterpret_cast<const uint4*>(wb + (gr + 8) * kRowBytes + 16 * (4 * p + tq));
-      mma_bf16(c0, W.x, X.x, W.y, X.y, qb[p][0], qb[p][1]);
-      mma_bf16(c1, W.z, X.z, W.w, X.w, qb[p][2], qb[p][3]);
-    }
-    // C: (row gr, head 2tq), (row gr, head 2tq+1), (row gr+8, 2tq), (row gr+8, 2tq+1)
-    const int64_t r0 = (int64_t)tile * kTileRows;
-    const int64_t rowA = r0 + warp * 16 + gr;
-    const bool pool_tile = r0 >= a.n_init && r0 + kTileRows <= cur_L - a.n_recent;
-    float zv[4];
-    unsigned emit = 0u;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int64_t i = rowA + ((e >> 1) << 3);
-      zv[e] = (c0[e] + c1[e]) * a.scale;
-      if (on[e & 1] && i < cur_L) {
-        const uint32_t bin = f2key(zv[e]) >> kHistShift;
-        if (!pool_tile && in_window(i, cur_L, a.n_init, a.n_recent)) {
-          if (p0) {
-            const int64_t wa = a.n_init < cur_L ? a.n_init : cur_L;
-            const int64_t lo = cur_L - a.n_recent > wa ? cur_L - a.n_recent : wa;
-            const int64_t wj = i < wa ? i : wa + (i - lo);
-            a.wz[(int64_t)(head0 + 2 * tq + (e & 1)) * a.wz_stride + wj] = zv[e];
-          }
-        } else {
-          if (p0)
-            atomicAdd(&hist[(2 * tq + (e & 1)) * kHistWords + (bin >> 1)], 1u << ((bin & 1) << 4));
-          if ((int)bin >= hint[e & 1]) emit |= 1u << e;
-        }
-      }
-    }
-    // emission: one slot reservation per (warp, head) with emitting lanes
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const unsigned m = __ballot_sync(0xffffffffu, (emit >> e) & 1u);
-      if (!m) continue;
-      const int64_t i = rowA + ((e >> 1) << 3);
-#pragma unroll
-      for (int g4 = 0; g4 < 4; ++g4) {
-        const unsigned grp = m & (0x11111111u << g4);
-        if (!grp) continue;
-        const int leader = __ffs(grp) - 1;
-        const int bh = head0 + 2 * g4 + (e & 1);
-        int base = 0;
-        if (lane == leader) base = atomicAdd(&a.emit_n[bh], __popc(grp));
-        base = __shfl_sync(0xffffffffu, base, leader);
-        if ((grp >> lane) & 1u) {
-          const int64_t slot = base + __popc(grp & ((1u << lane) - 1u));
-          if (slot < a.cand_stride)
-            a.cand[(int64_t)bh * a.cand_stride + slot] =
-                make_uint2((uint32_t)i, __float_as_uint(zv[e]));
-        }
-      }
-    }
     rows_since_flush += kTileRows;
-    __syncthreads();  // stage s fully consumed
-    if (tid == 0 && j + kStages < ntile) {
-      fence_proxy_async();
-      issue(t + kStages, s);
+    const int tile = t - unit_tiles[cur_unit];
+    if (!dead && !mbar_wait_or_abort(&full[s], (uint32_t)((j / kStages) & 1), &s_abort)) {
+      dead = true;
+      s_abort = 1;
+    }
+    if (j == 0) trace.mark(1);
+    if (!dead) {
+      // ---- 16 keys x 8 heads on the tensor cores ----
+      const uint8_t* wb = ring + s * kTileBytes + warp * 16 * kRowBytes;
+      float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const uint4 W = *reinterpret_cast<const uint4*>(wb + gr * kRowBytes + 16 * (4 * p + tq));
+        const uint4 X =
+            *reinterpret_cast<const uint4*>(wb + (gr + 8) * kRowBytes + 16 * (4 * p + tq));
+        mma_bf16(c0, W.x, X.x, W.y, X.y, qb[p][0], qb[p][1]);
+        mma_bf16(c1, W.z, X.z, W.w, X.w, qb[p][2], qb[p][3]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with stage s
+      // C: (row gr, head 2tq), (row gr, head 2tq+1), (row gr+8, 2tq), (row gr+8, 2tq+1)
+      const int64_t r0 = (int64_t)tile * kTileRows;
+      const int64_t rowA = r0 + warp * 16 + gr;
+      const bool pool_tile = r0 >= a.n_init && r0 + kTileRows <= cur_L - a.n_recent;
+      float zv[4];
+      unsigned emit = 0u;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int64_t i = rowA + ((e >> 1) << 3);
+        zv[e] = (c0[e] + c1[e]) * a.scale;
+        if (on[e & 1] && i < cur_L) {
+          const uint32_t bin = f2key(zv[e]) >> kHistShift;
+          if (!pool_tile && in_window(i, cur_L, a.n_init, a.n_recent)) {
+            if (p0) {
+              const int64_t wa = a.n_init < cur_L ? a.n_init : cur_L;
+              const int64_t lo = cur_L - a.n_recent > wa ? cur_L - a.n_recent : wa;
+              const int64_t wj = i < wa ? i : wa + (i - lo);
+              a.wz[(int64_t)(head0 + 2 * tq + (e & 1)) * a.wz_stride + wj] = zv[e];
+            }
+          } else {
+            if (p0)
+              atomicAdd(&hist[(2 * tq + (e & 1)) * kHistWords + (bin >> 1)],
+                        1u << ((bin & 1) << 4));
+            if ((int)bin >= hint[e & 1]) emit |= 1u << e;
+          }
+        }
+      }
+      // emission: per head, this warp's pairs of the tile (rows gr, then
+      // gr+8, by lane) continue its current run; lane h extends the run by
+      // bump allocation (one atomic per 8 slots) and broadcasts where they go
+      unsigned m[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) m[e] = __ballot_sync(0xffffffffu, (emit >> e) & 1u);
+      int64_t p1 = 0, p2 = 0;
+      int take = 0;
+      if (lane_on) {  // lane = head in group
+        const unsigned M = 0x11111111u << (lane >> 1);
+        const unsigned ma = (lane & 1) ? m[1] : m[0], mb = (lane & 1) ? m[3] : m[2];
+        const int cnt = __popc(ma & M) + __popc(mb & M);
+        if (cnt) {
+          take = cnt < run_left ? cnt : run_left;
+          p1 = run_ptr;
+          const int over = cnt - take;
+          if (over > 0) {
+            const int size = (over + 7) & ~7;
+            p2 = atomicAdd(&a.dense_n[head0 + lane], size);
+            run_ptr = p2 + over;
+            run_left = size - over;
+          } else {
+            run_ptr += cnt;
+            run_left -= cnt;
+          }
+          wsum += cnt;
+        }
+      }
+      if (m[0] | m[1] | m[2] | m[3]) {
+        const unsigned M = 0x11111111u << tq;
+        const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+        for (int par = 0; par < 2; ++par) {
+          const int src = 2 * tq + par;  // lane owning head 2tq+par's run
+          const int64_t q1 = __shfl_sync(0xffffffffu, p1, src);
+          const int64_t q2 = __shfl_sync(0xffffffffu, p2, src);
+          const int qt = __shfl_sync(0xffffffffu, take, src);
+#pragma unroll
+          for (int hi = 0; hi < 2; ++hi) {
+            const int e = par + 2 * hi;
+            if (!((emit >> e) & 1u)) continue;
+            const int r = hi == 0 ? __popc(m[par] & M & lt)
+                                  : __popc(m[par] & M) + __popc(m[par + 2] & M & lt);
+            const int64_t slot = r < qt ? q1 + r : q2 + (r - qt);
+            if (slot < a.dense_stride)
+              a.dense[(int64_t)(head0 + src) * a.dense_stride + slot] =
+                  make_uint2((uint32_t)(rowA + 8 * hi), __float_as_uint(zv[e]));
+          }
+        }
+      }
+    } else {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // keep the producer moving
     }
   }
 
-  if (j < ntile) {  // a bounded wait expired: report, drain in-flight copies, leave
-    if (tid == 0) {
-      atomicOr(a.status, kStatusTimeout);
-      const int last = ntile < j + kStages ? ntile : j + kStages;
-      for (int jj = j; jj < last; ++jj)
-        (void)mbar_wait(&full[jj % kStages], (uint32_t)((jj / kStages) & 1));
-    }
-    __syncthreads();
+  // one decision for all consumer warps (a named barrier needs all of them)
+  named_sync(kConsumers);
+  if (tid == 0) s_flag = s_abort;
+  named_sync(kConsumers);
+  if (s_flag) {
+    if (tid == 0) atomicOr(a.status, kStatusTimeout);
     return;
   }
   trace.mark(2);
-  if (cur_unit >= 0 && p0) finish_unit(cur_unit);
+  if (cur_unit >= 0) {
+    if (p0) finish_unit(cur_unit);
+    else close_runs();
+  }
 }
 
 template <int HP>
@@ -429,6 +529,7 @@ static cudaError_t launch_scan_t(const ScanArgs& a, int grid, cudaStream_t st, b
 static int hist_heads(int G) { return G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8; }
 
 int scan_tile_rows() { return kTileRows; }
+int scan_tile_warps() { return kScanWarps; }
 
 cudaError_t launch_scan(const ScanArgs& a, int grid, cudaStream_t st, bool pdl) {
   const int G = a.Hq / a.kv.Hkv;

@@ -156,6 +156,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     if ((long long)(globaltimer_ns() - t0) > kWaitLimitNs) return false;
   }
 }
+// Bounded wait that also gives up as soon as *abort is set (CTA-wide stop).
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity,
+                                                   volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if ((long long)(globaltimer_ns() - t0) > kWaitLimitNs) return false;
+  }
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// Named barrier over the first `nthreads` threads of the CTA (id 1).
+__device__ __forceinline__ void named_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -223,7 +243,7 @@ struct TraceScope {
   }
 };
 enum TraceKernel : uint32_t {
-  kTrScan = 1, kTrSelect = 2, kTrAttend = 3, kTrSelector = 4, kTrRescore = 5
+  kTrScan = 1, kTrSelect = 2, kTrAttend = 3, kTrSelector = 4, kTrRescore = 5, kTrScan1 = 6
 };
 
 // ------------------------------------------------------ warp/block utils

@@ -14,9 +14,11 @@ namespace tsa {
 //
 // Key scan, pass 0: logits of every active head; window logits go to wz, pool
 // positions feed the 11-bit histogram and are emitted as (position, logit)
-// pairs when their bin is >= the head's hint bin.  The CTA that completes a
-// (sequence, KV head) unit turns the histograms into the threshold bin b*
-// and decides per head whether the emitted pairs provably contain the top-K
+// pairs when their bin is >= the head's hint bin.  Pairs go to the head's
+// dense list: every warp bump-allocates runs of 8 slots from dense_n and pads
+// the unused tail of its last run with sentinel pairs (position 0xffffffff).  The CTA that completes a
+// (sequence, KV head) unit turns the histograms into the threshold bin b* and
+// decides per head whether the emitted pairs provably contain the top-K
 // (hint <= b* and not too many emitted); if not, the head is flagged for
 // pass 1, which re-emits with the exact bin (b*, or 0 when every pool
 // position is selected).  The hint for the next call is b* - 1.
@@ -38,9 +40,10 @@ struct ScanArgs {
   int32_t* rescan;           // [B][Hq] (zeroed) 1: pass 1 needed; pass 1 reads it
   int32_t* rescan_bin;       // [B][Hq] exact emission bin for pass 1
   int32_t* bstar;            // [B][Hq] threshold bin (-1: all pool / none)
-  int32_t* emit_n;           // [B][Hq] (zeroed) emitted pairs
-  uint2* cand;               // [B][Hq][cand_stride] (position, logit bits)
-  int64_t cand_stride;       // >= l_cap
+  int32_t* emit_n;           // [B][Hq] (zeroed) emitted pairs, pass 0 totals
+  uint2* dense;              // [B][Hq][dense_stride] (position, logit bits)
+  int32_t* dense_n;          // [B][Hq] (zeroed) slots allocated (pairs + sentinels)
+  int64_t dense_stride;      // >= l_cap + slack for the padding
   float* wz;                 // [B][Hq][wz_stride] window logits, pass 0
   int wz_stride;
   int* status;
@@ -48,8 +51,8 @@ struct ScanArgs {
 };
 cudaError_t launch_scan(const ScanArgs& a, int grid, cudaStream_t st, bool pdl);
 
-// Resolve: one CTA per head keeps the top min(K, |pool|) of the emitted
-// pairs (ties to the smaller position) and writes the selected set.
+// Resolve: one CTA per head reads the head's dense pair list, keeps the top
+// min(K, |pool|) (ties to the smaller position) and writes the selected set.
 struct ResolveArgs {
   const int32_t* lens;
   int64_t len_host;
@@ -58,9 +61,11 @@ struct ResolveArgs {
   int n_init, n_recent;
   const int32_t* head_active;
   int active_value;
-  const int32_t* emit_n;
-  const uint2* cand;
-  int64_t cand_stride;
+  const int32_t* bstar;      // threshold bins (-1: every pool position)
+  const uint2* dense;
+  const int32_t* dense_n;
+  int64_t dense_stride;
+  uint64_t* spill;           // [B][Hq][dense_stride] radix scratch (large candidate sets)
   int32_t* sel_idx;          // [B][Hq][K]
   float* sel_z;              // [B][Hq][K]
   int32_t* sel_n;            // [B][Hq]
@@ -76,13 +81,11 @@ struct AttendArgs {
   const float* wz;           // window logits, [B][Hq][wz_stride]
   int wz_stride;
   int n_init, n_recent;
-  int n_wsplit, n_ssplit;    // splits per head (window, selected)
+  int window;                // 0: no static window on this path
   const int32_t* sel_idx;    // [B][Hq][K]
   const float* sel_z;
   const int32_t* sel_n;      // [B][Hq]
   int K;
-  float* part;               // [B][Hq][n_wsplit+n_ssplit][kD + 2]
-  uint32_t* ticket;          // [B][Hq] (zeroed)
   float* out;                // [B][Hq][128]
   float* lse_out;            // [B][Hq] or nullptr
   // ReTopK cache push (push_qbar == nullptr: none)
@@ -91,10 +94,6 @@ struct AttendArgs {
   int32_t* cache_sup;        // [Hq][C][K]
   int32_t* cache_sup_n;      // [Hq][C]
   int C, slot;
-  // window splits may start before the predecessor kernel finishes (set only
-  // when that predecessor is the selection kernel, which itself waited for
-  // the key scan)
-  int early_window;
   TraceBuf trace;
 };
 cudaError_t launch_attend(const AttendArgs& a, cudaStream_t st);
