@@ -25,7 +25,38 @@ struct ResShared {
   RadixScratch rs;
   int slot;   // selected so far
   int ncand;  // threshold-bin candidates
+  int total;
 };
+
+// Block-wide exclusive scan of one value per thread; returns the thread's
+// offset and writes the block total to *total.  All threads call.
+__device__ int block_excl_scan(int v, uint32_t* warp_tot, int* total) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[wid] = (uint32_t)incl;
+  __syncthreads();
+  if (wid == 0) {
+    constexpr int nw = kResThreads / 32;
+    const int w = lane < nw ? (int)warp_tot[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    if (lane < nw) warp_tot[lane] = (uint32_t)(wi - w);
+    if (lane == nw - 1) *total = wi;
+  }
+  __syncthreads();
+  const int off = incl - v + (int)warp_tot[wid];
+  __syncthreads();
+  return off;
+}
 
 __global__ void __launch_bounds__(kResThreads) resolve_kernel(ResolveArgs a) {
   TraceScope trace(a.trace, kTrSelect);
@@ -57,6 +88,7 @@ __global__ void __launch_bounds__(kResThreads) resolve_kernel(ResolveArgs a) {
     }
     __syncthreads();
     constexpr int kU = 8;  // pairs in flight per thread
+    int base_sel = 0, base_cand = 0;  // running totals (block-uniform)
     for (int jb = 0; jb < n; jb += kResThreads * kU) {
       uint2 pv[kU];
 #pragma unroll
@@ -64,26 +96,43 @@ __global__ void __launch_bounds__(kResThreads) resolve_kernel(ResolveArgs a) {
         const int j = jb + u * kResThreads + tid;
         pv[u] = j < n ? __ldcg(row + j) : make_uint2(0xffffffffu, 0u);
       }
+      uint64_t v[kU];
+      uint32_t sel = 0u, cnd = 0u;  // bit masks over the kU pairs
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
-        int cls = 0;  // 1: selected, 2: threshold-bin candidate
-        uint64_t v = 0;
+        v[u] = 0;
         if (pv[u].x != 0xffffffffu) {
-          v = rank_key(__uint_as_float(pv[u].y), pv[u].x);
-          const int bin = (int)(v >> (64 - kHistBits));
-          cls = (bstar < 0 || bin > bstar) ? 1 : (bin == bstar ? 2 : 0);
-        }
-        const int s1 = warp_reserve(cls == 1, &sh.slot);
-        if (cls == 1 && s1 < need) {
-          sidx[s1] = (int32_t)rank_pos(v);
-          sz[s1] = key2f((uint32_t)(v >> 32));
-        }
-        const int s2 = warp_reserve(cls == 2, &sh.ncand);
-        if (cls == 2) {
-          if (s2 < kResCache) cache[s2] = v;
-          else if (s2 - kResCache < a.dense_stride) spill[s2 - kResCache] = v;
+          v[u] = rank_key(__uint_as_float(pv[u].y), pv[u].x);
+          const int bin = (int)(v[u] >> (64 - kHistBits));
+          if (bstar < 0 || bin > bstar) sel |= 1u << u;
+          else if (bin == bstar) cnd |= 1u << u;
         }
       }
+      // one block scan of (selected << 16 | candidates) per batch
+      const int packed = (__popc(sel) << 16) | __popc(cnd);
+      const int off = block_excl_scan(packed, sh.rs.warp_tot, &sh.total);
+      const int tot = sh.total;
+      int s1 = base_sel + (off >> 16), s2 = base_cand + (off & 0xffff);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        if ((sel >> u) & 1u) {
+          if (s1 < need) {
+            sidx[s1] = (int32_t)rank_pos(v[u]);
+            sz[s1] = key2f((uint32_t)(v[u] >> 32));
+          }
+          ++s1;
+        } else if ((cnd >> u) & 1u) {
+          if (s2 < kResCache) cache[s2] = v[u];
+          else if (s2 - kResCache < a.dense_stride) spill[s2 - kResCache] = v[u];
+          ++s2;
+        }
+      }
+      base_sel += tot >> 16;
+      base_cand += tot & 0xffff;
+    }
+    if (tid == 0) {
+      sh.slot = base_sel;
+      sh.ncand = base_cand;
     }
     __syncthreads();
     trace.mark(2);
