@@ -191,12 +191,14 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    n_launch0 = tsa.kernel_launches()
     t0.record(stream)
     for i in range(args.steps):
         tsa.set_stage_events(ev[i])
         step(args.warmup + i)
     tsa.set_stage_events(None)
     t1.record(stream)
+    n_launches = tsa.kernel_launches() - n_launch0
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
@@ -232,7 +234,7 @@ def run_ours(args, ws, rank, local):
         "metric": METRIC, "value": round(us_per_layer_step, 3), "unit": UNIT,
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 5), "higher_is_better": False, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16 in, fp32 accumulate/out", "data": "synthetic",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {
             "workload": name, "B": B, "Hq": Hq, "Hkv": wl.Hkv, "d": d,
             "context": wl.L0 if B > 1 else wl.L0[0], "K": K,
@@ -250,7 +252,7 @@ def run_ours(args, ws, rank, local):
                      "frac_of_8tbs": round(achieved / 8000.0, 4),
                      "traffic": None, "algorithmic_bytes_per_launch": ab["scan"]},
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": n_launches,
         "clocks": clk,
     }
     if args.cpu_baseline and rank == 0:
@@ -304,57 +306,63 @@ def run_trace(args, step, tsa, torch, dev, nsteps=3):
 
 
 def run_e2e(args, wl, kv, work, tsa, torch, dev):
-    """Per step: pinned host -> device copy of the step's query, its appended
-    K/V token rows and the lengths; the decode call; device -> host read of the
-    output and lse.  Wall-clock per step, synchronised."""
-    B, Hq, d, G = wl.B, wl.Hq, wl.d, wl.Hq // wl.Hkv
-    q_host = wl.q_all.cpu().pin_memory()
-    lens_host = torch.tensor([wl.lens(t) for t in range(wl.steps)], dtype=torch.int32).pin_memory()
+    """End to end through the public API with host buffers.  Per step: one
+    pinned host -> device copy of the step's packed inputs (query, appended K
+    and V token rows, lengths), the append of the token rows into the cache,
+    the decode call, and one device -> host copy of the packed result (output
+    and lse), then a stream synchronisation.  Wall-clock per step."""
+    import numpy as np
+    B, Hq, d, Hkv = wl.B, wl.Hq, wl.d, wl.Hkv
     paged = wl.page_table is not None
-    # the token appended at step t sits at row L0+t; keep host copies of those rows
-    if paged:
-        tok_k = torch.zeros((wl.steps, B, wl.Hkv, d), dtype=torch.bfloat16)
-        tok_v = torch.zeros_like(tok_k)
-        pt = wl.page_table.cpu()
-        for t in range(wl.steps):
-            for b in range(B):
-                pos = wl.L0[b] + t
+    qb, tb, lb = B * Hq * d * 2, B * Hkv * d * 2, B * 4
+    nbytes = qb + 2 * tb + lb
+    host = torch.empty((wl.steps, nbytes), dtype=torch.uint8).pin_memory()
+    pt = wl.page_table.cpu() if paged else None
+    page_idx = torch.empty((wl.steps, B), dtype=torch.int64)
+    row_idx = torch.empty((wl.steps, B), dtype=torch.int64)
+    for t in range(wl.steps):
+        lens_t = np.asarray(wl.lens(t), dtype=np.int32)
+        tok_k = torch.empty((B, Hkv, d), dtype=torch.bfloat16)
+        tok_v = torch.empty_like(tok_k)
+        for b in range(B):  # the token appended at step t sits at row L0 + t
+            pos = wl.L0[b] + t
+            if paged:
                 page = int(pt[b, pos // wl.page_size])
-                tok_k[t, b] = wl.k_pages[page, :, pos % wl.page_size].cpu()
-                tok_v[t, b] = wl.v_pages[page, :, pos % wl.page_size].cpu()
-    else:
-        idx = torch.tensor([[l0 + t for l0 in wl.L0] for t in range(wl.steps)])
-        tok_k = torch.stack([torch.stack([wl.k[b, :, int(idx[t, b])].cpu() for b in range(B)])
-                             for t in range(wl.steps)])
-        tok_v = torch.stack([torch.stack([wl.v[b, :, int(idx[t, b])].cpu() for b in range(B)])
-                             for t in range(wl.steps)])
-    tok_k, tok_v = tok_k.pin_memory(), tok_v.pin_memory()
-    q_dev = torch.empty((B, Hq, d), dtype=torch.bfloat16, device=dev)
-    lens_dev = torch.empty((B,), dtype=torch.int32, device=dev)
-    out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
-    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
-    out_host = torch.empty((B, Hq, d), dtype=torch.float32).pin_memory()
-    lse_host = torch.empty((B, Hq), dtype=torch.float32).pin_memory()
-    pt_host = wl.page_table.cpu() if paged else None
+                page_idx[t, b], row_idx[t, b] = page, pos % wl.page_size
+                tok_k[b] = wl.k_pages[page, :, pos % wl.page_size].cpu()
+                tok_v[b] = wl.v_pages[page, :, pos % wl.page_size].cpu()
+            else:
+                page_idx[t, b], row_idx[t, b] = b, pos
+                tok_k[b] = wl.k[b, :, pos].cpu()
+                tok_v[b] = wl.v[b, :, pos].cpu()
+        row = host[t]
+        row[:qb] = wl.q_all[t].cpu().contiguous().view(torch.uint8).reshape(-1)
+        row[qb:qb + tb] = tok_k.view(torch.uint8).reshape(-1)
+        row[qb + tb:qb + 2 * tb] = tok_v.view(torch.uint8).reshape(-1)
+        row[qb + 2 * tb:] = torch.from_numpy(lens_t.view(np.uint8))
+    page_idx, row_idx = page_idx.to(dev), row_idx.to(dev)  # bookkeeping, resident
+    stage = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    q_dev = stage[:qb].view(torch.bfloat16).view(B, Hq, d)
+    tok_k_dev = stage[qb:qb + tb].view(torch.bfloat16).view(B, Hkv, d)
+    tok_v_dev = stage[qb + tb:qb + 2 * tb].view(torch.bfloat16).view(B, Hkv, d)
+    lens_dev = stage[qb + 2 * tb:].view(torch.int32)
+    res = torch.empty(B * Hq * (d + 1), dtype=torch.float32, device=dev)
+    out = res[:B * Hq * d].view(B, Hq, d)
+    lse = res[B * Hq * d:].view(B, Hq)
+    res_host = torch.empty_like(res, device="cpu").pin_memory()
+    kc, vc = (wl.k_pages, wl.v_pages) if paged else (wl.k, wl.v)
+    stream = torch.cuda.current_stream()
 
     def one(i):
         t = i % wl.steps
-        q_dev.copy_(q_host[t], non_blocking=True)
-        lens_dev.copy_(lens_host[t], non_blocking=True)
-        for b in range(B):  # append this step's token rows
-            pos = wl.L0[b] + t
-            if paged:
-                page = int(pt_host[b, pos // wl.page_size])
-                wl.k_pages[page, :, pos % wl.page_size].copy_(tok_k[t, b], non_blocking=True)
-                wl.v_pages[page, :, pos % wl.page_size].copy_(tok_v[t, b], non_blocking=True)
-            else:
-                wl.k[b, :, pos].copy_(tok_k[t, b], non_blocking=True)
-                wl.v[b, :, pos].copy_(tok_v[t, b], non_blocking=True)
+        stage.copy_(host[t], non_blocking=True)
+        # append the step's token rows: cache[page, :, row] = token (one scatter each)
+        kc[page_idx[t], :, row_idx[t]] = tok_k_dev
+        vc[page_idx[t], :, row_idx[t]] = tok_v_dev
         tsa.sparse_attn_decode(q_dev, kv, lens_dev, wl.K, wl.n_init, wl.n_recent, wl.scale,
-                               out=out, lse_out=lse, workspace=work)
-        out_host.copy_(out, non_blocking=True)
-        lse_host.copy_(lse, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+                               out=out, lse_out=lse, workspace=work, stream=stream)
+        res_host.copy_(res, non_blocking=True)
+        stream.synchronize()
 
     for i in range(args.warmup):
         one(i)
@@ -363,10 +371,8 @@ def run_e2e(args, wl, kv, work, tsa, torch, dev):
     for i in range(n):
         one(args.warmup + i)
     dt = time.perf_counter() - t0
-    h2d = q_host[0].numel() * 2 + B * 4 + 2 * B * wl.Hkv * d * 2
-    d2h = out_host.numel() * 4 + lse_host.numel() * 4
-    return {"value": round(1e6 * dt / n, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h}
+    return {"value": round(1e6 * dt / n, 3), "unit": UNIT, "h2d_bytes_per_step": nbytes,
+            "d2h_bytes_per_step": res_host.numel() * 4}
 
 
 def oracle_baseline(wl, budget_s=12.0, steps=1):

@@ -90,6 +90,11 @@ TSA_API const char* tsa_last_error(void);
 /* Version string of the library build. */
 TSA_API const char* tsa_version(void);
 
+/* Number of kernels this library has launched in this process so far (all
+ * threads, all entry points; a memset of workspace counters is not a
+ * kernel and is not counted). */
+TSA_API unsigned long long tsa_kernel_launches(void);
+
 /* Per-stage timing (optional, thread-local).  With n >= 4 cudaEvent_t
  * handles (cast to void*), every later sparse_attn_decode / retopk_step call
  * on this thread records events[0] after zeroing its workspace counters

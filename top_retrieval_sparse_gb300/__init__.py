@@ -23,7 +23,7 @@ from . import build as _build
 __all__ = [
     "TsaError", "lib", "KV", "kv_contiguous", "kv_paged", "decode_workspace_size",
     "sparse_attn_decode", "lse_merge", "ReTopK", "library_path", "set_stage_events",
-    "set_trace", "read_trace",
+    "set_trace", "read_trace", "kernel_launches",
 ]
 
 TSA_OK = 0
@@ -78,6 +78,7 @@ def lib():
             L.retopk_destroy.argtypes = [P]
             L.tsa_set_stage_events.argtypes = [C.POINTER(P), i32]
             L.tsa_set_trace.argtypes = [P, sz]
+            L.tsa_kernel_launches.restype = C.c_ulonglong
             _lib = L
     return _lib
 
@@ -102,6 +103,11 @@ def _want(t: torch.Tensor, dtype, name: str):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+
+
+def kernel_launches() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(lib().tsa_kernel_launches())
 
 
 def set_stage_events(events) -> None:

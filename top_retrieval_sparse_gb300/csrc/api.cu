@@ -2,6 +2,7 @@
 //
 // Host-side validation, workspace layout and the launch sequence of each
 // entry point.  Nothing here allocates device memory, synchronises or prints.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -24,6 +25,13 @@ namespace {
 thread_local std::string g_err;
 thread_local cudaEvent_t g_stage[4] = {nullptr, nullptr, nullptr, nullptr};
 thread_local TraceBuf g_trace = {nullptr, nullptr, 0};
+std::atomic<unsigned long long> g_launches{0};
+
+// Count a kernel launch of this library once it has been issued.
+cudaError_t counted(cudaError_t e) {
+  if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+  return e;
+}
 
 // Record stage event i on stream st when stage timing is on.
 cudaError_t stage_mark(int i, cudaStream_t st) {
@@ -170,14 +178,14 @@ cudaError_t launch_exact_topk(const uint16_t* q, const KvView& view, const int32
   int64_t grid = num_sms();
   if (grid > tiles) grid = tiles;
   if (grid < 1) grid = 1;
-  cudaError_t e = launch_scan(s, (int)grid, st, false);
+  cudaError_t e = counted(launch_scan(s, (int)grid, st, false));
   if (e != cudaSuccess) return e;
   if ((e = stage_mark(1, st)) != cudaSuccess) return e;
   if (K <= 0) return stage_mark(2, st);
   s.pass = 1;  // heads whose hint failed re-emit with their exact bin
   s.head_active = w.rescan;
   s.active_value = 1;
-  if ((e = launch_scan(s, (int)grid, st, true)) != cudaSuccess) return e;
+  if ((e = counted(launch_scan(s, (int)grid, st, true))) != cudaSuccess) return e;
   ResolveArgs r{};
   r.lens = lens;
   r.len_host = len_host;
@@ -198,7 +206,7 @@ cudaError_t launch_exact_topk(const uint16_t* q, const KvView& view, const int32
   r.sel_z = sel_z;
   r.sel_n = sel_n;
   r.trace = g_trace;
-  if ((e = launch_resolve(r, st)) != cudaSuccess) return e;
+  if ((e = counted(launch_resolve(r, st))) != cudaSuccess) return e;
   return stage_mark(2, st);
 }
 
@@ -256,6 +264,10 @@ extern "C" {
 const char* tsa_last_error(void) { return g_err.c_str(); }
 
 const char* tsa_version(void) { return "tsa 0.1 (sm_103a)"; }
+
+unsigned long long tsa_kernel_launches(void) {
+  return g_launches.load(std::memory_order_relaxed);
+}
 
 int tsa_set_stage_events(void* const* events, int n) {
   if (events && n > 0 && n < 4)
@@ -357,7 +369,7 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
     a.out = out;
     a.lse_out = lse_out;
     a.trace = g_trace;
-    if ((e = launch_attend(a, st)) != cudaSuccess) return cuda_fail(e, "attend launch");
+    if ((e = counted(launch_attend(a, st))) != cudaSuccess) return cuda_fail(e, "attend launch");
   }
   if ((e = stage_mark(3, st)) != cudaSuccess) return cuda_fail(e, "event record");
   return ok();
@@ -369,8 +381,8 @@ int lse_merge(const float* o_a, const float* lse_a, const float* o_b, const floa
   if (rows == 0) return ok();
   if (!o_a || !lse_a || !o_b || !lse_b || !o_out || !lse_out)
     return fail(TSA_ERR_INVALID_ARG, "NULL pointer");
-  cudaError_t e = launch_lse_merge(o_a, lse_a, o_b, lse_b, o_out, lse_out, rows, d,
-                                   static_cast<cudaStream_t>(stream));
+  cudaError_t e = counted(launch_lse_merge(o_a, lse_a, o_b, lse_b, o_out, lse_out, rows, d,
+                                   static_cast<cudaStream_t>(stream)));
   if (e != cudaSuccess) return cuda_fail(e, "lse_merge launch");
   return ok();
 }
@@ -514,7 +526,7 @@ int retopk_init(tsa_retopk* st, const void* prefill_q, const int32_t* prefill_su
   a.cache_qbar = st->qbar;
   a.cache_sup = st->sup;
   a.cache_sup_n = st->sup_n;
-  cudaError_t e = launch_retopk_init(a, static_cast<cudaStream_t>(stream));
+  cudaError_t e = counted(launch_retopk_init(a, static_cast<cudaStream_t>(stream)));
   if (e != cudaSuccess) return cuda_fail(e, "retopk init launch");
   st->t = 0;
   st->fifo_head = 0;
@@ -602,7 +614,7 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
     a.cand_out = cand_out;
     a.trace = g_trace;
     const size_t smem = up((size_t)a.bitmap_words * 4, 16);
-    if ((e = launch_retopk_selector(a, smem, s)) != cudaSuccess)
+    if ((e = counted(launch_retopk_selector(a, smem, s))) != cudaSuccess)
       return cuda_fail(e, "retopk selector launch");
   }
   // 2. exact path heads: key scan + exact top-K over all keys (no window)
@@ -630,7 +642,7 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
     a.sel_n = sel_n;
     a.trace = g_trace;
     const int chunks = (Lw.cand_cap + a.chunk - 1) / a.chunk;
-    if ((e = launch_retopk_rescore(a, chunks, s)) != cudaSuccess)
+    if ((e = counted(launch_retopk_rescore(a, chunks, s))) != cudaSuccess)
       return cuda_fail(e, "retopk rescore launch");
   }
   // 4. sparse softmax.V over S_t (no window) and the FIFO push
@@ -659,7 +671,7 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
     a.C = st->C;
     a.slot = st->fifo_head;
     a.trace = g_trace;
-    if ((e = launch_attend(a, s)) != cudaSuccess) return cuda_fail(e, "attend launch");
+    if ((e = counted(launch_attend(a, s))) != cudaSuccess) return cuda_fail(e, "attend launch");
   }
   if ((e = stage_mark(3, s)) != cudaSuccess) return cuda_fail(e, "event record");
   st->t += 1;
