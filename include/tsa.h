@@ -152,6 +152,38 @@ TSA_API int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* l
                        int32_t* topk_idx, float* topk_score, void* workspace,
                        size_t ws_bytes, void* stream);
 
+/* sparse_attn_decode_noalloc -- sparse_attn_decode without a caller
+ * workspace.  The pages have no counterpart: this is a library service.
+ *
+ * For callers that cannot allocate device memory when they decode: a serving
+ * engine that gives nearly all device memory to its KV-cache pool at start-up
+ * and allows no later allocation, or a host for which cudaMalloc (it may
+ * synchronise the device) is off limits inside the decode loop.  The scratch
+ * lives in one array of tsa_noalloc_scratch_bytes() (32 MiB) of device
+ * memory per device, which the library's module holds from the time it is
+ * loaded on that device until the process exits.
+ *
+ * Same arguments and results as sparse_attn_decode, minus the workspace.
+ *   - Problems whose tsa_decode_workspace_size() exceeds the array are
+ *     rejected with TSA_ERR_WORKSPACE (nothing launched); e.g. B*Hq = 4 fits
+ *     caches up to about 0.5 M positions, B*Hq = 32 fits none beyond a few
+ *     thousand.
+ *   - The first call on a device looks the array's device address up
+ *     (cudaGetSymbolAddress, with that device current), which may load the
+ *     library's module; make that first call before any stream capture.
+ *   - Every call on a device, from any thread or stream, uses the same
+ *     array, which keeps the previous call's contents; each call clears the
+ *     counters that must start at zero on its stream.  Calls that overlap on
+ *     the GPU race: order them on one stream.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+TSA_API size_t tsa_noalloc_scratch_bytes(void);
+
+TSA_API int sparse_attn_decode_noalloc(const void* q, const tsa_kv* kv,
+                       const int32_t* lens, int B, int Hq, int Hkv, int d, int K,
+                       int n_init, int n_recent, float scale, float* out,
+                       float* lse_out, int32_t* topk_idx, float* topk_score,
+                       void* stream);
+
 /* ------------------------------------------------------------------ */
 /* lse_merge -- [RA] Eq. 4-5 on precomputed partials.
  *

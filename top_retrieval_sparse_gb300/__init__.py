@@ -23,7 +23,8 @@ from . import build as _build
 __all__ = [
     "TsaError", "lib", "KV", "kv_contiguous", "kv_paged", "decode_workspace_size",
     "sparse_attn_decode", "lse_merge", "ReTopK", "library_path", "set_stage_events",
-    "set_trace", "read_trace", "kernel_launches",
+    "set_trace", "read_trace", "kernel_launches", "sparse_attn_decode_noalloc",
+    "noalloc_scratch_bytes",
 ]
 
 TSA_OK = 0
@@ -65,6 +66,9 @@ def lib():
             L.sparse_attn_decode.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32, f32,
                                              P, P, P, P, P, sz, P]
             L.lse_merge.argtypes = [P, P, P, P, P, P, i32, i32, P]
+            L.sparse_attn_decode_noalloc.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32,
+                                                     i32, f32, P, P, P, P, P]
+            L.tsa_noalloc_scratch_bytes.restype = sz
             L.retopk_state_size.argtypes = [i32, i32, i32, i32]
             L.retopk_state_size.restype = sz
             L.retopk_create.argtypes = [C.POINTER(P), i32, i32, i32, i32, i32, i32, i32, f32,
@@ -208,6 +212,33 @@ def sparse_attn_decode(q: torch.Tensor, kv: KV, lens: torch.Tensor, K: int, n_in
         float(scale), _p(out), _p(lse_out), _p(topk_idx), _p(topk_score), _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
     return out, lse_out, topk_idx, topk_score
+
+
+def sparse_attn_decode_noalloc(q: torch.Tensor, kv: KV, lens: torch.Tensor, K: int,
+                               n_init: int, n_recent: int, scale: Optional[float] = None,
+                               out: Optional[torch.Tensor] = None,
+                               lse_out: Optional[torch.Tensor] = None,
+                               topk_idx: Optional[torch.Tensor] = None,
+                               topk_score: Optional[torch.Tensor] = None, stream=None):
+    """sparse_attn_decode with the library's own fixed scratch array instead
+    of a workspace (for callers that cannot allocate while decoding; limits
+    and concurrency rules in include/tsa.h).  The output buffers are the
+    caller's: pass them to allocate nothing here either."""
+    _want(q, torch.bfloat16, "q")
+    _want(lens, torch.int32, "lens")
+    B, Hq, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    _check(lib().sparse_attn_decode_noalloc(
+        _p(q), C.byref(kv.struct), _p(lens), B, Hq, kv.Hkv, d, K, n_init, n_recent,
+        float(scale), _p(out), _p(lse_out), _p(topk_idx), _p(topk_score), _stream(stream)))
+    return out, lse_out, topk_idx, topk_score
+
+
+def noalloc_scratch_bytes() -> int:
+    return int(lib().tsa_noalloc_scratch_bytes())
 
 
 def lse_merge(o_a, lse_a, o_b, lse_b, o_out=None, lse_out=None, stream=None):

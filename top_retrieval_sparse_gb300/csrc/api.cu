@@ -259,6 +259,12 @@ int check_heads(int B, int Hq, int Hkv, int d) {
 
 }  // namespace
 
+namespace tsa {
+// Sets this thread's error message for an entry point defined in another
+// translation unit of the library; returns `code`.
+int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace tsa
+
 extern "C" {
 
 const char* tsa_last_error(void) { return g_err.c_str(); }
