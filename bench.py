@@ -148,6 +148,34 @@ def algorithmic_bytes(wl) -> dict:
     return {"scan": k_bytes, "gather": v_bytes, "io": io, "total": k_bytes + v_bytes + io}
 
 
+SCAN_SOURCES = ("scan.cu", "tsa_internal.cuh", "tsa_kernels.h")
+
+
+def scan_traffic(wl, rows_per_launch: int):
+    """DRAM bytes (read + write) of one scan launch from the committed ncu
+    summary, or None when the scan sources changed since it was captured.
+    The summary's per-row traffic is scaled to this launch's key rows."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "scan_llama128k.md")
+    if not os.path.exists(path):
+        return None, None
+    fields = {}
+    for line in open(path):
+        k, _, v = line.strip().partition(":")
+        if k in ("traffic_bytes_per_launch", "key_rows_per_launch", "source_sha256"):
+            fields[k] = v.strip()
+    h = hashlib.sha256()
+    for f in SCAN_SOURCES:
+        with open(os.path.join(ROOT, "top_retrieval_sparse_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    if fields.get("source_sha256") != h.hexdigest():
+        return None, "scan sources changed since the ncu capture"
+    per_row = int(fields["traffic_bytes_per_launch"]) / int(fields["key_rows_per_launch"])
+    note = "ncu capture of llama128k" if wl.name == "llama128k" else \
+        "llama128k ncu capture scaled by key rows"
+    return int(round(per_row * rows_per_launch)), note
+
+
 def run_ours(args, ws, rank, local):
     import torch
     import top_retrieval_sparse_gb300 as tsa
@@ -240,6 +268,7 @@ def run_ours(args, ws, rank, local):
                               "select": round(statistics.mean(sel_ms), 5),
                               "attend+merge": round(statistics.mean(att_ms), 5)},
                 "scan_gbs": round(achieved, 1), "trace": trace_summary} if rank == 0 else None
+    traffic, traffic_note = scan_traffic(wl, ab["scan"] // (wl.d * 2))
     # ---- end to end through the public API with host buffers ----
     e2e = run_e2e(args, wl, kv, work, tsa, torch, dev)
 
@@ -264,7 +293,8 @@ def run_ours(args, ws, rank, local):
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "frac_of_8tbs": round(achieved / 8000.0, 4),
-                     "traffic": None, "algorithmic_bytes_per_launch": ab["scan"]},
+                     "traffic": traffic, "traffic_source": traffic_note,
+                     "algorithmic_bytes_per_launch": ab["scan"]},
         "e2e": e2e,
         "gpu_launches": n_launches,
         "clocks": clk,
