@@ -146,7 +146,7 @@ def read_trace(buf: torch.Tensor):
     for r in rec:
         t = r[4:12].view(np.uint64)
         out.append({"kernel": int(r[0]), "cta": int(r[1]), "sm": int(r[2]),
-                    "t": [int(x) for x in t]})
+                    "info": int(r[3]), "t": [int(x) for x in t]})
     return out
 
 

@@ -60,9 +60,9 @@ constexpr size_t kAlign = 256;
 size_t up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 
 // Dense pair list capacity per head: every position once plus the sentinel
-// padding of at most 7 slots per (CTA, warp) run.
+// padding of at most 7 slots per (CTA, warp, unit visit) run.
 int64_t dense_stride_for(int64_t l_cap) {
-  return (int64_t)up((size_t)(l_cap > 0 ? l_cap : 1) + 32768, 64);
+  return (int64_t)up((size_t)(l_cap > 0 ? l_cap : 1) + 65536, 64);
 }
 
 int num_sms() {
@@ -85,6 +85,7 @@ struct SelWs {
   int* status;
   uint32_t* hist;        // zeroed per call
   uint32_t* tick_unit;   // zeroed per call
+  uint32_t* tile_ctr;    // zeroed per call
   int32_t* emit_n;       // zeroed per call
   int32_t* rescan;       // zeroed per call
   int32_t* hint_bin;     // persists between calls (any content is safe)
@@ -101,7 +102,7 @@ struct SelWs {
 // Workspace of one decode call (offsets from the base).  [zero_begin,
 // zero_end) is cleared by every call; the hint bins after it persist.
 struct DecodeLayout {
-  size_t zero_begin, status, hist, sel_n, tick_unit, emit_n, dense_n, rescan, zero_end;
+  size_t zero_begin, status, tile_ctr, hist, sel_n, tick_unit, emit_n, dense_n, rescan, zero_end;
   size_t hint_bin, rescan_bin, bstar, wz, dense, spill, sel_idx, sel_z, total;
   int64_t dense_stride;
   int wz_stride;
@@ -119,6 +120,7 @@ DecodeLayout decode_layout(int B, int Hq, int Hkv, int64_t l_cap, int K, int n_i
   size_t o = 0;
   L.zero_begin = o;
   L.status = o; o = up(o + 4);
+  L.tile_ctr = o; o = up(o + 8);
   L.hist = o; o = up(o + rows * kHistBins * 4);
   L.sel_n = o; o = up(o + rows * 4);
   L.tick_unit = o; o = up(o + units * 4);
@@ -139,13 +141,10 @@ DecodeLayout decode_layout(int B, int Hq, int Hkv, int64_t l_cap, int K, int n_i
   return L;
 }
 
-// Key scan (pass 0), re-emission for heads whose hint failed (pass 1) and
-// the per-head resolve, all on stream st.  Marks stage events 1 and 2.
-cudaError_t launch_exact_topk(const uint16_t* q, const KvView& view, const int32_t* lens,
-                              int64_t len_host, int64_t max_len, int B, int Hq, int K,
-                              int n_init, int n_recent, float scale,
-                              const int32_t* head_active, int active_value, const SelWs& w,
-                              int32_t* sel_idx, float* sel_z, int32_t* sel_n, cudaStream_t st) {
+// Argument block of the key scan (pass 0) over workspace w.
+ScanArgs scan_args(const uint16_t* q, const KvView& view, const int32_t* lens, int64_t len_host,
+                   int B, int Hq, int K, int n_init, int n_recent, float scale,
+                   const int32_t* head_active, int active_value, const SelWs& w) {
   ScanArgs s{};
   s.q = q;
   s.kv = view;
@@ -158,10 +157,12 @@ cudaError_t launch_exact_topk(const uint16_t* q, const KvView& view, const int32
   s.n_recent = n_recent;
   s.K = K;
   s.pass = 0;
+  s.decide = 1;
   s.head_active = head_active;
   s.active_value = active_value;
   s.hist = w.hist;
   s.unit_ticket = w.tick_unit;
+  s.tile_ctr = w.tile_ctr;
   s.hint_bin = w.hint_bin;
   s.rescan = w.rescan;
   s.rescan_bin = w.rescan_bin;
@@ -174,10 +175,30 @@ cudaError_t launch_exact_topk(const uint16_t* q, const KvView& view, const int32
   s.wz_stride = w.wz_stride;
   s.status = w.status;
   s.trace = g_trace;
-  const int64_t tiles = (int64_t)B * view.Hkv * ((max_len + scan_tile_rows() - 1) / scan_tile_rows());
+  return s;
+}
+
+// Persistent scan grid: one CTA per SM, at most one per tile.
+int scan_grid(int B, const KvView& view, int64_t max_len) {
+  const int64_t tiles =
+      (int64_t)B * view.Hkv * ((max_len + scan_tile_rows() - 1) / scan_tile_rows());
   int64_t grid = num_sms();
   if (grid > tiles) grid = tiles;
   if (grid < 1) grid = 1;
+  return (int)grid;
+}
+
+// Key scan (pass 0), re-emission for heads whose hint failed (pass 1) and
+// the per-head resolve, all on stream st (the ReTopK exact path).  Marks
+// stage events 1 and 2.
+cudaError_t launch_exact_topk(const uint16_t* q, const KvView& view, const int32_t* lens,
+                              int64_t len_host, int64_t max_len, int B, int Hq, int K,
+                              int n_init, int n_recent, float scale,
+                              const int32_t* head_active, int active_value, const SelWs& w,
+                              int32_t* sel_idx, float* sel_z, int32_t* sel_n, cudaStream_t st) {
+  ScanArgs s = scan_args(q, view, lens, len_host, B, Hq, K, n_init, n_recent, scale,
+                         head_active, active_value, w);
+  const int grid = scan_grid(B, view, max_len);
   cudaError_t e = counted(launch_scan(s, (int)grid, st, false));
   if (e != cudaSuccess) return e;
   if ((e = stage_mark(1, st)) != cudaSuccess) return e;
@@ -330,13 +351,11 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
   if ((e = stage_mark(0, st)) != cudaSuccess) return cuda_fail(e, "event record");
 
   const KvView view = make_view(kv, Hkv);
-  int32_t* sel_idx = topk_idx ? topk_idx : reinterpret_cast<int32_t*>(ws + Lw.sel_idx);
-  float* sel_z = topk_score ? topk_score : reinterpret_cast<float*>(ws + Lw.sel_z);
-  int32_t* sel_n = reinterpret_cast<int32_t*>(ws + Lw.sel_n);
   SelWs w{};
   w.status = reinterpret_cast<int*>(ws + Lw.status);
   w.hist = reinterpret_cast<uint32_t*>(ws + Lw.hist);
   w.tick_unit = reinterpret_cast<uint32_t*>(ws + Lw.tick_unit);
+  w.tile_ctr = reinterpret_cast<uint32_t*>(ws + Lw.tile_ctr);
   w.emit_n = reinterpret_cast<int32_t*>(ws + Lw.emit_n);
   w.rescan = reinterpret_cast<int32_t*>(ws + Lw.rescan);
   w.hint_bin = reinterpret_cast<int32_t*>(ws + Lw.hint_bin);
@@ -349,33 +368,44 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
   w.wz = reinterpret_cast<float*>(ws + Lw.wz);
   w.wz_stride = Lw.wz_stride;
 
-  // 1-2. key scan, exact top-K outside the window
+  // 1. key scan (logits, histograms, emitted pairs, window logits)
   if (kv->l_cap > 0) {
-    if ((e = launch_exact_topk(static_cast<const uint16_t*>(q), view, lens, 0, kv->l_cap, B, Hq,
-                               K, n_init, n_recent, scale, nullptr, 0, w, sel_idx, sel_z, sel_n,
-                               st)) != cudaSuccess)
-      return cuda_fail(e, "top-K launch");
+    ScanArgs s = scan_args(static_cast<const uint16_t*>(q), view, lens, 0, B, Hq, K, n_init,
+                           n_recent, scale, nullptr, 0, w);
+    s.decide = 0;  // the finish kernel decides
+    if ((e = counted(launch_scan(s, scan_grid(B, view, kv->l_cap), st, false))) != cudaSuccess)
+      return cuda_fail(e, "scan launch");
   }
-  // 3. window + selected partials and the gamma merge
+  if ((e = stage_mark(1, st)) != cudaSuccess) return cuda_fail(e, "event record");
+  if ((e = stage_mark(2, st)) != cudaSuccess) return cuda_fail(e, "event record");
+  // 2-3. exact top-K outside the window, window + selected partials, gamma merge
   {
-    AttendArgs a{};
-    a.kv = view;
-    a.lens = lens;
-    a.B = B;
-    a.Hq = Hq;
-    a.wz = w.wz;
-    a.wz_stride = w.wz_stride;
-    a.n_init = n_init;
-    a.n_recent = n_recent;
-    a.window = 1;
-    a.sel_idx = sel_idx;
-    a.sel_z = sel_z;
-    a.sel_n = sel_n;
-    a.K = K;
-    a.out = out;
-    a.lse_out = lse_out;
-    a.trace = g_trace;
-    if ((e = counted(launch_attend(a, st))) != cudaSuccess) return cuda_fail(e, "attend launch");
+    FinishArgs f{};
+    f.q = static_cast<const uint16_t*>(q);
+    f.kv = view;
+    f.lens = lens;
+    f.B = B;
+    f.Hq = Hq;
+    f.scale = scale;
+    f.K = K;
+    f.n_init = n_init;
+    f.n_recent = n_recent;
+    f.hist = w.hist;
+    f.hint_bin = w.hint_bin;
+    f.dense = w.dense;
+    f.dense_n = w.dense_n;
+    f.dense_stride = w.dense_stride;
+    f.spill = w.spill;
+    f.sel_pos = reinterpret_cast<int32_t*>(ws + Lw.sel_idx);
+    f.sel_z = reinterpret_cast<float*>(ws + Lw.sel_z);
+    f.wz = w.wz;
+    f.wz_stride = w.wz_stride;
+    f.out = out;
+    f.lse_out = lse_out;
+    f.topk_idx = topk_idx;
+    f.topk_score = topk_score;
+    f.trace = g_trace;
+    if ((e = counted(launch_finish(f, st))) != cudaSuccess) return cuda_fail(e, "finish launch");
   }
   if ((e = stage_mark(3, st)) != cudaSuccess) return cuda_fail(e, "event record");
   return ok();
@@ -413,7 +443,8 @@ namespace {
 constexpr uint32_t kMagic = 0x52544b31u;  // "RTK1"
 
 struct RetopkLayout {
-  size_t zero_begin, status, hist, sel_n, tick_rs, tick_unit, emit_n, dense_n, rescan, zero_end;
+  size_t zero_begin, status, tile_ctr, hist, sel_n, tick_rs, tick_unit, emit_n, dense_n, rescan,
+      zero_end;
   size_t hint_bin, rescan_bin, bstar, wz, dense, spill, qbar_new, path, cand, mcand, ehat,
       sel_idx, sel_z, total;
   int64_t dense_stride;
@@ -428,6 +459,7 @@ RetopkLayout retopk_layout(const tsa_retopk* s) {
   size_t o = 0;
   L.zero_begin = o;
   L.status = o; o = up(o + 4);
+  L.tile_ctr = o; o = up(o + 8);
   L.hist = o; o = up(o + H * kHistBins * 4);
   L.sel_n = o; o = up(o + H * 4);
   L.tick_rs = o; o = up(o + H * 4);
@@ -581,6 +613,7 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
   w.status = reinterpret_cast<int*>(ws + Lw.status);
   w.hist = reinterpret_cast<uint32_t*>(ws + Lw.hist);
   w.tick_unit = reinterpret_cast<uint32_t*>(ws + Lw.tick_unit);
+  w.tile_ctr = reinterpret_cast<uint32_t*>(ws + Lw.tile_ctr);
   w.emit_n = reinterpret_cast<int32_t*>(ws + Lw.emit_n);
   w.rescan = reinterpret_cast<int32_t*>(ws + Lw.rescan);
   w.hint_bin = reinterpret_cast<int32_t*>(ws + Lw.hint_bin);

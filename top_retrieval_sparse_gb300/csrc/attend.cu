@@ -35,18 +35,6 @@ struct AttPart {                               // [0] window rows, [1] selected 
   float o[2][kD];
 };
 
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n"
-               "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-}
-__device__ __forceinline__ float ld_dsmem(const float* p, uint32_t cta) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(cta));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
-}
-
 // Merge (m1, l1, o1) into (m0, l0, o0) for one lane's 4 output elements.
 __device__ __forceinline__ void merge4(float& m0, float& l0, float (&o0)[4], float m1, float l1,
                                        const float (&o1)[4]) {

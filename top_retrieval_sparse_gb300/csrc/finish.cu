@@ -1,0 +1,699 @@
+// finish.cu -- the rest of a decode step after the key scan, in one kernel:
+// exact top-K selection from the pairs the scan emitted, softmax.V over the
+// static window and over the selected rows, and the gamma1/gamma2 merge.
+//
+// "RetrievalAttention" Eq. 2 (the selected set: exact top-k by inner
+// product, as in the Flat baseline, ties to the smaller position), Eq. 3
+// (o_W and o_Omega over disjoint W and Omega, each with its local max) and
+// Eq. 4-5 (o_t = g1 o_W + g2 o_Omega).
+//
+// One thread-block cluster of 8 CTAs per (sequence, query head):
+//   0. every CTA reads the head's 11-bit histogram and finds the threshold
+//      bin b* (the largest bin whose suffix count reaches K); if the scan's
+//      emission bin (the hint) was above b*, the cluster re-emits the head's
+//      pool pairs with bin >= b*, recomputing the logits with the scan's own
+//      tensor-core fragment arithmetic so that every logit -- and so every
+//      bin -- is bit-identical to the scan's; the next call's hint is stored;
+//   1. every CTA reads the whole dense pair list (a few thousand pairs, from
+//      L2) and classifies it in the same order: pairs above b* are selected
+//      outright and dealt round-robin to the 8 CTAs, pairs in b* are the
+//      candidates, all of which every CTA keeps in shared memory;
+//   2. every CTA finds the same exact threshold T among the candidates: CTA
+//      radix rounds of 11 bits on the 64-bit rank key (order-preserving
+//      logit key, then ~position, so ties go to the smaller position); a
+//      candidate is selected iff its key >= T;
+//   3. each CTA gathers V for its rows -- 1/8 of the window, its share of
+//      the selected pairs and of the selected candidates -- 32 rows per warp
+//      in flight, keeping (max, sum, o) per set in base 2; rank 0 merges the
+//      8 CTA partials through distributed shared memory and applies Eq. 4-5.
+// No step before the merge needs a cluster barrier.
+// Launched as a programmatic dependent of the scan.
+#include "tsa_internal.cuh"
+#include "tsa_kernels.h"
+
+namespace tsa {
+
+constexpr int kFinMaxCluster = 8;  // CTAs per head: 1, 2, 4 or 8 (chosen at launch)
+constexpr int kFinWarps = 16;
+constexpr int kFinThreads = 32 * kFinWarps;
+constexpr int kSelCap = 2048;   // this CTA's above-b* pairs in shared memory
+constexpr int kMyCap = 2048;    // this CTA's threshold-bin candidates in shared memory
+constexpr int kAllCap = 6144;   // the cluster's threshold-bin candidates, copied locally
+constexpr int kFinU = 8;        // pairs per thread per batch
+constexpr int kRankShift = 64 - kHistBits;  // b* = the rank key's top 11 bits
+constexpr float kFinLog2e = 1.4426950408889634f;
+constexpr float kFinLn2 = 0.6931471805599453f;
+
+struct FinShared {
+  uint64_t cand[kAllCap];         // rank keys of all threshold-bin candidates, cluster order
+  uint64_t mycand[kMyCap];        // this CTA's candidates (read by the cluster)
+  uint2 sel[kSelCap];             // this CTA's above-b* pairs (position, logit bits)
+  uint32_t hist[kHistBins];       // radix round histogram
+  float wo[kFinWarps][2][kD];     // warp partials: [set][d], set 0 window, 1 selected
+  float wm[kFinWarps][2], wl[kFinWarps][2];
+  float po[2][kD];                // CTA partial (read by rank 0)
+  float pm[2], pl[2];
+  uint32_t warp_tot[32];
+  int cnt[2];                     // read by the cluster: above-b* pairs, candidates
+  int aoff[kFinMaxCluster + 1];   // cluster prefix of the above-b* counts
+  int coff[kFinMaxCluster + 1];   // cluster prefix of the candidate counts
+  int scal[8];
+};
+
+// Block-wide exclusive scan of one int per thread (all threads call).
+__device__ int fin_scan(int v, FinShared& sh, int* total) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sh.warp_tot[wid] = (uint32_t)incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int w = lane < kFinWarps ? (int)sh.warp_tot[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    if (lane < kFinWarps) sh.warp_tot[lane] = (uint32_t)(wi - w);
+    if (lane == kFinWarps - 1) sh.scal[7] = wi;
+  }
+  __syncthreads();
+  const int off = incl - v + (int)sh.warp_tot[wid];
+  *total = sh.scal[7];
+  __syncthreads();
+  return off;
+}
+
+// Step 0: re-emit the pool pairs of head bh whose bin is >= ebin.  The CTA
+// of cluster rank `rank` covers rows [L*rank/8, L*(rank+1)/8) in blocks of
+// 16 rows per warp; fragments, k order and the final (c0 + c1) * scale are
+// those of the key scan, so each logit equals the scan's bit for bit.
+__device__ void reemit(const FinishArgs& a, int b, int h, int g, int G, int64_t L, int ebin,
+                       int rank, int nc) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int gr = lane >> 2, tq = lane & 3;
+  const int hl = h - g * G;
+  const int bh = b * a.Hq + h;
+  const int head0 = b * a.Hq + g * G;
+  uint32_t qb[4][4];
+  const uint16_t* qp = a.q + ((int64_t)head0 + (gr < G ? gr : 0)) * kD;
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (gr < G) w = *reinterpret_cast<const uint4*>(qp + 8 * (4 * p + tq));
+    qb[p][0] = w.x; qb[p][1] = w.y; qb[p][2] = w.z; qb[p][3] = w.w;
+  }
+  uint2* drow = a.dense + (int64_t)bh * a.dense_stride;
+  const int64_t r0 = L * rank / nc, r1 = L * (rank + 1) / nc;
+  const bool mine = tq == (hl >> 1);  // lanes holding head hl's column
+  for (int64_t base = r0 + 16 * wid; base < r1; base += 16 * kFinWarps) {
+    const int64_t ia = base + gr, ib = base + gr + 8;
+    uint4 W[4], X[4];
+    const uint16_t* ka = a.kv.k + kv_row(a.kv, b, g, ia < r1 ? ia : r0);
+    const uint16_t* kb = a.kv.k + kv_row(a.kv, b, g, ib < r1 ? ib : r0);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      W[p] = ia < r1 ? *reinterpret_cast<const uint4*>(ka + 8 * (4 * p + tq))
+                     : make_uint4(0u, 0u, 0u, 0u);
+      X[p] = ib < r1 ? *reinterpret_cast<const uint4*>(kb + 8 * (4 * p + tq))
+                     : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      mma_bf16(c0, W[p].x, X[p].x, W[p].y, X[p].y, qb[p][0], qb[p][1]);
+      mma_bf16(c1, W[p].z, X[p].z, W[p].w, X[p].w, qb[p][2], qb[p][3]);
+    }
+    const bool odd = hl & 1;
+    const float za = (odd ? c0[1] + c1[1] : c0[0] + c1[0]) * a.scale;
+    const float zb = (odd ? c0[3] + c1[3] : c0[2] + c1[2]) * a.scale;
+    const bool ea = mine && ia < r1 && !in_window(ia, L, a.n_init, a.n_recent) &&
+                    (int)(f2key(za) >> kHistShift) >= ebin;
+    const bool eb = mine && ib < r1 && !in_window(ib, L, a.n_init, a.n_recent) &&
+                    (int)(f2key(zb) >> kHistShift) >= ebin;
+    const unsigned ma = __ballot_sync(0xffffffffu, ea), mb = __ballot_sync(0xffffffffu, eb);
+    const int cnt = __popc(ma) + __popc(mb);
+    if (!cnt) continue;
+    int64_t slot0 = 0;
+    if (lane == 0) slot0 = atomicAdd(a.dense_n + bh, cnt);
+    slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+    const unsigned lt = (1u << lane) - 1u;
+    if (ea) {
+      const int64_t s = slot0 + __popc(ma & lt);
+      if (s < a.dense_stride) drow[s] = make_uint2((uint32_t)ia, __float_as_uint(za));
+    }
+    if (eb) {
+      const int64_t s = slot0 + __popc(ma) + __popc(mb & lt);
+      if (s < a.dense_stride) drow[s] = make_uint2((uint32_t)ib, __float_as_uint(zb));
+    }
+  }
+}
+
+template <int NC>
+__global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
+  TraceScope trace(a.trace, kTrFinish);         // start, waited, threshold found, exit
+  TraceScope phases(a.trace, kTrFinishPhases);  // start, decided, slice read, rows gathered
+  extern __shared__ __align__(16) uint8_t fin_smem[];
+  FinShared& sh = *reinterpret_cast<FinShared*>(fin_smem);
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int rank = blockIdx.x;  // cluster rank (the cluster spans gridDim.x)
+  const int bh = blockIdx.y;
+  const int b = bh / a.Hq, h = bh % a.Hq;
+  const int G = a.Hq / a.kv.Hkv;
+  const int g = h / G;
+  pdl_wait();  // pairs, bins and window logits come from the scan
+  trace.mark(1);
+
+  const int64_t L = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
+  const int64_t nw = window_count(L, a.n_init, a.n_recent);
+  const int64_t P = L - nw;
+  const int need = (int64_t)a.K < P ? a.K : (int)P;
+  uint64_t* spill = a.spill + (int64_t)bh * a.dense_stride;
+
+  // ---- 0. threshold bin b*, the emission check, the next hint ----
+  // Every CTA of the cluster reads the head's histogram and decides alike.
+  int bstar = -1, redo = 0, ebin = 0, next_hint = 0;
+  bool wide = false;
+  if (need > 0) {
+    const int32_t hw = __ldcg(a.hint_bin + bh);
+    const int used = hint_bin_of(hw);
+    wide = hint_wide_of(hw);
+    if (need < P) {
+      // pairs one call may emit, and the margin (bins below b*) the hint
+      // keeps: wider for a head whose b* has once fallen below its hint
+      const int64_t budget = wide ? 8 * (int64_t)need + 16384 : 3 * (int64_t)need + 4096;
+      const int margin = wide ? 4 : 2;
+      const uint32_t tgt[2] = {(uint32_t)need, (uint32_t)(budget + 1 < P ? budget + 1 : P + 1)};
+      const uint32_t* hh = a.hist + (int64_t)bh * kHistBins;
+      // thread t: bins 2047-4t-r, r < 4 (from the top)
+      const uint4 x = __ldcg(reinterpret_cast<const uint4*>(hh + kHistBins - 4 - 4 * tid));
+      const uint32_t c[4] = {x.w, x.z, x.y, x.x};
+      const uint32_t mine = c[0] + c[1] + c[2] + c[3];
+      if (tid == 0) sh.scal[0] = sh.scal[1] = -1;
+      int tot;
+      const uint32_t excl = (uint32_t)fin_scan((int)mine, sh, &tot);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        uint32_t acc = excl;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          if (acc < tgt[k] && acc + c[r] >= tgt[k]) sh.scal[k] = kHistBins - 1 - 4 * tid - r;
+          acc += c[r];
+        }
+      }
+      __syncthreads();
+      bstar = sh.scal[0];  // largest bin whose suffix count reaches need
+      const int bbud = sh.scal[1];
+      // next hint: `margin` bins (a quarter octave of logit each) below b*,
+      // so that step-to-step shifts of b* keep it valid, and no lower than
+      // the emission budget allows (bins above bbud hold at most `budget`
+      // pairs).  A lower hint that still fits the budget is kept: the hint
+      // falls at once and rises only when the emission outgrows the budget.
+      const int lo = bbud + 1 > 0 ? bbud + 1 : 0;
+      const int target = bstar - margin > lo ? bstar - margin : lo;
+      int hnt = used < target && used >= lo ? used : target;
+      next_hint = hnt < bstar ? hnt : bstar;
+      redo = used > bstar;  // the scan skipped pairs of bins >= b*
+      ebin = bstar;
+    } else {  // every pool position is selected
+      redo = used > 0;
+      ebin = 0;
+      next_hint = 0;
+    }
+  }
+  phases.mark(1);
+  trace.info = (uint32_t)min((int64_t)__ldcg(a.dense_n + bh), (int64_t)0x7fffffff);
+  phases.info = ((uint32_t)redo << 31) | ((uint32_t)(bstar & 0x7fff) << 16) |
+                (uint32_t)(need > 0 ? hint_bin_of(__ldcg(a.hint_bin + bh)) : 0);
+  // ---- re-emission when the scan's hint missed (rare: first call, shifts) ----
+  if (redo) {  // uniform over the cluster
+    cluster_sync_all();  // every CTA has read the old list size
+    if (rank == 0 && tid == 0) {
+      a.dense_n[bh] = 0;
+      __threadfence();
+    }
+    cluster_sync_all();
+    reemit(a, b, h, g, G, L, ebin, rank, NC);
+    __threadfence();
+    cluster_sync_all();
+  }
+
+  // ---- 1. this CTA's slice of the pair list ----
+  // Pairs above b* are this CTA's selected rows; pairs in b* are candidates.
+  // After one cluster barrier every CTA copies all the cluster's candidates
+  // (a few thousand at most in practice) through distributed shared memory.
+  int nmy = 0, nmc = 0;
+  int64_t n = 0, s0 = 0, s1 = 0;
+  if (need > 0) {
+    n = __ldcg(a.dense_n + bh);
+    if (n > a.dense_stride) n = a.dense_stride;
+    s0 = n * rank / NC;
+    s1 = n * (rank + 1) / NC;
+    const uint2* row = a.dense + (int64_t)bh * a.dense_stride;
+    for (int64_t jb = s0; jb < s1; jb += kFinThreads * kFinU) {
+      uint2 pv[kFinU];
+#pragma unroll
+      for (int u = 0; u < kFinU; ++u) {
+        const int64_t jj = jb + u * kFinThreads + tid;
+        pv[u] = jj < s1 ? __ldcg(row + jj) : make_uint2(0xffffffffu, 0u);
+      }
+      uint64_t v[kFinU];
+      uint32_t selm = 0u, cndm = 0u;
+#pragma unroll
+      for (int u = 0; u < kFinU; ++u) {
+        v[u] = 0;
+        if (pv[u].x != 0xffffffffu) {
+          v[u] = rank_key(__uint_as_float(pv[u].y), pv[u].x);
+          const int bin = (int)(v[u] >> kRankShift);
+          if (bstar < 0 || bin > bstar) selm |= 1u << u;
+          else if (bin == bstar) cndm |= 1u << u;
+        }
+      }
+      int tot;
+      const int off = fin_scan((__popc(selm) << 16) | __popc(cndm), sh, &tot);
+      int i1 = nmy + (off >> 16), i2 = nmc + (off & 0xffff);
+#pragma unroll
+      for (int u = 0; u < kFinU; ++u) {
+        if ((selm >> u) & 1u) {  // slice-relative spill from the bottom
+          if (i1 < kSelCap) sh.sel[i1] = pv[u];
+          else spill[s0 + (i1 - kSelCap)] = v[u];
+          ++i1;
+        } else if ((cndm >> u) & 1u) {  // ... and from the top
+          if (i2 < kMyCap) sh.mycand[i2] = v[u];
+          else spill[s1 - 1 - (i2 - kMyCap)] = v[u];
+          ++i2;
+        }
+      }
+      nmy += tot >> 16;
+      nmc += tot & 0xffff;
+    }
+  }
+  if (tid == 0) {
+    sh.cnt[0] = nmy;
+    sh.cnt[1] = nmc;
+  }
+  phases.mark(2);
+  cluster_sync_all();  // every CTA's lists and counts are complete
+  if (wid == 0) {
+    int ca = 0, cc = 0;
+    if (lane < NC) {
+      ca = (int)ld_dsmem_u32(reinterpret_cast<const uint32_t*>(&sh.cnt[0]), lane);
+      cc = (int)ld_dsmem_u32(reinterpret_cast<const uint32_t*>(&sh.cnt[1]), lane);
+    }
+    int ia = ca, ic = cc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int ya = __shfl_up_sync(0xffffffffu, ia, o), yc = __shfl_up_sync(0xffffffffu, ic, o);
+      if (lane >= o) {
+        ia += ya;
+        ic += yc;
+      }
+    }
+    if (lane < NC) {
+      sh.aoff[lane + 1] = ia;
+      sh.coff[lane + 1] = ic;
+    }
+    if (lane == 0) sh.aoff[0] = sh.coff[0] = 0;
+  }
+  __syncthreads();
+  const int nabove = sh.aoff[NC], ncand = sh.coff[NC];
+  // candidate j of the cluster (cluster order): CTA c's list, local index i
+  auto cand_remote = [&](int jc) -> uint64_t {
+    int c = 0;
+#pragma unroll
+    for (int k = 1; k < NC; ++k) c += jc >= sh.coff[k] ? 1 : 0;
+    const int i = jc - sh.coff[c];
+    if (i < kMyCap) return ld_dsmem_u64(&sh.mycand[i], (uint32_t)c);
+    const int64_t c1 = n * (c + 1) / NC;
+    return __ldcg(spill + (c1 - 1 - (i - kMyCap)));
+  };
+  for (int jc = tid; jc < ncand && jc < kAllCap; jc += kFinThreads) sh.cand[jc] = cand_remote(jc);
+  __syncthreads();
+  auto cand_at = [&](int jc) -> uint64_t {
+    return jc < kAllCap ? sh.cand[jc] : cand_remote(jc);
+  };
+
+  // ---- 2. the threshold among the candidates (same result in every CTA) ----
+  // cmode 0: no candidate selected, 1: all, 2: those with rank key >= T
+  int cmode = 0;
+  uint64_t T = 0;
+  const int need_rem = need - nabove;
+  if (need > 0 && bstar >= 0 && need_rem > 0) {
+    if (need_rem >= ncand) {
+      cmode = 1;
+    } else {
+      cmode = 2;
+      uint64_t prefix = (uint64_t)bstar << kRankShift;
+      uint64_t mask = (uint64_t)(kHistBins - 1) << kRankShift;
+      int shift = kRankShift, match = ncand, rem = need_rem;
+      while (true) {
+        if (match <= rem) {  // everything still matching is selected
+          T = prefix;
+          break;
+        }
+        const int db = shift < kHistBits ? shift : kHistBits;
+        shift -= db;
+        const uint32_t dmask = (1u << db) - 1u;
+        for (int q = tid; q < kHistBins; q += kFinThreads) sh.hist[q] = 0;
+        __syncthreads();
+        for (int jc = tid; jc < ncand; jc += kFinThreads) {
+          const uint64_t v = cand_at(jc);
+          if ((v & mask) == prefix) atomicAdd(&sh.hist[(uint32_t)(v >> shift) & dmask], 1u);
+        }
+        __syncthreads();
+        // thread t: bins nb-1-4t-r (from the top); digits past nb are empty
+        const int nb = 1 << db;
+        uint32_t c[4], mine = 0;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int bin = nb - 1 - 4 * tid - r;
+          c[r] = bin >= 0 ? sh.hist[bin] : 0u;
+          mine += c[r];
+        }
+        int tot;
+        const uint32_t excl = (uint32_t)fin_scan((int)mine, sh, &tot);
+        if (excl < (uint32_t)rem && excl + mine >= (uint32_t)rem) {
+          uint32_t acc = excl;
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            if (acc < (uint32_t)rem && acc + c[r] >= (uint32_t)rem) {
+              sh.scal[2] = nb - 1 - 4 * tid - r;  // threshold digit d*
+              sh.scal[3] = (int)acc;              // candidates above it
+              sh.scal[4] = (int)c[r];             // candidates equal to it
+            }
+            acc += c[r];
+          }
+        }
+        __syncthreads();
+        const uint32_t dstar = (uint32_t)sh.scal[2];
+        rem -= sh.scal[3];
+        match = sh.scal[4];
+        __syncthreads();  // scal is rewritten by the next round
+        prefix |= (uint64_t)dstar << shift;
+        mask |= (uint64_t)dmask << shift;
+        if (rem == 0) {  // the digits above d* were exactly enough
+          T = prefix + (1ull << shift);
+          break;
+        }
+        if (shift == 0) {
+          T = prefix;
+          break;
+        }
+      }
+    }
+  }
+  auto cand_selected = [&](uint64_t v) -> bool { return cmode == 1 || (cmode == 2 && v >= T); };
+  trace.mark(2);
+
+  // ---- 3. softmax.V over this CTA's rows ----
+  // rows: 1/8 of the window, this CTA's above-b* pairs, and the cluster's
+  // candidates j = rank + 8k that are selected
+  const int64_t wr0 = nw * rank / NC, wr1 = nw * (rank + 1) / NC;
+  const int nwr = (int)(wr1 - wr0);
+  const int ncmine = cmode != 0 && ncand > rank ? (ncand - rank + NC - 1) / NC : 0;
+  const int R = nwr + nmy + ncmine;
+  const int w0 = (int)((int64_t)R * wid / kFinWarps), w1 = (int)((int64_t)R * (wid + 1) / kFinWarps);
+  const uint16_t* vbase = a.kv.page_table ? a.kv.v : a.kv.v + kv_row(a.kv, b, g, 0);
+  const float* wzrow = a.wz + (int64_t)bh * a.wz_stride;
+  // 32 rows per warp at a time: lane l holds row base + l's position and
+  // logit; V rows are read by half-warps (16 lanes x 16 bytes = one row), so
+  // load k brings rows base + 2k (lanes 0-15) and base + 2k + 1 (lanes
+  // 16-31), and each lane accumulates 8 columns, 8 * (lane % 16) onwards.
+  const int half = lane >> 4, col = 8 * (lane & 15);
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+  float o[2][8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) o[0][e] = o[1][e] = 0.f;
+  for (int base = w0; base < w1; base += 32) {
+    float z = -INFINITY;
+    int pos = 0, set = 0;
+    bool lv = false;
+    const int j = base + lane;
+    if (j < w1) {
+      if (j < nwr) {  // window row: its logit is loaded after the V loads issue
+        pos = (int)window_pos(wr0 + j, L, a.n_init, a.n_recent);
+        lv = true;
+      } else if (j < nwr + nmy) {
+        const int li = j - nwr;
+        if (li < kSelCap) {
+          const uint2 pr = sh.sel[li];
+          pos = (int)pr.x;
+          z = __uint_as_float(pr.y);
+        } else {
+          const uint64_t v = __ldcg(spill + s0 + (li - kSelCap));
+          pos = (int)rank_pos(v);
+          z = key2f((uint32_t)(v >> 32));
+        }
+        set = 1;
+        lv = true;
+      } else {
+        const uint64_t v = cand_at(rank + NC * (j - nwr - nmy));
+        if (cand_selected(v)) {
+          pos = (int)rank_pos(v);
+          z = key2f((uint32_t)(v >> 32));
+          lv = true;
+        }
+        set = 1;
+      }
+    }
+    const unsigned live = __ballot_sync(0xffffffffu, lv);
+    const unsigned sel1 = __ballot_sync(0xffffffffu, set == 1);
+    uint4 vv[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const int r = 2 * k + half;
+      const int pk = __shfl_sync(0xffffffffu, pos, r);
+      const uint16_t* vr =
+          a.kv.page_table ? vbase + kv_row(a.kv, b, g, pk) : vbase + (int64_t)pk * kD;
+      vv[k] = ((live >> r) & 1u) ? __ldg(reinterpret_cast<const uint4*>(vr + col))
+                                 : make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (lv && j < nwr) z = __ldcg(wzrow + wr0 + j);
+    z = lv ? z * kFinLog2e : -INFINITY;
+    // chunk maxima per set, rescale, then each lane weights its own row
+#pragma unroll
+    for (int st = 0; st < 2; ++st) {
+      const float bm = warp_max(set == st ? z : -INFINITY);
+      if (bm > m[st]) {
+        const float sc = m[st] == -INFINITY ? 0.f : exp2f(m[st] - bm);
+        l[st] *= sc;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[st][e] *= sc;
+        m[st] = bm;
+      }
+    }
+    const float p = lv ? exp2f(z - (set ? m[1] : m[0])) : 0.f;
+    l[0] += warp_sum(set == 0 ? p : 0.f);
+    l[1] += warp_sum(set == 1 ? p : 0.f);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      if (!((live >> (2 * k)) & 3u)) continue;  // warp-uniform: both rows absent
+      const int r = 2 * k + half;
+      const float pr = __shfl_sync(0xffffffffu, p, r);  // 0 for an absent row
+      const uint4 w = vv[k];
+      const float v[8] = {bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y),
+                          bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w)};
+      if ((sel1 >> r) & 1u) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[1][e] = fmaf(pr, v[e], o[1][e]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[0][e] = fmaf(pr, v[e], o[0][e]);
+      }
+    }
+  }
+  // the two half-warps hold the same columns for different rows
+#pragma unroll
+  for (int st = 0; st < 2; ++st)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[st][e] += __shfl_xor_sync(0xffffffffu, o[st][e], 16);
+  // combine the warps of this CTA
+  phases.mark(3);
+#pragma unroll
+  for (int st = 0; st < 2; ++st) {
+    if (lane == 0) {
+      sh.wm[wid][st] = m[st];
+      sh.wl[wid][st] = l[st];
+    }
+    if (lane < 16) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sh.wo[wid][st][col + e] = o[st][e];
+    }
+  }
+  __syncthreads();
+  if (tid < 2 * kD) {
+    const int st = tid / kD, t = tid % kD;  // (set, element)
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kFinWarps; ++w) M = fmaxf(M, sh.wm[w][st]);
+    float acc = 0.f, lsum = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kFinWarps; ++w) {
+        if (sh.wm[w][st] == -INFINITY) continue;
+        const float e = exp2f(sh.wm[w][st] - M);
+        acc = fmaf(e, sh.wo[w][st][t], acc);
+        lsum = fmaf(e, sh.wl[w][st], lsum);
+      }
+    }
+    sh.po[st][t] = acc;
+    if (t == 0) {
+      sh.pm[st] = M;
+      sh.pl[st] = lsum;
+    }
+  }
+  const bool want_idx = a.topk_idx != nullptr || a.topk_score != nullptr;
+  cluster_sync_all();  // every CTA's partial is in its shared memory
+
+  // ---- rank 0: Eq. 4-5 over the cluster's partials ----
+  if (rank == 0 && tid < kD) {
+    float mc[2][NC], lc[2][NC], oc[2][NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c)
+#pragma unroll
+      for (int st = 0; st < 2; ++st) {
+        mc[st][c] = ld_dsmem(&sh.pm[st], c);
+        lc[st][c] = ld_dsmem(&sh.pl[st], c);
+        oc[st][c] = ld_dsmem(&sh.po[st][tid], c);
+      }
+    float zt[2], lsum[2], osum[2];
+#pragma unroll
+    for (int st = 0; st < 2; ++st) {
+      float M = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) M = fmaxf(M, mc[st][c]);
+      float ls = 0.f, os = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          const float e = mc[st][c] == -INFINITY ? 0.f : exp2f(mc[st][c] - M);
+          ls = fmaf(e, lc[st][c], ls);
+          os = fmaf(e, oc[st][c], os);
+        }
+      }
+      zt[st] = M;  // z~1 (window), z~2 (selected), base 2
+      lsum[st] = ls;
+      osum[st] = os;
+    }
+    float outv = 0.f, lse = -INFINITY;
+    const bool eW = !(lsum[0] > 0.f), eO = !(lsum[1] > 0.f);
+    if (!(eW && eO)) {
+      const float z = eW ? zt[1] : (eO ? zt[0] : fmaxf(zt[0], zt[1]));
+      const float aW = eW ? 0.f : exp2f(zt[0] - z);
+      const float aO = eO ? 0.f : exp2f(zt[1] - z);
+      const float den = aW * lsum[0] + aO * lsum[1];
+      outv = (aW * osum[0] + aO * osum[1]) / den;  // g1 o_W + g2 o_Omega
+      lse = (z + log2f(den)) * kFinLn2;
+    }
+    a.out[(int64_t)bh * kD + tid] = outv;
+    if (tid == 0 && a.lse_out) a.lse_out[bh] = lse;
+  }
+  // ---- optional top-K outputs: each CTA writes its above-b* pairs at its
+  // cluster offset; rank 0 appends the selected candidates in cluster order ----
+  if (want_idx) {
+    int32_t* oidx = a.topk_idx ? a.topk_idx + (int64_t)bh * a.K : nullptr;
+    float* osc = a.topk_score ? a.topk_score + (int64_t)bh * a.K : nullptr;
+    for (int li = tid; li < nmy; li += kFinThreads) {
+      const int i = sh.aoff[rank] + li;
+      int32_t pos;
+      float z;
+      if (li < kSelCap) {
+        pos = (int32_t)sh.sel[li].x;
+        z = __uint_as_float(sh.sel[li].y);
+      } else {
+        const uint64_t v = __ldcg(spill + s0 + (li - kSelCap));
+        pos = (int32_t)rank_pos(v);
+        z = key2f((uint32_t)(v >> 32));
+      }
+      if (i < a.K) {
+        if (oidx) oidx[i] = pos;
+        if (osc) osc[i] = z;
+      }
+    }
+    if (rank == 0) {
+      if (cmode != 0) {
+        int done = 0;
+        for (int jb = 0; jb < ncand; jb += kFinThreads) {
+          const int jc = jb + tid;
+          uint64_t v = 0;
+          const bool s = jc < ncand && cand_selected(v = cand_at(jc));
+          int tot;
+          const int r = fin_scan(s ? 1 : 0, sh, &tot);
+          const int at = nabove + done + r;
+          if (s && at < a.K) {
+            if (oidx) oidx[at] = (int32_t)rank_pos(v);
+            if (osc) osc[at] = key2f((uint32_t)(v >> 32));
+          }
+          done += tot;
+        }
+      }
+      for (int q = (need > 0 ? need : 0) + tid; q < a.K; q += kFinThreads) {
+        if (oidx) oidx[q] = -1;
+        if (osc) osc[q] = -INFINITY;
+      }
+    }
+  }
+  if (need > 0 && rank == 0 && tid == 0)  // read by every CTA long before this point
+    a.hint_bin[bh] = next_hint | ((wide || redo) ? 1 << 16 : 0);
+  cluster_sync_all();  // rank 0 and the offsets have finished reading shared memory
+}
+
+template <int NC>
+static cudaError_t launch_finish_t(const FinishArgs& a, cudaStream_t st) {
+  const size_t smem = sizeof(FinShared);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(NC, a.B * a.Hq);
+  cfg.blockDim = dim3(kFinThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = NC;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(finish_kernel<NC>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  return cudaLaunchKernelEx(&cfg, finish_kernel<NC>, a);
+}
+
+// Cluster size: the largest of 8, 4, 2 whose CTAs for every head (one CTA
+// per SM: the kernel holds ~200 registers per thread) fill at most 85 % of
+// the SMs.  A cluster must sit in one GPC, so a nearly full device places
+// fewer large clusters than its SM count suggests: 32 clusters of 8 CTAs at
+// two per SM left two clusters for a second wave.  1 when even pairs would
+// exceed that (many heads: every head in one CTA).
+cudaError_t launch_finish(const FinishArgs& a, cudaStream_t st) {
+  static int sms[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!sms[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    sms[dev] = v > 0 ? v : 148;
+  }
+  const int64_t heads = (int64_t)a.B * a.Hq;
+  const int64_t slots = (int64_t)sms[dev] * 85 / 100;
+  if (heads * 8 <= slots) return launch_finish_t<8>(a, st);
+  if (heads * 4 <= slots) return launch_finish_t<4>(a, st);
+  if (heads * 2 <= slots) return launch_finish_t<2>(a, st);
+  return launch_finish_t<1>(a, st);
+}
+
+}  // namespace tsa

@@ -55,22 +55,27 @@ size_t scan_smem_bytes() {
          (kMaxUnits + 1) * 4 + 64;
 }
 
-// D += A * B, m16n8k16, bf16 operands, fp32 accumulators.
-__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
+// Barrier over the consumer warps with a bounded wait: an mbarrier that
+// takes one arrival per warp.  Returns false after the wait limit, so that
+// a warp that has stopped (after an abort) cannot hang the others.
+struct ConsumerBar {
+  uint64_t* bar;
+  uint32_t phase;
+  __device__ bool sync() {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+    const bool ok = mbar_wait(bar, phase);
+    phase ^= 1u;
+    return ok;
+  }
+};
 
 // Consumer-wide, on a head's histogram in global memory: out[0] = the
 // largest bin whose suffix count reaches `need` (the threshold bin b*, or -1),
 // out[1] = the largest bin whose suffix count reaches `budget` (or -1).  All
 // consumer threads call; every caller gets both bins.
 __device__ void find_bins(const uint32_t* hh, uint32_t need, uint32_t budget, uint32_t* warp_tot,
-                          int* out, int& bstar, int& bbud) {
+                          int* out, int& bstar, int& bbud, ConsumerBar& cb, volatile int* abort) {
   constexpr int per = kHistBins / kConsumers;  // 4 bins per thread, from the top
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   if (tid == 0) out[0] = out[1] = -1;
@@ -87,7 +92,7 @@ __device__ void find_bins(const uint32_t* hh, uint32_t need, uint32_t budget, ui
     if (lane >= o) incl += y;
   }
   if (lane == 31) warp_tot[wid] = incl;
-  named_sync(kConsumers);
+  if (!cb.sync()) *abort = 1;
   if (wid == 0) {
     const uint32_t w = lane < kScanWarps ? warp_tot[lane] : 0u;
     uint32_t wi = w;
@@ -98,7 +103,7 @@ __device__ void find_bins(const uint32_t* hh, uint32_t need, uint32_t budget, ui
     }
     if (lane < kScanWarps) warp_tot[lane] = wi - w;
   }
-  named_sync(kConsumers);
+  if (!cb.sync()) *abort = 1;
   const uint32_t excl = incl - mine + warp_tot[wid];
   const uint32_t target[2] = {need, budget};
 #pragma unroll
@@ -112,10 +117,10 @@ __device__ void find_bins(const uint32_t* hh, uint32_t need, uint32_t budget, ui
       }
     }
   }
-  named_sync(kConsumers);
+  if (!cb.sync()) *abort = 1;
   bstar = out[0];
   bbud = out[1];
-  named_sync(kConsumers);
+  if (!cb.sync()) *abort = 1;
 }
 
 template <int HP>
@@ -130,6 +135,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
   __shared__ uint32_t warp_tot[kScanWarps];
   __shared__ int s_flag, s_bins[2];
   __shared__ volatile int s_abort;
+  __shared__ uint64_t cons_bar;
+  __shared__ int stage_tile[kStages];  // tile of each ring stage (-1: no more tiles)
 
   if (a.pass == 1) pdl_wait();  // rescan flags come from pass 0
   pdl_trigger();
@@ -173,17 +180,22 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kScanWarps);
     }
+    mbar_init(&cons_bar, kScanWarps);
     fence_mbar_init();
     s_abort = 0;
   }
   __syncthreads();
 
+  // Contiguous static ranges over the first 85 % of the tiles; the rest is
+  // claimed one tile at a time (global counter) by whichever CTA is free
+  // first, so that CTAs whose share of HBM bandwidth is smaller end no later.
   const int total = unit_tiles[nunits];
+  if (total == 0) return;
   const int grid = gridDim.x;
-  const int t_begin = (int)((int64_t)total * blockIdx.x / grid);
-  const int t_end = (int)((int64_t)total * (blockIdx.x + 1) / grid);
-  const int ntile = t_end - t_begin;
-  if (ntile <= 0) return;
+  const int dyn = total >= 4 * grid ? total * 3 / 20 : 0;
+  const int stat = total - dyn;
+  const int t_begin = (int)((int64_t)stat * blockIdx.x / grid);
+  const int t_end = (int)((int64_t)stat * (blockIdx.x + 1) / grid);
 
   // global tile index -> unit (last unit whose first tile is <= t)
   auto locate = [&](int t) {
@@ -199,46 +211,82 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
   const int warp = tid >> 5, lane = tid & 31;
 
   // ======================= producer warp: the bulk-copy ring ==================
+  // Lane 0 waits for free stages and arms the full barrier; a contiguous tile
+  // is one copy (lane 0), a paged tile one copy per page, issued by the lanes
+  // in parallel so that the page-table reads overlap (tiles start on a page
+  // boundary: 256 rows is a multiple of every page size).
   if (warp == kScanWarps) {
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      int j = 0;
-      for (; j < ntile; ++j) {
-        const int s = j % kStages;
+    const uint64_t pol = policy_evict_first();
+    int next_static = t_begin;
+    int claim = -1;  // lane 0: dynamic claim requested one tile ahead (-1: none)
+    int j = 0;
+    bool marker = false;
+    for (;; ++j) {
+      const int s = j % kStages;
+      int go = 1, t = -1;
+      if (lane == 0) {
         if (j >= kStages &&
             !mbar_wait_or_abort(&empty[s], (uint32_t)((j / kStages - 1) & 1), &s_abort)) {
           s_abort = 1;
-          break;
+          go = 0;
         }
-        if (s_abort) break;
-        const int t = t_begin + j;
-        const int unit = locate(t);
-        const int tile = t - unit_tiles[unit];
-        const int b = unit / a.kv.Hkv, g = unit % a.kv.Hkv;
-        const int64_t L = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
-        const int64_t r0 = (int64_t)tile * kTileRows;
-        const int64_t r1 = r0 + kTileRows < L ? r0 + kTileRows : L;
-        const uint32_t bytes = (uint32_t)(r1 - r0) * kRowBytes;
-        fence_proxy_async();
-        mbar_expect_tx(&full[s], bytes);
-        uint8_t* dst = ring + s * kTileBytes;
-        if (!a.kv.page_table) {
-          bulk_g2s(dst, a.kv.k + kv_row(a.kv, b, g, r0), bytes, &full[s], pol);
-        } else {
-          const int64_t ps = (int64_t)1 << a.kv.page_shift;
-          for (int64_t r = r0; r < r1;) {
-            const int64_t pe = ((r >> a.kv.page_shift) + 1) * ps;
-            const int64_t e = pe < r1 ? pe : r1;
-            bulk_g2s(dst + (r - r0) * kRowBytes, a.kv.k + kv_row(a.kv, b, g, r),
-                     (uint32_t)(e - r) * kRowBytes, &full[s], pol);
-            r = e;
+        if (s_abort) go = 0;
+        if (go) {
+          if (next_static < t_end) {
+            t = next_static++;
+          } else if (dyn > 0) {
+            const int c = claim >= 0 ? claim : (int)atomicAdd(a.tile_ctr + a.pass, 1u);
+            claim = -1;
+            t = c < dyn ? stat + c : -1;
           }
+          // the next tile is a dynamic one: claim it now, so that the
+          // atomic's round trip overlaps the wait for a free stage
+          if (t >= 0 && next_static >= t_end && dyn > 0)
+            claim = (int)atomicAdd(a.tile_ctr + a.pass, 1u);
+          stage_tile[s] = t;
+          if (t < 0) mbar_arrive(&full[s]);  // no more tiles: release the consumers
         }
       }
-      // copies of the last (up to kStages) issued tiles may still be landing
-      for (int jj = j - kStages > 0 ? j - kStages : 0; jj < j; ++jj)
-        (void)mbar_wait(&full[jj % kStages], (uint32_t)((jj / kStages) & 1));
+      go = __shfl_sync(0xffffffffu, go, 0);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      if (!go) break;
+      if (t < 0) {
+        marker = true;
+        break;
+      }
+      const int unit = locate(t);
+      const int tile = t - unit_tiles[unit];
+      const int b = unit / a.kv.Hkv, g = unit % a.kv.Hkv;
+      const int64_t L = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
+      const int64_t r0 = (int64_t)tile * kTileRows;
+      const int64_t r1 = r0 + kTileRows < L ? r0 + kTileRows : L;
+      const uint32_t bytes = (uint32_t)(r1 - r0) * kRowBytes;
+      uint8_t* dst = ring + s * kTileBytes;
+      if (lane == 0) {
+        fence_proxy_async();
+        mbar_expect_tx(&full[s], bytes);
+      }
+      __syncwarp();
+      if (!a.kv.page_table) {
+        if (lane == 0) bulk_g2s(dst, a.kv.k + kv_row(a.kv, b, g, r0), bytes, &full[s], pol);
+      } else {
+        const int64_t ps = (int64_t)1 << a.kv.page_shift;
+        const int nseg = (int)((r1 - r0 + ps - 1) >> a.kv.page_shift);  // <= 16
+        for (int k = lane; k < nseg; k += 32) {
+          const int64_t r = r0 + (int64_t)k * ps;
+          const int64_t e = r + ps < r1 ? r + ps : r1;
+          fence_proxy_async();
+          bulk_g2s(dst + (r - r0) * kRowBytes, a.kv.k + kv_row(a.kv, b, g, r),
+                   (uint32_t)(e - r) * kRowBytes, &full[s], pol);
+        }
+      }
     }
+    // copies of the last (up to kStages) tiles may still be landing; after the
+    // end marker, the stage it used had been seen consumed
+    if (lane == 0)
+      for (int jj = j - kStages + (marker ? 1 : 0) > 0 ? j - kStages + (marker ? 1 : 0) : 0; jj < j;
+           ++jj)
+        (void)mbar_wait(&full[jj % kStages], (uint32_t)((jj / kStages) & 1));
     return;
   }
 
@@ -256,12 +304,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
   int cur_unit = -1, unit_end = 0, cur_b = 0, cur_g = 0, head0 = 0;
   int64_t cur_L = 0;
   int rows_since_flush = 0;
-  bool dead = false;
+  int visit_tiles = 0;          // tiles of the current unit processed in this visit
+  ConsumerBar cb{&cons_bar, 0u};
 
   // flush the shared histogram of `unit` into global memory (consumers)
   auto flush_hist = [&](int unit) {
     const int b = unit / a.kv.Hkv, g = unit % a.kv.Hkv;
-    named_sync(kConsumers);
+    if (!cb.sync()) s_abort = 1;  // every warp's counts are in the shared histogram
     for (int w = tid; w < HP * kHistWords; w += kConsumers) {
       const uint32_t v = hist[w];
       if (v) {
@@ -273,7 +322,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
         hist[w] = 0;
       }
     }
-    __threadfence();
+    if (a.decide) __threadfence();  // before this CTA's unit ticket
     rows_since_flush = 0;
   };
   // pass 0: unit finished by this CTA -- flush, add its tiles to the unit
@@ -293,21 +342,20 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
   auto finish_unit = [&](int unit) {
     flush_hist(unit);
     close_runs();
-    if (lane < G) {  // publish this warp's emission count
-      if (wsum) atomicAdd(&a.emit_n[head0 + lane], wsum);
-      __threadfence();
-    }
+    if (lane < G && wsum) atomicAdd(&a.emit_n[head0 + lane], wsum);  // this warp's pairs
     wsum = 0;
-    named_sync(kConsumers);
+    if (!a.decide) return;  // the finish kernel decides from the histograms
+    if (lane < G) __threadfence();
+    if (!cb.sync()) s_abort = 1;
     if (tid == 0) {  // the ticket counts tiles: the CTA completing the count is last
       const int u0 = unit_tiles[unit], u1 = unit_tiles[unit + 1];
-      const uint32_t mine = (uint32_t)((t_end < u1 ? t_end : u1) - (t_begin > u0 ? t_begin : u0));
+      const uint32_t mine = (uint32_t)visit_tiles;
       __threadfence();
       const uint32_t n = atomicAdd(&a.unit_ticket[unit], mine);
       s_flag = (n + mine == (uint32_t)(u1 - u0));
     }
-    named_sync(kConsumers);
-    if (!s_flag) return;
+    if (!cb.sync()) s_abort = 1;
+    if (!s_flag || s_abort) return;
     __threadfence();
     const int b = unit / a.kv.Hkv, g = unit % a.kv.Hkv;
     const int64_t L = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
@@ -316,7 +364,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
     for (int hl = 0; hl < G; ++hl) {
       const int bh = b * a.Hq + g * G + hl;
       if (a.head_active && a.head_active[bh] != a.active_value) continue;
-      const int used = min(max(__ldcg(a.hint_bin + bh), 0), kHistBins - 1);
+      const int used = hint_bin_of(__ldcg(a.hint_bin + bh));
       int bin = -1, exact_bin = 0, redo = 0, next_hint = 0;
       if (need > 0 && need < P) {
         // next call's hint: the lowest bin whose suffix stays within the
@@ -324,7 +372,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
         const int64_t budget = 3 * need + 4096;
         int bbud;
         find_bins(a.hist + (int64_t)bh * kHistBins, (uint32_t)need,
-                  (uint32_t)(budget + 1 < P ? budget + 1 : P + 1), warp_tot, s_bins, bin, bbud);
+                  (uint32_t)(budget + 1 < P ? budget + 1 : P + 1), warp_tot, s_bins, bin, bbud,
+                  cb, &s_abort);
         exact_bin = bin;
         next_hint = bbud < 0 ? 0 : (bbud + 1 < bin ? bbud + 1 : bin);
         const int64_t emitted = __ldcg(a.emit_n + bh);
@@ -346,9 +395,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
     }
   };
 
-  for (int j = 0; j < ntile; ++j) {
+  for (int j = 0;; ++j) {
     const int s = j % kStages;
-    const int t = t_begin + j;
+    if (!mbar_wait_or_abort(&full[s], (uint32_t)((j / kStages) & 1), &s_abort)) {
+      s_abort = 1;
+      break;
+    }
+    const int t = stage_tile[s];  // written by the producer before it armed the stage
+    if (t < 0) break;             // no more tiles (same stage, same j, for every warp)
     if (t >= unit_end) {  // entering a new unit (all consumers at the same tile)
       const int unit = locate(t);
       if (cur_unit >= 0) {
@@ -357,6 +411,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
       }
       cur_unit = unit;
       unit_end = unit_tiles[unit + 1];
+      visit_tiles = 0;
       cur_b = unit / a.kv.Hkv;
       cur_g = unit % a.kv.Hkv;
       head0 = cur_b * a.Hq + cur_g * G;
@@ -368,7 +423,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
         on[e] = hl < G && (!a.head_active || a.head_active[bh] == a.active_value);
         hint[e] = 0;
         if (on[e])
-          hint[e] = p0 ? min(max(__ldcg(a.hint_bin + bh), 0), kHistBins - 1)
+          hint[e] = p0 ? hint_bin_of(__ldcg(a.hint_bin + bh))
                        : __ldcg(a.rescan_bin + bh);
       }
       lane_on = lane < G && (!a.head_active || a.head_active[head0 + lane] == a.active_value);
@@ -383,13 +438,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
       flush_hist(cur_unit);
     }
     rows_since_flush += kTileRows;
+    ++visit_tiles;
     const int tile = t - unit_tiles[cur_unit];
-    if (!dead && !mbar_wait_or_abort(&full[s], (uint32_t)((j / kStages) & 1), &s_abort)) {
-      dead = true;
-      s_abort = 1;
-    }
     if (j == 0) trace.mark(1);
-    if (!dead) {
+    {
       // ---- 16 keys x 8 heads on the tensor cores ----
       const uint8_t* wb = ring + s * kTileBytes + warp * 16 * kRowBytes;
       float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -480,17 +532,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
           }
         }
       }
-    } else {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);  // keep the producer moving
     }
   }
 
-  // one decision for all consumer warps (a named barrier needs all of them)
-  named_sync(kConsumers);
-  if (tid == 0) s_flag = s_abort;
-  named_sync(kConsumers);
-  if (s_flag) {
+  // every consumer warp has left the loop (bounded: a warp that stopped
+  // early makes the others time out here instead of hanging)
+  if (!cb.sync()) s_abort = 1;
+  if (s_abort) {
     if (tid == 0) atomicOr(a.status, kStatusTimeout);
     return;
   }

@@ -20,6 +20,16 @@ constexpr int kMaxGroup = 8;                    // query heads per KV head
 constexpr int kMaxUnits = 512;                  // B * Hkv limit of one call
 constexpr long long kWaitLimitNs = 1000000000;  // bounded waits: 1 s
 
+// Per-head hint word kept in the workspace between calls: bits 0-15 the bin
+// from which the key scan emits (clamped to [0, kHistBins)), bit 16 set once
+// the head's threshold bin has moved by more than the default margin (the
+// head then gets a wider margin).  Any value is safe.
+__device__ __forceinline__ int hint_bin_of(int32_t w) {
+  const int b = w & 0xffff;
+  return b < kHistBins ? b : kHistBins - 1;
+}
+__device__ __forceinline__ bool hint_wide_of(int32_t w) { return (w >> 16) & 1; }
+
 // Status word codes written by kernels into the workspace (host maps them).
 constexpr int kStatusTimeout = 1;
 
@@ -192,6 +202,58 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// ---------------------------------------------------------- tensor cores
+// D += A * B, m16n8k16, bf16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ------------------------------------------------------------- clusters
+// Full barrier over the thread-block cluster (release / acquire: shared and
+// global writes before it are visible to the cluster's threads after it).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n"
+               "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// Loads from the shared memory of CTA `cta` of this cluster (distributed
+// shared memory): p is the address of the same variable in this CTA.
+__device__ __forceinline__ float ld_dsmem(const float* p, uint32_t cta) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(cta));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_dsmem_u32(const uint32_t* p, uint32_t cta) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(cta));
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t ld_dsmem_u64(const uint64_t* p, uint32_t cta) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(cta));
+  uint64_t v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(remote) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 ld_dsmem_v4(const uint32_t* p, uint32_t cta) {  // 16-B aligned
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(cta));
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(remote)
+               : "memory");
+  return v;
+}
+
 // ------------------------------------------------------------- tracing
 // Optional per-CTA timeline: when a kernel's argument block carries a trace
 // buffer, thread 0 of every CTA appends one record with the kernel id, the
@@ -217,6 +279,7 @@ struct TraceScope {
   TraceBuf tb;
   bool on;
   uint32_t kernel;
+  uint32_t info = 0;  // kernel-specific word stored in the record's pad field
   uint64_t t[4];
   __device__ TraceScope(const TraceBuf& b, uint32_t k) : tb(b), kernel(k) {
     on = b.rec != nullptr && threadIdx.x == 0;
@@ -228,14 +291,14 @@ struct TraceScope {
   }
   __device__ ~TraceScope() {
     if (on) {
-      t[3] = globaltimer_ns();
+      if (!t[3]) t[3] = globaltimer_ns();
       const uint32_t slot = atomicAdd(tb.count, 1u);
       if (slot < tb.cap) {
         TraceRec r;
         r.kernel = kernel;
         r.block = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
         r.smid = smid_u32();
-        r.pad = 0;
+        r.pad = info;
         for (int i = 0; i < 4; ++i) r.t[i] = t[i];
         tb.rec[slot] = r;
       }
@@ -243,7 +306,8 @@ struct TraceScope {
   }
 };
 enum TraceKernel : uint32_t {
-  kTrScan = 1, kTrSelect = 2, kTrAttend = 3, kTrSelector = 4, kTrRescore = 5, kTrScan1 = 6
+  kTrScan = 1, kTrSelect = 2, kTrAttend = 3, kTrSelector = 4, kTrRescore = 5, kTrScan1 = 6,
+  kTrFinish = 7, kTrFinishPhases = 8
 };
 
 // ------------------------------------------------------ warp/block utils

@@ -32,10 +32,13 @@ struct ScanArgs {
   int n_init, n_recent;      // static window (logits to wz, not emitted)
   int K;                     // top-K budget
   int pass;                  // 0 or 1
+  int decide;                // 1: the CTA completing a unit sets b*, pass-1 flags and the next
+                             // hint; 0: histograms and pairs only (the finish kernel decides)
   const int32_t* head_active;
   int active_value;
   uint32_t* hist;            // [B][Hq][kHistBins] (zeroed), pass 0
   uint32_t* unit_ticket;     // [B][Hkv] (zeroed), pass 0
+  uint32_t* tile_ctr;        // [2] (zeroed) dynamic tile claims of pass 0 / pass 1
   int32_t* hint_bin;         // [B][Hq] persistent across calls (any value is safe)
   int32_t* rescan;           // [B][Hq] (zeroed) 1: pass 1 needed; pass 1 reads it
   int32_t* rescan_bin;       // [B][Hq] exact emission bin for pass 1
@@ -72,6 +75,40 @@ struct ResolveArgs {
   TraceBuf trace;
 };
 cudaError_t launch_resolve(const ResolveArgs& a, cudaStream_t st);
+
+// Finish (decode step after a scan with decide = 0): one cluster of 8 CTAs
+// per (sequence, query head) finds the threshold bin b* from the head's
+// histogram, checks the scan's emission against it and re-emits the head's
+// pairs itself when the hint failed (same tensor-core arithmetic as the
+// scan, so the pairs agree with the histogram), stores the next call's
+// hint, selects the exact top-K from the emitted pairs (pairs above b*
+// outright, the rest of the K by a cluster-wide radix over b*'s candidates)
+// and attends over the window and the selected rows with the gamma merge.
+struct FinishArgs {
+  const uint16_t* q;         // bf16 [B][Hq][128] (re-emission only)
+  KvView kv;
+  const int32_t* lens;
+  int64_t len_host;
+  int B, Hq;
+  float scale;
+  int K, n_init, n_recent;
+  const uint32_t* hist;      // [B][Hq][kHistBins] pool histograms from the scan
+  int32_t* hint_bin;         // [B][Hq] the scan's emission bin; the next call's is stored
+  uint2* dense;              // [B][Hq][dense_stride] emitted pairs
+  int32_t* dense_n;
+  int64_t dense_stride;
+  uint64_t* spill;           // [B][Hq][dense_stride] candidates past shared memory
+  int32_t* sel_pos;          // [B][Hq][K] above-b* pairs past a CTA's shared memory
+  float* sel_z;              // [B][Hq][K]
+  const float* wz;           // window logits [B][Hq][wz_stride]
+  int wz_stride;
+  float* out;                // [B][Hq][128]
+  float* lse_out;            // [B][Hq] or nullptr
+  int32_t* topk_idx;         // [B][Hq][K] or nullptr
+  float* topk_score;         // [B][Hq][K] or nullptr
+  TraceBuf trace;
+};
+cudaError_t launch_finish(const FinishArgs& a, cudaStream_t st);
 
 struct AttendArgs {
   KvView kv;
