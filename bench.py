@@ -197,7 +197,7 @@ def run_ours(args, ws, rank, local):
         torch.cuda.empty_cache()
     B, Hq, d, K = wl.B, wl.Hq, wl.d, wl.K
     nb = tsa.decode_workspace_size(B, Hq, wl.Hkv, d, kv.l_cap, K, wl.n_init, wl.n_recent)
-    work = torch.empty(nb, dtype=torch.uint8, device=dev)
+    work = torch.zeros(nb, dtype=torch.uint8, device=dev)  # zeroed once, then reused
     out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
     lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
     lens_all = torch.tensor([wl.lens(t) for t in range(wl.steps)], dtype=torch.int32, device=dev)

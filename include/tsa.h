@@ -146,8 +146,13 @@ TSA_API int tsa_set_trace(void* buf, size_t bytes);
  *             with -1 when fewer than K positions exist
  * topk_score: fp32 [B][Hq][K] or NULL: z of topk_idx (padding: -inf)
  * workspace:  device scratch of at least tsa_decode_workspace_size() bytes,
- *             256-byte aligned; its contents need no initialisation and are
- *             overwritten by every call
+ *             256-byte aligned, zero-filled (e.g. cudaMemsetAsync 0) before
+ *             its first use.  Every call leaves it ready for the next call
+ *             with the same B, Hq, Hkv, l_cap, K, n_init and n_recent, so
+ *             it is reused as is; zero it again before other sizes and after
+ *             a call that failed.  It also keeps per-head state
+ *             that speeds up the next call (never its result): use one
+ *             workspace per layer.
  * Returns TSA_OK or an error; see the conventions above. */
 TSA_API size_t tsa_decode_workspace_size(int B, int Hq, int Hkv, int d, int64_t l_cap,
                                  int K, int n_init, int n_recent);

@@ -41,7 +41,7 @@ def _run_both(wl, steps, dev="cuda"):
     B, Hq, d, K = wl.B, wl.Hq, wl.d, wl.K
     n = tsa.decode_workspace_size(B, Hq, wl.Hkv, d, wl.lcap, K, wl.n_init, wl.n_recent)
     assert n <= tsa.noalloc_scratch_bytes()
-    work = torch.empty(n, dtype=torch.uint8, device=dev)
+    work = torch.zeros(n, dtype=torch.uint8, device=dev)
 
     def bufs():
         return (torch.empty((B, Hq, d), dtype=torch.float32, device=dev),

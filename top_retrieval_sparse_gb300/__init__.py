@@ -195,6 +195,8 @@ def sparse_attn_decode(q: torch.Tensor, kv: KV, lens: torch.Tensor, K: int, n_in
     """One decode step over every sequence and query head (see include/tsa.h).
 
     q: bf16 [B][Hq][d] on the device; lens: int32 [B] on the device.
+    workspace: uint8, zero-filled before its first use and then reused as
+    is (each call leaves it ready for the next); None allocates a fresh one.
     Returns (out, lse_out, topk_idx, topk_score) (the optional ones may be None).
     """
     _want(q, torch.bfloat16, "q")
@@ -206,7 +208,7 @@ def sparse_attn_decode(q: torch.Tensor, kv: KV, lens: torch.Tensor, K: int, n_in
         out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
     if workspace is None:
         nb = decode_workspace_size(B, Hq, kv.Hkv, d, kv.l_cap, K, n_init, n_recent)
-        workspace = torch.empty(max(nb, 256), dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(max(nb, 256), dtype=torch.uint8, device=q.device)
     _check(lib().sparse_attn_decode(
         _p(q), C.byref(kv.struct), _p(lens), B, Hq, kv.Hkv, d, K, n_init, n_recent,
         float(scale), _p(out), _p(lse_out), _p(topk_idx), _p(topk_score), _p(workspace),

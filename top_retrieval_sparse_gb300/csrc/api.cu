@@ -284,6 +284,10 @@ namespace tsa {
 // Sets this thread's error message for an entry point defined in another
 // translation unit of the library; returns `code`.
 int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
+// Bytes at the start of a decode workspace that must be zero before a call.
+size_t decode_zero_bytes(int B, int Hq, int Hkv, int64_t l_cap, int K, int n_init, int n_recent) {
+  return decode_layout(B, Hq, Hkv, l_cap, K, n_init, n_recent).zero_end;
+}
 }  // namespace tsa
 
 extern "C" {
@@ -344,11 +348,14 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
   if (ws_bytes < Lw.total)
     return fail(TSA_ERR_WORKSPACE, "workspace %zu bytes < required %zu", ws_bytes, Lw.total);
 
+  // The workspace counters start at zero: the caller zeroes a new workspace
+  // once and every call's finish kernel clears them again for the next call,
+  // so no memset sits between consecutive calls and the key scan can be
+  // launched as a programmatic dependent of the previous call's kernels.
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  cudaError_t e = cudaMemsetAsync(ws + Lw.zero_begin, 0, Lw.zero_end - Lw.zero_begin, st);
-  if (e != cudaSuccess) return cuda_fail(e, "memset");
-  if ((e = stage_mark(0, st)) != cudaSuccess) return cuda_fail(e, "event record");
+  cudaError_t e = stage_mark(0, st);
+  if (e != cudaSuccess) return cuda_fail(e, "event record");
 
   const KvView view = make_view(kv, Hkv);
   SelWs w{};
@@ -373,7 +380,7 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
     ScanArgs s = scan_args(static_cast<const uint16_t*>(q), view, lens, 0, B, Hq, K, n_init,
                            n_recent, scale, nullptr, 0, w);
     s.decide = 0;  // the finish kernel decides
-    if ((e = counted(launch_scan(s, scan_grid(B, view, kv->l_cap), st, false))) != cudaSuccess)
+    if ((e = counted(launch_scan(s, scan_grid(B, view, kv->l_cap), st, true))) != cudaSuccess)
       return cuda_fail(e, "scan launch");
   }
   if ((e = stage_mark(1, st)) != cudaSuccess) return cuda_fail(e, "event record");
@@ -392,6 +399,9 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
     f.n_recent = n_recent;
     f.hist = w.hist;
     f.hint_bin = w.hint_bin;
+    f.emit_n = w.emit_n;
+    f.tile_ctr = w.tile_ctr;
+    f.status = w.status;
     f.dense = w.dense;
     f.dense_n = w.dense_n;
     f.dense_stride = w.dense_stride;

@@ -166,7 +166,9 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
   const int b = bh / a.Hq, h = bh % a.Hq;
   const int G = a.Hq / a.kv.Hkv;
   const int g = h / G;
-  pdl_wait();  // pairs, bins and window logits come from the scan
+  pdl_wait();     // pairs, bins and window logits come from the scan
+  pdl_trigger();  // the next call's key scan may start streaming keys (it
+                  // writes nothing until this kernel has completed)
   trace.mark(1);
 
   const int64_t L = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
@@ -322,6 +324,21 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
   }
   __syncthreads();
   const int nabove = sh.aoff[NC], ncand = sh.coff[NC];
+  // Every CTA of the cluster has read the head's histogram, list size and
+  // hint: clear the counters for the next call (the workspace contract).
+  if (rank == 0) {
+    uint4* hz = reinterpret_cast<uint4*>(a.hist + (int64_t)bh * kHistBins);
+    for (int q = tid; q < kHistBins / 4; q += kFinThreads) hz[q] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid == 0) {
+      a.dense_n[bh] = 0;
+      a.emit_n[bh] = 0;
+      if (bh == 0) {
+        a.tile_ctr[0] = 0;
+        a.tile_ctr[1] = 0;
+        *a.status = 0;
+      }
+    }
+  }
   // candidate j of the cluster (cluster order): CTA c's list, local index i
   auto cand_remote = [&](int jc) -> uint64_t {
     int c = 0;

@@ -20,6 +20,7 @@
 
 namespace tsa {
 int report_error(int code, const char* msg);
+size_t decode_zero_bytes(int B, int Hq, int Hkv, int64_t l_cap, int K, int n_init, int n_recent);
 }  // namespace tsa
 
 namespace {
@@ -77,8 +78,16 @@ int sparse_attn_decode_noalloc(const void* q, const tsa_kv* kv, const int32_t* l
   void* scratch = nullptr;
   const int rc = scratch_address(&scratch);
   if (rc != TSA_OK) return rc;
-  // sparse_attn_decode clears, on the stream, every scratch counter that must
-  // start at zero; the rest of the array needs no initialisation.
+  // Calls of any size share the array, so the counters that must start at
+  // zero are cleared on the stream every time; the rest needs no
+  // initialisation.
+  if (B > 0 && Hq > 0 && Hkv > 0 && kv->l_cap > 0 && K >= 0 && n_init >= 0 && n_recent >= 0) {
+    const cudaError_t e =
+        cudaMemsetAsync(scratch, 0, tsa::decode_zero_bytes(B, Hq, Hkv, kv->l_cap, K, n_init,
+                                                           n_recent),
+                        static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return tsa::report_error(TSA_ERR_CUDA, cudaGetErrorString(e));
+  }
   return sparse_attn_decode(q, kv, lens, B, Hq, Hkv, d, K, n_init, n_recent, scale, out,
                             lse_out, topk_idx, topk_score, scratch, kScratchBytes, stream);
 }

@@ -291,6 +291,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
   }
 
   // ============================ consumer warps ================================
+  // Launched as a programmatic dependent, the scan streams keys while the
+  // previous kernel finishes; its consumers read hints and write counters,
+  // pairs and logits only after that kernel has completed.
+  pdl_wait();
   const int gr = lane >> 2;  // A rows gr, gr+8 / B column (query head) gr
   const int tq = lane & 3;   // k-slot group / C columns 2tq, 2tq+1
 

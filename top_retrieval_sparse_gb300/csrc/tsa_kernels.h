@@ -92,8 +92,11 @@ struct FinishArgs {
   int B, Hq;
   float scale;
   int K, n_init, n_recent;
-  const uint32_t* hist;      // [B][Hq][kHistBins] pool histograms from the scan
+  uint32_t* hist;            // [B][Hq][kHistBins] pool histograms from the scan (cleared)
   int32_t* hint_bin;         // [B][Hq] the scan's emission bin; the next call's is stored
+  int32_t* emit_n;           // [B][Hq] (cleared for the next call)
+  uint32_t* tile_ctr;        // [2] the scan's tile claims (cleared)
+  int* status;               // (cleared)
   uint2* dense;              // [B][Hq][dense_stride] emitted pairs
   int32_t* dense_n;
   int64_t dense_stride;
