@@ -289,7 +289,7 @@ def run_ours(args, ws, rank, local):
                       "topk+attend+merge": round(statistics.mean(sel_ms) + statistics.mean(att_ms), 5),
                       "note": "second timed region with per-stage events"},
         "path_algorithmic_gbs": round(path_gbs, 1),
-        "roofline": {"kernel": "scan_kernel (GQA key scan + pass-1 histogram)",
+        "roofline": {"kernel": "scan_kernel (GQA key scan, histograms, pair emission)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "frac_of_8tbs": round(achieved / 8000.0, 4),
@@ -356,64 +356,90 @@ def run_trace(args, step, tsa, torch, dev, nsteps=3):
     return out
 
 
+def _cudart():
+    """The CUDA runtime the library is linked against (already loaded)."""
+    import ctypes as C
+    path = None
+    with open("/proc/self/maps") as f:
+        for line in f:
+            if "libcudart.so" in line:
+                path = line.split()[-1]
+                break
+    rt = C.CDLL(path or "libcudart.so")
+    P, sz, i32 = C.c_void_p, C.c_size_t, C.c_int
+    rt.cudaMemcpyAsync.argtypes = [P, P, sz, i32, P]
+    rt.cudaMemcpy2DAsync.argtypes = [P, sz, P, sz, sz, sz, i32, P]
+    rt.cudaStreamSynchronize.argtypes = [P]
+    return rt
+
+
 def run_e2e(args, wl, kv, work, tsa, torch, dev):
-    """End to end through the public API with host buffers.  Per step: one
-    pinned host -> device copy of the step's packed inputs (query, appended K
-    and V token rows, lengths), the append of the token rows into the cache,
-    the decode call, and one device -> host copy of the packed result (output
-    and lse), then a stream synchronisation.  Wall-clock per step."""
+    """End to end through the C ABI with host buffers.  Per step, on one
+    stream: a host -> device copy of the step's query and lengths (pinned,
+    one copy), the append of the step's K and V token rows from pinned host
+    memory straight into their cache rows (one strided copy per sequence and
+    tensor), the sparse_attn_decode call, a device -> host copy of the output
+    and lse (one copy), and a stream synchronisation.  Wall-clock per step."""
+    import ctypes as C
     import numpy as np
+    rt = _cudart()
+    H2D, D2H = 1, 2
     B, Hq, d, Hkv = wl.B, wl.Hq, wl.d, wl.Hkv
     paged = wl.page_table is not None
-    qb, tb, lb = B * Hq * d * 2, B * Hkv * d * 2, B * 4
-    nbytes = qb + 2 * tb + lb
-    host = torch.empty((wl.steps, nbytes), dtype=torch.uint8).pin_memory()
+    qb, lb, rowb = B * Hq * d * 2, B * 4, d * 2
+    host_ql = torch.empty((wl.steps, qb + lb), dtype=torch.uint8).pin_memory()
+    host_k = torch.empty((wl.steps, B, Hkv, d), dtype=torch.bfloat16).pin_memory()
+    host_v = torch.empty_like(host_k).pin_memory()
     pt = wl.page_table.cpu() if paged else None
-    page_idx = torch.empty((wl.steps, B), dtype=torch.int64)
-    row_idx = torch.empty((wl.steps, B), dtype=torch.int64)
+    kc, vc = (wl.k_pages, wl.v_pages) if paged else (wl.k, wl.v)
+    dst_rows = []  # per step: [(k address, v address, pitch)] per sequence
     for t in range(wl.steps):
-        lens_t = np.asarray(wl.lens(t), dtype=np.int32)
-        tok_k = torch.empty((B, Hkv, d), dtype=torch.bfloat16)
-        tok_v = torch.empty_like(tok_k)
+        host_ql[t, :qb] = wl.q_all[t].cpu().contiguous().view(torch.uint8).reshape(-1)
+        host_ql[t, qb:] = torch.from_numpy(np.asarray(wl.lens(t), dtype=np.int32).view(np.uint8))
+        rows = []
         for b in range(B):  # the token appended at step t sits at row L0 + t
             pos = wl.L0[b] + t
             if paged:
-                page = int(pt[b, pos // wl.page_size])
-                page_idx[t, b], row_idx[t, b] = page, pos % wl.page_size
-                tok_k[b] = wl.k_pages[page, :, pos % wl.page_size].cpu()
-                tok_v[b] = wl.v_pages[page, :, pos % wl.page_size].cpu()
+                page, r = int(pt[b, pos // wl.page_size]), pos % wl.page_size
+                host_k[t, b] = wl.k_pages[page, :, r].cpu()
+                host_v[t, b] = wl.v_pages[page, :, r].cpu()
+                off = ((page * Hkv) * wl.page_size + r) * rowb
+                pitch = wl.page_size * rowb
             else:
-                page_idx[t, b], row_idx[t, b] = b, pos
-                tok_k[b] = wl.k[b, :, pos].cpu()
-                tok_v[b] = wl.v[b, :, pos].cpu()
-        row = host[t]
-        row[:qb] = wl.q_all[t].cpu().contiguous().view(torch.uint8).reshape(-1)
-        row[qb:qb + tb] = tok_k.view(torch.uint8).reshape(-1)
-        row[qb + tb:qb + 2 * tb] = tok_v.view(torch.uint8).reshape(-1)
-        row[qb + 2 * tb:] = torch.from_numpy(lens_t.view(np.uint8))
-    page_idx, row_idx = page_idx.to(dev), row_idx.to(dev)  # bookkeeping, resident
-    stage = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    q_dev = stage[:qb].view(torch.bfloat16).view(B, Hq, d)
-    tok_k_dev = stage[qb:qb + tb].view(torch.bfloat16).view(B, Hkv, d)
-    tok_v_dev = stage[qb + tb:qb + 2 * tb].view(torch.bfloat16).view(B, Hkv, d)
-    lens_dev = stage[qb + 2 * tb:].view(torch.int32)
+                host_k[t, b] = wl.k[b, :, pos].cpu()
+                host_v[t, b] = wl.v[b, :, pos].cpu()
+                off = ((b * Hkv) * kv.l_cap + pos) * rowb
+                pitch = kv.l_cap * rowb
+            rows.append((kc.data_ptr() + off, vc.data_ptr() + off, pitch))
+        dst_rows.append(rows)
+    stage = torch.empty(qb + lb, dtype=torch.uint8, device=dev)
     res = torch.empty(B * Hq * (d + 1), dtype=torch.float32, device=dev)
-    out = res[:B * Hq * d].view(B, Hq, d)
-    lse = res[B * Hq * d:].view(B, Hq)
     res_host = torch.empty_like(res, device="cpu").pin_memory()
-    kc, vc = (wl.k_pages, wl.v_pages) if paged else (wl.k, wl.v)
     stream = torch.cuda.current_stream()
+    sp = C.c_void_p(stream.cuda_stream)
+    lib = tsa.lib()
+    # the C ABI call's arguments, fixed for the run
+    call = (C.c_void_p(stage.data_ptr()), C.byref(kv.struct), C.c_void_p(stage.data_ptr() + qb),
+            B, Hq, Hkv, d, wl.K, wl.n_init, wl.n_recent, C.c_float(wl.scale),
+            C.c_void_p(res.data_ptr()), C.c_void_p(res.data_ptr() + B * Hq * d * 4), None, None,
+            C.c_void_p(work.data_ptr()), C.c_size_t(work.numel()), sp)
+    hk, hv, hq = host_k.data_ptr(), host_v.data_ptr(), host_ql.data_ptr()
+    tokb = Hkv * rowb
 
     def one(i):
         t = i % wl.steps
-        stage.copy_(host[t], non_blocking=True)
-        # append the step's token rows: cache[page, :, row] = token (one scatter each)
-        kc[page_idx[t], :, row_idx[t]] = tok_k_dev
-        vc[page_idx[t], :, row_idx[t]] = tok_v_dev
-        tsa.sparse_attn_decode(q_dev, kv, lens_dev, wl.K, wl.n_init, wl.n_recent, wl.scale,
-                               out=out, lse_out=lse, workspace=work, stream=stream)
-        res_host.copy_(res, non_blocking=True)
-        stream.synchronize()
+        err = rt.cudaMemcpyAsync(stage.data_ptr(), hq + t * (qb + lb), qb + lb, H2D, sp)
+        for b, (kd, vd, pitch) in enumerate(dst_rows[t]):
+            src = (t * B + b) * tokb
+            err |= rt.cudaMemcpy2DAsync(kd, pitch, hk + src, rowb, rowb, Hkv, H2D, sp)
+            err |= rt.cudaMemcpy2DAsync(vd, pitch, hv + src, rowb, rowb, Hkv, H2D, sp)
+        rc = lib.sparse_attn_decode(*call)
+        if rc:
+            raise tsa.TsaError(rc, lib.tsa_last_error().decode())
+        err |= rt.cudaMemcpyAsync(res_host.data_ptr(), res.data_ptr(), res.numel() * 4, D2H, sp)
+        err |= rt.cudaStreamSynchronize(sp)
+        if err:
+            raise RuntimeError(f"CUDA copy or synchronise failed ({err})")
 
     for i in range(args.warmup):
         one(i)
@@ -422,7 +448,8 @@ def run_e2e(args, wl, kv, work, tsa, torch, dev):
     for i in range(n):
         one(args.warmup + i)
     dt = time.perf_counter() - t0
-    return {"value": round(1e6 * dt / n, 3), "unit": UNIT, "h2d_bytes_per_step": nbytes,
+    return {"value": round(1e6 * dt / n, 3), "unit": UNIT,
+            "h2d_bytes_per_step": qb + lb + 2 * B * Hkv * rowb,
             "d2h_bytes_per_step": res_host.numel() * 4}
 
 
