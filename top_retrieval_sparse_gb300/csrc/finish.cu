@@ -166,6 +166,16 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
   const int b = bh / a.Hq, h = bh % a.Hq;
   const int G = a.Hq / a.kv.Hkv;
   const int g = h / G;
+  {  // the V rows of this CTA's share of the window do not depend on the scan:
+     // start bringing them into L2 while it finishes
+    const int64_t L = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
+    const int64_t nw = window_count(L, a.n_init, a.n_recent);
+    for (int64_t j = nw * rank / NC + tid; j < nw * (rank + 1) / NC; j += kFinThreads) {
+      const uint16_t* vr = a.kv.v + kv_row(a.kv, b, g, window_pos(j, L, a.n_init, a.n_recent));
+      prefetch_l2(vr);
+      prefetch_l2(vr + kD / 2);
+    }
+  }
   pdl_wait();     // pairs, bins and window logits come from the scan
   pdl_trigger();  // the next call's key scan may start streaming keys (it
                   // writes nothing until this kernel has completed)
@@ -301,6 +311,18 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
   }
   phases.mark(2);
   cluster_sync_all();  // every CTA's lists and counts are complete
+  {  // this CTA's above-b* rows are selected: start bringing their V rows into
+     // L2 while the cluster settles the threshold (after the barrier: the
+     // list entries of other threads are complete)
+    const uint16_t* vb = a.kv.page_table ? a.kv.v : a.kv.v + kv_row(a.kv, b, g, 0);
+    for (int li = tid; li < nmy && li < kSelCap; li += kFinThreads) {
+      const int64_t pk = sh.sel[li].x;
+      if (pk >= L) continue;
+      const uint16_t* vr = a.kv.page_table ? vb + kv_row(a.kv, b, g, pk) : vb + pk * kD;
+      prefetch_l2(vr);
+      prefetch_l2(vr + kD / 2);
+    }
+  }
   if (wid == 0) {
     int ca = 0, cc = 0;
     if (lane < NC) {
@@ -428,13 +450,15 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
   trace.mark(2);
 
   // ---- 3. softmax.V over this CTA's rows ----
-  // rows: 1/8 of the window, this CTA's above-b* pairs, and the cluster's
-  // candidates j = rank + 8k that are selected
-  const int64_t wr0 = nw * rank / NC, wr1 = nw * (rank + 1) / NC;
-  const int nwr = (int)(wr1 - wr0);
-  const int ncmine = cmode != 0 && ncand > rank ? (ncand - rank + NC - 1) / NC : 0;
-  const int R = nwr + nmy + ncmine;
-  const int w0 = (int)((int64_t)R * wid / kFinWarps), w1 = (int)((int64_t)R * (wid + 1) / kFinWarps);
+  // The cluster's rows in one index space -- the window, then the above-b*
+  // pairs in cluster order (CTA c's i-th pair at nw + aoff[c] + i), then the
+  // candidates (absent when not selected) -- split evenly over the CTAs and
+  // their warps; a row held by another CTA is read through distributed
+  // shared memory.
+  const int Rtot = (int)nw + nabove + (cmode != 0 ? ncand : 0);
+  const int c0r = (int)((int64_t)Rtot * rank / NC), c1r = (int)((int64_t)Rtot * (rank + 1) / NC);
+  const int w0 = c0r + (int)((int64_t)(c1r - c0r) * wid / kFinWarps);
+  const int w1 = c0r + (int)((int64_t)(c1r - c0r) * (wid + 1) / kFinWarps);
   const uint16_t* vbase = a.kv.page_table ? a.kv.v : a.kv.v + kv_row(a.kv, b, g, 0);
   const float* wzrow = a.wz + (int64_t)bh * a.wz_stride;
   // 32 rows per warp at a time: lane l holds row base + l's position and
@@ -452,24 +476,30 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
     bool lv = false;
     const int j = base + lane;
     if (j < w1) {
-      if (j < nwr) {  // window row: its logit is loaded after the V loads issue
-        pos = (int)window_pos(wr0 + j, L, a.n_init, a.n_recent);
+      if (j < nw) {  // window row: its logit is loaded after the V loads issue
+        pos = (int)window_pos(j, L, a.n_init, a.n_recent);
         lv = true;
-      } else if (j < nwr + nmy) {
-        const int li = j - nwr;
+      } else if (j < nw + nabove) {
+        const int k = j - (int)nw;
+        int c = 0;
+#pragma unroll
+        for (int q = 1; q < NC; ++q) c += k >= sh.aoff[q] ? 1 : 0;
+        const int li = k - sh.aoff[c];
         if (li < kSelCap) {
-          const uint2 pr = sh.sel[li];
-          pos = (int)pr.x;
-          z = __uint_as_float(pr.y);
+          const uint64_t pr = c == rank ? *reinterpret_cast<const uint64_t*>(&sh.sel[li])
+                                        : ld_dsmem_u64(reinterpret_cast<const uint64_t*>(&sh.sel[li]),
+                                                       (uint32_t)c);
+          pos = (int)(uint32_t)pr;
+          z = __uint_as_float((uint32_t)(pr >> 32));
         } else {
-          const uint64_t v = __ldcg(spill + s0 + (li - kSelCap));
+          const uint64_t v = __ldcg(spill + n * c / NC + (li - kSelCap));
           pos = (int)rank_pos(v);
           z = key2f((uint32_t)(v >> 32));
         }
         set = 1;
         lv = true;
       } else {
-        const uint64_t v = cand_at(rank + NC * (j - nwr - nmy));
+        const uint64_t v = cand_at(j - (int)nw - nabove);
         if (cand_selected(v)) {
           pos = (int)rank_pos(v);
           z = key2f((uint32_t)(v >> 32));
@@ -490,7 +520,7 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
       vv[k] = ((live >> r) & 1u) ? __ldg(reinterpret_cast<const uint4*>(vr + col))
                                  : make_uint4(0u, 0u, 0u, 0u);
     }
-    if (lv && j < nwr) z = __ldcg(wzrow + wr0 + j);
+    if (lv && j < nw) z = __ldcg(wzrow + j);
     z = lv ? z * kFinLog2e : -INFINITY;
     // chunk maxima per set, rescale, then each lane weights its own row
 #pragma unroll

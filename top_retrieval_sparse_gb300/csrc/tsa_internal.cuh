@@ -213,6 +213,11 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Hint that the line holding p will be read soon (fetched into L2).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ------------------------------------------------------------- clusters
 // Full barrier over the thread-block cluster (release / acquire: shared and
 // global writes before it are visible to the cluster's threads after it).
