@@ -186,6 +186,20 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
   const int64_t P = L - nw;
   const int need = (int64_t)a.K < P ? a.K : (int)P;
   uint64_t* spill = a.spill + (int64_t)bh * a.dense_stride;
+  const uint2* lrow = a.dense + (int64_t)bh * a.dense_stride;
+
+  // The list size, the hint word and the histogram are read together, and
+  // the first batch of this CTA's slice of the list is in flight while the
+  // threshold bin is found (it is discarded if the list is re-emitted).
+  int64_t n = need > 0 ? __ldcg(a.dense_n + bh) : 0;
+  if (n > a.dense_stride) n = a.dense_stride;
+  int64_t s0 = n * rank / NC, s1 = n * (rank + 1) / NC;
+  uint2 pre[kFinU];
+#pragma unroll
+  for (int u = 0; u < kFinU; ++u) {
+    const int64_t jj = s0 + u * kFinThreads + tid;
+    pre[u] = jj < s1 ? __ldcg(lrow + jj) : make_uint2(0xffffffffu, 0u);
+  }
 
   // ---- 0. threshold bin b*, the emission check, the next hint ----
   // Every CTA of the cluster reads the head's histogram and decides alike.
@@ -239,7 +253,7 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
     }
   }
   phases.mark(1);
-  trace.info = (uint32_t)min((int64_t)__ldcg(a.dense_n + bh), (int64_t)0x7fffffff);
+  trace.info = (uint32_t)min(n, (int64_t)0x7fffffff);
   phases.info = ((uint32_t)redo << 31) | ((uint32_t)(bstar & 0x7fff) << 16) |
                 (uint32_t)(need > 0 ? hint_bin_of(__ldcg(a.hint_bin + bh)) : 0);
   // ---- re-emission when the scan's hint missed (rare: first call, shifts) ----
@@ -260,19 +274,20 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
   // After one cluster barrier every CTA copies all the cluster's candidates
   // (a few thousand at most in practice) through distributed shared memory.
   int nmy = 0, nmc = 0;
-  int64_t n = 0, s0 = 0, s1 = 0;
   if (need > 0) {
-    n = __ldcg(a.dense_n + bh);
-    if (n > a.dense_stride) n = a.dense_stride;
-    s0 = n * rank / NC;
-    s1 = n * (rank + 1) / NC;
-    const uint2* row = a.dense + (int64_t)bh * a.dense_stride;
+    if (redo) {  // the list was re-emitted: new size, new slice
+      n = __ldcg(a.dense_n + bh);
+      if (n > a.dense_stride) n = a.dense_stride;
+      s0 = n * rank / NC;
+      s1 = n * (rank + 1) / NC;
+    }
     for (int64_t jb = s0; jb < s1; jb += kFinThreads * kFinU) {
       uint2 pv[kFinU];
 #pragma unroll
       for (int u = 0; u < kFinU; ++u) {
         const int64_t jj = jb + u * kFinThreads + tid;
-        pv[u] = jj < s1 ? __ldcg(row + jj) : make_uint2(0xffffffffu, 0u);
+        pv[u] = jb == s0 && !redo ? pre[u]
+                                  : (jj < s1 ? __ldcg(lrow + jj) : make_uint2(0xffffffffu, 0u));
       }
       uint64_t v[kFinU];
       uint32_t selm = 0u, cndm = 0u;

@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
   int hint[2] = {0, 0};         // emission bins of heads 2tq, 2tq+1
   bool lane_on = false;         // lane h < G: head h takes part (run owner)
   int wsum = 0;                 // lane h < G: pairs this warp emitted for head h, this unit
-  int64_t run_ptr = 0;          // lane h < G: next free slot of this warp's run for head h
+  int run_ptr = 0;              // lane h < G: next free slot of this warp's run for head h
   int run_left = 0;             //            slots left in that run
   int cur_unit = -1, unit_end = 0, cur_b = 0, cur_g = 0, head0 = 0;
   int64_t cur_L = 0;
@@ -336,9 +336,9 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
   // sentinels (both passes)
   auto close_runs = [&]() {
     if (lane < G && run_left > 0) {
-      uint2* drow = a.dense + (int64_t)(head0 + lane) * a.dense_stride;
+      uint2* row = a.dense + (int64_t)(head0 + lane) * a.dense_stride;
       for (int k = 0; k < run_left; ++k)
-        if (run_ptr + k < a.dense_stride) drow[run_ptr + k] = make_uint2(0xffffffffu, 0u);
+        if ((int64_t)run_ptr + k < a.dense_stride) row[run_ptr + k] = make_uint2(0xffffffffu, 0u);
     }
     run_ptr = 0;
     run_left = 0;
@@ -492,47 +492,47 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
       unsigned m[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) m[e] = __ballot_sync(0xffffffffu, (emit >> e) & 1u);
-      int64_t p1 = 0, p2 = 0;
-      int take = 0;
-      if (lane_on) {  // lane = head in group
-        const unsigned M = 0x11111111u << (lane >> 1);
-        const unsigned ma = (lane & 1) ? m[1] : m[0], mb = (lane & 1) ? m[3] : m[2];
-        const int cnt = __popc(ma & M) + __popc(mb & M);
-        if (cnt) {
-          take = cnt < run_left ? cnt : run_left;
-          p1 = run_ptr;
-          const int over = cnt - take;
-          if (over > 0) {
-            const int size = (over + 7) & ~7;
-            p2 = atomicAdd(&a.dense_n[head0 + lane], size);
-            run_ptr = p2 + over;
-            run_left = size - over;
-          } else {
-            run_ptr += cnt;
-            run_left -= cnt;
-          }
-          wsum += cnt;
-        }
-      }
       if (m[0] | m[1] | m[2] | m[3]) {
+        int p1 = 0, p2 = 0, take = 0;  // slots fit in 32 bits (lists are < 2^31)
+        if (lane_on) {  // lane = head in group
+          const unsigned M = 0x11111111u << (lane >> 1);
+          const unsigned ma = (lane & 1) ? m[1] : m[0], mb = (lane & 1) ? m[3] : m[2];
+          const int cnt = __popc(ma & M) + __popc(mb & M);
+          if (cnt) {
+            take = cnt < run_left ? cnt : run_left;
+            p1 = run_ptr;
+            const int over = cnt - take;
+            if (over > 0) {
+              const int size = (over + 7) & ~7;
+              p2 = atomicAdd(&a.dense_n[head0 + lane], size);
+              run_ptr = p2 + over;
+              run_left = size - over;
+            } else {
+              run_ptr += cnt;
+              run_left -= cnt;
+            }
+            wsum += cnt;
+          }
+        }
         const unsigned M = 0x11111111u << tq;
         const unsigned lt = (1u << lane) - 1u;
 #pragma unroll
         for (int par = 0; par < 2; ++par) {
+          if (!(m[par] | m[par + 2])) continue;  // warp-uniform: no pair of this parity
           const int src = 2 * tq + par;  // lane owning head 2tq+par's run
-          const int64_t q1 = __shfl_sync(0xffffffffu, p1, src);
-          const int64_t q2 = __shfl_sync(0xffffffffu, p2, src);
+          const int q1 = __shfl_sync(0xffffffffu, p1, src);
+          const int q2 = __shfl_sync(0xffffffffu, p2, src);
           const int qt = __shfl_sync(0xffffffffu, take, src);
+          const int below = __popc(m[par] & M);
+          uint2* drow = a.dense + (int64_t)(head0 + src) * a.dense_stride;
 #pragma unroll
           for (int hi = 0; hi < 2; ++hi) {
             const int e = par + 2 * hi;
             if (!((emit >> e) & 1u)) continue;
-            const int r = hi == 0 ? __popc(m[par] & M & lt)
-                                  : __popc(m[par] & M) + __popc(m[par + 2] & M & lt);
-            const int64_t slot = r < qt ? q1 + r : q2 + (r - qt);
+            const int r = hi == 0 ? __popc(m[par] & M & lt) : below + __popc(m[par + 2] & M & lt);
+            const int slot = r < qt ? q1 + r : q2 + (r - qt);
             if (slot < a.dense_stride)
-              a.dense[(int64_t)(head0 + src) * a.dense_stride + slot] =
-                  make_uint2((uint32_t)(rowA + 8 * hi), __float_as_uint(zv[e]));
+              drow[slot] = make_uint2((uint32_t)(rowA + 8 * hi), __float_as_uint(zv[e]));
           }
         }
       }
