@@ -51,8 +51,8 @@ struct FinShared {
   uint32_t hist[kHistBins];       // radix round histogram
   float wo[kFinWarps][2][kD];     // warp partials: [set][d], set 0 window, 1 selected
   float wm[kFinWarps][2], wl[kFinWarps][2];
-  float po[2][kD];                // CTA partial (read by rank 0)
-  float pm[2], pl[2];
+  float mo[kFinMaxCluster][2][kD];  // rank 0: the CTA partials, pushed by each CTA
+  float mm[kFinMaxCluster][2], ml[kFinMaxCluster][2];
   uint32_t warp_tot[32];
   int cnt[2];                     // read by the cluster: above-b* pairs, candidates
   int aoff[kFinMaxCluster + 1];   // cluster prefix of the above-b* counts
@@ -603,14 +603,16 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
         lsum = fmaf(e, sh.wl[w][st], lsum);
       }
     }
-    sh.po[st][t] = acc;
+    // push this CTA's partial into rank 0's shared memory
+    st_dsmem(&sh.mo[rank][st][t], 0, acc);
     if (t == 0) {
-      sh.pm[st] = M;
-      sh.pl[st] = lsum;
+      st_dsmem(&sh.mm[rank][st], 0, M);
+      st_dsmem(&sh.ml[rank][st], 0, lsum);
     }
   }
   const bool want_idx = a.topk_idx != nullptr || a.topk_score != nullptr;
-  cluster_sync_all();  // every CTA's partial is in its shared memory
+  cluster_sync_all();  // every CTA's partial is in rank 0's shared memory; after this
+                       // barrier no CTA reads another CTA's shared memory (but see below)
 
   // ---- rank 0: Eq. 4-5 over the cluster's partials ----
   if (rank == 0 && tid < kD) {
@@ -619,9 +621,9 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
     for (int c = 0; c < NC; ++c)
 #pragma unroll
       for (int st = 0; st < 2; ++st) {
-        mc[st][c] = ld_dsmem(&sh.pm[st], c);
-        lc[st][c] = ld_dsmem(&sh.pl[st], c);
-        oc[st][c] = ld_dsmem(&sh.po[st][tid], c);
+        mc[st][c] = sh.mm[c][st];
+        lc[st][c] = sh.ml[c][st];
+        oc[st][c] = sh.mo[c][st][tid];
       }
     float zt[2], lsum[2], osum[2];
 #pragma unroll
@@ -702,7 +704,9 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
   }
   if (need > 0 && rank == 0 && tid == 0)  // read by every CTA long before this point
     a.hint_bin[bh] = next_hint | ((wide || redo) ? 1 << 16 : 0);
-  cluster_sync_all();  // rank 0 and the offsets have finished reading shared memory
+  // Candidates past rank 0's copy are read from the other CTAs: keep them
+  // resident until rank 0 has written the outputs (a uniform decision).
+  if (want_idx && cmode != 0 && ncand > kAllCap) cluster_sync_all();
 }
 
 template <int NC>

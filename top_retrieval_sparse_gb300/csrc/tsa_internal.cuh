@@ -241,6 +241,12 @@ __device__ __forceinline__ uint32_t ld_dsmem_u32(const uint32_t* p, uint32_t cta
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
   return v;
 }
+// Stores into the shared memory of CTA `cta` of this cluster.
+__device__ __forceinline__ void st_dsmem(float* p, uint32_t cta, float v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(cta));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
 __device__ __forceinline__ uint64_t ld_dsmem_u64(const uint64_t* p, uint32_t cta) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(cta));
