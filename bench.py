@@ -306,6 +306,151 @@ def run_ours(args, ws, rank, local):
     return res if rank == 0 else None
 
 
+def run_retopk(args, ws, rank, local):
+    """ReTopK decode (Qwen2.5-7B geometry, 64K): one layer-step is retopk_step
+    for all 28 query heads -- cosine recall, candidate union, rescoring and
+    re-top-K on reuse heads, the exact scan + top-K on exact heads, sparse
+    softmax.V and the FIFO push.  Reports microseconds per layer-step over the
+    config's 512-step stream, per path class, and the path mix."""
+    import torch
+    import top_retrieval_sparse_gb300 as tsa
+    from workloads.gen import make_retopk
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    wl = make_retopk("retopk64k", device=dev, seed=rank)
+    kv = tsa.kv_contiguous(wl.k, wl.v)
+    g = tsa.ReTopK(wl.Hq, wl.Hkv, wl.d, wl.K, wl.C, wl.R, wl.W, wl.tau, wl.T_r, wl.lcap,
+                   device=dev)
+    # the FIFO starts from the last C prefill queries and their exact causal top-K
+    sup = torch.full((wl.C, wl.Hq, wl.K), -1, dtype=torch.int32, device=dev)
+    for c in range(wl.C):
+        idx = torch.empty((1, wl.Hq, wl.K), dtype=torch.int32, device=dev)
+        lens = torch.tensor([wl.L0 - wl.C + c + 1], dtype=torch.int32, device=dev)
+        tsa.sparse_attn_decode(wl.q_prefill[c][None].contiguous(), kv, lens, wl.K, 0, 0,
+                               wl.scale, topk_idx=idx)
+        sup[c] = idx[0]
+    cnt = (sup >= 0).sum(-1).to(torch.int32)
+    g.init(wl.q_prefill.contiguous(), sup, cnt)
+    out = torch.empty((wl.Hq, wl.d), dtype=torch.float32, device=dev)
+    path = torch.empty((wl.steps, wl.Hq), dtype=torch.int32, device=dev)
+    mc = torch.empty((wl.steps, wl.Hq), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    steps = min(args.steps, wl.steps)
+    state0, counters0 = g.state.clone(), g.counters()
+
+    def stream_steps(record_path, ev=None):
+        g.state.copy_(state0)
+        g.set_counters(*counters0)
+        n0 = tsa.kernel_launches()
+        for t in range(steps):
+            if ev is not None:
+                ev[t][0].record(stream)
+            g.step(wl.q_all[t], kv, wl.length(t), wl.scale, out=out,
+                   path_out=path[t] if record_path else None,
+                   mcand_out=mc[t] if record_path else None, stream=stream)
+            if ev is not None:
+                ev[t][1].record(stream)
+        return tsa.kernel_launches() - n0
+
+    for _ in range(max(1, args.warmup // 8)):
+        stream_steps(False)
+    torch.cuda.synchronize()
+    clocks = Clocks(torch.cuda.current_device() if ws == 1 else local)
+    clocks.start()
+    # Launched from the host one call at a time, a reuse step's kernels are
+    # shorter than the host's launch work, so the device time is measured on
+    # a CUDA graph of the whole step stream (captured from the same calls);
+    # the host-launched time is reported beside it.
+    side = torch.cuda.Stream(device=dev)
+    graph = torch.cuda.CUDAGraph()
+    g.state.copy_(state0)
+    g.set_counters(*counters0)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=side):
+        n_launch0 = tsa.kernel_launches()
+        for t in range(steps):
+            g.step(wl.q_all[t], kv, wl.length(t), wl.scale, out=out, stream=side)
+        launches = tsa.kernel_launches() - n_launch0
+    for _ in range(2):  # warm-up replays
+        g.state.copy_(state0)
+        graph.replay()
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    g.state.copy_(state0)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    total_ms = max_over_ranks(t0.elapsed_time(t1), ws, dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    stream_steps(False)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    eager_us = 1000.0 * e0.elapsed_time(e1) / steps
+    # per-step events and the path of every head (a second pass over the same stream)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    stream_steps(True, ev)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    per = [e[0].elapsed_time(e[1]) * 1000 for e in ev]
+    p_h, m_h = path[:steps].cpu(), mc[:steps].cpu()
+    exact_steps = [t for t in range(steps) if int(p_h[t].sum()) > 0]
+    reuse_steps = [t for t in range(steps) if int(p_h[t].sum()) == 0]
+    reuse_heads = int((p_h == 0).sum())
+    mean_m = float(m_h[p_h == 0].float().mean()) if reuse_heads else None
+    us = 1000.0 * total_ms / steps / ws
+    # bytes a step must move: exact heads scan the K cache of their KV heads and
+    # gather their selected V rows; reuse heads read M_t K rows, their K V rows
+    # and their cached supports (R*K indices) and queries (C*128 floats)
+    L = wl.length(0)
+    k_scan = wl.Hkv * L * wl.d * 2
+    v_rows = wl.Hq * wl.K * wl.d * 2
+    reuse_bytes = (mean_m or 0) * wl.d * 2 * wl.Hq + v_rows + wl.Hq * (wl.R * wl.K * 4 + wl.C * wl.d * 4)
+    res = {
+        "metric": METRIC, "value": round(us, 3), "unit": UNIT, "n_gpus": ws, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / steps, 5),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "retopk64k", "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
+                   "context": wl.L0, "K": wl.K, "C": wl.C, "R": wl.R, "W": wl.W,
+                   "tau": wl.tau, "T_r": wl.T_r, "decode_steps": steps,
+                   "l2": "K cache 64 MiB < L2 on exact steps; the stream is run as is",
+                   "parallelism": f"replicas{ws}" if ws > 1 else "single"},
+        "host_launched_us_per_step": round(eager_us, 3),
+        "timing": "CUDA graph of the 512-step stream captured from retopk_step calls",
+        "paths": {"steps_with_exact_heads": len(exact_steps), "all_reuse_steps": len(reuse_steps),
+                  "reuse_head_fraction": round(reuse_heads / (steps * wl.Hq), 4),
+                  "mean_candidates_reuse": round(mean_m, 1) if mean_m else None,
+                  "us_steps_with_exact": round(statistics.median([per[t] for t in exact_steps]), 2)
+                  if exact_steps else None,
+                  "us_all_reuse_steps": round(statistics.median([per[t] for t in reuse_steps]), 2)
+                  if reuse_steps else None},
+        "roofline": {"kernel": "whole reuse step (selector, rescore, attend)", "bound": "hbm",
+                     "achieved": round(reuse_bytes / (statistics.median([per[t] for t in reuse_steps])
+                                                      * 1e-6) / 1e9, 1) if reuse_steps else None,
+                     "peak": peaks()[0], "peak_kind": peaks()[1], "unit": "GB/s",
+                     "frac": None, "traffic": None,
+                     "algorithmic_bytes_per_reuse_step": int(reuse_bytes),
+                     "algorithmic_bytes_per_exact_step": int(k_scan + v_rows)},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if res["roofline"]["achieved"]:
+        res["roofline"]["frac"] = round(res["roofline"]["achieved"] / peaks()[0], 4)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return res if rank == 0 else None
+
+
 def run_trace(args, step, tsa, torch, dev, nsteps=3):
     """Run a few steps with the per-CTA trace on and summarise each kernel:
     span (first CTA start -> last CTA exit), gap from the previous kernel,
@@ -490,6 +635,9 @@ def run_reference(args, ws, rank):
         return None
     import torch
     from workloads.gen import make_decode
+    if args.workload == "retopk64k":
+        raise SystemExit("--impl reference times the decode workloads (the oracle's ReTopK "
+                         "step is exercised by the parity tests)")
     wl = make_decode(args.workload, device="cpu")
     # the whole run stays within a few minutes: each step is a bounded sample
     # (at least one query head) of the workload
@@ -522,7 +670,7 @@ def main():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="llama128k",
-                    choices=["tiny", "llama128k", "llama1m", "yi_paged"])
+                    choices=["tiny", "llama128k", "llama1m", "yi_paged", "retopk64k"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
@@ -536,6 +684,8 @@ def main():
     ws, rank, local = dist_env()
     if args.impl == "reference":
         res = run_reference(args, ws, rank)
+    elif args.workload == "retopk64k":
+        res = run_retopk(args, ws, rank, local)
     else:
         res = run_ours(args, ws, rank, local)
     if rank == 0 and res is not None:

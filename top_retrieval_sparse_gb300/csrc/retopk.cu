@@ -23,8 +23,9 @@ constexpr int kRescoreCache = 8192;  // candidates held in shared memory
 constexpr int kMaxC = 64;
 
 __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(RetopkSelArgs a) {
+  TraceScope trace(a.trace, kTrSelector);
   extern __shared__ __align__(16) uint32_t bitmap[];
-  __shared__ float qs[kD];
+  __shared__ __align__(16) float qs[kD];
   __shared__ float rho[kMaxC];
   __shared__ float red[kSelectorThreads / 32];
   __shared__ int chosen[kMaxC];
@@ -56,47 +57,55 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
   }
   __syncthreads();
 
-  // 2. cosine against the cached queries (one warp per entry)
-  for (int c = wid; c < a.C; c += kSelectorThreads / 32) {
-    const float* qc = a.cache_qbar + ((int64_t)h * a.C + c) * kD;
-    float acc = 0.f;
+  // 2. cosine against the cached queries (warp w: entries w, w + 8, ...; all of
+  //    a warp's loads are issued before any is used)
+  {
+    constexpr int kPer = kMaxC / (kSelectorThreads / 32);  // entries per warp, at most
+    float4 qv[kPer];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) acc = fmaf(qs[lane * 4 + e], qc[lane * 4 + e], acc);
-    acc = warp_sum(acc);
-    if (lane == 0) rho[c] = acc;
+    for (int k = 0; k < kPer; ++k) {
+      const int c = wid + k * (kSelectorThreads / 32);
+      qv[k] = c < a.C ? *reinterpret_cast<const float4*>(a.cache_qbar +
+                                                         ((int64_t)h * a.C + c) * kD + lane * 4)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const float4 mq = *reinterpret_cast<const float4*>(qs + lane * 4);
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int c = wid + k * (kSelectorThreads / 32);
+      float acc = mq.x * qv[k].x;
+      acc = fmaf(mq.y, qv[k].y, acc);
+      acc = fmaf(mq.z, qv[k].z, acc);
+      acc = fmaf(mq.w, qv[k].w, acc);
+      acc = warp_sum(acc);
+      if (lane == 0 && c < a.C) rho[c] = acc;
+    }
   }
   __syncthreads();
 
-  // 3. fallback / refresh decision and top-R recall
-  if (tid == 0) {
+  // 3. fallback / refresh decision and top-R recall: entry c is recalled iff
+  //    fewer than R entries beat it (larger rho, or equal rho and older)
+  if (wid == 0) {
     float mx = -INFINITY;
-    for (int c = 0; c < a.C; ++c) mx = fmaxf(mx, rho[c]);
+    for (int c = lane; c < a.C; c += 32) mx = fmaxf(mx, rho[c]);
+    mx = warp_max(mx);
     const int path = (mx < a.tau || a.refresh) ? 1 : 0;
-    s_path = path;
-    a.path[h] = path;
-    if (a.path_out) a.path_out[h] = path;
-    if (!path) {
-      unsigned used = 0u;  // C <= 64 entries, two words
-      unsigned used_hi = 0u;
-      for (int r = 0; r < a.R; ++r) {
-        int best = -1;
-        float bv = -INFINITY;
-        int bage = 1 << 30;
-        for (int c = 0; c < a.C; ++c) {
-          const bool u = c < 32 ? ((used >> c) & 1u) : ((used_hi >> (c - 32)) & 1u);
-          if (u) continue;
-          const int age = (c - a.fifo_head + a.C) % a.C;  // 0 = oldest
-          if (best < 0 || rho[c] > bv || (rho[c] == bv && age < bage)) {
-            best = c;
-            bv = rho[c];
-            bage = age;
-          }
-        }
-        chosen[r] = best;
-        if (best < 32) used |= 1u << best;
-        else used_hi |= 1u << (best - 32);
-      }
+    if (lane == 0) {
+      s_path = path;
+      a.path[h] = path;
+      if (a.path_out) a.path_out[h] = path;
     }
+  }
+  if (tid < a.C) {
+    const float rc = rho[tid];
+    const int agec = (tid - a.fifo_head + a.C) % a.C;  // 0 = oldest
+    int beat = 0;
+    for (int c = 0; c < a.C; ++c) {
+      const float r = rho[c];
+      const int age = (c - a.fifo_head + a.C) % a.C;
+      beat += (r > rc || (r == rc && age < agec)) ? 1 : 0;
+    }
+    if (beat < a.R) chosen[beat] = tid;  // ranks are distinct: one entry per rank
   }
   __syncthreads();
   uint32_t* crow = a.cand + (int64_t)h * a.cand_cap;
@@ -115,12 +124,25 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
   const int nwords = (int)((a.L + 31) >> 5);
   for (int w = tid; w < nwords; w += kSelectorThreads) bitmap[w] = 0u;
   __syncthreads();
-  for (int r = 0; r < a.R; ++r) {
-    const int64_t hc = (int64_t)h * a.C + chosen[r];
-    const int n = a.cache_sup_n[hc];
-    for (int j = tid; j < n; j += kSelectorThreads) {
-      const int32_t p = a.cache_sup[hc * a.K + j];
-      if (p >= 0 && p < a.L) atomicOr(&bitmap[p >> 5], 1u << (p & 31));
+  // the R recalled supports as one flat index space of R*K entries (entries
+  // past a support's size are skipped), several loads in flight per thread
+  {
+    const int64_t total = (int64_t)a.R * a.K;
+    for (int64_t j0 = tid; j0 < total; j0 += 4 * kSelectorThreads) {
+      int32_t pv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t j = j0 + (int64_t)u * kSelectorThreads;
+        pv[u] = -1;
+        if (j < total) {
+          const int r = (int)(j / a.K), i = (int)(j - (int64_t)r * a.K);
+          const int64_t hc = (int64_t)h * a.C + chosen[r];
+          if (i < a.cache_sup_n[hc]) pv[u] = a.cache_sup[hc * a.K + i];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (pv[u] >= 0 && pv[u] < a.L) atomicOr(&bitmap[pv[u] >> 5], 1u << (pv[u] & 31));
     }
   }
   const int64_t lo = a.L - a.W > 0 ? a.L - a.W : 0;
@@ -193,6 +215,7 @@ struct RescoreShared {
 };
 
 __global__ void __launch_bounds__(kRescoreThreads) retopk_rescore_kernel(RetopkRescoreArgs a) {
+  TraceScope trace(a.trace, kTrRescore);
   extern __shared__ __align__(16) uint64_t cache[];
   __shared__ RescoreShared sh;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
