@@ -252,13 +252,17 @@ TSA_API int retopk_init(tsa_retopk* st, const void* prefill_q,
                 const int32_t* prefill_supports, const int32_t* prefill_counts,
                 void* stream);
 
-/* Workspace needed by retopk_step for caches up to max_len keys. */
+/* Workspace needed by retopk_step for caches up to max_len keys: device
+ * scratch, 256-byte aligned, zero-filled before the handle's first step.
+ * Like the decode workspace it keeps per-head state that speeds up the next
+ * step (never its result), so one workspace serves one handle. */
 TSA_API size_t retopk_workspace_size(const tsa_retopk* st);
 
 /* One decode step (see above).  q: bf16 [Hq][128]; kv: this layer's cache
  * with B = 1 (lens are the host value `len`, 1 <= len <= min(kv->l_cap,
  * max_len)); out: fp32 [Hq][128].  Optional outputs (NULL to skip):
- *   support_out int32 [Hq][K] (S_t, unspecified order, -1 padded),
+ *   support_out int32 [Hq][K] (S_t, unspecified order, -1 padded; a copy
+ *     of the FIFO entry this step pushed),
  *   path_out int32 [Hq] (1 exact, 0 reuse),
  *   mcand_out int32 [Hq] (|A_t| on the reuse path, len on the exact path),
  *   cand_out int32 [Hq][R*K+W] (A_t ascending, -1 padded; reuse heads only),

@@ -271,7 +271,7 @@ class ReTopK:
                                    T_r, max_len, _p(self.state), n))
         self.Hq, self.Hkv, self.d, self.K, self.C, self.R, self.W = Hq, Hkv, d, K, C_, R, W
         self.cand_cap = R * K + W
-        self.workspace = torch.empty(int(lib().retopk_workspace_size(self.handle)),
+        self.workspace = torch.zeros(int(lib().retopk_workspace_size(self.handle)),
                                      dtype=torch.uint8, device=device)
 
     def __del__(self):

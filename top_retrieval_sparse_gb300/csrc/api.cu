@@ -406,14 +406,13 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
     f.dense_n = w.dense_n;
     f.dense_stride = w.dense_stride;
     f.spill = w.spill;
-    f.sel_pos = reinterpret_cast<int32_t*>(ws + Lw.sel_idx);
-    f.sel_z = reinterpret_cast<float*>(ws + Lw.sel_z);
     f.wz = w.wz;
     f.wz_stride = w.wz_stride;
     f.out = out;
     f.lse_out = lse_out;
     f.topk_idx = topk_idx;
     f.topk_score = topk_score;
+    f.topk_stride = K;
     f.trace = g_trace;
     if ((e = counted(launch_finish(f, st))) != cudaSuccess) return cuda_fail(e, "finish launch");
   }
@@ -616,9 +615,6 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
   const int Hq = st->Hq;
   int32_t* path = reinterpret_cast<int32_t*>(ws + Lw.path);
   float* qbar_new = reinterpret_cast<float*>(ws + Lw.qbar_new);
-  int32_t* sel_idx = support_out ? support_out : reinterpret_cast<int32_t*>(ws + Lw.sel_idx);
-  float* sel_z = reinterpret_cast<float*>(ws + Lw.sel_z);
-  int32_t* sel_n = reinterpret_cast<int32_t*>(ws + Lw.sel_n);
   SelWs w{};
   w.status = reinterpret_cast<int*>(ws + Lw.status);
   w.hist = reinterpret_cast<uint32_t*>(ws + Lw.hist);
@@ -666,12 +662,17 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
     if ((e = counted(launch_retopk_selector(a, smem, s))) != cudaSuccess)
       return cuda_fail(e, "retopk selector launch");
   }
-  // 2. exact path heads: key scan + exact top-K over all keys (no window)
-  if ((e = launch_exact_topk(static_cast<const uint16_t*>(q), view, nullptr, len, len, 1, Hq,
-                             st->K, 0, 0, scale, path, 1, w, sel_idx, sel_z, sel_n, s)) !=
-      cudaSuccess)
-    return cuda_fail(e, "top-K launch");
-  // 3. reuse path heads: indexed rescoring + re-top-K over A_t
+  // 2. exact-path heads: key scan over all keys (no window): histograms and
+  //    emitted pairs; launched after the selector has decided the paths
+  if ((e = counted(launch_scan([&] {
+         ScanArgs a = scan_args(static_cast<const uint16_t*>(q), view, nullptr, len, 1, Hq, st->K,
+                                0, 0, scale, path, 1, w);
+         a.decide = 0;
+         return a;
+       }(), scan_grid(1, view, len), s, false))) != cudaSuccess)
+    return cuda_fail(e, "scan launch");
+  if ((e = stage_mark(1, s)) != cudaSuccess) return cuda_fail(e, "event record");
+  // 3. reuse-path heads: e_i on A_t as pairs + histogram, the scan's format
   {
     RetopkRescoreArgs a{};
     a.q = static_cast<const uint16_t*>(q);
@@ -682,45 +683,62 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
     a.cand = reinterpret_cast<const uint32_t*>(ws + Lw.cand);
     a.mcand = reinterpret_cast<const int32_t*>(ws + Lw.mcand);
     a.cand_cap = Lw.cand_cap;
-    a.K = st->K;
     a.chunk = 256;
-    a.ehat = reinterpret_cast<float*>(ws + Lw.ehat);
-    a.ticket = reinterpret_cast<uint32_t*>(ws + Lw.tick_rs);
-    a.sel_idx = sel_idx;
-    a.sel_z = sel_z;
-    a.sel_n = sel_n;
+    a.dense = w.dense;
+    a.dense_n = w.dense_n;
+    a.dense_stride = w.dense_stride;
+    a.hist = w.hist;
     a.trace = g_trace;
     const int chunks = (Lw.cand_cap + a.chunk - 1) / a.chunk;
     if ((e = counted(launch_retopk_rescore(a, chunks, s))) != cudaSuccess)
       return cuda_fail(e, "retopk rescore launch");
   }
-  // 4. sparse softmax.V over S_t (no window) and the FIFO push
+  if ((e = stage_mark(2, s)) != cudaSuccess) return cuda_fail(e, "event record");
+  // 4. every head: exact top-K of its pairs, softmax.V over S_t (no window),
+  //    and the FIFO push of (qbar_t, S_t) -- S_t is written into the slot
   {
-    AttendArgs a{};
-    a.kv = view;
-    a.lens = nullptr;
-    a.len_host = len;
-    a.B = 1;
-    a.Hq = Hq;
-    a.wz = w.wz;
-    a.wz_stride = 1;
-    a.n_init = 0;
-    a.n_recent = 0;
-    a.window = 0;
-    a.sel_idx = sel_idx;
-    a.sel_z = sel_z;
-    a.sel_n = sel_n;
-    a.K = st->K;
-    a.out = out;
-    a.lse_out = lse_out;
-    a.push_qbar = qbar_new;
-    a.cache_qbar = st->qbar;
-    a.cache_sup = st->sup;
-    a.cache_sup_n = st->sup_n;
-    a.C = st->C;
-    a.slot = st->fifo_head;
-    a.trace = g_trace;
-    if ((e = counted(launch_attend(a, s))) != cudaSuccess) return cuda_fail(e, "attend launch");
+    FinishArgs f{};
+    f.q = static_cast<const uint16_t*>(q);
+    f.kv = view;
+    f.lens = nullptr;
+    f.len_host = len;
+    f.B = 1;
+    f.Hq = Hq;
+    f.scale = scale;
+    f.K = st->K;
+    f.n_init = 0;
+    f.n_recent = 0;
+    f.hist = w.hist;
+    f.hint_bin = w.hint_bin;
+    f.emit_n = w.emit_n;
+    f.tile_ctr = w.tile_ctr;
+    f.status = w.status;
+    f.dense = w.dense;
+    f.dense_n = w.dense_n;
+    f.dense_stride = w.dense_stride;
+    f.spill = w.spill;
+    f.wz = w.wz;
+    f.wz_stride = 1;
+    f.out = out;
+    f.lse_out = lse_out;
+    f.topk_idx = st->sup + (int64_t)st->fifo_head * st->K;
+    f.topk_score = nullptr;
+    f.topk_stride = (int64_t)st->C * st->K;
+    f.path = path;
+    f.mcand = reinterpret_cast<const int32_t*>(ws + Lw.mcand);
+    f.push_qbar = qbar_new;
+    f.cache_qbar = st->qbar;
+    f.cache_sup_n = st->sup_n;
+    f.C = st->C;
+    f.slot = st->fifo_head;
+    f.trace = g_trace;
+    if ((e = counted(launch_finish(f, s))) != cudaSuccess) return cuda_fail(e, "finish launch");
+  }
+  if (support_out) {  // S_t rows, copied out of the FIFO slot
+    e = cudaMemcpy2DAsync(support_out, (size_t)st->K * 4, st->sup + (int64_t)st->fifo_head * st->K,
+                          (size_t)st->C * st->K * 4, (size_t)st->K * 4, (size_t)Hq,
+                          cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "support copy");
   }
   if ((e = stage_mark(3, s)) != cudaSuccess) return cuda_fail(e, "event record");
   st->t += 1;

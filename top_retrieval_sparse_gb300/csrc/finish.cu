@@ -183,7 +183,9 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
 
   const int64_t L = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
   const int64_t nw = window_count(L, a.n_init, a.n_recent);
-  const int64_t P = L - nw;
+  // a ReTopK reuse head selects among its |A_t| rescored candidates
+  const bool reuse = a.path != nullptr && a.path[bh] == 0;
+  const int64_t P = reuse ? (int64_t)a.mcand[bh] : L - nw;
   const int need = (int64_t)a.K < P ? a.K : (int)P;
   uint64_t* spill = a.spill + (int64_t)bh * a.dense_stride;
   const uint2* lrow = a.dense + (int64_t)bh * a.dense_stride;
@@ -207,7 +209,7 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
   bool wide = false;
   if (need > 0) {
     const int32_t hw = __ldcg(a.hint_bin + bh);
-    const int used = hint_bin_of(hw);
+    const int used = reuse ? 0 : hint_bin_of(hw);  // a reuse head's list holds every candidate
     wide = hint_wide_of(hw);
     if (need < P) {
       // pairs one call may emit, and the margin (bins below b*) the hint
@@ -660,8 +662,8 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
   // ---- optional top-K outputs: each CTA writes its above-b* pairs at its
   // cluster offset; rank 0 appends the selected candidates in cluster order ----
   if (want_idx) {
-    int32_t* oidx = a.topk_idx ? a.topk_idx + (int64_t)bh * a.K : nullptr;
-    float* osc = a.topk_score ? a.topk_score + (int64_t)bh * a.K : nullptr;
+    int32_t* oidx = a.topk_idx ? a.topk_idx + (int64_t)bh * a.topk_stride : nullptr;
+    float* osc = a.topk_score ? a.topk_score + (int64_t)bh * a.topk_stride : nullptr;
     for (int li = tid; li < nmy; li += kFinThreads) {
       const int i = sh.aoff[rank] + li;
       int32_t pos;
@@ -702,8 +704,13 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
       }
     }
   }
-  if (need > 0 && rank == 0 && tid == 0)  // read by every CTA long before this point
+  if (need > 0 && !reuse && rank == 0 && tid == 0)  // read by every CTA long before this point
     a.hint_bin[bh] = next_hint | ((wide || redo) ? 1 << 16 : 0);
+  if (a.push_qbar && rank == 0) {  // ReTopK: (qbar_t, S_t) over the oldest FIFO entry
+    const int64_t hc = (int64_t)bh * a.C + a.slot;
+    if (tid < kD) a.cache_qbar[hc * kD + tid] = a.push_qbar[(int64_t)bh * kD + tid];
+    if (tid == 0) a.cache_sup_n[hc] = need > 0 ? need : 0;
+  }
   // Candidates past rank 0's copy are read from the other CTAs: keep them
   // resident until rank 0 has written the outputs (a uniform decision).
   if (want_idx && cmode != 0 && ncand > kAllCap) cluster_sync_all();

@@ -19,7 +19,6 @@ namespace tsa {
 
 constexpr int kSelectorThreads = 256;
 constexpr int kRescoreThreads = 256;
-constexpr int kRescoreCache = 8192;  // candidates held in shared memory
 constexpr int kMaxC = 64;
 
 __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(RetopkSelArgs a) {
@@ -208,111 +207,93 @@ cudaError_t launch_retopk_selector(const RetopkSelArgs& a, size_t smem, cudaStre
 }
 
 // --------------------------------------------------------------- rescore
-struct RescoreShared {
-  RadixScratch rs;
-  int last;
-  int slot;
-};
-
-__global__ void __launch_bounds__(kRescoreThreads) retopk_rescore_kernel(RetopkRescoreArgs a) {
-  TraceScope trace(a.trace, kTrRescore);
-  extern __shared__ __align__(16) uint64_t cache[];
-  __shared__ RescoreShared sh;
+// One chunk of head h's candidates: (position, logit) pairs into the head's
+// list, and the histogram of their keys.
+__device__ void rescore_chunk(const RetopkRescoreArgs& a, int h) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int h = blockIdx.y;
-  if (a.path[h] != 0) return;
   const int G = a.Hq / a.kv.Hkv;
   const int g = h / G;
   const int M = a.mcand[h] < a.cand_cap ? a.mcand[h] : a.cand_cap;
+  if (blockIdx.x == 0 && tid == 0) a.dense_n[h] = M;
   const uint32_t* crow = a.cand + (int64_t)h * a.cand_cap;
-  float* erow = a.ehat + (int64_t)h * a.cand_cap;
+  uint2* drow = a.dense + (int64_t)h * a.dense_stride;
+  uint32_t* hh = a.hist + (int64_t)h * kHistBins;
 
-  // query slice: 4 elements per lane
-  const uint2 qw = *reinterpret_cast<const uint2*>(a.q + (int64_t)h * kD + lane * 4);
-  const float q0 = bf_lo(qw.x), q1 = bf_hi(qw.x), q2 = bf_lo(qw.y), q3 = bf_hi(qw.y);
-
+  // query slice of this lane's column block: 8 elements (half-warp rows)
+  const int half = lane >> 4, col = 8 * (lane & 15);
+  const uint4 qw = *reinterpret_cast<const uint4*>(a.q + (int64_t)h * kD + col);
+  const float qv[8] = {bf_lo(qw.x), bf_hi(qw.x), bf_lo(qw.y), bf_hi(qw.y),
+                       bf_lo(qw.z), bf_hi(qw.z), bf_lo(qw.w), bf_hi(qw.w)};
+  // a warp takes 32 candidates at a time: lane l fetches candidate base + l's
+  // position; key rows are read by half-warps (16 lanes x 16 bytes), two
+  // rows per load, all 16 loads in flight before any is used
   const int c0 = blockIdx.x * a.chunk;
   const int c1 = c0 + a.chunk < M ? c0 + a.chunk : M;
-  constexpr int U = 4;  // rows in flight per warp
-  for (int base = c0 + wid * U; base < c1; base += (kRescoreThreads / 32) * U) {
-    uint2 kw[U];
+  for (int base = c0 + 32 * wid; base < c1; base += 32 * (kRescoreThreads / 32)) {
+    const int j = base + lane;
+    const uint32_t pos = j < c1 ? crow[j] : 0u;
+    uint4 kv4[16];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int j = base + u;
-      kw[u] = j < c1 ? *reinterpret_cast<const uint2*>(a.kv.k + kv_row(a.kv, 0, g, crow[j]) +
-                                                       lane * 4)
-                     : make_uint2(0u, 0u);
+    for (int k = 0; k < 16; ++k) {
+      const int r = 2 * k + half;
+      const uint32_t pk = __shfl_sync(0xffffffffu, pos, r);
+      kv4[k] = base + r < c1
+                   ? *reinterpret_cast<const uint4*>(a.kv.k + kv_row(a.kv, 0, g, pk) + col)
+                   : make_uint4(0u, 0u, 0u, 0u);
     }
+    float mine = 0.f;  // lane l ends with the logit of row base + l
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      float acc = q0 * bf_lo(kw[u].x);
-      acc = fmaf(q1, bf_hi(kw[u].x), acc);
-      acc = fmaf(q2, bf_lo(kw[u].y), acc);
-      acc = fmaf(q3, bf_hi(kw[u].y), acc);
-      acc = warp_sum(acc);
-      const int j = base + u;
-      if (lane == 0 && j < c1) erow[j] = acc * a.scale;
+    for (int k = 0; k < 16; ++k) {
+      const uint4 w = kv4[k];
+      float acc = qv[0] * bf_lo(w.x);
+      acc = fmaf(qv[1], bf_hi(w.x), acc);
+      acc = fmaf(qv[2], bf_lo(w.y), acc);
+      acc = fmaf(qv[3], bf_hi(w.y), acc);
+      acc = fmaf(qv[4], bf_lo(w.z), acc);
+      acc = fmaf(qv[5], bf_hi(w.z), acc);
+      acc = fmaf(qv[6], bf_lo(w.w), acc);
+      acc = fmaf(qv[7], bf_hi(w.w), acc);
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      // lanes 0-15 hold row 2k's logit, lanes 16-31 row 2k+1's
+      const float e0 = __shfl_sync(0xffffffffu, acc, 0), e1 = __shfl_sync(0xffffffffu, acc, 16);
+      if (lane == 2 * k) mine = e0;
+      if (lane == 2 * k + 1) mine = e1;
+    }
+    if (j < c1) {
+      const float z = mine * a.scale;
+      drow[j] = make_uint2(pos, __float_as_uint(z));
+      atomicAdd(&hh[f2key(z) >> kHistShift], 1u);
     }
   }
+}
 
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    const uint32_t t = atomicAdd(&a.ticket[h], 1u);
-    sh.last = (t == gridDim.x - 1);
-  }
-  __syncthreads();
-  if (!sh.last) return;
-  __threadfence();
-
-  const int need = a.K < M ? a.K : M;
-  int32_t* sidx = a.sel_idx + (int64_t)h * a.K;
-  float* sz = a.sel_z + (int64_t)h * a.K;
-  if (tid == 0) sh.slot = 0;
-  const bool in_smem = M <= kRescoreCache;
-  if (in_smem)
-    for (int j = tid; j < M; j += kRescoreThreads)
-      cache[j] = rank_key(__ldcg(erow + j), crow[j]);
-  __syncthreads();
-  auto val = [&](int j) -> uint64_t {
-    if (in_smem) return cache[j];
-    return rank_key(__ldcg(erow + j), crow[j]);
-  };
-  auto emit = [&](uint64_t v) {
-    const int s = atomicAdd(&sh.slot, 1);
-    if (s < need) {
-      sidx[s] = (int32_t)rank_pos(v);
-      sz[s] = key2f((uint32_t)(v >> 32));
-    }
-  };
-  cta_radix_select(M, need, 0ull, 0ull, 64, val, emit, sh.rs);
-  for (int j = need + tid; j < a.K; j += kRescoreThreads) {
-    sidx[j] = -1;
-    sz[j] = -INFINITY;
-  }
-  if (tid == 0) {
-    a.sel_n[h] = need;
-    a.ticket[h] = 0;
-  }
+// Path and candidates come from the selector, which completed before the key
+// scan started.  The scan serves the exact-path heads only, so the reuse
+// heads are rescored alongside it; the kernel waits for the scan just before
+// it exits, so the finish kernel, which waits for this grid, sees both.
+__global__ void __launch_bounds__(kRescoreThreads) retopk_rescore_kernel(RetopkRescoreArgs a) {
+  TraceScope trace(a.trace, kTrRescore);
+  const int h = blockIdx.y;
+  if (a.path[h] == 0) rescore_chunk(a, h);
+  pdl_trigger();
+  pdl_wait();
 }
 
 cudaError_t launch_retopk_rescore(const RetopkRescoreArgs& a, int chunks, cudaStream_t st) {
-  const size_t smem = (size_t)kRescoreCache * sizeof(uint64_t);
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(retopk_rescore_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured[dev] = 1;
-  }
-  dim3 grid(chunks, a.Hq);
-  retopk_rescore_kernel<<<grid, kRescoreThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(chunks, a.Hq);
+  cfg.blockDim = dim3(kRescoreThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, retopk_rescore_kernel, a);
 }
 
-// ------------------------------------------------------------------ init
 __global__ void retopk_init_kernel(RetopkInitArgs a) {
   __shared__ float red[kD / 32];
   const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
