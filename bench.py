@@ -464,8 +464,8 @@ def run_trace(args, step, tsa, torch, dev, nsteps=3):
     torch.cuda.synchronize()
     tsa.set_trace(None)
     recs = tsa.read_trace(buf)
-    names = {1: "scan", 2: "resolve", 3: "attend", 4: "retopk_selector", 5: "retopk_rescore",
-             6: "scan_pass1", 7: "finish", 8: "finish_phases"}
+    names = {1: "scan", 4: "retopk_selector", 5: "retopk_rescore", 7: "finish",
+             8: "finish_phases"}
     # records of one launch share the kernel id; a launch of a kernel starts
     # after the previous launch of that kernel has ended
     by_kernel = {}

@@ -39,6 +39,17 @@ def test_group_sizes(Hq, Hkv):
     run_and_check(wl, range(2))
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(28, 4), (12, 4)])
+def test_unit_switches_keep_histograms_exact(Hq, Hkv):
+    """~1000 scan tiles over 4 KV heads: CTAs cross unit boundaries inside
+    their static ranges and through dynamic claims, so a shared histogram is
+    flushed and reused for another unit mid-kernel.  Groups of 7 and 3 heads
+    also leave padding slots in it.  Every head must still select exactly."""
+    wl = make_decode("llama128k", L0=65_000, steps=2, B=1, K=512, Hq=Hq, Hkv=Hkv,
+                     n_init=0, n_recent=0)
+    run_and_check(wl, range(2))
+
+
 def test_llama_geometry_downsized_ragged():
     wl = make_decode("llama128k", L0=40_001, steps=3)  # K=2048, window 128+512
     run_and_check(wl, range(3))

@@ -80,19 +80,14 @@ int num_sms() {
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 
-// Device pointers of the exact top-K machinery (scan passes + resolve).
+// Device pointers of the exact top-K machinery (key scan + finish).
 struct SelWs {
   int* status;
-  uint32_t* hist;        // zeroed per call
-  uint32_t* tick_unit;   // zeroed per call
-  uint32_t* tile_ctr;    // zeroed per call
-  int32_t* emit_n;       // zeroed per call
-  int32_t* rescan;       // zeroed per call
-  int32_t* hint_bin;     // persists between calls (any content is safe)
-  int32_t* rescan_bin;
-  int32_t* bstar;
-  uint2* dense;
+  uint32_t* hist;        // counters: zero before a call, cleared by its finish kernel
+  uint32_t* tile_ctr;
   int32_t* dense_n;
+  int32_t* hint_bin;     // persists between calls (any content is safe)
+  uint2* dense;
   int64_t dense_stride;
   uint64_t* spill;
   float* wz;
@@ -100,19 +95,19 @@ struct SelWs {
 };
 
 // Workspace of one decode call (offsets from the base).  [zero_begin,
-// zero_end) is cleared by every call; the hint bins after it persist.
+// zero_end) holds the counters that start every call at zero; the hint
+// bins after them persist.
 struct DecodeLayout {
-  size_t zero_begin, status, tile_ctr, hist, sel_n, tick_unit, emit_n, dense_n, rescan, zero_end;
-  size_t hint_bin, rescan_bin, bstar, wz, dense, spill, sel_idx, sel_z, total;
+  size_t zero_begin, status, tile_ctr, hist, dense_n, zero_end;
+  size_t hint_bin, wz, dense, spill, total;
   int64_t dense_stride;
   int wz_stride;
 };
 
-DecodeLayout decode_layout(int B, int Hq, int Hkv, int64_t l_cap, int K, int n_init,
-                           int n_recent) {
+DecodeLayout decode_layout(int B, int Hq, int Hkv, int64_t l_cap, int n_init, int n_recent) {
   DecodeLayout L{};
   const size_t rows = (size_t)B * Hq;
-  const size_t units = (size_t)B * (Hkv > 0 ? Hkv : 1);
+  (void)Hkv;
   L.dense_stride = dense_stride_for(l_cap);
   int64_t win = (int64_t)n_init + n_recent;
   if (win > l_cap) win = l_cap;
@@ -120,30 +115,21 @@ DecodeLayout decode_layout(int B, int Hq, int Hkv, int64_t l_cap, int K, int n_i
   size_t o = 0;
   L.zero_begin = o;
   L.status = o; o = up(o + 4);
-  L.tile_ctr = o; o = up(o + 8);
+  L.tile_ctr = o; o = up(o + 4);
   L.hist = o; o = up(o + rows * kHistBins * 4);
-  L.sel_n = o; o = up(o + rows * 4);
-  L.tick_unit = o; o = up(o + units * 4);
-  L.emit_n = o; o = up(o + rows * 4);
   L.dense_n = o; o = up(o + rows * 4);
-  L.rescan = o; o = up(o + rows * 4);
   L.zero_end = o;
   L.hint_bin = o; o = up(o + rows * 4);
-  L.rescan_bin = o; o = up(o + rows * 4);
-  L.bstar = o; o = up(o + rows * 4);
   L.wz = o; o = up(o + rows * (size_t)L.wz_stride * 4);
   L.dense = o; o = up(o + rows * (size_t)L.dense_stride * 8);
   L.spill = o; o = up(o + rows * (size_t)L.dense_stride * 8);
-  const size_t kk = (size_t)(K > 0 ? K : 1);
-  L.sel_idx = o; o = up(o + rows * kk * 4);
-  L.sel_z = o; o = up(o + rows * kk * 4);
   L.total = o;
   return L;
 }
 
-// Argument block of the key scan (pass 0) over workspace w.
+// Argument block of the key scan over workspace w.
 ScanArgs scan_args(const uint16_t* q, const KvView& view, const int32_t* lens, int64_t len_host,
-                   int B, int Hq, int K, int n_init, int n_recent, float scale,
+                   int B, int Hq, int n_init, int n_recent, float scale,
                    const int32_t* head_active, int active_value, const SelWs& w) {
   ScanArgs s{};
   s.q = q;
@@ -155,19 +141,11 @@ ScanArgs scan_args(const uint16_t* q, const KvView& view, const int32_t* lens, i
   s.scale = scale;
   s.n_init = n_init;
   s.n_recent = n_recent;
-  s.K = K;
-  s.pass = 0;
-  s.decide = 1;
   s.head_active = head_active;
   s.active_value = active_value;
   s.hist = w.hist;
-  s.unit_ticket = w.tick_unit;
   s.tile_ctr = w.tile_ctr;
   s.hint_bin = w.hint_bin;
-  s.rescan = w.rescan;
-  s.rescan_bin = w.rescan_bin;
-  s.bstar = w.bstar;
-  s.emit_n = w.emit_n;
   s.dense = w.dense;
   s.dense_n = w.dense_n;
   s.dense_stride = w.dense_stride;
@@ -178,6 +156,29 @@ ScanArgs scan_args(const uint16_t* q, const KvView& view, const int32_t* lens, i
   return s;
 }
 
+// Finish-kernel arguments common to both entry points.
+FinishArgs finish_args(const uint16_t* q, const KvView& view, int Hq, float scale, int K,
+                       const SelWs& w) {
+  FinishArgs f{};
+  f.q = q;
+  f.kv = view;
+  f.Hq = Hq;
+  f.scale = scale;
+  f.K = K;
+  f.hist = w.hist;
+  f.hint_bin = w.hint_bin;
+  f.tile_ctr = w.tile_ctr;
+  f.status = w.status;
+  f.dense = w.dense;
+  f.dense_n = w.dense_n;
+  f.dense_stride = w.dense_stride;
+  f.spill = w.spill;
+  f.wz = w.wz;
+  f.wz_stride = w.wz_stride;
+  f.trace = g_trace;
+  return f;
+}
+
 // Persistent scan grid: one CTA per SM, at most one per tile.
 int scan_grid(int B, const KvView& view, int64_t max_len) {
   const int64_t tiles =
@@ -186,49 +187,6 @@ int scan_grid(int B, const KvView& view, int64_t max_len) {
   if (grid > tiles) grid = tiles;
   if (grid < 1) grid = 1;
   return (int)grid;
-}
-
-// Key scan (pass 0), re-emission for heads whose hint failed (pass 1) and
-// the per-head resolve, all on stream st (the ReTopK exact path).  Marks
-// stage events 1 and 2.
-cudaError_t launch_exact_topk(const uint16_t* q, const KvView& view, const int32_t* lens,
-                              int64_t len_host, int64_t max_len, int B, int Hq, int K,
-                              int n_init, int n_recent, float scale,
-                              const int32_t* head_active, int active_value, const SelWs& w,
-                              int32_t* sel_idx, float* sel_z, int32_t* sel_n, cudaStream_t st) {
-  ScanArgs s = scan_args(q, view, lens, len_host, B, Hq, K, n_init, n_recent, scale,
-                         head_active, active_value, w);
-  const int grid = scan_grid(B, view, max_len);
-  cudaError_t e = counted(launch_scan(s, (int)grid, st, false));
-  if (e != cudaSuccess) return e;
-  if ((e = stage_mark(1, st)) != cudaSuccess) return e;
-  if (K <= 0) return stage_mark(2, st);
-  s.pass = 1;  // heads whose hint failed re-emit with their exact bin
-  s.head_active = w.rescan;
-  s.active_value = 1;
-  if ((e = counted(launch_scan(s, (int)grid, st, true))) != cudaSuccess) return e;
-  ResolveArgs r{};
-  r.lens = lens;
-  r.len_host = len_host;
-  r.l_cap = view.l_cap;
-  r.B = B;
-  r.Hq = Hq;
-  r.K = K;
-  r.n_init = n_init;
-  r.n_recent = n_recent;
-  r.head_active = head_active;
-  r.active_value = active_value;
-  r.bstar = w.bstar;
-  r.dense = w.dense;
-  r.dense_n = w.dense_n;
-  r.dense_stride = w.dense_stride;
-  r.spill = w.spill;
-  r.sel_idx = sel_idx;
-  r.sel_z = sel_z;
-  r.sel_n = sel_n;
-  r.trace = g_trace;
-  if ((e = counted(launch_resolve(r, st))) != cudaSuccess) return e;
-  return stage_mark(2, st);
 }
 
 int check_kv(const tsa_kv* kv, int B, int Hkv) {
@@ -286,7 +244,8 @@ namespace tsa {
 int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
 // Bytes at the start of a decode workspace that must be zero before a call.
 size_t decode_zero_bytes(int B, int Hq, int Hkv, int64_t l_cap, int K, int n_init, int n_recent) {
-  return decode_layout(B, Hq, Hkv, l_cap, K, n_init, n_recent).zero_end;
+  (void)K;
+  return decode_layout(B, Hq, Hkv, l_cap, n_init, n_recent).zero_end;
 }
 }  // namespace tsa
 
@@ -325,7 +284,7 @@ size_t tsa_decode_workspace_size(int B, int Hq, int Hkv, int d, int64_t l_cap, i
   (void)d;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || l_cap < 0 || K < 0 || n_init < 0 || n_recent < 0)
     return 0;
-  return decode_layout(B, Hq, Hkv, l_cap, K, n_init, n_recent).total;
+  return decode_layout(B, Hq, Hkv, l_cap, n_init, n_recent).total;
 }
 
 int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int B, int Hq,
@@ -342,7 +301,7 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
   if (K < 0 || n_init < 0 || n_recent < 0)
     return fail(TSA_ERR_INVALID_ARG, "K, n_init, n_recent must be >= 0");
   if (!std::isfinite(scale)) return fail(TSA_ERR_INVALID_ARG, "scale must be finite");
-  const DecodeLayout Lw = decode_layout(B, Hq, Hkv, kv->l_cap, K, n_init, n_recent);
+  const DecodeLayout Lw = decode_layout(B, Hq, Hkv, kv->l_cap, n_init, n_recent);
   if (!workspace || !aligned(workspace, kAlign))
     return fail(TSA_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
   if (ws_bytes < Lw.total)
@@ -361,13 +320,8 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
   SelWs w{};
   w.status = reinterpret_cast<int*>(ws + Lw.status);
   w.hist = reinterpret_cast<uint32_t*>(ws + Lw.hist);
-  w.tick_unit = reinterpret_cast<uint32_t*>(ws + Lw.tick_unit);
   w.tile_ctr = reinterpret_cast<uint32_t*>(ws + Lw.tile_ctr);
-  w.emit_n = reinterpret_cast<int32_t*>(ws + Lw.emit_n);
-  w.rescan = reinterpret_cast<int32_t*>(ws + Lw.rescan);
   w.hint_bin = reinterpret_cast<int32_t*>(ws + Lw.hint_bin);
-  w.rescan_bin = reinterpret_cast<int32_t*>(ws + Lw.rescan_bin);
-  w.bstar = reinterpret_cast<int32_t*>(ws + Lw.bstar);
   w.dense = reinterpret_cast<uint2*>(ws + Lw.dense);
   w.dense_n = reinterpret_cast<int32_t*>(ws + Lw.dense_n);
   w.dense_stride = Lw.dense_stride;
@@ -377,9 +331,8 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
 
   // 1. key scan (logits, histograms, emitted pairs, window logits)
   if (kv->l_cap > 0) {
-    ScanArgs s = scan_args(static_cast<const uint16_t*>(q), view, lens, 0, B, Hq, K, n_init,
-                           n_recent, scale, nullptr, 0, w);
-    s.decide = 0;  // the finish kernel decides
+    const ScanArgs s = scan_args(static_cast<const uint16_t*>(q), view, lens, 0, B, Hq, n_init,
+                                 n_recent, scale, nullptr, 0, w);
     if ((e = counted(launch_scan(s, scan_grid(B, view, kv->l_cap), st, true))) != cudaSuccess)
       return cuda_fail(e, "scan launch");
   }
@@ -387,33 +340,16 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
   if ((e = stage_mark(2, st)) != cudaSuccess) return cuda_fail(e, "event record");
   // 2-3. exact top-K outside the window, window + selected partials, gamma merge
   {
-    FinishArgs f{};
-    f.q = static_cast<const uint16_t*>(q);
-    f.kv = view;
+    FinishArgs f = finish_args(static_cast<const uint16_t*>(q), view, Hq, scale, K, w);
     f.lens = lens;
     f.B = B;
-    f.Hq = Hq;
-    f.scale = scale;
-    f.K = K;
     f.n_init = n_init;
     f.n_recent = n_recent;
-    f.hist = w.hist;
-    f.hint_bin = w.hint_bin;
-    f.emit_n = w.emit_n;
-    f.tile_ctr = w.tile_ctr;
-    f.status = w.status;
-    f.dense = w.dense;
-    f.dense_n = w.dense_n;
-    f.dense_stride = w.dense_stride;
-    f.spill = w.spill;
-    f.wz = w.wz;
-    f.wz_stride = w.wz_stride;
     f.out = out;
     f.lse_out = lse_out;
     f.topk_idx = topk_idx;
     f.topk_score = topk_score;
     f.topk_stride = K;
-    f.trace = g_trace;
     if ((e = counted(launch_finish(f, st))) != cudaSuccess) return cuda_fail(e, "finish launch");
   }
   if ((e = stage_mark(3, st)) != cudaSuccess) return cuda_fail(e, "event record");
@@ -452,10 +388,8 @@ namespace {
 constexpr uint32_t kMagic = 0x52544b31u;  // "RTK1"
 
 struct RetopkLayout {
-  size_t zero_begin, status, tile_ctr, hist, sel_n, tick_rs, tick_unit, emit_n, dense_n, rescan,
-      zero_end;
-  size_t hint_bin, rescan_bin, bstar, wz, dense, spill, qbar_new, path, cand, mcand, ehat,
-      sel_idx, sel_z, total;
+  size_t zero_begin, status, tile_ctr, hist, dense_n, zero_end;
+  size_t hint_bin, wz, dense, spill, qbar_new, path, cand, mcand, total;
   int64_t dense_stride;
   int cand_cap;
 };
@@ -468,18 +402,11 @@ RetopkLayout retopk_layout(const tsa_retopk* s) {
   size_t o = 0;
   L.zero_begin = o;
   L.status = o; o = up(o + 4);
-  L.tile_ctr = o; o = up(o + 8);
+  L.tile_ctr = o; o = up(o + 4);
   L.hist = o; o = up(o + H * kHistBins * 4);
-  L.sel_n = o; o = up(o + H * 4);
-  L.tick_rs = o; o = up(o + H * 4);
-  L.tick_unit = o; o = up(o + (size_t)s->Hkv * 4);
-  L.emit_n = o; o = up(o + H * 4);
   L.dense_n = o; o = up(o + H * 4);
-  L.rescan = o; o = up(o + H * 4);
   L.zero_end = o;
   L.hint_bin = o; o = up(o + H * 4);
-  L.rescan_bin = o; o = up(o + H * 4);
-  L.bstar = o; o = up(o + H * 4);
   L.wz = o; o = up(o + 64);  // no window on this path
   L.dense = o; o = up(o + H * (size_t)L.dense_stride * 8);
   L.spill = o; o = up(o + H * (size_t)L.dense_stride * 8);
@@ -487,9 +414,6 @@ RetopkLayout retopk_layout(const tsa_retopk* s) {
   L.path = o; o = up(o + H * 4);
   L.cand = o; o = up(o + H * (size_t)L.cand_cap * 4);
   L.mcand = o; o = up(o + H * 4);
-  L.ehat = o; o = up(o + H * (size_t)L.cand_cap * 4);
-  L.sel_idx = o; o = up(o + H * (size_t)s->K * 4);
-  L.sel_z = o; o = up(o + H * (size_t)s->K * 4);
   L.total = o;
   return L;
 }
@@ -608,9 +532,11 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  cudaError_t e = cudaMemsetAsync(ws + Lw.zero_begin, 0, Lw.zero_end - Lw.zero_begin, s);
-  if (e != cudaSuccess) return cuda_fail(e, "memset");
-  if ((e = stage_mark(0, s)) != cudaSuccess) return cuda_fail(e, "event record");
+  // As on the decode path, the workspace counters start at zero (the caller
+  // zeroes a new workspace once; every step's finish kernel clears them), so
+  // the four kernels form one chain of programmatic dependents.
+  cudaError_t e = stage_mark(0, s);
+  if (e != cudaSuccess) return cuda_fail(e, "event record");
   const KvView view = make_view(kv, st->Hkv);
   const int Hq = st->Hq;
   int32_t* path = reinterpret_cast<int32_t*>(ws + Lw.path);
@@ -618,13 +544,8 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
   SelWs w{};
   w.status = reinterpret_cast<int*>(ws + Lw.status);
   w.hist = reinterpret_cast<uint32_t*>(ws + Lw.hist);
-  w.tick_unit = reinterpret_cast<uint32_t*>(ws + Lw.tick_unit);
   w.tile_ctr = reinterpret_cast<uint32_t*>(ws + Lw.tile_ctr);
-  w.emit_n = reinterpret_cast<int32_t*>(ws + Lw.emit_n);
-  w.rescan = reinterpret_cast<int32_t*>(ws + Lw.rescan);
   w.hint_bin = reinterpret_cast<int32_t*>(ws + Lw.hint_bin);
-  w.rescan_bin = reinterpret_cast<int32_t*>(ws + Lw.rescan_bin);
-  w.bstar = reinterpret_cast<int32_t*>(ws + Lw.bstar);
   w.dense = reinterpret_cast<uint2*>(ws + Lw.dense);
   w.dense_n = reinterpret_cast<int32_t*>(ws + Lw.dense_n);
   w.dense_stride = Lw.dense_stride;
@@ -664,12 +585,9 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
   }
   // 2. exact-path heads: key scan over all keys (no window): histograms and
   //    emitted pairs; launched after the selector has decided the paths
-  if ((e = counted(launch_scan([&] {
-         ScanArgs a = scan_args(static_cast<const uint16_t*>(q), view, nullptr, len, 1, Hq, st->K,
-                                0, 0, scale, path, 1, w);
-         a.decide = 0;
-         return a;
-       }(), scan_grid(1, view, len), s, false))) != cudaSuccess)
+  if ((e = counted(launch_scan(scan_args(static_cast<const uint16_t*>(q), view, nullptr, len, 1,
+                                         Hq, 0, 0, scale, path, 1, w),
+                               scan_grid(1, view, len), s, true))) != cudaSuccess)
     return cuda_fail(e, "scan launch");
   if ((e = stage_mark(1, s)) != cudaSuccess) return cuda_fail(e, "event record");
   // 3. reuse-path heads: e_i on A_t as pairs + histogram, the scan's format
@@ -697,28 +615,12 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
   // 4. every head: exact top-K of its pairs, softmax.V over S_t (no window),
   //    and the FIFO push of (qbar_t, S_t) -- S_t is written into the slot
   {
-    FinishArgs f{};
-    f.q = static_cast<const uint16_t*>(q);
-    f.kv = view;
+    FinishArgs f = finish_args(static_cast<const uint16_t*>(q), view, Hq, scale, st->K, w);
     f.lens = nullptr;
     f.len_host = len;
     f.B = 1;
-    f.Hq = Hq;
-    f.scale = scale;
-    f.K = st->K;
     f.n_init = 0;
     f.n_recent = 0;
-    f.hist = w.hist;
-    f.hint_bin = w.hint_bin;
-    f.emit_n = w.emit_n;
-    f.tile_ctr = w.tile_ctr;
-    f.status = w.status;
-    f.dense = w.dense;
-    f.dense_n = w.dense_n;
-    f.dense_stride = w.dense_stride;
-    f.spill = w.spill;
-    f.wz = w.wz;
-    f.wz_stride = 1;
     f.out = out;
     f.lse_out = lse_out;
     f.topk_idx = st->sup + (int64_t)st->fifo_head * st->K;
@@ -731,7 +633,6 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
     f.cache_sup_n = st->sup_n;
     f.C = st->C;
     f.slot = st->fifo_head;
-    f.trace = g_trace;
     if ((e = counted(launch_finish(f, s))) != cudaSuccess) return cuda_fail(e, "finish launch");
   }
   if (support_out) {  // S_t rows, copied out of the FIFO slot

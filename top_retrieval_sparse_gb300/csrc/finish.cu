@@ -7,27 +7,32 @@
 // (o_W and o_Omega over disjoint W and Omega, each with its local max) and
 // Eq. 4-5 (o_t = g1 o_W + g2 o_Omega).
 //
-// One thread-block cluster of 8 CTAs per (sequence, query head):
+// One thread-block cluster of NC CTAs (NC = 8, 4, 2 or 1, chosen at launch
+// so that all clusters are resident at once, one CTA per SM) per (sequence,
+// query head):
 //   0. every CTA reads the head's 11-bit histogram and finds the threshold
 //      bin b* (the largest bin whose suffix count reaches K); if the scan's
 //      emission bin (the hint) was above b*, the cluster re-emits the head's
 //      pool pairs with bin >= b*, recomputing the logits with the scan's own
 //      tensor-core fragment arithmetic so that every logit -- and so every
 //      bin -- is bit-identical to the scan's; the next call's hint is stored;
-//   1. every CTA reads the whole dense pair list (a few thousand pairs, from
-//      L2) and classifies it in the same order: pairs above b* are selected
-//      outright and dealt round-robin to the 8 CTAs, pairs in b* are the
-//      candidates, all of which every CTA keeps in shared memory;
-//   2. every CTA finds the same exact threshold T among the candidates: CTA
+//   1. each CTA reads its 1/NC slice of the head's pair list (the first
+//      batch is already in flight during step 0): pairs above b* are
+//      selected outright and kept in shared memory, pairs in b* are the
+//      candidates; after the one cluster barrier every CTA copies all the
+//      cluster's candidates through distributed shared memory;
+//   2. every CTA finds the same exact threshold among the candidates: CTA
 //      radix rounds of 11 bits on the 64-bit rank key (order-preserving
-//      logit key, then ~position, so ties go to the smaller position); a
-//      candidate is selected iff its key >= T;
-//   3. each CTA gathers V for its rows -- 1/8 of the window, its share of
-//      the selected pairs and of the selected candidates -- 32 rows per warp
-//      in flight, keeping (max, sum, o) per set in base 2; rank 0 merges the
-//      8 CTA partials through distributed shared memory and applies Eq. 4-5.
-// No step before the merge needs a cluster barrier.
-// Launched as a programmatic dependent of the scan.
+//      logit key, then ~position, so ties go to the smaller position);
+//   3. the selected rows (window, above-b* pairs, selected candidates) are
+//      split evenly over the cluster; each warp gathers V for its rows with
+//      half-warp 16-byte loads, keeping (max, sum, o) per set in base 2;
+//      every CTA pushes its partials into rank 0's shared memory, and rank
+//      0 applies Eq. 4-5.
+// ReTopK steps use the same kernel: a reuse head's list holds its rescored
+// candidates A_t (all of them: no hint, no re-emission), no head has a
+// window, and rank 0 pushes (qbar_t, S_t) into the query-support FIFO.
+// Launched as a programmatic dependent of the kernel that wrote the lists.
 #include "tsa_internal.cuh"
 #include "tsa_kernels.h"
 
@@ -177,8 +182,8 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
     }
   }
   pdl_wait();     // pairs, bins and window logits come from the scan
-  pdl_trigger();  // the next call's key scan may start streaming keys (it
-                  // writes nothing until this kernel has completed)
+  pdl_trigger();  // the next kernel may be scheduled (it writes nothing
+                  // this kernel reads until this kernel has completed)
   trace.mark(1);
 
   const int64_t L = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
@@ -370,10 +375,8 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
     for (int q = tid; q < kHistBins / 4; q += kFinThreads) hz[q] = make_uint4(0u, 0u, 0u, 0u);
     if (tid == 0) {
       a.dense_n[bh] = 0;
-      a.emit_n[bh] = 0;
       if (bh == 0) {
-        a.tile_ctr[0] = 0;
-        a.tile_ctr[1] = 0;
+        *a.tile_ctr = 0;
         *a.status = 0;
       }
     }

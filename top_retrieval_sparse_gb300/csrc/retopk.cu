@@ -49,6 +49,10 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
   }
   __syncthreads();
   const float nrm = sqrtf(red[0]);
+  // the cache and this step's buffers belong to the previous step's kernels
+  // until they have completed; the key scan may be scheduled from here on
+  pdl_wait();
+  pdl_trigger();
   if (tid < kD) {
     const float qb = nrm > 0.f ? qs[tid] / nrm : 0.f;
     qs[tid] = qb;
@@ -202,8 +206,17 @@ cudaError_t launch_retopk_selector(const RetopkSelArgs& a, size_t smem, cudaStre
     if (e != cudaSuccess) return e;
     configured[dev] = smem;
   }
-  retopk_selector_kernel<<<a.Hq, kSelectorThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.Hq);
+  cfg.blockDim = dim3(kSelectorThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, retopk_selector_kernel, a);
 }
 
 // --------------------------------------------------------------- rescore
@@ -268,16 +281,14 @@ __device__ void rescore_chunk(const RetopkRescoreArgs& a, int h) {
   }
 }
 
-// Path and candidates come from the selector, which completed before the key
-// scan started.  The scan serves the exact-path heads only, so the reuse
-// heads are rescored alongside it; the kernel waits for the scan just before
-// it exits, so the finish kernel, which waits for this grid, sees both.
+// Path and candidates come from the selector: the key scan before this
+// kernel waited for it, so they are read once the scan has completed.
 __global__ void __launch_bounds__(kRescoreThreads) retopk_rescore_kernel(RetopkRescoreArgs a) {
   TraceScope trace(a.trace, kTrRescore);
   const int h = blockIdx.y;
-  if (a.path[h] == 0) rescore_chunk(a, h);
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
+  if (a.path[h] == 0) rescore_chunk(a, h);
 }
 
 cudaError_t launch_retopk_rescore(const RetopkRescoreArgs& a, int chunks, cudaStream_t st) {

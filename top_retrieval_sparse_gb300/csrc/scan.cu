@@ -29,11 +29,10 @@
 //     bump-allocates runs of 8 slots (one global atomic per run) and pads the
 //     tail of its last run with sentinels -- no logit array is written or
 //     re-read;
-//   * the CTA that completes a (sequence, KV head) unit (ticket) finds the
-//     threshold bin b* of each head and checks that the emitted pairs hold
-//     every position of bins >= b*; heads that fail (hint above b*, or far
-//     too many pairs) are re-emitted by a second pass with the exact bin.
-//     Exactness never depends on the hint, only the cost does.
+//   * the threshold bin b* of each head, the check that the emitted pairs
+//     hold every position of bins >= b* and the re-emission of heads whose
+//     hint was above b* are the finish kernel's: exactness never depends on
+//     the hint, only the cost does.
 #include "tsa_internal.cuh"
 #include "tsa_kernels.h"
 
@@ -70,80 +69,24 @@ struct ConsumerBar {
   }
 };
 
-// Consumer-wide, on a head's histogram in global memory: out[0] = the
-// largest bin whose suffix count reaches `need` (the threshold bin b*, or -1),
-// out[1] = the largest bin whose suffix count reaches `budget` (or -1).  All
-// consumer threads call; every caller gets both bins.
-__device__ void find_bins(const uint32_t* hh, uint32_t need, uint32_t budget, uint32_t* warp_tot,
-                          int* out, int& bstar, int& bbud, ConsumerBar& cb, volatile int* abort) {
-  constexpr int per = kHistBins / kConsumers;  // 4 bins per thread, from the top
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  if (tid == 0) out[0] = out[1] = -1;
-  uint32_t c[per], mine = 0;
-#pragma unroll
-  for (int r = 0; r < per; ++r) {
-    c[r] = __ldcg(hh + kHistBins - 1 - (tid * per + r));
-    mine += c[r];
-  }
-  uint32_t incl = mine;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) warp_tot[wid] = incl;
-  if (!cb.sync()) *abort = 1;
-  if (wid == 0) {
-    const uint32_t w = lane < kScanWarps ? warp_tot[lane] : 0u;
-    uint32_t wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += y;
-    }
-    if (lane < kScanWarps) warp_tot[lane] = wi - w;
-  }
-  if (!cb.sync()) *abort = 1;
-  const uint32_t excl = incl - mine + warp_tot[wid];
-  const uint32_t target[2] = {need, budget};
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    uint32_t acc = excl;
-    if (acc < target[k] && acc + mine >= target[k]) {
-#pragma unroll
-      for (int r = 0; r < per; ++r) {
-        if (acc < target[k] && acc + c[r] >= target[k]) out[k] = kHistBins - 1 - (tid * per + r);
-        acc += c[r];
-      }
-    }
-  }
-  if (!cb.sync()) *abort = 1;
-  bstar = out[0];
-  bbud = out[1];
-  if (!cb.sync()) *abort = 1;
-}
-
 template <int HP>
 __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
-  TraceScope trace(a.trace, a.pass ? kTrScan1 : kTrScan);
+  TraceScope trace(a.trace, kTrScan);
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kStages * kTileBytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(hist + HP * kHistWords);
   uint64_t* empty = full + kStages;
   int* unit_tiles = reinterpret_cast<int*>(empty + kStages);  // prefix over units
-  __shared__ uint32_t warp_tot[kScanWarps];
-  __shared__ int s_flag, s_bins[2];
   __shared__ volatile int s_abort;
   __shared__ uint64_t cons_bar;
   __shared__ int stage_tile[kStages];  // tile of each ring stage (-1: no more tiles)
 
-  if (a.pass == 1) pdl_wait();  // rescan flags come from pass 0
+  if (a.head_active) pdl_wait();  // the activity flags come from the previous grid
   pdl_trigger();
   const int tid = threadIdx.x;
   const int G = a.Hq / a.kv.Hkv;
   const int nunits = a.B * a.kv.Hkv;
-  const bool p0 = a.pass == 0;
 
   // ---- prefix of tiles over (sequence, KV head) units with an active head ----
   if (tid < 32) {
@@ -173,8 +116,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
     }
     if (tid == 0) unit_tiles[nunits] = run;
   }
-  if (p0)
-    for (int i = tid; i < HP * kHistWords; i += kScanThreads) hist[i] = 0;
+  for (int i = tid; i < HP * kHistWords; i += kScanThreads) hist[i] = 0;
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -219,6 +161,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
     const uint64_t pol = policy_evict_first();
     int next_static = t_begin;
     int claim = -1;  // lane 0: dynamic claim requested one tile ahead (-1: none)
+    // the claim counter is cleared by the previous grid: claims wait for it
+    bool waited = a.head_active != nullptr;
     int j = 0;
     bool marker = false;
     for (;; ++j) {
@@ -235,14 +179,23 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
           if (next_static < t_end) {
             t = next_static++;
           } else if (dyn > 0) {
-            const int c = claim >= 0 ? claim : (int)atomicAdd(a.tile_ctr + a.pass, 1u);
+            if (!waited) {
+              pdl_wait();
+              waited = true;
+            }
+            const int c = claim >= 0 ? claim : (int)atomicAdd(a.tile_ctr, 1u);
             claim = -1;
             t = c < dyn ? stat + c : -1;
           }
           // the next tile is a dynamic one: claim it now, so that the
           // atomic's round trip overlaps the wait for a free stage
-          if (t >= 0 && next_static >= t_end && dyn > 0)
-            claim = (int)atomicAdd(a.tile_ctr + a.pass, 1u);
+          if (t >= 0 && next_static >= t_end && dyn > 0) {
+            if (!waited) {
+              pdl_wait();
+              waited = true;
+            }
+            claim = (int)atomicAdd(a.tile_ctr, 1u);
+          }
           stage_tile[s] = t;
           if (t < 0) mbar_arrive(&full[s]);  // no more tiles: release the consumers
         }
@@ -299,16 +252,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
   const int tq = lane & 3;   // k-slot group / C columns 2tq, 2tq+1
 
   uint32_t qb[4][4];         // B fragments: head gr, d in [8(4p+tq), +8) for p < 4
-  bool on[2] = {false, false};  // heads 2tq, 2tq+1 take part in this pass
+  bool on[2] = {false, false};  // heads 2tq, 2tq+1 are active
   int hint[2] = {0, 0};         // emission bins of heads 2tq, 2tq+1
   bool lane_on = false;         // lane h < G: head h takes part (run owner)
-  int wsum = 0;                 // lane h < G: pairs this warp emitted for head h, this unit
   int run_ptr = 0;              // lane h < G: next free slot of this warp's run for head h
   int run_left = 0;             //            slots left in that run
   int cur_unit = -1, unit_end = 0, cur_b = 0, cur_g = 0, head0 = 0;
   int64_t cur_L = 0;
   int rows_since_flush = 0;
-  int visit_tiles = 0;          // tiles of the current unit processed in this visit
   ConsumerBar cb{&cons_bar, 0u};
 
   // flush the shared histogram of `unit` into global memory (consumers)
@@ -326,14 +277,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
         hist[w] = 0;
       }
     }
-    if (a.decide) __threadfence();  // before this CTA's unit ticket
+    // no warp counts the next tile (possibly of another unit) into a word
+    // that another thread has yet to flush and clear
+    if (!cb.sync()) s_abort = 1;
     rows_since_flush = 0;
   };
-  // pass 0: unit finished by this CTA -- flush, add its tiles to the unit
-  // ticket; the CTA that completes the unit decides, per head, the threshold
-  // bin, whether pass 1 must re-emit, and the next call's hint
   // this warp leaves the current unit: pad the unused tail of its runs with
-  // sentinels (both passes)
+  // sentinels
   auto close_runs = [&]() {
     if (lane < G && run_left > 0) {
       uint2* row = a.dense + (int64_t)(head0 + lane) * a.dense_stride;
@@ -346,57 +296,6 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
   auto finish_unit = [&](int unit) {
     flush_hist(unit);
     close_runs();
-    if (lane < G && wsum) atomicAdd(&a.emit_n[head0 + lane], wsum);  // this warp's pairs
-    wsum = 0;
-    if (!a.decide) return;  // the finish kernel decides from the histograms
-    if (lane < G) __threadfence();
-    if (!cb.sync()) s_abort = 1;
-    if (tid == 0) {  // the ticket counts tiles: the CTA completing the count is last
-      const int u0 = unit_tiles[unit], u1 = unit_tiles[unit + 1];
-      const uint32_t mine = (uint32_t)visit_tiles;
-      __threadfence();
-      const uint32_t n = atomicAdd(&a.unit_ticket[unit], mine);
-      s_flag = (n + mine == (uint32_t)(u1 - u0));
-    }
-    if (!cb.sync()) s_abort = 1;
-    if (!s_flag || s_abort) return;
-    __threadfence();
-    const int b = unit / a.kv.Hkv, g = unit % a.kv.Hkv;
-    const int64_t L = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
-    const int64_t P = L - window_count(L, a.n_init, a.n_recent);
-    const int64_t need = a.K < P ? a.K : P;
-    for (int hl = 0; hl < G; ++hl) {
-      const int bh = b * a.Hq + g * G + hl;
-      if (a.head_active && a.head_active[bh] != a.active_value) continue;
-      const int used = hint_bin_of(__ldcg(a.hint_bin + bh));
-      int bin = -1, exact_bin = 0, redo = 0, next_hint = 0;
-      if (need > 0 && need < P) {
-        // next call's hint: the lowest bin whose suffix stays within the
-        // emission budget, never above b*
-        const int64_t budget = 3 * need + 4096;
-        int bbud;
-        find_bins(a.hist + (int64_t)bh * kHistBins, (uint32_t)need,
-                  (uint32_t)(budget + 1 < P ? budget + 1 : P + 1), warp_tot, s_bins, bin, bbud,
-                  cb, &s_abort);
-        exact_bin = bin;
-        next_hint = bbud < 0 ? 0 : (bbud + 1 < bin ? bbud + 1 : bin);
-        const int64_t emitted = __ldcg(a.emit_n + bh);
-        redo = used > bin || emitted > 4 * need + 8192;
-      } else if (need > 0) {  // every pool position is selected
-        exact_bin = 0;
-        redo = used > 0;
-      }
-      if (tid == 0) {
-        a.bstar[bh] = bin;
-        a.rescan[bh] = redo;
-        a.rescan_bin[bh] = exact_bin;
-        if (redo) {
-          a.emit_n[bh] = 0;
-          a.dense_n[bh] = 0;
-        }
-        if (need > 0) a.hint_bin[bh] = next_hint;
-      }
-    }
   };
 
   for (int j = 0;; ++j) {
@@ -409,13 +308,9 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
     if (t < 0) break;             // no more tiles (same stage, same j, for every warp)
     if (t >= unit_end) {  // entering a new unit (all consumers at the same tile)
       const int unit = locate(t);
-      if (cur_unit >= 0) {
-        if (p0) finish_unit(cur_unit);
-        else close_runs();
-      }
+      if (cur_unit >= 0) finish_unit(cur_unit);
       cur_unit = unit;
       unit_end = unit_tiles[unit + 1];
-      visit_tiles = 0;
       cur_b = unit / a.kv.Hkv;
       cur_g = unit % a.kv.Hkv;
       head0 = cur_b * a.Hq + cur_g * G;
@@ -425,10 +320,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
         const int hl = 2 * tq + e;
         const int bh = head0 + hl;
         on[e] = hl < G && (!a.head_active || a.head_active[bh] == a.active_value);
-        hint[e] = 0;
-        if (on[e])
-          hint[e] = p0 ? hint_bin_of(__ldcg(a.hint_bin + bh))
-                       : __ldcg(a.rescan_bin + bh);
+        hint[e] = on[e] ? hint_bin_of(__ldcg(a.hint_bin + bh)) : 0;
       }
       lane_on = lane < G && (!a.head_active || a.head_active[head0 + lane] == a.active_value);
       const uint16_t* qp = a.q + ((int64_t)head0 + (gr < G ? gr : 0)) * kD;
@@ -438,11 +330,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
         if (gr < G) w = *reinterpret_cast<const uint4*>(qp + 8 * (4 * p + tq));
         qb[p][0] = w.x; qb[p][1] = w.y; qb[p][2] = w.z; qb[p][3] = w.w;
       }
-    } else if (p0 && rows_since_flush > kFlushRows) {
+    } else if (rows_since_flush > kFlushRows) {
       flush_hist(cur_unit);
     }
     rows_since_flush += kTileRows;
-    ++visit_tiles;
     const int tile = t - unit_tiles[cur_unit];
     if (j == 0) trace.mark(1);
     {
@@ -472,16 +363,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
         if (on[e & 1] && i < cur_L) {
           const uint32_t bin = f2key(zv[e]) >> kHistShift;
           if (!pool_tile && in_window(i, cur_L, a.n_init, a.n_recent)) {
-            if (p0) {
-              const int64_t wa = a.n_init < cur_L ? a.n_init : cur_L;
-              const int64_t lo = cur_L - a.n_recent > wa ? cur_L - a.n_recent : wa;
-              const int64_t wj = i < wa ? i : wa + (i - lo);
-              a.wz[(int64_t)(head0 + 2 * tq + (e & 1)) * a.wz_stride + wj] = zv[e];
-            }
+            const int64_t wa = a.n_init < cur_L ? a.n_init : cur_L;
+            const int64_t lo = cur_L - a.n_recent > wa ? cur_L - a.n_recent : wa;
+            const int64_t wj = i < wa ? i : wa + (i - lo);
+            a.wz[(int64_t)(head0 + 2 * tq + (e & 1)) * a.wz_stride + wj] = zv[e];
           } else {
-            if (p0)
-              atomicAdd(&hist[(2 * tq + (e & 1)) * kHistWords + (bin >> 1)],
-                        1u << ((bin & 1) << 4));
+            atomicAdd(&hist[(2 * tq + (e & 1)) * kHistWords + (bin >> 1)],
+                      1u << ((bin & 1) << 4));
             if ((int)bin >= hint[e & 1]) emit |= 1u << e;
           }
         }
@@ -511,7 +399,6 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
               run_ptr += cnt;
               run_left -= cnt;
             }
-            wsum += cnt;
           }
         }
         const unsigned M = 0x11111111u << tq;
@@ -547,10 +434,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
     return;
   }
   trace.mark(2);
-  if (cur_unit >= 0) {
-    if (p0) finish_unit(cur_unit);
-    else close_runs();
-  }
+  if (cur_unit >= 0) finish_unit(cur_unit);
 }
 
 template <int HP>

@@ -57,16 +57,6 @@ __device__ __forceinline__ uint32_t rank_pos(uint64_t v) {
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Packed fp32x2 FMA (sm_100+): d = a * b + c on both halves.
-__device__ __forceinline__ void ffma2(float2& d, float2 a, float2 b) {
-  uint64_t ar, br, dr;
-  asm("mov.b64 %0, {%1,%2};" : "=l"(ar) : "f"(a.x), "f"(a.y));
-  asm("mov.b64 %0, {%1,%2};" : "=l"(br) : "f"(b.x), "f"(b.y));
-  asm("mov.b64 %0, {%1,%2};" : "=l"(dr) : "f"(d.x), "f"(d.y));
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(dr) : "l"(ar), "l"(br));
-  asm("mov.b64 {%0,%1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(dr));
-}
-
 // ------------------------------------------------------------- KV address
 struct KvView {
   const uint16_t* k;          // bf16 bits
@@ -181,11 +171,6 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parit
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-// Named barrier over the first `nthreads` threads of the CTA (id 1).
-__device__ __forceinline__ void named_sync(int nthreads) {
-  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-}
-
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -227,13 +212,6 @@ __device__ __forceinline__ void cluster_sync_all() {
 }
 // Loads from the shared memory of CTA `cta` of this cluster (distributed
 // shared memory): p is the address of the same variable in this CTA.
-__device__ __forceinline__ float ld_dsmem(const float* p, uint32_t cta) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(cta));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
-}
 __device__ __forceinline__ uint32_t ld_dsmem_u32(const uint32_t* p, uint32_t cta) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(cta));
@@ -252,16 +230,6 @@ __device__ __forceinline__ uint64_t ld_dsmem_u64(const uint64_t* p, uint32_t cta
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(cta));
   uint64_t v;
   asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(remote) : "memory");
-  return v;
-}
-__device__ __forceinline__ uint4 ld_dsmem_v4(const uint32_t* p, uint32_t cta) {  // 16-B aligned
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(cta));
-  uint4 v;
-  asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(remote)
-               : "memory");
   return v;
 }
 
@@ -316,9 +284,8 @@ struct TraceScope {
     }
   }
 };
-enum TraceKernel : uint32_t {
-  kTrScan = 1, kTrSelect = 2, kTrAttend = 3, kTrSelector = 4, kTrRescore = 5, kTrScan1 = 6,
-  kTrFinish = 7, kTrFinishPhases = 8
+enum TraceKernel : uint32_t {  // 2, 3 and 6 are retired ids
+  kTrScan = 1, kTrSelector = 4, kTrRescore = 5, kTrFinish = 7, kTrFinishPhases = 8
 };
 
 // ------------------------------------------------------ warp/block utils
@@ -331,131 +298,6 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
-}
-
-// Warp-aggregated slot reservation: every lane with `pred` gets a distinct
-// index from *counter (one atomic per warp).
-__device__ __forceinline__ int warp_reserve(bool pred, int* counter) {
-  unsigned m = __ballot_sync(0xffffffffu, pred);
-  if (!m) return -1;
-  int lane = threadIdx.x & 31;
-  int leader = __ffs(m) - 1;
-  int base = 0;
-  if (lane == leader) base = atomicAdd(counter, __popc(m));
-  base = __shfl_sync(0xffffffffu, base, leader);
-  return pred ? base + __popc(m & ((1u << lane) - 1)) : -1;
-}
-
-// ------------------------------------------------------ CTA radix select
-// Selects the `need` largest of n distinct 64-bit values val(j), j < n, all
-// of which share the bits `prefix` under `mask` (the known high bits), and
-// calls emit(v) once for each selected value (in no particular order).
-// Digit of 11 bits per round, scanned from the top; every round either
-// emits the elements above the threshold digit or finishes.  smem_hist
-// needs kHistBins uint32; uses __syncthreads (all threads must call).
-struct RadixScratch {
-  uint32_t hist[kHistBins];
-  uint32_t warp_tot[32];
-  int digit;
-  int above;
-  int match;
-};
-
-template <class ValFn, class EmitFn>
-__device__ void cta_radix_select(int n, int need, uint64_t prefix, uint64_t mask, int shift,
-                                 ValFn val, EmitFn emit, RadixScratch& s) {
-  const int tid = threadIdx.x, nt = blockDim.x;
-  int match = n;  // elements currently matching prefix/mask
-  while (need > 0) {
-    if (match <= need) {  // everything still matching is selected
-      for (int j = tid; j < n; j += nt) {
-        uint64_t v = val(j);
-        if ((v & mask) == prefix) emit(v);
-      }
-      break;
-    }
-    int db = shift < kHistBits ? shift : kHistBits;
-    shift -= db;
-    const uint32_t dmask = (1u << db) - 1u;
-    for (int i = tid; i < kHistBins; i += nt) s.hist[i] = 0;
-    __syncthreads();
-    for (int j = tid; j < n; j += nt) {
-      uint64_t v = val(j);
-      if ((v & mask) == prefix) atomicAdd(&s.hist[(uint32_t)(v >> shift) & dmask], 1u);
-    }
-    __syncthreads();
-    // threshold digit: largest d with sum_{e >= d} hist[e] >= need.
-    // Thread t owns bins scanned from the top in blocks of `per`.
-    const int nb = 1 << db;
-    const int per = (nb + nt - 1) / nt;
-    uint32_t mine = 0;
-    for (int r = 0; r < per; ++r) {
-      int idx = tid * per + r;  // position from the top
-      if (idx < nb) mine += s.hist[nb - 1 - idx];
-    }
-    // inclusive scan of `mine` over threads (top-down order)
-    uint32_t incl = mine;
-    const int lane = tid & 31, wid = tid >> 5;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (lane == 31) s.warp_tot[wid] = incl;
-    __syncthreads();
-    if (wid == 0) {
-      int nw = (nt + 31) >> 5;
-      uint32_t w = lane < nw ? s.warp_tot[lane] : 0;
-      uint32_t wi = w;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        uint32_t y = __shfl_up_sync(0xffffffffu, wi, o);
-        if (lane >= o) wi += y;
-      }
-      if (lane < nw) s.warp_tot[lane] = wi - w;  // exclusive warp offsets
-    }
-    __syncthreads();
-    uint32_t excl = incl - mine + s.warp_tot[wid];
-    if (excl < (uint32_t)need && excl + mine >= (uint32_t)need) {
-      uint32_t acc = excl;
-      for (int r = 0; r < per; ++r) {
-        int idx = tid * per + r;
-        if (idx >= nb) break;
-        uint32_t c = s.hist[nb - 1 - idx];
-        if (acc + c >= (uint32_t)need) {
-          s.digit = nb - 1 - idx;
-          s.above = (int)acc;
-          s.match = (int)c;
-          break;
-        }
-        acc += c;
-      }
-    }
-    __syncthreads();
-    const uint32_t dstar = (uint32_t)s.digit;
-    const int above = s.above;
-    const int cnt = s.match;
-    __syncthreads();
-    if (above > 0) {
-      for (int j = tid; j < n; j += nt) {
-        uint64_t v = val(j);
-        if ((v & mask) == prefix && ((uint32_t)(v >> shift) & dmask) > dstar) emit(v);
-      }
-    }
-    need -= above;
-    prefix |= (uint64_t)dstar << shift;
-    mask |= (uint64_t)dmask << shift;
-    match = cnt;
-    if (shift == 0) {  // fully determined: `match` (= 1) element equals prefix
-      if (need > 0)
-        for (int j = tid; j < n; j += nt) {
-          uint64_t v = val(j);
-          if (v == prefix) emit(v);
-        }
-      break;
-    }
-  }
-  __syncthreads();
 }
 
 }  // namespace tsa

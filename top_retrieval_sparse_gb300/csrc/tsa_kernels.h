@@ -12,16 +12,14 @@ namespace tsa {
 // Per-head activity filter: a head takes part iff
 // head_active == nullptr || head_active[b*Hq + h] == active_value.
 //
-// Key scan, pass 0: logits of every active head; window logits go to wz, pool
+// Key scan: logits of every active head; window logits go to wz, pool
 // positions feed the 11-bit histogram and are emitted as (position, logit)
 // pairs when their bin is >= the head's hint bin.  Pairs go to the head's
 // dense list: every warp bump-allocates runs of 8 slots from dense_n and pads
-// the unused tail of its last run with sentinel pairs (position 0xffffffff).  The CTA that completes a
-// (sequence, KV head) unit turns the histograms into the threshold bin b* and
-// decides per head whether the emitted pairs provably contain the top-K
-// (hint <= b* and not too many emitted); if not, the head is flagged for
-// pass 1, which re-emits with the exact bin (b*, or 0 when every pool
-// position is selected).  The hint for the next call is b* - 1.
+// the unused tail of its last run with sentinel pairs (position 0xffffffff).
+// The finish kernel turns the histograms into b* and checks the emission.
+// With head_active set, the kernel waits for the previous grid (which wrote
+// it) before it starts; otherwise its producer streams keys at once.
 struct ScanArgs {
   const uint16_t* q;         // bf16 [B][Hq][128]
   KvView kv;
@@ -30,54 +28,22 @@ struct ScanArgs {
   int B, Hq;
   float scale;
   int n_init, n_recent;      // static window (logits to wz, not emitted)
-  int K;                     // top-K budget
-  int pass;                  // 0 or 1
-  int decide;                // 1: the CTA completing a unit sets b*, pass-1 flags and the next
-                             // hint; 0: histograms and pairs only (the finish kernel decides)
-  const int32_t* head_active;
-  int active_value;
-  uint32_t* hist;            // [B][Hq][kHistBins] (zeroed), pass 0
-  uint32_t* unit_ticket;     // [B][Hkv] (zeroed), pass 0
-  uint32_t* tile_ctr;        // [2] (zeroed) dynamic tile claims of pass 0 / pass 1
-  int32_t* hint_bin;         // [B][Hq] persistent across calls (any value is safe)
-  int32_t* rescan;           // [B][Hq] (zeroed) 1: pass 1 needed; pass 1 reads it
-  int32_t* rescan_bin;       // [B][Hq] exact emission bin for pass 1
-  int32_t* bstar;            // [B][Hq] threshold bin (-1: all pool / none)
-  int32_t* emit_n;           // [B][Hq] (zeroed) emitted pairs, pass 0 totals
+  const int32_t* head_active;  // heads with head_active[bh] == active_value take part
+  int active_value;            // (nullptr: every head); written by the previous kernel
+  uint32_t* hist;            // [B][Hq][kHistBins] (zeroed)
+  uint32_t* tile_ctr;        // (zeroed) dynamic tile claims
+  int32_t* hint_bin;         // [B][Hq] emission bins, persistent across calls (any value is safe)
   uint2* dense;              // [B][Hq][dense_stride] (position, logit bits)
   int32_t* dense_n;          // [B][Hq] (zeroed) slots allocated (pairs + sentinels)
   int64_t dense_stride;      // >= l_cap + slack for the padding
-  float* wz;                 // [B][Hq][wz_stride] window logits, pass 0
+  float* wz;                 // [B][Hq][wz_stride] window logits
   int wz_stride;
   int* status;
   TraceBuf trace;
 };
 cudaError_t launch_scan(const ScanArgs& a, int grid, cudaStream_t st, bool pdl);
 
-// Resolve: one CTA per head reads the head's dense pair list, keeps the top
-// min(K, |pool|) (ties to the smaller position) and writes the selected set.
-struct ResolveArgs {
-  const int32_t* lens;
-  int64_t len_host;
-  int64_t l_cap;
-  int B, Hq, K;
-  int n_init, n_recent;
-  const int32_t* head_active;
-  int active_value;
-  const int32_t* bstar;      // threshold bins (-1: every pool position)
-  const uint2* dense;
-  const int32_t* dense_n;
-  int64_t dense_stride;
-  uint64_t* spill;           // [B][Hq][dense_stride] radix scratch (large candidate sets)
-  int32_t* sel_idx;          // [B][Hq][K]
-  float* sel_z;              // [B][Hq][K]
-  int32_t* sel_n;            // [B][Hq]
-  TraceBuf trace;
-};
-cudaError_t launch_resolve(const ResolveArgs& a, cudaStream_t st);
-
-// Finish (decode step after a scan with decide = 0): one cluster of 8 CTAs
-// per (sequence, query head) finds the threshold bin b* from the head's
+// Finish: one cluster of NC CTAs per (sequence, query head) finds the threshold bin b* from the head's
 // histogram, checks the scan's emission against it and re-emits the head's
 // pairs itself when the hint failed (same tensor-core arithmetic as the
 // scan, so the pairs agree with the histogram), stores the next call's
@@ -94,8 +60,7 @@ struct FinishArgs {
   int K, n_init, n_recent;
   uint32_t* hist;            // [B][Hq][kHistBins] pool histograms from the scan (cleared)
   int32_t* hint_bin;         // [B][Hq] the scan's emission bin; the next call's is stored
-  int32_t* emit_n;           // [B][Hq] (cleared for the next call)
-  uint32_t* tile_ctr;        // [2] the scan's tile claims (cleared)
+  uint32_t* tile_ctr;        // the scan's tile claims (cleared)
   int* status;               // (cleared)
   uint2* dense;              // [B][Hq][dense_stride] emitted pairs
   int32_t* dense_n;
@@ -121,31 +86,6 @@ struct FinishArgs {
   TraceBuf trace;
 };
 cudaError_t launch_finish(const FinishArgs& a, cudaStream_t st);
-
-struct AttendArgs {
-  KvView kv;
-  const int32_t* lens;
-  int64_t len_host;
-  int B, Hq;
-  const float* wz;           // window logits, [B][Hq][wz_stride]
-  int wz_stride;
-  int n_init, n_recent;
-  int window;                // 0: no static window on this path
-  const int32_t* sel_idx;    // [B][Hq][K]
-  const float* sel_z;
-  const int32_t* sel_n;      // [B][Hq]
-  int K;
-  float* out;                // [B][Hq][128]
-  float* lse_out;            // [B][Hq] or nullptr
-  // ReTopK cache push (push_qbar == nullptr: none)
-  const float* push_qbar;    // [Hq][128] normalised queries of this step
-  float* cache_qbar;         // [Hq][C][128]
-  int32_t* cache_sup;        // [Hq][C][K]
-  int32_t* cache_sup_n;      // [Hq][C]
-  int C, slot;
-  TraceBuf trace;
-};
-cudaError_t launch_attend(const AttendArgs& a, cudaStream_t st);
 
 cudaError_t launch_lse_merge(const float* oa, const float* la, const float* ob,
                              const float* lb, float* oo, float* lo, int rows, int d,
