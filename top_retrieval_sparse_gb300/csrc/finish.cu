@@ -42,8 +42,8 @@ constexpr int kFinMaxCluster = 8;  // CTAs per head: 1, 2, 4 or 8 (chosen at lau
 constexpr int kFinWarps = 16;
 constexpr int kFinThreads = 32 * kFinWarps;
 constexpr int kSelCap = 2048;   // this CTA's above-b* pairs in shared memory
-constexpr int kMyCap = 2048;    // this CTA's threshold-bin candidates in shared memory
-constexpr int kAllCap = 6144;   // the cluster's threshold-bin candidates, copied locally
+constexpr int kMyCap = 4096;    // this CTA's threshold-bin candidates in shared memory
+constexpr int kAllCap = 16384;  // the cluster's threshold-bin candidates, copied locally
 constexpr int kFinU = 8;        // pairs per thread per batch
 constexpr int kRankShift = 64 - kHistBits;  // b* = the rank key's top 11 bits
 constexpr float kFinLog2e = 1.4426950408889634f;
@@ -391,7 +391,23 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
     const int64_t c1 = n * (c + 1) / NC;
     return __ldcg(spill + (c1 - 1 - (i - kMyCap)));
   };
-  for (int jc = tid; jc < ncand && jc < kAllCap; jc += kFinThreads) sh.cand[jc] = cand_remote(jc);
+  {  // eight remote loads in flight per thread before any is stored
+    constexpr int kCopyU = 8;
+    const int lim = ncand < kAllCap ? ncand : kAllCap;
+    for (int jb = 0; jb < lim; jb += kFinThreads * kCopyU) {
+      uint64_t v[kCopyU];
+#pragma unroll
+      for (int u = 0; u < kCopyU; ++u) {
+        const int jc = jb + u * kFinThreads + tid;
+        v[u] = jc < lim ? cand_remote(jc) : 0ull;
+      }
+#pragma unroll
+      for (int u = 0; u < kCopyU; ++u) {
+        const int jc = jb + u * kFinThreads + tid;
+        if (jc < lim) sh.cand[jc] = v[u];
+      }
+    }
+  }
   __syncthreads();
   auto cand_at = [&](int jc) -> uint64_t {
     return jc < kAllCap ? sh.cand[jc] : cand_remote(jc);

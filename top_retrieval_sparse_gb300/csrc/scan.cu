@@ -391,7 +391,9 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
             p1 = run_ptr;
             const int over = cnt - take;
             if (over > 0) {
-              const int size = (over + 7) & ~7;
+              // runs of 8 within a static range; a dynamic tile is a visit of
+              // its own: it rounds its pairs up to a 32-byte sector only
+              const int size = t < stat ? (over + 7) & ~7 : (over + 3) & ~3;
               p2 = atomicAdd(&a.dense_n[head0 + lane], size);
               run_ptr = p2 + over;
               run_left = size - over;
