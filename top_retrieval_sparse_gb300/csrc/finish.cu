@@ -39,25 +39,26 @@
 namespace tsa {
 
 constexpr int kFinMaxCluster = 8;  // CTAs per head: 1, 2, 4 or 8 (chosen at launch)
-constexpr int kFinWarps = 16;
-constexpr int kFinThreads = 32 * kFinWarps;
 constexpr int kSelCap = 2048;   // this CTA's above-b* pairs in shared memory
 constexpr int kMyCap = 4096;    // this CTA's threshold-bin candidates in shared memory
-constexpr int kAllCap = 16384;  // the cluster's threshold-bin candidates, copied locally
+constexpr int kAllCap = 16384;  // the cluster's threshold-bin candidates, copied locally (NC > 1)
 constexpr int kFinU = 8;        // pairs per thread per batch
 constexpr int kRankShift = 64 - kHistBits;  // b* = the rank key's top 11 bits
 constexpr float kFinLog2e = 1.4426950408889634f;
 constexpr float kFinLn2 = 0.6931471805599453f;
 
+// NC CTAs per head (a cluster), W warps per CTA.  A single-CTA head reads
+// its candidates in place, so it keeps no cluster-wide copy.
+template <int NC, int W>
 struct FinShared {
-  uint64_t cand[kAllCap];         // rank keys of all threshold-bin candidates, cluster order
+  uint64_t cand[NC > 1 ? kAllCap : 1];  // rank keys of all threshold-bin candidates, cluster order
   uint64_t mycand[kMyCap];        // this CTA's candidates (read by the cluster)
   uint2 sel[kSelCap];             // this CTA's above-b* pairs (position, logit bits)
   uint32_t hist[kHistBins];       // radix round histogram
-  float wo[kFinWarps][2][kD];     // warp partials: [set][d], set 0 window, 1 selected
-  float wm[kFinWarps][2], wl[kFinWarps][2];
-  float mo[kFinMaxCluster][2][kD];  // rank 0: the CTA partials, pushed by each CTA
-  float mm[kFinMaxCluster][2], ml[kFinMaxCluster][2];
+  float wo[W][2][kD];             // warp partials: [set][d], set 0 window, 1 selected
+  float wm[W][2], wl[W][2];
+  float mo[NC][2][kD];            // rank 0: the CTA partials, pushed by each CTA
+  float mm[NC][2], ml[NC][2];
   uint32_t warp_tot[32];
   int cnt[2];                     // read by the cluster: above-b* pairs, candidates
   int aoff[kFinMaxCluster + 1];   // cluster prefix of the above-b* counts
@@ -66,7 +67,8 @@ struct FinShared {
 };
 
 // Block-wide exclusive scan of one int per thread (all threads call).
-__device__ int fin_scan(int v, FinShared& sh, int* total) {
+template <int W, class Sh>
+__device__ int fin_scan(int v, Sh& sh, int* total) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   int incl = v;
 #pragma unroll
@@ -77,15 +79,15 @@ __device__ int fin_scan(int v, FinShared& sh, int* total) {
   if (lane == 31) sh.warp_tot[wid] = (uint32_t)incl;
   __syncthreads();
   if (wid == 0) {
-    const int w = lane < kFinWarps ? (int)sh.warp_tot[lane] : 0;
+    const int w = lane < W ? (int)sh.warp_tot[lane] : 0;
     int wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, wi, o);
       if (lane >= o) wi += y;
     }
-    if (lane < kFinWarps) sh.warp_tot[lane] = (uint32_t)(wi - w);
-    if (lane == kFinWarps - 1) sh.scal[7] = wi;
+    if (lane < W) sh.warp_tot[lane] = (uint32_t)(wi - w);
+    if (lane == W - 1) sh.scal[7] = wi;
   }
   __syncthreads();
   const int off = incl - v + (int)sh.warp_tot[wid];
@@ -98,6 +100,7 @@ __device__ int fin_scan(int v, FinShared& sh, int* total) {
 // of cluster rank `rank` covers rows [L*rank/8, L*(rank+1)/8) in blocks of
 // 16 rows per warp; fragments, k order and the final (c0 + c1) * scale are
 // those of the key scan, so each logit equals the scan's bit for bit.
+template <int W>
 __device__ void reemit(const FinishArgs& a, int b, int h, int g, int G, int64_t L, int ebin,
                        int rank, int nc) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -116,7 +119,7 @@ __device__ void reemit(const FinishArgs& a, int b, int h, int g, int G, int64_t 
   uint2* drow = a.dense + (int64_t)bh * a.dense_stride;
   const int64_t r0 = L * rank / nc, r1 = L * (rank + 1) / nc;
   const bool mine = tq == (hl >> 1);  // lanes holding head hl's column
-  for (int64_t base = r0 + 16 * wid; base < r1; base += 16 * kFinWarps) {
+  for (int64_t base = r0 + 16 * wid; base < r1; base += 16 * W) {
     const int64_t ia = base + gr, ib = base + gr + 8;
     uint4 W[4], X[4];
     const uint16_t* ka = a.kv.k + kv_row(a.kv, b, g, ia < r1 ? ia : r0);
@@ -159,12 +162,15 @@ __device__ void reemit(const FinishArgs& a, int b, int h, int g, int G, int64_t 
   }
 }
 
-template <int NC>
-__global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
+template <int NC, int W>
+__global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
+  constexpr int kFinWarps = W, kFinThreads = 32 * W;
+  constexpr int kBpt = kHistBins / kFinThreads;  // histogram bins per thread: 4 or 8
+  static_assert(kBpt % 4 == 0 && kFinThreads >= 2 * kD, "block shape");
   TraceScope trace(a.trace, kTrFinish);         // start, waited, threshold found, exit
   TraceScope phases(a.trace, kTrFinishPhases);  // start, decided, slice read, rows gathered
   extern __shared__ __align__(16) uint8_t fin_smem[];
-  FinShared& sh = *reinterpret_cast<FinShared*>(fin_smem);
+  FinShared<NC, W>& sh = *reinterpret_cast<FinShared<NC, W>*>(fin_smem);
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int rank = blockIdx.x;  // cluster rank (the cluster spans gridDim.x)
   const int bh = blockIdx.y;
@@ -223,19 +229,28 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
       const int margin = wide ? 4 : 2;
       const uint32_t tgt[2] = {(uint32_t)need, (uint32_t)(budget + 1 < P ? budget + 1 : P + 1)};
       const uint32_t* hh = a.hist + (int64_t)bh * kHistBins;
-      // thread t: bins 2047-4t-r, r < 4 (from the top)
-      const uint4 x = __ldcg(reinterpret_cast<const uint4*>(hh + kHistBins - 4 - 4 * tid));
-      const uint32_t c[4] = {x.w, x.z, x.y, x.x};
-      const uint32_t mine = c[0] + c[1] + c[2] + c[3];
+      // thread t: bins 2047-kBpt*t-r, r < kBpt (from the top)
+      uint32_t c[kBpt], mine = 0;
+#pragma unroll
+      for (int q = 0; q < kBpt / 4; ++q) {
+        const uint4 x = __ldcg(
+            reinterpret_cast<const uint4*>(hh + kHistBins - 4 * (q + 1) - kBpt * tid));
+        c[4 * q] = x.w;
+        c[4 * q + 1] = x.z;
+        c[4 * q + 2] = x.y;
+        c[4 * q + 3] = x.x;
+      }
+#pragma unroll
+      for (int r = 0; r < kBpt; ++r) mine += c[r];
       if (tid == 0) sh.scal[0] = sh.scal[1] = -1;
       int tot;
-      const uint32_t excl = (uint32_t)fin_scan((int)mine, sh, &tot);
+      const uint32_t excl = (uint32_t)fin_scan<W>((int)mine, sh, &tot);
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         uint32_t acc = excl;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          if (acc < tgt[k] && acc + c[r] >= tgt[k]) sh.scal[k] = kHistBins - 1 - 4 * tid - r;
+        for (int r = 0; r < kBpt; ++r) {
+          if (acc < tgt[k] && acc + c[r] >= tgt[k]) sh.scal[k] = kHistBins - 1 - kBpt * tid - r;
           acc += c[r];
         }
       }
@@ -271,7 +286,7 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
       __threadfence();
     }
     cluster_sync_all();
-    reemit(a, b, h, g, G, L, ebin, rank, NC);
+    reemit<W>(a, b, h, g, G, L, ebin, rank, NC);
     __threadfence();
     cluster_sync_all();
   }
@@ -309,7 +324,7 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
         }
       }
       int tot;
-      const int off = fin_scan((__popc(selm) << 16) | __popc(cndm), sh, &tot);
+      const int off = fin_scan<W>((__popc(selm) << 16) | __popc(cndm), sh, &tot);
       int i1 = nmy + (off >> 16), i2 = nmc + (off & 0xffff);
 #pragma unroll
       for (int u = 0; u < kFinU; ++u) {
@@ -391,7 +406,7 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
     const int64_t c1 = n * (c + 1) / NC;
     return __ldcg(spill + (c1 - 1 - (i - kMyCap)));
   };
-  {  // eight remote loads in flight per thread before any is stored
+  if constexpr (NC > 1) {  // eight remote loads in flight per thread before any is stored
     constexpr int kCopyU = 8;
     const int lim = ncand < kAllCap ? ncand : kAllCap;
     for (int jb = 0; jb < lim; jb += kFinThreads * kCopyU) {
@@ -410,7 +425,11 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
   }
   __syncthreads();
   auto cand_at = [&](int jc) -> uint64_t {
-    return jc < kAllCap ? sh.cand[jc] : cand_remote(jc);
+    if constexpr (NC == 1) {  // a single CTA reads its own list in place
+      return jc < kMyCap ? sh.mycand[jc] : __ldcg(spill + (n - 1 - (jc - kMyCap)));
+    } else {
+      return jc < kAllCap ? sh.cand[jc] : cand_remote(jc);
+    }
   };
 
   // ---- 2. the threshold among the candidates (same result in every CTA) ----
@@ -441,23 +460,23 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
           if ((v & mask) == prefix) atomicAdd(&sh.hist[(uint32_t)(v >> shift) & dmask], 1u);
         }
         __syncthreads();
-        // thread t: bins nb-1-4t-r (from the top); digits past nb are empty
+        // thread t: bins nb-1-kBpt*t-r (from the top); digits past nb are empty
         const int nb = 1 << db;
-        uint32_t c[4], mine = 0;
+        uint32_t c[kBpt], mine = 0;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int bin = nb - 1 - 4 * tid - r;
+        for (int r = 0; r < kBpt; ++r) {
+          const int bin = nb - 1 - kBpt * tid - r;
           c[r] = bin >= 0 ? sh.hist[bin] : 0u;
           mine += c[r];
         }
         int tot;
-        const uint32_t excl = (uint32_t)fin_scan((int)mine, sh, &tot);
+        const uint32_t excl = (uint32_t)fin_scan<W>((int)mine, sh, &tot);
         if (excl < (uint32_t)rem && excl + mine >= (uint32_t)rem) {
           uint32_t acc = excl;
 #pragma unroll
-          for (int r = 0; r < 4; ++r) {
+          for (int r = 0; r < kBpt; ++r) {
             if (acc < (uint32_t)rem && acc + c[r] >= (uint32_t)rem) {
-              sh.scal[2] = nb - 1 - 4 * tid - r;  // threshold digit d*
+              sh.scal[2] = nb - 1 - kBpt * tid - r;  // threshold digit d*
               sh.scal[3] = (int)acc;              // candidates above it
               sh.scal[4] = (int)c[r];             // candidates equal to it
             }
@@ -506,44 +525,65 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
   float o[2][8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) o[0][e] = o[1][e] = 0.f;
-  for (int base = w0; base < w1; base += 32) {
-    float z = -INFINITY;
-    int pos = 0, set = 0;
-    bool lv = false;
-    const int j = base + lane;
-    if (j < w1) {
-      if (j < nw) {  // window row: its logit is loaded after the V loads issue
-        pos = (int)window_pos(j, L, a.n_init, a.n_recent);
-        lv = true;
-      } else if (j < nw + nabove) {
-        const int k = j - (int)nw;
-        int c = 0;
+  // row j of the cluster's index space: position, logit, set (0 window, 1
+  // selected) and whether it is attended (an unselected candidate is not)
+  auto row_meta = [&](int j, int& pos, float& z, int& set, bool& lv) {
+    z = -INFINITY;
+    pos = 0;
+    set = 0;
+    lv = false;
+    if (j >= w1) return;
+    if (j < nw) {  // window row: its logit is loaded after the V loads issue
+      pos = (int)window_pos(j, L, a.n_init, a.n_recent);
+      lv = true;
+    } else if (j < nw + nabove) {
+      const int k = j - (int)nw;
+      int c = 0;
 #pragma unroll
-        for (int q = 1; q < NC; ++q) c += k >= sh.aoff[q] ? 1 : 0;
-        const int li = k - sh.aoff[c];
-        if (li < kSelCap) {
-          const uint64_t pr = c == rank ? *reinterpret_cast<const uint64_t*>(&sh.sel[li])
-                                        : ld_dsmem_u64(reinterpret_cast<const uint64_t*>(&sh.sel[li]),
-                                                       (uint32_t)c);
-          pos = (int)(uint32_t)pr;
-          z = __uint_as_float((uint32_t)(pr >> 32));
-        } else {
-          const uint64_t v = __ldcg(spill + n * c / NC + (li - kSelCap));
-          pos = (int)rank_pos(v);
-          z = key2f((uint32_t)(v >> 32));
-        }
-        set = 1;
-        lv = true;
+      for (int q = 1; q < NC; ++q) c += k >= sh.aoff[q] ? 1 : 0;
+      const int li = k - sh.aoff[c];
+      if (li < kSelCap) {
+        const uint64_t pr = c == rank ? *reinterpret_cast<const uint64_t*>(&sh.sel[li])
+                                      : ld_dsmem_u64(reinterpret_cast<const uint64_t*>(&sh.sel[li]),
+                                                     (uint32_t)c);
+        pos = (int)(uint32_t)pr;
+        z = __uint_as_float((uint32_t)(pr >> 32));
       } else {
-        const uint64_t v = cand_at(j - (int)nw - nabove);
-        if (cand_selected(v)) {
-          pos = (int)rank_pos(v);
-          z = key2f((uint32_t)(v >> 32));
-          lv = true;
-        }
-        set = 1;
+        const uint64_t v = __ldcg(spill + n * c / NC + (li - kSelCap));
+        pos = (int)rank_pos(v);
+        z = key2f((uint32_t)(v >> 32));
       }
+      set = 1;
+      lv = true;
+    } else {
+      const uint64_t v = cand_at(j - (int)nw - nabove);
+      if (cand_selected(v)) {
+        pos = (int)rank_pos(v);
+        z = key2f((uint32_t)(v >> 32));
+        lv = true;
+      }
+      set = 1;
     }
+  };
+  float nz;
+  int npos, nset;
+  bool nlv;
+  row_meta(w0 + lane, npos, nz, nset, nlv);
+  for (int base = w0; base < w1; base += 32) {
+    const float z0 = nz;
+    const int pos = npos, set = nset;
+    const bool lv = nlv;
+    const int j = base + lane;
+    // the next batch's row: fetch its description now and start its V row
+    // towards L2, so that the next batch's loads find it there
+    row_meta(base + 32 + lane, npos, nz, nset, nlv);
+    if (nlv) {
+      const uint16_t* vr =
+          a.kv.page_table ? vbase + kv_row(a.kv, b, g, npos) : vbase + (int64_t)npos * kD;
+      prefetch_l2(vr);
+      prefetch_l2(vr + kD / 2);
+    }
+    float z = z0;
     const unsigned live = __ballot_sync(0xffffffffu, lv);
     const unsigned sel1 = __ballot_sync(0xffffffffu, set == 1);
     uint4 vv[16];
@@ -708,7 +748,7 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
           uint64_t v = 0;
           const bool s = jc < ncand && cand_selected(v = cand_at(jc));
           int tot;
-          const int r = fin_scan(s ? 1 : 0, sh, &tot);
+          const int r = fin_scan<W>(s ? 1 : 0, sh, &tot);
           const int at = nabove + done + r;
           if (s && at < a.K) {
             if (oidx) oidx[at] = (int32_t)rank_pos(v);
@@ -732,15 +772,15 @@ __global__ void __launch_bounds__(kFinThreads, 1) finish_kernel(FinishArgs a) {
   }
   // Candidates past rank 0's copy are read from the other CTAs: keep them
   // resident until rank 0 has written the outputs (a uniform decision).
-  if (want_idx && cmode != 0 && ncand > kAllCap) cluster_sync_all();
+  if (NC > 1 && want_idx && cmode != 0 && ncand > kAllCap) cluster_sync_all();
 }
 
-template <int NC>
+template <int NC, int W>
 static cudaError_t launch_finish_t(const FinishArgs& a, cudaStream_t st) {
-  const size_t smem = sizeof(FinShared);
+  const size_t smem = sizeof(FinShared<NC, W>);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(NC, a.B * a.Hq);
-  cfg.blockDim = dim3(kFinThreads);
+  cfg.blockDim = dim3(32 * W);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
@@ -756,20 +796,21 @@ static cudaError_t launch_finish_t(const FinishArgs& a, cudaStream_t st) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(finish_kernel<NC>,
+    cudaError_t e = cudaFuncSetAttribute(finish_kernel<NC, W>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  return cudaLaunchKernelEx(&cfg, finish_kernel<NC>, a);
+  return cudaLaunchKernelEx(&cfg, finish_kernel<NC, W>, a);
 }
 
-// Cluster size: the largest of 8, 4, 2 whose CTAs for every head (one CTA
-// per SM: the kernel holds ~200 registers per thread) fill at most 85 % of
-// the SMs.  A cluster must sit in one GPC, so a nearly full device places
-// fewer large clusters than its SM count suggests: 32 clusters of 8 CTAs at
-// two per SM left two clusters for a second wave.  1 when even pairs would
-// exceed that (many heads: every head in one CTA).
+// Cluster size: the largest of 8, 4, 2 whose CTAs for every head (one CTA of
+// 16 warps per SM: 512 threads x 128 registers) fill at most 85 % of the SMs.
+// A cluster must sit in one GPC, so a nearly full device places fewer large
+// clusters than its SM count suggests: 32 clusters of 8 CTAs at two per SM
+// left two clusters for a second wave.  With more heads than that every head
+// is one CTA of 16 warps (two CTAs of 8 warps per SM were measured slower:
+// the gather is bound by each warp's rows in flight).
 cudaError_t launch_finish(const FinishArgs& a, cudaStream_t st) {
   static int sms[64] = {0};
   int dev = 0;
@@ -782,10 +823,10 @@ cudaError_t launch_finish(const FinishArgs& a, cudaStream_t st) {
   }
   const int64_t heads = (int64_t)a.B * a.Hq;
   const int64_t slots = (int64_t)sms[dev] * 85 / 100;
-  if (heads * 8 <= slots) return launch_finish_t<8>(a, st);
-  if (heads * 4 <= slots) return launch_finish_t<4>(a, st);
-  if (heads * 2 <= slots) return launch_finish_t<2>(a, st);
-  return launch_finish_t<1>(a, st);
+  if (heads * 8 <= slots) return launch_finish_t<8, 16>(a, st);
+  if (heads * 4 <= slots) return launch_finish_t<4, 16>(a, st);
+  if (heads * 2 <= slots) return launch_finish_t<2, 16>(a, st);
+  return launch_finish_t<1, 16>(a, st);
 }
 
 }  // namespace tsa
