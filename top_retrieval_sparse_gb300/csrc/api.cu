@@ -117,7 +117,7 @@ DecodeLayout decode_layout(int B, int Hq, int Hkv, int64_t l_cap, int n_init, in
   L.status = o; o = up(o + 4);
   L.tile_ctr = o; o = up(o + 4);
   L.hist = o; o = up(o + rows * kHistBins * 4);
-  L.dense_n = o; o = up(o + rows * 4);
+  L.dense_n = o; o = up(o + rows * kCtrStride * 4);
   L.zero_end = o;
   L.hint_bin = o; o = up(o + rows * 4);
   L.wz = o; o = up(o + rows * (size_t)L.wz_stride * 4);
@@ -404,7 +404,7 @@ RetopkLayout retopk_layout(const tsa_retopk* s) {
   L.status = o; o = up(o + 4);
   L.tile_ctr = o; o = up(o + 4);
   L.hist = o; o = up(o + H * kHistBins * 4);
-  L.dense_n = o; o = up(o + H * 4);
+  L.dense_n = o; o = up(o + H * kCtrStride * 4);
   L.zero_end = o;
   L.hint_bin = o; o = up(o + H * 4);
   L.wz = o; o = up(o + 64);  // no window on this path

@@ -148,7 +148,7 @@ __device__ void reemit(const FinishArgs& a, int b, int h, int g, int G, int64_t 
     const int cnt = __popc(ma) + __popc(mb);
     if (!cnt) continue;
     int64_t slot0 = 0;
-    if (lane == 0) slot0 = atomicAdd(a.dense_n + bh, cnt);
+    if (lane == 0) slot0 = atomicAdd(a.dense_n + (int64_t)bh * kCtrStride, cnt);
     slot0 = __shfl_sync(0xffffffffu, slot0, 0);
     const unsigned lt = (1u << lane) - 1u;
     if (ea) {
@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   // The list size, the hint word and the histogram are read together, and
   // the first batch of this CTA's slice of the list is in flight while the
   // threshold bin is found (it is discarded if the list is re-emitted).
-  int64_t n = need > 0 ? __ldcg(a.dense_n + bh) : 0;
+  int64_t n = need > 0 ? __ldcg(a.dense_n + (int64_t)bh * kCtrStride) : 0;
   if (n > a.dense_stride) n = a.dense_stride;
   int64_t s0 = n * rank / NC, s1 = n * (rank + 1) / NC;
   uint2 pre[kFinU];
@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   if (redo) {  // uniform over the cluster
     cluster_sync_all();  // every CTA has read the old list size
     if (rank == 0 && tid == 0) {
-      a.dense_n[bh] = 0;
+      a.dense_n[(int64_t)bh * kCtrStride] = 0;
       __threadfence();
     }
     cluster_sync_all();
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   int nmy = 0, nmc = 0;
   if (need > 0) {
     if (redo) {  // the list was re-emitted: new size, new slice
-      n = __ldcg(a.dense_n + bh);
+      n = __ldcg(a.dense_n + (int64_t)bh * kCtrStride);
       if (n > a.dense_stride) n = a.dense_stride;
       s0 = n * rank / NC;
       s1 = n * (rank + 1) / NC;
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
     uint4* hz = reinterpret_cast<uint4*>(a.hist + (int64_t)bh * kHistBins);
     for (int q = tid; q < kHistBins / 4; q += kFinThreads) hz[q] = make_uint4(0u, 0u, 0u, 0u);
     if (tid == 0) {
-      a.dense_n[bh] = 0;
+      a.dense_n[(int64_t)bh * kCtrStride] = 0;
       if (bh == 0) {
         *a.tile_ctr = 0;
         *a.status = 0;

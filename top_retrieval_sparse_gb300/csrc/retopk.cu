@@ -227,7 +227,7 @@ __device__ void rescore_chunk(const RetopkRescoreArgs& a, int h) {
   const int G = a.Hq / a.kv.Hkv;
   const int g = h / G;
   const int M = a.mcand[h] < a.cand_cap ? a.mcand[h] : a.cand_cap;
-  if (blockIdx.x == 0 && tid == 0) a.dense_n[h] = M;
+  if (blockIdx.x == 0 && tid == 0) a.dense_n[(int64_t)h * kCtrStride] = M;
   const uint32_t* crow = a.cand + (int64_t)h * a.cand_cap;
   uint2* drow = a.dense + (int64_t)h * a.dense_stride;
   uint32_t* hh = a.hist + (int64_t)h * kHistBins;

@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
               // runs of 8 within a static range; a dynamic tile is a visit of
               // its own: it rounds its pairs up to a 32-byte sector only
               const int size = t < stat ? (over + 7) & ~7 : (over + 3) & ~3;
-              p2 = atomicAdd(&a.dense_n[head0 + lane], size);
+              p2 = atomicAdd(&a.dense_n[(int64_t)(head0 + lane) * kCtrStride], size);
               run_ptr = p2 + over;
               run_left = size - over;
             } else {

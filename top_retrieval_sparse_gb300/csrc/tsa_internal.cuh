@@ -18,6 +18,10 @@ constexpr int kHistBins = 1 << kHistBits;
 constexpr int kHistShift = 32 - kHistBits;
 constexpr int kMaxGroup = 8;                    // query heads per KV head
 constexpr int kMaxUnits = 512;                  // B * Hkv limit of one call
+// Each head's pair-list fill counter sits in its own 128-byte line: the
+// slot atomics of all heads then spread over the L2 slices instead of
+// queueing in one.
+constexpr int kCtrStride = 32;
 constexpr long long kWaitLimitNs = 1000000000;  // bounded waits: 1 s
 
 // Per-head hint word kept in the workspace between calls: bits 0-15 the bin

@@ -34,7 +34,7 @@ struct ScanArgs {
   uint32_t* tile_ctr;        // (zeroed) dynamic tile claims
   int32_t* hint_bin;         // [B][Hq] emission bins, persistent across calls (any value is safe)
   uint2* dense;              // [B][Hq][dense_stride] (position, logit bits)
-  int32_t* dense_n;          // [B][Hq] (zeroed) slots allocated (pairs + sentinels)
+  int32_t* dense_n;          // [B][Hq] x kCtrStride (zeroed) slots allocated (pairs + sentinels)
   int64_t dense_stride;      // >= l_cap + slack for the padding
   float* wz;                 // [B][Hq][wz_stride] window logits
   int wz_stride;
@@ -130,7 +130,7 @@ struct RetopkRescoreArgs {
   const int32_t* mcand;      // [Hq] |A_t|
   int cand_cap, chunk;
   uint2* dense;              // [Hq][dense_stride]
-  int32_t* dense_n;          // [Hq]
+  int32_t* dense_n;          // [Hq] x kCtrStride
   int64_t dense_stride;
   uint32_t* hist;            // [Hq][kHistBins] (zero on entry)
   TraceBuf trace;
