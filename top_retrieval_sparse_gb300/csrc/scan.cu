@@ -128,13 +128,16 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
   }
   __syncthreads();
 
-  // Contiguous static ranges over the first 85 % of the tiles; the rest is
+  // Contiguous static ranges; with many tiles per CTA the last 10 % are
   // claimed one tile at a time (global counter) by whichever CTA is free
   // first, so that CTAs whose share of HBM bandwidth is smaller end no later.
+  // A claimed tile is usually a unit switch of its own (a histogram flush),
+  // which costs more than it balances when each CTA has few tiles (measured:
+  // fully static is fastest at 27 tiles per CTA, 10 % at 216).
   const int total = unit_tiles[nunits];
   if (total == 0) return;
   const int grid = gridDim.x;
-  const int dyn = total >= 4 * grid ? total * 3 / 20 : 0;
+  const int dyn = total >= 64 * grid ? total / 10 : 0;
   const int stat = total - dyn;
   const int t_begin = (int)((int64_t)stat * blockIdx.x / grid);
   const int t_end = (int)((int64_t)stat * (blockIdx.x + 1) / grid);
