@@ -275,8 +275,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
         const int hl = w / kHistWords;
         uint32_t* gh = a.hist + (int64_t)(b * a.Hq + g * G + hl) * kHistBins +
                        2 * (w % kHistWords);
-        if (v & 0xffffu) atomicAdd(gh, v & 0xffffu);
-        if (v >> 16) atomicAdd(gh + 1, v >> 16);
+        // both bins of the word in one 64-bit atomic: a bin's count stays
+        // below 2^31, so the low half never carries into the high one
+        atomicAdd(reinterpret_cast<unsigned long long*>(gh),
+                  (unsigned long long)(v & 0xffffu) | ((unsigned long long)(v >> 16) << 32));
         hist[w] = 0;
       }
     }
