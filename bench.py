@@ -434,7 +434,7 @@ def run_retopk(args, ws, rank, local):
                   if exact_steps else None,
                   "us_all_reuse_steps": round(statistics.median([per[t] for t in reuse_steps]), 2)
                   if reuse_steps else None},
-        "roofline": {"kernel": "whole reuse step (selector, rescore, attend)", "bound": "hbm",
+        "roofline": {"kernel": "whole reuse step (selector, key scan with no exact head, finish)", "bound": "hbm",
                      "achieved": round(reuse_bytes / (statistics.median([per[t] for t in reuse_steps])
                                                       * 1e-6) / 1e9, 1) if reuse_steps else None,
                      "peak": peaks()[0], "peak_kind": peaks()[1], "unit": "GB/s",
@@ -464,7 +464,7 @@ def run_trace(args, step, tsa, torch, dev, nsteps=3):
     torch.cuda.synchronize()
     tsa.set_trace(None)
     recs = tsa.read_trace(buf)
-    names = {1: "scan", 4: "retopk_selector", 5: "retopk_rescore", 7: "finish",
+    names = {1: "scan", 4: "retopk_selector", 7: "finish",
              8: "finish_phases"}
     # records of one launch share the kernel id; a launch of a kernel starts
     # after the previous launch of that kernel has ended

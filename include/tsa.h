@@ -98,10 +98,10 @@ TSA_API unsigned long long tsa_kernel_launches(void);
 /* Per-stage timing (optional, thread-local).  With n >= 4 cudaEvent_t
  * handles (cast to void*), every later sparse_attn_decode / retopk_step call
  * on this thread records, on the call's stream, events[0] before its first
- * kernel, events[1] after the key scan, events[2] after the ReTopK
- * rescoring (sparse_attn_decode has none: its events[2] follows events[1]
- * at once) and events[3] after the finish kernel (selection, attention and
- * merge).  Events between kernels cost the overlap of their
+ * kernel, events[1] after the key scan, events[2] at once after events[1]
+ * (the selection is the finish kernel's) and events[3] after the finish
+ * kernel (selection, attention and merge; on ReTopK steps also the reuse
+ * heads' rescoring and the FIFO push).  Events between kernels cost the overlap of their
  * launches.  events == NULL (or n == 0) turns it off.  The events stay owned
  * by the caller. */
 TSA_API int tsa_set_stage_events(void* const* events, int n);
@@ -109,9 +109,8 @@ TSA_API int tsa_set_stage_events(void* const* events, int n);
 /* Per-CTA kernel timeline (optional, thread-local).  `buf` is device memory
  * (64-byte aligned) holding a uint32 record count at offset 0, which the
  * caller zeroes, followed from offset 64 by records of 48 bytes:
- *   uint32 kernel (1 key scan, 4 ReTopK selector, 5 ReTopK rescore,
- *   7 finish (selection + attention), 8 finish phases; 2, 3 and 6 are
- *   unused), uint32 CTA
+ *   uint32 kernel (1 key scan, 4 ReTopK selector, 7 finish (selection +
+ *   attention), 8 finish phases; 2, 3, 5 and 6 are unused), uint32 CTA
  *   (linear block index), uint32 SM id, uint32 info (kernel 7: pairs the
  *   scan emitted for the head; kernel 8: bit 31 re-emission, bits 16-30
  *   the threshold bin, bits 0-15 the emission bin used; else 0),

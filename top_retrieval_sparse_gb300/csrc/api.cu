@@ -590,30 +590,10 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
                                scan_grid(1, view, len), s, true))) != cudaSuccess)
     return cuda_fail(e, "scan launch");
   if ((e = stage_mark(1, s)) != cudaSuccess) return cuda_fail(e, "event record");
-  // 3. reuse-path heads: e_i on A_t as pairs + histogram, the scan's format
-  {
-    RetopkRescoreArgs a{};
-    a.q = static_cast<const uint16_t*>(q);
-    a.kv = view;
-    a.Hq = Hq;
-    a.scale = scale;
-    a.path = path;
-    a.cand = reinterpret_cast<const uint32_t*>(ws + Lw.cand);
-    a.mcand = reinterpret_cast<const int32_t*>(ws + Lw.mcand);
-    a.cand_cap = Lw.cand_cap;
-    a.chunk = 256;
-    a.dense = w.dense;
-    a.dense_n = w.dense_n;
-    a.dense_stride = w.dense_stride;
-    a.hist = w.hist;
-    a.trace = g_trace;
-    const int chunks = (Lw.cand_cap + a.chunk - 1) / a.chunk;
-    if ((e = counted(launch_retopk_rescore(a, chunks, s))) != cudaSuccess)
-      return cuda_fail(e, "retopk rescore launch");
-  }
   if ((e = stage_mark(2, s)) != cudaSuccess) return cuda_fail(e, "event record");
-  // 4. every head: exact top-K of its pairs, softmax.V over S_t (no window),
-  //    and the FIFO push of (qbar_t, S_t) -- S_t is written into the slot
+  // 3. every head: exact top-K (of its pairs; a reuse head rescores A_t
+  //    itself), softmax.V over S_t (no window), and the FIFO push of
+  //    (qbar_t, S_t) -- S_t is written into the slot
   {
     FinishArgs f = finish_args(static_cast<const uint16_t*>(q), view, Hq, scale, st->K, w);
     f.lens = nullptr;
@@ -628,6 +608,8 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
     f.topk_stride = (int64_t)st->C * st->K;
     f.path = path;
     f.mcand = reinterpret_cast<const int32_t*>(ws + Lw.mcand);
+    f.cand = reinterpret_cast<const uint32_t*>(ws + Lw.cand);
+    f.cand_cap = Lw.cand_cap;
     f.push_qbar = qbar_new;
     f.cache_qbar = st->qbar;
     f.cache_sup_n = st->sup_n;

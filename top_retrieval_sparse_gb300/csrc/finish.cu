@@ -29,9 +29,11 @@
 //      half-warp 16-byte loads, keeping (max, sum, o) per set in base 2;
 //      every CTA pushes its partials into rank 0's shared memory, and rank
 //      0 applies Eq. 4-5.
-// ReTopK steps use the same kernel: a reuse head's list holds its rescored
-// candidates A_t (all of them: no hint, no re-emission), no head has a
-// window, and rank 0 pushes (qbar_t, S_t) into the query-support FIFO.
+// ReTopK steps use the same kernel: a reuse head has no pair list; each CTA
+// rescores its share of the head's candidates A_t (exact logits e_i on the
+// key rows) and all of them compete in the radix (no histogram, no hint); no
+// head has a window, and rank 0 pushes (qbar_t, S_t) into the query-support
+// FIFO.
 // Launched as a programmatic dependent of the kernel that wrote the lists.
 #include "tsa_internal.cuh"
 #include "tsa_kernels.h"
@@ -162,7 +164,62 @@ __device__ void reemit(const FinishArgs& a, int b, int h, int g, int G, int64_t 
   }
 }
 
-template <int NC, int W>
+// A ReTopK reuse head's logits on its candidates [c0, c1) of A_t, as rank
+// keys into this CTA's candidate list (shared memory, then the top of the
+// slice's spill area).  A warp takes 32 candidates at a time: lane l holds
+// candidate base + l's position; key rows are read by half-warps (16 lanes x
+// 16 bytes), two rows per load, all 16 loads in flight before any is used.
+template <int W, class Sh>
+__device__ void reuse_logits(const FinishArgs& a, int b, int bh, int g, int64_t c0, int64_t c1,
+                             Sh& sh, uint64_t* spill) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int half = lane >> 4, col = 8 * (lane & 15);
+  const uint4 qw = *reinterpret_cast<const uint4*>(a.q + (int64_t)bh * kD + col);
+  const float qv[8] = {bf_lo(qw.x), bf_hi(qw.x), bf_lo(qw.y), bf_hi(qw.y),
+                       bf_lo(qw.z), bf_hi(qw.z), bf_lo(qw.w), bf_hi(qw.w)};
+  const uint32_t* crow = a.cand + (int64_t)bh * a.cand_cap;
+  for (int64_t base = c0 + 32 * wid; base < c1; base += 32 * W) {
+    const int64_t j = base + lane;
+    const uint32_t pos = j < c1 ? crow[j] : 0u;
+    uint4 kv4[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const int r = 2 * k + half;
+      const uint32_t pk = __shfl_sync(0xffffffffu, pos, r);
+      kv4[k] = base + r < c1 ? *reinterpret_cast<const uint4*>(a.kv.k + kv_row(a.kv, b, g, pk) + col)
+                             : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float mine = 0.f;  // lane l ends with the logit of candidate base + l
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const uint4 w = kv4[k];
+      float acc = qv[0] * bf_lo(w.x);
+      acc = fmaf(qv[1], bf_hi(w.x), acc);
+      acc = fmaf(qv[2], bf_lo(w.y), acc);
+      acc = fmaf(qv[3], bf_hi(w.y), acc);
+      acc = fmaf(qv[4], bf_lo(w.z), acc);
+      acc = fmaf(qv[5], bf_hi(w.z), acc);
+      acc = fmaf(qv[6], bf_lo(w.w), acc);
+      acc = fmaf(qv[7], bf_hi(w.w), acc);
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      // lanes 0-15 hold row 2k's logit, lanes 16-31 row 2k+1's
+      const float e0 = __shfl_sync(0xffffffffu, acc, 0), e1 = __shfl_sync(0xffffffffu, acc, 16);
+      if (lane == 2 * k) mine = e0;
+      if (lane == 2 * k + 1) mine = e1;
+    }
+    if (j < c1) {
+      const uint64_t v = rank_key(mine * a.scale, pos);
+      const int64_t i = j - c0;
+      if (i < kMyCap) sh.mycand[i] = v;
+      else spill[c1 - 1 - (i - kMyCap)] = v;
+    }
+  }
+}
+
+// RT: a ReTopK step (reuse heads, the FIFO push); the decode instantiation
+// carries none of that code.
+template <int NC, int W, bool RT>
 __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   constexpr int kFinWarps = W, kFinThreads = 32 * W;
   constexpr int kBpt = kHistBins / kFinThreads;  // histogram bins per thread: 4 or 8
@@ -195,8 +252,8 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   const int64_t L = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
   const int64_t nw = window_count(L, a.n_init, a.n_recent);
   // a ReTopK reuse head selects among its |A_t| rescored candidates
-  const bool reuse = a.path != nullptr && a.path[bh] == 0;
-  const int64_t P = reuse ? (int64_t)a.mcand[bh] : L - nw;
+  const bool reuse = RT && a.path[bh] == 0;
+  const int64_t P = reuse ? (int64_t)(a.mcand[bh] < a.cand_cap ? a.mcand[bh] : a.cand_cap) : L - nw;
   const int need = (int64_t)a.K < P ? a.K : (int)P;
   uint64_t* spill = a.spill + (int64_t)bh * a.dense_stride;
   const uint2* lrow = a.dense + (int64_t)bh * a.dense_stride;
@@ -218,9 +275,9 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   // Every CTA of the cluster reads the head's histogram and decides alike.
   int bstar = -1, redo = 0, ebin = 0, next_hint = 0;
   bool wide = false;
-  if (need > 0) {
+  if (need > 0 && !reuse) {  // (a reuse head has no histogram: all its candidates compete)
     const int32_t hw = __ldcg(a.hint_bin + bh);
-    const int used = reuse ? 0 : hint_bin_of(hw);  // a reuse head's list holds every candidate
+    const int used = hint_bin_of(hw);
     wide = hint_wide_of(hw);
     if (need < P) {
       // pairs one call may emit, and the margin (bins below b*) the hint
@@ -342,6 +399,15 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
       nmc += tot & 0xffff;
     }
   }
+  if (need > 0 && reuse) {  // this CTA's share of A_t, rescored: every one a candidate
+    const int m = a.mcand[bh] < a.cand_cap ? a.mcand[bh] : a.cand_cap;
+    n = m;  // the candidate index space (spill layout as for a list slice)
+    s0 = n * rank / NC;
+    s1 = n * (rank + 1) / NC;
+    reuse_logits<W>(a, b, bh, g, s0, s1, sh, spill);
+    nmc = (int)(s1 - s0);
+    __syncthreads();
+  }
   if (tid == 0) {
     sh.cnt[0] = nmy;
     sh.cnt[1] = nmc;
@@ -437,14 +503,15 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   int cmode = 0;
   uint64_t T = 0;
   const int need_rem = need - nabove;
-  if (need > 0 && bstar >= 0 && need_rem > 0) {
+  if (need > 0 && (bstar >= 0 || reuse) && need_rem > 0) {
     if (need_rem >= ncand) {
       cmode = 1;
     } else {
       cmode = 2;
-      uint64_t prefix = (uint64_t)bstar << kRankShift;
-      uint64_t mask = (uint64_t)(kHistBins - 1) << kRankShift;
-      int shift = kRankShift, match = ncand, rem = need_rem;
+      // the candidates share b*'s 11 bits (a reuse head's: no known bits)
+      uint64_t prefix = reuse ? 0ull : (uint64_t)bstar << kRankShift;
+      uint64_t mask = reuse ? 0ull : (uint64_t)(kHistBins - 1) << kRankShift;
+      int shift = reuse ? 64 : kRankShift, match = ncand, rem = need_rem;
       while (true) {
         if (match <= rem) {  // everything still matching is selected
           T = prefix;
@@ -765,7 +832,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   }
   if (need > 0 && !reuse && rank == 0 && tid == 0)  // read by every CTA long before this point
     a.hint_bin[bh] = next_hint | ((wide || redo) ? 1 << 16 : 0);
-  if (a.push_qbar && rank == 0) {  // ReTopK: (qbar_t, S_t) over the oldest FIFO entry
+  if (RT && rank == 0) {  // ReTopK: (qbar_t, S_t) over the oldest FIFO entry
     const int64_t hc = (int64_t)bh * a.C + a.slot;
     if (tid < kD) a.cache_qbar[hc * kD + tid] = a.push_qbar[(int64_t)bh * kD + tid];
     if (tid == 0) a.cache_sup_n[hc] = need > 0 ? need : 0;
@@ -775,7 +842,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   if (NC > 1 && want_idx && cmode != 0 && ncand > kAllCap) cluster_sync_all();
 }
 
-template <int NC, int W>
+template <int NC, int W, bool RT>
 static cudaError_t launch_finish_t(const FinishArgs& a, cudaStream_t st) {
   const size_t smem = sizeof(FinShared<NC, W>);
   cudaLaunchConfig_t cfg = {};
@@ -796,12 +863,12 @@ static cudaError_t launch_finish_t(const FinishArgs& a, cudaStream_t st) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(finish_kernel<NC, W>,
+    cudaError_t e = cudaFuncSetAttribute(finish_kernel<NC, W, RT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  return cudaLaunchKernelEx(&cfg, finish_kernel<NC, W>, a);
+  return cudaLaunchKernelEx(&cfg, finish_kernel<NC, W, RT>, a);
 }
 
 // Cluster size: the largest of 8, 4, 2 whose CTAs for every head (one CTA of
@@ -823,10 +890,21 @@ cudaError_t launch_finish(const FinishArgs& a, cudaStream_t st) {
   }
   const int64_t heads = (int64_t)a.B * a.Hq;
   const int64_t slots = (int64_t)sms[dev] * 85 / 100;
-  if (heads * 8 <= slots) return launch_finish_t<8, 16>(a, st);
-  if (heads * 4 <= slots) return launch_finish_t<4, 16>(a, st);
-  if (heads * 2 <= slots) return launch_finish_t<2, 16>(a, st);
-  return launch_finish_t<1, 16>(a, st);
+  const int nc = heads * 8 <= slots ? 8 : heads * 4 <= slots ? 4 : heads * 2 <= slots ? 2 : 1;
+  if (a.path) {  // a ReTopK step
+    switch (nc) {
+      case 8: return launch_finish_t<8, 16, true>(a, st);
+      case 4: return launch_finish_t<4, 16, true>(a, st);
+      case 2: return launch_finish_t<2, 16, true>(a, st);
+      default: return launch_finish_t<1, 16, true>(a, st);
+    }
+  }
+  switch (nc) {
+    case 8: return launch_finish_t<8, 16, false>(a, st);
+    case 4: return launch_finish_t<4, 16, false>(a, st);
+    case 2: return launch_finish_t<2, 16, false>(a, st);
+    default: return launch_finish_t<1, 16, false>(a, st);
+  }
 }
 
 }  // namespace tsa

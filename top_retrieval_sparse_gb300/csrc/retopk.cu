@@ -7,10 +7,8 @@
 //           step; otherwise the R most similar entries (ties: older entry
 //           first), the union of their supports and the last W positions as a
 //           shared-memory bitmap, compacted in ascending order -> A_t, M_t.
-// rescore   (CTAs per reuse head): e_i = scale * q . k_i for i in A_t, reading
-//           K rows straight from the candidate positions (no gathered copy);
-//           the last CTA of the head (ticket) keeps the top-K of A_t by
-//           (e desc, position asc) with a CTA radix select.
+// The indexed QK on A_t, the candidate top-K and the sparse softmax.V are
+// the finish kernel's (finish.cu), for reuse heads as for exact ones.
 // init      fills the FIFO from the last C prefill queries and their supports.
 #include "tsa_internal.cuh"
 #include "tsa_kernels.h"
@@ -18,7 +16,6 @@
 namespace tsa {
 
 constexpr int kSelectorThreads = 256;
-constexpr int kRescoreThreads = 256;
 constexpr int kMaxC = 64;
 
 __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(RetopkSelArgs a) {
@@ -217,92 +214,6 @@ cudaError_t launch_retopk_selector(const RetopkSelArgs& a, size_t smem, cudaStre
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, retopk_selector_kernel, a);
-}
-
-// --------------------------------------------------------------- rescore
-// One chunk of head h's candidates: (position, logit) pairs into the head's
-// list, and the histogram of their keys.
-__device__ void rescore_chunk(const RetopkRescoreArgs& a, int h) {
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int G = a.Hq / a.kv.Hkv;
-  const int g = h / G;
-  const int M = a.mcand[h] < a.cand_cap ? a.mcand[h] : a.cand_cap;
-  if (blockIdx.x == 0 && tid == 0) a.dense_n[(int64_t)h * kCtrStride] = M;
-  const uint32_t* crow = a.cand + (int64_t)h * a.cand_cap;
-  uint2* drow = a.dense + (int64_t)h * a.dense_stride;
-  uint32_t* hh = a.hist + (int64_t)h * kHistBins;
-
-  // query slice of this lane's column block: 8 elements (half-warp rows)
-  const int half = lane >> 4, col = 8 * (lane & 15);
-  const uint4 qw = *reinterpret_cast<const uint4*>(a.q + (int64_t)h * kD + col);
-  const float qv[8] = {bf_lo(qw.x), bf_hi(qw.x), bf_lo(qw.y), bf_hi(qw.y),
-                       bf_lo(qw.z), bf_hi(qw.z), bf_lo(qw.w), bf_hi(qw.w)};
-  // a warp takes 32 candidates at a time: lane l fetches candidate base + l's
-  // position; key rows are read by half-warps (16 lanes x 16 bytes), two
-  // rows per load, all 16 loads in flight before any is used
-  const int c0 = blockIdx.x * a.chunk;
-  const int c1 = c0 + a.chunk < M ? c0 + a.chunk : M;
-  for (int base = c0 + 32 * wid; base < c1; base += 32 * (kRescoreThreads / 32)) {
-    const int j = base + lane;
-    const uint32_t pos = j < c1 ? crow[j] : 0u;
-    uint4 kv4[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const int r = 2 * k + half;
-      const uint32_t pk = __shfl_sync(0xffffffffu, pos, r);
-      kv4[k] = base + r < c1
-                   ? *reinterpret_cast<const uint4*>(a.kv.k + kv_row(a.kv, 0, g, pk) + col)
-                   : make_uint4(0u, 0u, 0u, 0u);
-    }
-    float mine = 0.f;  // lane l ends with the logit of row base + l
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const uint4 w = kv4[k];
-      float acc = qv[0] * bf_lo(w.x);
-      acc = fmaf(qv[1], bf_hi(w.x), acc);
-      acc = fmaf(qv[2], bf_lo(w.y), acc);
-      acc = fmaf(qv[3], bf_hi(w.y), acc);
-      acc = fmaf(qv[4], bf_lo(w.z), acc);
-      acc = fmaf(qv[5], bf_hi(w.z), acc);
-      acc = fmaf(qv[6], bf_lo(w.w), acc);
-      acc = fmaf(qv[7], bf_hi(w.w), acc);
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      // lanes 0-15 hold row 2k's logit, lanes 16-31 row 2k+1's
-      const float e0 = __shfl_sync(0xffffffffu, acc, 0), e1 = __shfl_sync(0xffffffffu, acc, 16);
-      if (lane == 2 * k) mine = e0;
-      if (lane == 2 * k + 1) mine = e1;
-    }
-    if (j < c1) {
-      const float z = mine * a.scale;
-      drow[j] = make_uint2(pos, __float_as_uint(z));
-      atomicAdd(&hh[f2key(z) >> kHistShift], 1u);
-    }
-  }
-}
-
-// Path and candidates come from the selector: the key scan before this
-// kernel waited for it, so they are read once the scan has completed.
-__global__ void __launch_bounds__(kRescoreThreads) retopk_rescore_kernel(RetopkRescoreArgs a) {
-  TraceScope trace(a.trace, kTrRescore);
-  const int h = blockIdx.y;
-  pdl_wait();
-  pdl_trigger();
-  if (a.path[h] == 0) rescore_chunk(a, h);
-}
-
-cudaError_t launch_retopk_rescore(const RetopkRescoreArgs& a, int chunks, cudaStream_t st) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(chunks, a.Hq);
-  cfg.blockDim = dim3(kRescoreThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, retopk_rescore_kernel, a);
 }
 
 __global__ void retopk_init_kernel(RetopkInitArgs a) {

@@ -288,8 +288,8 @@ struct TraceScope {
     }
   }
 };
-enum TraceKernel : uint32_t {  // 2, 3 and 6 are retired ids
-  kTrScan = 1, kTrSelector = 4, kTrRescore = 5, kTrFinish = 7, kTrFinishPhases = 8
+enum TraceKernel : uint32_t {  // 2, 3, 5 and 6 are retired ids
+  kTrScan = 1, kTrSelector = 4, kTrFinish = 7, kTrFinishPhases = 8
 };
 
 // ------------------------------------------------------ warp/block utils

@@ -73,12 +73,15 @@ struct FinishArgs {
   int32_t* topk_idx;         // [B][Hq] rows of topk_stride, or nullptr
   float* topk_score;         // same layout, or nullptr
   int64_t topk_stride;       // elements between heads' output rows (K for decode)
-  // ReTopK (all nullptr for decode): heads with path == 0 select among their
-  // |A_t| = mcand rescored candidates (no hint, no re-emission); every head
-  // pushes (qbar_t, S_t) into FIFO slot `slot` (S_t is written through
-  // topk_idx, which then points at the slot's support rows)
+  // ReTopK (all nullptr for decode): heads with path == 0 rescore their
+  // |A_t| = mcand candidates cand (ascending positions, rows of cand_cap)
+  // and select among them (no histogram, no hint); every head pushes
+  // (qbar_t, S_t) into FIFO slot `slot` (S_t is written through topk_idx,
+  // which then points at the slot's support rows)
   const int32_t* path;
   const int32_t* mcand;
+  const uint32_t* cand;
+  int cand_cap;
   const float* push_qbar;    // [Hq][128]
   float* cache_qbar;         // [Hq][C][128]
   int32_t* cache_sup_n;      // [Hq][C]
@@ -114,28 +117,6 @@ struct RetopkSelArgs {
   TraceBuf trace;
 };
 cudaError_t launch_retopk_selector(const RetopkSelArgs& a, size_t smem, cudaStream_t st);
-
-// Rescore (reuse heads, path == 0): e_i = scale * q . k_i for every
-// candidate i of A_t, written as (position, logit) pairs to the head's dense
-// list (dense_n = |A_t|) and counted in its 11-bit histogram, the same
-// format the key scan produces for exact heads, so that one finish kernel
-// selects and attends for both kinds of head.
-struct RetopkRescoreArgs {
-  const uint16_t* q;
-  KvView kv;
-  int Hq;
-  float scale;
-  const int32_t* path;       // reuse heads are path == 0
-  const uint32_t* cand;      // [Hq][cand_cap] ascending positions
-  const int32_t* mcand;      // [Hq] |A_t|
-  int cand_cap, chunk;
-  uint2* dense;              // [Hq][dense_stride]
-  int32_t* dense_n;          // [Hq] x kCtrStride
-  int64_t dense_stride;
-  uint32_t* hist;            // [Hq][kHistBins] (zero on entry)
-  TraceBuf trace;
-};
-cudaError_t launch_retopk_rescore(const RetopkRescoreArgs& a, int chunks, cudaStream_t st);
 
 struct RetopkInitArgs {
   const uint16_t* prefill_q;     // [C][Hq][128]
