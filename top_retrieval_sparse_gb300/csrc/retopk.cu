@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
   __shared__ float rho[kMaxC];
   __shared__ float red[kSelectorThreads / 32];
   __shared__ int chosen[kMaxC];
+  __shared__ int chosen_n[kMaxC];  // support sizes of the recalled entries
   __shared__ int s_path;
   __shared__ uint32_t wtot[kSelectorThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -46,6 +47,9 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
   }
   __syncthreads();
   const float nrm = sqrtf(red[0]);
+  // the bitmap of step 4 is this CTA's shared memory: clear it now
+  const int nwords = (int)((a.L + 31) >> 5);
+  for (int w = tid; w < nwords; w += kSelectorThreads) bitmap[w] = 0u;
   // the cache and this step's buffers belong to the previous step's kernels
   // until they have completed; the key scan may be scheduled from here on
   pdl_wait();
@@ -105,7 +109,10 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
       const int age = (c - a.fifo_head + a.C) % a.C;
       beat += (r > rc || (r == rc && age < agec)) ? 1 : 0;
     }
-    if (beat < a.R) chosen[beat] = tid;  // ranks are distinct: one entry per rank
+    if (beat < a.R) {  // ranks are distinct: one entry per rank
+      chosen[beat] = tid;
+      chosen_n[beat] = a.cache_sup_n[(int64_t)h * a.C + tid];
+    }
   }
   __syncthreads();
   uint32_t* crow = a.cand + (int64_t)h * a.cand_cap;
@@ -121,27 +128,24 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
   }
 
   // 4. bitmap union of the recalled supports and the recent window
-  const int nwords = (int)((a.L + 31) >> 5);
-  for (int w = tid; w < nwords; w += kSelectorThreads) bitmap[w] = 0u;
-  __syncthreads();
   // the R recalled supports as one flat index space of R*K entries (entries
-  // past a support's size are skipped), several loads in flight per thread
+  // past a support's size are skipped), eight loads in flight per thread
   {
+    constexpr int kU = 8;
     const int64_t total = (int64_t)a.R * a.K;
-    for (int64_t j0 = tid; j0 < total; j0 += 4 * kSelectorThreads) {
-      int32_t pv[4];
+    for (int64_t j0 = tid; j0 < total; j0 += kU * kSelectorThreads) {
+      int32_t pv[kU];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kU; ++u) {
         const int64_t j = j0 + (int64_t)u * kSelectorThreads;
         pv[u] = -1;
         if (j < total) {
           const int r = (int)(j / a.K), i = (int)(j - (int64_t)r * a.K);
-          const int64_t hc = (int64_t)h * a.C + chosen[r];
-          if (i < a.cache_sup_n[hc]) pv[u] = a.cache_sup[hc * a.K + i];
+          if (i < chosen_n[r]) pv[u] = a.cache_sup[((int64_t)h * a.C + chosen[r]) * a.K + i];
         }
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < kU; ++u)
         if (pv[u] >= 0 && pv[u] < a.L) atomicOr(&bitmap[pv[u] >> 5], 1u << (pv[u] & 31));
     }
   }
