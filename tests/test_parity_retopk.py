@@ -112,6 +112,15 @@ def test_retopk_downsized_lockstep():
           "mean M_t", np.mean(st["mcand"]))
 
 
+def test_retopk_single_recall_keeps_whole_candidate_set():
+    """R = 1 and W = 0: A_t is one cached support, |A_t| <= K, so S_t = A_t
+    (every candidate selected; the radix is never needed)."""
+    wl = make_retopk(L0=4000, steps=12, K=48, C=4, R=1, W=0, T_r=1000, tau=-2.0)
+    st = run_lockstep(wl, 12)
+    assert st["reuse"] > 0
+    assert max(st["mcand"]) <= wl.K
+
+
 def test_retopk_fallback_mix():
     """A slow-moving walk with tau high enough that the fallback fires."""
     wl = make_retopk(L0=5000, steps=30, K=48, C=6, R=3, W=5, T_r=1000, tau=0.97)

@@ -43,7 +43,8 @@ namespace tsa {
 constexpr int kFinMaxCluster = 8;  // CTAs per head: 1, 2, 4 or 8 (chosen at launch)
 constexpr int kSelCap = 2048;   // this CTA's above-b* pairs in shared memory
 constexpr int kMyCap = 4096;    // this CTA's threshold-bin candidates in shared memory
-constexpr int kAllCap = 16384;  // the cluster's threshold-bin candidates, copied locally (NC > 1)
+constexpr int kAllCap = 16384;
+constexpr int kPtabCap = 8192;  // pages of one sequence held in shared memory (single-CTA heads)  // the cluster's threshold-bin candidates, copied locally (NC > 1)
 constexpr int kFinU = 8;        // pairs per thread per batch
 constexpr int kRankShift = 64 - kHistBits;  // b* = the rank key's top 11 bits
 constexpr float kFinLog2e = 1.4426950408889634f;
@@ -60,6 +61,7 @@ struct FinShared {
   float wo[W][2][kD];             // warp partials: [set][d], set 0 window, 1 selected
   float wm[W][2], wl[W][2];
   float mo[NC][2][kD];            // rank 0: the CTA partials, pushed by each CTA
+  int32_t ptab[NC == 1 ? kPtabCap : 1];  // a single-CTA head: its sequence's page table
   float mm[NC][2], ml[NC][2];
   uint32_t warp_tot[32];
   int cnt[2];                     // read by the cluster: above-b* pairs, candidates
@@ -234,12 +236,37 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   const int b = bh / a.Hq, h = bh % a.Hq;
   const int G = a.Hq / a.kv.Hkv;
   const int g = h / G;
+  // A single-CTA head of a paged cache keeps its sequence's page table in
+  // shared memory, so that a V row's address needs no dependent global load
+  // (the table is an input: it is read before the scan completes).
+  bool ptab_ok = false;
+  if constexpr (NC == 1) {
+    if (a.kv.page_table) {
+      const int64_t Lq = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
+      const int64_t np = (Lq + (1 << a.kv.page_shift) - 1) >> a.kv.page_shift;
+      if (np <= kPtabCap) {
+        const int32_t* pt = a.kv.page_table + (int64_t)b * a.kv.max_pages;
+        for (int64_t q = tid; q < np; q += kFinThreads) sh.ptab[q] = __ldg(pt + q);
+        ptab_ok = true;
+      }
+      __syncthreads();
+    }
+  }
+  // element offset of V/K row i of this head's KV head
+  auto row_off = [&](int64_t i) -> int64_t {
+    if (ptab_ok) {
+      const int64_t page = sh.ptab[i >> a.kv.page_shift];
+      const int64_t r = i & ((1 << a.kv.page_shift) - 1);
+      return (((page * a.kv.Hkv + g) << a.kv.page_shift) + r) * kD;
+    }
+    return kv_row(a.kv, b, g, i);
+  };
   {  // the V rows of this CTA's share of the window do not depend on the scan:
      // start bringing them into L2 while it finishes
     const int64_t L = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
     const int64_t nw = window_count(L, a.n_init, a.n_recent);
     for (int64_t j = nw * rank / NC + tid; j < nw * (rank + 1) / NC; j += kFinThreads) {
-      const uint16_t* vr = a.kv.v + kv_row(a.kv, b, g, window_pos(j, L, a.n_init, a.n_recent));
+      const uint16_t* vr = a.kv.v + row_off(window_pos(j, L, a.n_init, a.n_recent));
       prefetch_l2(vr);
       prefetch_l2(vr + kD / 2);
     }
@@ -421,7 +448,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
     for (int li = tid; li < nmy && li < kSelCap; li += kFinThreads) {
       const int64_t pk = sh.sel[li].x;
       if (pk >= L) continue;
-      const uint16_t* vr = a.kv.page_table ? vb + kv_row(a.kv, b, g, pk) : vb + pk * kD;
+      const uint16_t* vr = a.kv.page_table ? a.kv.v + row_off(pk) : vb + pk * kD;
       prefetch_l2(vr);
       prefetch_l2(vr + kD / 2);
     }
@@ -646,7 +673,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
     row_meta(base + 32 + lane, npos, nz, nset, nlv);
     if (nlv) {
       const uint16_t* vr =
-          a.kv.page_table ? vbase + kv_row(a.kv, b, g, npos) : vbase + (int64_t)npos * kD;
+          a.kv.page_table ? a.kv.v + row_off(npos) : vbase + (int64_t)npos * kD;
       prefetch_l2(vr);
       prefetch_l2(vr + kD / 2);
     }
@@ -659,7 +686,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
       const int r = 2 * k + half;
       const int pk = __shfl_sync(0xffffffffu, pos, r);
       const uint16_t* vr =
-          a.kv.page_table ? vbase + kv_row(a.kv, b, g, pk) : vbase + (int64_t)pk * kD;
+          a.kv.page_table ? a.kv.v + row_off(pk) : vbase + (int64_t)pk * kD;
       vv[k] = ((live >> r) & 1u) ? __ldg(reinterpret_cast<const uint4*>(vr + col))
                                  : make_uint4(0u, 0u, 0u, 0u);
     }
