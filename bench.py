@@ -307,7 +307,7 @@ def run_ours(args, ws, rank, local):
 
 
 def run_retopk(args, ws, rank, local):
-    """ReTopK decode (Qwen2.5-7B geometry, 64K): one layer-step is retopk_step
+    """ReTopK decode (Qwen2.5-7B geometry, 64K or 1M): one layer-step is retopk_step
     for all 28 query heads -- cosine recall, candidate union, rescoring and
     re-top-K on reuse heads, the exact scan + top-K on exact heads, sparse
     softmax.V and the FIFO push.  Reports microseconds per layer-step over the
@@ -320,7 +320,7 @@ def run_retopk(args, ws, rank, local):
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    wl = make_retopk("retopk64k", device=dev, seed=rank)
+    wl = make_retopk(args.workload, device=dev, seed=rank)
     kv = tsa.kv_contiguous(wl.k, wl.v)
     g = tsa.ReTopK(wl.Hq, wl.Hkv, wl.d, wl.K, wl.C, wl.R, wl.W, wl.tau, wl.T_r, wl.lcap,
                    device=dev)
@@ -420,13 +420,14 @@ def run_retopk(args, ws, rank, local):
         "warmup": args.warmup, "ms_per_step": round(total_ms / steps, 5),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "retopk64k", "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
+        "config": {"workload": args.workload, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
                    "context": wl.L0, "K": wl.K, "C": wl.C, "R": wl.R, "W": wl.W,
                    "tau": wl.tau, "T_r": wl.T_r, "decode_steps": steps,
-                   "l2": "K cache 64 MiB < L2 on exact steps; the stream is run as is",
+                   "l2": (f"K cache {wl.Hkv * wl.lcap * wl.d * 2 >> 20} MiB on exact steps "
+                          "(L2 126 MiB); the stream is run as is"),
                    "parallelism": f"replicas{ws}" if ws > 1 else "single"},
         "host_launched_us_per_step": round(eager_us, 3),
-        "timing": "CUDA graph of the 512-step stream captured from retopk_step calls",
+        "timing": f"CUDA graph of the {steps}-step stream captured from retopk_step calls",
         "paths": {"steps_with_exact_heads": len(exact_steps), "all_reuse_steps": len(reuse_steps),
                   "reuse_head_fraction": round(reuse_heads / (steps * wl.Hq), 4),
                   "mean_candidates_reuse": round(mean_m, 1) if mean_m else None,
@@ -635,7 +636,7 @@ def run_reference(args, ws, rank):
         return None
     import torch
     from workloads.gen import make_decode
-    if args.workload == "retopk64k":
+    if args.workload.startswith("retopk"):
         raise SystemExit("--impl reference times the decode workloads (the oracle's ReTopK "
                          "step is exercised by the parity tests)")
     wl = make_decode(args.workload, device="cpu")
@@ -670,7 +671,8 @@ def main():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="llama128k",
-                    choices=["tiny", "llama128k", "llama1m", "yi_paged", "retopk64k"])
+                    choices=["tiny", "llama128k", "llama1m", "yi_paged", "retopk64k",
+                             "retopk1m"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
@@ -684,7 +686,7 @@ def main():
     ws, rank, local = dist_env()
     if args.impl == "reference":
         res = run_reference(args, ws, rank)
-    elif args.workload == "retopk64k":
+    elif args.workload.startswith("retopk"):
         res = run_retopk(args, ws, rank, local)
     else:
         res = run_ours(args, ws, rank, local)

@@ -579,7 +579,8 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
     a.mcand_out = mcand_out;
     a.cand_out = cand_out;
     a.trace = g_trace;
-    const size_t smem = up((size_t)a.bitmap_words * 4, 16);
+    // the bitmap and its second level (one bit per bitmap word)
+    const size_t smem = up((size_t)(a.bitmap_words + (a.bitmap_words + 31) / 32) * 4, 16);
     if ((e = counted(launch_retopk_selector(a, smem, s))) != cudaSuccess)
       return cuda_fail(e, "retopk selector launch");
   }

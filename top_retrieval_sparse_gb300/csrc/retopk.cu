@@ -47,9 +47,12 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
   }
   __syncthreads();
   const float nrm = sqrtf(red[0]);
-  // the bitmap of step 4 is this CTA's shared memory: clear it now
+  // the bitmap of step 4 is this CTA's shared memory: clear it now.  A
+  // second level (one bit per bitmap word) marks the words that hold a bit.
   const int nwords = (int)((a.L + 31) >> 5);
-  for (int w = tid; w < nwords; w += kSelectorThreads) bitmap[w] = 0u;
+  const int nl2 = (nwords + 31) >> 5;
+  uint32_t* l2 = bitmap + nwords;
+  for (int w = tid; w < nwords + nl2; w += kSelectorThreads) bitmap[w] = 0u;
   // the cache and this step's buffers belong to the previous step's kernels
   // until they have completed; the key scan may be scheduled from here on
   pdl_wait();
@@ -146,20 +149,29 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
       }
 #pragma unroll
       for (int u = 0; u < kU; ++u)
-        if (pv[u] >= 0 && pv[u] < a.L) atomicOr(&bitmap[pv[u] >> 5], 1u << (pv[u] & 31));
+        if (pv[u] >= 0 && pv[u] < a.L) {
+          atomicOr(&bitmap[pv[u] >> 5], 1u << (pv[u] & 31));
+          atomicOr(&l2[pv[u] >> 10], 1u << ((pv[u] >> 5) & 31));
+        }
     }
   }
   const int64_t lo = a.L - a.W > 0 ? a.L - a.W : 0;
   for (int64_t p = lo + tid; p < a.L; p += kSelectorThreads)
+  {
     atomicOr(&bitmap[p >> 5], 1u << (p & 31));
+    atomicOr(&l2[p >> 10], 1u << ((p >> 5) & 31));
+  }
   __syncthreads();
 
-  // 5. ascending compaction: contiguous word ranges per thread + block scan
-  const int per = (nwords + kSelectorThreads - 1) / kSelectorThreads;
-  const int w0 = tid * per;
-  const int w1 = w0 + per < nwords ? w0 + per : nwords;
+  // 5. ascending compaction over the non-empty words only: thread t owns a
+  // contiguous range of second-level words, counts the bits of the words
+  // they mark, and after one block scan writes its positions in order.
+  const int per = (nl2 + kSelectorThreads - 1) / kSelectorThreads;
+  const int q0 = tid * per;
+  const int q1 = q0 + per < nl2 ? q0 + per : nl2;
   uint32_t cnt = 0;
-  for (int w = w0; w < w1; ++w) cnt += __popc(bitmap[w]);
+  for (int q = q0; q < q1; ++q)
+    for (uint32_t m = l2[q]; m; m &= m - 1) cnt += __popc(bitmap[(q << 5) + __ffs(m) - 1]);
   uint32_t incl = cnt;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -180,13 +192,13 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
   }
   __syncthreads();
   uint32_t pos = incl - cnt + wtot[wid];
-  for (int w = w0; w < w1; ++w) {
-    uint32_t bits = bitmap[w];
-    while (bits) {
-      const int bit = __ffs(bits) - 1;
-      bits &= bits - 1;
-      if (pos < (uint32_t)a.cand_cap) crow[pos] = ((uint32_t)w << 5) + bit;
-      ++pos;
+  for (int q = q0; q < q1; ++q) {
+    for (uint32_t m = l2[q]; m; m &= m - 1) {
+      const int w = (q << 5) + __ffs(m) - 1;
+      for (uint32_t bits = bitmap[w]; bits; bits &= bits - 1) {
+        if (pos < (uint32_t)a.cand_cap) crow[pos] = ((uint32_t)w << 5) + __ffs(bits) - 1;
+        ++pos;
+      }
     }
   }
   if (a.cand_out) {
