@@ -115,7 +115,8 @@ TSA_API int tsa_set_stage_events(void* const* events, int n);
  *   scan emitted for the head; kernel 8: bit 31 re-emission, bits 16-30
  *   the threshold bin, bits 0-15 the emission bin used; else 0),
  *   uint64 t[4] (%globaltimer ns: start, two kernel-specific phase marks
- *   or 0, exit; kernel 8: start, threshold bin found, list read, rows
+ *   or 0, exit; kernel 4: start, dependency wait over, candidate bitmap
+ *   built, exit; kernel 8: start, threshold bin found, list read, rows
  *   gathered).
  * Later calls on this thread append one record per CTA while it fits.
  * buf == NULL (or too small) turns tracing off. */

@@ -534,7 +534,7 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   // As on the decode path, the workspace counters start at zero (the caller
   // zeroes a new workspace once; every step's finish kernel clears them), so
-  // the four kernels form one chain of programmatic dependents.
+  // the three kernels form one chain of programmatic dependents.
   cudaError_t e = stage_mark(0, s);
   if (e != cudaSuccess) return cuda_fail(e, "event record");
   const KvView view = make_view(kv, st->Hkv);

@@ -15,11 +15,14 @@
 
 namespace tsa {
 
-constexpr int kSelectorThreads = 256;
 constexpr int kMaxC = 64;
 
+// 1024 threads: the support loads of the union and the compaction's walk
+// over the bitmap are latency chains split over the CTA's threads.
+constexpr int kSelectorThreads = 1024;
+
 __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(RetopkSelArgs a) {
-  TraceScope trace(a.trace, kTrSelector);
+  TraceScope trace(a.trace, kTrSelector);  // start, waited, union built, exit
   extern __shared__ __align__(16) uint32_t bitmap[];
   __shared__ __align__(16) float qs[kD];
   __shared__ float rho[kMaxC];
@@ -57,6 +60,7 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
   // until they have completed; the key scan may be scheduled from here on
   pdl_wait();
   pdl_trigger();
+  trace.mark(1);
   if (tid < kD) {
     const float qb = nrm > 0.f ? qs[tid] / nrm : 0.f;
     qs[tid] = qb;
@@ -64,7 +68,7 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
   }
   __syncthreads();
 
-  // 2. cosine against the cached queries (warp w: entries w, w + 8, ...; all of
+  // 2. cosine against the cached queries (warp w: entries w and w + 32; all of
   //    a warp's loads are issued before any is used)
   {
     constexpr int kPer = kMaxC / (kSelectorThreads / 32);  // entries per warp, at most
@@ -132,18 +136,18 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
 
   // 4. bitmap union of the recalled supports and the recent window
   // the R recalled supports as one flat index space of R*K entries (entries
-  // past a support's size are skipped), eight loads in flight per thread
+  // past a support's size are skipped), four loads in flight per thread
   {
-    constexpr int kU = 8;
-    const int64_t total = (int64_t)a.R * a.K;
-    for (int64_t j0 = tid; j0 < total; j0 += kU * kSelectorThreads) {
+    constexpr int kU = 4;
+    const int total = a.R * a.K;  // <= C*K entries of the cache
+    for (int j0 = tid; j0 < total; j0 += kU * kSelectorThreads) {
       int32_t pv[kU];
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
-        const int64_t j = j0 + (int64_t)u * kSelectorThreads;
+        const int j = j0 + u * kSelectorThreads;
         pv[u] = -1;
         if (j < total) {
-          const int r = (int)(j / a.K), i = (int)(j - (int64_t)r * a.K);
+          const int r = j / a.K, i = j - r * a.K;
           if (i < chosen_n[r]) pv[u] = a.cache_sup[((int64_t)h * a.C + chosen[r]) * a.K + i];
         }
       }
@@ -162,6 +166,7 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
     atomicOr(&l2[p >> 10], 1u << ((p >> 5) & 31));
   }
   __syncthreads();
+  trace.mark(2);
 
   // 5. ascending compaction over the non-empty words only: thread t owns a
   // contiguous range of second-level words, counts the bits of the words
@@ -180,15 +185,19 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
   }
   if (lane == 31) wtot[wid] = incl;
   __syncthreads();
-  if (tid == 0) {
-    uint32_t run = 0;
-    for (int w = 0; w < kSelectorThreads / 32; ++w) {
-      const uint32_t t = wtot[w];
-      wtot[w] = run;
-      run += t;
+  if (wid == 0) {  // exclusive scan of the warp totals
+    const uint32_t t = wtot[lane];
+    uint32_t inc = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
     }
-    a.mcand[h] = (int32_t)run;
-    if (a.mcand_out) a.mcand_out[h] = (int32_t)run;
+    wtot[lane] = inc - t;
+    if (lane == 31) {
+      a.mcand[h] = (int32_t)inc;
+      if (a.mcand_out) a.mcand_out[h] = (int32_t)inc;
+    }
   }
   __syncthreads();
   uint32_t pos = incl - cnt + wtot[wid];
