@@ -276,19 +276,40 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
                   // this kernel reads until this kernel has completed)
   trace.mark(1);
 
+  // The first decisions' inputs sit at fixed addresses: the list size, the
+  // hint word, this thread's histogram bins (kBpt of them, from the top) and,
+  // on a ReTopK step, the head's path and candidate count are all requested
+  // before any is used (with the sequence length), not one after another.
+  const int64_t n_in = __ldcg(a.dense_n + (int64_t)bh * kCtrStride);
+  const int32_t hw = __ldcg(a.hint_bin + bh);
+  uint32_t hb[kBpt];  // bins 2047-kBpt*tid-r, r < kBpt
+  {
+    const uint32_t* hh = a.hist + (int64_t)bh * kHistBins;
+#pragma unroll
+    for (int q = 0; q < kBpt / 4; ++q) {
+      const uint4 x =
+          __ldcg(reinterpret_cast<const uint4*>(hh + kHistBins - 4 * (q + 1) - kBpt * tid));
+      hb[4 * q] = x.w;
+      hb[4 * q + 1] = x.z;
+      hb[4 * q + 2] = x.y;
+      hb[4 * q + 3] = x.x;
+    }
+  }
+  const int path_in = RT ? __ldcg(a.path + bh) : 1;
+  const int mc_in = RT ? __ldcg(a.mcand + bh) : 0;
   const int64_t L = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
   const int64_t nw = window_count(L, a.n_init, a.n_recent);
   // a ReTopK reuse head selects among its |A_t| rescored candidates
-  const bool reuse = RT && a.path[bh] == 0;
-  const int64_t P = reuse ? (int64_t)(a.mcand[bh] < a.cand_cap ? a.mcand[bh] : a.cand_cap) : L - nw;
+  const bool reuse = RT && path_in == 0;
+  const int mcand = mc_in < a.cand_cap ? mc_in : a.cand_cap;
+  const int64_t P = reuse ? (int64_t)mcand : L - nw;
   const int need = (int64_t)a.K < P ? a.K : (int)P;
   uint64_t* spill = a.spill + (int64_t)bh * a.dense_stride;
   const uint2* lrow = a.dense + (int64_t)bh * a.dense_stride;
 
-  // The list size, the hint word and the histogram are read together, and
-  // the first batch of this CTA's slice of the list is in flight while the
+  // The first batch of this CTA's slice of the list is in flight while the
   // threshold bin is found (it is discarded if the list is re-emitted).
-  int64_t n = need > 0 ? __ldcg(a.dense_n + (int64_t)bh * kCtrStride) : 0;
+  int64_t n = need > 0 ? n_in : 0;
   if (n > a.dense_stride) n = a.dense_stride;
   int64_t s0 = n * rank / NC, s1 = n * (rank + 1) / NC;
   uint2 pre[kFinU];
@@ -303,7 +324,6 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   int bstar = -1, redo = 0, ebin = 0, next_hint = 0;
   bool wide = false;
   if (need > 0 && !reuse) {  // (a reuse head has no histogram: all its candidates compete)
-    const int32_t hw = __ldcg(a.hint_bin + bh);
     const int used = hint_bin_of(hw);
     wide = hint_wide_of(hw);
     if (need < P) {
@@ -312,20 +332,9 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
       const int64_t budget = wide ? 8 * (int64_t)need + 16384 : 3 * (int64_t)need + 4096;
       const int margin = wide ? 4 : 2;
       const uint32_t tgt[2] = {(uint32_t)need, (uint32_t)(budget + 1 < P ? budget + 1 : P + 1)};
-      const uint32_t* hh = a.hist + (int64_t)bh * kHistBins;
-      // thread t: bins 2047-kBpt*t-r, r < kBpt (from the top)
-      uint32_t c[kBpt], mine = 0;
+      uint32_t mine = 0;
 #pragma unroll
-      for (int q = 0; q < kBpt / 4; ++q) {
-        const uint4 x = __ldcg(
-            reinterpret_cast<const uint4*>(hh + kHistBins - 4 * (q + 1) - kBpt * tid));
-        c[4 * q] = x.w;
-        c[4 * q + 1] = x.z;
-        c[4 * q + 2] = x.y;
-        c[4 * q + 3] = x.x;
-      }
-#pragma unroll
-      for (int r = 0; r < kBpt; ++r) mine += c[r];
+      for (int r = 0; r < kBpt; ++r) mine += hb[r];
       if (tid == 0) sh.scal[0] = sh.scal[1] = -1;
       int tot;
       const uint32_t excl = (uint32_t)fin_scan<W>((int)mine, sh, &tot);
@@ -334,8 +343,8 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
         uint32_t acc = excl;
 #pragma unroll
         for (int r = 0; r < kBpt; ++r) {
-          if (acc < tgt[k] && acc + c[r] >= tgt[k]) sh.scal[k] = kHistBins - 1 - kBpt * tid - r;
-          acc += c[r];
+          if (acc < tgt[k] && acc + hb[r] >= tgt[k]) sh.scal[k] = kHistBins - 1 - kBpt * tid - r;
+          acc += hb[r];
         }
       }
       __syncthreads();
@@ -361,7 +370,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   phases.mark(1);
   trace.info = (uint32_t)min(n, (int64_t)0x7fffffff);
   phases.info = ((uint32_t)redo << 31) | ((uint32_t)(bstar & 0x7fff) << 16) |
-                (uint32_t)(need > 0 ? hint_bin_of(__ldcg(a.hint_bin + bh)) : 0);
+                (uint32_t)(need > 0 ? hint_bin_of(hw) : 0);
   // ---- re-emission when the scan's hint missed (rare: first call, shifts) ----
   if (redo) {  // uniform over the cluster
     cluster_sync_all();  // every CTA has read the old list size
@@ -427,8 +436,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
     }
   }
   if (need > 0 && reuse) {  // this CTA's share of A_t, rescored: every one a candidate
-    const int m = a.mcand[bh] < a.cand_cap ? a.mcand[bh] : a.cand_cap;
-    n = m;  // the candidate index space (spill layout as for a list slice)
+    n = mcand;  // the candidate index space (spill layout as for a list slice)
     s0 = n * rank / NC;
     s1 = n * (rank + 1) / NC;
     reuse_logits<W>(a, b, bh, g, s0, s1, sh, spill);
