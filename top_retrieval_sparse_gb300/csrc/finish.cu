@@ -43,8 +43,8 @@ namespace tsa {
 constexpr int kFinMaxCluster = 8;  // CTAs per head: 1, 2, 4 or 8 (chosen at launch)
 constexpr int kSelCap = 2048;   // this CTA's above-b* pairs in shared memory
 constexpr int kMyCap = 4096;    // this CTA's threshold-bin candidates in shared memory
-constexpr int kAllCap = 16384;
-constexpr int kPtabCap = 8192;  // pages of one sequence held in shared memory (single-CTA heads)  // the cluster's threshold-bin candidates, copied locally (NC > 1)
+constexpr int kAllCap = 16384;  // the cluster's threshold-bin candidates, copied locally (NC > 1)
+constexpr int kPtabCap = 8192;  // pages of one sequence held in shared memory (single-CTA heads)
 constexpr int kFinU = 8;        // pairs per thread per batch
 constexpr int kRankShift = 64 - kHistBits;  // b* = the rank key's top 11 bits
 constexpr float kFinLog2e = 1.4426950408889634f;
