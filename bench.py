@@ -447,6 +447,10 @@ def run_retopk(args, ws, rank, local):
     }
     if res["roofline"]["achieved"]:
         res["roofline"]["frac"] = round(res["roofline"]["achieved"] / peaks()[0], 4)
+    if not args.device_only:
+        res["e2e"] = run_retopk_e2e(args, wl, kv, g, tsa, torch, dev, state0, counters0, steps)
+        if args.cpu_baseline and rank == 0:
+            res["cpu_baseline"] = oracle_retopk_baseline(wl, budget_s=args.cpu_budget)
     if ws > 1:
         torch.distributed.destroy_process_group()
     return res if rank == 0 else None
@@ -630,15 +634,132 @@ def oracle_baseline(wl, budget_s=12.0, steps=1):
                       f"{t_used:.1f} s, scaled to a whole layer-step"}
 
 
+def run_retopk_e2e(args, wl, kv, g, tsa, torch, dev, state0, counters0, steps):
+    """ReTopK end to end through the C ABI with host buffers, over the step
+    stream from its start (the FIFO state is stateful).  Per step, on one
+    stream: a host -> device copy of the step's query (pinned), the append of
+    the step's K and V token rows (row L0 + t of each KV head) from pinned
+    host memory, the retopk_step call, a device -> host copy of the output
+    and lse (one copy), and a stream synchronisation.  Wall-clock per step
+    over the steps after the warm-up ones."""
+    import ctypes as C
+    rt = _cudart()
+    H2D, D2H = 1, 2
+    Hq, Hkv, d = wl.Hq, wl.Hkv, wl.d
+    qb, rowb = Hq * d * 2, d * 2
+    host_q = torch.empty((steps, qb), dtype=torch.uint8).pin_memory()
+    host_k = torch.empty((steps, Hkv, d), dtype=torch.bfloat16).pin_memory()
+    host_v = torch.empty_like(host_k).pin_memory()
+    for t in range(steps):
+        host_q[t] = wl.q_all[t].cpu().contiguous().view(torch.uint8).reshape(-1)
+        host_k[t] = wl.k[0, :, wl.L0 + t].cpu()
+        host_v[t] = wl.v[0, :, wl.L0 + t].cpu()
+    stage = torch.empty(qb, dtype=torch.uint8, device=dev)
+    res = torch.empty(Hq * (d + 1), dtype=torch.float32, device=dev)
+    res_host = torch.empty_like(res, device="cpu").pin_memory()
+    stream = torch.cuda.current_stream()
+    sp = C.c_void_p(stream.cuda_stream)
+    lib = tsa.lib()
+    pitch = kv.l_cap * rowb
+    hq, hk, hv = host_q.data_ptr(), host_k.data_ptr(), host_v.data_ptr()
+    kc, vc = wl.k.data_ptr(), wl.v.data_ptr()
+    tokb = Hkv * rowb
+
+    def one(t):
+        err = rt.cudaMemcpyAsync(stage.data_ptr(), hq + t * qb, qb, H2D, sp)
+        off = (wl.L0 + t) * rowb
+        err |= rt.cudaMemcpy2DAsync(kc + off, pitch, hk + t * tokb, rowb, rowb, Hkv, H2D, sp)
+        err |= rt.cudaMemcpy2DAsync(vc + off, pitch, hv + t * tokb, rowb, rowb, Hkv, H2D, sp)
+        rc = lib.retopk_step(g.handle, stage.data_ptr(), C.byref(kv.struct), wl.length(t),
+                             C.c_float(wl.scale), res.data_ptr(), None, None, None, None,
+                             res.data_ptr() + Hq * d * 4, g.workspace.data_ptr(),
+                             g.workspace.numel(), sp)
+        if rc:
+            raise tsa.TsaError(rc, lib.tsa_last_error().decode())
+        err |= rt.cudaMemcpyAsync(res_host.data_ptr(), res.data_ptr(), res.numel() * 4, D2H, sp)
+        err |= rt.cudaStreamSynchronize(sp)
+        if err:
+            raise RuntimeError(f"CUDA copy or synchronise failed ({err})")
+
+    torch.cuda.synchronize()
+    g.state.copy_(state0)
+    g.set_counters(*counters0)
+    torch.cuda.synchronize()
+    w = min(args.warmup, steps // 4)
+    for t in range(w):
+        one(t)
+    t0 = time.perf_counter()
+    for t in range(w, steps):
+        one(t)
+    dt = time.perf_counter() - t0
+    return {"value": round(1e6 * dt / (steps - w), 3), "unit": UNIT,
+            "h2d_bytes_per_step": qb + 2 * tokb, "d2h_bytes_per_step": res_host.numel() * 4,
+            "steps_timed": steps - w}
+
+
+def oracle_retopk_baseline(wl, budget_s=12.0):
+    """fp64 single-threaded oracle ReTopK on a bounded sample: query head 0
+    from the start of the step stream.  Its FIFO holds the oracle's own exact
+    causal top-K of the last C prefill queries (built untimed); its steps are
+    timed per path class (exact: step 0 is a refresh; reuse: the following
+    steps, until the budget), and the layer-step estimate weighs the classes
+    by the refresh period T_r (one exact step in T_r) over all query heads."""
+    import oracle as orc
+    from workloads.gen import bits
+    h = 0
+    G = wl.Hq // wl.Hkv
+    o = orc.ReTopK(wl.Hq, wl.d, wl.K, wl.C, wl.R, wl.W, wl.tau, wl.T_r)
+    kb, vb = bits(wl.k[0, h // G]), bits(wl.v[0, h // G])
+    qpre, qall = bits(wl.q_prefill[:, h]), bits(wl.q_all[:, h])
+    for c in range(wl.C):
+        p = wl.L0 - wl.C + c
+        r = orc.decode_head(qpre[c], kb[: p + 1], vb[: p + 1], wl.K, 0, 0, wl.scale)
+        o.set_slot(h, c, qpre[c], r["sel"])
+    times = {0: [], 1: []}
+    used = 0.0
+    for t in range(wl.steps):
+        L = wl.length(t)
+        t0 = time.perf_counter()
+        r = o.step_head(h, qall[t], kb[:L], vb[:L], wl.scale)
+        dt = time.perf_counter() - t0
+        o.advance()
+        times[int(r["path"])].append(dt)
+        used += dt
+        if used >= budget_s and times[0] and times[1]:
+            break
+    te = statistics.mean(times[1]) if times[1] else 0.0
+    tr = statistics.mean(times[0]) if times[0] else te
+    per_step = wl.Hq * (te / wl.T_r + tr * (1.0 - 1.0 / wl.T_r))
+    return {"value": round(1e6 * per_step, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": (f"query head 0, steps 0-{len(times[0]) + len(times[1]) - 1} of the stream "
+                       f"({len(times[1])} exact at {1e3 * te:.1f} ms, {len(times[0])} reuse at "
+                       f"{1e3 * tr:.2f} ms, {used:.1f} s), weighted one exact step in T_r = "
+                       f"{wl.T_r} and scaled to {wl.Hq} query heads")}
+
+
 def run_reference(args, ws, rank):
     """The reference arm: the fp64 oracle on the host cores, bounded sample."""
     if rank != 0:
         return None
     import torch
-    from workloads.gen import make_decode
+    from workloads.gen import make_decode, make_retopk
     if args.workload.startswith("retopk"):
-        raise SystemExit("--impl reference times the decode workloads (the oracle's ReTopK "
-                         "step is exercised by the parity tests)")
+        # the ReTopK stream is stateful: one pass of the oracle over its start
+        # (FIFO built untimed, then timed steps per path class, bounded)
+        wl = make_retopk(args.workload, device="cpu")
+        t0 = time.perf_counter()
+        base = oracle_retopk_baseline(wl, budget_s=args.cpu_budget)
+        dt = time.perf_counter() - t0
+        v = base["value"]
+        return {
+            "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT,
+            "n_gpus": ws, "steps": 1, "warmup": 0, "ms_per_step": round(1000 * dt, 3),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload},
+            "timing": "one bounded pass of the oracle over the start of the step stream",
+            "cpu_baseline": base,
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
     wl = make_decode(args.workload, device="cpu")
     # the whole run stays within a few minutes: each step is a bounded sample
     # (at least one query head) of the workload
