@@ -152,6 +152,54 @@ def test_retopk_always_exact_matches_decode():
         assert torch.max(torch.abs(out - ref[0])).item() < 1e-5
 
 
+def test_retopk_paged_cache_matches_contiguous():
+    """The same stream over a paged copy of the cache (16-token pages in a
+    seeded random order): every step's paths, candidate sets, supports and
+    outputs equal those of the contiguous run (the kernels read the same rows,
+    only through the page table; exact steps included: T_r = 8)."""
+    import top_retrieval_sparse_gb300 as tsa
+    wl = make_retopk(L0=5000, steps=20, K=48, C=6, R=3, W=5, T_r=8)
+    dev = "cuda"
+    k, v = wl.k.to(dev), wl.v.to(dev)
+    ps = 16
+    npg = wl.lcap // ps
+    perm = torch.randperm(npg, generator=torch.Generator().manual_seed(7)).to(torch.int32)
+    kp = torch.zeros((npg, wl.Hkv, ps, wl.d), dtype=torch.bfloat16, device=dev)
+    vp = torch.zeros_like(kp)
+    kp[perm.long().to(dev)] = k[0].reshape(wl.Hkv, npg, ps, wl.d).transpose(0, 1)
+    vp[perm.long().to(dev)] = v[0].reshape(wl.Hkv, npg, ps, wl.d).transpose(0, 1)
+    kvc = tsa.kv_contiguous(k, v)
+    kvp = tsa.kv_paged(kp, vp, perm[None].to(dev).contiguous())
+    sup, cnt = gpu_prefill_supports(tsa, wl, kvc, dev)
+    runs = []
+    for kv in (kvc, kvp):
+        g = tsa.ReTopK(wl.Hq, wl.Hkv, 128, wl.K, wl.C, wl.R, wl.W, wl.tau, wl.T_r, wl.lcap)
+        g.init(wl.q_prefill.to(dev).contiguous(), sup, cnt)
+        rec = []
+        cap = wl.R * wl.K + wl.W
+        for t in range(wl.steps):
+            so = torch.empty((wl.Hq, wl.K), dtype=torch.int32, device=dev)
+            po = torch.empty((wl.Hq,), dtype=torch.int32, device=dev)
+            mo = torch.empty((wl.Hq,), dtype=torch.int32, device=dev)
+            co = torch.empty((wl.Hq, cap), dtype=torch.int32, device=dev)
+            out = g.step(wl.q_all[t].to(dev).contiguous(), kv, wl.length(t), wl.scale,
+                         support_out=so, path_out=po, mcand_out=mo, cand_out=co)
+            rec.append((out.clone(), so, po, mo, co))
+        torch.cuda.synchronize()
+        runs.append(rec)
+    n_exact = n_reuse = 0
+    for t, (a, b) in enumerate(zip(*runs)):
+        assert torch.equal(a[2], b[2]), f"t={t}: paths differ"
+        assert torch.equal(a[3], b[3]), f"t={t}: candidate counts differ"
+        assert torch.equal(a[4], b[4]), f"t={t}: candidate sets differ"
+        for h in range(wl.Hq):
+            assert set(a[1][h].tolist()) == set(b[1][h].tolist()), f"t={t} h={h}: supports"
+        assert torch.max(torch.abs(a[0] - b[0])).item() < 1e-5, f"t={t}: outputs"
+        n_exact += int(a[2].sum())
+        n_reuse += int((a[2] == 0).sum())
+    assert n_exact >= wl.Hq and n_reuse > 0
+
+
 @pytest.mark.slow
 def test_retopk_full_config_lockstep():
     wl = make_retopk()  # Qwen2.5-7B geometry, 64K, C=32 R=4 K=512 W=32 tau=0.85 T_r=128
