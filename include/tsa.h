@@ -237,7 +237,8 @@ TSA_API size_t retopk_state_size(int Hq, int d, int K, int C);
 /* Create a handle over `state_mem`.  Hyper-parameters: 1 <= R <= C <= 64,
  * K >= 1, W >= 0, T_r >= 1, tau any float (tau > 1: always exact;
  * tau <= -1 with a large T_r: reuse after step 0).  max_len bounds every
- * later L_t (it sizes the candidate bitmap, <= 1<<21).  Nothing is launched. */
+ * later L_t (it sizes the candidate bitmap, which one CTA keeps in shared
+ * memory: max_len <= 1572864, 192 KiB of bits).  Nothing is launched. */
 TSA_API int retopk_create(tsa_retopk** st, int Hq, int Hkv, int d, int K, int C,
                   int R, int W, float tau, int T_r, int64_t max_len,
                   void* state_mem, size_t state_bytes);

@@ -132,3 +132,12 @@ def test_retopk_host_state_machine(lib):
                              FAKE, n) == -1  # T_r < 1
     assert lib.retopk_create(C.byref(bad), 28, 4, 128, 512, 32, 4, 32, 0.85, 128, 70000,
                              FAKE, n - 1) == -1  # state too small
+    # the selector's candidate bitmap (plus its second level) must fit one
+    # CTA's shared memory: 192 KiB of bits, 1572864 positions
+    cap = 192 * 1024 * 8
+    ok = C.c_void_p()
+    assert lib.retopk_create(C.byref(ok), 28, 4, 128, 512, 32, 4, 32, 0.85, 128, cap,
+                             FAKE, n) == 0
+    assert lib.retopk_destroy(ok) == 0
+    assert lib.retopk_create(C.byref(bad), 28, 4, 128, 512, 32, 4, 32, 0.85, 128, cap + 1,
+                             FAKE, n) == -1  # max_len beyond the bitmap
