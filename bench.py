@@ -270,7 +270,7 @@ def run_ours(args, ws, rank, local):
                 "scan_gbs": round(achieved, 1), "trace": trace_summary} if rank == 0 else None
     traffic, traffic_note = scan_traffic(wl, ab["scan"] // (wl.d * 2))
     # ---- end to end through the public API with host buffers ----
-    e2e = run_e2e(args, wl, kv, work, tsa, torch, dev)
+    e2e = run_e2e(args, wl, kv, work, tsa, torch, dev, ws)
 
     res = {
         "metric": METRIC, "value": round(us_per_layer_step, 3), "unit": UNIT,
@@ -448,7 +448,8 @@ def run_retopk(args, ws, rank, local):
     if res["roofline"]["achieved"]:
         res["roofline"]["frac"] = round(res["roofline"]["achieved"] / peaks()[0], 4)
     if not args.device_only:
-        res["e2e"] = run_retopk_e2e(args, wl, kv, g, tsa, torch, dev, state0, counters0, steps)
+        res["e2e"] = run_retopk_e2e(args, wl, kv, g, tsa, torch, dev, state0, counters0, steps,
+                                    ws)
         if args.cpu_baseline and rank == 0:
             res["cpu_baseline"] = oracle_retopk_baseline(wl, budget_s=args.cpu_budget)
     if ws > 1:
@@ -523,7 +524,7 @@ def _cudart():
     return rt
 
 
-def run_e2e(args, wl, kv, work, tsa, torch, dev):
+def run_e2e(args, wl, kv, work, tsa, torch, dev, ws=1):
     """End to end through the C ABI with host buffers.  Per step, on one
     stream: a host -> device copy of the step's query and lengths (pinned,
     one copy), the append of the step's K and V token rows from pinned host
@@ -594,10 +595,14 @@ def run_e2e(args, wl, kv, work, tsa, torch, dev):
     for i in range(args.warmup):
         one(i)
     n = args.steps
+    if ws > 1:
+        torch.distributed.barrier()
     t0 = time.perf_counter()
     for i in range(n):
         one(args.warmup + i)
     dt = time.perf_counter() - t0
+    # whole job: the slowest rank's wall time over every rank's layer-steps
+    dt = max_over_ranks(dt, ws, dev) / ws
     return {"value": round(1e6 * dt / n, 3), "unit": UNIT,
             "h2d_bytes_per_step": qb + lb + 2 * B * Hkv * rowb,
             "d2h_bytes_per_step": res_host.numel() * 4}
@@ -634,7 +639,7 @@ def oracle_baseline(wl, budget_s=12.0, steps=1):
                       f"{t_used:.1f} s, scaled to a whole layer-step"}
 
 
-def run_retopk_e2e(args, wl, kv, g, tsa, torch, dev, state0, counters0, steps):
+def run_retopk_e2e(args, wl, kv, g, tsa, torch, dev, state0, counters0, steps, ws=1):
     """ReTopK end to end through the C ABI with host buffers, over the step
     stream from its start (the FIFO state is stateful).  Per step, on one
     stream: a host -> device copy of the step's query (pinned), the append of
@@ -688,10 +693,13 @@ def run_retopk_e2e(args, wl, kv, g, tsa, torch, dev, state0, counters0, steps):
     w = min(args.warmup, steps // 4)
     for t in range(w):
         one(t)
+    if ws > 1:
+        torch.distributed.barrier()
     t0 = time.perf_counter()
     for t in range(w, steps):
         one(t)
     dt = time.perf_counter() - t0
+    dt = max_over_ranks(dt, ws, dev) / ws  # whole job, as for the decode leg
     return {"value": round(1e6 * dt / (steps - w), 3), "unit": UNIT,
             "h2d_bytes_per_step": qb + 2 * tokb, "d2h_bytes_per_step": res_host.numel() * 4,
             "steps_timed": steps - w}
