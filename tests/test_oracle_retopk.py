@@ -215,3 +215,155 @@ def test_candidate_bound_golden():
     r = st.step_head(0, e0, k[:L0 + 2], v[:L0 + 2], 1 / math.sqrt(D))
     assert r["path"] == 0
     assert r["n_cand"] == bound
+
+
+# ---------------------------------------------------------------------------
+# Lockstep adoption.  The parity tests run the oracle beside the GPU and let
+# the oracle take the GPU's decision where its own lies within a rounding
+# margin of a boundary (ReTopK "Fallback and refresh": max rho vs tau; the
+# top-R recall at the R-th / (R+1)-th cosine; the exact top-K near-tie).  The
+# cases below drive every such branch with cosines and logits that are known
+# in closed form, inside and just outside each margin.
+MARGIN = 1e-5  # the parity tests' path_abs / rho_abs
+
+
+def vec(*pairs):
+    """bf16 bits of the query with the given (channel, value) entries; every
+    value used here is exact in bf16."""
+    x = np.zeros(D, np.float32)
+    for j, val in pairs:
+        x[j] = val
+    return f32_to_bf16_bits(x)
+
+
+def tie_state(tau, R=2, T_r=10_000, margin=MARGIN):
+    """Five slots against the step-1 query 2*e0 (closed-form cosines):
+        slot 0: evicted by step 0 (a refresh step with query e5)
+        slot 1: 2*e0                    rho = 1
+        slot 2: e0 + 0.5 e1             rho = 1/sqrt(1.25)
+        slot 3: e0 + 0.5 e1 + 2^-12 e2  rho = 1/sqrt(1.25 + 2^-24)  (2.1e-8 below slot 2)
+        slot 4: e1                      rho = 0
+    Supports are disjoint blocks, so every recalled set has its own union."""
+    K, Cn, W, L0 = 4, 5, 2, 120
+    k, v, _ = make_case(L0 + 3, steps=1)
+    st = orc.ReTopK(1, D, K, Cn, R, W, tau=tau, T_r=T_r,
+                    path_abs=margin, rho_abs=margin, topk_rel=1e-6)
+    sup = {c: list(range(10 * c, 10 * c + K)) for c in range(Cn)}
+    slots = [vec((5, 1.0)), vec((0, 2.0)), vec((0, 1.0), (1, 0.5)),
+             vec((0, 1.0), (1, 0.5), (2, 2.0 ** -12)), vec((1, 1.0))]
+    for c in range(Cn):
+        st.set_slot(0, c, slots[c], sup[c])
+    # step 0: refresh (t % T_r == 0), evicts slot 0 (the oldest)
+    st.step_head(0, vec((5, 2.0)), k[:L0 + 1], v[:L0 + 1], 1 / math.sqrt(D))
+    st.advance()
+    L = L0 + 2
+    recent = list(range(L - W, L))
+    return st, k[:L], v[:L], sup, recent
+
+
+def union(*parts):
+    return sorted(set().union(*[set(p) for p in parts]))
+
+
+def test_closed_form_cosines_of_the_tie_state():
+    st, k, v, sup, recent = tie_state(tau=-1.5)
+    r = st.step_head(0, vec((0, 2.0)), k, v, 1 / math.sqrt(D))
+    assert r["max_rho"] == 1.0
+    r2, r3 = 1 / math.sqrt(1.25), 1 / math.sqrt(1.25 + 2.0 ** -24)
+    assert 0 < r2 - r3 < MARGIN
+    # free run: R = 2 recalls slots 1 and 2 (slot 2's cosine is the larger of the tie)
+    assert r["path"] == 0 and r["adopt_path"] == 0 and r["adopt_cand"] == 0
+    assert r["cand"].tolist() == union(sup[1], sup[2], recent)
+
+
+@pytest.mark.parametrize("offset,own,other,adopted", [
+    (+0.5, 1, 0, True),    # own exact (1 < tau), inside the margin: take the other's reuse
+    (+2.0, 1, 0, False),   # just outside the margin: keep exact
+    (-0.5, 0, 1, True),    # own reuse (1 >= tau), inside: take the other's exact path
+    (-2.0, 0, 1, False),   # outside: keep reuse
+])
+def test_path_adoption_only_within_margin(offset, own, other, adopted):
+    tau = 1.0 + offset * MARGIN
+    st, k, v, sup, recent = tie_state(tau=tau)
+    q = vec((0, 2.0))
+    r = st.step_head(0, q, k, v, 1 / math.sqrt(D), other_path=other)
+    assert r["own_path"] == own
+    assert r["adopt_path"] == int(adopted)
+    assert r["path"] == (other if adopted else own)
+    if r["path"] == 1:  # exact path: the exact top-K of every key, no window
+        assert set(r["sup"].tolist()) == np_topk(q, k, len(k), 4)
+        assert r["n_cand"] == len(k)
+    else:
+        assert r["cand"].tolist() == union(sup[1], sup[2], recent)
+
+
+def test_refresh_step_never_adopts_a_reuse_path():
+    # step 1 with T_r = 1 is a refresh: max rho = 1 sits right at tau, the
+    # other side claims reuse, the oracle stays exact
+    st, k, v, sup, recent = tie_state(tau=1.0 - 0.5 * MARGIN, T_r=1)
+    r = st.step_head(0, vec((0, 2.0)), k, v, 1 / math.sqrt(D), other_path=0)
+    assert r["path"] == 1 and r["own_path"] == 1 and r["adopt_path"] == 0
+
+
+@pytest.mark.parametrize("which,ok,adopt", [
+    ("own", 1, 0),          # the same union: equal, nothing adopted
+    ("tie_swap", 2, 1),     # the tied slot 3 instead of slot 2: an admissible choice
+    ("drop_sure", 0, 0),    # both tied slots, the sure slot 1 dropped
+    ("below_band", 0, 0),   # slot 4 (rho = 0) instead of a tied slot
+    ("extra", 0, 0),        # the admissible union plus one stray position
+])
+def test_candidate_adoption_at_the_recall_boundary(which, ok, adopt):
+    st, k, v, sup, recent = tie_state(tau=-1.5)
+    other = {"own": union(sup[1], sup[2], recent),
+             "tie_swap": union(sup[1], sup[3], recent),
+             "drop_sure": union(sup[2], sup[3], recent),
+             "below_band": union(sup[1], sup[4], recent),
+             "extra": union(sup[1], sup[3], recent, [77])}[which]
+    r = st.step_head(0, vec((0, 2.0)), k, v, 1 / math.sqrt(D), other_path=0,
+                     other_cand=other)
+    assert r["path"] == 0
+    assert r["cand_ok"] == ok and r["adopt_cand"] == adopt
+    if ok:  # the oracle continues with the other side's (admissible) union
+        assert r["cand"].tolist() == other
+    else:   # it keeps its own union, and the step counts as a mismatch
+        assert r["cand"].tolist() == union(sup[1], sup[2], recent)
+
+
+def test_candidate_adoption_needs_a_near_tie():
+    # the same unions with margins far below the 2.1e-8 gap between slots 2
+    # and 3: no tie at the boundary, so the swapped union is rejected
+    st, k, v, sup, recent = tie_state(tau=-1.5, margin=1e-9)
+    r = st.step_head(0, vec((0, 2.0)), k, v, 1 / math.sqrt(D), other_path=0,
+                     other_cand=union(sup[1], sup[3], recent))
+    assert r["cand_ok"] == 0 and r["adopt_cand"] == 0
+
+
+@pytest.mark.parametrize("swap,ok", [(20, 2), (30, 0)])
+def test_support_adoption_pushes_the_accepted_set(swap, ok):
+    """Exact path (step 0 refresh), K = 3: positions 5 and 6 score 6s, 10 scores
+    (2 + 2^-20)s and 20 scores 2s, every other key 0.  {5, 6, 20} differs from
+    the exact {5, 6, 10} by a relative gap of 4.8e-7 < 1e-6 (accepted, and the
+    FIFO receives it); {5, 6, 30} swaps in a key of logit 0 (rejected: the FIFO
+    receives the oracle's own set)."""
+    K, L = 3, 64
+    k = np.zeros((L, D), np.float32)
+    k[5, 0] = k[6, 0] = 3.0
+    k[10, 0], k[10, 1] = 1.0, 1.0
+    k[20, 0] = 1.0
+    k = f32_to_bf16_bits(k)
+    v = f32_to_bf16_bits(rng.standard_normal((L, D)))
+    q = vec((0, 2.0), (1, 2.0 ** -20))
+    st = orc.ReTopK(1, D, K, 2, 1, 2, tau=0.5, T_r=10_000,
+                    path_abs=MARGIN, rho_abs=MARGIN, topk_rel=1e-6)
+    st.set_slot(0, 0, vec((3, 1.0)), [1, 2, 3])
+    st.set_slot(0, 1, vec((4, 1.0)), [1, 2, 3])
+    other = [5, 6, swap]
+    r = st.step_head(0, q, k, v, 1 / math.sqrt(D), other_path=1, other_sup=other)
+    assert r["path"] == 1 and r["sup_ok"] == ok
+    pushed = sorted(st.slot_support(0, 0).tolist())   # slot 0 was the oldest
+    want = other if ok == 2 else [5, 6, 10]
+    assert pushed == sorted(want) and sorted(r["sup"].tolist()) == sorted(want)
+    # the output is the softmax over the pushed set
+    from scipy.special import softmax
+    z = (widen(k[want]) @ widen(q)) / math.sqrt(D)
+    np.testing.assert_allclose(r["out"], softmax(z) @ widen(v[want]), rtol=1e-11, atol=1e-12)
