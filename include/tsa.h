@@ -27,13 +27,17 @@
  *     Hq / Hkv <= 8, B * Hkv <= 512 and B * Hq <= 65535.
  *   - Ownership: the caller allocates every buffer (device memory unless
  *     stated) and the workspace, and owns the stream.  No entry point
- *     allocates, frees, synchronises or prints; launches are asynchronous
- *     on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *     allocates, frees or prints, and none but tsa_workspace_status
+ *     synchronises; launches are asynchronous on `stream` (a cudaStream_t;
+ *     NULL = legacy default stream).
  *   - Errors: every call returns a tsa_status.  Arguments are validated on
  *     the host before any launch; on an error nothing is launched and
  *     tsa_last_error() describes the problem (thread-local).  Launch
  *     failures are reported as TSA_ERR_CUDA.  Faults inside a kernel surface
- *     through the stream as usual CUDA errors.
+ *     through the stream as usual CUDA errors.  What the kernels detect
+ *     themselves (a bounded wait that expired, a length outside the cache)
+ *     goes into a sticky status word in the workspace, which
+ *     tsa_workspace_status() reads after the calls have run.
  *   - Concurrency: calls that share a workspace or a ReTopK state must be
  *     ordered on one stream.
  */
@@ -60,7 +64,7 @@ typedef enum tsa_status {
   TSA_ERR_CUDA = -3,        /* a CUDA runtime call or launch failed           */
   TSA_ERR_STATE = -4,       /* ReTopK state handle invalid or not initialised */
   TSA_ERR_DEVICE_CHECK = -5,/* a device-side check flagged bad input          */
-  TSA_ERR_TIMEOUT = -6      /* reserved: a bounded device wait expired        */
+  TSA_ERR_TIMEOUT = -6      /* a bounded device wait expired (status word)    */
 } tsa_status;
 
 /* KV cache of one layer.
@@ -152,6 +156,14 @@ TSA_API int tsa_set_trace(void* buf, size_t bytes);
  *             a call that failed.  It also keeps per-head state
  *             that speeds up the next call (never its result): use one
  *             workspace per layer.
+ * Device-detected errors (read them with tsa_workspace_status):
+ *   - every wait inside the kernels is bounded (1 s); if one expires the
+ *     kernel gives up, the call's out / lse / topk_score are NaN and
+ *     topk_idx is -1, the workspace stays consistent, and the status word
+ *     keeps TSA_ERR_TIMEOUT: every later call on the workspace also outputs
+ *     NaN until tsa_workspace_status(..., clear = 1) has cleared it;
+ *   - a lens[b] outside [0, l_cap] is clamped to that range and reported as
+ *     TSA_ERR_DEVICE_CHECK (the outputs are those of the clamped length).
  * Returns TSA_OK or an error; see the conventions above. */
 TSA_API size_t tsa_decode_workspace_size(int B, int Hq, int Hkv, int d, int64_t l_cap,
                                  int K, int n_init, int n_recent);
@@ -175,9 +187,14 @@ TSA_API int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* l
  *
  * Same arguments and results as sparse_attn_decode, minus the workspace.
  *   - Problems whose tsa_decode_workspace_size() exceeds the array are
- *     rejected with TSA_ERR_WORKSPACE (nothing launched); e.g. B*Hq = 4 fits
- *     caches up to about 0.5 M positions, B*Hq = 32 fits none beyond a few
- *     thousand.
+ *     rejected with TSA_ERR_WORKSPACE (nothing launched).  The size grows as
+ *     B*Hq*16*(l_cap + 65536) bytes plus 8 KiB per head: B*Hq = 4 fits
+ *     caches up to about 458 K positions, B*Hq = 16 about 65 K, and
+ *     B*Hq >= 32 fits none.
+ *   - The arguments are checked as in sparse_attn_decode before the array
+ *     or the stream is touched.
+ *   - Each call clears the array's status word with its counters, so a
+ *     timeout shows as NaN outputs of that call only.
  *   - The first call on a device looks the array's device address up
  *     (cudaGetSymbolAddress, with that device current), which may load the
  *     library's module; make that first call before any stream capture.
@@ -193,6 +210,32 @@ TSA_API int sparse_attn_decode_noalloc(const void* q, const tsa_kv* kv,
                        int n_init, int n_recent, float scale, float* out,
                        float* lse_out, int32_t* topk_idx, float* topk_score,
                        void* stream);
+
+/* tsa_workspace_status -- the device-side status of a decode or ReTopK
+ * workspace.  The pages have no counterpart: this is error reporting.
+ *
+ * Synchronises `stream` (the only entry point that does), then reads the
+ * workspace's status word (written by the kernels of earlier calls on it):
+ *   TSA_OK               nothing was flagged;
+ *   TSA_ERR_TIMEOUT      a bounded wait expired in some call (its outputs,
+ *                        and those of every later call, are NaN);
+ *   TSA_ERR_DEVICE_CHECK a device-side check flagged bad input (a sequence
+ *                        length outside [0, l_cap], clamped).
+ * With clear != 0 the word is reset to zero, so the next call runs normally
+ * (the rest of the workspace needs no reset).  workspace: the pointer given
+ * to sparse_attn_decode or retopk_step (256-byte aligned). */
+TSA_API int tsa_workspace_status(void* workspace, int clear, void* stream);
+
+/* tsa_inject_scan_stall -- fault injection for tests of the error path.
+ *
+ * Makes the next sparse_attn_decode or retopk_step call on this thread
+ * wait at most wait_limit_ns (1 .. 1e9) in its key scan, and makes the
+ * scan's first CTA withhold the copy of its first key tile, so that the
+ * bounded waits of that CTA expire: the call then reports TSA_ERR_TIMEOUT
+ * through tsa_workspace_status, with NaN outputs, and the device stays
+ * usable.  One call only; 0 cancels a pending injection.  Nothing is
+ * launched by this function. */
+TSA_API int tsa_inject_scan_stall(long long wait_limit_ns);
 
 /* ------------------------------------------------------------------ */
 /* lse_merge -- [RA] Eq. 4-5 on precomputed partials.
@@ -267,7 +310,11 @@ TSA_API size_t retopk_workspace_size(const tsa_retopk* st);
  *   mcand_out int32 [Hq] (|A_t| on the reuse path, len on the exact path),
  *   cand_out int32 [Hq][R*K+W] (A_t ascending, -1 padded; reuse heads only),
  *   lse_out fp32 [Hq].
- * Advances the step counter and the FIFO head. */
+ * Advances the step counter and the FIFO head.  If a bounded wait of the
+ * step's key scan expires (see tsa_workspace_status), out and lse are NaN
+ * and the FIFO entry is not rewritten (it keeps an older entry): restore
+ * the state memory and counters from a copy taken before the step to redo
+ * it. */
 TSA_API int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len,
                 float scale, float* out, int32_t* support_out,
                 int32_t* path_out, int32_t* mcand_out, int32_t* cand_out,

@@ -141,3 +141,70 @@ def test_retopk_host_state_machine(lib):
     assert lib.retopk_destroy(ok) == 0
     assert lib.retopk_create(C.byref(bad), 28, 4, 128, 512, 32, 4, 32, 0.85, 128, cap + 1,
                              FAKE, n) == -1  # max_len beyond the bitmap
+
+
+def test_status_and_injection_validation(lib):
+    """The status query refuses a bad workspace before any CUDA call; the
+    injection hook checks its limit and launches nothing."""
+    assert lib.tsa_workspace_status(None, 1, None) == -2
+    assert lib.tsa_workspace_status(C.c_void_p((1 << 20) + 8), 1, None) == -2
+    assert lib.tsa_inject_scan_stall(-1) == -1
+    assert lib.tsa_inject_scan_stall(2_000_000_000) == -1
+    n0 = lib.tsa_kernel_launches()
+    assert lib.tsa_inject_scan_stall(1_000_000) == 0
+    assert lib.tsa_inject_scan_stall(0) == 0   # cancel
+    assert lib.tsa_kernel_launches() == n0
+
+
+def _noalloc(lib, tsa, **kw):
+    a = dict(q=FAKE, kv=_kv(tsa), lens=FAKE, B=1, Hq=8, Hkv=2, d=128, K=16, n_init=4,
+             n_recent=8, scale=0.1, out=FAKE, lse=None, idx=None, sc=None, stream=None)
+    a.update(kw)
+    return lib.sparse_attn_decode_noalloc(a["q"], C.byref(a["kv"]), a["lens"], a["B"], a["Hq"],
+                                          a["Hkv"], a["d"], a["K"], a["n_init"], a["n_recent"],
+                                          a["scale"], a["out"], a["lse"], a["idx"], a["sc"],
+                                          a["stream"])
+
+
+@pytest.mark.parametrize("kw", [dict(d=64), dict(Hq=6, Hkv=4), dict(K=-1), dict(q=None),
+                                dict(out=C.c_void_p((1 << 20) + 4)), dict(scale=float("inf")),
+                                dict(lens=None)])
+def test_noalloc_validates_before_touching_the_device(lib, kw):
+    """Invalid arguments are refused with the decode entry point's own code
+    before the scratch array or the stream is touched: without a GPU any CUDA
+    call would fail with TSA_ERR_CUDA (-3), and no launch is counted."""
+    import top_retrieval_sparse_gb300 as tsa
+    n0 = lib.tsa_kernel_launches()
+    assert _noalloc(lib, tsa, **kw) == -1
+    assert lib.tsa_kernel_launches() == n0
+
+
+def test_noalloc_size_limit_boundaries(lib):
+    """The scratch need grows as B*Hq*16*(l_cap + 65536) bytes plus ~8 KiB per
+    head: B*Hq = 4 fits up to about 458 K positions, B*Hq = 16 about 65 K, and
+    B*Hq = 32 fits no cache at all; an oversize problem is refused (-2) before
+    any CUDA call."""
+    import top_retrieval_sparse_gb300 as tsa
+    cap = lib.tsa_noalloc_scratch_bytes()
+    assert cap == 32 << 20
+
+    def need(B, Hq, Hkv, l_cap):
+        return lib.tsa_decode_workspace_size(B, Hq, Hkv, 128, l_cap, 64, 4, 64)
+
+    def largest_fit(B, Hq, Hkv):
+        lo, hi = 0, 1 << 22
+        if need(B, Hq, Hkv, 0) > cap:
+            return -1
+        while lo < hi:
+            mid = (lo + hi + 1) // 2
+            if need(B, Hq, Hkv, mid) <= cap:
+                lo = mid
+            else:
+                hi = mid - 1
+        return lo
+    l4 = largest_fit(1, 4, 1)
+    assert 450_000 < l4 < 460_000
+    assert 60_000 < largest_fit(1, 16, 2) < 66_000
+    assert largest_fit(1, 32, 8) == -1 and largest_fit(2, 16, 4) == -1
+    assert _noalloc(lib, tsa, Hq=4, Hkv=1, kv=_kv(tsa, l4 + 64)) == -2
+    assert "scratch" in lib.tsa_last_error().decode()

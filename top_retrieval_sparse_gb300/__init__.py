@@ -83,6 +83,8 @@ def lib():
             L.tsa_set_stage_events.argtypes = [C.POINTER(P), i32]
             L.tsa_set_trace.argtypes = [P, sz]
             L.tsa_kernel_launches.restype = C.c_ulonglong
+            L.tsa_workspace_status.argtypes = [P, i32, P]
+            L.tsa_inject_scan_stall.argtypes = [C.c_longlong]
             _lib = L
     return _lib
 
@@ -241,6 +243,18 @@ def sparse_attn_decode_noalloc(q: torch.Tensor, kv: KV, lens: torch.Tensor, K: i
 
 def noalloc_scratch_bytes() -> int:
     return int(lib().tsa_noalloc_scratch_bytes())
+
+
+def workspace_status(workspace: torch.Tensor, clear: bool = True, stream=None) -> int:
+    """Device-side status of a decode or ReTopK workspace (synchronises the
+    stream): 0, TSA_ERR_TIMEOUT (-6) or TSA_ERR_DEVICE_CHECK (-5)."""
+    return int(lib().tsa_workspace_status(_p(workspace), 1 if clear else 0, _stream(stream)))
+
+
+def inject_scan_stall(wait_limit_ns: int) -> None:
+    """Fault injection for tests: the next call's key scan gives up a wait
+    after wait_limit_ns (its first CTA withholds a tile copy)."""
+    _check(lib().tsa_inject_scan_stall(int(wait_limit_ns)))
 
 
 def lse_merge(o_a, lse_a, o_b, lse_b, o_out=None, lse_out=None, stream=None):

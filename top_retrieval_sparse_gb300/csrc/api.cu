@@ -25,6 +25,9 @@ namespace {
 thread_local std::string g_err;
 thread_local cudaEvent_t g_stage[4] = {nullptr, nullptr, nullptr, nullptr};
 thread_local TraceBuf g_trace = {nullptr, nullptr, 0};
+// Fault injection for tests: the wait limit of the next key scan on this
+// thread, whose CTA 0 then withholds its first tile copy (0: off).
+thread_local long long g_stall_ns = 0;
 std::atomic<unsigned long long> g_launches{0};
 
 // Count a kernel launch of this library once it has been issued.
@@ -153,6 +156,9 @@ ScanArgs scan_args(const uint16_t* q, const KvView& view, const int32_t* lens, i
   s.wz_stride = w.wz_stride;
   s.status = w.status;
   s.trace = g_trace;
+  s.wait_ns = g_stall_ns;
+  s.stall_first_copy = g_stall_ns > 0;
+  g_stall_ns = 0;  // one call only
   return s;
 }
 
@@ -236,12 +242,35 @@ int check_heads(int B, int Hq, int Hkv, int d) {
   return TSA_OK;
 }
 
+// Every host check of sparse_attn_decode except the workspace's.
+int check_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int B, int Hq, int Hkv,
+                 int d, int K, int n_init, int n_recent, float scale, const float* out) {
+  int rc = check_heads(B, Hq, Hkv, d);
+  if (rc) return rc;
+  if ((rc = check_kv(kv, B, Hkv))) return rc;
+  if (B == 0) return TSA_OK;
+  if (!q || !out || !lens) return fail(TSA_ERR_INVALID_ARG, "q, out and lens must be non-NULL");
+  if (!aligned(q, 16)) return fail(TSA_ERR_INVALID_ARG, "q must be 16-byte aligned");
+  if (!aligned(out, 16)) return fail(TSA_ERR_INVALID_ARG, "out must be 16-byte aligned");
+  if (K < 0 || n_init < 0 || n_recent < 0)
+    return fail(TSA_ERR_INVALID_ARG, "K, n_init, n_recent must be >= 0");
+  if (!std::isfinite(scale)) return fail(TSA_ERR_INVALID_ARG, "scale must be finite");
+  return TSA_OK;
+}
+
 }  // namespace
 
 namespace tsa {
 // Sets this thread's error message for an entry point defined in another
 // translation unit of the library; returns `code`.
 int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
+// The host checks of sparse_attn_decode other than the workspace's (TSA_OK,
+// or the error code with this thread's message set).
+int validate_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int B, int Hq,
+                    int Hkv, int d, int K, int n_init, int n_recent, float scale,
+                    const float* out) {
+  return check_decode(q, kv, lens, B, Hq, Hkv, d, K, n_init, n_recent, scale, out);
+}
 // Bytes at the start of a decode workspace that must be zero before a call.
 size_t decode_zero_bytes(int B, int Hq, int Hkv, int64_t l_cap, int K, int n_init, int n_recent) {
   (void)K;
@@ -291,16 +320,9 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
                        int Hkv, int d, int K, int n_init, int n_recent, float scale, float* out,
                        float* lse_out, int32_t* topk_idx, float* topk_score, void* workspace,
                        size_t ws_bytes, void* stream) {
-  int rc = check_heads(B, Hq, Hkv, d);
+  int rc = check_decode(q, kv, lens, B, Hq, Hkv, d, K, n_init, n_recent, scale, out);
   if (rc) return rc;
-  if ((rc = check_kv(kv, B, Hkv))) return rc;
   if (B == 0) return ok();
-  if (!q || !out || !lens) return fail(TSA_ERR_INVALID_ARG, "q, out and lens must be non-NULL");
-  if (!aligned(q, 16)) return fail(TSA_ERR_INVALID_ARG, "q must be 16-byte aligned");
-  if (!aligned(out, 16)) return fail(TSA_ERR_INVALID_ARG, "out must be 16-byte aligned");
-  if (K < 0 || n_init < 0 || n_recent < 0)
-    return fail(TSA_ERR_INVALID_ARG, "K, n_init, n_recent must be >= 0");
-  if (!std::isfinite(scale)) return fail(TSA_ERR_INVALID_ARG, "scale must be finite");
   const DecodeLayout Lw = decode_layout(B, Hq, Hkv, kv->l_cap, n_init, n_recent);
   if (!workspace || !aligned(workspace, kAlign))
     return fail(TSA_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
@@ -353,6 +375,38 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
     if ((e = counted(launch_finish(f, st))) != cudaSuccess) return cuda_fail(e, "finish launch");
   }
   if ((e = stage_mark(3, st)) != cudaSuccess) return cuda_fail(e, "event record");
+  return ok();
+}
+
+int tsa_workspace_status(void* workspace, int clear, void* stream) {
+  if (!workspace || !aligned(workspace, kAlign))
+    return fail(TSA_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int word = 0;  // the status word sits at offset 0 of both workspace layouts
+  cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (clear && word) {
+    e = cudaMemsetAsync(workspace, 0, sizeof word, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "status clear");
+  }
+  if (word & kStatusTimeout)
+    return fail(TSA_ERR_TIMEOUT,
+                "a bounded device wait expired: the outputs of the calls since the last "
+                "status read are NaN");
+  if (word & kStatusBadLength)
+    return fail(TSA_ERR_DEVICE_CHECK,
+                "a sequence length outside [0, l_cap] was clamped to that range");
+  if (word) return fail(TSA_ERR_DEVICE_CHECK, "device status word 0x%x", word);
+  return ok();
+}
+
+int tsa_inject_scan_stall(long long wait_limit_ns) {
+  if (wait_limit_ns < 0 || wait_limit_ns > kWaitLimitNs)
+    return fail(TSA_ERR_INVALID_ARG, "wait_limit_ns must be in [0, %lld]",
+                (long long)kWaitLimitNs);
+  g_stall_ns = wait_limit_ns;
   return ok();
 }
 

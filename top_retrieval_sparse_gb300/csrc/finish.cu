@@ -276,6 +276,37 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
                   // this kernel reads until this kernel has completed)
   trace.mark(1);
 
+  // A bounded wait of the key scan (this call's, or an earlier one on this
+  // workspace: the bit is sticky until the host reads it) gave up: the lists
+  // and histograms are incomplete.  Every CTA reads the same word, so the
+  // whole grid takes this path: NaN outputs, the counters cleared for the next
+  // call, no FIFO push (the ReTopK state keeps its previous entry).
+  if (__ldcg(a.status) & kStatusTimeout) {
+    if (rank == 0) {
+      const float nan = __int_as_float(0x7fc00000);
+      if (tid < kD) a.out[(int64_t)bh * kD + tid] = nan;
+      if (tid == 0 && a.lse_out) a.lse_out[bh] = nan;
+      if (!RT)
+        for (int q = tid; q < a.K; q += kFinThreads) {
+          if (a.topk_idx) a.topk_idx[(int64_t)bh * a.topk_stride + q] = -1;
+          if (a.topk_score) a.topk_score[(int64_t)bh * a.topk_stride + q] = nan;
+        }
+      uint4* hz = reinterpret_cast<uint4*>(a.hist + (int64_t)bh * kHistBins);
+      for (int q = tid; q < kHistBins / 4; q += kFinThreads) hz[q] = make_uint4(0u, 0u, 0u, 0u);
+      if (tid == 0) {
+        a.dense_n[(int64_t)bh * kCtrStride] = 0;
+        if (bh == 0) *a.tile_ctr = 0;
+      }
+    }
+    return;
+  }
+  // The length contract (0 <= lens[b] <= l_cap) is checked here: an
+  // out-of-range length was clamped by both kernels; flag it for the host.
+  if (a.lens && rank == 0 && h == 0 && tid == 0) {
+    const int32_t Lr = a.lens[b];
+    if (Lr < 0 || (int64_t)Lr > a.kv.l_cap) atomicOr(a.status, kStatusBadLength);
+  }
+
   // The first decisions' inputs sit at fixed addresses: the list size, the
   // hint word, this thread's histogram bins (kBpt of them, from the top) and,
   // on a ReTopK step, the head's path and candidate count are all requested
@@ -491,10 +522,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
     for (int q = tid; q < kHistBins / 4; q += kFinThreads) hz[q] = make_uint4(0u, 0u, 0u, 0u);
     if (tid == 0) {
       a.dense_n[(int64_t)bh * kCtrStride] = 0;
-      if (bh == 0) {
-        *a.tile_ctr = 0;
-        *a.status = 0;
-      }
+      if (bh == 0) *a.tile_ctr = 0;
     }
   }
   // candidate j of the cluster (cluster order): CTA c's list, local index i

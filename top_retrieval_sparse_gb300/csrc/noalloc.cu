@@ -20,6 +20,9 @@
 
 namespace tsa {
 int report_error(int code, const char* msg);
+int validate_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int B, int Hq,
+                    int Hkv, int d, int K, int n_init, int n_recent, float scale,
+                    const float* out);
 size_t decode_zero_bytes(int B, int Hq, int Hkv, int64_t l_cap, int K, int n_init, int n_recent);
 }  // namespace tsa
 
@@ -65,7 +68,13 @@ int sparse_attn_decode_noalloc(const void* q, const tsa_kv* kv, const int32_t* l
                                int Hq, int Hkv, int d, int K, int n_init, int n_recent,
                                float scale, float* out, float* lse_out, int32_t* topk_idx,
                                float* topk_score, void* stream) {
-  if (!kv) return tsa::report_error(TSA_ERR_INVALID_ARG, "kv is NULL");
+  // The same host checks as sparse_attn_decode first: an invalid call
+  // touches neither the array nor the stream.
+  int rc = tsa::validate_decode(q, kv, lens, B, Hq, Hkv, d, K, n_init, n_recent, scale, out);
+  if (rc != TSA_OK) return rc;
+  if (B == 0) return sparse_attn_decode(q, kv, lens, B, Hq, Hkv, d, K, n_init, n_recent,
+                                        scale, out, lse_out, topk_idx, topk_score, nullptr, 0,
+                                        stream);
   const size_t need = tsa_decode_workspace_size(B, Hq, Hkv, d, kv->l_cap, K, n_init, n_recent);
   if (need > kScratchBytes) {
     char msg[256];
@@ -76,12 +85,12 @@ int sparse_attn_decode_noalloc(const void* q, const tsa_kv* kv, const int32_t* l
     return tsa::report_error(TSA_ERR_WORKSPACE, msg);
   }
   void* scratch = nullptr;
-  const int rc = scratch_address(&scratch);
+  rc = scratch_address(&scratch);
   if (rc != TSA_OK) return rc;
   // Calls of any size share the array, so the counters that must start at
-  // zero are cleared on the stream every time; the rest needs no
-  // initialisation.
-  if (B > 0 && Hq > 0 && Hkv > 0 && kv->l_cap > 0 && K >= 0 && n_init >= 0 && n_recent >= 0) {
+  // zero (and the status word) are cleared on the stream every time; the rest
+  // needs no initialisation.
+  if (kv->l_cap > 0) {
     const cudaError_t e =
         cudaMemsetAsync(scratch, 0, tsa::decode_zero_bytes(B, Hq, Hkv, kv->l_cap, K, n_init,
                                                            n_recent),

@@ -60,10 +60,11 @@ size_t scan_smem_bytes() {
 struct ConsumerBar {
   uint64_t* bar;
   uint32_t phase;
+  long long limit_ns;
   __device__ bool sync() {
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-    const bool ok = mbar_wait(bar, phase);
+    const bool ok = mbar_wait(bar, phase, limit_ns);
     phase ^= 1u;
     return ok;
   }
@@ -154,6 +155,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
   };
 
   const int warp = tid >> 5, lane = tid & 31;
+  const long long lim = a.wait_ns > 0 ? a.wait_ns : kWaitLimitNs;
 
   // ======================= producer warp: the bulk-copy ring ==================
   // Lane 0 waits for free stages and arms the full barrier; a contiguous tile
@@ -173,7 +175,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
       int go = 1, t = -1;
       if (lane == 0) {
         if (j >= kStages &&
-            !mbar_wait_or_abort(&empty[s], (uint32_t)((j / kStages - 1) & 1), &s_abort)) {
+            !mbar_wait_or_abort(&empty[s], (uint32_t)((j / kStages - 1) & 1), &s_abort, lim)) {
           s_abort = 1;
           go = 0;
         }
@@ -218,6 +220,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
       const int64_t r1 = r0 + kTileRows < L ? r0 + kTileRows : L;
       const uint32_t bytes = (uint32_t)(r1 - r0) * kRowBytes;
       uint8_t* dst = ring + s * kTileBytes;
+      // fault injection (tests only): the first stage is never armed or filled
+      if (a.stall_first_copy && blockIdx.x == 0 && j == 0) continue;
       if (lane == 0) {
         fence_proxy_async();
         mbar_expect_tx(&full[s], bytes);
@@ -242,7 +246,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
     if (lane == 0)
       for (int jj = j - kStages + (marker ? 1 : 0) > 0 ? j - kStages + (marker ? 1 : 0) : 0; jj < j;
            ++jj)
-        (void)mbar_wait(&full[jj % kStages], (uint32_t)((jj / kStages) & 1));
+        (void)mbar_wait(&full[jj % kStages], (uint32_t)((jj / kStages) & 1), lim);
     return;
   }
 
@@ -263,7 +267,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
   int cur_unit = -1, unit_end = 0, cur_b = 0, cur_g = 0, head0 = 0;
   int64_t cur_L = 0;
   int rows_since_flush = 0;
-  ConsumerBar cb{&cons_bar, 0u};
+  ConsumerBar cb{&cons_bar, 0u, lim};
 
   // flush the shared histogram of `unit` into global memory (consumers)
   auto flush_hist = [&](int unit) {
@@ -305,7 +309,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
 
   for (int j = 0;; ++j) {
     const int s = j % kStages;
-    if (!mbar_wait_or_abort(&full[s], (uint32_t)((j / kStages) & 1), &s_abort)) {
+    if (!mbar_wait_or_abort(&full[s], (uint32_t)((j / kStages) & 1), &s_abort, lim)) {
       s_abort = 1;
       break;
     }

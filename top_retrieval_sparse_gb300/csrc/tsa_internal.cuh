@@ -34,8 +34,10 @@ __device__ __forceinline__ int hint_bin_of(int32_t w) {
 }
 __device__ __forceinline__ bool hint_wide_of(int32_t w) { return (w >> 16) & 1; }
 
-// Status word codes written by kernels into the workspace (host maps them).
-constexpr int kStatusTimeout = 1;
+// Status word bits written by kernels into the workspace (sticky: only the
+// host clears them, through tsa_workspace_status).
+constexpr int kStatusTimeout = 1;    // a bounded wait expired: the call's outputs are NaN
+constexpr int kStatusBadLength = 2;  // a sequence length outside [0, l_cap] was clamped
 
 // ---------------------------------------------------------------- encoding
 // Order-preserving key of an fp32 value: a > b  <=>  key(a) > key(b).
@@ -150,26 +152,28 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
   return t;
 }
-// Bounded wait on an mbarrier phase: false after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Bounded wait on an mbarrier phase: false after limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer_ns();
   while (true) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if ((long long)(globaltimer_ns() - t0) > kWaitLimitNs) return false;
+    if ((long long)(globaltimer_ns() - t0) > limit_ns) return false;
   }
 }
 // Bounded wait that also gives up as soon as *abort is set (CTA-wide stop).
 __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity,
-                                                   volatile int* abort) {
+                                                   volatile int* abort,
+                                                   long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer_ns();
   while (true) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if ((long long)(globaltimer_ns() - t0) > kWaitLimitNs) return false;
+    if ((long long)(globaltimer_ns() - t0) > limit_ns) return false;
   }
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {

@@ -39,6 +39,12 @@ struct ScanArgs {
   float* wz;                 // [B][Hq][wz_stride] window logits
   int wz_stride;
   int* status;
+  // Bounded waits give up after wait_ns (0: the default limit).  Fault
+  // injection for tests of the error path: with stall_first_copy set, CTA 0
+  // never issues the copy of its first tile, so that its consumers' wait
+  // runs out (bounded) and the call reports a timeout.
+  long long wait_ns;
+  int stall_first_copy;
   TraceBuf trace;
 };
 cudaError_t launch_scan(const ScanArgs& a, int grid, cudaStream_t st, bool pdl);
@@ -61,7 +67,7 @@ struct FinishArgs {
   uint32_t* hist;            // [B][Hq][kHistBins] pool histograms from the scan (cleared)
   int32_t* hint_bin;         // [B][Hq] the scan's emission bin; the next call's is stored
   uint32_t* tile_ctr;        // the scan's tile claims (cleared)
-  int* status;               // (cleared)
+  int* status;               // sticky error bits: a timeout makes the outputs NaN
   uint2* dense;              // [B][Hq][dense_stride] emitted pairs
   int32_t* dense_n;
   int64_t dense_stride;
