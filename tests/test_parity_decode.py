@@ -40,11 +40,12 @@ def test_group_sizes(Hq, Hkv):
 
 
 @pytest.mark.parametrize("Hq,Hkv", [(28, 4), (12, 4)])
-def test_unit_switches_keep_histograms_exact(Hq, Hkv):
+def test_unit_switches_keep_emission_exact(Hq, Hkv):
     """~1000 scan tiles over 4 KV heads: CTAs cross unit boundaries inside
-    their static ranges and through dynamic claims, so a shared histogram is
-    flushed and reused for another unit mid-kernel.  Groups of 7 and 3 heads
-    also leave padding slots in it.  Every head must still select exactly."""
+    their static ranges and through dynamic claims, so every warp closes its
+    emission runs of one head and opens runs of another mid-kernel.  Groups of
+    7 and 3 heads also leave unused query-head columns.  Every head must still
+    select exactly."""
     wl = make_decode("llama128k", L0=65_000, steps=2, B=1, K=512, Hq=Hq, Hkv=Hkv,
                      n_init=0, n_recent=0)
     run_and_check(wl, range(2))
@@ -127,8 +128,8 @@ def test_many_ties_at_threshold():
 
 def test_repeated_calls_reuse_workspace():
     """A zeroed workspace serves call after call: every call clears the
-    counters it used for the next one and keeps only the hint words (whose
-    content never affects the result)."""
+    counters it used for the next one and keeps only the per-head emission
+    keys and margins (whose content never affects the result)."""
     import top_retrieval_sparse_gb300 as tsa
     wl = make_decode("tiny", L0=9000, steps=2)
     dev = "cuda"
@@ -149,11 +150,12 @@ def test_repeated_calls_reuse_workspace():
 
 
 def test_threshold_hint_fallbacks():
-    """The workspace carries a per-head hint bin between calls; exactness must
-    not depend on it.  A zeroed workspace (hint 0: every pool position is
-    emitted, far too many), a hint left by a workload with much larger logits
-    (hint above the new threshold bin) and a hint from a smaller one must all
-    give the oracle's result."""
+    """The workspace carries a per-head emission key between calls; exactness
+    must not depend on it.  A zeroed workspace (key 0: every pool position is
+    emitted, far too many), a key left by a workload with much larger logits
+    (above the new K-th logit: fewer than K pairs, the re-emission path) and a
+    key from a smaller one (far below: many pairs) must all give the oracle's
+    result."""
     import top_retrieval_sparse_gb300 as tsa
     dev = "cuda"
     big = make_decode("tiny", L0=30_000, steps=1, K=300)

@@ -86,10 +86,11 @@ bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 // Device pointers of the exact top-K machinery (key scan + finish).
 struct SelWs {
   int* status;
-  uint32_t* hist;        // counters: zero before a call, cleared by its finish kernel
-  uint32_t* tile_ctr;
+  uint32_t* pf_ctr;      // the key scan's L2 prefetch claims (in the status block)
+  uint32_t* tile_ctr;    // counters: zero before a call, cleared by its finish kernel
   int32_t* dense_n;
-  int32_t* hint_bin;     // persists between calls (any content is safe)
+  uint32_t* emit_key;    // persist between calls (any content is safe)
+  float* emit_margin;
   uint2* dense;
   int64_t dense_stride;
   uint64_t* spill;
@@ -101,8 +102,8 @@ struct SelWs {
 // zero_end) holds the counters that start every call at zero; the hint
 // bins after them persist.
 struct DecodeLayout {
-  size_t zero_begin, status, tile_ctr, hist, dense_n, zero_end;
-  size_t hint_bin, wz, dense, spill, total;
+  size_t zero_begin, status, tile_ctr, dense_n, zero_end;
+  size_t emit_key, emit_margin, wz, dense, spill, total;
   int64_t dense_stride;
   int wz_stride;
 };
@@ -119,10 +120,10 @@ DecodeLayout decode_layout(int B, int Hq, int Hkv, int64_t l_cap, int n_init, in
   L.zero_begin = o;
   L.status = o; o = up(o + 4);
   L.tile_ctr = o; o = up(o + 4);
-  L.hist = o; o = up(o + rows * kHistBins * 4);
   L.dense_n = o; o = up(o + rows * kCtrStride * 4);
   L.zero_end = o;
-  L.hint_bin = o; o = up(o + rows * 4);
+  L.emit_key = o; o = up(o + rows * 4);
+  L.emit_margin = o; o = up(o + rows * 4);
   L.wz = o; o = up(o + rows * (size_t)L.wz_stride * 4);
   L.dense = o; o = up(o + rows * (size_t)L.dense_stride * 8);
   L.spill = o; o = up(o + rows * (size_t)L.dense_stride * 8);
@@ -146,15 +147,15 @@ ScanArgs scan_args(const uint16_t* q, const KvView& view, const int32_t* lens, i
   s.n_recent = n_recent;
   s.head_active = head_active;
   s.active_value = active_value;
-  s.hist = w.hist;
   s.tile_ctr = w.tile_ctr;
-  s.hint_bin = w.hint_bin;
+  s.emit_key = w.emit_key;
   s.dense = w.dense;
   s.dense_n = w.dense_n;
   s.dense_stride = w.dense_stride;
   s.wz = w.wz;
   s.wz_stride = w.wz_stride;
   s.status = w.status;
+  s.pf_ctr = w.pf_ctr;
   s.trace = g_trace;
   s.wait_ns = g_stall_ns;
   s.stall_first_copy = g_stall_ns > 0;
@@ -171,10 +172,11 @@ FinishArgs finish_args(const uint16_t* q, const KvView& view, int Hq, float scal
   f.Hq = Hq;
   f.scale = scale;
   f.K = K;
-  f.hist = w.hist;
-  f.hint_bin = w.hint_bin;
+  f.emit_key = w.emit_key;
+  f.emit_margin = w.emit_margin;
   f.tile_ctr = w.tile_ctr;
   f.status = w.status;
+  f.pf_ctr = w.pf_ctr;
   f.dense = w.dense;
   f.dense_n = w.dense_n;
   f.dense_stride = w.dense_stride;
@@ -183,6 +185,16 @@ FinishArgs finish_args(const uint16_t* q, const KvView& view, int Hq, float scal
   f.wz_stride = w.wz_stride;
   f.trace = g_trace;
   return f;
+}
+
+// The key scan's L2 prefetch (while the previous kernel runs): its claim
+// counter sits in the status block, and it prefetches up to ~80 MiB of key
+// tiles (of the 126 MiB L2), the first tiles of every CTA's range.
+constexpr size_t kPfCtrOffset = 64;
+int prefetch_tiles(int grid) {
+  const int64_t budget = (int64_t)80 << 20;
+  const int64_t per = budget / ((int64_t)(grid > 0 ? grid : 1) * 256 * kRowBytes);
+  return (int)(per > 16 ? 16 : per);
 }
 
 // Persistent scan grid: one CTA per SM, at most one per tile.
@@ -341,9 +353,10 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
   const KvView view = make_view(kv, Hkv);
   SelWs w{};
   w.status = reinterpret_cast<int*>(ws + Lw.status);
-  w.hist = reinterpret_cast<uint32_t*>(ws + Lw.hist);
+  w.pf_ctr = reinterpret_cast<uint32_t*>(ws + Lw.status + kPfCtrOffset);
   w.tile_ctr = reinterpret_cast<uint32_t*>(ws + Lw.tile_ctr);
-  w.hint_bin = reinterpret_cast<int32_t*>(ws + Lw.hint_bin);
+  w.emit_key = reinterpret_cast<uint32_t*>(ws + Lw.emit_key);
+  w.emit_margin = reinterpret_cast<float*>(ws + Lw.emit_margin);
   w.dense = reinterpret_cast<uint2*>(ws + Lw.dense);
   w.dense_n = reinterpret_cast<int32_t*>(ws + Lw.dense_n);
   w.dense_stride = Lw.dense_stride;
@@ -351,11 +364,13 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
   w.wz = reinterpret_cast<float*>(ws + Lw.wz);
   w.wz_stride = Lw.wz_stride;
 
-  // 1. key scan (logits, histograms, emitted pairs, window logits)
+  // 1. key scan (logits, emitted pairs, window logits)
   if (kv->l_cap > 0) {
-    const ScanArgs s = scan_args(static_cast<const uint16_t*>(q), view, lens, 0, B, Hq, n_init,
-                                 n_recent, scale, nullptr, 0, w);
-    if ((e = counted(launch_scan(s, scan_grid(B, view, kv->l_cap), st, true))) != cudaSuccess)
+    ScanArgs s = scan_args(static_cast<const uint16_t*>(q), view, lens, 0, B, Hq, n_init,
+                           n_recent, scale, nullptr, 0, w);
+    const int grid = scan_grid(B, view, kv->l_cap);
+    s.pf_tiles = prefetch_tiles(grid);
+    if ((e = counted(launch_scan(s, grid, st, true))) != cudaSuccess)
       return cuda_fail(e, "scan launch");
   }
   if ((e = stage_mark(1, st)) != cudaSuccess) return cuda_fail(e, "event record");
@@ -442,8 +457,8 @@ namespace {
 constexpr uint32_t kMagic = 0x52544b31u;  // "RTK1"
 
 struct RetopkLayout {
-  size_t zero_begin, status, tile_ctr, hist, dense_n, zero_end;
-  size_t hint_bin, wz, dense, spill, qbar_new, path, cand, mcand, total;
+  size_t zero_begin, status, tile_ctr, dense_n, zero_end;
+  size_t emit_key, emit_margin, wz, dense, spill, qbar_new, path, cand, mcand, total;
   int64_t dense_stride;
   int cand_cap;
 };
@@ -457,10 +472,10 @@ RetopkLayout retopk_layout(const tsa_retopk* s) {
   L.zero_begin = o;
   L.status = o; o = up(o + 4);
   L.tile_ctr = o; o = up(o + 4);
-  L.hist = o; o = up(o + H * kHistBins * 4);
   L.dense_n = o; o = up(o + H * kCtrStride * 4);
   L.zero_end = o;
-  L.hint_bin = o; o = up(o + H * 4);
+  L.emit_key = o; o = up(o + H * 4);
+  L.emit_margin = o; o = up(o + H * 4);
   L.wz = o; o = up(o + 64);  // no window on this path
   L.dense = o; o = up(o + H * (size_t)L.dense_stride * 8);
   L.spill = o; o = up(o + H * (size_t)L.dense_stride * 8);
@@ -597,9 +612,10 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
   float* qbar_new = reinterpret_cast<float*>(ws + Lw.qbar_new);
   SelWs w{};
   w.status = reinterpret_cast<int*>(ws + Lw.status);
-  w.hist = reinterpret_cast<uint32_t*>(ws + Lw.hist);
+  w.pf_ctr = reinterpret_cast<uint32_t*>(ws + Lw.status + kPfCtrOffset);
   w.tile_ctr = reinterpret_cast<uint32_t*>(ws + Lw.tile_ctr);
-  w.hint_bin = reinterpret_cast<int32_t*>(ws + Lw.hint_bin);
+  w.emit_key = reinterpret_cast<uint32_t*>(ws + Lw.emit_key);
+  w.emit_margin = reinterpret_cast<float*>(ws + Lw.emit_margin);
   w.dense = reinterpret_cast<uint2*>(ws + Lw.dense);
   w.dense_n = reinterpret_cast<int32_t*>(ws + Lw.dense_n);
   w.dense_stride = Lw.dense_stride;
@@ -638,7 +654,7 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
     if ((e = counted(launch_retopk_selector(a, smem, s))) != cudaSuccess)
       return cuda_fail(e, "retopk selector launch");
   }
-  // 2. exact-path heads: key scan over all keys (no window): histograms and
+  // 2. exact-path heads: key scan over all keys (no window): the
   //    emitted pairs; launched after the selector has decided the paths
   if ((e = counted(launch_scan(scan_args(static_cast<const uint16_t*>(q), view, nullptr, len, 1,
                                          Hq, 0, 0, scale, path, 1, w),

@@ -10,12 +10,18 @@
 // One thread-block cluster of NC CTAs (NC = 8, 4, 2 or 1, chosen at launch
 // so that all clusters are resident at once, one CTA per SM) per (sequence,
 // query head):
-//   0. every CTA reads the head's 11-bit histogram and finds the threshold
-//      bin b* (the largest bin whose suffix count reaches K); if the scan's
-//      emission bin (the hint) was above b*, the cluster re-emits the head's
-//      pool pairs with bin >= b*, recomputing the logits with the scan's own
-//      tensor-core fragment arithmetic so that every logit -- and so every
-//      bin -- is bit-identical to the scan's; the next call's hint is stored;
+//   0. every CTA counts the 11-bit bins (top bits of the order-preserving
+//      logit key) of its slice of the head's emitted pairs, the counts are
+//      summed over the cluster (distributed shared memory), and the
+//      threshold bin b* is the largest bin whose suffix count reaches K.  The
+//      scan emitted every pool position whose logit key is >= the head's
+//      emission key, so when that is at least K pairs the K-th largest key
+//      is among them and b* (and the selection below) is exact, even if b*'s
+//      bin was emitted only in part; otherwise the cluster re-scores the
+//      head's keys to count every bin, then re-emits the pool pairs with bin
+//      >= b*, recomputing the logits with the scan's own tensor-core fragment
+//      arithmetic so that every logit -- and so every bin -- is bit-identical
+//      to the scan's;
 //   1. each CTA reads its 1/NC slice of the head's pair list (the first
 //      batch is already in flight during step 0): pairs above b* are
 //      selected outright and kept in shared memory, pairs in b* are the
@@ -28,10 +34,11 @@
 //      split evenly over the cluster; each warp gathers V for its rows with
 //      half-warp 16-byte loads, keeping (max, sum, o) per set in base 2;
 //      every CTA pushes its partials into rank 0's shared memory, and rank
-//      0 applies Eq. 4-5.
+//      0 applies Eq. 4-5 and stores the next call's emission key (the K-th
+//      logit minus a margin).
 // ReTopK steps use the same kernel: a reuse head has no pair list; each CTA
 // rescores its share of the head's candidates A_t (exact logits e_i on the
-// key rows) and all of them compete in the radix (no histogram, no hint); no
+// key rows) and all of them compete in the radix (no bins, no emission key); no
 // head has a window, and rank 0 pushes (qbar_t, S_t) into the query-support
 // FIFO.
 // Launched as a programmatic dependent of the kernel that wrote the lists.
@@ -57,7 +64,8 @@ struct FinShared {
   uint64_t cand[NC > 1 ? kAllCap : 1];  // rank keys of all threshold-bin candidates, cluster order
   uint64_t mycand[kMyCap];        // this CTA's candidates (read by the cluster)
   uint2 sel[kSelCap];             // this CTA's above-b* pairs (position, logit bits)
-  uint32_t hist[kHistBins];       // radix round histogram
+  uint32_t hist[kHistBins];       // this CTA's bin counts, then the radix round histogram
+  uint32_t chist[kHistBins];      // the cluster's bin counts (bins at or above a floor)
   float wo[W][2][kD];             // warp partials: [set][d], set 0 window, 1 selected
   float wm[W][2], wl[W][2];
   float mo[NC][2][kD];            // rank 0: the CTA partials, pushed by each CTA
@@ -162,6 +170,59 @@ __device__ void reemit(const FinishArgs& a, int b, int h, int g, int G, int64_t 
     if (eb) {
       const int64_t s = slot0 + __popc(ma) + __popc(mb & lt);
       if (s < a.dense_stride) drow[s] = make_uint2((uint32_t)ib, __float_as_uint(zb));
+    }
+  }
+}
+
+// The rare path's count: the 11-bit bins of head bh's pool logits on the
+// rows of cluster rank `rank` (the rows and arithmetic of reemit), added to
+// sh.hist (zeroed by the caller) with one shared atomic per distinct bin per
+// warp instruction.
+template <int W, class Sh>
+__device__ void rescore_count(const FinishArgs& a, int b, int h, int g, int G, int64_t L,
+                              int rank, int nc, Sh& sh) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int gr = lane >> 2, tq = lane & 3;
+  const int hl = h - g * G;
+  const int head0 = b * a.Hq + g * G;
+  uint32_t qb[4][4];
+  const uint16_t* qp = a.q + ((int64_t)head0 + (gr < G ? gr : 0)) * kD;
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (gr < G) w = *reinterpret_cast<const uint4*>(qp + 8 * (4 * p + tq));
+    qb[p][0] = w.x; qb[p][1] = w.y; qb[p][2] = w.z; qb[p][3] = w.w;
+  }
+  const int64_t r0 = L * rank / nc, r1 = L * (rank + 1) / nc;
+  const bool mine = tq == (hl >> 1);
+  for (int64_t base = r0 + 16 * wid; base < r1; base += 16 * W) {
+    const int64_t ia = base + gr, ib = base + gr + 8;
+    uint4 W4[4], X4[4];
+    const uint16_t* ka = a.kv.k + kv_row(a.kv, b, g, ia < r1 ? ia : r0);
+    const uint16_t* kb = a.kv.k + kv_row(a.kv, b, g, ib < r1 ? ib : r0);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      W4[p] = ia < r1 ? *reinterpret_cast<const uint4*>(ka + 8 * (4 * p + tq))
+                      : make_uint4(0u, 0u, 0u, 0u);
+      X4[p] = ib < r1 ? *reinterpret_cast<const uint4*>(kb + 8 * (4 * p + tq))
+                      : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      mma_bf16(c0, W4[p].x, X4[p].x, W4[p].y, X4[p].y, qb[p][0], qb[p][1]);
+      mma_bf16(c1, W4[p].z, X4[p].z, W4[p].w, X4[p].w, qb[p][2], qb[p][3]);
+    }
+    const bool odd = hl & 1;
+    const float za = (odd ? c0[1] + c1[1] : c0[0] + c1[0]) * a.scale;
+    const float zb = (odd ? c0[3] + c1[3] : c0[2] + c1[2]) * a.scale;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int64_t i = k ? ib : ia;
+      const bool ok = mine && i < r1 && !in_window(i, L, a.n_init, a.n_recent);
+      const uint32_t bin = ok ? f2key(k ? zb : za) >> kHistShift : 0xffffffffu;
+      const unsigned peers = __match_any_sync(0xffffffffu, bin);
+      if (ok && __ffs(peers) - 1 == lane) atomicAdd(&sh.hist[bin], (uint32_t)__popc(peers));
     }
   }
 }
@@ -272,16 +333,36 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
     }
   }
   pdl_wait();     // pairs, bins and window logits come from the scan
+  // The next key scan's prefetch claims start from zero; the reset is made
+  // visible before this CTA lets the next kernel be scheduled.
+  if (bh == 0 && rank == 0) {
+    if (tid == 0 && a.pf_ctr) {
+      *a.pf_ctr = 0u;
+      __threadfence();
+    }
+    __syncthreads();
+  }
   pdl_trigger();  // the next kernel may be scheduled (it writes nothing
                   // this kernel reads until this kernel has completed)
   trace.mark(1);
+
+  // The first decisions' inputs sit at fixed addresses: the status word, the
+  // list size, the emission key and margin factor and, on a ReTopK step, the
+  // head's path and candidate count are all requested before any is used
+  // (with the sequence length), not one after another.
+  const int status_in = __ldcg(a.status);
+  const int64_t n_in = __ldcg(a.dense_n + (int64_t)bh * kCtrStride);
+  const uint32_t ekey = __ldcg(a.emit_key + bh);
+  const float mg_in = __ldcg(a.emit_margin + bh);
+  const int path_in = RT ? __ldcg(a.path + bh) : 1;
+  const int mc_in = RT ? __ldcg(a.mcand + bh) : 0;
 
   // A bounded wait of the key scan (this call's, or an earlier one on this
   // workspace: the bit is sticky until the host reads it) gave up: the lists
   // and histograms are incomplete.  Every CTA reads the same word, so the
   // whole grid takes this path: NaN outputs, the counters cleared for the next
   // call, no FIFO push (the ReTopK state keeps its previous entry).
-  if (__ldcg(a.status) & kStatusTimeout) {
+  if (status_in & kStatusTimeout) {
     if (rank == 0) {
       const float nan = __int_as_float(0x7fc00000);
       if (tid < kD) a.out[(int64_t)bh * kD + tid] = nan;
@@ -291,8 +372,6 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
           if (a.topk_idx) a.topk_idx[(int64_t)bh * a.topk_stride + q] = -1;
           if (a.topk_score) a.topk_score[(int64_t)bh * a.topk_stride + q] = nan;
         }
-      uint4* hz = reinterpret_cast<uint4*>(a.hist + (int64_t)bh * kHistBins);
-      for (int q = tid; q < kHistBins / 4; q += kFinThreads) hz[q] = make_uint4(0u, 0u, 0u, 0u);
       if (tid == 0) {
         a.dense_n[(int64_t)bh * kCtrStride] = 0;
         if (bh == 0) *a.tile_ctr = 0;
@@ -300,34 +379,6 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
     }
     return;
   }
-  // The length contract (0 <= lens[b] <= l_cap) is checked here: an
-  // out-of-range length was clamped by both kernels; flag it for the host.
-  if (a.lens && rank == 0 && h == 0 && tid == 0) {
-    const int32_t Lr = a.lens[b];
-    if (Lr < 0 || (int64_t)Lr > a.kv.l_cap) atomicOr(a.status, kStatusBadLength);
-  }
-
-  // The first decisions' inputs sit at fixed addresses: the list size, the
-  // hint word, this thread's histogram bins (kBpt of them, from the top) and,
-  // on a ReTopK step, the head's path and candidate count are all requested
-  // before any is used (with the sequence length), not one after another.
-  const int64_t n_in = __ldcg(a.dense_n + (int64_t)bh * kCtrStride);
-  const int32_t hw = __ldcg(a.hint_bin + bh);
-  uint32_t hb[kBpt];  // bins 2047-kBpt*tid-r, r < kBpt
-  {
-    const uint32_t* hh = a.hist + (int64_t)bh * kHistBins;
-#pragma unroll
-    for (int q = 0; q < kBpt / 4; ++q) {
-      const uint4 x =
-          __ldcg(reinterpret_cast<const uint4*>(hh + kHistBins - 4 * (q + 1) - kBpt * tid));
-      hb[4 * q] = x.w;
-      hb[4 * q + 1] = x.z;
-      hb[4 * q + 2] = x.y;
-      hb[4 * q + 3] = x.x;
-    }
-  }
-  const int path_in = RT ? __ldcg(a.path + bh) : 1;
-  const int mc_in = RT ? __ldcg(a.mcand + bh) : 0;
   const int64_t L = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
   const int64_t nw = window_count(L, a.n_init, a.n_recent);
   // a ReTopK reuse head selects among its |A_t| rescored candidates
@@ -350,61 +401,100 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
     pre[u] = jj < s1 ? __ldcg(lrow + jj) : make_uint2(0xffffffffu, 0u);
   }
 
-  // ---- 0. threshold bin b*, the emission check, the next hint ----
-  // Every CTA of the cluster reads the head's histogram and decides alike.
-  int bstar = -1, redo = 0, ebin = 0, next_hint = 0;
-  bool wide = false;
-  if (need > 0 && !reuse) {  // (a reuse head has no histogram: all its candidates compete)
-    const int used = hint_bin_of(hw);
-    wide = hint_wide_of(hw);
-    if (need < P) {
-      // pairs one call may emit, and the margin (bins below b*) the hint
-      // keeps: wider for a head whose b* has once fallen below its hint
-      const int64_t budget = wide ? 8 * (int64_t)need + 16384 : 3 * (int64_t)need + 4096;
-      const int margin = wide ? 4 : 2;
-      const uint32_t tgt[2] = {(uint32_t)need, (uint32_t)(budget + 1 < P ? budget + 1 : P + 1)};
-      uint32_t mine = 0;
+  // ---- 0. threshold bin b* and the emission check ----
+  // The largest bin whose suffix count reaches tgt[k], over a count array in
+  // shared memory restricted to bins >= floor (-1: no such bin).
+  auto suffix_bins = [&](const uint32_t* cnt, int floor, const uint32_t (&tgt)[2],
+                         int (&fb)[2]) -> uint32_t {
+    uint32_t c[kBpt], mine = 0;
 #pragma unroll
-      for (int r = 0; r < kBpt; ++r) mine += hb[r];
-      if (tid == 0) sh.scal[0] = sh.scal[1] = -1;
-      int tot;
-      const uint32_t excl = (uint32_t)fin_scan<W>((int)mine, sh, &tot);
+    for (int r = 0; r < kBpt; ++r) {
+      const int bin = kHistBins - 1 - kBpt * tid - r;
+      c[r] = bin >= floor ? cnt[bin] : 0u;
+      mine += c[r];
+    }
+    if (tid == 0) sh.scal[0] = sh.scal[1] = -1;
+    int tot;
+    const uint32_t excl = (uint32_t)fin_scan<W>((int)mine, sh, &tot);
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        uint32_t acc = excl;
+    for (int k = 0; k < 2; ++k) {
+      uint32_t acc = excl;
 #pragma unroll
-        for (int r = 0; r < kBpt; ++r) {
-          if (acc < tgt[k] && acc + hb[r] >= tgt[k]) sh.scal[k] = kHistBins - 1 - kBpt * tid - r;
-          acc += hb[r];
-        }
+      for (int r = 0; r < kBpt; ++r) {
+        if (acc < tgt[k] && acc + c[r] >= tgt[k]) sh.scal[k] = kHistBins - 1 - kBpt * tid - r;
+        acc += c[r];
       }
-      __syncthreads();
-      bstar = sh.scal[0];  // largest bin whose suffix count reaches need
-      const int bbud = sh.scal[1];
-      // next hint: `margin` bins (a quarter octave of logit each) below b*,
-      // so that step-to-step shifts of b* keep it valid, and no lower than
-      // the emission budget allows (bins above bbud hold at most `budget`
-      // pairs).  A lower hint that still fits the budget is kept: the hint
-      // falls at once and rises only when the emission outgrows the budget.
-      const int lo = bbud + 1 > 0 ? bbud + 1 : 0;
-      const int target = bstar - margin > lo ? bstar - margin : lo;
-      int hnt = used < target && used >= lo ? used : target;
-      next_hint = hnt < bstar ? hnt : bstar;
-      redo = used > bstar;  // the scan skipped pairs of bins >= b*
+    }
+    __syncthreads();
+    fb[0] = sh.scal[0];
+    fb[1] = sh.scal[1];
+    __syncthreads();  // scal is rewritten later
+    return (uint32_t)tot;
+  };
+  // The cluster's counts of bins >= floor into sh.chist.  After the cluster
+  // barrier every CTA reads the others' sh.hist: none may rewrite it before
+  // the next cluster barrier.
+  auto cluster_counts = [&](int floor) {
+    cluster_sync_all();
+    for (int q = floor + tid; q < kHistBins; q += kFinThreads) {
+      uint32_t c = sh.hist[q];
+#pragma unroll
+      for (int r = 1; r < NC; ++r) c += ld_dsmem_u32(&sh.hist[q], (uint32_t)((rank + r) % NC));
+      sh.chist[q] = c;
+    }
+    __syncthreads();
+  };
+  int bstar = -1, redo = 0, ebin = 0;
+  const int used = need > 0 ? (int)(ekey >> kHistShift) : 0;  // the emission key's bin
+  const uint32_t tgt[2] = {(uint32_t)need, (uint32_t)need};
+  if (need > 0 && !reuse) {  // (a reuse head has no bins: all its candidates compete)
+    // the bins of this CTA's slice of the emitted pairs (the first batch is
+    // in registers), one shared atomic per distinct bin per warp instruction
+    for (int q = tid; q < kHistBins; q += kFinThreads) sh.hist[q] = 0;
+    __syncthreads();
+    for (int64_t jb = s0; jb < s1; jb += kFinThreads * kFinU) {
+#pragma unroll
+      for (int u = 0; u < kFinU; ++u) {
+        const int64_t jj = jb + u * kFinThreads + tid;
+        const uint2 pv = jb == s0 ? pre[u]
+                                  : (jj < s1 ? __ldcg(lrow + jj) : make_uint2(0xffffffffu, 0u));
+        const bool ok = pv.x != 0xffffffffu;
+        const uint32_t bin = ok ? f2key(__uint_as_float(pv.y)) >> kHistShift : 0xffffffffu;
+        const unsigned peers = __match_any_sync(0xffffffffu, bin);
+        if (ok && __ffs(peers) - 1 == lane) atomicAdd(&sh.hist[bin], (uint32_t)__popc(peers));
+      }
+    }
+    __syncthreads();
+    cluster_counts(used);
+    int fb[2];
+    const uint32_t total = suffix_bins(sh.chist, used, tgt, fb);
+    if (need < P) {
+      bstar = fb[0];  // -1: fewer than K pairs emitted, b* lies below the emission key
+      redo = bstar < 0;
       ebin = bstar;
-    } else {  // every pool position is selected
-      redo = used > 0;
+    } else {  // every pool position is selected: all of them must have been emitted
+      redo = (int64_t)total < P;
       ebin = 0;
-      next_hint = 0;
     }
   }
   phases.mark(1);
   trace.info = (uint32_t)min(n, (int64_t)0x7fffffff);
-  phases.info = ((uint32_t)redo << 31) | ((uint32_t)(bstar & 0x7fff) << 16) |
-                (uint32_t)(need > 0 ? hint_bin_of(hw) : 0);
-  // ---- re-emission when the scan's hint missed (rare: first call, shifts) ----
+  phases.info = ((uint32_t)redo << 31) | ((uint32_t)(bstar & 0x7fff) << 16) | (uint32_t)used;
+  // ---- re-emission when the emission key missed the top-K (rare) ----
   if (redo) {  // uniform over the cluster
-    cluster_sync_all();  // every CTA has read the old list size
+    cluster_sync_all();  // every CTA has read the old list size and the remote counts
+    if (need < P) {  // b* over every pool key of the head
+      for (int q = tid; q < kHistBins; q += kFinThreads) sh.hist[q] = 0;
+      __syncthreads();
+      rescore_count<W>(a, b, h, g, G, L, rank, NC, sh);
+      __syncthreads();
+      cluster_counts(0);
+      int fb[2];
+      suffix_bins(sh.chist, 0, tgt, fb);
+      bstar = fb[0];  // exists: the pool holds P > need positions
+      ebin = bstar;
+      cluster_sync_all();  // the remote counts have been read
+    }
     if (rank == 0 && tid == 0) {
       a.dense_n[(int64_t)bh * kCtrStride] = 0;
       __threadfence();
@@ -515,15 +605,11 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   }
   __syncthreads();
   const int nabove = sh.aoff[NC], ncand = sh.coff[NC];
-  // Every CTA of the cluster has read the head's histogram, list size and
-  // hint: clear the counters for the next call (the workspace contract).
-  if (rank == 0) {
-    uint4* hz = reinterpret_cast<uint4*>(a.hist + (int64_t)bh * kHistBins);
-    for (int q = tid; q < kHistBins / 4; q += kFinThreads) hz[q] = make_uint4(0u, 0u, 0u, 0u);
-    if (tid == 0) {
-      a.dense_n[(int64_t)bh * kCtrStride] = 0;
-      if (bh == 0) *a.tile_ctr = 0;
-    }
+  // Every CTA of the cluster has read the head's list size and key: clear
+  // the counters for the next call (the workspace contract).
+  if (rank == 0 && tid == 0) {
+    a.dense_n[(int64_t)bh * kCtrStride] = 0;
+    if (bh == 0) *a.tile_ctr = 0;
   }
   // candidate j of the cluster (cluster order): CTA c's list, local index i
   auto cand_remote = [&](int jc) -> uint64_t {
@@ -893,8 +979,34 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
       }
     }
   }
-  if (need > 0 && !reuse && rank == 0 && tid == 0)  // read by every CTA long before this point
-    a.hint_bin[bh] = next_hint | ((wide || redo) ? 1 << 16 : 0);
+  // The length contract (0 <= lens[b] <= l_cap) is checked here: an
+  // out-of-range length was clamped by both kernels; flag it for the host.
+  if (a.lens && rank == 0 && h == 0 && tid == 0) {
+    const int32_t Lr = a.lens[b];
+    if (Lr < 0 || (int64_t)Lr > a.kv.l_cap) atomicOr(a.status, kStatusBadLength);
+  }
+  // The next call's emission key: the K-th logit z_T (the threshold's logit,
+  // or the lower edge of b*'s bin when all its candidates were taken) minus a
+  // margin f * 0.2 * (|z_T| + 1).  Across the decode steps of the synthetic
+  // workloads the K-th logit fell by at most 16 % of |z| + 1 from one step to
+  // the next, and a margin of 0.2 (|z| + 1) emits about 2.5 K pairs.  The
+  // per-head factor f doubles after a re-emission (at most 8) and decays back
+  // to 1 by 10 % per call.  Any stored value is safe: only the cost depends
+  // on it.
+  if (need > 0 && !reuse && rank == 0 && tid == 0) {  // read by every CTA long before this point
+    float f = mg_in;
+    if (!(f >= 1.f) || !(f <= 8.f)) f = 1.f;  // a new or unset state
+    f = redo ? fminf(2.f * f, 8.f) : fmaxf(1.f, 0.9f * f);
+    uint32_t next = 0u;
+    if (need < P && bstar >= 0) {
+      const float zref = cmode == 2 ? key2f((uint32_t)(T >> 32))
+                                    : key2f((uint32_t)bstar << kHistShift);
+      const float ze = zref - f * 0.2f * (fabsf(zref) + 1.f);
+      next = ze == ze && fabsf(ze) < INFINITY ? f2key(ze) : 0u;
+    }
+    a.emit_key[bh] = next;
+    a.emit_margin[bh] = f;
+  }
   if (RT && rank == 0) {  // ReTopK: (qbar_t, S_t) over the oldest FIFO entry
     const int64_t hc = (int64_t)bh * a.C + a.slot;
     if (tid < kD) a.cache_qbar[hc * kD + tid] = a.push_qbar[(int64_t)bh * kD + tid];

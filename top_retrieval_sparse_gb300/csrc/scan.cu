@@ -20,19 +20,19 @@
 //     both operands so that every lane reads its A fragment of two k-steps
 //     as one contiguous 16-byte shared load (rows are 256 bytes apart, so a
 //     load phase sees a 2-way bank conflict);
-//   * the radix histogram (top 11 bits of the order-preserving key) of every
-//     active head is built in shared memory (two 16-bit counters per word)
-//     over positions outside the static window and flushed to global memory
-//     with one atomic per non-empty bin; window logits are written out;
-//   * pool positions whose bin is >= the head's hint bin are emitted as
-//     (position, logit) pairs into the head's dense list; each warp
-//     bump-allocates runs of 8 slots (one global atomic per run) and pads the
-//     tail of its last run with sentinels -- no logit array is written or
-//     re-read;
-//   * the threshold bin b* of each head, the check that the emitted pairs
-//     hold every position of bins >= b* and the re-emission of heads whose
-//     hint was above b* are the finish kernel's: exactness never depends on
-//     the hint, only the cost does.
+//   * pool positions (outside the static window) whose bin -- the top 11
+//     bits of the order-preserving logit key -- is >= the head's hint bin
+//     are emitted as (position, logit) pairs into the head's dense list; each
+//     warp bump-allocates runs of 8 slots (one global atomic per run) and
+//     pads the tail of its last run with sentinels -- no logit array is
+//     written or re-read; window logits are written out;
+//   * no histogram is kept here: the finish kernel counts the emitted pairs'
+//     bins itself to find the threshold bin b*, checks that the emission
+//     reached below b* and, when it did not, re-scores the head's keys to
+//     find b* and re-emits: exactness never depends on the hint, only the
+//     cost does.  (A shared-memory histogram of every pool position cost the
+//     consumers as much as the emission: with both, the 128K step's tile
+//     loop was 17 % slower than with either alone.)
 #include "tsa_internal.cuh"
 #include "tsa_kernels.h"
 
@@ -44,43 +44,20 @@ constexpr int kScanThreads = kConsumers + 32;      // + one producer warp
 constexpr int kTileRows = 16 * kScanWarps;         // one m16 block per consumer warp
 constexpr int kTileBytes = kTileRows * kRowBytes;  // 64 KiB
 constexpr int kStages = 3;
-constexpr int kHistWords = kHistBins / 2;          // two 16-bit bins per word
-constexpr int kFlushRows = 65535 - kTileRows;      // flush before a 16-bit bin can wrap
 
-// HP: query heads per KV head rounded up to 1, 2, 4 or 8 (histogram slots).
-template <int HP>
 size_t scan_smem_bytes() {
-  return (size_t)kStages * kTileBytes + (size_t)HP * kHistWords * 4 + 2 * kStages * 8 +
-         (kMaxUnits + 1) * 4 + 64;
+  return (size_t)kStages * kTileBytes + 2 * kStages * 8 + (kMaxUnits + 1) * 4 + 64;
 }
 
-// Barrier over the consumer warps with a bounded wait: an mbarrier that
-// takes one arrival per warp.  Returns false after the wait limit, so that
-// a warp that has stopped (after an abort) cannot hang the others.
-struct ConsumerBar {
-  uint64_t* bar;
-  uint32_t phase;
-  long long limit_ns;
-  __device__ bool sync() {
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-    const bool ok = mbar_wait(bar, phase, limit_ns);
-    phase ^= 1u;
-    return ok;
-  }
-};
-
-template <int HP>
 __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
   TraceScope trace(a.trace, kTrScan);
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
-  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kStages * kTileBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(hist + HP * kHistWords);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kTileBytes);
   uint64_t* empty = full + kStages;
   int* unit_tiles = reinterpret_cast<int*>(empty + kStages);  // prefix over units
   __shared__ volatile int s_abort;
-  __shared__ uint64_t cons_bar;
+  __shared__ volatile int s_started;  // the consumers have passed the dependency wait
   __shared__ int stage_tile[kStages];  // tile of each ring stage (-1: no more tiles)
 
   if (a.head_active) pdl_wait();  // the activity flags come from the previous grid
@@ -117,24 +94,20 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
     }
     if (tid == 0) unit_tiles[nunits] = run;
   }
-  for (int i = tid; i < HP * kHistWords; i += kScanThreads) hist[i] = 0;
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kScanWarps);
     }
-    mbar_init(&cons_bar, kScanWarps);
     fence_mbar_init();
     s_abort = 0;
+    s_started = 0;
   }
   __syncthreads();
 
   // Contiguous static ranges; with many tiles per CTA the last 10 % are
   // claimed one tile at a time (global counter) by whichever CTA is free
   // first, so that CTAs whose share of HBM bandwidth is smaller end no later.
-  // A claimed tile is usually a unit switch of its own (a histogram flush),
-  // which costs more than it balances when each CTA has few tiles (measured:
-  // fully static is fastest at 27 tiles per CTA, 10 % at 216).
   const int total = unit_tiles[nunits];
   if (total == 0) return;
   const int grid = gridDim.x;
@@ -173,6 +146,41 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
     for (;; ++j) {
       const int s = j % kStages;
       int go = 1, t = -1;
+      // The ring is full and the consumers still wait for the previous
+      // kernel: put the time to use by prefetching key tiles into L2, for
+      // any CTA (the claim order is tile-major, so every CTA's first tiles
+      // come first: CTAs that only start when the previous kernel leaves
+      // their SM find their first tiles in L2).
+      // Lane 0 claims 32 items per atomic and every lane prefetches one.
+      if (j == kStages && a.pf_ctr && a.pf_tiles > 0) {
+        const uint32_t items = (uint32_t)grid * (uint32_t)a.pf_tiles;
+        while (true) {
+          uint32_t base = 0xffffffffu;
+          if (lane == 0 && !s_started && !s_abort) base = atomicAdd(a.pf_ctr, 32u);
+          base = __shfl_sync(0xffffffffu, base, 0);
+          if (base >= items) break;
+          const uint32_t i = base + (uint32_t)lane;
+          const int c = (int)(i % (uint32_t)grid), jj = (int)(i / (uint32_t)grid);
+          const int tt = (int)((int64_t)stat * c / grid) + jj;
+          if (i < items && tt < (int)((int64_t)stat * (c + 1) / grid)) {
+            const int unit = locate(tt);
+            const int b = unit / a.kv.Hkv, g = unit % a.kv.Hkv;
+            const int64_t L = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
+            const int64_t r0 = (int64_t)(tt - unit_tiles[unit]) * kTileRows;
+            const int64_t r1 = r0 + kTileRows < L ? r0 + kTileRows : L;
+            if (!a.kv.page_table) {
+              bulk_prefetch_l2(a.kv.k + kv_row(a.kv, b, g, r0), (uint32_t)(r1 - r0) * kRowBytes);
+            } else {
+              const int64_t ps = (int64_t)1 << a.kv.page_shift;
+              for (int64_t r = r0; r < r1; r += ps) {
+                const int64_t e = r + ps < r1 ? r + ps : r1;
+                bulk_prefetch_l2(a.kv.k + kv_row(a.kv, b, g, r), (uint32_t)(e - r) * kRowBytes);
+              }
+            }
+          }
+          __syncwarp();
+        }
+      }
       if (lane == 0) {
         if (j >= kStages &&
             !mbar_wait_or_abort(&empty[s], (uint32_t)((j / kStages - 1) & 1), &s_abort, lim)) {
@@ -255,42 +263,20 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
   // previous kernel finishes; its consumers read hints and write counters,
   // pairs and logits only after that kernel has completed.
   pdl_wait();
+  if (tid == 0) s_started = 1;  // the producer stops prefetching
   const int gr = lane >> 2;  // A rows gr, gr+8 / B column (query head) gr
   const int tq = lane & 3;   // k-slot group / C columns 2tq, 2tq+1
 
   uint32_t qb[4][4];         // B fragments: head gr, d in [8(4p+tq), +8) for p < 4
   bool on[2] = {false, false};  // heads 2tq, 2tq+1 are active
-  int hint[2] = {0, 0};         // emission bins of heads 2tq, 2tq+1
+  uint32_t ekey[2] = {0u, 0u};  // emission keys of heads 2tq, 2tq+1
   bool lane_on = false;         // lane h < G: head h takes part (run owner)
   int run_ptr = 0;              // lane h < G: next free slot of this warp's run for head h
   int run_left = 0;             //            slots left in that run
   int cur_unit = -1, unit_end = 0, cur_b = 0, cur_g = 0, head0 = 0;
   int64_t cur_L = 0;
-  int rows_since_flush = 0;
-  ConsumerBar cb{&cons_bar, 0u, lim};
+  bool aborted = false;
 
-  // flush the shared histogram of `unit` into global memory (consumers)
-  auto flush_hist = [&](int unit) {
-    const int b = unit / a.kv.Hkv, g = unit % a.kv.Hkv;
-    if (!cb.sync()) s_abort = 1;  // every warp's counts are in the shared histogram
-    for (int w = tid; w < HP * kHistWords; w += kConsumers) {
-      const uint32_t v = hist[w];
-      if (v) {
-        const int hl = w / kHistWords;
-        uint32_t* gh = a.hist + (int64_t)(b * a.Hq + g * G + hl) * kHistBins +
-                       2 * (w % kHistWords);
-        // both bins of the word in one 64-bit atomic: a bin's count stays
-        // below 2^31, so the low half never carries into the high one
-        atomicAdd(reinterpret_cast<unsigned long long*>(gh),
-                  (unsigned long long)(v & 0xffffu) | ((unsigned long long)(v >> 16) << 32));
-        hist[w] = 0;
-      }
-    }
-    // no warp counts the next tile (possibly of another unit) into a word
-    // that another thread has yet to flush and clear
-    if (!cb.sync()) s_abort = 1;
-    rows_since_flush = 0;
-  };
   // this warp leaves the current unit: pad the unused tail of its runs with
   // sentinels
   auto close_runs = [&]() {
@@ -302,22 +288,18 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
     run_ptr = 0;
     run_left = 0;
   };
-  auto finish_unit = [&](int unit) {
-    flush_hist(unit);
-    close_runs();
-  };
-
   for (int j = 0;; ++j) {
     const int s = j % kStages;
     if (!mbar_wait_or_abort(&full[s], (uint32_t)((j / kStages) & 1), &s_abort, lim)) {
       s_abort = 1;
+      aborted = true;
       break;
     }
     const int t = stage_tile[s];  // written by the producer before it armed the stage
     if (t < 0) break;             // no more tiles (same stage, same j, for every warp)
-    if (t >= unit_end) {  // entering a new unit (all consumers at the same tile)
+    if (t >= unit_end) {  // entering a new unit (each warp on its own: no barrier)
       const int unit = locate(t);
-      if (cur_unit >= 0) finish_unit(cur_unit);
+      if (cur_unit >= 0) close_runs();
       cur_unit = unit;
       unit_end = unit_tiles[unit + 1];
       cur_b = unit / a.kv.Hkv;
@@ -329,7 +311,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
         const int hl = 2 * tq + e;
         const int bh = head0 + hl;
         on[e] = hl < G && (!a.head_active || a.head_active[bh] == a.active_value);
-        hint[e] = on[e] ? hint_bin_of(__ldcg(a.hint_bin + bh)) : 0;
+        ekey[e] = on[e] ? __ldcg(a.emit_key + bh) : 0u;
       }
       lane_on = lane < G && (!a.head_active || a.head_active[head0 + lane] == a.active_value);
       const uint16_t* qp = a.q + ((int64_t)head0 + (gr < G ? gr : 0)) * kD;
@@ -339,10 +321,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
         if (gr < G) w = *reinterpret_cast<const uint4*>(qp + 8 * (4 * p + tq));
         qb[p][0] = w.x; qb[p][1] = w.y; qb[p][2] = w.z; qb[p][3] = w.w;
       }
-    } else if (rows_since_flush > kFlushRows) {
-      flush_hist(cur_unit);
     }
-    rows_since_flush += kTileRows;
     const int tile = t - unit_tiles[cur_unit];
     if (j == 0) trace.mark(1);
     {
@@ -370,16 +349,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
         const int64_t i = rowA + ((e >> 1) << 3);
         zv[e] = (c0[e] + c1[e]) * a.scale;
         if (on[e & 1] && i < cur_L) {
-          const uint32_t bin = f2key(zv[e]) >> kHistShift;
           if (!pool_tile && in_window(i, cur_L, a.n_init, a.n_recent)) {
             const int64_t wa = a.n_init < cur_L ? a.n_init : cur_L;
             const int64_t lo = cur_L - a.n_recent > wa ? cur_L - a.n_recent : wa;
             const int64_t wj = i < wa ? i : wa + (i - lo);
             a.wz[(int64_t)(head0 + 2 * tq + (e & 1)) * a.wz_stride + wj] = zv[e];
           } else {
-            atomicAdd(&hist[(2 * tq + (e & 1)) * kHistWords + (bin >> 1)],
-                      1u << ((bin & 1) << 4));
-            if ((int)bin >= hint[e & 1]) emit |= 1u << e;
+            if (f2key(zv[e]) >= ekey[e & 1]) emit |= 1u << e;
           }
         }
       }
@@ -437,25 +413,22 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
     }
   }
 
-  // every consumer warp has left the loop (bounded: a warp that stopped
-  // early makes the others time out here instead of hanging)
-  if (!cb.sync()) s_abort = 1;
-  if (s_abort) {
-    if (tid == 0) atomicOr(a.status, kStatusTimeout);
+  // a warp whose bounded wait expired reports it; its pairs are incomplete
+  if (aborted) {
+    if (lane == 0) atomicOr(a.status, kStatusTimeout);
     return;
   }
   trace.mark(2);
-  if (cur_unit >= 0) finish_unit(cur_unit);
+  if (cur_unit >= 0) close_runs();
 }
 
-template <int HP>
 static cudaError_t launch_scan_t(const ScanArgs& a, int grid, cudaStream_t st, bool pdl) {
-  const size_t smem = scan_smem_bytes<HP>();
+  const size_t smem = scan_smem_bytes();
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(scan_kernel<HP>,
+    cudaError_t e = cudaFuncSetAttribute(scan_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
@@ -470,22 +443,14 @@ static cudaError_t launch_scan_t(const ScanArgs& a, int grid, cudaStream_t st, b
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, scan_kernel<HP>, a);
+  return cudaLaunchKernelEx(&cfg, scan_kernel, a);
 }
-
-static int hist_heads(int G) { return G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8; }
 
 int scan_tile_rows() { return kTileRows; }
 int scan_tile_warps() { return kScanWarps; }
 
 cudaError_t launch_scan(const ScanArgs& a, int grid, cudaStream_t st, bool pdl) {
-  const int G = a.Hq / a.kv.Hkv;
-  switch (hist_heads(G)) {
-    case 1: return launch_scan_t<1>(a, grid, st, pdl);
-    case 2: return launch_scan_t<2>(a, grid, st, pdl);
-    case 4: return launch_scan_t<4>(a, grid, st, pdl);
-    default: return launch_scan_t<8>(a, grid, st, pdl);
-  }
+  return launch_scan_t(a, grid, st, pdl);
 }
 
 }  // namespace tsa

@@ -24,15 +24,6 @@ constexpr int kMaxUnits = 512;                  // B * Hkv limit of one call
 constexpr int kCtrStride = 32;
 constexpr long long kWaitLimitNs = 1000000000;  // bounded waits: 1 s
 
-// Per-head hint word kept in the workspace between calls: bits 0-15 the bin
-// from which the key scan emits (clamped to [0, kHistBins)), bit 16 set once
-// the head's threshold bin has moved by more than the default margin (the
-// head then gets a wider margin).  Any value is safe.
-__device__ __forceinline__ int hint_bin_of(int32_t w) {
-  const int b = w & 0xffff;
-  return b < kHistBins ? b : kHistBins - 1;
-}
-__device__ __forceinline__ bool hint_wide_of(int32_t w) { return (w >> 16) & 1; }
 
 // Status word bits written by kernels into the workspace (sticky: only the
 // host clears them, through tsa_workspace_status).
@@ -209,6 +200,10 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
 // Hint that the line holding p will be read soon (fetched into L2).
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+// Bulk L2 prefetch of `bytes` (a multiple of 16) from a 16-byte aligned address.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // ------------------------------------------------------------- clusters

@@ -13,11 +13,12 @@ namespace tsa {
 // head_active == nullptr || head_active[b*Hq + h] == active_value.
 //
 // Key scan: logits of every active head; window logits go to wz, pool
-// positions feed the 11-bit histogram and are emitted as (position, logit)
-// pairs when their bin is >= the head's hint bin.  Pairs go to the head's
-// dense list: every warp bump-allocates runs of 8 slots from dense_n and pads
-// the unused tail of its last run with sentinel pairs (position 0xffffffff).
-// The finish kernel turns the histograms into b* and checks the emission.
+// positions are emitted as (position, logit) pairs when their
+// order-preserving logit key is >= the head's emission key.
+// Pairs go to the head's dense list: every warp bump-allocates runs of 8
+// slots from dense_n and pads the unused tail of its last run with sentinel
+// pairs (position 0xffffffff).  The finish kernel counts the pairs' bins to
+// find b* and checks the emission.
 // With head_active set, the kernel waits for the previous grid (which wrote
 // it) before it starts; otherwise its producer streams keys at once.
 struct ScanArgs {
@@ -30,15 +31,21 @@ struct ScanArgs {
   int n_init, n_recent;      // static window (logits to wz, not emitted)
   const int32_t* head_active;  // heads with head_active[bh] == active_value take part
   int active_value;            // (nullptr: every head); written by the previous kernel
-  uint32_t* hist;            // [B][Hq][kHistBins] (zeroed)
   uint32_t* tile_ctr;        // (zeroed) dynamic tile claims
-  int32_t* hint_bin;         // [B][Hq] emission bins, persistent across calls (any value is safe)
+  const uint32_t* emit_key;   // [B][Hq] emission keys, persistent across calls (any value is safe)
   uint2* dense;              // [B][Hq][dense_stride] (position, logit bits)
   int32_t* dense_n;          // [B][Hq] x kCtrStride (zeroed) slots allocated (pairs + sentinels)
   int64_t dense_stride;      // >= l_cap + slack for the padding
   float* wz;                 // [B][Hq][wz_stride] window logits
   int wz_stride;
   int* status;
+  // L2 prefetch while the previous kernel runs: until its consumers start,
+  // a CTA whose ring is full claims items i = atomicAdd(pf_ctr) and prefetches
+  // tile i / grid of the static range of CTA i % grid into L2, for i below
+  // grid * pf_tiles (pf_ctr is reset by the previous finish kernel; a stale
+  // value only changes what is prefetched).
+  uint32_t* pf_ctr;
+  int pf_tiles;
   // Bounded waits give up after wait_ns (0: the default limit).  Fault
   // injection for tests of the error path: with stall_first_copy set, CTA 0
   // never issues the copy of its first tile, so that its consumers' wait
@@ -49,13 +56,14 @@ struct ScanArgs {
 };
 cudaError_t launch_scan(const ScanArgs& a, int grid, cudaStream_t st, bool pdl);
 
-// Finish: one cluster of NC CTAs per (sequence, query head) finds the threshold bin b* from the head's
-// histogram, checks the scan's emission against it and re-emits the head's
-// pairs itself when the hint failed (same tensor-core arithmetic as the
-// scan, so the pairs agree with the histogram), stores the next call's
-// hint, selects the exact top-K from the emitted pairs (pairs above b*
-// outright, the rest of the K by a cluster-wide radix over b*'s candidates)
-// and attends over the window and the selected rows with the gamma merge.
+// Finish: one cluster of NC CTAs per (sequence, query head) takes every
+// emitted pair as a candidate and selects the exact top-K among them with a
+// cluster-wide radix on the 64-bit rank key; when fewer pairs than K were
+// emitted it re-scores the head's keys to count every 11-bit bin, finds the
+// threshold bin b* and re-emits the pairs with bin >= b* itself (same
+// tensor-core arithmetic as the scan, so every logit is bit-identical); it
+// stores the next call's emission key and attends over the window and the
+// selected rows with the gamma merge.
 struct FinishArgs {
   const uint16_t* q;         // bf16 [B][Hq][128] (re-emission only)
   KvView kv;
@@ -64,9 +72,10 @@ struct FinishArgs {
   int B, Hq;
   float scale;
   int K, n_init, n_recent;
-  uint32_t* hist;            // [B][Hq][kHistBins] pool histograms from the scan (cleared)
-  int32_t* hint_bin;         // [B][Hq] the scan's emission bin; the next call's is stored
+  uint32_t* emit_key;        // [B][Hq] the scan's emission key; the next call's is stored
+  float* emit_margin;        // [B][Hq] per-head margin of the emission key (persistent)
   uint32_t* tile_ctr;        // the scan's tile claims (cleared)
+  uint32_t* pf_ctr;          // the next scan's prefetch claims (reset before the trigger)
   int* status;               // sticky error bits: a timeout makes the outputs NaN
   uint2* dense;              // [B][Hq][dense_stride] emitted pairs
   int32_t* dense_n;
