@@ -9,6 +9,12 @@ heads, K = 2048, window 128 + 512); --workload picks another one.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--impl ours|reference]
 
+The default run (llama128k at N = 1) also times, in the same process and
+reported under "secondary", the 1M-token decode step (the metric's second
+context) and the 64K ReTopK reuse stream (CUDA-graph timed over its 512
+steps); --no-secondary skips them.  cpu_baseline is the fp64 oracle on one
+host core, cpu_baseline_parallel the same code with one thread per query head.
+
 --impl reference times the fp64 CPU oracle (the test oracle, as it stands) on
 a bounded sample of the same workload, on the host cores.
 
@@ -81,13 +87,14 @@ class Clocks:
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
+        import tempfile
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        fd, self.path = tempfile.mkstemp(prefix=f"tsa_clocks_{index}_", suffix=".csv")
+        os.close(fd)
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             if os.path.exists(self.path):
                 os.remove(self.path)
             self.proc = subprocess.Popen(
@@ -116,7 +123,10 @@ class Clocks:
         if not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        with open(self.path) as f:
+            lines = f.readlines()
+        os.remove(self.path)
+        for line in lines:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -151,26 +161,28 @@ def algorithmic_bytes(wl) -> dict:
 SCAN_SOURCES = ("scan.cu", "tsa_internal.cuh", "tsa_kernels.h")
 
 
-def scan_traffic(wl, rows_per_launch: int):
-    """DRAM bytes (read + write) of one scan launch from the committed ncu
-    summary, or None when the scan sources changed since it was captured.
-    The summary's per-row traffic is scaled to this launch's key rows."""
+def scan_sources_sha256() -> str:
     import hashlib
-    path = os.path.join(ROOT, "profiles", "scan_llama128k.md")
-    if not os.path.exists(path):
-        return None, None
-    fields = {}
-    for line in open(path):
-        k, _, v = line.strip().partition(":")
-        if k in ("traffic_bytes_per_launch", "key_rows_per_launch", "source_sha256"):
-            fields[k] = v.strip()
     h = hashlib.sha256()
     for f in SCAN_SOURCES:
         with open(os.path.join(ROOT, "top_retrieval_sparse_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
-    if fields.get("source_sha256") != h.hexdigest():
+    return h.hexdigest()
+
+
+def scan_traffic(wl, rows_per_launch: int):
+    """DRAM bytes (read + write) of one scan launch from the tracked ncu
+    record profiles/scan_llama128k.json, or None when the scan sources changed
+    since it was captured.  Its per-row traffic is scaled to this launch's key
+    rows."""
+    path = os.path.join(ROOT, "profiles", "scan_llama128k.json")
+    if not os.path.exists(path):
+        return None, "no ncu record"
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("source_sha256") != scan_sources_sha256():
         return None, "scan sources changed since the ncu capture"
-    per_row = int(fields["traffic_bytes_per_launch"]) / int(fields["key_rows_per_launch"])
+    per_row = rec["traffic_bytes_per_launch"] / rec["key_rows_per_launch"]
     note = "ncu capture of llama128k" if wl.name == "llama128k" else \
         "llama128k ncu capture scaled by key rows"
     return int(round(per_row * rows_per_launch)), note
@@ -301,6 +313,7 @@ def run_ours(args, ws, rank, local):
     }
     if args.cpu_baseline and rank == 0:
         res["cpu_baseline"] = oracle_baseline(wl, budget_s=args.cpu_budget)
+        res["cpu_baseline_parallel"] = oracle_baseline_parallel(wl, budget_s=args.cpu_budget)
     if ws > 1:
         torch.distributed.destroy_process_group()
     return res if rank == 0 else None
@@ -608,6 +621,70 @@ def run_e2e(args, wl, kv, work, tsa, torch, dev, ws=1):
             "d2h_bytes_per_step": res_host.numel() * 4}
 
 
+def cpu_model() -> str:
+    """The host CPU's model string (x86 'model name', else Arm implementer/part)."""
+    try:
+        info = open("/proc/cpuinfo").read()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model name", "Model"):
+        for line in info.splitlines():
+            if line.startswith(key) and ":" in line:
+                return line.split(":", 1)[1].strip()
+    impl = part = None
+    for line in info.splitlines():
+        if line.startswith("CPU implementer") and ":" in line:
+            impl = line.split(":", 1)[1].strip()
+        if line.startswith("CPU part") and ":" in line:
+            part = line.split(":", 1)[1].strip()
+    if impl or part:
+        name = {("0x41", "0xd4f"): "Arm Neoverse V2"}.get((impl, part), "")
+        return f"{name} (implementer {impl}, part {part})".strip()
+    import platform
+    return platform.processor() or "unknown"
+
+
+def oracle_baseline_parallel(wl, budget_s=10.0):
+    """The same fp64 oracle with one thread per query head (the pages' own CPU
+    axis): whole query heads of decode step 0 run concurrently, a wave of as
+    many heads as there are threads at a time, until the budget; the wall time
+    is scaled to a layer-step.  The oracle's C code releases the interpreter
+    lock, so the threads run in parallel."""
+    import oracle as orc
+    from concurrent.futures import ThreadPoolExecutor
+    from workloads.gen import bits
+    G = wl.Hq // wl.Hkv
+    L = wl.lens(0)
+    threads = max(1, min(wl.Hq, os.cpu_count() or 1))
+    pairs = [(b, h) for b in range(wl.B) for h in range(wl.Hq)]
+    done, t_used = 0, 0.0
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        for i in range(0, len(pairs), threads):
+            wave = pairs[i:i + threads]
+            kv = {}
+            for b, h in wave:  # the wave's KV heads, widened outside the timed part
+                if (b, h // G) not in kv:
+                    kv[(b, h // G)] = (bits(wl.k[b, h // G, :L[b]]), bits(wl.v[b, h // G, :L[b]]))
+            qs = {(b, h): bits(wl.q(0)[b, h]) for b, h in wave}
+
+            def job(bh):
+                b, h = bh
+                kb, vb = kv[(b, h // G)]
+                orc.decode_head(qs[bh], kb, vb, wl.K, wl.n_init, wl.n_recent, wl.scale)
+
+            t0 = time.perf_counter()
+            list(ex.map(job, wave))
+            t_used += time.perf_counter() - t0
+            done += len(wave)
+            if t_used >= budget_s:
+                break
+    return {"value": round(1e6 * t_used / done * wl.B * wl.Hq, 1), "unit": UNIT, "cores": threads,
+            "kind": "oracle", "cpu": cpu_model(),
+            "sample": f"{done} of {wl.B * wl.Hq} (sequence, query head) pairs of decode step 0 in "
+                      f"waves of {threads} threads (one per query head), {t_used:.1f} s, scaled "
+                      f"to a whole layer-step"}
+
+
 def oracle_baseline(wl, budget_s=12.0, steps=1):
     """fp64 single-threaded oracle on a bounded sample: whole query heads of
     decode step 0, as many as fit the time budget, scaled to one layer-step."""
@@ -634,7 +711,7 @@ def oracle_baseline(wl, budget_s=12.0, steps=1):
             break
     per_head = t_used / done
     return {"value": round(1e6 * per_head * wl.B * wl.Hq, 1), "unit": UNIT, "cores": 1,
-            "kind": "oracle",
+            "kind": "oracle", "cpu": cpu_model(),
             "sample": f"{done} of {wl.B * wl.Hq} (sequence, query head) pairs of decode step 0, "
                       f"{t_used:.1f} s, scaled to a whole layer-step"}
 
@@ -794,6 +871,26 @@ def run_reference(args, ws, rank):
     }
 
 
+def run_secondary(args, ws, rank, local):
+    """The other workloads the metric names, timed in the same run (N = 1):
+    the 1M-token decode step (the metric's second context) and the ReTopK
+    reuse stream at 64K (CUDA-graph timed over its 512 steps)."""
+    import torch
+    out = {}
+    for name, over in (("llama1m", dict(steps=20, warmup=max(16, args.warmup))),
+                       ("retopk64k", dict(steps=512, warmup=args.warmup))):
+        torch.cuda.empty_cache()
+        sub = argparse.Namespace(**{**vars(args), "workload": name, "cpu_baseline": False,
+                                    "trace": False, "device_only": False, **over})
+        r = run_retopk(sub, ws, rank, local) if name.startswith("retopk") else \
+            run_ours(sub, ws, rank, local)
+        keep = ("value", "unit", "ms_per_step", "steps", "warmup", "config", "stages_ms",
+                "path_algorithmic_gbs", "roofline", "e2e", "gpu_launches", "clocks",
+                "host_launched_us_per_step", "timing", "paths")
+        out[name] = {k: r[k] for k in keep if k in r}
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -809,6 +906,8 @@ def main():
                     help="also record a per-CTA kernel timeline of 3 extra steps")
     ap.add_argument("--device-only", action="store_true",
                     help="profiling mode: time only the device path (no e2e, no baseline)")
+    ap.add_argument("--no-secondary", dest="secondary", action="store_false",
+                    help="skip the 1M decode and 64K ReTopK legs of the default run")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -819,6 +918,9 @@ def main():
         res = run_retopk(args, ws, rank, local)
     else:
         res = run_ours(args, ws, rank, local)
+        if (args.secondary and ws == 1 and args.workload == "llama128k" and not args.device_only
+                and res is not None):
+            res["secondary"] = run_secondary(args, ws, rank, local)
     if rank == 0 and res is not None:
         print(json.dumps(res))
 

@@ -86,7 +86,6 @@ bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 // Device pointers of the exact top-K machinery (key scan + finish).
 struct SelWs {
   int* status;
-  uint32_t* pf_ctr;      // the key scan's L2 prefetch claims (in the status block)
   uint32_t* tile_ctr;    // counters: zero before a call, cleared by its finish kernel
   int32_t* dense_n;
   uint32_t* emit_key;    // persist between calls (any content is safe)
@@ -155,7 +154,6 @@ ScanArgs scan_args(const uint16_t* q, const KvView& view, const int32_t* lens, i
   s.wz = w.wz;
   s.wz_stride = w.wz_stride;
   s.status = w.status;
-  s.pf_ctr = w.pf_ctr;
   s.trace = g_trace;
   s.wait_ns = g_stall_ns;
   s.stall_first_copy = g_stall_ns > 0;
@@ -176,7 +174,6 @@ FinishArgs finish_args(const uint16_t* q, const KvView& view, int Hq, float scal
   f.emit_margin = w.emit_margin;
   f.tile_ctr = w.tile_ctr;
   f.status = w.status;
-  f.pf_ctr = w.pf_ctr;
   f.dense = w.dense;
   f.dense_n = w.dense_n;
   f.dense_stride = w.dense_stride;
@@ -185,16 +182,6 @@ FinishArgs finish_args(const uint16_t* q, const KvView& view, int Hq, float scal
   f.wz_stride = w.wz_stride;
   f.trace = g_trace;
   return f;
-}
-
-// The key scan's L2 prefetch (while the previous kernel runs): its claim
-// counter sits in the status block, and it prefetches up to ~80 MiB of key
-// tiles (of the 126 MiB L2), the first tiles of every CTA's range.
-constexpr size_t kPfCtrOffset = 64;
-int prefetch_tiles(int grid) {
-  const int64_t budget = (int64_t)80 << 20;
-  const int64_t per = budget / ((int64_t)(grid > 0 ? grid : 1) * 256 * kRowBytes);
-  return (int)(per > 16 ? 16 : per);
 }
 
 // Persistent scan grid: one CTA per SM, at most one per tile.
@@ -353,7 +340,6 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
   const KvView view = make_view(kv, Hkv);
   SelWs w{};
   w.status = reinterpret_cast<int*>(ws + Lw.status);
-  w.pf_ctr = reinterpret_cast<uint32_t*>(ws + Lw.status + kPfCtrOffset);
   w.tile_ctr = reinterpret_cast<uint32_t*>(ws + Lw.tile_ctr);
   w.emit_key = reinterpret_cast<uint32_t*>(ws + Lw.emit_key);
   w.emit_margin = reinterpret_cast<float*>(ws + Lw.emit_margin);
@@ -366,11 +352,9 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
 
   // 1. key scan (logits, emitted pairs, window logits)
   if (kv->l_cap > 0) {
-    ScanArgs s = scan_args(static_cast<const uint16_t*>(q), view, lens, 0, B, Hq, n_init,
-                           n_recent, scale, nullptr, 0, w);
-    const int grid = scan_grid(B, view, kv->l_cap);
-    s.pf_tiles = prefetch_tiles(grid);
-    if ((e = counted(launch_scan(s, grid, st, true))) != cudaSuccess)
+    const ScanArgs s = scan_args(static_cast<const uint16_t*>(q), view, lens, 0, B, Hq, n_init,
+                                 n_recent, scale, nullptr, 0, w);
+    if ((e = counted(launch_scan(s, scan_grid(B, view, kv->l_cap), st, true))) != cudaSuccess)
       return cuda_fail(e, "scan launch");
   }
   if ((e = stage_mark(1, st)) != cudaSuccess) return cuda_fail(e, "event record");
@@ -612,7 +596,6 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
   float* qbar_new = reinterpret_cast<float*>(ws + Lw.qbar_new);
   SelWs w{};
   w.status = reinterpret_cast<int*>(ws + Lw.status);
-  w.pf_ctr = reinterpret_cast<uint32_t*>(ws + Lw.status + kPfCtrOffset);
   w.tile_ctr = reinterpret_cast<uint32_t*>(ws + Lw.tile_ctr);
   w.emit_key = reinterpret_cast<uint32_t*>(ws + Lw.emit_key);
   w.emit_margin = reinterpret_cast<float*>(ws + Lw.emit_margin);

@@ -280,6 +280,67 @@ __device__ void reuse_logits(const FinishArgs& a, int b, int bh, int g, int64_t 
   }
 }
 
+// The rare path, out of line so that the kernel's common path keeps a small
+// instruction footprint: the emission key missed part of the top-K.  The
+// cluster re-scores the head's keys to count every 11-bit bin, takes the
+// threshold bin b* (the largest bin whose suffix count reaches `need`; with
+// `all`, bin 0: the whole pool is selected) and re-emits the head's pool
+// pairs with bin >= b*.  Every CTA of the cluster calls it; returns b*
+// (-1 with `all`).
+template <int NC, int W>
+__device__ __noinline__ int reemit_head(const FinishArgs& a, FinShared<NC, W>& sh, int b, int h,
+                                        int g, int G, int64_t L, int rank, int need, bool all) {
+  constexpr int kFinThreads = 32 * W;
+  constexpr int kBpt = kHistBins / kFinThreads;
+  const int tid = threadIdx.x;
+  const int bh = b * a.Hq + h;
+  int bstar = -1;
+  cluster_sync_all();  // every CTA has read the old list size and the remote counts
+  if (!all) {
+    for (int q = tid; q < kHistBins; q += kFinThreads) sh.hist[q] = 0;
+    __syncthreads();
+    rescore_count<W>(a, b, h, g, G, L, rank, NC, sh);
+    __syncthreads();
+    cluster_sync_all();  // every CTA's counts are complete
+    for (int q = tid; q < kHistBins; q += kFinThreads) {
+      uint32_t c = sh.hist[q];
+#pragma unroll
+      for (int r = 1; r < NC; ++r) c += ld_dsmem_u32(&sh.hist[q], (uint32_t)((rank + r) % NC));
+      sh.chist[q] = c;
+    }
+    __syncthreads();
+    // thread t holds bins 2047 - kBpt*t - r, r < kBpt
+    uint32_t c[kBpt], mine = 0;
+#pragma unroll
+    for (int r = 0; r < kBpt; ++r) {
+      c[r] = sh.chist[kHistBins - 1 - kBpt * tid - r];
+      mine += c[r];
+    }
+    if (tid == 0) sh.scal[0] = 0;
+    int tot;
+    uint32_t acc = (uint32_t)fin_scan<W>((int)mine, sh, &tot);
+#pragma unroll
+    for (int r = 0; r < kBpt; ++r) {
+      if (acc < (uint32_t)need && acc + c[r] >= (uint32_t)need)
+        sh.scal[0] = kHistBins - 1 - kBpt * tid - r;
+      acc += c[r];
+    }
+    __syncthreads();
+    bstar = sh.scal[0];  // exists: the pool holds more than need positions
+    __syncthreads();
+    cluster_sync_all();  // the remote counts have been read
+  }
+  if (rank == 0 && tid == 0) {
+    a.dense_n[(int64_t)bh * kCtrStride] = 0;
+    __threadfence();
+  }
+  cluster_sync_all();
+  reemit<W>(a, b, h, g, G, L, all ? 0 : bstar, rank, NC);
+  __threadfence();
+  cluster_sync_all();
+  return bstar;
+}
+
 // RT: a ReTopK step (reuse heads, the FIFO push); the decode instantiation
 // carries none of that code.
 template <int NC, int W, bool RT>
@@ -332,16 +393,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
       prefetch_l2(vr + kD / 2);
     }
   }
-  pdl_wait();     // pairs, bins and window logits come from the scan
-  // The next key scan's prefetch claims start from zero; the reset is made
-  // visible before this CTA lets the next kernel be scheduled.
-  if (bh == 0 && rank == 0) {
-    if (tid == 0 && a.pf_ctr) {
-      *a.pf_ctr = 0u;
-      __threadfence();
-    }
-    __syncthreads();
-  }
+  pdl_wait();     // pairs and window logits come from the scan
   pdl_trigger();  // the next kernel may be scheduled (it writes nothing
                   // this kernel reads until this kernel has completed)
   trace.mark(1);
@@ -449,8 +501,9 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   const uint32_t tgt[2] = {(uint32_t)need, (uint32_t)need};
   if (need > 0 && !reuse) {  // (a reuse head has no bins: all its candidates compete)
     // the bins of this CTA's slice of the emitted pairs (the first batch is
-    // in registers), one shared atomic per distinct bin per warp instruction
-    for (int q = tid; q < kHistBins; q += kFinThreads) sh.hist[q] = 0;
+    // in registers), one shared atomic per distinct bin per warp instruction;
+    // every emitted pair's bin is >= the emission key's
+    for (int q = used + tid; q < kHistBins; q += kFinThreads) sh.hist[q] = 0;
     __syncthreads();
     for (int64_t jb = s0; jb < s1; jb += kFinThreads * kFinU) {
 #pragma unroll
@@ -482,27 +535,8 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   phases.info = ((uint32_t)redo << 31) | ((uint32_t)(bstar & 0x7fff) << 16) | (uint32_t)used;
   // ---- re-emission when the emission key missed the top-K (rare) ----
   if (redo) {  // uniform over the cluster
-    cluster_sync_all();  // every CTA has read the old list size and the remote counts
-    if (need < P) {  // b* over every pool key of the head
-      for (int q = tid; q < kHistBins; q += kFinThreads) sh.hist[q] = 0;
-      __syncthreads();
-      rescore_count<W>(a, b, h, g, G, L, rank, NC, sh);
-      __syncthreads();
-      cluster_counts(0);
-      int fb[2];
-      suffix_bins(sh.chist, 0, tgt, fb);
-      bstar = fb[0];  // exists: the pool holds P > need positions
-      ebin = bstar;
-      cluster_sync_all();  // the remote counts have been read
-    }
-    if (rank == 0 && tid == 0) {
-      a.dense_n[(int64_t)bh * kCtrStride] = 0;
-      __threadfence();
-    }
-    cluster_sync_all();
-    reemit<W>(a, b, h, g, G, L, ebin, rank, NC);
-    __threadfence();
-    cluster_sync_all();
+    const int bs = reemit_head<NC, W>(a, sh, b, h, g, G, L, rank, need, need >= P);
+    if (need < P) bstar = ebin = bs;
   }
 
   // ---- 1. this CTA's slice of the pair list ----

@@ -39,13 +39,6 @@ struct ScanArgs {
   float* wz;                 // [B][Hq][wz_stride] window logits
   int wz_stride;
   int* status;
-  // L2 prefetch while the previous kernel runs: until its consumers start,
-  // a CTA whose ring is full claims items i = atomicAdd(pf_ctr) and prefetches
-  // tile i / grid of the static range of CTA i % grid into L2, for i below
-  // grid * pf_tiles (pf_ctr is reset by the previous finish kernel; a stale
-  // value only changes what is prefetched).
-  uint32_t* pf_ctr;
-  int pf_tiles;
   // Bounded waits give up after wait_ns (0: the default limit).  Fault
   // injection for tests of the error path: with stall_first_copy set, CTA 0
   // never issues the copy of its first tile, so that its consumers' wait
@@ -75,7 +68,6 @@ struct FinishArgs {
   uint32_t* emit_key;        // [B][Hq] the scan's emission key; the next call's is stored
   float* emit_margin;        // [B][Hq] per-head margin of the emission key (persistent)
   uint32_t* tile_ctr;        // the scan's tile claims (cleared)
-  uint32_t* pf_ctr;          // the next scan's prefetch claims (reset before the trigger)
   int* status;               // sticky error bits: a timeout makes the outputs NaN
   uint2* dense;              // [B][Hq][dense_stride] emitted pairs
   int32_t* dense_n;
