@@ -898,7 +898,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="llama128k",
                     choices=["tiny", "llama128k", "llama1m", "yi_paged", "retopk64k",
-                             "retopk1m"])
+                             "retopk1m", "retopk4m"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=12.0)

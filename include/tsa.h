@@ -278,10 +278,14 @@ typedef struct tsa_retopk tsa_retopk;
 TSA_API size_t retopk_state_size(int Hq, int d, int K, int C);
 
 /* Create a handle over `state_mem`.  Hyper-parameters: 1 <= R <= C <= 64,
- * K >= 1, W >= 0, T_r >= 1, tau any float (tau > 1: always exact;
- * tau <= -1 with a large T_r: reuse after step 0).  max_len bounds every
- * later L_t (it sizes the candidate bitmap, which one CTA keeps in shared
- * memory: max_len <= 1572864, 192 KiB of bits).  Nothing is launched. */
+ * K >= 1, W >= 0, T_r >= 1, R*K + W <= 8192, tau any float (tau > 1: always
+ * exact; tau <= -1 with a large T_r: reuse after step 0).  max_len bounds
+ * every later L_t and sizes the workspace: the candidate union is a bitmap
+ * over the positions with a second level of one bit per 32-bit word; one CTA
+ * keeps both in shared memory up to 1.5 M positions (192 KiB), and for
+ * longer caches the bitmap lives in the workspace (max_len / 8 bytes per
+ * query head) with only the second level in shared memory: max_len <=
+ * 50331648.  Nothing is launched. */
 TSA_API int retopk_create(tsa_retopk** st, int Hq, int Hkv, int d, int K, int C,
                   int R, int W, float tau, int T_r, int64_t max_len,
                   void* state_mem, size_t state_bytes);

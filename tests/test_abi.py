@@ -132,15 +132,24 @@ def test_retopk_host_state_machine(lib):
                              FAKE, n) == -1  # T_r < 1
     assert lib.retopk_create(C.byref(bad), 28, 4, 128, 512, 32, 4, 32, 0.85, 128, 70000,
                              FAKE, n - 1) == -1  # state too small
-    # the selector's candidate bitmap (plus its second level) must fit one
-    # CTA's shared memory: 192 KiB of bits, 1572864 positions
-    cap = 192 * 1024 * 8
+    # the selector's candidate bitmap: in one CTA's shared memory up to 1.5 M
+    # positions, beyond that in the workspace (1 bit per position and query
+    # head) with its second level (1 bit per word) in 192 KiB of shared
+    # memory: 50331648 positions at most
+    small = C.c_void_p()
+    assert lib.retopk_create(C.byref(small), 28, 4, 128, 512, 32, 4, 32, 0.85, 128,
+                             1_500_000, FAKE, n) == 0
+    cap = 192 * 1024 * 8 * 32
     ok = C.c_void_p()
     assert lib.retopk_create(C.byref(ok), 28, 4, 128, 512, 32, 4, 32, 0.85, 128, cap,
                              FAKE, n) == 0
-    assert lib.retopk_destroy(ok) == 0
+    # the long cache's bitmap is workspace: max_len / 8 bytes per query head more
+    grow = lib.retopk_workspace_size(ok) - lib.retopk_workspace_size(small)
+    dense = 28 * (cap - 1_500_000 - 64) * 16   # the pair list and spill area grow too
+    assert grow >= dense + 28 * cap // 8
+    assert lib.retopk_destroy(ok) == 0 and lib.retopk_destroy(small) == 0
     assert lib.retopk_create(C.byref(bad), 28, 4, 128, 512, 32, 4, 32, 0.85, 128, cap + 1,
-                             FAKE, n) == -1  # max_len beyond the bitmap
+                             FAKE, n) == -1  # max_len beyond the second level
 
 
 def test_status_and_injection_validation(lib):

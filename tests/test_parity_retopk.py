@@ -236,3 +236,18 @@ def test_retopk_1m_context_k1024_first_steps():
     assert st["exact"] >= wl.Hq and st["reuse"] > 0
     print("retopk1m:", {k: v for k, v in st.items() if k != "mcand"},
           "mean M_t", float(np.mean(st["mcand"])), "max M_t", max(st["mcand"]))
+
+
+@pytest.mark.slow
+def test_retopk_4m_context_first_steps():
+    """Beyond the 1.5 M positions one CTA's shared memory holds as a bitmap:
+    4M keys, K = 1024, where the selector keeps the candidate bitmap in the
+    workspace (cleared word by word as the compaction reads it) and only its
+    second level in shared memory.  The first steps in lockstep: step 0
+    refreshes (every head exact over 4M keys), the next ones mostly reuse, and
+    every reuse head's A_t must equal the oracle's union bit for bit."""
+    wl = make_retopk("retopk4m", device="cuda", steps=6)
+    st = run_lockstep(wl, 6, verify_prefill=False)
+    assert st["exact"] >= wl.Hq and st["reuse"] > 0
+    print("retopk4m:", {k: v for k, v in st.items() if k != "mcand"},
+          "mean M_t", float(np.mean(st["mcand"])), "max M_t", max(st["mcand"]))

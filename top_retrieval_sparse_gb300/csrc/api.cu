@@ -441,11 +441,22 @@ namespace {
 constexpr uint32_t kMagic = 0x52544b31u;  // "RTK1"
 
 struct RetopkLayout {
-  size_t zero_begin, status, tile_ctr, dense_n, zero_end;
+  size_t zero_begin, status, tile_ctr, dense_n, gbitmap, zero_end;
   size_t emit_key, emit_margin, wz, dense, spill, qbar_new, path, cand, mcand, total;
-  int64_t dense_stride;
+  int64_t dense_stride, gbitmap_stride;
   int cand_cap;
 };
+
+// The selector keeps its candidate bitmap (one bit per cache position, plus a
+// second level of one bit per 32-bit word) in one CTA's shared memory while
+// that fits in 192 KiB; longer caches keep the bitmap in the workspace and
+// only the second level in shared memory (192 KiB of it: 50 M positions).
+constexpr int64_t kSmemBitmapBytes = (int64_t)192 * 1024;
+bool bitmap_in_smem(int64_t len) {
+  const int64_t words = (len + 31) / 32;
+  return (words + (words + 31) / 32) * 4 <= kSmemBitmapBytes;
+}
+constexpr int64_t kMaxRetopkLen = kSmemBitmapBytes * 8 * 32;  // second level in 192 KiB
 
 RetopkLayout retopk_layout(const tsa_retopk* s) {
   RetopkLayout L{};
@@ -457,6 +468,9 @@ RetopkLayout retopk_layout(const tsa_retopk* s) {
   L.status = o; o = up(o + 4);
   L.tile_ctr = o; o = up(o + 4);
   L.dense_n = o; o = up(o + H * kCtrStride * 4);
+  // the bitmap of long caches (zero once; every step leaves it zero)
+  L.gbitmap_stride = bitmap_in_smem(s->max_len) ? 0 : (int64_t)up((size_t)(s->max_len + 31) / 32, 64);
+  L.gbitmap = o; o = up(o + H * (size_t)L.gbitmap_stride * 4);
   L.zero_end = o;
   L.emit_key = o; o = up(o + H * 4);
   L.emit_margin = o; o = up(o + H * 4);
@@ -480,7 +494,6 @@ int check_state(const tsa_retopk* s) {
   return TSA_OK;
 }
 
-constexpr int64_t kMaxBitmapLen = (int64_t)192 * 1024 * 8;  // positions in 192 KiB of bits
 }  // namespace
 
 extern "C" {
@@ -502,8 +515,8 @@ int retopk_create(tsa_retopk** st, int Hq, int Hkv, int d, int K, int C, int R, 
   if (W < 0) return fail(TSA_ERR_INVALID_ARG, "W must be >= 0");
   if (T_r < 1) return fail(TSA_ERR_INVALID_ARG, "T_r must be >= 1");
   if (std::isnan(tau)) return fail(TSA_ERR_INVALID_ARG, "tau is NaN");
-  if (max_len < 1 || max_len > kMaxBitmapLen)
-    return fail(TSA_ERR_INVALID_ARG, "max_len must be in [1, %lld]", (long long)kMaxBitmapLen);
+  if (max_len < 1 || max_len > kMaxRetopkLen)
+    return fail(TSA_ERR_INVALID_ARG, "max_len must be in [1, %lld]", (long long)kMaxRetopkLen);
   if ((int64_t)R * K + W > 8192)
     return fail(TSA_ERR_INVALID_ARG, "R*K + W = %lld > 8192", (long long)R * K + W);
   if (!state_mem || !aligned(state_mem, kAlign))
@@ -632,8 +645,13 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
     a.mcand_out = mcand_out;
     a.cand_out = cand_out;
     a.trace = g_trace;
-    // the bitmap and its second level (one bit per bitmap word)
-    const size_t smem = up((size_t)(a.bitmap_words + (a.bitmap_words + 31) / 32) * 4, 16);
+    // the bitmap (or, for a long cache, only its second level: the bitmap is
+    // the workspace's) in shared memory
+    const size_t l2w = (size_t)(a.bitmap_words + 31) / 32;
+    const bool in_smem = bitmap_in_smem(len);
+    a.gbitmap = in_smem ? nullptr : reinterpret_cast<uint32_t*>(ws + Lw.gbitmap);
+    a.gbitmap_stride = Lw.gbitmap_stride;
+    const size_t smem = up((in_smem ? (size_t)a.bitmap_words + l2w : l2w) * 4, 16);
     if ((e = counted(launch_retopk_selector(a, smem, s))) != cudaSuccess)
       return cuda_fail(e, "retopk selector launch");
   }

@@ -6,7 +6,9 @@
 //           the C cached queries; exact path iff max rho < tau or a refresh
 //           step; otherwise the R most similar entries (ties: older entry
 //           first), the union of their supports and the last W positions as a
-//           shared-memory bitmap, compacted in ascending order -> A_t, M_t.
+//           bitmap over the cache's positions (in shared memory up to 1.5 M
+//           positions, else in the workspace) with a second level in shared
+//           memory, compacted in ascending order -> A_t, M_t.
 // The indexed QK on A_t, the candidate top-K and the sparse softmax.V are
 // the finish kernel's (finish.cu), for reuse heads as for exact ones.
 // init      fills the FIFO from the last C prefill queries and their supports.
@@ -23,7 +25,7 @@ constexpr int kSelectorThreads = 1024;
 
 __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(RetopkSelArgs a) {
   TraceScope trace(a.trace, kTrSelector);  // start, waited, union built, exit
-  extern __shared__ __align__(16) uint32_t bitmap[];
+  extern __shared__ __align__(16) uint32_t sbits[];
   __shared__ __align__(16) float qs[kD];
   __shared__ float rho[kMaxC];
   __shared__ float red[kSelectorThreads / 32];
@@ -50,12 +52,16 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
   }
   __syncthreads();
   const float nrm = sqrtf(red[0]);
-  // the bitmap of step 4 is this CTA's shared memory: clear it now.  A
-  // second level (one bit per bitmap word) marks the words that hold a bit.
+  // the bitmap of step 4: this CTA's shared memory (cleared now), or for a
+  // long cache the head's zeroed words in the workspace.  A second level
+  // (one bit per bitmap word, always in shared memory) marks the words that
+  // hold a bit.
   const int nwords = (int)((a.L + 31) >> 5);
   const int nl2 = (nwords + 31) >> 5;
-  uint32_t* l2 = bitmap + nwords;
-  for (int w = tid; w < nwords + nl2; w += kSelectorThreads) bitmap[w] = 0u;
+  const bool gbm = a.gbitmap != nullptr;
+  uint32_t* bitmap = gbm ? a.gbitmap + (int64_t)h * a.gbitmap_stride : sbits;
+  uint32_t* l2 = gbm ? sbits : sbits + nwords;
+  for (int w = tid; w < (gbm ? nl2 : nwords + nl2); w += kSelectorThreads) sbits[w] = 0u;
   // the cache and this step's buffers belong to the previous step's kernels
   // until they have completed; the key scan may be scheduled from here on
   pdl_wait();
@@ -204,7 +210,9 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
   for (int q = q0; q < q1; ++q) {
     for (uint32_t m = l2[q]; m; m &= m - 1) {
       const int w = (q << 5) + __ffs(m) - 1;
-      for (uint32_t bits = bitmap[w]; bits; bits &= bits - 1) {
+      const uint32_t word = bitmap[w];
+      if (gbm) bitmap[w] = 0u;  // the workspace bitmap is all zero again after the step
+      for (uint32_t bits = word; bits; bits &= bits - 1) {
         if (pos < (uint32_t)a.cand_cap) crow[pos] = ((uint32_t)w << 5) + __ffs(bits) - 1;
         ++pos;
       }

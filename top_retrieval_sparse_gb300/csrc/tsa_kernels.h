@@ -113,6 +113,12 @@ struct RetopkSelArgs {
   float tau;
   int64_t L;
   int bitmap_words;
+  // Long caches: the candidate bitmap lives in global memory, gbitmap_stride
+  // words per head (all zero between steps: the compaction clears every word
+  // it reads), and only its second level in shared memory; nullptr: both in
+  // shared memory.
+  uint32_t* gbitmap;
+  int64_t gbitmap_stride;
   float* qbar_new;           // [Hq][128]
   int32_t* path;             // [Hq] 1 exact, 0 reuse
   uint32_t* cand;            // [Hq][cand_cap] ascending

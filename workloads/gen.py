@@ -51,6 +51,9 @@ CONFIGS = {
     # context setting for the reuse path)
     "retopk1m": dict(B=1, Hq=28, Hkv=4, d=128, L0=1 << 20, steps=512, K=1024,
                      C=32, R=4, W=32, tau=0.85, T_r=128, family="walk", seed=0),
+    # ReTopK at 4M context (the 1M-5M cross-model setting, K = 1024)
+    "retopk4m": dict(B=1, Hq=28, Hkv=4, d=128, L0=1 << 22, steps=512, K=1024,
+                     C=32, R=4, W=32, tau=0.85, T_r=128, family="walk", seed=0),
     # 4: batched paged decode, Yi-9B geometry
     "yi_paged": dict(B=16, Hq=32, Hkv=4, d=128, Lmin=8192, Lmax=131072,
                      steps=32, K=1024, n_init=64, n_recent=256, family="iid",
