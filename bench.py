@@ -337,15 +337,9 @@ def run_retopk(args, ws, rank, local):
     kv = tsa.kv_contiguous(wl.k, wl.v)
     g = tsa.ReTopK(wl.Hq, wl.Hkv, wl.d, wl.K, wl.C, wl.R, wl.W, wl.tau, wl.T_r, wl.lcap,
                    device=dev)
-    # the FIFO starts from the last C prefill queries and their exact causal top-K
-    sup = torch.full((wl.C, wl.Hq, wl.K), -1, dtype=torch.int32, device=dev)
-    for c in range(wl.C):
-        idx = torch.empty((1, wl.Hq, wl.K), dtype=torch.int32, device=dev)
-        lens = torch.tensor([wl.L0 - wl.C + c + 1], dtype=torch.int32, device=dev)
-        tsa.sparse_attn_decode(wl.q_prefill[c][None].contiguous(), kv, lens, wl.K, 0, 0,
-                               wl.scale, topk_idx=idx)
-        sup[c] = idx[0]
-    cnt = (sup >= 0).sum(-1).to(torch.int32)
+    # the FIFO starts from the last C prefill queries and their exact causal
+    # top-K (one library call for all of them)
+    sup, cnt = tsa.prefill_supports(wl.q_prefill.contiguous(), kv, wl.L0, wl.K, wl.scale)
     g.init(wl.q_prefill.contiguous(), sup, cnt)
     out = torch.empty((wl.Hq, wl.d), dtype=torch.float32, device=dev)
     path = torch.empty((wl.steps, wl.Hq), dtype=torch.int32, device=dev)

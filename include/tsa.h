@@ -325,6 +325,35 @@ TSA_API int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t
                 float* lse_out, void* workspace, size_t ws_bytes,
                 void* stream);
 
+/* retopk_prefill_supports -- the FIFO's initial supports ([RTK] method
+ * section 1: the cache starts from the last C prefill queries; the same exact
+ * prefill-query top-K is [RA]'s attention-aware index, phase 1).
+ *
+ * For the last C prefill queries of one sequence -- query c (0 = oldest) at
+ * position p_c = L0 - C + c -- and every query head h: the exact top-K of
+ * z_i = scale * q_{c,h} . k_i over the causal prefix i in [0, p_c] (no
+ * window), ties to the smaller position.  One call runs one key scan and one
+ * selection for all C * Hq (query, head) pairs: the queries are a batch of C
+ * sequences that all read this sequence's cache (each still reads its own
+ * prefix of keys).
+ * q_prefill:  bf16 [C][Hq][128] (device), the layout retopk_init takes
+ * kv:         the sequence's cache (B = 1), L0 <= kv->l_cap, C <= L0
+ * supports:   int32 [C][Hq][K] (device): the positions, unspecified order,
+ *             padded with -1 past min(K, p_c + 1)
+ * counts:     int32 [C][Hq] (device) or NULL: min(K, p_c + 1)
+ * workspace:  retopk_prefill_workspace_size() bytes, 256-byte aligned,
+ *             zero-filled before its first use; like the decode workspace
+ *             it keeps per-head emission state between calls (a first call
+ *             emits every key and costs more).
+ * Limits as sparse_attn_decode with B = C (C * Hkv <= 512, C * Hq <= 65535).
+ * Device-detected errors: tsa_workspace_status. */
+TSA_API size_t retopk_prefill_workspace_size(int C, int Hq, int Hkv, int d, int64_t l_cap,
+                                             int K);
+TSA_API int retopk_prefill_supports(const void* q_prefill, const tsa_kv* kv, int64_t L0, int C,
+                                    int Hq, int Hkv, int d, int K, float scale,
+                                    int32_t* supports, int32_t* counts, void* workspace,
+                                    size_t ws_bytes, void* stream);
+
 /* Host-side counters of the handle (for checkpointing). */
 TSA_API int retopk_get_counters(const tsa_retopk* st, int64_t* t, int32_t* fifo_head);
 TSA_API int retopk_set_counters(tsa_retopk* st, int64_t t, int32_t fifo_head);

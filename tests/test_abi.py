@@ -217,3 +217,30 @@ def test_noalloc_size_limit_boundaries(lib):
     assert largest_fit(1, 32, 8) == -1 and largest_fit(2, 16, 4) == -1
     assert _noalloc(lib, tsa, Hq=4, Hkv=1, kv=_kv(tsa, l4 + 64)) == -2
     assert "scratch" in lib.tsa_last_error().decode()
+
+
+def test_prefill_supports_validation(lib):
+    """retopk_prefill_supports checks its sizes, pointers and workspace on the
+    host (no CUDA call: the codes are the validation ones, not -3)."""
+    import top_retrieval_sparse_gb300 as tsa
+    kv = _kv(tsa, 1024)
+    n = lib.retopk_prefill_workspace_size(8, 28, 4, 128, 1024, 64)
+    assert n > lib.tsa_decode_workspace_size(8, 28, 4, 128, 1024, 64, 0, 0)
+    assert lib.retopk_prefill_workspace_size(0, 28, 4, 128, 1024, 64) == 0
+
+    def call(**kw):
+        a = dict(q=FAKE, L0=1000, C=8, Hq=28, Hkv=4, d=128, K=64, sup=FAKE, cnt=None, ws=FAKE,
+                 nb=n, kv=kv)
+        a.update(kw)
+        return lib.retopk_prefill_supports(a["q"], C.byref(a["kv"]), a["L0"], a["C"], a["Hq"],
+                                           a["Hkv"], a["d"], a["K"], 0.1, a["sup"], a["cnt"],
+                                           a["ws"], a["nb"], None)
+    assert call(C=0) == -1
+    assert call(K=0) == -1
+    assert call(L0=5) == -1         # fewer positions than queries
+    assert call(L0=2000) == -1      # beyond l_cap
+    assert call(sup=None) == -1
+    assert call(d=64) == -1
+    assert call(C=200) == -1        # C * Hkv > 512
+    assert call(nb=n - 1) == -2
+    assert call(ws=None) == -2

@@ -25,7 +25,12 @@ pytestmark = pytest.mark.gpu
 
 def gpu_prefill_supports(tsa, wl, kv, dev):
     """Exact top-K of each prefill query over its causal prefix (no window),
-    computed with sparse_attn_decode."""
+    computed with the library's prefill entry point (one call)."""
+    return tsa.prefill_supports(wl.q_prefill.to(dev).contiguous(), kv, wl.L0, wl.K, wl.scale)
+
+
+def decode_prefill_supports(tsa, wl, kv, dev):
+    """The same supports from one sparse_attn_decode call per prefill query."""
     Cn, Hq, K = wl.C, wl.Hq, wl.K
     sup = torch.full((Cn, Hq, K), -1, dtype=torch.int32, device=dev)
     for c in range(Cn):
@@ -251,3 +256,61 @@ def test_retopk_4m_context_first_steps():
     assert st["exact"] >= wl.Hq and st["reuse"] > 0
     print("retopk4m:", {k: v for k, v in st.items() if k != "mcand"},
           "mean M_t", float(np.mean(st["mcand"])), "max M_t", max(st["mcand"]))
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_prefill_supports_match_oracle(paged):
+    """retopk_prefill_supports: every (prefill query, head)'s support is the
+    oracle's exact top-K over its causal prefix (near-tie rule), counts are
+    min(K, p + 1), padding is -1; a paged copy of the cache gives the same."""
+    import top_retrieval_sparse_gb300 as tsa
+    wl = make_retopk(L0=6000, steps=1, K=64, C=8, R=2, W=8)
+    dev = "cuda"
+    k, v = wl.k.to(dev), wl.v.to(dev)
+    if paged:
+        ps = 16
+        npg = wl.lcap // ps
+        perm = torch.randperm(npg, generator=torch.Generator().manual_seed(3)).to(torch.int32)
+        kp = torch.zeros((npg, wl.Hkv, ps, wl.d), dtype=torch.bfloat16, device=dev)
+        vp = torch.zeros_like(kp)
+        kp[perm.long().to(dev)] = k[0].reshape(wl.Hkv, npg, ps, wl.d).transpose(0, 1)
+        vp[perm.long().to(dev)] = v[0].reshape(wl.Hkv, npg, ps, wl.d).transpose(0, 1)
+        kv = tsa.kv_paged(kp, vp, perm[None].to(dev).contiguous())
+    else:
+        kv = tsa.kv_contiguous(k, v)
+    sup, cnt = gpu_prefill_supports(tsa, wl, kv, dev)
+    torch.cuda.synchronize()
+    sup, cnt = sup.cpu().numpy(), cnt.cpu().numpy()
+    G = wl.Hq // wl.Hkv
+    kb = [bits(wl.k[0, i]) for i in range(wl.Hkv)]
+    qpre = bits(wl.q_prefill)
+    for c in range(wl.C):
+        p = wl.L0 - wl.C + c
+        for h in range(wl.Hq):
+            assert cnt[c, h] == min(wl.K, p + 1)
+            got = sup[c, h, : cnt[c, h]]
+            assert np.all(sup[c, h, cnt[c, h]:] == -1)
+            z = orc.scores(qpre[c, h], kb[h // G][: p + 1], wl.scale)
+            assert orc.topk_check(z, np.arange(p + 1), wl.K, got, TIE_REL) in (1, 2), (c, h)
+
+
+def test_prefill_supports_equal_per_query_decode_and_repeat():
+    """The one-call supports equal C separate decode calls (window 0, length
+    p + 1), on a fresh workspace and again on the reused one (whose emission
+    keys now come from the first call)."""
+    import top_retrieval_sparse_gb300 as tsa
+    wl = make_retopk(L0=20_000, steps=1, K=128, C=12, R=2, W=8)
+    dev = "cuda"
+    kv = tsa.kv_contiguous(wl.k.to(dev), wl.v.to(dev))
+    ref, rcnt = decode_prefill_supports(tsa, wl, kv, dev)
+    n = tsa.prefill_workspace_size(wl.C, wl.Hq, wl.Hkv, wl.d, kv.l_cap, wl.K)
+    ws = torch.zeros(n, dtype=torch.uint8, device=dev)
+    q = wl.q_prefill.to(dev).contiguous()
+    for _ in range(2):
+        sup, cnt = tsa.prefill_supports(q, kv, wl.L0, wl.K, wl.scale, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(cnt, rcnt)
+        for c in range(wl.C):
+            for h in range(wl.Hq):
+                assert set(sup[c, h].tolist()) == set(ref[c, h].tolist()), (c, h)
+    assert tsa.workspace_status(ws) == 0

@@ -84,6 +84,10 @@ def lib():
             L.tsa_set_trace.argtypes = [P, sz]
             L.tsa_kernel_launches.restype = C.c_ulonglong
             L.tsa_workspace_status.argtypes = [P, i32, P]
+            L.retopk_prefill_workspace_size.argtypes = [i32, i32, i32, i32, i64, i32]
+            L.retopk_prefill_workspace_size.restype = sz
+            L.retopk_prefill_supports.argtypes = [P, P, i64, i32, i32, i32, i32, i32, f32, P, P,
+                                                  P, sz, P]
             L.tsa_inject_scan_stall.argtypes = [C.c_longlong]
             _lib = L
     return _lib
@@ -243,6 +247,34 @@ def sparse_attn_decode_noalloc(q: torch.Tensor, kv: KV, lens: torch.Tensor, K: i
 
 def noalloc_scratch_bytes() -> int:
     return int(lib().tsa_noalloc_scratch_bytes())
+
+
+def prefill_workspace_size(C, Hq, Hkv, d, l_cap, K) -> int:
+    return int(lib().retopk_prefill_workspace_size(C, Hq, Hkv, d, l_cap, K))
+
+
+def prefill_supports(q_prefill: torch.Tensor, kv: "KV", L0: int, K: int, scale=None,
+                     supports=None, counts=None, workspace=None, stream=None):
+    """Exact causal top-K of the last C prefill queries (q_prefill bf16
+    [C][Hq][128], query c at position L0 - C + c) over their prefixes, in one
+    call: returns (supports int32 [C][Hq][K] padded with -1, counts int32
+    [C][Hq])."""
+    _want(q_prefill, torch.bfloat16, "q_prefill")
+    Cn, Hq, d = q_prefill.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dev = q_prefill.device
+    if supports is None:
+        supports = torch.empty((Cn, Hq, K), dtype=torch.int32, device=dev)
+    if counts is None:
+        counts = torch.empty((Cn, Hq), dtype=torch.int32, device=dev)
+    if workspace is None:
+        n = prefill_workspace_size(Cn, Hq, kv.Hkv, d, kv.l_cap, K)
+        workspace = torch.zeros(n, dtype=torch.uint8, device=dev)
+    _check(lib().retopk_prefill_supports(_p(q_prefill), C.byref(kv.struct), int(L0), Cn, Hq,
+                                         kv.Hkv, d, K, float(scale), _p(supports), _p(counts),
+                                         _p(workspace), workspace.numel(), _stream(stream)))
+    return supports, counts
 
 
 def workspace_status(workspace: torch.Tensor, clear: bool = True, stream=None) -> int:

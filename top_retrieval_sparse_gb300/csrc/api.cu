@@ -225,6 +225,8 @@ KvView make_view(const tsa_kv* kv, int Hkv) {
   v.max_pages = kv->max_pages;
   v.l_cap = kv->l_cap;
   v.Hkv = Hkv;
+  v.seq_rows = (int64_t)Hkv * kv->l_cap;
+  v.pt_stride = kv->max_pages;
   return v;
 }
 
@@ -698,6 +700,80 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
   if ((e = stage_mark(3, s)) != cudaSuccess) return cuda_fail(e, "event record");
   st->t += 1;
   st->fifo_head = (st->fifo_head + 1) % st->C;
+  return ok();
+}
+
+size_t retopk_prefill_workspace_size(int C, int Hq, int Hkv, int d, int64_t l_cap, int K) {
+  (void)d;
+  if (C <= 0 || Hq <= 0 || Hkv <= 0 || l_cap < 0 || K <= 0) return 0;
+  // the decode workspace of C sequences without a window, plus the
+  // attention outputs the finish kernel writes (not returned)
+  return decode_layout(C, Hq, Hkv, l_cap, 0, 0).total + up((size_t)C * Hq * kD * 4);
+}
+
+int retopk_prefill_supports(const void* q_prefill, const tsa_kv* kv, int64_t L0, int C, int Hq,
+                            int Hkv, int d, int K, float scale, int32_t* supports,
+                            int32_t* counts, void* workspace, size_t ws_bytes, void* stream) {
+  int rc = check_heads(C, Hq, Hkv, d);
+  if (rc) return rc;
+  if ((rc = check_kv(kv, 1, Hkv))) return rc;
+  if (C < 1) return fail(TSA_ERR_INVALID_ARG, "C must be >= 1");
+  if (K < 1) return fail(TSA_ERR_INVALID_ARG, "K must be >= 1");
+  if (L0 < C || L0 > kv->l_cap)
+    return fail(TSA_ERR_INVALID_ARG, "L0 = %lld outside [C, l_cap]", (long long)L0);
+  if (!q_prefill || !supports) return fail(TSA_ERR_INVALID_ARG, "q_prefill and supports must be non-NULL");
+  if (!aligned(q_prefill, 16)) return fail(TSA_ERR_INVALID_ARG, "q_prefill must be 16-byte aligned");
+  if (!std::isfinite(scale)) return fail(TSA_ERR_INVALID_ARG, "scale must be finite");
+  const DecodeLayout Lw = decode_layout(C, Hq, Hkv, kv->l_cap, 0, 0);
+  const size_t need = retopk_prefill_workspace_size(C, Hq, Hkv, d, kv->l_cap, K);
+  if (!workspace || !aligned(workspace, kAlign))
+    return fail(TSA_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
+  if (ws_bytes < need)
+    return fail(TSA_ERR_WORKSPACE, "workspace %zu bytes < required %zu", ws_bytes, need);
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  // The C queries are C sequences of one batch that all read the cache of
+  // sequence 0 (sequence stride 0); query c sees positions [0, L0 - C + c].
+  KvView view = make_view(kv, Hkv);
+  view.seq_rows = 0;
+  view.pt_stride = 0;
+  SelWs w{};
+  w.status = reinterpret_cast<int*>(ws + Lw.status);
+  w.tile_ctr = reinterpret_cast<uint32_t*>(ws + Lw.tile_ctr);
+  w.emit_key = reinterpret_cast<uint32_t*>(ws + Lw.emit_key);
+  w.emit_margin = reinterpret_cast<float*>(ws + Lw.emit_margin);
+  w.dense = reinterpret_cast<uint2*>(ws + Lw.dense);
+  w.dense_n = reinterpret_cast<int32_t*>(ws + Lw.dense_n);
+  w.dense_stride = Lw.dense_stride;
+  w.spill = reinterpret_cast<uint64_t*>(ws + Lw.spill);
+  w.wz = reinterpret_cast<float*>(ws + Lw.wz);
+  w.wz_stride = Lw.wz_stride;
+  const int64_t len0 = L0 - C + 1;
+  cudaError_t e;
+  {
+    ScanArgs sa = scan_args(static_cast<const uint16_t*>(q_prefill), view, nullptr, len0, C, Hq,
+                            0, 0, scale, nullptr, 0, w);
+    sa.len_step = 1;
+    if ((e = counted(launch_scan(sa, scan_grid(C, view, L0), st, true))) != cudaSuccess)
+      return cuda_fail(e, "scan launch");
+  }
+  {
+    FinishArgs f = finish_args(static_cast<const uint16_t*>(q_prefill), view, Hq, scale, K, w);
+    f.lens = nullptr;
+    f.len_host = len0;
+    f.len_step = 1;
+    f.B = C;
+    f.n_init = 0;
+    f.n_recent = 0;
+    f.out = reinterpret_cast<float*>(ws + Lw.total);
+    f.lse_out = nullptr;
+    f.topk_idx = supports;
+    f.topk_score = nullptr;
+    f.topk_stride = K;
+    f.counts_out = counts;
+    if ((e = counted(launch_finish(f, st))) != cudaSuccess) return cuda_fail(e, "finish launch");
+  }
   return ok();
 }
 

@@ -364,10 +364,10 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   bool ptab_ok = false;
   if constexpr (NC == 1) {
     if (a.kv.page_table) {
-      const int64_t Lq = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
+      const int64_t Lq = seq_len(a.lens, a.len_host, a.len_step, b, a.kv.l_cap);
       const int64_t np = (Lq + (1 << a.kv.page_shift) - 1) >> a.kv.page_shift;
       if (np <= kPtabCap) {
-        const int32_t* pt = a.kv.page_table + (int64_t)b * a.kv.max_pages;
+        const int32_t* pt = a.kv.page_table + (int64_t)b * a.kv.pt_stride;
         for (int64_t q = tid; q < np; q += kFinThreads) sh.ptab[q] = __ldg(pt + q);
         ptab_ok = true;
       }
@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   };
   {  // the V rows of this CTA's share of the window do not depend on the scan:
      // start bringing them into L2 while it finishes
-    const int64_t L = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
+    const int64_t L = seq_len(a.lens, a.len_host, a.len_step, b, a.kv.l_cap);
     const int64_t nw = window_count(L, a.n_init, a.n_recent);
     for (int64_t j = nw * rank / NC + tid; j < nw * (rank + 1) / NC; j += kFinThreads) {
       const uint16_t* vr = a.kv.v + row_off(window_pos(j, L, a.n_init, a.n_recent));
@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
     }
     return;
   }
-  const int64_t L = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
+  const int64_t L = seq_len(a.lens, a.len_host, a.len_step, b, a.kv.l_cap);
   const int64_t nw = window_count(L, a.n_init, a.n_recent);
   // a ReTopK reuse head selects among its |A_t| rescored candidates
   const bool reuse = RT && path_in == 0;
@@ -1013,6 +1013,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
       }
     }
   }
+  if (a.counts_out && rank == 0 && tid == 0) a.counts_out[bh] = need > 0 ? need : 0;
   // The length contract (0 <= lens[b] <= l_cap) is checked here: an
   // out-of-range length was clamped by both kernels; flag it for the host.
   if (a.lens && rank == 0 && h == 0 && tid == 0) {

@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
           for (int j = 0; j < G; ++j)
             act |= a.head_active[b * a.Hq + g * G + j] == a.active_value;
         }
-        const int64_t L = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
+        const int64_t L = seq_len(a.lens, a.len_host, a.len_step, b, a.kv.l_cap);
         tiles = act ? (int)((L + kTileRows - 1) / kTileRows) : 0;
       }
       int incl = tiles;
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
       const int unit = locate(t);
       const int tile = t - unit_tiles[unit];
       const int b = unit / a.kv.Hkv, g = unit % a.kv.Hkv;
-      const int64_t L = seq_len(a.lens, a.len_host, b, a.kv.l_cap);
+      const int64_t L = seq_len(a.lens, a.len_host, a.len_step, b, a.kv.l_cap);
       const int64_t r0 = (int64_t)tile * kTileRows;
       const int64_t r1 = r0 + kTileRows < L ? r0 + kTileRows : L;
       const uint32_t bytes = (uint32_t)(r1 - r0) * kRowBytes;
@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
       cur_b = unit / a.kv.Hkv;
       cur_g = unit % a.kv.Hkv;
       head0 = cur_b * a.Hq + cur_g * G;
-      cur_L = seq_len(a.lens, a.len_host, cur_b, a.kv.l_cap);
+      cur_L = seq_len(a.lens, a.len_host, a.len_step, cur_b, a.kv.l_cap);
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int hl = 2 * tq + e;

@@ -63,23 +63,29 @@ struct KvView {
   int max_pages;
   int64_t l_cap;
   int Hkv;
+  // Rows between sequences (contiguous: Hkv * l_cap) and page-table entries
+  // between sequences (paged: max_pages); 0 makes every sequence index read
+  // sequence 0's cache (several queries of one sequence as a batch).
+  int64_t seq_rows;
+  int64_t pt_stride;
 };
 
 // Element offset of row i of KV head g of sequence b.
 __device__ __forceinline__ int64_t kv_row(const KvView& kv, int b, int g, int64_t i) {
   if (kv.page_table) {
-    int64_t page = kv.page_table[(int64_t)b * kv.max_pages + (i >> kv.page_shift)];
+    int64_t page = kv.page_table[(int64_t)b * kv.pt_stride + (i >> kv.page_shift)];
     int64_t r = i & ((1 << kv.page_shift) - 1);
     return (((page * kv.Hkv + g) << kv.page_shift) + r) * kD;
   }
-  return (((int64_t)b * kv.Hkv + g) * kv.l_cap + i) * kD;
+  return ((int64_t)b * kv.seq_rows + (int64_t)g * kv.l_cap + i) * kD;
 }
 
-// Sequence length, clamped to [0, cap] so that no position past the cache is
-// ever addressed.
-__device__ __forceinline__ int64_t seq_len(const int32_t* lens, int64_t len_host, int b,
-                                           int64_t cap) {
-  int64_t L = lens ? (int64_t)lens[b] : len_host;
+// Sequence length (lens[b], or len_host + b * len_step without a lens
+// array), clamped to [0, cap] so that no position past the cache is ever
+// addressed.
+__device__ __forceinline__ int64_t seq_len(const int32_t* lens, int64_t len_host,
+                                           int64_t len_step, int b, int64_t cap) {
+  int64_t L = lens ? (int64_t)lens[b] : len_host + (int64_t)b * len_step;
   return L < 0 ? 0 : (L > cap ? cap : L);
 }
 

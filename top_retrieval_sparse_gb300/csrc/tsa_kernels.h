@@ -24,8 +24,8 @@ namespace tsa {
 struct ScanArgs {
   const uint16_t* q;         // bf16 [B][Hq][128]
   KvView kv;
-  const int32_t* lens;       // [B] device, or nullptr -> len_host
-  int64_t len_host;
+  const int32_t* lens;       // [B] device, or nullptr -> len_host + b * len_step
+  int64_t len_host, len_step;
   int B, Hq;
   float scale;
   int n_init, n_recent;      // static window (logits to wz, not emitted)
@@ -61,10 +61,11 @@ struct FinishArgs {
   const uint16_t* q;         // bf16 [B][Hq][128] (re-emission only)
   KvView kv;
   const int32_t* lens;
-  int64_t len_host;
+  int64_t len_host, len_step;
   int B, Hq;
   float scale;
   int K, n_init, n_recent;
+  int32_t* counts_out;       // [B][Hq] or nullptr: |selected set| = min(K, |P|)
   uint32_t* emit_key;        // [B][Hq] the scan's emission key; the next call's is stored
   float* emit_margin;        // [B][Hq] per-head margin of the emission key (persistent)
   uint32_t* tile_ctr;        // the scan's tile claims (cleared)
