@@ -237,6 +237,55 @@ TSA_API int tsa_workspace_status(void* workspace, int clear, void* stream);
  * launched by this function. */
 TSA_API int tsa_inject_scan_stall(long long wait_limit_ns);
 
+/* sparse_attn_decode_shard -- one shard of a sequence split over devices
+ * ([RA] Eq. 4-5: partial attentions over disjoint sets merge exactly).
+ *
+ * The cache `kv` (B = 1) holds positions [pos_offset, pos_offset +
+ * shard_len) of a sequence of global_len positions, local row i being global
+ * position pos_offset + i.  For each query head this computes, over the
+ * shard's rows, what sparse_attn_decode computes over a whole cache, with the
+ * static window taken in global positions ([0, n_init) u [global_len -
+ * n_recent, global_len), met by the shard in a prefix and a suffix of it):
+ *   topk_idx / topk_score: the shard's local top-K outside the window, as
+ *     LOCAL row indices (add pos_offset for global positions) and logits;
+ *   out / lse_out: attention over the shard's window rows and that local
+ *     top-K (Eq. 4-5).
+ * A split decode step: every shard runs this, the shards exchange their K
+ * (logit, global position) pairs per head, every shard keeps the pairs of the
+ * global top-K that it holds and runs attend_set over them plus its window
+ * rows, and lse_merge folds the shards' (out, lse).
+ * q: bf16 [Hq][128]; out fp32 [Hq][128]; lse_out fp32 [Hq] or NULL;
+ * topk_idx int32 [Hq][K] or NULL; topk_score fp32 [Hq][K] or NULL.
+ * 0 <= shard_len <= kv->l_cap, pos_offset >= 0, pos_offset + shard_len <=
+ * global_len.  workspace: tsa_decode_workspace_size(1, Hq, Hkv, d, l_cap, K,
+ * n_init, n_recent) bytes, as for sparse_attn_decode. */
+TSA_API int sparse_attn_decode_shard(const void* q, const tsa_kv* kv, int64_t shard_len,
+                                     int64_t pos_offset, int64_t global_len, int Hq, int Hkv,
+                                     int d, int K, int n_init, int n_recent, float scale,
+                                     float* out, float* lse_out, int32_t* topk_idx,
+                                     float* topk_score, void* workspace, size_t ws_bytes,
+                                     void* stream);
+
+/* attend_set -- attention over a given set of rows ([RA] Eq. 3: the partial
+ * o_Omega over a set Omega chosen elsewhere).
+ *
+ * For each sequence b and query head h: z_i = scale * q_h . k_i for the
+ * counts[b][h] positions positions[b][h][0 .. counts-1] (rows of this
+ * cache), out = softmax(z) . V over them, lse = log sum e^z (an empty set:
+ * out 0, lse -inf).  No window is added; each listed row counts once per
+ * listing.  q: bf16 [B][Hq][128]; positions: int32 [B][Hq][M] (device),
+ * entries past counts ignored; counts: int32 [B][Hq] (device), 0..M;
+ * out fp32 [B][Hq][128]; lse_out fp32 [B][Hq] or NULL.  A position outside
+ * [0, kv->l_cap) is never read: it is left out and reported as
+ * TSA_ERR_DEVICE_CHECK by tsa_workspace_status.  1 <= M <= 2^24.
+ * workspace: tsa_attend_set_workspace_size(B, Hq, M) bytes, 256-byte
+ * aligned, zero-filled before its first use (calls leave it ready). */
+TSA_API size_t tsa_attend_set_workspace_size(int B, int Hq, int M);
+TSA_API int attend_set(const void* q, const tsa_kv* kv, int B, int Hq, int Hkv, int d,
+                       const int32_t* positions, const int32_t* counts, int M, float scale,
+                       float* out, float* lse_out, void* workspace, size_t ws_bytes,
+                       void* stream);
+
 /* ------------------------------------------------------------------ */
 /* lse_merge -- [RA] Eq. 4-5 on precomputed partials.
  *

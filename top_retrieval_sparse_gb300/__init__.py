@@ -84,6 +84,11 @@ def lib():
             L.tsa_set_trace.argtypes = [P, sz]
             L.tsa_kernel_launches.restype = C.c_ulonglong
             L.tsa_workspace_status.argtypes = [P, i32, P]
+            L.sparse_attn_decode_shard.argtypes = [P, P, i64, i64, i64, i32, i32, i32, i32, i32,
+                                                   i32, f32, P, P, P, P, P, sz, P]
+            L.tsa_attend_set_workspace_size.argtypes = [i32, i32, i32]
+            L.tsa_attend_set_workspace_size.restype = sz
+            L.attend_set.argtypes = [P, P, i32, i32, i32, i32, P, P, i32, f32, P, P, P, sz, P]
             L.retopk_prefill_workspace_size.argtypes = [i32, i32, i32, i32, i64, i32]
             L.retopk_prefill_workspace_size.restype = sz
             L.retopk_prefill_supports.argtypes = [P, P, i64, i32, i32, i32, i32, i32, f32, P, P,
@@ -247,6 +252,51 @@ def sparse_attn_decode_noalloc(q: torch.Tensor, kv: KV, lens: torch.Tensor, K: i
 
 def noalloc_scratch_bytes() -> int:
     return int(lib().tsa_noalloc_scratch_bytes())
+
+
+def decode_shard(q: torch.Tensor, kv: "KV", shard_len: int, pos_offset: int, global_len: int,
+                 K: int, n_init: int, n_recent: int, scale=None, out=None, lse_out=None,
+                 topk_idx=None, topk_score=None, workspace=None, stream=None):
+    """One shard [pos_offset, pos_offset + shard_len) of a sequence of
+    global_len positions (q bf16 [Hq][128]): local top-K (local row indices)
+    and attention over the shard's window rows and that top-K."""
+    _want(q, torch.bfloat16, "q")
+    Hq, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((Hq, d), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        n = decode_workspace_size(1, Hq, kv.Hkv, d, kv.l_cap, K, n_init, n_recent)
+        workspace = torch.zeros(n, dtype=torch.uint8, device=q.device)
+    _check(lib().sparse_attn_decode_shard(_p(q), C.byref(kv.struct), int(shard_len),
+                                          int(pos_offset), int(global_len), Hq, kv.Hkv, d, K,
+                                          n_init, n_recent, float(scale), _p(out), _p(lse_out),
+                                          _p(topk_idx), _p(topk_score), _p(workspace),
+                                          workspace.numel(), _stream(stream)))
+    return out
+
+
+def attend_set(q: torch.Tensor, kv: "KV", positions: torch.Tensor, counts: torch.Tensor,
+               scale=None, out=None, lse_out=None, workspace=None, stream=None):
+    """Attention over given rows: q bf16 [B][Hq][128], positions int32
+    [B][Hq][M], counts int32 [B][Hq]; returns out fp32 [B][Hq][128]."""
+    _want(q, torch.bfloat16, "q")
+    _want(positions, torch.int32, "positions")
+    _want(counts, torch.int32, "counts")
+    B, Hq, d = q.shape
+    M = positions.shape[-1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        n = int(lib().tsa_attend_set_workspace_size(B, Hq, M))
+        workspace = torch.zeros(n, dtype=torch.uint8, device=q.device)
+    _check(lib().attend_set(_p(q), C.byref(kv.struct), B, Hq, kv.Hkv, d, _p(positions),
+                            _p(counts), M, float(scale), _p(out), _p(lse_out), _p(workspace),
+                            workspace.numel(), _stream(stream)))
+    return out
 
 
 def prefill_workspace_size(C, Hq, Hkv, d, l_cap, K) -> int:

@@ -317,29 +317,25 @@ size_t tsa_decode_workspace_size(int B, int Hq, int Hkv, int d, int64_t l_cap, i
   return decode_layout(B, Hq, Hkv, l_cap, n_init, n_recent).total;
 }
 
-int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int B, int Hq,
-                       int Hkv, int d, int K, int n_init, int n_recent, float scale, float* out,
-                       float* lse_out, int32_t* topk_idx, float* topk_score, void* workspace,
-                       size_t ws_bytes, void* stream) {
-  int rc = check_decode(q, kv, lens, B, Hq, Hkv, d, K, n_init, n_recent, scale, out);
-  if (rc) return rc;
-  if (B == 0) return ok();
-  const DecodeLayout Lw = decode_layout(B, Hq, Hkv, kv->l_cap, n_init, n_recent);
-  if (!workspace || !aligned(workspace, kAlign))
-    return fail(TSA_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
-  if (ws_bytes < Lw.total)
-    return fail(TSA_ERR_WORKSPACE, "workspace %zu bytes < required %zu", ws_bytes, Lw.total);
+}  // extern "C"
 
+namespace {
+
+// The decode step's launches on workspace layout Lw: lengths from `lens`
+// (device) or, without it, len_host; the static window given as the number
+// of leading (n_init) and trailing (n_recent) positions of each sequence's
+// cache.
+int decode_run(const void* q, const KvView& view, const int32_t* lens, int64_t len_host, int B,
+               int Hq, int K, int n_init, int n_recent, float scale, float* out, float* lse_out,
+               int32_t* topk_idx, float* topk_score, const DecodeLayout& Lw, void* workspace,
+               cudaStream_t st) {
   // The workspace counters start at zero: the caller zeroes a new workspace
   // once and every call's finish kernel clears them again for the next call,
   // so no memset sits between consecutive calls and the key scan can be
   // launched as a programmatic dependent of the previous call's kernels.
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaError_t e = stage_mark(0, st);
   if (e != cudaSuccess) return cuda_fail(e, "event record");
-
-  const KvView view = make_view(kv, Hkv);
   SelWs w{};
   w.status = reinterpret_cast<int*>(ws + Lw.status);
   w.tile_ctr = reinterpret_cast<uint32_t*>(ws + Lw.tile_ctr);
@@ -353,10 +349,10 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
   w.wz_stride = Lw.wz_stride;
 
   // 1. key scan (logits, emitted pairs, window logits)
-  if (kv->l_cap > 0) {
-    const ScanArgs s = scan_args(static_cast<const uint16_t*>(q), view, lens, 0, B, Hq, n_init,
-                                 n_recent, scale, nullptr, 0, w);
-    if ((e = counted(launch_scan(s, scan_grid(B, view, kv->l_cap), st, true))) != cudaSuccess)
+  if (view.l_cap > 0) {
+    const ScanArgs s = scan_args(static_cast<const uint16_t*>(q), view, lens, len_host, B, Hq,
+                                 n_init, n_recent, scale, nullptr, 0, w);
+    if ((e = counted(launch_scan(s, scan_grid(B, view, view.l_cap), st, true))) != cudaSuccess)
       return cuda_fail(e, "scan launch");
   }
   if ((e = stage_mark(1, st)) != cudaSuccess) return cuda_fail(e, "event record");
@@ -365,6 +361,7 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
   {
     FinishArgs f = finish_args(static_cast<const uint16_t*>(q), view, Hq, scale, K, w);
     f.lens = lens;
+    f.len_host = len_host;
     f.B = B;
     f.n_init = n_init;
     f.n_recent = n_recent;
@@ -376,6 +373,140 @@ int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int
     if ((e = counted(launch_finish(f, st))) != cudaSuccess) return cuda_fail(e, "finish launch");
   }
   if ((e = stage_mark(3, st)) != cudaSuccess) return cuda_fail(e, "event record");
+  return ok();
+}
+
+// attend_set's workspace: the finish kernel's counters and per-head state
+// (the path words are zero: every head "reuses" its given set) and a spill
+// area of the set's size per head.
+struct AttendLayout {
+  size_t status, tile_ctr, dense_n, path, emit_key, emit_margin, zero_end, spill, total;
+  int64_t stride;
+};
+AttendLayout attend_layout(int B, int Hq, int M) {
+  AttendLayout L{};
+  const size_t rows = (size_t)B * Hq;
+  L.stride = (int64_t)up((size_t)(M > 0 ? M : 1) + 64, 64);
+  size_t o = 0;
+  L.status = o; o = up(o + 4);
+  L.tile_ctr = o; o = up(o + 4);
+  L.dense_n = o; o = up(o + rows * kCtrStride * 4);
+  L.path = o; o = up(o + rows * 4);
+  L.emit_key = o; o = up(o + rows * 4);
+  L.emit_margin = o; o = up(o + rows * 4);
+  L.zero_end = o;
+  L.spill = o; o = up(o + rows * (size_t)L.stride * 8);
+  L.total = o;
+  return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* lens, int B, int Hq,
+                       int Hkv, int d, int K, int n_init, int n_recent, float scale, float* out,
+                       float* lse_out, int32_t* topk_idx, float* topk_score, void* workspace,
+                       size_t ws_bytes, void* stream) {
+  int rc = check_decode(q, kv, lens, B, Hq, Hkv, d, K, n_init, n_recent, scale, out);
+  if (rc) return rc;
+  if (B == 0) return ok();
+  const DecodeLayout Lw = decode_layout(B, Hq, Hkv, kv->l_cap, n_init, n_recent);
+  if (!workspace || !aligned(workspace, kAlign))
+    return fail(TSA_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
+  if (ws_bytes < Lw.total)
+    return fail(TSA_ERR_WORKSPACE, "workspace %zu bytes < required %zu", ws_bytes, Lw.total);
+  return decode_run(q, make_view(kv, Hkv), lens, 0, B, Hq, K, n_init, n_recent, scale, out,
+                    lse_out, topk_idx, topk_score, Lw, workspace, static_cast<cudaStream_t>(stream));
+}
+
+int sparse_attn_decode_shard(const void* q, const tsa_kv* kv, int64_t shard_len,
+                             int64_t pos_offset, int64_t global_len, int Hq, int Hkv, int d, int K,
+                             int n_init, int n_recent, float scale, float* out, float* lse_out,
+                             int32_t* topk_idx, float* topk_score, void* workspace,
+                             size_t ws_bytes, void* stream) {
+  int rc = check_heads(1, Hq, Hkv, d);
+  if (rc) return rc;
+  if ((rc = check_kv(kv, 1, Hkv))) return rc;
+  if (!q || !out) return fail(TSA_ERR_INVALID_ARG, "q and out must be non-NULL");
+  if (!aligned(q, 16) || !aligned(out, 16))
+    return fail(TSA_ERR_INVALID_ARG, "q / out must be 16-byte aligned");
+  if (K < 0 || n_init < 0 || n_recent < 0)
+    return fail(TSA_ERR_INVALID_ARG, "K, n_init, n_recent must be >= 0");
+  if (!std::isfinite(scale)) return fail(TSA_ERR_INVALID_ARG, "scale must be finite");
+  if (shard_len < 0 || shard_len > kv->l_cap)
+    return fail(TSA_ERR_INVALID_ARG, "shard_len %lld outside [0, l_cap]", (long long)shard_len);
+  if (pos_offset < 0 || pos_offset + shard_len > global_len)
+    return fail(TSA_ERR_INVALID_ARG, "shard [%lld, %lld) outside [0, global_len = %lld)",
+                (long long)pos_offset, (long long)(pos_offset + shard_len), (long long)global_len);
+  const DecodeLayout Lw = decode_layout(1, Hq, Hkv, kv->l_cap, n_init, n_recent);
+  if (!workspace || !aligned(workspace, kAlign))
+    return fail(TSA_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
+  if (ws_bytes < Lw.total)
+    return fail(TSA_ERR_WORKSPACE, "workspace %zu bytes < required %zu", ws_bytes, Lw.total);
+  // The global window [0, n_init) u [global_len - n_recent, global_len)
+  // meets the shard [pos_offset, pos_offset + shard_len) in a prefix and a
+  // suffix of it: n_init - pos_offset leading and
+  // n_recent - (global_len - pos_offset - shard_len) trailing positions.
+  auto clampl = [&](int64_t x) { return x < 0 ? 0 : (x > shard_len ? shard_len : x); };
+  const int ni = (int)clampl((int64_t)n_init - pos_offset);
+  const int nr = (int)clampl((int64_t)n_recent - (global_len - pos_offset - shard_len));
+  return decode_run(q, make_view(kv, Hkv), nullptr, shard_len, 1, Hq, K, ni, nr, scale, out,
+                    lse_out, topk_idx, topk_score, Lw, workspace, static_cast<cudaStream_t>(stream));
+}
+
+size_t tsa_attend_set_workspace_size(int B, int Hq, int M) {
+  if (B <= 0 || Hq <= 0 || M < 1) return 0;
+  return attend_layout(B, Hq, M).total;
+}
+
+int attend_set(const void* q, const tsa_kv* kv, int B, int Hq, int Hkv, int d,
+               const int32_t* positions, const int32_t* counts, int M, float scale, float* out,
+               float* lse_out, void* workspace, size_t ws_bytes, void* stream) {
+  int rc = check_heads(B, Hq, Hkv, d);
+  if (rc) return rc;
+  if ((rc = check_kv(kv, B, Hkv))) return rc;
+  if (B == 0) return ok();
+  if (M < 1 || M > (1 << 24)) return fail(TSA_ERR_INVALID_ARG, "M must be in [1, 2^24]");
+  if (!q || !out || !positions || !counts)
+    return fail(TSA_ERR_INVALID_ARG, "q, positions, counts and out must be non-NULL");
+  if (!aligned(q, 16) || !aligned(out, 16))
+    return fail(TSA_ERR_INVALID_ARG, "q / out must be 16-byte aligned");
+  if (!std::isfinite(scale)) return fail(TSA_ERR_INVALID_ARG, "scale must be finite");
+  const AttendLayout Lw = attend_layout(B, Hq, M);
+  if (!workspace || !aligned(workspace, kAlign))
+    return fail(TSA_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
+  if (ws_bytes < Lw.total)
+    return fail(TSA_ERR_WORKSPACE, "workspace %zu bytes < required %zu", ws_bytes, Lw.total);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  // Every head takes the finish kernel's given-set path (a ReTopK reuse head
+  // without the FIFO push): its rows are rescored, all of them are selected
+  // (K = M >= count), and softmax.V runs over them without a window.
+  SelWs w{};
+  w.status = reinterpret_cast<int*>(ws + Lw.status);
+  w.tile_ctr = reinterpret_cast<uint32_t*>(ws + Lw.tile_ctr);
+  w.emit_key = reinterpret_cast<uint32_t*>(ws + Lw.emit_key);
+  w.emit_margin = reinterpret_cast<float*>(ws + Lw.emit_margin);
+  w.dense = nullptr;
+  w.dense_n = reinterpret_cast<int32_t*>(ws + Lw.dense_n);
+  w.dense_stride = Lw.stride;
+  w.spill = reinterpret_cast<uint64_t*>(ws + Lw.spill);
+  w.wz = nullptr;
+  w.wz_stride = 1;
+  const KvView view = make_view(kv, Hkv);
+  FinishArgs f = finish_args(static_cast<const uint16_t*>(q), view, Hq, scale, M, w);
+  f.lens = nullptr;
+  f.len_host = kv->l_cap;  // positions must lie below l_cap
+  f.B = B;
+  f.out = out;
+  f.lse_out = lse_out;
+  f.topk_stride = M;
+  f.path = reinterpret_cast<const int32_t*>(ws + Lw.path);
+  f.mcand = counts;
+  f.cand = reinterpret_cast<const uint32_t*>(positions);
+  f.cand_cap = M;
+  cudaError_t e = counted(launch_finish(f, static_cast<cudaStream_t>(stream)));
+  if (e != cudaSuccess) return cuda_fail(e, "attend_set launch");
   return ok();
 }
 

@@ -227,14 +227,16 @@ __device__ void rescore_count(const FinishArgs& a, int b, int h, int g, int G, i
   }
 }
 
-// A ReTopK reuse head's logits on its candidates [c0, c1) of A_t, as rank
-// keys into this CTA's candidate list (shared memory, then the top of the
-// slice's spill area).  A warp takes 32 candidates at a time: lane l holds
-// candidate base + l's position; key rows are read by half-warps (16 lanes x
-// 16 bytes), two rows per load, all 16 loads in flight before any is used.
+// A given candidate set's logits (a ReTopK reuse head's A_t, or attend_set's
+// rows) on candidates [c0, c1), as rank keys into this CTA's candidate list
+// (shared memory, then the top of the slice's spill area).  A warp takes 32
+// candidates at a time: lane l holds candidate base + l's position; key rows
+// are read by half-warps (16 lanes x 16 bytes), two rows per load, all 16
+// loads in flight before any is used.  A position at or past L is never read:
+// its logit is -inf (it is not attended) and the status word flags it.
 template <int W, class Sh>
 __device__ void reuse_logits(const FinishArgs& a, int b, int bh, int g, int64_t c0, int64_t c1,
-                             Sh& sh, uint64_t* spill) {
+                             int64_t L, Sh& sh, uint64_t* spill) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int half = lane >> 4, col = 8 * (lane & 15);
   const uint4 qw = *reinterpret_cast<const uint4*>(a.q + (int64_t)bh * kD + col);
@@ -244,13 +246,16 @@ __device__ void reuse_logits(const FinishArgs& a, int b, int bh, int g, int64_t 
   for (int64_t base = c0 + 32 * wid; base < c1; base += 32 * W) {
     const int64_t j = base + lane;
     const uint32_t pos = j < c1 ? crow[j] : 0u;
+    const bool inside = (int64_t)pos < L;
+    if (__any_sync(0xffffffffu, j < c1 && !inside) && lane == 0) atomicOr(a.status, kStatusBadLength);
     uint4 kv4[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
       const int r = 2 * k + half;
       const uint32_t pk = __shfl_sync(0xffffffffu, pos, r);
-      kv4[k] = base + r < c1 ? *reinterpret_cast<const uint4*>(a.kv.k + kv_row(a.kv, b, g, pk) + col)
-                             : make_uint4(0u, 0u, 0u, 0u);
+      kv4[k] = base + r < c1 && (int64_t)pk < L
+                   ? *reinterpret_cast<const uint4*>(a.kv.k + kv_row(a.kv, b, g, pk) + col)
+                   : make_uint4(0u, 0u, 0u, 0u);
     }
     float mine = 0.f;  // lane l ends with the logit of candidate base + l
 #pragma unroll
@@ -272,7 +277,7 @@ __device__ void reuse_logits(const FinishArgs& a, int b, int bh, int g, int64_t 
       if (lane == 2 * k + 1) mine = e1;
     }
     if (j < c1) {
-      const uint64_t v = rank_key(mine * a.scale, pos);
+      const uint64_t v = rank_key(inside ? mine * a.scale : -INFINITY, pos);
       const int64_t i = j - c0;
       if (i < kMyCap) sh.mycand[i] = v;
       else spill[c1 - 1 - (i - kMyCap)] = v;
@@ -594,7 +599,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
     n = mcand;  // the candidate index space (spill layout as for a list slice)
     s0 = n * rank / NC;
     s1 = n * (rank + 1) / NC;
-    reuse_logits<W>(a, b, bh, g, s0, s1, sh, spill);
+    reuse_logits<W>(a, b, bh, g, s0, s1, L, sh, spill);
     nmc = (int)(s1 - s0);
     __syncthreads();
   }
@@ -807,7 +812,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
       lv = true;
     } else {
       const uint64_t v = cand_at(j - (int)nw - nabove);
-      if (cand_selected(v)) {
+      if (cand_selected(v) && (int64_t)rank_pos(v) < L) {  // (given sets: only rows < L)
         pos = (int)rank_pos(v);
         z = key2f((uint32_t)(v >> 32));
         lv = true;
@@ -1042,7 +1047,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
     a.emit_key[bh] = next;
     a.emit_margin[bh] = f;
   }
-  if (RT && rank == 0) {  // ReTopK: (qbar_t, S_t) over the oldest FIFO entry
+  if (RT && a.cache_qbar && rank == 0) {  // ReTopK: (qbar_t, S_t) over the oldest FIFO entry
     const int64_t hc = (int64_t)bh * a.C + a.slot;
     if (tid < kD) a.cache_qbar[hc * kD + tid] = a.push_qbar[(int64_t)bh * kD + tid];
     if (tid == 0) a.cache_sup_n[hc] = need > 0 ? need : 0;
