@@ -363,7 +363,8 @@ TSA_API size_t retopk_workspace_size(const tsa_retopk* st);
  *   mcand_out int32 [Hq] (|A_t| on the reuse path, len on the exact path),
  *   cand_out int32 [Hq][R*K+W] (A_t ascending, -1 padded; reuse heads only),
  *   lse_out fp32 [Hq].
- * Advances the step counter and the FIFO head.  If a bounded wait of the
+ * Advances the step counter and the FIFO head.  (The same as
+ * retopk_step_batched with one handle.)  If a bounded wait of the
  * step's key scan expires (see tsa_workspace_status), out and lse are NaN
  * and the FIFO entry is not rewritten (it keeps an older entry): restore
  * the state memory and counters from a copy taken before the step to redo
@@ -402,6 +403,34 @@ TSA_API int retopk_prefill_supports(const void* q_prefill, const tsa_kv* kv, int
                                     int Hq, int Hkv, int d, int K, float scale,
                                     int32_t* supports, int32_t* counts, void* workspace,
                                     size_t ws_bytes, void* stream);
+
+/* retopk_step_batched -- one decode step of n sequences at once, each with
+ * its own ReTopK state (continuous batching: any set of initialised handles,
+ * in any order, may form a call; a sequence joins after retopk_init on its
+ * handle and retires by no longer being passed).
+ *
+ * handles: n distinct handles (1 <= n <= 64) with equal Hq, Hkv, K, C, R, W,
+ *   tau, T_r and max_len; each keeps its own step counter and FIFO head
+ *   (both advance by one).
+ * q: bf16 [n][Hq][128]; kv: the n sequences' caches in call order (B = n:
+ *   contiguous [n][Hkv][l_cap][128], or paged with page-table rows in call
+ *   order); lens: host int64 [n], 1 <= lens[b] <= min(l_cap, max_len).
+ * Per sequence b everything is as for retopk_step (its path decisions, A_t,
+ * S_t, output and FIFO push use only its own state and cache).  Outputs are
+ * retopk_step's with a leading [n] (out fp32 [n][Hq][128]; support_out int32
+ * [n][Hq][K]; path_out, mcand_out int32 [n][Hq]; cand_out int32
+ * [n][Hq][R*K+W]; lse_out fp32 [n][Hq]; optional ones NULL to skip).
+ * workspace: retopk_batched_workspace_size(handles[0], n_max) bytes for any
+ *   n <= n_max, 256-byte aligned, zero-filled before its first use; it keeps
+ *   per-row emission state (only the cost depends on it).  Its layout follows
+ *   from ws_bytes (the most sequences it holds), so pass the same ws_bytes
+ *   with a workspace on every call. */
+TSA_API size_t retopk_batched_workspace_size(const tsa_retopk* proto, int n_max);
+TSA_API int retopk_step_batched(tsa_retopk* const* handles, int n, const void* q,
+                                const tsa_kv* kv, const int64_t* lens, float scale, float* out,
+                                int32_t* support_out, int32_t* path_out, int32_t* mcand_out,
+                                int32_t* cand_out, float* lse_out, void* workspace,
+                                size_t ws_bytes, void* stream);
 
 /* Host-side counters of the handle (for checkpointing). */
 TSA_API int retopk_get_counters(const tsa_retopk* st, int64_t* t, int32_t* fifo_head);

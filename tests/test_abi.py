@@ -244,3 +244,43 @@ def test_prefill_supports_validation(lib):
     assert call(C=200) == -1        # C * Hkv > 512
     assert call(nb=n - 1) == -2
     assert call(ws=None) == -2
+
+
+def test_retopk_batched_validation(lib):
+    """retopk_step_batched checks its handles (count, initialised, equal
+    shapes, no shared state), lengths and workspace on the host."""
+    import top_retrieval_sparse_gb300 as tsa
+    n = lib.retopk_state_size(28, 128, 512, 32)
+    hs = []
+    for j in range(3):
+        h = C.c_void_p()
+        assert lib.retopk_create(C.byref(h), 28, 4, 128, 512, 32, 4, 32, 0.85, 128, 70000,
+                                 C.c_void_p((1 << 20) * (j + 1)), n) == 0
+        assert lib.retopk_set_counters(h, 0, 0) == 0  # marks it initialised (host only)
+        hs.append(h)
+    other = C.c_void_p()
+    assert lib.retopk_create(C.byref(other), 28, 4, 128, 256, 32, 4, 32, 0.85, 128, 70000,
+                             C.c_void_p(1 << 26), n) == 0
+    assert lib.retopk_set_counters(other, 0, 0) == 0
+    w1 = lib.retopk_batched_workspace_size(hs[0], 1)
+    w3 = lib.retopk_batched_workspace_size(hs[0], 3)
+    assert w1 == lib.retopk_workspace_size(hs[0]) and w3 > 2 * w1
+    assert lib.retopk_batched_workspace_size(hs[0], 65) == 0
+    kv = tsa._KvStruct(1 << 20, 1 << 21, None, 0, 0, 70000)
+
+    def call(handles, lens, nb=1 << 40):
+        arr = (C.c_void_p * len(handles))(*[h.value for h in handles])
+        ls = (C.c_int64 * len(lens))(*lens)
+        return lib.retopk_step_batched(arr, len(handles), FAKE, C.byref(kv), ls, 0.1, FAKE,
+                                       None, None, None, None, None, FAKE, nb, None)
+    assert call([hs[0], other], [100, 200]) == -1          # different K
+    assert call([hs[0], hs[0]], [100, 200]) == -1          # the same state twice
+    assert call(hs, [100, 0, 50]) == -1                    # a length below 1
+    assert call(hs, [100, 70001, 50]) == -1                # beyond max_len
+    assert call(hs, [100, 200, 300], nb=w3 - 1) == -2      # workspace too small
+    fresh = C.c_void_p()
+    assert lib.retopk_create(C.byref(fresh), 28, 4, 128, 512, 32, 4, 32, 0.85, 128, 70000,
+                             C.c_void_p(1 << 27), n) == 0
+    assert call([hs[0], fresh], [100, 200]) == -4          # not initialised
+    for h in hs + [other, fresh]:
+        assert lib.retopk_destroy(h) == 0

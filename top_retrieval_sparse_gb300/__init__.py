@@ -77,6 +77,9 @@ def lib():
             L.retopk_workspace_size.argtypes = [P]
             L.retopk_workspace_size.restype = sz
             L.retopk_step.argtypes = [P, P, P, i64, f32, P, P, P, P, P, P, P, sz, P]
+            L.retopk_batched_workspace_size.argtypes = [P, i32]
+            L.retopk_batched_workspace_size.restype = sz
+            L.retopk_step_batched.argtypes = [P, i32, P, P, P, f32, P, P, P, P, P, P, P, sz, P]
             L.retopk_get_counters.argtypes = [P, C.POINTER(i64), C.POINTER(C.c_int32)]
             L.retopk_set_counters.argtypes = [P, i64, C.c_int32]
             L.retopk_destroy.argtypes = [P]
@@ -396,6 +399,34 @@ class ReTopK:
                                  float(scale), _p(out), _p(support_out), _p(path_out),
                                  _p(mcand_out), _p(cand_out), _p(lse_out), _p(self.workspace),
                                  self.workspace.numel(), _stream(stream)))
+        return out
+
+    @staticmethod
+    def batched_workspace_size(proto: "ReTopK", n_max: int) -> int:
+        return int(lib().retopk_batched_workspace_size(proto.handle, n_max))
+
+    @staticmethod
+    def step_batched(handles, q, kv: KV, lens, scale=None, out=None, support_out=None,
+                     path_out=None, mcand_out=None, cand_out=None, lse_out=None,
+                     workspace=None, stream=None):
+        """One step of len(handles) sequences, each with its own state: q bf16
+        [n][Hq][128], kv with the n sequences in call order, lens (host ints)."""
+        _want(q, torch.bfloat16, "q")
+        n = len(handles)
+        Hq, d = handles[0].Hq, handles[0].d
+        if scale is None:
+            scale = 1.0 / math.sqrt(d)
+        if out is None:
+            out = torch.empty((n, Hq, d), dtype=torch.float32, device=q.device)
+        if workspace is None:
+            workspace = torch.zeros(ReTopK.batched_workspace_size(handles[0], n),
+                                    dtype=torch.uint8, device=q.device)
+        hs = (C.c_void_p * n)(*[h.handle.value for h in handles])
+        ls = (C.c_int64 * n)(*[int(x) for x in lens])
+        _check(lib().retopk_step_batched(hs, n, _p(q), C.byref(kv.struct), ls, float(scale),
+                                         _p(out), _p(support_out), _p(path_out), _p(mcand_out),
+                                         _p(cand_out), _p(lse_out), _p(workspace),
+                                         workspace.numel(), _stream(stream)))
         return out
 
     def counters(self):

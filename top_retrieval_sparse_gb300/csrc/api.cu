@@ -575,7 +575,7 @@ constexpr uint32_t kMagic = 0x52544b31u;  // "RTK1"
 
 struct RetopkLayout {
   size_t zero_begin, status, tile_ctr, dense_n, gbitmap, zero_end;
-  size_t emit_key, emit_margin, wz, dense, spill, qbar_new, path, cand, mcand, total;
+  size_t emit_key, emit_margin, wz, dense, spill, qbar_new, path, cand, mcand, lens, seqs, total;
   int64_t dense_stride, gbitmap_stride;
   int cand_cap;
 };
@@ -591,9 +591,10 @@ bool bitmap_in_smem(int64_t len) {
 }
 constexpr int64_t kMaxRetopkLen = kSmemBitmapBytes * 8 * 32;  // second level in 192 KiB
 
-RetopkLayout retopk_layout(const tsa_retopk* s) {
+// Workspace of a step over up to n sequences of handles shaped like s.
+RetopkLayout retopk_layout(const tsa_retopk* s, int n) {
   RetopkLayout L{};
-  const size_t H = (size_t)s->Hq;
+  const size_t H = (size_t)n * s->Hq;
   L.dense_stride = dense_stride_for(s->max_len);
   L.cand_cap = s->R * s->K + s->W;
   size_t o = 0;
@@ -614,6 +615,8 @@ RetopkLayout retopk_layout(const tsa_retopk* s) {
   L.path = o; o = up(o + H * 4);
   L.cand = o; o = up(o + H * (size_t)L.cand_cap * 4);
   L.mcand = o; o = up(o + H * 4);
+  L.lens = o; o = up(o + (size_t)n * 4);
+  L.seqs = o; o = up(o + (size_t)n * sizeof(RetopkSeq));
   L.total = o;
   return L;
 }
@@ -706,28 +709,60 @@ int retopk_init(tsa_retopk* st, const void* prefill_q, const int32_t* prefill_su
 
 size_t retopk_workspace_size(const tsa_retopk* st) {
   if (!st || st->magic != kMagic) return 0;
-  return retopk_layout(st).total;
+  return retopk_layout(st, 1).total;
 }
 
-int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, float scale,
-                float* out, int32_t* support_out, int32_t* path_out, int32_t* mcand_out,
-                int32_t* cand_out, float* lse_out, void* workspace, size_t ws_bytes,
-                void* stream) {
-  int rc = check_state(st);
+size_t retopk_batched_workspace_size(const tsa_retopk* st, int n_max) {
+  if (!st || st->magic != kMagic || n_max < 1 || n_max > kMaxRetopkBatch) return 0;
+  return retopk_layout(st, n_max).total;
+}
+
+int retopk_step_batched(tsa_retopk* const* sts, int n, const void* q, const tsa_kv* kv,
+                        const int64_t* lens, float scale, float* out, int32_t* support_out,
+                        int32_t* path_out, int32_t* mcand_out, int32_t* cand_out, float* lse_out,
+                        void* workspace, size_t ws_bytes, void* stream) {
+  if (!sts || n < 1 || n > kMaxRetopkBatch)
+    return fail(TSA_ERR_INVALID_ARG, "n must be in [1, %d] with a handle array", kMaxRetopkBatch);
+  if (!lens) return fail(TSA_ERR_INVALID_ARG, "lens (host array) is NULL");
+  const tsa_retopk* s0 = sts[0];
+  int rc = check_state(s0);
   if (rc) return rc;
-  if (!st->initialised) return fail(TSA_ERR_STATE, "retopk_init has not been called");
-  if ((rc = check_kv(kv, 1, st->Hkv))) return rc;
+  for (int b = 0; b < n; ++b) {
+    const tsa_retopk* sb = sts[b];
+    if ((rc = check_state(sb))) return rc;
+    if (!sb->initialised) return fail(TSA_ERR_STATE, "handle %d: retopk_init has not been called", b);
+    if (sb->Hq != s0->Hq || sb->Hkv != s0->Hkv || sb->K != s0->K || sb->C != s0->C ||
+        sb->R != s0->R || sb->W != s0->W || sb->T_r != s0->T_r || sb->tau != s0->tau ||
+        sb->max_len != s0->max_len)
+      return fail(TSA_ERR_INVALID_ARG, "handle %d: sizes and hyper-parameters differ from handle 0", b);
+    for (int c = 0; c < b; ++c)
+      if (sts[c] == sb || sts[c]->qbar == sb->qbar)
+        return fail(TSA_ERR_INVALID_ARG, "handles %d and %d share their state", c, b);
+  }
+  if ((rc = check_heads(n, s0->Hq, s0->Hkv, kD))) return rc;
+  if ((rc = check_kv(kv, n, s0->Hkv))) return rc;
   if (!q || !out) return fail(TSA_ERR_INVALID_ARG, "q and out must be non-NULL");
   if (!aligned(q, 16) || !aligned(out, 16))
     return fail(TSA_ERR_INVALID_ARG, "q/out must be 16-byte aligned");
-  if (len < 1 || len > kv->l_cap || len > st->max_len)
-    return fail(TSA_ERR_INVALID_ARG, "len %lld outside [1, min(l_cap, max_len)]", (long long)len);
+  int64_t lmax = 0;
+  for (int b = 0; b < n; ++b) {
+    if (lens[b] < 1 || lens[b] > kv->l_cap || lens[b] > s0->max_len)
+      return fail(TSA_ERR_INVALID_ARG, "lens[%d] = %lld outside [1, min(l_cap, max_len)]", b,
+                  (long long)lens[b]);
+    lmax = lens[b] > lmax ? lens[b] : lmax;
+  }
   if (!std::isfinite(scale)) return fail(TSA_ERR_INVALID_ARG, "scale must be finite");
-  const RetopkLayout Lw = retopk_layout(st);
   if (!workspace || !aligned(workspace, kAlign))
     return fail(TSA_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
-  if (ws_bytes < Lw.total)
-    return fail(TSA_ERR_WORKSPACE, "workspace %zu bytes < required %zu", ws_bytes, Lw.total);
+  // The layout follows from the workspace's capacity (the most sequences its
+  // ws_bytes hold), not from this call's n: calls with different n then see
+  // every counter and per-row state at the same place.
+  int ncap = 0;
+  for (int c = 1; c <= kMaxRetopkBatch && retopk_layout(s0, c).total <= ws_bytes; ++c) ncap = c;
+  if (ncap < n)
+    return fail(TSA_ERR_WORKSPACE, "workspace %zu bytes < required %zu", ws_bytes,
+                retopk_layout(s0, n).total);
+  const RetopkLayout Lw = retopk_layout(s0, ncap);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -736,10 +771,12 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
   // the three kernels form one chain of programmatic dependents.
   cudaError_t e = stage_mark(0, s);
   if (e != cudaSuccess) return cuda_fail(e, "event record");
-  const KvView view = make_view(kv, st->Hkv);
-  const int Hq = st->Hq;
+  const KvView view = make_view(kv, s0->Hkv);
+  const int Hq = s0->Hq;
   int32_t* path = reinterpret_cast<int32_t*>(ws + Lw.path);
   float* qbar_new = reinterpret_cast<float*>(ws + Lw.qbar_new);
+  int32_t* lens_ws = reinterpret_cast<int32_t*>(ws + Lw.lens);
+  RetopkSeq* seq_ws = reinterpret_cast<RetopkSeq*>(ws + Lw.seqs);
   SelWs w{};
   w.status = reinterpret_cast<int*>(ws + Lw.status);
   w.tile_ctr = reinterpret_cast<uint32_t*>(ws + Lw.tile_ctr);
@@ -752,23 +789,27 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
   w.wz = reinterpret_cast<float*>(ws + Lw.wz);
   w.wz_stride = 1;
 
-  // 1. selector: cosine recall, path decision, candidate union
+  // 1. selector: cosine recall, path decision, candidate union, per (sequence, head)
   {
     RetopkSelArgs a{};
     a.q = static_cast<const uint16_t*>(q);
-    a.cache_qbar = st->qbar;
-    a.cache_sup = st->sup;
-    a.cache_sup_n = st->sup_n;
+    a.n = n;
+    for (int b = 0; b < n; ++b) {
+      const tsa_retopk* sb = sts[b];
+      a.seq[b].qbar = sb->qbar;
+      a.seq[b].sup = sb->sup;
+      a.seq[b].sup_n = sb->sup_n;
+      a.seq[b].L = lens[b];
+      a.seq[b].fifo_head = sb->fifo_head;
+      a.seq[b].refresh = (sb->t % sb->T_r) == 0;
+    }
     a.Hq = Hq;
-    a.C = st->C;
-    a.R = st->R;
-    a.K = st->K;
-    a.W = st->W;
-    a.fifo_head = st->fifo_head;
-    a.refresh = (st->t % st->T_r) == 0;
-    a.tau = st->tau;
-    a.L = len;
-    a.bitmap_words = (int)((len + 31) / 32);
+    a.C = s0->C;
+    a.R = s0->R;
+    a.K = s0->K;
+    a.W = s0->W;
+    a.tau = s0->tau;
+    a.bitmap_words = (int)((lmax + 31) / 32);
     a.qbar_new = qbar_new;
     a.path = path;
     a.cand = reinterpret_cast<uint32_t*>(ws + Lw.cand);
@@ -777,61 +818,73 @@ int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, fl
     a.path_out = path_out;
     a.mcand_out = mcand_out;
     a.cand_out = cand_out;
+    a.lens_ws = lens_ws;
+    a.seq_ws = seq_ws;
     a.trace = g_trace;
     // the bitmap (or, for a long cache, only its second level: the bitmap is
     // the workspace's) in shared memory
     const size_t l2w = (size_t)(a.bitmap_words + 31) / 32;
-    const bool in_smem = bitmap_in_smem(len);
+    const bool in_smem = bitmap_in_smem(lmax);
     a.gbitmap = in_smem ? nullptr : reinterpret_cast<uint32_t*>(ws + Lw.gbitmap);
     a.gbitmap_stride = Lw.gbitmap_stride;
     const size_t smem = up((in_smem ? (size_t)a.bitmap_words + l2w : l2w) * 4, 16);
     if ((e = counted(launch_retopk_selector(a, smem, s))) != cudaSuccess)
       return cuda_fail(e, "retopk selector launch");
   }
-  // 2. exact-path heads: key scan over all keys (no window): the
-  //    emitted pairs; launched after the selector has decided the paths
-  if ((e = counted(launch_scan(scan_args(static_cast<const uint16_t*>(q), view, nullptr, len, 1,
+  // 2. exact-path heads: key scan over all keys (no window): the emitted
+  //    pairs; it waits for the selector (paths and lengths) before it starts
+  if ((e = counted(launch_scan(scan_args(static_cast<const uint16_t*>(q), view, lens_ws, 0, n,
                                          Hq, 0, 0, scale, path, 1, w),
-                               scan_grid(1, view, len), s, true))) != cudaSuccess)
+                               scan_grid(n, view, lmax), s, true))) != cudaSuccess)
     return cuda_fail(e, "scan launch");
   if ((e = stage_mark(1, s)) != cudaSuccess) return cuda_fail(e, "event record");
   if ((e = stage_mark(2, s)) != cudaSuccess) return cuda_fail(e, "event record");
   // 3. every head: exact top-K (of its pairs; a reuse head rescores A_t
   //    itself), softmax.V over S_t (no window), and the FIFO push of
-  //    (qbar_t, S_t) -- S_t is written into the slot
+  //    (qbar_t, S_t) -- S_t is written into the entry it overwrites
   {
-    FinishArgs f = finish_args(static_cast<const uint16_t*>(q), view, Hq, scale, st->K, w);
-    f.lens = nullptr;
-    f.len_host = len;
-    f.B = 1;
+    FinishArgs f = finish_args(static_cast<const uint16_t*>(q), view, Hq, scale, s0->K, w);
+    f.lens = lens_ws;
+    f.B = n;
     f.n_init = 0;
     f.n_recent = 0;
     f.out = out;
     f.lse_out = lse_out;
-    f.topk_idx = st->sup + (int64_t)st->fifo_head * st->K;
+    f.topk_idx = support_out;
     f.topk_score = nullptr;
-    f.topk_stride = (int64_t)st->C * st->K;
+    f.topk_stride = s0->K;
     f.path = path;
     f.mcand = reinterpret_cast<const int32_t*>(ws + Lw.mcand);
     f.cand = reinterpret_cast<const uint32_t*>(ws + Lw.cand);
     f.cand_cap = Lw.cand_cap;
     f.push_qbar = qbar_new;
-    f.cache_qbar = st->qbar;
-    f.cache_sup_n = st->sup_n;
-    f.C = st->C;
-    f.slot = st->fifo_head;
+    f.seqs = seq_ws;
+    f.C = s0->C;
     if ((e = counted(launch_finish(f, s))) != cudaSuccess) return cuda_fail(e, "finish launch");
   }
-  if (support_out) {  // S_t rows, copied out of the FIFO slot
-    e = cudaMemcpy2DAsync(support_out, (size_t)st->K * 4, st->sup + (int64_t)st->fifo_head * st->K,
-                          (size_t)st->C * st->K * 4, (size_t)st->K * 4, (size_t)Hq,
-                          cudaMemcpyDeviceToDevice, s);
-    if (e != cudaSuccess) return cuda_fail(e, "support copy");
-  }
   if ((e = stage_mark(3, s)) != cudaSuccess) return cuda_fail(e, "event record");
-  st->t += 1;
-  st->fifo_head = (st->fifo_head + 1) % st->C;
+  for (int b = 0; b < n; ++b) {
+    tsa_retopk* sb = sts[b];
+    sb->t += 1;
+    sb->fifo_head = (sb->fifo_head + 1) % sb->C;
+  }
   return ok();
+}
+
+int retopk_step(tsa_retopk* st, const void* q, const tsa_kv* kv, int64_t len, float scale,
+                float* out, int32_t* support_out, int32_t* path_out, int32_t* mcand_out,
+                int32_t* cand_out, float* lse_out, void* workspace, size_t ws_bytes,
+                void* stream) {
+  int rc = check_state(st);
+  if (rc) return rc;
+  if (!st->initialised) return fail(TSA_ERR_STATE, "retopk_init has not been called");
+  if ((rc = check_kv(kv, 1, st->Hkv))) return rc;
+  if (len < 1 || len > kv->l_cap || len > st->max_len)
+    return fail(TSA_ERR_INVALID_ARG, "len %lld outside [1, min(l_cap, max_len)]", (long long)len);
+  tsa_retopk* one[1] = {st};
+  const int64_t lens[1] = {len};
+  return retopk_step_batched(one, 1, q, kv, lens, scale, out, support_out, path_out, mcand_out,
+                             cand_out, lse_out, workspace, ws_bytes, stream);
 }
 
 size_t retopk_prefill_workspace_size(int C, int Hq, int Hkv, int d, int64_t l_cap, int K) {

@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   // shared memory, so that a V row's address needs no dependent global load
   // (the table is an input: it is read before the scan completes).
   bool ptab_ok = false;
-  if constexpr (NC == 1) {
+  if constexpr (NC == 1 && !RT) {  // (a ReTopK step's lengths come from the selector)
     if (a.kv.page_table) {
       const int64_t Lq = seq_len(a.lens, a.len_host, a.len_step, b, a.kv.l_cap);
       const int64_t np = (Lq + (1 << a.kv.page_shift) - 1) >> a.kv.page_shift;
@@ -926,7 +926,15 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
       st_dsmem(&sh.ml[rank][st], 0, lsum);
     }
   }
-  const bool want_idx = a.topk_idx != nullptr || a.topk_score != nullptr;
+  // a ReTopK step writes S_t straight into the FIFO entry it overwrites
+  int32_t* ofifo = nullptr;
+  if (RT && a.seqs) {  // the record was written by the selector, complete since pdl_wait
+    const RetopkSeq* sq = a.seqs + b;
+    int32_t* sup = reinterpret_cast<int32_t*>(
+        __ldcg(reinterpret_cast<const unsigned long long*>(&sq->sup)));
+    ofifo = sup + ((int64_t)h * a.C + __ldcg(&sq->fifo_head)) * a.K;
+  }
+  const bool want_idx = a.topk_idx != nullptr || a.topk_score != nullptr || ofifo != nullptr;
   cluster_sync_all();  // every CTA's partial is in rank 0's shared memory; after this
                        // barrier no CTA reads another CTA's shared memory (but see below)
 
@@ -992,6 +1000,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
       }
       if (i < a.K) {
         if (oidx) oidx[i] = pos;
+        if (ofifo) ofifo[i] = pos;
         if (osc) osc[i] = z;
       }
     }
@@ -1007,6 +1016,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
           const int at = nabove + done + r;
           if (s && at < a.K) {
             if (oidx) oidx[at] = (int32_t)rank_pos(v);
+            if (ofifo) ofifo[at] = (int32_t)rank_pos(v);
             if (osc) osc[at] = key2f((uint32_t)(v >> 32));
           }
           done += tot;
@@ -1014,6 +1024,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
       }
       for (int q = (need > 0 ? need : 0) + tid; q < a.K; q += kFinThreads) {
         if (oidx) oidx[q] = -1;
+        if (ofifo) ofifo[q] = -1;
         if (osc) osc[q] = -INFINITY;
       }
     }
@@ -1047,10 +1058,15 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
     a.emit_key[bh] = next;
     a.emit_margin[bh] = f;
   }
-  if (RT && a.cache_qbar && rank == 0) {  // ReTopK: (qbar_t, S_t) over the oldest FIFO entry
-    const int64_t hc = (int64_t)bh * a.C + a.slot;
-    if (tid < kD) a.cache_qbar[hc * kD + tid] = a.push_qbar[(int64_t)bh * kD + tid];
-    if (tid == 0) a.cache_sup_n[hc] = need > 0 ? need : 0;
+  if (RT && a.seqs && rank == 0) {  // ReTopK: (qbar_t, S_t) over the oldest FIFO entry
+    const RetopkSeq* sq = a.seqs + b;
+    float* qbar = reinterpret_cast<float*>(
+        __ldcg(reinterpret_cast<const unsigned long long*>(&sq->qbar)));
+    int32_t* sup_n = reinterpret_cast<int32_t*>(
+        __ldcg(reinterpret_cast<const unsigned long long*>(&sq->sup_n)));
+    const int64_t hc = (int64_t)h * a.C + __ldcg(&sq->fifo_head);
+    if (tid < kD) qbar[hc * kD + tid] = a.push_qbar[(int64_t)bh * kD + tid];
+    if (tid == 0) sup_n[hc] = need > 0 ? need : 0;
   }
   // Candidates past rank 0's copy are read from the other CTAs: keep them
   // resident until rank 0 has written the outputs (a uniform decision).

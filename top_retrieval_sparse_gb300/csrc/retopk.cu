@@ -2,7 +2,7 @@
 // Top-K Reuse for Efficient Long-Context Attention", method sections 1-5 and
 // "GPU Kernel": fused selector, indexed QK, candidate top-K).
 //
-// selector  (one CTA per query head): qbar = q/|q|; rho_c = qbar . qbar_c over
+// selector  (one CTA per (sequence, query head)): qbar = q/|q|; rho_c = qbar . qbar_c over
 //           the C cached queries; exact path iff max rho < tau or a refresh
 //           step; otherwise the R most similar entries (ties: older entry
 //           first), the union of their supports and the last W positions as a
@@ -34,12 +34,18 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
   __shared__ int s_path;
   __shared__ uint32_t wtot[kSelectorThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int h = blockIdx.x;
+  const int bh = blockIdx.x;  // (sequence, query head) of the batch
+  const int b = bh / a.Hq, h = bh % a.Hq;
+  const RetopkSeq& sq = a.seq[b];
+  const int64_t L = sq.L;
+  const float* cache_qbar = sq.qbar;
+  const int32_t* cache_sup = sq.sup;
+  const int32_t* cache_sup_n = sq.sup_n;
 
   // 1. normalise the query
   float x = 0.f;
   if (tid < kD) {
-    x = __uint_as_float((uint32_t)a.q[(int64_t)h * kD + tid] << 16);
+    x = __uint_as_float((uint32_t)a.q[(int64_t)bh * kD + tid] << 16);
     qs[tid] = x;
   }
   float ss = warp_sum(x * x);
@@ -56,10 +62,10 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
   // long cache the head's zeroed words in the workspace.  A second level
   // (one bit per bitmap word, always in shared memory) marks the words that
   // hold a bit.
-  const int nwords = (int)((a.L + 31) >> 5);
+  const int nwords = (int)((L + 31) >> 5);
   const int nl2 = (nwords + 31) >> 5;
   const bool gbm = a.gbitmap != nullptr;
-  uint32_t* bitmap = gbm ? a.gbitmap + (int64_t)h * a.gbitmap_stride : sbits;
+  uint32_t* bitmap = gbm ? a.gbitmap + (int64_t)bh * a.gbitmap_stride : sbits;
   uint32_t* l2 = gbm ? sbits : sbits + nwords;
   for (int w = tid; w < (gbm ? nl2 : nwords + nl2); w += kSelectorThreads) sbits[w] = 0u;
   // the cache and this step's buffers belong to the previous step's kernels
@@ -67,10 +73,14 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
   pdl_wait();
   pdl_trigger();
   trace.mark(1);
+  if (h == 0 && tid == 0) {  // this step's length and FIFO entry, for the next kernels
+    a.lens_ws[b] = (int32_t)L;
+    a.seq_ws[b] = sq;
+  }
   if (tid < kD) {
     const float qb = nrm > 0.f ? qs[tid] / nrm : 0.f;
     qs[tid] = qb;
-    a.qbar_new[(int64_t)h * kD + tid] = qb;
+    a.qbar_new[(int64_t)bh * kD + tid] = qb;
   }
   __syncthreads();
 
@@ -82,7 +92,7 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
       const int c = wid + k * (kSelectorThreads / 32);
-      qv[k] = c < a.C ? *reinterpret_cast<const float4*>(a.cache_qbar +
+      qv[k] = c < a.C ? *reinterpret_cast<const float4*>(cache_qbar +
                                                          ((int64_t)h * a.C + c) * kD + lane * 4)
                       : make_float4(0.f, 0.f, 0.f, 0.f);
     }
@@ -106,37 +116,37 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
     float mx = -INFINITY;
     for (int c = lane; c < a.C; c += 32) mx = fmaxf(mx, rho[c]);
     mx = warp_max(mx);
-    const int path = (mx < a.tau || a.refresh) ? 1 : 0;
+    const int path = (mx < a.tau || sq.refresh) ? 1 : 0;
     if (lane == 0) {
       s_path = path;
-      a.path[h] = path;
-      if (a.path_out) a.path_out[h] = path;
+      a.path[bh] = path;
+      if (a.path_out) a.path_out[bh] = path;
     }
   }
   if (tid < a.C) {
     const float rc = rho[tid];
-    const int agec = (tid - a.fifo_head + a.C) % a.C;  // 0 = oldest
+    const int agec = (tid - sq.fifo_head + a.C) % a.C;  // 0 = oldest
     int beat = 0;
     for (int c = 0; c < a.C; ++c) {
       const float r = rho[c];
-      const int age = (c - a.fifo_head + a.C) % a.C;
+      const int age = (c - sq.fifo_head + a.C) % a.C;
       beat += (r > rc || (r == rc && age < agec)) ? 1 : 0;
     }
     if (beat < a.R) {  // ranks are distinct: one entry per rank
       chosen[beat] = tid;
-      chosen_n[beat] = a.cache_sup_n[(int64_t)h * a.C + tid];
+      chosen_n[beat] = cache_sup_n[(int64_t)h * a.C + tid];
     }
   }
   __syncthreads();
-  uint32_t* crow = a.cand + (int64_t)h * a.cand_cap;
+  uint32_t* crow = a.cand + (int64_t)bh * a.cand_cap;
   if (s_path) {
     if (tid == 0) {
-      a.mcand[h] = 0;
-      if (a.mcand_out) a.mcand_out[h] = (int32_t)a.L;
+      a.mcand[bh] = 0;
+      if (a.mcand_out) a.mcand_out[bh] = (int32_t)L;
     }
     if (a.cand_out)
       for (int j = tid; j < a.cand_cap; j += kSelectorThreads)
-        a.cand_out[(int64_t)h * a.cand_cap + j] = -1;
+        a.cand_out[(int64_t)bh * a.cand_cap + j] = -1;
     return;
   }
 
@@ -154,19 +164,19 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
         pv[u] = -1;
         if (j < total) {
           const int r = j / a.K, i = j - r * a.K;
-          if (i < chosen_n[r]) pv[u] = a.cache_sup[((int64_t)h * a.C + chosen[r]) * a.K + i];
+          if (i < chosen_n[r]) pv[u] = cache_sup[((int64_t)h * a.C + chosen[r]) * a.K + i];
         }
       }
 #pragma unroll
       for (int u = 0; u < kU; ++u)
-        if (pv[u] >= 0 && pv[u] < a.L) {
+        if (pv[u] >= 0 && pv[u] < L) {
           atomicOr(&bitmap[pv[u] >> 5], 1u << (pv[u] & 31));
           atomicOr(&l2[pv[u] >> 10], 1u << ((pv[u] >> 5) & 31));
         }
     }
   }
-  const int64_t lo = a.L - a.W > 0 ? a.L - a.W : 0;
-  for (int64_t p = lo + tid; p < a.L; p += kSelectorThreads)
+  const int64_t lo = L - a.W > 0 ? L - a.W : 0;
+  for (int64_t p = lo + tid; p < L; p += kSelectorThreads)
   {
     atomicOr(&bitmap[p >> 5], 1u << (p & 31));
     atomicOr(&l2[p >> 10], 1u << ((p >> 5) & 31));
@@ -201,8 +211,8 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
     }
     wtot[lane] = inc - t;
     if (lane == 31) {
-      a.mcand[h] = (int32_t)inc;
-      if (a.mcand_out) a.mcand_out[h] = (int32_t)inc;
+      a.mcand[bh] = (int32_t)inc;
+      if (a.mcand_out) a.mcand_out[bh] = (int32_t)inc;
     }
   }
   __syncthreads();
@@ -220,9 +230,9 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
   }
   if (a.cand_out) {
     __syncthreads();
-    const int m = a.mcand[h];
+    const int m = a.mcand[bh];
     for (int j = tid; j < a.cand_cap; j += kSelectorThreads)
-      a.cand_out[(int64_t)h * a.cand_cap + j] = j < m ? (int32_t)crow[j] : -1;
+      a.cand_out[(int64_t)bh * a.cand_cap + j] = j < m ? (int32_t)crow[j] : -1;
   }
 }
 
@@ -237,7 +247,7 @@ cudaError_t launch_retopk_selector(const RetopkSelArgs& a, size_t smem, cudaStre
     configured[dev] = smem;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.Hq);
+  cfg.gridDim = dim3(a.n * a.Hq);
   cfg.blockDim = dim3(kSelectorThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;

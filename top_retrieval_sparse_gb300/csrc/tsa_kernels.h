@@ -49,6 +49,8 @@ struct ScanArgs {
 };
 cudaError_t launch_scan(const ScanArgs& a, int grid, cudaStream_t st, bool pdl);
 
+struct RetopkSeq;  // one sequence of a ReTopK step (below)
+
 // Finish: one cluster of NC CTAs per (sequence, query head) takes every
 // emitted pair as a candidate and selects the exact top-K among them with a
 // cluster-wide radix on the 64-bit rank key; when fewer pairs than K were
@@ -81,19 +83,19 @@ struct FinishArgs {
   int32_t* topk_idx;         // [B][Hq] rows of topk_stride, or nullptr
   float* topk_score;         // same layout, or nullptr
   int64_t topk_stride;       // elements between heads' output rows (K for decode)
-  // ReTopK (all nullptr for decode): heads with path == 0 rescore their
-  // |A_t| = mcand candidates cand (ascending positions, rows of cand_cap)
-  // and select among them (no histogram, no hint); every head pushes
-  // (qbar_t, S_t) into FIFO slot `slot` (S_t is written through topk_idx,
-  // which then points at the slot's support rows)
+  // Given-set heads (all nullptr for decode): heads with path == 0 rescore
+  // their mcand candidates cand (positions, rows of cand_cap) and select
+  // among them (no bins, no emission key).  With seqs set (a ReTopK step)
+  // every head of sequence b pushes (qbar_t, S_t) into the FIFO entry
+  // seqs[b].fifo_head of its state (S_t written straight into the entry's
+  // support row); attend_set leaves seqs null.
   const int32_t* path;
   const int32_t* mcand;
   const uint32_t* cand;
   int cand_cap;
-  const float* push_qbar;    // [Hq][128]
-  float* cache_qbar;         // [Hq][C][128]
-  int32_t* cache_sup_n;      // [Hq][C]
-  int C, slot;
+  const float* push_qbar;    // [B][Hq][128]
+  const RetopkSeq* seqs;     // [B] (device, written by the selector)
+  int C;
   TraceBuf trace;
 };
 cudaError_t launch_finish(const FinishArgs& a, cudaStream_t st);
@@ -103,31 +105,41 @@ cudaError_t launch_lse_merge(const float* oa, const float* la, const float* ob,
                              cudaStream_t st);
 
 // ReTopK ------------------------------------------------------------------
+// One sequence of a ReTopK step: its FIFO state (caller memory) and this
+// step's length, oldest entry and refresh flag.
+struct RetopkSeq {
+  float* qbar;               // [Hq][C][128]
+  int32_t* sup;              // [Hq][C][K]
+  int32_t* sup_n;            // [Hq][C]
+  int64_t L;                 // cache length this step
+  int32_t fifo_head;         // slot of the oldest entry (overwritten by this step)
+  int32_t refresh;           // t % T_r == 0
+};
+constexpr int kMaxRetopkBatch = 64;  // sequences of one step (kernel-parameter table)
+
 struct RetopkSelArgs {
-  const uint16_t* q;         // bf16 [Hq][128]
-  const float* cache_qbar;   // [Hq][C][128]
-  const int32_t* cache_sup;  // [Hq][C][K]
-  const int32_t* cache_sup_n;// [Hq][C]
+  const uint16_t* q;         // bf16 [n][Hq][128]
+  int n;                     // sequences
+  RetopkSeq seq[kMaxRetopkBatch];
   int Hq, C, R, K, W;
-  int fifo_head;             // slot of the oldest entry
-  int refresh;               // t % T_r == 0
   float tau;
-  int64_t L;
-  int bitmap_words;
+  int bitmap_words;          // of the longest sequence
   // Long caches: the candidate bitmap lives in global memory, gbitmap_stride
   // words per head (all zero between steps: the compaction clears every word
   // it reads), and only its second level in shared memory; nullptr: both in
   // shared memory.
   uint32_t* gbitmap;
   int64_t gbitmap_stride;
-  float* qbar_new;           // [Hq][128]
-  int32_t* path;             // [Hq] 1 exact, 0 reuse
-  uint32_t* cand;            // [Hq][cand_cap] ascending
-  int32_t* mcand;            // [Hq]
+  float* qbar_new;           // [n][Hq][128]
+  int32_t* path;             // [n][Hq] 1 exact, 0 reuse
+  uint32_t* cand;            // [n][Hq][cand_cap] ascending
+  int32_t* mcand;            // [n][Hq]
   int cand_cap;              // R*K + W
   int32_t* path_out;         // optional copies
   int32_t* mcand_out;
-  int32_t* cand_out;         // [Hq][cand_cap], -1 padded
+  int32_t* cand_out;         // [n][Hq][cand_cap], -1 padded
+  int32_t* lens_ws;          // [n] this step's lengths, for the scan and finish kernels
+  RetopkSeq* seq_ws;         // [n] the table above, for the finish kernel's push
   TraceBuf trace;
 };
 cudaError_t launch_retopk_selector(const RetopkSelArgs& a, size_t smem, cudaStream_t st);
