@@ -464,6 +464,97 @@ def run_retopk(args, ws, rank, local):
     return res if rank == 0 else None
 
 
+def run_retopk_batched(args, ws, rank, local, nseq=4):
+    """Batched ReTopK (continuous batching with per-request state): nseq
+    sequences of the 64K ReTopK workload (Qwen2.5-7B geometry, their own
+    seeds), each with its own FIFO state, stepped together by
+    retopk_step_batched; CUDA-graph timed over the step stream."""
+    import torch
+    import top_retrieval_sparse_gb300 as tsa
+    from workloads.gen import make_retopk
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    steps = min(args.steps, 512)
+    wls = [make_retopk("retopk64k", device=dev, seed=97 * rank + i, steps=steps)
+           for i in range(nseq)]
+    w0 = wls[0]
+    k = torch.stack([w.k[0] for w in wls]).contiguous()
+    v = torch.stack([w.v[0] for w in wls]).contiguous()
+    for w in wls:
+        w.k = w.v = None
+    torch.cuda.empty_cache()
+    kv = tsa.kv_contiguous(k, v)
+    hs = []
+    for i, w in enumerate(wls):
+        kv1 = tsa.kv_contiguous(k[i:i + 1], v[i:i + 1])
+        sup, cnt = tsa.prefill_supports(w.q_prefill.contiguous(), kv1, w.L0, w.K, w.scale)
+        g = tsa.ReTopK(w.Hq, w.Hkv, w.d, w.K, w.C, w.R, w.W, w.tau, w.T_r, w.lcap, device=dev)
+        g.init(w.q_prefill.contiguous(), sup, cnt)
+        hs.append(g)
+    state0 = [(g.state.clone(), g.counters()) for g in hs]
+    work = torch.zeros(tsa.ReTopK.batched_workspace_size(hs[0], nseq), dtype=torch.uint8,
+                       device=dev)
+    q_all = torch.stack([torch.stack([w.q_all[t] for w in wls]) for t in range(steps)]).contiguous()
+    out = torch.empty((nseq, w0.Hq, w0.d), dtype=torch.float32, device=dev)
+    path = torch.empty((steps, nseq, w0.Hq), dtype=torch.int32, device=dev)
+
+    def reset():
+        for g, (st, cn) in zip(hs, state0):
+            g.state.copy_(st)
+            g.set_counters(*cn)
+
+    def run(stream, record=False):
+        for t in range(steps):
+            tsa.ReTopK.step_batched(hs, q_all[t], kv, [w.length(t) for w in wls], w0.scale,
+                                    out=out, path_out=path[t] if record else None,
+                                    workspace=work, stream=stream)
+
+    stream = torch.cuda.current_stream()
+    reset()
+    run(stream, record=True)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream(device=dev)
+    graph = torch.cuda.CUDAGraph()
+    reset()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=side):
+        n0 = tsa.kernel_launches()
+        run(side)
+        launches = tsa.kernel_launches() - n0
+    for _ in range(2):
+        for g, (st, _) in zip(hs, state0):
+            g.state.copy_(st)
+        graph.replay()
+    torch.cuda.synchronize()
+    clocks = Clocks(torch.cuda.current_device())
+    clocks.start()
+    for g, (st, _) in zip(hs, state0):
+        g.state.copy_(st)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    p_h = path.cpu()
+    return {
+        "metric": "us per batched ReTopK decode layer-step", "value": round(1000 * ms / steps, 3),
+        "unit": "us/batched-layer-step", "n_gpus": 1, "steps": steps, "warmup": 2,
+        "ms_per_step": round(ms / steps, 5), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "us_per_sequence_step": round(1000 * ms / steps / nseq, 3),
+        "config": {"workload": "retopk_batched", "sequences": nseq, "Hq": w0.Hq, "Hkv": w0.Hkv,
+                   "context": w0.L0, "K": w0.K, "C": w0.C, "R": w0.R, "W": w0.W, "tau": w0.tau,
+                   "T_r": w0.T_r, "decode_steps": steps},
+        "timing": f"CUDA graph of the {steps}-step stream of retopk_step_batched calls",
+        "paths": {"reuse_head_fraction": round(float((p_h == 0).float().mean()), 4)},
+        "gpu_launches": launches, "clocks": clk,
+    }
+
+
 def run_trace(args, step, tsa, torch, dev, nsteps=3):
     """Run a few steps with the per-CTA trace on and summarise each kernel:
     span (first CTA start -> last CTA exit), gap from the previous kernel,
@@ -825,13 +916,18 @@ def run_reference(args, ws, rank):
     if args.workload.startswith("retopk"):
         # the ReTopK stream is stateful: one pass of the oracle over its start
         # (FIFO built untimed, then timed steps per path class, bounded)
-        wl = make_retopk(args.workload, device="cpu")
+        batched = args.workload == "retopk_batched"  # 4 sequences of the 64K stream
+        wl = make_retopk("retopk64k" if batched else args.workload, device="cpu")
         t0 = time.perf_counter()
         base = oracle_retopk_baseline(wl, budget_s=args.cpu_budget)
         dt = time.perf_counter() - t0
+        if batched:
+            base["value"] = round(4 * base["value"], 1)
+            base["unit"] = "us/batched-layer-step"
+            base["sample"] += "; times 4 sequences of the batch"
         v = base["value"]
         return {
-            "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT,
+            "impl": "reference", "metric": METRIC, "value": v, "unit": base["unit"],
             "n_gpus": ws, "steps": 1, "warmup": 0, "ms_per_step": round(1000 * dt, 3),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": args.workload},
@@ -892,7 +988,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="llama128k",
                     choices=["tiny", "llama128k", "llama1m", "yi_paged", "retopk64k",
-                             "retopk1m", "retopk4m"])
+                             "retopk1m", "retopk4m", "retopk_batched"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
@@ -908,6 +1004,8 @@ def main():
     ws, rank, local = dist_env()
     if args.impl == "reference":
         res = run_reference(args, ws, rank)
+    elif args.workload == "retopk_batched":
+        res = run_retopk_batched(args, ws, rank, local) if rank == 0 else None
     elif args.workload.startswith("retopk"):
         res = run_retopk(args, ws, rank, local)
     else:

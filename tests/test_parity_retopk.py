@@ -314,3 +314,45 @@ def test_prefill_supports_equal_per_query_decode_and_repeat():
             for h in range(wl.Hq):
                 assert set(sup[c, h].tolist()) == set(ref[c, h].tolist()), (c, h)
     assert tsa.workspace_status(ws) == 0
+
+
+def test_checkpoint_resume_in_a_fresh_handle():
+    """The ReTopK state is the caller's memory plus two host counters: a copy
+    of both taken mid-stream, restored into a new handle over new memory (and a
+    new, zeroed workspace), continues exactly as the uninterrupted run --
+    same paths, candidate sets and supports, outputs within 1e-5."""
+    import top_retrieval_sparse_gb300 as tsa
+    wl = make_retopk(L0=5000, steps=12, K=48, C=6, R=3, W=5, T_r=5)
+    dev = "cuda"
+    kv = tsa.kv_contiguous(wl.k.to(dev), wl.v.to(dev))
+    sup, cnt = gpu_prefill_supports(tsa, wl, kv, dev)
+    a = tsa.ReTopK(wl.Hq, wl.Hkv, 128, wl.K, wl.C, wl.R, wl.W, wl.tau, wl.T_r, wl.lcap)
+    a.init(wl.q_prefill.to(dev).contiguous(), sup, cnt)
+    cap = wl.R * wl.K + wl.W
+
+    def step(g, t):
+        so = torch.empty((wl.Hq, wl.K), dtype=torch.int32, device=dev)
+        po = torch.empty((wl.Hq,), dtype=torch.int32, device=dev)
+        co = torch.empty((wl.Hq, cap), dtype=torch.int32, device=dev)
+        out = g.step(wl.q_all[t].to(dev).contiguous(), kv, wl.length(t), wl.scale,
+                     support_out=so, path_out=po, cand_out=co)
+        torch.cuda.synchronize()
+        return out.cpu(), so.cpu(), po.cpu(), co.cpu()
+
+    for t in range(6):
+        step(a, t)
+    saved_state, saved_counters = a.state.clone(), a.counters()
+    b = tsa.ReTopK(wl.Hq, wl.Hkv, 128, wl.K, wl.C, wl.R, wl.W, wl.tau, wl.T_r, wl.lcap)
+    b.state.copy_(saved_state)
+    b.set_counters(*saved_counters)
+    n_exact = 0
+    for t in range(6, 12):
+        ra, rb = step(a, t), step(b, t)
+        assert torch.equal(ra[2], rb[2]), f"t={t}: paths"
+        assert torch.equal(ra[3], rb[3]), f"t={t}: candidate sets"
+        for h in range(wl.Hq):
+            assert set(ra[1][h].tolist()) == set(rb[1][h].tolist()), (t, h)
+        assert torch.max(torch.abs(ra[0] - rb[0])).item() < 1e-5
+        n_exact += int(ra[2].sum())
+    assert a.counters() == b.counters() == (12, 12 % wl.C)
+    assert n_exact >= wl.Hq  # the resumed part crosses a refresh step (t = 10)
