@@ -102,6 +102,10 @@ def lib():
                                                f64, _P, i32, _P, i64, _P, i64,
                                                _P, _P, _P, _P]
             L.orc_retopk_advance.argtypes = [_P]
+            L.orc_q8_fit.argtypes = [_P, i64, i32, i64, _P, _P, _P]
+            L.orc_q8_append.argtypes = [_P, i64, i32, i64, _P, _P, _P]
+            L.orc_q8_bound.argtypes = [_P, i32, f64, _P]
+            L.orc_q8_bound.restype = f64
             _lib = L
     return _lib
 
@@ -272,3 +276,39 @@ class ReTopK:
     def slot_qbar(self, h: int, c: int) -> np.ndarray:
         base = (h * self.C + c) * self.d
         return np.array([self._st.qbar[base + j] for j in range(self.d)])
+
+
+# ---------------------------------------------------------------------------
+# f4. Scalar int8 key quantisation (RetrievalAttention review, Appendix C
+# "CPU memory minimization"; per-channel symmetric is the reading of the
+# scheme the pages leave open).  Definitions in oracle.h.
+
+def q8_fit(k: np.ndarray):
+    """k: [L, d] bf16 bits.  Returns (scale float32[d], codes uint8[L, d]
+    offset binary, err float64[d])."""
+    k = _u16(k)
+    L, d = k.shape
+    scale = np.zeros(d, np.float32)
+    codes = np.zeros((L, d), np.uint8)
+    err = np.zeros(d, np.float64)
+    lib().orc_q8_fit(_ptr(k), L, d, d, _ptr(scale), _ptr(codes), _ptr(err))
+    return scale, codes, err
+
+
+def q8_append(k: np.ndarray, scale: np.ndarray, err: np.ndarray):
+    """Codes of more rows k [n, d] with fitted scales; returns (codes,
+    err updated as a running maximum; the input is not modified)."""
+    k = _u16(k)
+    n, d = k.shape
+    scale = np.ascontiguousarray(scale, np.float32)
+    err = _f64(err).copy()
+    codes = np.zeros((n, d), np.uint8)
+    lib().orc_q8_append(_ptr(k), n, d, d, _ptr(scale), _ptr(codes), _ptr(err))
+    return codes, err
+
+
+def q8_bound(q: np.ndarray, scale: float, err: np.ndarray) -> float:
+    """scale * sum_j |q_j| e_j: the bound on a logit's quantisation error."""
+    q = _u16(q)
+    err = _f64(err)
+    return float(lib().orc_q8_bound(_ptr(q), len(q), scale, _ptr(err)))

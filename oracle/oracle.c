@@ -448,3 +448,51 @@ void orc_retopk_step_head(orc_retopk* st, int h, const uint16_t* q,
 }
 
 void orc_retopk_advance(orc_retopk* st) { st->t += 1; }
+
+/* ------------------------------------------------------------------ */
+/* f4. Scalar int8 key quantisation (see oracle.h for the definitions). */
+
+/* One code and its exact error; s is the channel's binary32 scale. */
+static uint8_t q8_code(uint16_t kbits, float s, double* e) {
+  const double kd = orc_bf16_to_f64(kbits);
+  long c = 0;
+  if (s != 0.0f) {
+    const float r = (float)kd / s; /* binary32 division */
+    double cr = rint((double)r);   /* nearest, ties to even */
+    if (cr > 127.0) cr = 127.0;
+    if (cr < -127.0) cr = -127.0;
+    c = (long)cr;
+  }
+  *e = fabs(kd - (double)s * (double)c); /* exact: 24 x 8 bit product */
+  return (uint8_t)(c + 128);
+}
+
+void orc_q8_fit(const uint16_t* k, int64_t L, int d, int64_t ld,
+                float* scale, uint8_t* codes, double* err) {
+  for (int j = 0; j < d; ++j) {
+    double m = 0.0;
+    for (int64_t i = 0; i < L; ++i) {
+      const double a = fabs(orc_bf16_to_f64(k[i * ld + j]));
+      if (a > m) m = a;
+    }
+    scale[j] = (float)m / 127.0f; /* m is a bf16 value: exact as float */
+    err[j] = 0.0;
+  }
+  orc_q8_append(k, L, d, ld, scale, codes, err);
+}
+
+void orc_q8_append(const uint16_t* k, int64_t n, int d, int64_t ld,
+                   const float* scale, uint8_t* codes, double* err) {
+  for (int64_t i = 0; i < n; ++i)
+    for (int j = 0; j < d; ++j) {
+      double e;
+      codes[i * d + j] = q8_code(k[i * ld + j], scale[j], &e);
+      if (e > err[j]) err[j] = e;
+    }
+}
+
+double orc_q8_bound(const uint16_t* q, int d, double scale, const double* err) {
+  double acc = 0.0;
+  for (int j = 0; j < d; ++j) acc += fabs(orc_bf16_to_f64(q[j])) * err[j];
+  return scale * acc;
+}

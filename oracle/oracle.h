@@ -179,6 +179,41 @@ void orc_retopk_step_head(orc_retopk* st, int h, const uint16_t* q,
 /* Advance the shared step counter after all heads ran step t. */
 void orc_retopk_advance(orc_retopk* st);
 
+/* ------------------------------------------------------------------ */
+/* f4. Scalar int8 key quantisation (RetrievalAttention review, Appendix
+ * C "CPU memory minimization" and "Scalar quantization of KV vectors with
+ * accuracy-preservation guarantees": 8-bit scalar quantisation of the key
+ * vectors, scheme left open; per-channel symmetric is the reading).
+ *
+ * One scale per channel j of one (sequence, KV head):
+ *   s_j  = fl32(maxabs_j / 127)       (binary32 division; maxabs over the
+ *                                      fitted rows, exact as a bf16 value)
+ *   c_ij = clamp(rint(fl32(k_ij / s_j)), -127, 127)   (rint: nearest, ties
+ *                                      to even; c = 0 where s_j = 0)
+ *   stored as the offset-binary byte u_ij = c_ij + 128
+ *   e_j  = max_i |k_ij - s_j c_ij|    (exact, in double)
+ * Rows appended later use the fitted s_j; a value past 127 s_j saturates
+ * and its larger error enters e_j.  The decisions that produce integers
+ * (s_j and the rounding of k/s) are taken in binary32, the precision of
+ * the quantiser under test; the error is exact. */
+
+/* Fit: scales over rows [0, L) and codes/errors of those rows.
+ * k: L rows of d bf16, stride ld; scale[d] (binary32), codes: L rows of d
+ * bytes (stride d), err[d]. */
+void orc_q8_fit(const uint16_t* k, int64_t L, int d, int64_t ld,
+                float* scale, uint8_t* codes, double* err);
+
+/* Append: codes of n more rows with the given scales; err[d] is updated in
+ * place (running maximum). */
+void orc_q8_append(const uint16_t* k, int64_t n, int d, int64_t ld,
+                   const float* scale, uint8_t* codes, double* err);
+
+/* The logit error bound of a quantised key: for every row i,
+ *   |scale * sum_j q_j k_ij - scale * sum_j q_j s_j c_ij|
+ *     <= scale * sum_j |q_j| e_j.
+ * Returns the right-hand side (double arithmetic). */
+double orc_q8_bound(const uint16_t* q, int d, double scale, const double* err);
+
 #ifdef __cplusplus
 }
 #endif
