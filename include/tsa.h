@@ -18,6 +18,10 @@
  *         Efficient Long-Context Attention" (ReTopK): sections 1-5 of the
  *         method (query-support cache, similar-query recall, candidate set,
  *         exact re-ranking, fallback and refresh) and "GPU Kernel".
+ *   [RA-review] the English review of RetrievalAttention: Appendix C "CPU
+ *         memory minimization" and the future-work item "Scalar
+ *         quantization of KV vectors with accuracy-preservation
+ *         guarantees" (8-bit scalar quantisation of the keys).
  *
  * Conventions shared by every entry point
  *   - Element types: q, K, V are bf16 (IEEE binary16-brain, 2 bytes);
@@ -210,6 +214,74 @@ TSA_API int sparse_attn_decode_noalloc(const void* q, const tsa_kv* kv,
                        int n_init, int n_recent, float scale, float* out,
                        float* lse_out, int32_t* topk_idx, float* topk_score,
                        void* stream);
+
+/* ------------------------------------------------------------------ */
+/* int8 key codes and the quantised decode -- [RA-review] Appendix C "CPU
+ * memory minimization" (8-bit scalar quantisation of the key vectors,
+ * scheme left open) and the future-work item "Scalar quantization of KV
+ * vectors with accuracy-preservation guarantees" (per-channel symmetric is
+ * the scheme used here; the worry there -- quantised keys shift the top-K --
+ * is removed by rescoring: the result is that of the bf16 keys).
+ *
+ * tsa_kq8: a quantised copy of a cache's keys, caller memory.
+ *   codes: uint8, the row geometry of kv->k with one byte per element
+ *          (contiguous [B][Hkv][l_cap][128], or paged [pages][Hkv]
+ *          [page_size][128] through kv->page_table); the code c in
+ *          [-127, 127] of k_ij is stored as the byte c + 128.  16-byte
+ *          aligned.
+ *   scale: fp32 [B][Hkv][128], the step s_j of each channel.
+ *   err:   fp32 [B][Hkv][128], an upper bound of |k_ij - s_j c_ij| over
+ *          every coded row of the channel.
+ *   Per channel: s_j = maxabs_j / 127 (binary32 division, maxabs over the
+ *   fitted rows), c_ij = clamp(rint(k_ij / s_j), -127, 127) (binary32
+ *   quotient, ties to even; c = 0 where s_j = 0). */
+typedef struct tsa_kq8 {
+  void* codes;
+  float* scale;
+  float* err;
+} tsa_kq8;
+
+/* tsa_quantize_keys -- codes of a cache's keys.
+ *   fit = 1: for each (sequence b, KV head, channel) s_j from the rows
+ *            [0, lens[b]), then codes and err of those rows (n_tail unused);
+ *   fit = 0: codes of the last n_tail rows [lens[b] - n_tail, lens[b])
+ *            (clipped at 0) with the stored scales; err is raised to cover
+ *            them (a value past 127 s_j saturates; its error counts).
+ * lens: int32 [B] (device), 0 <= lens[b] <= kv->l_cap.  Launches up to three
+ * kernels (and two memsets with fit) on `stream`; reads kv->k only.
+ * Returns TSA_OK or an error (nothing launched on an argument error). */
+TSA_API int tsa_quantize_keys(const tsa_kv* kv, const tsa_kq8* kq, const int32_t* lens,
+                              int B, int Hkv, int d, int64_t n_tail, int fit,
+                              void* stream);
+
+/* sparse_attn_decode_q8 -- sparse_attn_decode with the pool scanned through
+ * the key codes (128 bytes a key row instead of 256).
+ *
+ * Same arguments, contract and results as sparse_attn_decode: the selected
+ * set Omega, topk_idx / topk_score (the logits of the bf16 keys, bit for bit
+ * those sparse_attn_decode reports) and, up to the order of fp32 sums, out and
+ * lse.  The codes must cover rows [0, lens[b] - n_new) of every sequence
+ * when the call starts; the call first codes the last n_new rows (as
+ * tsa_quantize_keys with fit = 0), so a decode loop that appends one key a
+ * step passes n_new = 1.
+ * How: per query head a bound eps on |z_i - z^_i| (z^ the logit of the codes)
+ * is computed from err, the scales and the query; the scan emits the pool
+ * positions with z^ >= k^ (the head's emission key); the finish kernel
+ * rescores every emitted position on the bf16 keys and keeps those with
+ * z >= k^ + eps, which are all the pool positions with such a logit; when
+ * they are fewer than K it rescans the head's bf16 keys (slow, exact).
+ * workspace: tsa_decode_q8_workspace_size() bytes, same rules as
+ * sparse_attn_decode's (a q8 workspace is not interchangeable with a plain
+ * one). */
+TSA_API size_t tsa_decode_q8_workspace_size(int B, int Hq, int Hkv, int d, int64_t l_cap,
+                                            int K, int n_init, int n_recent);
+
+TSA_API int sparse_attn_decode_q8(const void* q, const tsa_kv* kv, const tsa_kq8* kq,
+                                  int n_new, const int32_t* lens, int B, int Hq, int Hkv,
+                                  int d, int K, int n_init, int n_recent, float scale,
+                                  float* out, float* lse_out, int32_t* topk_idx,
+                                  float* topk_score, void* workspace, size_t ws_bytes,
+                                  void* stream);
 
 /* tsa_workspace_status -- the device-side status of a decode or ReTopK
  * workspace.  The pages have no counterpart: this is error reporting.

@@ -284,3 +284,74 @@ def test_retopk_batched_validation(lib):
     assert call([hs[0], fresh], [100, 200]) == -4          # not initialised
     for h in hs + [other, fresh]:
         assert lib.retopk_destroy(h) == 0
+
+
+def _kq(tsa, codes=1 << 20, scale=1 << 21, err=1 << 22):
+    return tsa._Kq8Struct(codes, scale, err)
+
+
+def _decode_q8(lib, tsa, **kw):
+    a = dict(q=FAKE, kv=_kv(tsa), kq=_kq(tsa), n_new=1, lens=FAKE, B=1, Hq=8, Hkv=2, d=128,
+             K=16, n_init=4, n_recent=8, scale=0.1, out=FAKE, ws=FAKE, ws_bytes=1 << 40)
+    a.update(kw)
+    kq = C.byref(a["kq"]) if a["kq"] is not None else None
+    return lib.sparse_attn_decode_q8(a["q"], C.byref(a["kv"]), kq, a["n_new"], a["lens"],
+                                     a["B"], a["Hq"], a["Hkv"], a["d"], a["K"], a["n_init"],
+                                     a["n_recent"], a["scale"], a["out"], None, None, None,
+                                     a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=64), -1),
+    (dict(Hq=18, Hkv=2), -1),
+    (dict(K=-1), -1),
+    (dict(kq=None), -1),
+    (dict(n_new=-1), -1),
+    (dict(scale=float("inf")), -1),
+    (dict(lens=None), -1),
+    (dict(ws=None), -2),
+    (dict(ws_bytes=1000), -2),
+])
+def test_decode_q8_validation(lib, kw, code):
+    import top_retrieval_sparse_gb300 as tsa
+    if kw.get("kq", 0) is None:
+        assert _decode_q8(lib, tsa, kq=None) == code
+    else:
+        assert _decode_q8(lib, tsa, **kw) == code
+    assert lib.tsa_last_error().decode() != ""
+
+
+def test_decode_q8_rejects_bad_codes(lib):
+    import top_retrieval_sparse_gb300 as tsa
+    assert _decode_q8(lib, tsa, kq=_kq(tsa, codes=(1 << 20) + 8)) == -1  # codes not 16-aligned
+    assert _decode_q8(lib, tsa, kq=_kq(tsa, codes=0)) == -1
+    assert _decode_q8(lib, tsa, kq=_kq(tsa, err=0)) == -1
+    assert _decode_q8(lib, tsa, kq=_kq(tsa, scale=(1 << 21) + 2)) == -1  # scale not 4-aligned
+
+
+def _quantize(lib, tsa, **kw):
+    a = dict(kv=_kv(tsa), kq=_kq(tsa), lens=FAKE, B=1, Hkv=2, d=128, n_tail=1, fit=0)
+    a.update(kw)
+    kq = C.byref(a["kq"]) if a["kq"] is not None else None
+    return lib.tsa_quantize_keys(C.byref(a["kv"]), kq, a["lens"], a["B"], a["Hkv"], a["d"],
+                                 a["n_tail"], a["fit"], None)
+
+
+def test_quantize_keys_validation(lib):
+    import top_retrieval_sparse_gb300 as tsa
+    assert _quantize(lib, tsa, d=64) == -1
+    assert _quantize(lib, tsa, fit=2) == -1
+    assert _quantize(lib, tsa, n_tail=-1) == -1
+    assert _quantize(lib, tsa, kq=None) == -1
+    assert _quantize(lib, tsa, lens=None) == -1
+    assert _quantize(lib, tsa, Hkv=0) == -1
+    assert _quantize(lib, tsa, kv=_kv(tsa, 1024, 1 << 22, 24, 64)) == -1  # page size 24
+    assert _quantize(lib, tsa, B=0) == 0  # nothing to do: no launch
+
+
+def test_q8_workspace_extends_the_decode_one(lib):
+    args = (2, 32, 8, 128, 131136, 2048, 128, 512)
+    plain = lib.tsa_decode_workspace_size(*args)
+    q8 = lib.tsa_decode_q8_workspace_size(*args)
+    # fp16 prepared queries, two floats per head, each region 256-byte aligned
+    assert plain < q8 <= plain + 2 * 32 * (256 + 256 + 256) + 3 * 256

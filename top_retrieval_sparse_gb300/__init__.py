@@ -97,6 +97,11 @@ def lib():
             L.retopk_prefill_supports.argtypes = [P, P, i64, i32, i32, i32, i32, i32, f32, P, P,
                                                   P, sz, P]
             L.tsa_inject_scan_stall.argtypes = [C.c_longlong]
+            L.tsa_quantize_keys.argtypes = [P, P, P, i32, i32, i32, i64, i32, P]
+            L.tsa_decode_q8_workspace_size.argtypes = [i32, i32, i32, i32, i64, i32, i32, i32]
+            L.tsa_decode_q8_workspace_size.restype = sz
+            L.sparse_attn_decode_q8.argtypes = [P, P, P, i32, P, i32, i32, i32, i32, i32, i32,
+                                                i32, f32, P, P, P, P, P, sz, P]
             _lib = L
     return _lib
 
@@ -227,6 +232,67 @@ def sparse_attn_decode(q: torch.Tensor, kv: KV, lens: torch.Tensor, K: int, n_in
         _p(q), C.byref(kv.struct), _p(lens), B, Hq, kv.Hkv, d, K, n_init, n_recent,
         float(scale), _p(out), _p(lse_out), _p(topk_idx), _p(topk_score), _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out, lse_out, topk_idx, topk_score
+
+
+class _Kq8Struct(C.Structure):
+    _fields_ = [("codes", C.c_void_p), ("scale", C.c_void_p), ("err", C.c_void_p)]
+
+
+class KeyCodes:
+    """The int8 copy of a cache's keys (see tsa_kq8 in include/tsa.h): codes
+    with the row geometry of kv.k (one byte per element, offset binary),
+    per-(sequence, KV head, channel) scales and error bounds."""
+
+    def __init__(self, kv: "KV", B: Optional[int] = None):
+        dev = kv.k.device
+        self.B = kv.B if B is None else B
+        self.codes = torch.empty(kv.k.shape, dtype=torch.uint8, device=dev)
+        self.scale = torch.zeros((self.B, kv.Hkv, kv.d), dtype=torch.float32, device=dev)
+        self.err = torch.zeros((self.B, kv.Hkv, kv.d), dtype=torch.float32, device=dev)
+        self.struct = _Kq8Struct(self.codes.data_ptr(), self.scale.data_ptr(),
+                                 self.err.data_ptr())
+
+
+def quantize_keys(kv: "KV", codes: KeyCodes, lens: torch.Tensor, fit: bool = True,
+                  n_tail: int = 0, stream=None) -> KeyCodes:
+    """Fit scales and code rows [0, lens[b]) (fit), or code the last n_tail
+    rows of each sequence with the stored scales."""
+    _want(lens, torch.int32, "lens")
+    _check(lib().tsa_quantize_keys(C.byref(kv.struct), C.byref(codes.struct), _p(lens),
+                                   codes.B, kv.Hkv, kv.d, int(n_tail), 1 if fit else 0,
+                                   _stream(stream)))
+    return codes
+
+
+def decode_q8_workspace_size(B, Hq, Hkv, d, l_cap, K, n_init, n_recent) -> int:
+    return int(lib().tsa_decode_q8_workspace_size(B, Hq, Hkv, d, l_cap, K, n_init, n_recent))
+
+
+def sparse_attn_decode_q8(q: torch.Tensor, kv: KV, codes: KeyCodes, lens: torch.Tensor, K: int,
+                          n_init: int, n_recent: int, n_new: int = 0,
+                          scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                          lse_out: Optional[torch.Tensor] = None,
+                          topk_idx: Optional[torch.Tensor] = None,
+                          topk_score: Optional[torch.Tensor] = None,
+                          workspace: Optional[torch.Tensor] = None, stream=None):
+    """sparse_attn_decode through the key codes (same results; the last n_new
+    rows of each sequence are coded first).  The workspace is a q8 one."""
+    _want(q, torch.bfloat16, "q")
+    _want(lens, torch.int32, "lens")
+    B, Hq, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        nb = decode_q8_workspace_size(B, Hq, kv.Hkv, d, kv.l_cap, K, n_init, n_recent)
+        workspace = torch.zeros(max(nb, 256), dtype=torch.uint8, device=q.device)
+    _check(lib().sparse_attn_decode_q8(
+        _p(q), C.byref(kv.struct), C.byref(codes.struct), int(n_new), _p(lens), B, Hq, kv.Hkv,
+        d, K, n_init, n_recent, float(scale), _p(out), _p(lse_out), _p(topk_idx),
+        _p(topk_score), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
     return out, lse_out, topk_idx, topk_score
 
 

@@ -16,6 +16,7 @@
 
 namespace tsa {
 int scan_tile_rows();
+int scan_grid_rows(bool q8);
 }  // namespace tsa
 
 using namespace tsa;
@@ -185,9 +186,9 @@ FinishArgs finish_args(const uint16_t* q, const KvView& view, int Hq, float scal
 }
 
 // Persistent scan grid: one CTA per SM, at most one per tile.
-int scan_grid(int B, const KvView& view, int64_t max_len) {
-  const int64_t tiles =
-      (int64_t)B * view.Hkv * ((max_len + scan_tile_rows() - 1) / scan_tile_rows());
+int scan_grid(int B, const KvView& view, int64_t max_len, bool q8 = false) {
+  const int64_t tr = scan_grid_rows(q8);
+  const int64_t tiles = (int64_t)B * view.Hkv * ((max_len + tr - 1) / tr);
   int64_t grid = num_sms();
   if (grid > tiles) grid = tiles;
   if (grid < 1) grid = 1;
@@ -325,10 +326,20 @@ namespace {
 // (device) or, without it, len_host; the static window given as the number
 // of leading (n_init) and trailing (n_recent) positions of each sequence's
 // cache.
+// The quantised scan's inputs: the key codes and this call's query
+// preparation in the workspace.
+struct Q8Run {
+  uint8_t* codes;
+  const float* kscale;
+  float* kerr;
+  int n_new;
+  size_t qh, qts, eps;  // workspace offsets
+};
+
 int decode_run(const void* q, const KvView& view, const int32_t* lens, int64_t len_host, int B,
                int Hq, int K, int n_init, int n_recent, float scale, float* out, float* lse_out,
                int32_t* topk_idx, float* topk_score, const DecodeLayout& Lw, void* workspace,
-               cudaStream_t st) {
+               cudaStream_t st, const Q8Run* q8 = nullptr) {
   // The workspace counters start at zero: the caller zeroes a new workspace
   // once and every call's finish kernel clears them again for the next call,
   // so no memset sits between consecutive calls and the key scan can be
@@ -348,11 +359,39 @@ int decode_run(const void* q, const KvView& view, const int32_t* lens, int64_t l
   w.wz = reinterpret_cast<float*>(ws + Lw.wz);
   w.wz_stride = Lw.wz_stride;
 
-  // 1. key scan (logits, emitted pairs, window logits)
+  // 1. key scan (logits, emitted pairs, window logits); with key codes,
+  // after the query preparation (and the coding of the newest rows)
+  const bool quant = q8 && view.l_cap > 0;
+  if (quant) {
+    Q8PrepArgs p{};
+    p.q = static_cast<const uint16_t*>(q);
+    p.kv = view;
+    p.codes = q8->codes;
+    p.kscale = q8->kscale;
+    p.kerr = q8->kerr;
+    p.lens = lens;
+    p.len_host = len_host;
+    p.B = B;
+    p.Hq = Hq;
+    p.n_new = q8->n_new;
+    p.scale = scale;
+    p.qh = reinterpret_cast<uint16_t*>(ws + q8->qh);
+    p.qts = reinterpret_cast<float*>(ws + q8->qts);
+    p.eps = reinterpret_cast<float*>(ws + q8->eps);
+    if ((e = counted(launch_q8_prep(p, st, true))) != cudaSuccess)
+      return cuda_fail(e, "query preparation launch");
+  }
   if (view.l_cap > 0) {
-    const ScanArgs s = scan_args(static_cast<const uint16_t*>(q), view, lens, len_host, B, Hq,
-                                 n_init, n_recent, scale, nullptr, 0, w);
-    if ((e = counted(launch_scan(s, scan_grid(B, view, view.l_cap), st, true))) != cudaSuccess)
+    ScanArgs s = scan_args(static_cast<const uint16_t*>(q), view, lens, len_host, B, Hq, n_init,
+                           n_recent, scale, nullptr, 0, w);
+    if (quant) {
+      s.codes = q8->codes;
+      s.qh = reinterpret_cast<const uint16_t*>(ws + q8->qh);
+      s.qts = reinterpret_cast<const float*>(ws + q8->qts);
+      s.q8_new = q8->n_new;
+    }
+    if ((e = counted(launch_scan(s, scan_grid(B, view, view.l_cap, quant), st, true))) !=
+        cudaSuccess)
       return cuda_fail(e, "scan launch");
   }
   if ((e = stage_mark(1, st)) != cudaSuccess) return cuda_fail(e, "event record");
@@ -370,6 +409,29 @@ int decode_run(const void* q, const KvView& view, const int32_t* lens, int64_t l
     f.topk_idx = topk_idx;
     f.topk_score = topk_score;
     f.topk_stride = K;
+    if (quant) {  // the emitted pairs rescored exactly, the window logits
+      Q8RescoreArgs r{};
+      r.q = static_cast<const uint16_t*>(q);
+      r.kv = view;
+      r.lens = lens;
+      r.len_host = len_host;
+      r.B = B;
+      r.Hq = Hq;
+      r.scale = scale;
+      r.n_init = n_init;
+      r.n_recent = n_recent;
+      r.dense = w.dense;
+      r.dense_n = w.dense_n;
+      r.dense_stride = w.dense_stride;
+      r.emit_key = w.emit_key;
+      r.eps = reinterpret_cast<const float*>(ws + q8->eps);
+      r.wz = w.wz;
+      r.wz_stride = w.wz_stride;
+      r.trace = g_trace;
+      if ((e = counted(launch_q8_rescore(r, 2 * num_sms(), st))) != cudaSuccess)
+        return cuda_fail(e, "rescore launch");
+      f.q8_eps = r.eps;
+    }
     if ((e = counted(launch_finish(f, st))) != cudaSuccess) return cuda_fail(e, "finish launch");
   }
   if ((e = stage_mark(3, st)) != cudaSuccess) return cuda_fail(e, "event record");
@@ -453,6 +515,103 @@ int sparse_attn_decode_shard(const void* q, const tsa_kv* kv, int64_t shard_len,
   const int nr = (int)clampl((int64_t)n_recent - (global_len - pos_offset - shard_len));
   return decode_run(q, make_view(kv, Hkv), nullptr, shard_len, 1, Hq, K, ni, nr, scale, out,
                     lse_out, topk_idx, topk_score, Lw, workspace, static_cast<cudaStream_t>(stream));
+}
+
+// ---- int8 key codes and the quantised decode ----
+
+namespace {
+struct Q8Layout {
+  DecodeLayout d;
+  size_t qh, qts, eps, total;
+};
+Q8Layout decode_q8_layout(int B, int Hq, int Hkv, int64_t l_cap, int n_init, int n_recent) {
+  Q8Layout L{};
+  L.d = decode_layout(B, Hq, Hkv, l_cap, n_init, n_recent);
+  const size_t rows = (size_t)B * Hq;
+  size_t o = L.d.total;
+  L.qh = o; o = up(o + rows * kD * 2);
+  L.qts = o; o = up(o + rows * 4);
+  L.eps = o; o = up(o + rows * 4);
+  L.total = o;
+  return L;
+}
+int check_kq8(const tsa_kq8* kq) {
+  if (!kq || !kq->codes || !kq->scale || !kq->err)
+    return fail(TSA_ERR_INVALID_ARG, "kq, kq->codes, kq->scale and kq->err must be non-NULL");
+  if (!aligned(kq->codes, 16)) return fail(TSA_ERR_INVALID_ARG, "kq->codes must be 16-byte aligned");
+  if (!aligned(kq->scale, 4) || !aligned(kq->err, 4))
+    return fail(TSA_ERR_INVALID_ARG, "kq->scale / kq->err must be 4-byte aligned");
+  return TSA_OK;
+}
+}  // namespace
+
+size_t tsa_decode_q8_workspace_size(int B, int Hq, int Hkv, int d, int64_t l_cap, int K,
+                                    int n_init, int n_recent) {
+  (void)d;
+  (void)K;
+  if (B < 0 || Hq <= 0 || l_cap < 0) return 0;
+  return decode_q8_layout(B, Hq, Hkv, l_cap, n_init, n_recent).total;
+}
+
+int tsa_quantize_keys(const tsa_kv* kv, const tsa_kq8* kq, const int32_t* lens, int B, int Hkv,
+                      int d, int64_t n_tail, int fit, void* stream) {
+  if (d != kD) return fail(TSA_ERR_INVALID_ARG, "d = %d: only d = 128 is compiled", d);
+  if (B < 0 || Hkv <= 0) return fail(TSA_ERR_INVALID_ARG, "B/Hkv out of range");
+  int rc = check_kv(kv, B, Hkv);
+  if (rc) return rc;
+  if ((rc = check_kq8(kq))) return rc;
+  if (fit != 0 && fit != 1) return fail(TSA_ERR_INVALID_ARG, "fit must be 0 or 1");
+  if (!fit && n_tail < 0) return fail(TSA_ERR_INVALID_ARG, "n_tail must be >= 0");
+  if ((int64_t)B * Hkv > 65535) return fail(TSA_ERR_INVALID_ARG, "B*Hkv > 65535");
+  if (B == 0) return ok();
+  if (!lens) return fail(TSA_ERR_INVALID_ARG, "lens must be non-NULL");
+  const KvView view = make_view(kv, Hkv);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (fit) {
+    const size_t bytes = (size_t)B * Hkv * kD * 4;
+    if ((e = cudaMemsetAsync(kq->scale, 0, bytes, st)) != cudaSuccess)
+      return cuda_fail(e, "memset");
+    if ((e = cudaMemsetAsync(kq->err, 0, bytes, st)) != cudaSuccess)
+      return cuda_fail(e, "memset");
+  }
+  e = launch_q8_quantize(view, lens, B, fit ? 0 : n_tail, fit != 0,
+                         static_cast<uint8_t*>(kq->codes), kq->scale, kq->err, st);
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+  const int64_t rows = fit ? view.l_cap : (n_tail < view.l_cap ? n_tail : view.l_cap);
+  if (rows > 0) g_launches.fetch_add(fit ? 3 : 1, std::memory_order_relaxed);
+  return ok();
+}
+
+int sparse_attn_decode_q8(const void* q, const tsa_kv* kv, const tsa_kq8* kq, int n_new,
+                          const int32_t* lens, int B, int Hq, int Hkv, int d, int K, int n_init,
+                          int n_recent, float scale, float* out, float* lse_out,
+                          int32_t* topk_idx, float* topk_score, void* workspace, size_t ws_bytes,
+                          void* stream) {
+  int rc = check_decode(q, kv, lens, B, Hq, Hkv, d, K, n_init, n_recent, scale, out);
+  if (rc) return rc;
+  if ((rc = check_kq8(kq))) return rc;
+  if (n_new < 0) return fail(TSA_ERR_INVALID_ARG, "n_new must be >= 0");
+  if ((int64_t)B * Hq > kQ8MaxHeads)
+    return fail(TSA_ERR_INVALID_ARG, "B*Hq = %lld > %d for the quantised scan",
+                (long long)B * Hq, kQ8MaxHeads);
+  if (B == 0) return ok();
+  const Q8Layout Lq = decode_q8_layout(B, Hq, Hkv, kv->l_cap, n_init, n_recent);
+  if (!workspace || !aligned(workspace, kAlign))
+    return fail(TSA_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
+  if (ws_bytes < Lq.total)
+    return fail(TSA_ERR_WORKSPACE, "workspace %zu bytes < required %zu", ws_bytes, Lq.total);
+  Q8Run r{};
+  r.codes = static_cast<uint8_t*>(kq->codes);
+  r.kscale = kq->scale;
+  r.kerr = kq->err;
+  r.n_new = n_new;
+  r.qh = Lq.qh;
+  r.qts = Lq.qts;
+  r.eps = Lq.eps;
+  return decode_run(q, make_view(kv, Hkv), lens, 0, B, Hq, K, n_init, n_recent, scale, out,
+                    lse_out, topk_idx, topk_score, Lq.d, workspace,
+                    static_cast<cudaStream_t>(stream), &r);
 }
 
 size_t tsa_attend_set_workspace_size(int B, int Hq, int M) {

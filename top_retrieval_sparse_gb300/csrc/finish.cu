@@ -346,10 +346,12 @@ __device__ __noinline__ int reemit_head(const FinishArgs& a, FinShared<NC, W>& s
   return bstar;
 }
 
-// RT: a ReTopK step (reuse heads, the FIFO push); the decode instantiation
-// carries none of that code.
-template <int NC, int W, bool RT>
+// RT: a ReTopK step (reuse heads, the FIFO push); Q8: a decode step after
+// the quantised scan and the rescoring (the emission key in the codes'
+// domain); the plain decode instantiation carries neither.
+template <int NC, int W, bool RT, bool Q8>
 __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
+  static_assert(!(RT && Q8), "a ReTopK step scans bf16 keys");
   constexpr int kFinWarps = W, kFinThreads = 32 * W;
   constexpr int kBpt = kHistBins / kFinThreads;  // histogram bins per thread: 4 or 8
   static_assert(kBpt % 4 == 0 && kFinThreads >= 2 * kD, "block shape");
@@ -409,8 +411,10 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   // (with the sequence length), not one after another.
   const int status_in = __ldcg(a.status);
   const int64_t n_in = __ldcg(a.dense_n + (int64_t)bh * kCtrStride);
-  const uint32_t ekey = __ldcg(a.emit_key + bh);
+  uint32_t ekey = __ldcg(a.emit_key + bh);
   const float mg_in = __ldcg(a.emit_margin + bh);
+  // the rescored pairs are the pool positions with z >= k^ + eps
+  if constexpr (Q8) ekey = q8_exact_key(ekey, __ldcg(a.q8_eps + bh));
   const int path_in = RT ? __ldcg(a.path + bh) : 1;
   const int mc_in = RT ? __ldcg(a.mcand + bh) : 0;
 
@@ -1052,7 +1056,8 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
     if (need < P && bstar >= 0) {
       const float zref = cmode == 2 ? key2f((uint32_t)(T >> 32))
                                     : key2f((uint32_t)bstar << kHistShift);
-      const float ze = zref - f * 0.2f * (fabsf(zref) + 1.f);
+      float ze = zref - f * 0.2f * (fabsf(zref) + 1.f);
+      if constexpr (Q8) ze = __fsub_rd(ze, __ldcg(a.q8_eps + bh));  // the codes' domain
       next = ze == ze && fabsf(ze) < INFINITY ? f2key(ze) : 0u;
     }
     a.emit_key[bh] = next;
@@ -1073,7 +1078,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   if (NC > 1 && want_idx && cmode != 0 && ncand > kAllCap) cluster_sync_all();
 }
 
-template <int NC, int W, bool RT>
+template <int NC, int W, bool RT, bool Q8 = false>
 static cudaError_t launch_finish_t(const FinishArgs& a, cudaStream_t st) {
   const size_t smem = sizeof(FinShared<NC, W>);
   cudaLaunchConfig_t cfg = {};
@@ -1094,12 +1099,12 @@ static cudaError_t launch_finish_t(const FinishArgs& a, cudaStream_t st) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(finish_kernel<NC, W, RT>,
+    cudaError_t e = cudaFuncSetAttribute(finish_kernel<NC, W, RT, Q8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  return cudaLaunchKernelEx(&cfg, finish_kernel<NC, W, RT>, a);
+  return cudaLaunchKernelEx(&cfg, finish_kernel<NC, W, RT, Q8>, a);
 }
 
 // Cluster size: the largest of 8, 4, 2 whose CTAs for every head (one CTA of
@@ -1128,6 +1133,14 @@ cudaError_t launch_finish(const FinishArgs& a, cudaStream_t st) {
       case 4: return launch_finish_t<4, 16, true>(a, st);
       case 2: return launch_finish_t<2, 16, true>(a, st);
       default: return launch_finish_t<1, 16, true>(a, st);
+    }
+  }
+  if (a.q8_eps) {  // a decode step after the quantised scan
+    switch (nc) {
+      case 8: return launch_finish_t<8, 16, false, true>(a, st);
+      case 4: return launch_finish_t<4, 16, false, true>(a, st);
+      case 2: return launch_finish_t<2, 16, false, true>(a, st);
+      default: return launch_finish_t<1, 16, false, true>(a, st);
     }
   }
   switch (nc) {

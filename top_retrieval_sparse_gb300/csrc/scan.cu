@@ -41,15 +41,28 @@ namespace tsa {
 constexpr int kScanWarps = 16;                     // consumer warps
 constexpr int kConsumers = 32 * kScanWarps;
 constexpr int kScanThreads = kConsumers + 32;      // + one producer warp
-constexpr int kTileRows = 16 * kScanWarps;         // one m16 block per consumer warp
-constexpr int kTileBytes = kTileRows * kRowBytes;  // 64 KiB
+constexpr int kTileBytes = 16 * kScanWarps * kRowBytes;  // 64 KiB
 constexpr int kStages = 3;
+// Tile geometry: bf16 rows (256 bytes, one m16 block per consumer warp) or
+// key codes (128 bytes, two m16 blocks per consumer warp).
+template <bool Q8>
+struct Geom {
+  static constexpr int kRB = Q8 ? kD : kRowBytes;   // bytes per row
+  static constexpr int kTR = kTileBytes / kRB;      // rows per tile
+  static constexpr int kNB = kTR / (16 * kScanWarps);  // m16 blocks per warp
+};
 
 size_t scan_smem_bytes() {
   return (size_t)kStages * kTileBytes + 2 * kStages * 8 + (kMaxUnits + 1) * 4 + 64;
 }
 
+__device__ __forceinline__ uint32_t u4_word(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+template <bool Q8>
 __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
+  constexpr int kTileRows = Geom<Q8>::kTR, kRB = Geom<Q8>::kRB, kNB = Geom<Q8>::kNB;
   TraceScope trace(a.trace, kTrScan);
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
@@ -137,7 +150,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
   // Lane 0 waits for free stages and arms the full barrier; a contiguous tile
   // is one copy (lane 0), a paged tile one copy per page, issued by the lanes
   // in parallel so that the page-table reads overlap (tiles start on a page
-  // boundary: 256 rows is a multiple of every page size).
+  // boundary: 256 and 512 rows are multiples of every page size).
   if (warp == kScanWarps) {
     const uint64_t pol = policy_evict_first();
     int next_static = t_begin;
@@ -146,6 +159,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
     bool waited = a.head_active != nullptr;
     int j = 0;
     bool marker = false;
+    bool codes_ready = !Q8 || a.q8_new <= 0;  // (warp-uniform)
     for (;; ++j) {
       const int s = j % kStages;
       int go = 1, t = -1;
@@ -194,26 +208,34 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
       const int64_t L = seq_len(a.lens, a.len_host, a.len_step, b, a.kv.l_cap);
       const int64_t r0 = (int64_t)tile * kTileRows;
       const int64_t r1 = r0 + kTileRows < L ? r0 + kTileRows : L;
-      const uint32_t bytes = (uint32_t)(r1 - r0) * kRowBytes;
+      const uint32_t bytes = (uint32_t)(r1 - r0) * kRB;
       uint8_t* dst = ring + s * kTileBytes;
       // fault injection (tests only): the first stage is never armed or filled
       if (a.stall_first_copy && blockIdx.x == 0 && j == 0) continue;
+      // the newest rows' codes are written by the preceding kernel
+      if (!codes_ready && r1 > L - a.q8_new) {
+        pdl_wait();
+        codes_ready = true;
+      }
+      auto src = [&](int64_t r) -> const void* {
+        if constexpr (Q8) return a.codes + kv_row(a.kv, b, g, r);
+        else return a.kv.k + kv_row(a.kv, b, g, r);
+      };
       if (lane == 0) {
         fence_proxy_async();
         mbar_expect_tx(&full[s], bytes);
       }
       __syncwarp();
       if (!a.kv.page_table) {
-        if (lane == 0) bulk_g2s(dst, a.kv.k + kv_row(a.kv, b, g, r0), bytes, &full[s], pol);
+        if (lane == 0) bulk_g2s(dst, src(r0), bytes, &full[s], pol);
       } else {
         const int64_t ps = (int64_t)1 << a.kv.page_shift;
-        const int nseg = (int)((r1 - r0 + ps - 1) >> a.kv.page_shift);  // <= 16
+        const int nseg = (int)((r1 - r0 + ps - 1) >> a.kv.page_shift);  // <= 32
         for (int k = lane; k < nseg; k += 32) {
           const int64_t r = r0 + (int64_t)k * ps;
           const int64_t e = r + ps < r1 ? r + ps : r1;
           fence_proxy_async();
-          bulk_g2s(dst + (r - r0) * kRowBytes, a.kv.k + kv_row(a.kv, b, g, r),
-                   (uint32_t)(e - r) * kRowBytes, &full[s], pol);
+          bulk_g2s(dst + (r - r0) * kRB, src(r), (uint32_t)(e - r) * kRB, &full[s], pol);
         }
       }
     }
@@ -234,9 +256,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
   const int gr = lane >> 2;  // A rows gr, gr+8 / B column (query head) gr
   const int tq = lane & 3;   // k-slot group / C columns 2tq, 2tq+1
 
-  uint32_t qb[4][4];         // B fragments: head gr, d in [8(4p+tq), +8) for p < 4
+  // B fragments of head gr: bf16, d in [8(4p+tq), +8) for p < 4; or, for
+  // the codes, fp16 qh with d in [16 tq, +16) then [64 + 16 tq, +16)
+  uint32_t qb[4][4];
+  float qts[2] = {0.f, 0.f};    // codes: logit factors of heads 2tq, 2tq+1
   bool on[2] = {false, false};  // heads 2tq, 2tq+1 are active
-  uint32_t ekey[2] = {0u, 0u};  // emission keys of heads 2tq, 2tq+1
+  // emission thresholds of heads 2tq, 2tq+1 as floats: z >= thr exactly when
+  // f2key(z) >= the head's key (-inf: every logit; NaN: an inactive head)
+  float ethr[2] = {__int_as_float(0x7fc00000), __int_as_float(0x7fc00000)};
   bool lane_on = false;         // lane h < G: head h takes part (run owner)
   int run_ptr = 0;              // lane h < G: next free slot of this warp's run for head h
   int run_left = 0;             //            slots left in that run
@@ -272,27 +299,71 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
       cur_b = unit / a.kv.Hkv;
       cur_g = unit % a.kv.Hkv;
       head0 = cur_b * a.Hq + cur_g * G;
-      cur_L = seq_len(a.lens, a.len_host, a.len_step, cur_b, a.kv.l_cap);
+      cur_L = seq_len(a.lens, a.len_host, a.len_step, cur_b, a.kv.l_cap);  // < 2^31
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int hl = 2 * tq + e;
         const int bh = head0 + hl;
         on[e] = hl < G && (!a.head_active || a.head_active[bh] == a.active_value);
-        ekey[e] = on[e] ? __ldcg(a.emit_key + bh) : 0u;
+        const uint32_t ek = on[e] ? __ldcg(a.emit_key + bh) : 0u;
+        // keys at or below f2key(-inf) admit every finite logit
+        ethr[e] = !on[e] ? __int_as_float(0x7fc00000) : ek <= 0x007fffffu ? -INFINITY : key2f(ek);
+        if constexpr (Q8) qts[e] = on[e] ? __ldcg(a.qts + bh) : 0.f;
       }
       lane_on = lane < G && (!a.head_active || a.head_active[head0 + lane] == a.active_value);
-      const uint16_t* qp = a.q + ((int64_t)head0 + (gr < G ? gr : 0)) * kD;
+      if constexpr (Q8) {
+        const uint16_t* qp = a.qh + ((int64_t)head0 + (gr < G ? gr : 0)) * kD;
 #pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        if (gr < G) w = *reinterpret_cast<const uint4*>(qp + 8 * (4 * p + tq));
-        qb[p][0] = w.x; qb[p][1] = w.y; qb[p][2] = w.z; qb[p][3] = w.w;
+        for (int p = 0; p < 4; ++p) {  // p: dims 16 tq + 8p (p < 2), 64 + 16 tq + 8 (p - 2)
+          uint4 w = make_uint4(0u, 0u, 0u, 0u);
+          if (gr < G) w = __ldcg(reinterpret_cast<const uint4*>(qp + 64 * (p >> 1) + 16 * tq +
+                                                                8 * (p & 1)));
+          qb[p][0] = w.x; qb[p][1] = w.y; qb[p][2] = w.z; qb[p][3] = w.w;
+        }
+      } else {
+        const uint16_t* qp = a.q + ((int64_t)head0 + (gr < G ? gr : 0)) * kD;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          uint4 w = make_uint4(0u, 0u, 0u, 0u);
+          if (gr < G) w = *reinterpret_cast<const uint4*>(qp + 8 * (4 * p + tq));
+          qb[p][0] = w.x; qb[p][1] = w.y; qb[p][2] = w.z; qb[p][3] = w.w;
+        }
       }
     }
     const int tile = t - unit_tiles[cur_unit];
     if (j == 0) trace.mark(1);
-    {
-      // ---- 16 keys x 8 heads on the tensor cores ----
+    // ---- 16 keys x 8 heads on the tensor cores, per m16 block ----
+    // C: (row gr, head 2tq), (row gr, head 2tq+1), (row gr+8, 2tq), (row gr+8, 2tq+1)
+    float zb[kNB][4];
+    if constexpr (Q8) {
+      // lane: rows gr, gr+8 of each block, bytes [16 tq, +16) and [64 + 16 tq,
+      // +16); all loads first, so the stage is released before the math.  In
+      // k-step m, dims 4m..4m+3 of the lane's 32 (word m%4 of chunk m/4) are
+      // the k-slots (2tq, 2tq+1, 2tq+8, 2tq+9), and qb holds qh in that order.
+      const uint8_t* wb = ring + s * kTileBytes + warp * kNB * 16 * kD;
+      uint4 R[kNB][4];
+#pragma unroll
+      for (int blk = 0; blk < kNB; ++blk)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          R[blk][c] = *reinterpret_cast<const uint4*>(wb + (blk * 16 + gr + 8 * (c >> 1)) * kD +
+                                                      64 * (c & 1) + 16 * tq);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with stage s
+#pragma unroll
+      for (int blk = 0; blk < kNB; ++blk) {
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const uint32_t wa = u4_word(R[blk][m >> 2], m & 3);
+          const uint32_t wc = u4_word(R[blk][2 + (m >> 2)], m & 3);
+          mma_f16((m & 1) ? c1 : c0, codes_lo_f16x2(wa), codes_lo_f16x2(wc), codes_hi_f16x2(wa),
+                  codes_hi_f16x2(wc), qb[m >> 1][2 * (m & 1)], qb[m >> 1][2 * (m & 1) + 1]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) zb[blk][e] = (c0[e] + c1[e]) * qts[e & 1];
+      }
+    } else {
       const uint8_t* wb = ring + s * kTileBytes + warp * 16 * kRowBytes;
       float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -305,27 +376,40 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with stage s
-      // C: (row gr, head 2tq), (row gr, head 2tq+1), (row gr+8, 2tq), (row gr+8, 2tq+1)
-      const int64_t r0 = (int64_t)tile * kTileRows;
-      const int64_t rowA = r0 + warp * 16 + gr;
-      const bool pool_tile = r0 >= a.n_init && r0 + kTileRows <= cur_L - a.n_recent;
-      float zv[4];
-      unsigned emit = 0u;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int64_t i = rowA + ((e >> 1) << 3);
-        zv[e] = (c0[e] + c1[e]) * a.scale;
-        if (on[e & 1] && i < cur_L) {
-          if (!pool_tile && in_window(i, cur_L, a.n_init, a.n_recent)) {
-            const int64_t wa = a.n_init < cur_L ? a.n_init : cur_L;
-            const int64_t lo = cur_L - a.n_recent > wa ? cur_L - a.n_recent : wa;
-            const int64_t wj = i < wa ? i : wa + (i - lo);
-            a.wz[(int64_t)(head0 + 2 * tq + (e & 1)) * a.wz_stride + wj] = zv[e];
-          } else {
-            if (f2key(zv[e]) >= ekey[e & 1]) emit |= 1u << e;
+      for (int e = 0; e < 4; ++e) zb[0][e] = (c0[e] + c1[e]) * a.scale;
+    }
+#pragma unroll
+    for (int blk = 0; blk < kNB; ++blk) {
+      // row indices fit in 32 bits (l_cap < 2^31)
+      const int Lc = (int)cur_L;
+      const int rb = tile * kTileRows + (warp * kNB + blk) * 16;
+      const int rowA = rb + gr;
+      const float* zv = zb[blk];
+      unsigned emit = 0u;
+      if (rb >= a.n_init && rb + 16 <= Lc - a.n_recent) {  // a pool block (warp-uniform)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) emit |= (zv[e] >= ethr[e & 1] ? 1u : 0u) << e;
+      } else {  // meets the window or the end of the sequence
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = rowA + ((e >> 1) << 3);
+          if (on[e & 1] && i < Lc) {
+            if (in_window(i, Lc, a.n_init, a.n_recent)) {
+              // (the rescoring computes the codes' window logits exactly)
+              if constexpr (!Q8) {
+                const int wa = a.n_init < Lc ? a.n_init : Lc;
+                const int lo = Lc - a.n_recent > wa ? Lc - a.n_recent : wa;
+                const int wj = i < wa ? i : wa + (i - lo);
+                a.wz[(int64_t)(head0 + 2 * tq + (e & 1)) * a.wz_stride + wj] = zv[e];
+              }
+            } else if (zv[e] >= ethr[e & 1]) {
+              emit |= 1u << e;
+            }
           }
         }
       }
+      if (!__any_sync(0xffffffffu, emit)) continue;  // nothing to emit in this block
       // emission: per head, this warp's pairs of the tile (rows gr, then
       // gr+8, by lane) continue its current run; lane h extends the run by
       // bump allocation (one atomic per 8 slots) and broadcasts where they go
@@ -389,13 +473,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
   if (cur_unit >= 0) close_runs();
 }
 
+template <bool Q8>
 static cudaError_t launch_scan_t(const ScanArgs& a, int grid, cudaStream_t st, bool pdl) {
   const size_t smem = scan_smem_bytes();
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(scan_kernel,
+    cudaError_t e = cudaFuncSetAttribute(scan_kernel<Q8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
@@ -410,14 +495,15 @@ static cudaError_t launch_scan_t(const ScanArgs& a, int grid, cudaStream_t st, b
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, scan_kernel, a);
+  return cudaLaunchKernelEx(&cfg, scan_kernel<Q8>, a);
 }
 
-int scan_tile_rows() { return kTileRows; }
+int scan_tile_rows() { return Geom<false>::kTR; }
+int scan_grid_rows(bool q8) { return q8 ? Geom<true>::kTR : Geom<false>::kTR; }
 int scan_tile_warps() { return kScanWarps; }
 
 cudaError_t launch_scan(const ScanArgs& a, int grid, cudaStream_t st, bool pdl) {
-  return launch_scan_t(a, grid, st, pdl);
+  return a.codes ? launch_scan_t<true>(a, grid, st, pdl) : launch_scan_t<false>(a, grid, st, pdl);
 }
 
 }  // namespace tsa

@@ -203,6 +203,57 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D += A * B, m16n8k16, fp16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two offset-binary key codes (bytes 0-1, or 2-3, of w: u = c + 128) as an
+// fp16x2 word holding the integers c exactly: the byte becomes the low
+// mantissa bits of 1024 (0x6400 | u = 1024 + u) and 1152 is subtracted
+// (exact: every value involved is an integer below 2048).
+__device__ __forceinline__ uint32_t codes_lo_f16x2(uint32_t w) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(r) : "r"(w), "r"(0x64646464u));
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(r) : "r"(0x64806480u));
+  return r;
+}
+__device__ __forceinline__ uint32_t codes_hi_f16x2(uint32_t w) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(r) : "r"(w), "r"(0x64646464u));
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(r) : "r"(0x64806480u));
+  return r;
+}
+
+// B fragments of the query heads of group [head0, head0 + G) for the key
+// scan's bf16 contraction: lane (gr, tq) holds head gr's dims [8(4p+tq), +8)
+// for p < 4 (zero for gr >= G).
+__device__ __forceinline__ void load_q_frag(const uint16_t* q, int64_t head0, int G,
+                                            uint32_t (&qb)[4][4]) {
+  const int lane = threadIdx.x & 31, gr = lane >> 2, tq = lane & 3;
+  const uint16_t* qp = q + (head0 + (gr < G ? gr : 0)) * kD;
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (gr < G) w = *reinterpret_cast<const uint4*>(qp + 8 * (4 * p + tq));
+    qb[p][0] = w.x; qb[p][1] = w.y; qb[p][2] = w.z; qb[p][3] = w.w;
+  }
+}
+
+// The emission key of the exact logits that a quantised emission with key
+// k^ (order-preserving key; 0 admits everything) guarantees, for a logit
+// error bound eps: f2key(k^ + eps), the sum rounded up (NaN: nothing).
+__device__ __forceinline__ uint32_t q8_exact_key(uint32_t khat, float eps) {
+  if (khat == 0u) return 0u;
+  const float kz = __fadd_ru(key2f(khat), eps);
+  return kz == kz ? f2key(kz) : 0xffffffffu;
+}
+
 // Hint that the line holding p will be read soon (fetched into L2).
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
@@ -290,7 +341,7 @@ struct TraceScope {
   }
 };
 enum TraceKernel : uint32_t {  // 2, 3, 5 and 6 are retired ids
-  kTrScan = 1, kTrSelector = 4, kTrFinish = 7, kTrFinishPhases = 8
+  kTrScan = 1, kTrSelector = 4, kTrFinish = 7, kTrFinishPhases = 8, kTrQ8Rescore = 9
 };
 
 // ------------------------------------------------------ warp/block utils

@@ -45,9 +45,78 @@ struct ScanArgs {
   // runs out (bounded) and the call reports a timeout.
   long long wait_ns;
   int stall_first_copy;
+  // Quantised scan (codes != nullptr): pool logits are the approximations
+  // z^ = qts[bh] * sum_j qh[bh][j] c_ij from the offset-binary key codes
+  // (same row geometry as kv.k, one byte per element), emitted against the
+  // emission key in that domain; window rows are skipped (the finish
+  // computes their logits from the bf16 keys).
+  // The codes of each sequence's last q8_new rows are written by the
+  // preceding kernel: the producer waits for it before copying them.
+  const uint8_t* codes;
+  const uint16_t* qh;        // fp16 [B][Hq][128]
+  const float* qts;          // [B][Hq]
+  int q8_new;
   TraceBuf trace;
 };
 cudaError_t launch_scan(const ScanArgs& a, int grid, cudaStream_t st, bool pdl);
+int scan_grid_rows(bool q8);  // rows of one scan tile
+
+// Quantised decode, first kernel: codes the last n_new rows of every
+// sequence with the stored per-channel scales (raising err), then prepares
+// every query head of the group: qh = fp16(q_j s_j / t), qts = t * scale and
+// eps, a bound on |z - z^| for every row that holds for the tensor-core
+// arithmetic of both the scan and the exact rescoring.
+struct Q8PrepArgs {
+  const uint16_t* q;         // bf16 [B][Hq][128]
+  KvView kv;
+  uint8_t* codes;
+  const float* kscale;       // [B][Hkv][128]
+  float* kerr;               // [B][Hkv][128]
+  const int32_t* lens;
+  int64_t len_host, len_step;
+  int B, Hq, n_new;
+  float scale;
+  uint16_t* qh;              // fp16 [B][Hq][128]
+  float* qts;                // [B][Hq]
+  float* eps;                // [B][Hq]
+};
+cudaError_t launch_q8_prep(const Q8PrepArgs& a, cudaStream_t st, bool pdl);
+
+// Quantised decode, between the scan and the finish: every emitted pair is
+// rescored on the bf16 keys (the key scan's tensor-core arithmetic, so each
+// logit is bit-identical to the plain scan's) and kept, with its exact logit,
+// iff z >= k^ + eps; the others become sentinels.  A pool position that was
+// not emitted has z <= z^ + eps < k^ + eps, so the kept pairs are exactly the
+// pool positions with z >= k^ + eps (a plain emission with that key).  The
+// window logits, which the quantised scan skips, are computed here too.  The
+// work -- 32 pairs or window rows of one head -- is spread over the whole
+// grid, so a head with a long list does not hold up the others.
+struct Q8RescoreArgs {
+  const uint16_t* q;         // bf16 [B][Hq][128]
+  KvView kv;
+  const int32_t* lens;
+  int64_t len_host, len_step;
+  int B, Hq;
+  float scale;
+  int n_init, n_recent;
+  uint2* dense;              // [B][Hq][dense_stride]
+  const int32_t* dense_n;    // [B][Hq] x kCtrStride
+  int64_t dense_stride;
+  const uint32_t* emit_key;  // [B][Hq] the scan's keys k^
+  const float* eps;          // [B][Hq]
+  float* wz;                 // [B][Hq][wz_stride]
+  int wz_stride;
+  TraceBuf trace;
+};
+constexpr int kQ8MaxHeads = 8192;  // B * Hq of one quantised call
+cudaError_t launch_q8_rescore(const Q8RescoreArgs& a, int grid, cudaStream_t st);
+// Key coding outside a decode step: fit (scales from the absolute maxima of
+// rows [0, L_b), codes and errors of those rows) or append (codes of the last
+// n_tail rows with the stored scales, errors raised).  kscale and kerr must
+// be zero before a fit.
+cudaError_t launch_q8_quantize(const KvView& kv, const int32_t* lens, int B, int64_t n_tail,
+                               bool fit, uint8_t* codes, float* kscale, float* kerr,
+                               cudaStream_t st);
 
 struct RetopkSeq;  // one sequence of a ReTopK step (below)
 
@@ -96,6 +165,11 @@ struct FinishArgs {
   const float* push_qbar;    // [B][Hq][128]
   const RetopkSeq* seqs;     // [B] (device, written by the selector)
   int C;
+  // Quantised scan (decode only): the pairs were rescored (q8 rescore
+  // kernel) and are the pool positions with z >= k^ + q8_eps[bh], k^ the
+  // emission key the scan used; the next call's key is stored in the codes'
+  // domain (minus eps).  nullptr: a plain scan.
+  const float* q8_eps;
   TraceBuf trace;
 };
 cudaError_t launch_finish(const FinishArgs& a, cudaStream_t st);
