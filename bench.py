@@ -11,8 +11,10 @@ heads, K = 2048, window 128 + 512); --workload picks another one.
 
 The default run (llama128k at N = 1) also times, in the same process and
 reported under "secondary", the 1M-token decode step (the metric's second
-context) and the 64K ReTopK reuse stream (CUDA-graph timed over its 512
-steps); --no-secondary skips them.  cpu_baseline is the fp64 oracle on one
+context), the same two decode workloads through the int8 key codes with exact
+rescoring (sparse_attn_decode_q8; each step codes its newest key) and the 64K
+ReTopK reuse stream (CUDA-graph timed over its 512 steps); --no-secondary
+skips them.  --q8 times the quantised path alone.  cpu_baseline is the fp64 oracle on one
 host core, cpu_baseline_parallel the same code with one thread per query head.
 
 --impl reference times the fp64 CPU oracle (the test oracle, as it stands) on
@@ -170,12 +172,12 @@ def scan_sources_sha256() -> str:
     return h.hexdigest()
 
 
-def scan_traffic(wl, rows_per_launch: int):
-    """DRAM bytes (read + write) of one scan launch from the tracked ncu
-    record profiles/scan_llama128k.json, or None when the scan sources changed
-    since it was captured.  Its per-row traffic is scaled to this launch's key
-    rows."""
-    path = os.path.join(ROOT, "profiles", "scan_llama128k.json")
+def scan_traffic(wl, rows_per_launch: int, record: str = "scan_llama128k.json"):
+    """DRAM bytes (read + write) of one scan launch from a tracked ncu record
+    (profiles/scan_llama128k.json, or scan_q8_llama128k.json for the
+    quantised scan), or None when the scan sources changed since it was
+    captured.  Its per-row traffic is scaled to this launch's key rows."""
+    path = os.path.join(ROOT, "profiles", record)
     if not os.path.exists(path):
         return None, "no ncu record"
     with open(path) as f:
@@ -208,17 +210,28 @@ def run_ours(args, ws, rank, local):
         wl.v = wl.v.cpu() if args.cpu_baseline else None
         torch.cuda.empty_cache()
     B, Hq, d, K = wl.B, wl.Hq, wl.d, wl.K
-    nb = tsa.decode_workspace_size(B, Hq, wl.Hkv, d, kv.l_cap, K, wl.n_init, wl.n_recent)
+    q8 = getattr(args, "q8", False)
+    size_fn = tsa.decode_q8_workspace_size if q8 else tsa.decode_workspace_size
+    nb = size_fn(B, Hq, wl.Hkv, d, kv.l_cap, K, wl.n_init, wl.n_recent)
     work = torch.zeros(nb, dtype=torch.uint8, device=dev)  # zeroed once, then reused
     out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
     lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
     lens_all = torch.tensor([wl.lens(t) for t in range(wl.steps)], dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
+    codes = None
+    if q8:  # scales fitted on the prefill rows; each step codes its newest key
+        codes = tsa.KeyCodes(kv, B=B)
+        tsa.quantize_keys(kv, codes, lens_all[0] - 1, fit=True, stream=stream)
 
     def step(i):
         t = i % wl.steps
-        tsa.sparse_attn_decode(wl.q_all[t], kv, lens_all[t], K, wl.n_init, wl.n_recent,
-                               wl.scale, out=out, lse_out=lse, workspace=work, stream=stream)
+        if q8:
+            tsa.sparse_attn_decode_q8(wl.q_all[t], kv, codes, lens_all[t], K, wl.n_init,
+                                      wl.n_recent, n_new=1, scale=wl.scale, out=out,
+                                      lse_out=lse, workspace=work, stream=stream)
+        else:
+            tsa.sparse_attn_decode(wl.q_all[t], kv, lens_all[t], K, wl.n_init, wl.n_recent,
+                                   wl.scale, out=out, lse_out=lse, workspace=work, stream=stream)
 
     clocks = Clocks(torch.cuda.current_device() if ws == 1 else local)
     if not args.device_only:
@@ -265,6 +278,8 @@ def run_ours(args, ws, rank, local):
     us_per_layer_step = 1000.0 * ms_per_step / ws  # aggregate over all replicas
 
     ab = algorithmic_bytes(wl)
+    if q8:  # the quantised scan reads one byte per key element
+        ab["scan"] //= 2
     hbm, peak_kind = peaks()
     scan_avg = statistics.mean(scan_ms)
     achieved = ab["scan"] / (scan_avg * 1e-3) / 1e9
@@ -280,9 +295,11 @@ def run_ours(args, ws, rank, local):
                               "topk+attend+merge": round(statistics.mean(sel_ms)
                                                          + statistics.mean(att_ms), 5)},
                 "scan_gbs": round(achieved, 1), "trace": trace_summary} if rank == 0 else None
-    traffic, traffic_note = scan_traffic(wl, ab["scan"] // (wl.d * 2))
+    traffic, traffic_note = scan_traffic(
+        wl, ab["scan"] // (wl.d * (1 if q8 else 2)),
+        "scan_q8_llama128k.json" if q8 else "scan_llama128k.json")
     # ---- end to end through the public API with host buffers ----
-    e2e = run_e2e(args, wl, kv, work, tsa, torch, dev, ws)
+    e2e = run_e2e(args, wl, kv, work, tsa, torch, dev, ws, codes=codes)
 
     res = {
         "metric": METRIC, "value": round(us_per_layer_step, 3), "unit": UNIT,
@@ -296,12 +313,15 @@ def run_ours(args, ws, rank, local):
             "decode_steps_cycled": wl.steps,
             "l2": f"inputs larger than L2 (K cache {ab['scan'] / 2**20:.0f} MiB > 126 MiB); no flush",
             "parallelism": f"replicas{ws}" if ws > 1 else "single",
+            "keys": ("int8 codes (scan) + bf16 rows (exact rescoring); scales fitted on the "
+                     "prefill rows, each step codes its newest key") if q8 else "bf16",
         },
         "stages_ms": {"scan": round(scan_avg, 5),
                       "topk+attend+merge": round(statistics.mean(sel_ms) + statistics.mean(att_ms), 5),
                       "note": "second timed region with per-stage events"},
         "path_algorithmic_gbs": round(path_gbs, 1),
-        "roofline": {"kernel": "scan_kernel (GQA key scan, histograms, pair emission)",
+        "roofline": {"kernel": ("scan_kernel<q8> (query preparation + code scan, pair emission)"
+                                if q8 else "scan_kernel (GQA key scan, pair emission)"),
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "frac_of_8tbs": round(achieved / 8000.0, 4),
@@ -622,7 +642,7 @@ def _cudart():
     return rt
 
 
-def run_e2e(args, wl, kv, work, tsa, torch, dev, ws=1):
+def run_e2e(args, wl, kv, work, tsa, torch, dev, ws=1, codes=None):
     """End to end through the C ABI with host buffers.  Per step, on one
     stream: a host -> device copy of the step's query and lengths (pinned,
     one copy), the append of the step's K and V token rows from pinned host
@@ -667,11 +687,14 @@ def run_e2e(args, wl, kv, work, tsa, torch, dev, ws=1):
     stream = torch.cuda.current_stream()
     sp = C.c_void_p(stream.cuda_stream)
     lib = tsa.lib()
-    # the C ABI call's arguments, fixed for the run
+    # the C ABI call's arguments, fixed for the run (the quantised call codes
+    # the appended key itself: n_new = 1)
     call = (C.c_void_p(stage.data_ptr()), C.byref(kv.struct), C.c_void_p(stage.data_ptr() + qb),
             B, Hq, Hkv, d, wl.K, wl.n_init, wl.n_recent, C.c_float(wl.scale),
             C.c_void_p(res.data_ptr()), C.c_void_p(res.data_ptr() + B * Hq * d * 4), None, None,
             C.c_void_p(work.data_ptr()), C.c_size_t(work.numel()), sp)
+    if codes is not None:
+        call = call[:2] + (C.byref(codes.struct), 1) + call[2:]
     hk, hv, hq = host_k.data_ptr(), host_v.data_ptr(), host_ql.data_ptr()
     tokb = Hkv * rowb
 
@@ -682,7 +705,7 @@ def run_e2e(args, wl, kv, work, tsa, torch, dev, ws=1):
             src = (t * B + b) * tokb
             err |= rt.cudaMemcpy2DAsync(kd, pitch, hk + src, rowb, rowb, Hkv, H2D, sp)
             err |= rt.cudaMemcpy2DAsync(vd, pitch, hv + src, rowb, rowb, Hkv, H2D, sp)
-        rc = lib.sparse_attn_decode(*call)
+        rc = lib.sparse_attn_decode(*call) if codes is None else lib.sparse_attn_decode_q8(*call)
         if rc:
             raise tsa.TsaError(rc, lib.tsa_last_error().decode())
         err |= rt.cudaMemcpyAsync(res_host.data_ptr(), res.data_ptr(), res.numel() * 4, D2H, sp)
@@ -967,17 +990,21 @@ def run_secondary(args, ws, rank, local):
     reuse stream at 64K (CUDA-graph timed over its 512 steps)."""
     import torch
     out = {}
-    for name, over in (("llama1m", dict(steps=20, warmup=max(16, args.warmup))),
-                       ("retopk64k", dict(steps=512, warmup=args.warmup))):
+    for leg, name, over in (
+            ("llama1m", "llama1m", dict(steps=20, warmup=max(16, args.warmup))),
+            ("llama128k_q8", "llama128k", dict(q8=True)),
+            ("llama1m_q8", "llama1m", dict(steps=20, warmup=max(16, args.warmup), q8=True)),
+            ("retopk64k", "retopk64k", dict(steps=512, warmup=args.warmup))):
         torch.cuda.empty_cache()
         sub = argparse.Namespace(**{**vars(args), "workload": name, "cpu_baseline": False,
-                                    "trace": False, "device_only": False, **over})
+                                    "trace": False, "device_only": False, "q8": False,
+                                    **over})
         r = run_retopk(sub, ws, rank, local) if name.startswith("retopk") else \
             run_ours(sub, ws, rank, local)
         keep = ("value", "unit", "ms_per_step", "steps", "warmup", "config", "stages_ms",
                 "path_algorithmic_gbs", "roofline", "e2e", "gpu_launches", "clocks",
                 "host_launched_us_per_step", "timing", "paths")
-        out[name] = {k: r[k] for k in keep if k in r}
+        out[leg] = {k: r[k] for k in keep if k in r}
     return out
 
 
@@ -996,6 +1023,8 @@ def main():
                     help="also record a per-CTA kernel timeline of 3 extra steps")
     ap.add_argument("--device-only", action="store_true",
                     help="profiling mode: time only the device path (no e2e, no baseline)")
+    ap.add_argument("--q8", action="store_true",
+                    help="decode through the int8 key codes with exact rescoring")
     ap.add_argument("--no-secondary", dest="secondary", action="store_false",
                     help="skip the 1M decode and 64K ReTopK legs of the default run")
     args = ap.parse_args()
@@ -1011,7 +1040,7 @@ def main():
     else:
         res = run_ours(args, ws, rank, local)
         if (args.secondary and ws == 1 and args.workload == "llama128k" and not args.device_only
-                and res is not None):
+                and not args.q8 and res is not None):
             res["secondary"] = run_secondary(args, ws, rank, local)
     if rank == 0 and res is not None:
         print(json.dumps(res))
