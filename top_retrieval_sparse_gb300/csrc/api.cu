@@ -726,6 +726,7 @@ struct tsa_retopk {
   int32_t* sup_n;    // [Hq][C]
   int64_t t;
   int fifo_head;
+  int fresh;         // FIFO entry written by this handle's latest step (-1: none since init)
   bool initialised;
 };
 
@@ -837,6 +838,7 @@ int retopk_create(tsa_retopk** st, int Hq, int Hkv, int d, int K, int C, int R, 
   s->sup_n = reinterpret_cast<int32_t*>(m + up((size_t)Hq * C * kD * 4) + up((size_t)Hq * C * K * 4));
   s->t = 0;
   s->fifo_head = 0;
+  s->fresh = -1;
   s->initialised = false;
   *st = s;
   return ok();
@@ -862,6 +864,7 @@ int retopk_init(tsa_retopk* st, const void* prefill_q, const int32_t* prefill_su
   if (e != cudaSuccess) return cuda_fail(e, "retopk init launch");
   st->t = 0;
   st->fifo_head = 0;
+  st->fresh = -1;  // the init kernel completes before the next step's selector starts
   st->initialised = true;
   return ok();
 }
@@ -961,6 +964,7 @@ int retopk_step_batched(tsa_retopk* const* sts, int n, const void* q, const tsa_
       a.seq[b].L = lens[b];
       a.seq[b].fifo_head = sb->fifo_head;
       a.seq[b].refresh = (sb->t % sb->T_r) == 0;
+      a.seq[b].fresh = sb->fresh;
     }
     a.Hq = Hq;
     a.C = s0->C;
@@ -1025,6 +1029,7 @@ int retopk_step_batched(tsa_retopk* const* sts, int n, const void* q, const tsa_
   for (int b = 0; b < n; ++b) {
     tsa_retopk* sb = sts[b];
     sb->t += 1;
+    sb->fresh = sb->fifo_head;  // overwritten by this step's finish kernel
     sb->fifo_head = (sb->fifo_head + 1) % sb->C;
   }
   return ok();

@@ -23,15 +23,19 @@ constexpr int kMaxC = 64;
 // over the bitmap are latency chains split over the CTA's threads.
 constexpr int kSelectorThreads = 1024;
 
+// Supports entries per thread prefetched before the dependency wait (R*K
+// beyond kPre * 1024 entries are loaded after it).
+constexpr int kPre = 8;
+
 __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(RetopkSelArgs a) {
   TraceScope trace(a.trace, kTrSelector);  // start, waited, union built, exit
   extern __shared__ __align__(16) uint32_t sbits[];
   __shared__ __align__(16) float qs[kD];
   __shared__ float rho[kMaxC];
   __shared__ float red[kSelectorThreads / 32];
-  __shared__ int chosen[kMaxC];
-  __shared__ int chosen_n[kMaxC];  // support sizes of the recalled entries
-  __shared__ int s_path;
+  __shared__ int stab[kMaxC];    // the stable entries' top-R, by rank
+  __shared__ int stab_n[kMaxC];  // their support sizes
+  __shared__ int s_path, s_fresh_in;
   __shared__ uint32_t wtot[kSelectorThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int bh = blockIdx.x;  // (sequence, query head) of the batch
@@ -41,6 +45,12 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
   const float* cache_qbar = sq.qbar;
   const int32_t* cache_sup = sq.sup;
   const int32_t* cache_sup_n = sq.sup_n;
+  // The FIFO entry the previous step of this sequence wrote (-1: none) may
+  // belong to a kernel still running: it is read after the dependency wait.
+  // Every other entry was written by a kernel that has completed (the
+  // previous kernel of the stream waited for it), so its query, support size
+  // and support are read -- and the stable entries' top R chosen -- first.
+  const int fresh = sq.fresh;
 
   // 1. normalise the query
   float x = 0.f;
@@ -68,33 +78,21 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
   uint32_t* bitmap = gbm ? a.gbitmap + (int64_t)bh * a.gbitmap_stride : sbits;
   uint32_t* l2 = gbm ? sbits : sbits + nwords;
   for (int w = tid; w < (gbm ? nl2 : nwords + nl2); w += kSelectorThreads) sbits[w] = 0u;
-  // the cache and this step's buffers belong to the previous step's kernels
-  // until they have completed; the key scan may be scheduled from here on
-  pdl_wait();
-  pdl_trigger();
-  trace.mark(1);
-  if (h == 0 && tid == 0) {  // this step's length and FIFO entry, for the next kernels
-    a.lens_ws[b] = (int32_t)L;
-    a.seq_ws[b] = sq;
-  }
-  if (tid < kD) {
-    const float qb = nrm > 0.f ? qs[tid] / nrm : 0.f;
-    qs[tid] = qb;
-    a.qbar_new[(int64_t)bh * kD + tid] = qb;
-  }
+  if (tid < kD) qs[tid] = nrm > 0.f ? qs[tid] / nrm : 0.f;
   __syncthreads();
 
   // 2. cosine against the cached queries (warp w: entries w and w + 32; all of
-  //    a warp's loads are issued before any is used)
-  {
-    constexpr int kPer = kMaxC / (kSelectorThreads / 32);  // entries per warp, at most
+  //    a warp's loads are issued before any is used) -- the stable ones now
+  constexpr int kPer = kMaxC / (kSelectorThreads / 32);  // entries per warp, at most
+  auto cosine = [&](bool fresh_pass) {
     float4 qv[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
       const int c = wid + k * (kSelectorThreads / 32);
-      qv[k] = c < a.C ? *reinterpret_cast<const float4*>(cache_qbar +
-                                                         ((int64_t)h * a.C + c) * kD + lane * 4)
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      const bool mine = c < a.C && ((c == fresh) == fresh_pass);
+      qv[k] = mine ? *reinterpret_cast<const float4*>(cache_qbar + ((int64_t)h * a.C + c) * kD +
+                                                      lane * 4)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     const float4 mq = *reinterpret_cast<const float4*>(qs + lane * 4);
 #pragma unroll
@@ -105,36 +103,78 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
       acc = fmaf(mq.z, qv[k].z, acc);
       acc = fmaf(mq.w, qv[k].w, acc);
       acc = warp_sum(acc);
-      if (lane == 0 && c < a.C) rho[c] = acc;
+      if (lane == 0 && c < a.C && ((c == fresh) == fresh_pass)) rho[c] = acc;
+    }
+  };
+  cosine(false);
+  __syncthreads();
+  // the stable entries' top R: a stable entry is taken iff fewer than R stable
+  // entries beat it (larger rho, or equal rho and older)
+  const int nst = fresh >= 0 ? a.C - 1 : a.C;  // stable entries
+  const int Rs = a.R < nst ? a.R : nst;
+  if (tid < a.C && tid != fresh) {
+    const float rc = rho[tid];
+    const int agec = (tid - sq.fifo_head + a.C) % a.C;  // 0 = oldest
+    int beat = 0;
+    for (int c = 0; c < a.C; ++c) {
+      if (c == fresh) continue;
+      const float r = rho[c];
+      const int age = (c - sq.fifo_head + a.C) % a.C;
+      beat += (r > rc || (r == rc && age < agec)) ? 1 : 0;
+    }
+    if (beat < Rs) {  // ranks are distinct: one entry per rank
+      stab[beat] = tid;
+      stab_n[beat] = cache_sup_n[(int64_t)h * a.C + tid];
     }
   }
   __syncthreads();
+  // their supports as one flat index space of Rs*K entries (entries past a
+  // support's size are -1), in registers
+  int32_t pre[kPre];
+#pragma unroll
+  for (int u = 0; u < kPre; ++u) {
+    const int j = tid + u * kSelectorThreads;
+    pre[u] = -1;
+    if (j < Rs * a.K) {
+      const int r = j / a.K, i = j - r * a.K;
+      if (i < stab_n[r]) pre[u] = cache_sup[((int64_t)h * a.C + stab[r]) * a.K + i];
+    }
+  }
 
-  // 3. fallback / refresh decision and top-R recall: entry c is recalled iff
-  //    fewer than R entries beat it (larger rho, or equal rho and older)
+  // the cache and this step's buffers belong to the previous step's kernels
+  // until they have completed; the key scan may be scheduled from here on
+  pdl_wait();
+  pdl_trigger();
+  trace.mark(1);
+  if (h == 0 && tid == 0) {  // this step's length and FIFO entry, for the next kernels
+    a.lens_ws[b] = (int32_t)L;
+    a.seq_ws[b] = sq;
+  }
+  if (tid < kD) a.qbar_new[(int64_t)bh * kD + tid] = qs[tid];
+  if (fresh >= 0) cosine(true);
+  __syncthreads();
+
+  // 3. fallback / refresh decision; the final top R: the fresh entry is in
+  //    iff fewer than R entries beat it, and then it displaces the stable R-th
   if (wid == 0) {
     float mx = -INFINITY;
-    for (int c = lane; c < a.C; c += 32) mx = fmaxf(mx, rho[c]);
+    int nb = 0;  // stable entries that beat the fresh one
+    const float rf = fresh >= 0 ? rho[fresh] : 0.f;
+    const int agef = fresh >= 0 ? (fresh - sq.fifo_head + a.C) % a.C : 0;
+    for (int c = lane; c < a.C; c += 32) {
+      mx = fmaxf(mx, rho[c]);
+      const int age = (c - sq.fifo_head + a.C) % a.C;
+      if (fresh >= 0 && c != fresh && (rho[c] > rf || (rho[c] == rf && age < agef))) ++nb;
+    }
     mx = warp_max(mx);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) nb += __shfl_xor_sync(0xffffffffu, nb, o);
     const int path = (mx < a.tau || sq.refresh) ? 1 : 0;
     if (lane == 0) {
       s_path = path;
       a.path[bh] = path;
       if (a.path_out) a.path_out[bh] = path;
-    }
-  }
-  if (tid < a.C) {
-    const float rc = rho[tid];
-    const int agec = (tid - sq.fifo_head + a.C) % a.C;  // 0 = oldest
-    int beat = 0;
-    for (int c = 0; c < a.C; ++c) {
-      const float r = rho[c];
-      const int age = (c - sq.fifo_head + a.C) % a.C;
-      beat += (r > rc || (r == rc && age < agec)) ? 1 : 0;
-    }
-    if (beat < a.R) {  // ranks are distinct: one entry per rank
-      chosen[beat] = tid;
-      chosen_n[beat] = cache_sup_n[(int64_t)h * a.C + tid];
+      s_fresh_in = fresh >= 0 && nb < a.R ? 1 : 0;
     }
   }
   __syncthreads();
@@ -151,48 +191,48 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
   }
 
   // 4. bitmap union of the recalled supports and the recent window
-  // the R recalled supports as one flat index space of R*K entries (entries
-  // past a support's size are skipped), four loads in flight per thread
-  {
-    constexpr int kU = 4;
-    const int total = a.R * a.K;  // <= C*K entries of the cache
-    for (int j0 = tid; j0 < total; j0 += kU * kSelectorThreads) {
-      int32_t pv[kU];
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int j = j0 + u * kSelectorThreads;
-        pv[u] = -1;
-        if (j < total) {
-          const int r = j / a.K, i = j - r * a.K;
-          if (i < chosen_n[r]) pv[u] = cache_sup[((int64_t)h * a.C + chosen[r]) * a.K + i];
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kU; ++u)
-        if (pv[u] >= 0 && pv[u] < L) {
-          atomicOr(&bitmap[pv[u] >> 5], 1u << (pv[u] & 31));
-          atomicOr(&l2[pv[u] >> 10], 1u << ((pv[u] >> 5) & 31));
-        }
+  const int fin = s_fresh_in;
+  const int keep = fin && Rs == a.R ? Rs - 1 : Rs;  // stable supports kept
+  auto mark = [&](int32_t p) {
+    if (p >= 0 && p < L) {
+      atomicOr(&bitmap[p >> 5], 1u << (p & 31));
+      atomicOr(&l2[p >> 10], 1u << ((p >> 5) & 31));
     }
+  };
+#pragma unroll
+  for (int u = 0; u < kPre; ++u) {
+    const int j = tid + u * kSelectorThreads;
+    if (j < keep * a.K) mark(pre[u]);
+  }
+  for (int j = kPre * kSelectorThreads + tid; j < keep * a.K; j += kSelectorThreads) {
+    const int r = j / a.K, i = j - r * a.K;  // past the prefetched entries
+    if (i < stab_n[r]) mark(cache_sup[((int64_t)h * a.C + stab[r]) * a.K + i]);
+  }
+  if (fin) {
+    const int nf = cache_sup_n[(int64_t)h * a.C + fresh];
+    for (int i = tid; i < nf && i < a.K; i += kSelectorThreads)
+      mark(cache_sup[((int64_t)h * a.C + fresh) * a.K + i]);
   }
   const int64_t lo = L - a.W > 0 ? L - a.W : 0;
-  for (int64_t p = lo + tid; p < L; p += kSelectorThreads)
-  {
-    atomicOr(&bitmap[p >> 5], 1u << (p & 31));
-    atomicOr(&l2[p >> 10], 1u << ((p >> 5) & 31));
-  }
+  for (int64_t p = lo + tid; p < L; p += kSelectorThreads) mark((int32_t)p);
   __syncthreads();
   trace.mark(2);
 
-  // 5. ascending compaction over the non-empty words only: thread t owns a
-  // contiguous range of second-level words, counts the bits of the words
-  // they mark, and after one block scan writes its positions in order.
-  const int per = (nl2 + kSelectorThreads - 1) / kSelectorThreads;
+  // 5. ascending compaction: each thread owns a contiguous range of bitmap
+  // words (of second-level words when the bitmap is in the workspace: only
+  // the words they mark are read, and cleared), counts their bits, and after
+  // one block scan writes its positions in order.
+  const int nunits = gbm ? nl2 : nwords;
+  const int per = (nunits + kSelectorThreads - 1) / kSelectorThreads;
   const int q0 = tid * per;
-  const int q1 = q0 + per < nl2 ? q0 + per : nl2;
+  const int q1 = q0 + per < nunits ? q0 + per : nunits;
   uint32_t cnt = 0;
-  for (int q = q0; q < q1; ++q)
-    for (uint32_t m = l2[q]; m; m &= m - 1) cnt += __popc(bitmap[(q << 5) + __ffs(m) - 1]);
+  if (gbm) {
+    for (int q = q0; q < q1; ++q)
+      for (uint32_t m = l2[q]; m; m &= m - 1) cnt += __popc(bitmap[(q << 5) + __ffs(m) - 1]);
+  } else {
+    for (int q = q0; q < q1; ++q) cnt += __popc(bitmap[q]);
+  }
   uint32_t incl = cnt;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -217,16 +257,19 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
   }
   __syncthreads();
   uint32_t pos = incl - cnt + wtot[wid];
-  for (int q = q0; q < q1; ++q) {
-    for (uint32_t m = l2[q]; m; m &= m - 1) {
-      const int w = (q << 5) + __ffs(m) - 1;
-      const uint32_t word = bitmap[w];
-      if (gbm) bitmap[w] = 0u;  // the workspace bitmap is all zero again after the step
-      for (uint32_t bits = word; bits; bits &= bits - 1) {
-        if (pos < (uint32_t)a.cand_cap) crow[pos] = ((uint32_t)w << 5) + __ffs(bits) - 1;
-        ++pos;
-      }
+  auto emit_word = [&](int w) {
+    const uint32_t word = bitmap[w];
+    if (gbm) bitmap[w] = 0u;  // the workspace bitmap is all zero again after the step
+    for (uint32_t bits = word; bits; bits &= bits - 1) {
+      if (pos < (uint32_t)a.cand_cap) crow[pos] = ((uint32_t)w << 5) + __ffs(bits) - 1;
+      ++pos;
     }
+  };
+  if (gbm) {
+    for (int q = q0; q < q1; ++q)
+      for (uint32_t m = l2[q]; m; m &= m - 1) emit_word((q << 5) + __ffs(m) - 1);
+  } else {
+    for (int q = q0; q < q1; ++q) emit_word(q);
   }
   if (a.cand_out) {
     __syncthreads();

@@ -188,6 +188,7 @@ struct RetopkSeq {
   int64_t L;                 // cache length this step
   int32_t fifo_head;         // slot of the oldest entry (overwritten by this step)
   int32_t refresh;           // t % T_r == 0
+  int32_t fresh;             // slot the sequence's previous step wrote (-1: none)
 };
 constexpr int kMaxRetopkBatch = 64;  // sequences of one step (kernel-parameter table)
 
