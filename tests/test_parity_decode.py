@@ -230,3 +230,90 @@ def test_full_yi_paged_sampled():
     out, lse, idx, sc = gpu_decode(wl, 31)
     for b, h in [(0, 0), (3, 17), (7, 31), (12, 5), (15, 30)]:
         check_head(wl, 31, b, h, out[b, h], lse[b, h], idx[b, h])
+
+
+# ---------------------------------------------- calls on one workspace
+def stream_and_check(wl, steps, check_steps, heads=None):
+    """Decode steps on one workspace, the launch configuration the bench
+    times: from the second call on, the selection starts from the scan's fine
+    histogram of the emitted pairs (b* without a pass over the pair list).
+    The checked steps are compared with the oracle, and the device status
+    word must stay clean (the histogram's counts agree with the pair lists)."""
+    import top_retrieval_sparse_gb300 as tsa
+    dev = "cuda"
+    paged = wl.page_table is not None
+    kv = (tsa.kv_paged(wl.k_pages.to(dev), wl.v_pages.to(dev), wl.page_table.to(dev)) if paged
+          else tsa.kv_contiguous(wl.k.to(dev), wl.v.to(dev)))
+    n = tsa.decode_workspace_size(wl.B, wl.Hq, wl.Hkv, 128, kv.l_cap, wl.K, wl.n_init,
+                                  wl.n_recent)
+    ws = torch.zeros((n,), dtype=torch.uint8, device=dev)
+    stats = []
+    for t in steps:
+        q = wl.q(t).to(dev).contiguous()
+        lens = torch.tensor(wl.lens(t), dtype=torch.int32, device=dev)
+        lse = torch.empty((wl.B, wl.Hq), device=dev)
+        idx = torch.empty((wl.B, wl.Hq, max(wl.K, 1)), dtype=torch.int32, device=dev)
+        sc = torch.empty((wl.B, wl.Hq, max(wl.K, 1)), dtype=torch.float32, device=dev)
+        out, _, _, _ = tsa.sparse_attn_decode(q, kv, lens, wl.K, wl.n_init, wl.n_recent,
+                                              wl.scale, lse_out=lse, topk_idx=idx,
+                                              topk_score=sc, workspace=ws)
+        torch.cuda.synchronize()
+        if t not in check_steps:
+            continue
+        o, l, i, s = out.cpu().numpy(), lse.cpu().numpy(), idx.cpu().numpy(), sc.cpu().numpy()
+        for b in range(wl.B):
+            for h in (range(wl.Hq) if heads is None else heads):
+                stats.append(check_head(wl, t, b, h, o[b, h], l[b, h], i[b, h, :wl.K],
+                                        s[b, h, :wl.K]))
+    rc = tsa.workspace_status(ws)
+    assert rc == 0, f"device status: {rc}"
+    return stats
+
+
+def test_stream_fine_bins_downsized():
+    wl = make_decode("llama128k", L0=30_011, steps=10)  # K=2048, window 128+512
+    stream_and_check(wl, range(10), set(range(10)))
+
+
+def test_stream_fine_bins_group_sizes_and_small_K():
+    for Hq, Hkv, K in ((28, 4, 64), (12, 4, 1), (8, 8, 300)):
+        wl = make_decode("llama128k", L0=9000 + Hq, steps=6, B=1, K=K, Hq=Hq, Hkv=Hkv,
+                         n_init=16, n_recent=40)
+        stream_and_check(wl, range(6), {1, 3, 5})
+
+
+def test_stream_fine_bins_ties_at_threshold():
+    """Logits tie exactly around the K-th in every call: the threshold bin's
+    pairs share all 16 key bits and the radix decides by position."""
+    wl = make_decode("tiny", L0=20_000, steps=6, K=500)
+    kf = wl.k.float()
+    wl.k[:] = (torch.round(kf * 2) / 2).to(torch.bfloat16)
+    wl.q_all[:] = (torch.round(wl.q_all.float())).to(torch.bfloat16)
+    stream_and_check(wl, range(6), set(range(6)))
+
+
+def test_stream_fine_bins_all_equal_keys():
+    wl = make_decode("tiny", L0=3000, steps=4, K=100)
+    wl.k[:] = wl.k[:, :, :1, :]
+    stream_and_check(wl, range(4), set(range(4)))
+
+
+def test_stream_fine_bins_paged_batch():
+    wl = make_decode("yi_paged", L0=6000, steps=5, B=5, K=300)
+    stream_and_check(wl, range(5), {2, 4}, heads=range(0, 32, 5))
+
+
+def test_stream_fine_bins_every_position_selected():
+    """K >= |P| on a warm workspace: every emitted pair is selected."""
+    wl = make_decode("tiny", L0=4500, steps=4, K=50000)
+    stream_and_check(wl, range(4), set(range(4)))
+
+
+@pytest.mark.slow
+def test_full_llama128k_stream_all_heads():
+    """The bench's configuration: 128K keys, K = 2048, calls on one workspace;
+    the last of six steps is checked on every head."""
+    wl = make_decode("llama128k", steps=64)
+    st = stream_and_check(wl, range(58, 64), {63})
+    print("llama128k stream: tie-adopted heads", sum(s["verdict"] == 2 for s in st),
+          "max err", max(s["err"] for s in st))

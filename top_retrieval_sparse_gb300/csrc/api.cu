@@ -96,13 +96,14 @@ struct SelWs {
   uint64_t* spill;
   float* wz;
   int wz_stride;
+  uint32_t* hist16;      // decode layouts only (nullptr elsewhere): zero before a call
 };
 
 // Workspace of one decode call (offsets from the base).  [zero_begin,
 // zero_end) holds the counters that start every call at zero; the hint
 // bins after them persist.
 struct DecodeLayout {
-  size_t zero_begin, status, tile_ctr, dense_n, zero_end;
+  size_t zero_begin, status, tile_ctr, dense_n, hist16, zero_end;
   size_t emit_key, emit_margin, wz, dense, spill, total;
   int64_t dense_stride;
   int wz_stride;
@@ -121,6 +122,7 @@ DecodeLayout decode_layout(int B, int Hq, int Hkv, int64_t l_cap, int n_init, in
   L.status = o; o = up(o + 4);
   L.tile_ctr = o; o = up(o + 4);
   L.dense_n = o; o = up(o + rows * kCtrStride * 4);
+  L.hist16 = o; o = up(o + rows * kH16Bins * 4);
   L.zero_end = o;
   L.emit_key = o; o = up(o + rows * 4);
   L.emit_margin = o; o = up(o + rows * 4);
@@ -155,6 +157,7 @@ ScanArgs scan_args(const uint16_t* q, const KvView& view, const int32_t* lens, i
   s.wz = w.wz;
   s.wz_stride = w.wz_stride;
   s.status = w.status;
+  s.hist16 = w.hist16;
   s.trace = g_trace;
   s.wait_ns = g_stall_ns;
   s.stall_first_copy = g_stall_ns > 0;
@@ -181,6 +184,7 @@ FinishArgs finish_args(const uint16_t* q, const KvView& view, int Hq, float scal
   f.spill = w.spill;
   f.wz = w.wz;
   f.wz_stride = w.wz_stride;
+  f.hist16 = w.hist16;
   f.trace = g_trace;
   return f;
 }
@@ -358,6 +362,8 @@ int decode_run(const void* q, const KvView& view, const int32_t* lens, int64_t l
   w.spill = reinterpret_cast<uint64_t*>(ws + Lw.spill);
   w.wz = reinterpret_cast<float*>(ws + Lw.wz);
   w.wz_stride = Lw.wz_stride;
+  if (!q8)  // the plain scan's fine histogram of the emitted pairs
+    w.hist16 = reinterpret_cast<uint32_t*>(ws + Lw.hist16);
 
   // 1. key scan (logits, emitted pairs, window logits); with key codes,
   // after the query preparation (and the coding of the newest rows)
@@ -689,6 +695,9 @@ int tsa_workspace_status(void* workspace, int clear, void* stream) {
   if (word & kStatusBadLength)
     return fail(TSA_ERR_DEVICE_CHECK,
                 "a sequence length outside [0, l_cap] was clamped to that range");
+  if (word & kStatusCheck)
+    return fail(TSA_ERR_DEVICE_CHECK,
+                "an internal consistency check of a top-K selection failed (status 0x%x)", word);
   if (word) return fail(TSA_ERR_DEVICE_CHECK, "device status word 0x%x", word);
   return ok();
 }
@@ -1097,6 +1106,7 @@ int retopk_prefill_supports(const void* q_prefill, const tsa_kv* kv, int64_t L0,
   w.spill = reinterpret_cast<uint64_t*>(ws + Lw.spill);
   w.wz = reinterpret_cast<float*>(ws + Lw.wz);
   w.wz_stride = Lw.wz_stride;
+  w.hist16 = reinterpret_cast<uint32_t*>(ws + Lw.hist16);
   const int64_t len0 = L0 - C + 1;
   cudaError_t e;
   {

@@ -10,14 +10,16 @@
 // One thread-block cluster of NC CTAs (NC = 8, 4, 2 or 1, chosen at launch
 // so that all clusters are resident at once, one CTA per SM) per (sequence,
 // query head):
-//   0. every CTA counts the 11-bit bins (top bits of the order-preserving
-//      logit key) of its slice of the head's emitted pairs, the counts are
-//      summed over the cluster (distributed shared memory), and the
-//      threshold bin b* is the largest bin whose suffix count reaches K.  The
-//      scan emitted every pool position whose logit key is >= the head's
-//      emission key, so when that is at least K pairs the K-th largest key
-//      is among them and b* (and the selection below) is exact, even if b*'s
-//      bin was emitted only in part; otherwise the cluster re-scores the
+//   0. the threshold bin b* is the largest bin whose suffix count of the
+//      head's emitted pairs reaches K: from the scan's fine histogram (16 key
+//      bits; every CTA reads it, no exchange), or -- a first call, an
+//      emission key far below the logits -- every CTA counts the 11-bit bins
+//      (top bits of the order-preserving logit key) of its slice of the
+//      pairs and the counts are summed over the cluster (distributed shared
+//      memory).  The scan emitted every pool position whose logit key is >=
+//      the head's emission key, so when that is at least K pairs the K-th
+//      largest key is among them and b* (and the selection below) is exact,
+//      even if b*'s bin was emitted only in part; otherwise the cluster re-scores the
 //      head's keys to count every bin, then re-emits the pool pairs with bin
 //      >= b*, recomputing the logits with the scan's own tensor-core fragment
 //      arithmetic so that every logit -- and so every bin -- is bit-identical
@@ -417,6 +419,16 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   if constexpr (Q8) ekey = q8_exact_key(ekey, __ldcg(a.q8_eps + bh));
   const int path_in = RT ? __ldcg(a.path + bh) : 1;
   const int mc_in = RT ? __ldcg(a.mcand + bh) : 0;
+  // the scan's fine histogram of this head's emitted pairs (plain decode):
+  // thread t holds bins kH16Bins - 1 - kH16Bpt t - r, from the top
+  constexpr int kH16Bpt = kH16Bins / kFinThreads;
+  static_assert(kH16Bins % kFinThreads == 0, "fine bins per thread");
+  const bool fine_in = !RT && !Q8 && a.hist16 != nullptr;
+  uint32_t* hrow = fine_in ? a.hist16 + (int64_t)bh * kH16Bins : nullptr;
+  uint32_t h16[kH16Bpt];
+#pragma unroll
+  for (int r = 0; r < kH16Bpt; ++r)
+    h16[r] = fine_in ? __ldcg(hrow + kH16Bins - 1 - kH16Bpt * tid - r) : 0u;
 
   // A bounded wait of the key scan (this call's, or an earlier one on this
   // workspace: the bit is sticky until the host reads it) gave up: the lists
@@ -437,6 +449,8 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
         a.dense_n[(int64_t)bh * kCtrStride] = 0;
         if (bh == 0) *a.tile_ctr = 0;
       }
+      if (fine_in)
+        for (int q = tid; q < kH16Bins; q += kFinThreads) hrow[q] = 0u;
     }
     return;
   }
@@ -505,10 +519,56 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
     }
     __syncthreads();
   };
+  // b*: with `fine`, a fine bin relative to hb0 (the scan's histogram);
+  // otherwise an 11-bit bin of the logit key (counted here); -1 selects every
+  // pair
   int bstar = -1, redo = 0, ebin = 0;
+  bool fine = false;
+  uint32_t pred_above = 0, pred_cand = 0;  // the histogram's counts above b* and in it
+  const uint32_t hb0 = ekey >> kH16Shift;
   const int used = need > 0 ? (int)(ekey >> kHistShift) : 0;  // the emission key's bin
   const uint32_t tgt[2] = {(uint32_t)need, (uint32_t)need};
-  if (need > 0 && !reuse) {  // (a reuse head has no bins: all its candidates compete)
+  if (need > 0 && !reuse && fine_in) {
+    // The scan counted every emitted pair in its fine bin: b* is the largest
+    // fine bin whose suffix count reaches need, with no pass over the list
+    // and no exchange between the cluster's CTAs.
+    uint32_t mine = 0;
+#pragma unroll
+    for (int r = 0; r < kH16Bpt; ++r) mine += h16[r];
+    if (tid == 0) sh.scal[0] = -1;
+    int tot;
+    uint32_t acc = (uint32_t)fin_scan<W>((int)mine, sh, &tot);
+#pragma unroll
+    for (int r = 0; r < kH16Bpt; ++r) {
+      if (acc < (uint32_t)need && acc + h16[r] >= (uint32_t)need) {
+        sh.scal[0] = kH16Bins - 1 - kH16Bpt * tid - r;
+        sh.scal[1] = (int)acc;
+        sh.scal[2] = (int)h16[r];
+      }
+      acc += h16[r];
+    }
+    __syncthreads();
+    const int fb = sh.scal[0];
+    pred_above = (uint32_t)sh.scal[1];
+    pred_cand = (uint32_t)sh.scal[2];
+    __syncthreads();  // scal is rewritten later
+    fine = false;
+    if (need < P) {
+      if (fb < 0) {  // fewer than K pairs emitted: the re-emission counts 11-bit bins
+        redo = 1;
+      } else if (fb < kH16Bins - 1) {
+        fine = true;
+        bstar = fb;
+      }  // else b* is the last fine bin, which holds everything above it (a first
+         // call, or a far-off emission key): the 11-bit bins are counted below
+    } else {  // every pool position is selected: all of them must have been emitted
+      redo = (int64_t)tot < P;
+      fine = !redo;
+      pred_above = (uint32_t)tot;
+      pred_cand = 0;
+    }
+  }
+  if (need > 0 && !reuse && !fine && !redo) {  // (a reuse head has no bins: all its candidates compete)
     // the bins of this CTA's slice of the emitted pairs (the first batch is
     // in registers), one shared atomic per distinct bin per warp instruction;
     // every emitted pair's bin is >= the emission key's
@@ -575,7 +635,13 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
         v[u] = 0;
         if (pv[u].x != 0xffffffffu) {
           v[u] = rank_key(__uint_as_float(pv[u].y), pv[u].x);
-          const int bin = (int)(v[u] >> kRankShift);
+          int bin;
+          if (fine) {  // (emitted keys are >= the emission key: d >= 0)
+            const int dd = (int)(uint32_t)(v[u] >> (32 + kH16Shift)) - (int)hb0;
+            bin = dd < 0 ? -1 : (dd < kH16Bins ? dd : kH16Bins - 1);
+          } else {
+            bin = (int)(v[u] >> kRankShift);
+          }
           if (bstar < 0 || bin > bstar) selm |= 1u << u;
           else if (bin == bstar) cndm |= 1u << u;
         }
@@ -648,6 +714,13 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   }
   __syncthreads();
   const int nabove = sh.aoff[NC], ncand = sh.coff[NC];
+  // The fine histogram has been read by every CTA of the cluster: clear it
+  // for the next call.  Its counts must equal the classification's.
+  if (fine_in && rank == 0) {
+    for (int q = tid; q < kH16Bins; q += kFinThreads) hrow[q] = 0u;
+    if (fine && tid == 0 && ((uint32_t)nabove != pred_above || (uint32_t)ncand != pred_cand))
+      atomicOr(a.status, kStatusCheck);
+  }
   // Every CTA of the cluster has read the head's list size and key: clear
   // the counters for the next call (the workspace contract).
   if (rank == 0 && tid == 0) {
@@ -700,10 +773,20 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
       cmode = 1;
     } else {
       cmode = 2;
-      // the candidates share b*'s 11 bits (a reuse head's: no known bits)
-      uint64_t prefix = reuse ? 0ull : (uint64_t)bstar << kRankShift;
-      uint64_t mask = reuse ? 0ull : (uint64_t)(kHistBins - 1) << kRankShift;
-      int shift = reuse ? 64 : kRankShift, match = ncand, rem = need_rem;
+      // the candidates share b*'s 11 bits, or its 16 key bits (a reuse
+      // head's, or those of the last fine bin: no known bits)
+      uint64_t prefix = 0ull, mask = 0ull;
+      int shift = 64;
+      if (!reuse && !fine) {
+        prefix = (uint64_t)bstar << kRankShift;
+        mask = (uint64_t)(kHistBins - 1) << kRankShift;
+        shift = kRankShift;
+      } else if (!reuse && bstar < kH16Bins - 1) {
+        prefix = (uint64_t)(hb0 + (uint32_t)bstar) << (32 + kH16Shift);
+        mask = 0xffffull << (32 + kH16Shift);
+        shift = 32 + kH16Shift;
+      }
+      int match = ncand, rem = need_rem;
       while (true) {
         if (match <= rem) {  // everything still matching is selected
           T = prefix;
@@ -1054,7 +1137,9 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
     f = redo ? fminf(2.f * f, 8.f) : fmaxf(1.f, 0.9f * f);
     uint32_t next = 0u;
     if (need < P && bstar >= 0) {
+      const uint32_t fedge = min(hb0 + (uint32_t)bstar, 0xffffu) << kH16Shift;
       const float zref = cmode == 2 ? key2f((uint32_t)(T >> 32))
+                         : fine     ? key2f(fedge)
                                     : key2f((uint32_t)bstar << kHistShift);
       float ze = zref - f * 0.2f * (fabsf(zref) + 1.f);
       if constexpr (Q8) ze = __fsub_rd(ze, __ldcg(a.q8_eps + bh));  // the codes' domain

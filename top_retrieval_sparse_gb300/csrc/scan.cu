@@ -26,13 +26,18 @@
 //     warp bump-allocates runs of 8 slots (one global atomic per run) and
 //     pads the tail of its last run with sentinels -- no logit array is
 //     written or re-read; window logits are written out;
-//   * no histogram is kept here: the finish kernel counts the emitted pairs'
-//     bins itself to find the threshold bin b*, checks that the emission
-//     reached below b* and, when it did not, re-scores the head's keys to
-//     find b* and re-emits: exactness never depends on the hint, only the
-//     cost does.  (A shared-memory histogram of every pool position cost the
-//     consumers as much as the emission: with both, the 128K step's tile
-//     loop was 17 % slower than with either alone.)
+//   * every emitted pair is also counted, with one global reduction, in its
+//     fine bin -- 16 key bits, relative to the emission key -- of the head's
+//     histogram, from which the finish kernel takes the threshold bin b*
+//     without a pass over the pairs; when the emission fell short, or b* is
+//     the histogram's last bin (which holds everything above it), the finish
+//     kernel counts the pairs' 11-bit bins itself or re-scores the head's keys
+//     and re-emits: exactness never depends on the hint, only the cost does.
+//     (A shared-memory histogram of every pool position cost the consumers as
+//     much as the emission; counting only the emitted pairs, ~5 % of the
+//     rows, costs nothing measurable);
+//   * a plain scan of every head loads its first unit's query fragments, an
+//     input of the call, before the dependency wait.
 #include "tsa_internal.cuh"
 #include "tsa_kernels.h"
 
@@ -250,9 +255,9 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
 
   // ============================ consumer warps ================================
   // Launched as a programmatic dependent, the scan streams keys while the
-  // previous kernel finishes; its consumers read hints and write counters,
-  // pairs and logits only after that kernel has completed.
-  pdl_wait();
+  // previous kernel finishes; its consumers read the query fragments of their
+  // first unit (inputs of the call) before the dependency wait, and hints,
+  // counters, pairs and logits only after that kernel has completed.
   const int gr = lane >> 2;  // A rows gr, gr+8 / B column (query head) gr
   const int tq = lane & 3;   // k-slot group / C columns 2tq, 2tq+1
 
@@ -264,6 +269,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
   // emission thresholds of heads 2tq, 2tq+1 as floats: z >= thr exactly when
   // f2key(z) >= the head's key (-inf: every logit; NaN: an inactive head)
   float ethr[2] = {__int_as_float(0x7fc00000), __int_as_float(0x7fc00000)};
+  uint32_t hbase[2] = {0u, 0u};  // fine-histogram base bins (emission key >> 16)
   bool lane_on = false;         // lane h < G: head h takes part (run owner)
   int run_ptr = 0;              // lane h < G: next free slot of this warp's run for head h
   int run_left = 0;             //            slots left in that run
@@ -282,6 +288,58 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
     run_ptr = 0;
     run_left = 0;
   };
+  // entering a unit (each warp on its own: no barrier): what depends only on
+  // the call's inputs -- heads, length, query fragments ...
+  auto enter_inputs = [&](int unit) {
+    cur_unit = unit;
+    unit_end = unit_tiles[unit + 1];
+    cur_b = unit / a.kv.Hkv;
+    cur_g = unit % a.kv.Hkv;
+    head0 = cur_b * a.Hq + cur_g * G;
+    cur_L = seq_len(a.lens, a.len_host, a.len_step, cur_b, a.kv.l_cap);  // < 2^31
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int hl = 2 * tq + e;
+      on[e] = hl < G && (!a.head_active || a.head_active[head0 + hl] == a.active_value);
+    }
+    lane_on = lane < G && (!a.head_active || a.head_active[head0 + lane] == a.active_value);
+    if constexpr (Q8) {
+      const uint16_t* qp = a.qh + ((int64_t)head0 + (gr < G ? gr : 0)) * kD;
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {  // p: dims 16 tq + 8p (p < 2), 64 + 16 tq + 8 (p - 2)
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (gr < G) w = __ldcg(reinterpret_cast<const uint4*>(qp + 64 * (p >> 1) + 16 * tq +
+                                                              8 * (p & 1)));
+        qb[p][0] = w.x; qb[p][1] = w.y; qb[p][2] = w.z; qb[p][3] = w.w;
+      }
+    } else {
+      const uint16_t* qp = a.q + ((int64_t)head0 + (gr < G ? gr : 0)) * kD;
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (gr < G) w = *reinterpret_cast<const uint4*>(qp + 8 * (4 * p + tq));
+        qb[p][0] = w.x; qb[p][1] = w.y; qb[p][2] = w.z; qb[p][3] = w.w;
+      }
+    }
+  };
+  // ... and what the previous kernel wrote: the emission keys (and the
+  // codes' logit factors)
+  auto enter_state = [&]() {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int bh = head0 + 2 * tq + e;
+      const uint32_t ek = on[e] ? __ldcg(a.emit_key + bh) : 0u;
+      // keys at or below f2key(-inf) admit every finite logit
+      ethr[e] = !on[e] ? __int_as_float(0x7fc00000) : ek <= 0x007fffffu ? -INFINITY : key2f(ek);
+      hbase[e] = ek >> kH16Shift;
+      if constexpr (Q8) qts[e] = on[e] ? __ldcg(a.qts + bh) : 0.f;
+    }
+  };
+  // a plain scan of every head reads its first unit's query before the wait
+  const bool early = !Q8 && !a.head_active && t_begin < t_end;
+  if (early) enter_inputs(locate(t_begin));
+  pdl_wait();
+  if (early) enter_state();
   for (int j = 0;; ++j) {
     const int s = j % kStages;
     if (!mbar_wait_or_abort(&full[s], (uint32_t)((j / kStages) & 1), &s_abort, lim)) {
@@ -291,44 +349,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
     }
     const int t = stage_tile[s];  // written by the producer before it armed the stage
     if (t < 0) break;             // no more tiles (same stage, same j, for every warp)
-    if (t >= unit_end) {  // entering a new unit (each warp on its own: no barrier)
+    if (t >= unit_end) {  // entering a new unit
       const int unit = locate(t);
       if (cur_unit >= 0) close_runs();
-      cur_unit = unit;
-      unit_end = unit_tiles[unit + 1];
-      cur_b = unit / a.kv.Hkv;
-      cur_g = unit % a.kv.Hkv;
-      head0 = cur_b * a.Hq + cur_g * G;
-      cur_L = seq_len(a.lens, a.len_host, a.len_step, cur_b, a.kv.l_cap);  // < 2^31
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int hl = 2 * tq + e;
-        const int bh = head0 + hl;
-        on[e] = hl < G && (!a.head_active || a.head_active[bh] == a.active_value);
-        const uint32_t ek = on[e] ? __ldcg(a.emit_key + bh) : 0u;
-        // keys at or below f2key(-inf) admit every finite logit
-        ethr[e] = !on[e] ? __int_as_float(0x7fc00000) : ek <= 0x007fffffu ? -INFINITY : key2f(ek);
-        if constexpr (Q8) qts[e] = on[e] ? __ldcg(a.qts + bh) : 0.f;
-      }
-      lane_on = lane < G && (!a.head_active || a.head_active[head0 + lane] == a.active_value);
-      if constexpr (Q8) {
-        const uint16_t* qp = a.qh + ((int64_t)head0 + (gr < G ? gr : 0)) * kD;
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {  // p: dims 16 tq + 8p (p < 2), 64 + 16 tq + 8 (p - 2)
-          uint4 w = make_uint4(0u, 0u, 0u, 0u);
-          if (gr < G) w = __ldcg(reinterpret_cast<const uint4*>(qp + 64 * (p >> 1) + 16 * tq +
-                                                                8 * (p & 1)));
-          qb[p][0] = w.x; qb[p][1] = w.y; qb[p][2] = w.z; qb[p][3] = w.w;
-        }
-      } else {
-        const uint16_t* qp = a.q + ((int64_t)head0 + (gr < G ? gr : 0)) * kD;
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          uint4 w = make_uint4(0u, 0u, 0u, 0u);
-          if (gr < G) w = *reinterpret_cast<const uint4*>(qp + 8 * (4 * p + tq));
-          qb[p][0] = w.x; qb[p][1] = w.y; qb[p][2] = w.z; qb[p][3] = w.w;
-        }
-      }
+      enter_inputs(unit);
+      enter_state();
     }
     const int tile = t - unit_tiles[cur_unit];
     if (j == 0) trace.mark(1);
@@ -458,6 +483,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
             const int slot = r < qt ? q1 + r : q2 + (r - qt);
             if (slot < a.dense_stride)
               drow[slot] = make_uint2((uint32_t)(rowA + 8 * hi), __float_as_uint(zv[e]));
+            if constexpr (!Q8) {
+              if (a.hist16) {  // (the key is >= the emission key: the bin is >= 0)
+                const uint32_t fb =
+                    min((f2key(zv[e]) >> kH16Shift) - hbase[par], (uint32_t)kH16Bins - 1u);
+                atomicAdd(a.hist16 + (int64_t)(head0 + src) * kH16Bins + fb, 1u);
+              }
+            }
           }
         }
       }

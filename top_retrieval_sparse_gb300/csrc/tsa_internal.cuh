@@ -22,6 +22,12 @@ constexpr int kMaxUnits = 512;                  // B * Hkv limit of one call
 // slot atomics of all heads then spread over the L2 slices instead of
 // queueing in one.
 constexpr int kCtrStride = 32;
+// Fine per-head histogram of the emitted pairs (plain key scan): bin of a
+// pair = (its logit key >> 16) minus (the emission key >> 16), the last bin
+// also holding everything above it.  16 key bits resolve a logit to 1/128 of
+// its binade, so the threshold bin holds a few dozen pairs, not thousands.
+constexpr int kH16Bins = 1024;
+constexpr int kH16Shift = 16;
 constexpr long long kWaitLimitNs = 1000000000;  // bounded waits: 1 s
 
 
@@ -29,6 +35,7 @@ constexpr long long kWaitLimitNs = 1000000000;  // bounded waits: 1 s
 // host clears them, through tsa_workspace_status).
 constexpr int kStatusTimeout = 1;    // a bounded wait expired: the call's outputs are NaN
 constexpr int kStatusBadLength = 2;  // a sequence length outside [0, l_cap] was clamped
+constexpr int kStatusCheck = 4;      // an internal consistency check of a selection failed
 
 // ---------------------------------------------------------------- encoding
 // Order-preserving key of an fp32 value: a > b  <=>  key(a) > key(b).

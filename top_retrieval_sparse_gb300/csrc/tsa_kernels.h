@@ -39,6 +39,10 @@ struct ScanArgs {
   float* wz;                 // [B][Hq][wz_stride] window logits
   int wz_stride;
   int* status;
+  // Plain scan only (nullptr: none): [B][Hq][kH16Bins], zero before the
+  // call (the finish kernel clears it); every emitted pair is counted in its
+  // fine bin.
+  uint32_t* hist16;
   // Bounded waits give up after wait_ns (0: the default limit).  Fault
   // injection for tests of the error path: with stall_first_copy set, CTA 0
   // never issues the copy of its first tile, so that its consumers' wait
@@ -145,6 +149,9 @@ struct FinishArgs {
   int32_t* dense_n;
   int64_t dense_stride;
   uint64_t* spill;           // [B][Hq][dense_stride] candidates past shared memory
+  // The scan's fine histogram of the emitted pairs (plain decode; nullptr:
+  // the finish counts the pairs' 11-bit bins itself); cleared here.
+  uint32_t* hist16;
   const float* wz;           // window logits [B][Hq][wz_stride]
   int wz_stride;
   float* out;                // [B][Hq][128]
