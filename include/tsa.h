@@ -192,7 +192,7 @@ TSA_API int sparse_attn_decode(const void* q, const tsa_kv* kv, const int32_t* l
  * Same arguments and results as sparse_attn_decode, minus the workspace.
  *   - Problems whose tsa_decode_workspace_size() exceeds the array are
  *     rejected with TSA_ERR_WORKSPACE (nothing launched).  The size grows as
- *     B*Hq*16*(l_cap + 65536) bytes plus 8 KiB per head: B*Hq = 4 fits
+ *     B*Hq*16*(l_cap + 65536) bytes plus 12 KiB per head: B*Hq = 4 fits
  *     caches up to about 458 K positions, B*Hq = 16 about 65 K, and
  *     B*Hq >= 32 fits none.
  *   - The arguments are checked as in sparse_attn_decode before the array

@@ -189,7 +189,7 @@ def test_noalloc_validates_before_touching_the_device(lib, kw):
 
 
 def test_noalloc_size_limit_boundaries(lib):
-    """The scratch need grows as B*Hq*16*(l_cap + 65536) bytes plus ~8 KiB per
+    """The scratch need grows as B*Hq*16*(l_cap + 65536) bytes plus ~12 KiB per
     head: B*Hq = 4 fits up to about 458 K positions, B*Hq = 16 about 65 K, and
     B*Hq = 32 fits no cache at all; an oversize problem is refused (-2) before
     any CUDA call."""
