@@ -55,6 +55,16 @@ constexpr int kMyCap = 4096;    // this CTA's threshold-bin candidates in shared
 constexpr int kAllCap = 16384;  // the cluster's threshold-bin candidates, copied locally (NC > 1)
 constexpr int kPtabCap = 8192;  // pages of one sequence held in shared memory (single-CTA heads)
 constexpr int kFinU = 8;        // pairs per thread per batch
+// Rows a warp gathers (or rescores) at a time: lane l < rows holds row l and
+// every lane keeps rows / 2 16-byte loads in registers.  32 rows held 64
+// registers of loads and made the kernel spill, which serialised the loads;
+// 24 fit the clustered decode instantiations, 16 the ReTopK ones and the
+// single-CTA heads (whose page table in shared memory takes registers).
+template <bool RT, int NC>
+struct GatherRows {
+  static constexpr int value = RT || NC == 1 ? 16 : 24;
+};
+constexpr int kRescoreRows = 16;
 constexpr int kRankShift = 64 - kHistBits;  // b* = the rank key's top 11 bits
 constexpr float kFinLog2e = 1.4426950408889634f;
 constexpr float kFinLn2 = 0.6931471805599453f;
@@ -231,10 +241,10 @@ __device__ void rescore_count(const FinishArgs& a, int b, int h, int g, int G, i
 
 // A given candidate set's logits (a ReTopK reuse head's A_t, or attend_set's
 // rows) on candidates [c0, c1), as rank keys into this CTA's candidate list
-// (shared memory, then the top of the slice's spill area).  A warp takes 32
-// candidates at a time: lane l holds candidate base + l's position; key rows
-// are read by half-warps (16 lanes x 16 bytes), two rows per load, all 16
-// loads in flight before any is used.  A position at or past L is never read:
+// (shared memory, then the top of the slice's spill area).  A warp takes
+// kRescoreRows candidates at a time: lane l < kRescoreRows holds candidate
+// base + l's position; key rows are read by half-warps (16 lanes x 16
+// bytes), two rows per load, all loads in flight before any is used.  A position at or past L is never read:
 // its logit is -inf (it is not attended) and the status word flags it.
 template <int W, class Sh>
 __device__ void reuse_logits(const FinishArgs& a, int b, int bh, int g, int64_t c0, int64_t c1,
@@ -245,14 +255,14 @@ __device__ void reuse_logits(const FinishArgs& a, int b, int bh, int g, int64_t 
   const float qv[8] = {bf_lo(qw.x), bf_hi(qw.x), bf_lo(qw.y), bf_hi(qw.y),
                        bf_lo(qw.z), bf_hi(qw.z), bf_lo(qw.w), bf_hi(qw.w)};
   const uint32_t* crow = a.cand + (int64_t)bh * a.cand_cap;
-  for (int64_t base = c0 + 32 * wid; base < c1; base += 32 * W) {
-    const int64_t j = base + lane;
+  for (int64_t base = c0 + kRescoreRows * wid; base < c1; base += kRescoreRows * W) {
+    const int64_t j = lane < kRescoreRows ? base + lane : c1;
     const uint32_t pos = j < c1 ? crow[j] : 0u;
     const bool inside = (int64_t)pos < L;
     if (__any_sync(0xffffffffu, j < c1 && !inside) && lane == 0) atomicOr(a.status, kStatusBadLength);
-    uint4 kv4[16];
+    uint4 kv4[kRescoreRows / 2];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
+    for (int k = 0; k < kRescoreRows / 2; ++k) {
       const int r = 2 * k + half;
       const uint32_t pk = __shfl_sync(0xffffffffu, pos, r);
       kv4[k] = base + r < c1 && (int64_t)pk < L
@@ -261,7 +271,7 @@ __device__ void reuse_logits(const FinishArgs& a, int b, int bh, int g, int64_t 
     }
     float mine = 0.f;  // lane l ends with the logit of candidate base + l
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
+    for (int k = 0; k < kRescoreRows / 2; ++k) {
       const uint4 w = kv4[k];
       float acc = qv[0] * bf_lo(w.x);
       acc = fmaf(qv[1], bf_hi(w.x), acc);
@@ -858,10 +868,12 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   const int w1 = c0r + (int)((int64_t)(c1r - c0r) * (wid + 1) / kFinWarps);
   const uint16_t* vbase = a.kv.page_table ? a.kv.v : a.kv.v + kv_row(a.kv, b, g, 0);
   const float* wzrow = a.wz + (int64_t)bh * a.wz_stride;
-  // 32 rows per warp at a time: lane l holds row base + l's position and
-  // logit; V rows are read by half-warps (16 lanes x 16 bytes = one row), so
-  // load k brings rows base + 2k (lanes 0-15) and base + 2k + 1 (lanes
-  // 16-31), and each lane accumulates 8 columns, 8 * (lane % 16) onwards.
+  constexpr int kGatherRows = GatherRows<RT, NC>::value;
+  // kGatherRows rows per warp at a time: lane l < kGatherRows holds row
+  // base + l's position and logit; V rows are read by half-warps (16 lanes x
+  // 16 bytes = one row), so load k brings rows base + 2k (lanes 0-15) and
+  // base + 2k + 1 (lanes 16-31), and each lane accumulates 8 columns,
+  // 8 * (lane % 16) onwards.
   const int half = lane >> 4, col = 8 * (lane & 15);
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
   float o[2][8];
@@ -910,15 +922,15 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   float nz;
   int npos, nset;
   bool nlv;
-  row_meta(w0 + lane, npos, nz, nset, nlv);
-  for (int base = w0; base < w1; base += 32) {
+  row_meta(lane < kGatherRows ? w0 + lane : w1, npos, nz, nset, nlv);
+  for (int base = w0; base < w1; base += kGatherRows) {
     const float z0 = nz;
     const int pos = npos, set = nset;
     const bool lv = nlv;
     const int j = base + lane;
     // the next batch's row: fetch its description now and start its V row
     // towards L2, so that the next batch's loads find it there
-    row_meta(base + 32 + lane, npos, nz, nset, nlv);
+    row_meta(lane < kGatherRows ? base + kGatherRows + lane : w1, npos, nz, nset, nlv);
     if (nlv) {
       const uint16_t* vr =
           a.kv.page_table ? a.kv.v + row_off(npos) : vbase + (int64_t)npos * kD;
@@ -928,9 +940,9 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
     float z = z0;
     const unsigned live = __ballot_sync(0xffffffffu, lv);
     const unsigned sel1 = __ballot_sync(0xffffffffu, set == 1);
-    uint4 vv[16];
+    uint4 vv[kGatherRows / 2];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
+    for (int k = 0; k < kGatherRows / 2; ++k) {
       const int r = 2 * k + half;
       const int pk = __shfl_sync(0xffffffffu, pos, r);
       const uint16_t* vr =
@@ -956,7 +968,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
     l[0] += warp_sum(set == 0 ? p : 0.f);
     l[1] += warp_sum(set == 1 ? p : 0.f);
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
+    for (int k = 0; k < kGatherRows / 2; ++k) {
       if (!((live >> (2 * k)) & 3u)) continue;  // warp-uniform: both rows absent
       const int r = 2 * k + half;
       const float pr = __shfl_sync(0xffffffffu, p, r);  // 0 for an absent row

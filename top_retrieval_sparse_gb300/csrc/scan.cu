@@ -84,19 +84,23 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(ScanArgs a) {
   const int nunits = a.B * a.kv.Hkv;
 
   // ---- prefix of tiles over (sequence, KV head) units with an active head ----
+  // With an activity filter the block first marks the units with an active
+  // head (every head's flag read at once, one thread each).
+  if (a.head_active) {
+    for (int u = tid; u < nunits; u += kScanThreads) unit_tiles[u] = 0;
+    __syncthreads();
+    for (int i = tid; i < nunits * G; i += kScanThreads)
+      if (a.head_active[i] == a.active_value) unit_tiles[i / G] = 1;
+    __syncthreads();
+  }
   if (tid < 32) {
     int run = 0;
     for (int base = 0; base < nunits; base += 32) {
       const int u = base + tid;
       int tiles = 0;
       if (u < nunits) {
-        const int b = u / a.kv.Hkv, g = u % a.kv.Hkv;
-        bool act = true;
-        if (a.head_active) {
-          act = false;
-          for (int j = 0; j < G; ++j)
-            act |= a.head_active[b * a.Hq + g * G + j] == a.active_value;
-        }
+        const int b = u / a.kv.Hkv;
+        const bool act = !a.head_active || unit_tiles[u] != 0;
         const int64_t L = seq_len(a.lens, a.len_host, a.len_step, b, a.kv.l_cap);
         tiles = act ? (int)((L + kTileRows - 1) / kTileRows) : 0;
       }
