@@ -246,9 +246,9 @@ __device__ void rescore_count(const FinishArgs& a, int b, int h, int g, int G, i
 // base + l's position; key rows are read by half-warps (16 lanes x 16
 // bytes), two rows per load, all loads in flight before any is used.  A position at or past L is never read:
 // its logit is -inf (it is not attended) and the status word flags it.
-template <int W, class Sh>
+template <int W, int NC, class Sh>
 __device__ void reuse_logits(const FinishArgs& a, int b, int bh, int g, int64_t c0, int64_t c1,
-                             int64_t L, Sh& sh, uint64_t* spill) {
+                             int64_t L, Sh& sh, uint64_t* spill, bool push) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int half = lane >> 4, col = 8 * (lane & 15);
   const uint4 qw = *reinterpret_cast<const uint4*>(a.q + (int64_t)bh * kD + col);
@@ -290,6 +290,13 @@ __device__ void reuse_logits(const FinishArgs& a, int b, int bh, int g, int64_t 
     }
     if (j < c1) {
       const uint64_t v = rank_key(inside ? mine * a.scale : -INFINITY, pos);
+      if constexpr (NC > 1) {
+        if (push) {  // candidate j of every CTA's copy of the cluster's candidates
+#pragma unroll
+          for (int c = 0; c < NC; ++c) st_dsmem_u64(&sh.cand[j], (uint32_t)c, v);
+          continue;
+        }
+      }
       const int64_t i = j - c0;
       if (i < kMyCap) sh.mycand[i] = v;
       else spill[c1 - 1 - (i - kMyCap)] = v;
@@ -429,6 +436,10 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   if constexpr (Q8) ekey = q8_exact_key(ekey, __ldcg(a.q8_eps + bh));
   const int path_in = RT ? __ldcg(a.path + bh) : 1;
   const int mc_in = RT ? __ldcg(a.mcand + bh) : 0;
+  // A reuse head's CTAs store its rescored candidates into each other's
+  // shared memory before their first cluster barrier: every CTA of the
+  // cluster must have started (the wait is below, after the first loads).
+  if constexpr (RT && NC > 1) cluster_arrive_relaxed();
   // the scan's fine histogram of this head's emitted pairs (plain decode):
   // thread t holds bins kH16Bins - 1 - kH16Bpt t - r, from the top
   constexpr int kH16Bpt = kH16Bins / kFinThreads;
@@ -439,6 +450,8 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
 #pragma unroll
   for (int r = 0; r < kH16Bpt; ++r)
     h16[r] = fine_in ? __ldcg(hrow + kH16Bins - 1 - kH16Bpt * tid - r) : 0u;
+
+  if constexpr (RT && NC > 1) cluster_wait();
 
   // A bounded wait of the key scan (this call's, or an earlier one on this
   // workspace: the bit is sticky until the host reads it) gave up: the lists
@@ -675,11 +688,15 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
       nmc += tot & 0xffff;
     }
   }
+  // A reuse head whose A_t fits the cluster's candidate copy: every CTA
+  // stores its share's keys at their A_t index into every CTA's copy before
+  // the cluster barrier, so nothing is exchanged after it.
+  const bool rpush = NC > 1 && reuse && mcand <= kAllCap;
   if (need > 0 && reuse) {  // this CTA's share of A_t, rescored: every one a candidate
     n = mcand;  // the candidate index space (spill layout as for a list slice)
     s0 = n * rank / NC;
     s1 = n * (rank + 1) / NC;
-    reuse_logits<W>(a, b, bh, g, s0, s1, L, sh, spill);
+    reuse_logits<W, NC>(a, b, bh, g, s0, s1, L, sh, spill, rpush);
     nmc = (int)(s1 - s0);
     __syncthreads();
   }
@@ -703,7 +720,9 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   }
   if (wid == 0) {
     int ca = 0, cc = 0;
-    if (lane < NC) {
+    if (lane < NC && rpush) {  // no pairs; each CTA's share of A_t
+      cc = (int)((int64_t)mcand * (lane + 1) / NC - (int64_t)mcand * lane / NC);
+    } else if (lane < NC) {
       ca = (int)ld_dsmem_u32(reinterpret_cast<const uint32_t*>(&sh.cnt[0]), lane);
       cc = (int)ld_dsmem_u32(reinterpret_cast<const uint32_t*>(&sh.cnt[1]), lane);
     }
@@ -749,7 +768,7 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   };
   if constexpr (NC > 1) {  // eight remote loads in flight per thread before any is stored
     constexpr int kCopyU = 8;
-    const int lim = ncand < kAllCap ? ncand : kAllCap;
+    const int lim = rpush ? 0 : ncand < kAllCap ? ncand : kAllCap;
     for (int jb = 0; jb < lim; jb += kFinThreads * kCopyU) {
       uint64_t v[kCopyU];
 #pragma unroll
