@@ -409,16 +409,10 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
     }
     return kv_row(a.kv, b, g, i);
   };
-  {  // the V rows of this CTA's share of the window do not depend on the scan:
-     // start bringing them into L2 while it finishes
-    const int64_t L = seq_len(a.lens, a.len_host, a.len_step, b, a.kv.l_cap);
-    const int64_t nw = window_count(L, a.n_init, a.n_recent);
-    for (int64_t j = nw * rank / NC + tid; j < nw * (rank + 1) / NC; j += kFinThreads) {
-      const uint16_t* vr = a.kv.v + row_off(window_pos(j, L, a.n_init, a.n_recent));
-      prefetch_l2(vr);
-      prefetch_l2(vr + kD / 2);
-    }
-  }
+  // (No V row is prefetched into L2 anywhere in this kernel: the window's
+  // rows before the dependency wait, the selected rows once classified and
+  // each gather batch's successor were each measured slower than the plain
+  // loads -- 128K step 56.4 -> 55.4 us without all three.)
   pdl_wait();     // pairs and window logits come from the scan
   pdl_trigger();  // the next kernel may be scheduled (it writes nothing
                   // this kernel reads until this kernel has completed)
@@ -706,18 +700,6 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
   }
   phases.mark(2);
   cluster_sync_all();  // every CTA's lists and counts are complete
-  {  // this CTA's above-b* rows are selected: start bringing their V rows into
-     // L2 while the cluster settles the threshold (after the barrier: the
-     // list entries of other threads are complete)
-    const uint16_t* vb = a.kv.page_table ? a.kv.v : a.kv.v + kv_row(a.kv, b, g, 0);
-    for (int li = tid; li < nmy && li < kSelCap; li += kFinThreads) {
-      const int64_t pk = sh.sel[li].x;
-      if (pk >= L) continue;
-      const uint16_t* vr = a.kv.page_table ? a.kv.v + row_off(pk) : vb + pk * kD;
-      prefetch_l2(vr);
-      prefetch_l2(vr + kD / 2);
-    }
-  }
   if (wid == 0) {
     int ca = 0, cc = 0;
     if (lane < NC && rpush) {  // no pairs; each CTA's share of A_t
@@ -947,15 +929,8 @@ __global__ void __launch_bounds__(32 * W, 16 / W) finish_kernel(FinishArgs a) {
     const int pos = npos, set = nset;
     const bool lv = nlv;
     const int j = base + lane;
-    // the next batch's row: fetch its description now and start its V row
-    // towards L2, so that the next batch's loads find it there
+    // the next batch's row: fetch its description now
     row_meta(lane < kGatherRows ? base + kGatherRows + lane : w1, npos, nz, nset, nlv);
-    if (nlv) {
-      const uint16_t* vr =
-          a.kv.page_table ? a.kv.v + row_off(npos) : vbase + (int64_t)npos * kD;
-      prefetch_l2(vr);
-      prefetch_l2(vr + kD / 2);
-    }
     float z = z0;
     const unsigned live = __ballot_sync(0xffffffffu, lv);
     const unsigned sel1 = __ballot_sync(0xffffffffu, set == 1);

@@ -261,10 +261,6 @@ __device__ __forceinline__ uint32_t q8_exact_key(uint32_t khat, float eps) {
   return kz == kz ? f2key(kz) : 0xffffffffu;
 }
 
-// Hint that the line holding p will be read soon (fetched into L2).
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
 
 // ------------------------------------------------------------- clusters
 // Full barrier over the thread-block cluster (release / acquire: shared and
