@@ -1202,9 +1202,11 @@ static cudaError_t launch_finish_t(const FinishArgs& a, cudaStream_t st) {
 // 16 warps per SM: 512 threads x 128 registers) fill at most 85 % of the SMs.
 // A cluster must sit in one GPC, so a nearly full device places fewer large
 // clusters than its SM count suggests: 32 clusters of 8 CTAs at two per SM
-// left two clusters for a second wave.  With more heads than that every head
-// is one CTA of 16 warps (two CTAs of 8 warps per SM were measured slower:
-// the gather is bound by each warp's rows in flight).
+// left two clusters for a second wave.  With more heads than that every
+// decode head is one CTA of 8 warps, two per SM (one CTA of 16 warps per head
+// was measured 7 us slower on 16 paged sequences of 32 heads), and every
+// ReTopK head one CTA of 16 warps (8 warps: 4 sequences' batched step 35.3 ->
+// 40.2 us).
 cudaError_t launch_finish(const FinishArgs& a, cudaStream_t st) {
   static int sms[64] = {0};
   int dev = 0;
@@ -1231,14 +1233,14 @@ cudaError_t launch_finish(const FinishArgs& a, cudaStream_t st) {
       case 8: return launch_finish_t<8, 16, false, true>(a, st);
       case 4: return launch_finish_t<4, 16, false, true>(a, st);
       case 2: return launch_finish_t<2, 16, false, true>(a, st);
-      default: return launch_finish_t<1, 16, false, true>(a, st);
+      default: return launch_finish_t<1, 8, false, true>(a, st);
     }
   }
   switch (nc) {
     case 8: return launch_finish_t<8, 16, false>(a, st);
     case 4: return launch_finish_t<4, 16, false>(a, st);
     case 2: return launch_finish_t<2, 16, false>(a, st);
-    default: return launch_finish_t<1, 16, false>(a, st);
+    default: return launch_finish_t<1, 8, false>(a, st);
   }
 }
 
