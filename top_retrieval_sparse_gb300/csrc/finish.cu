@@ -7,9 +7,9 @@
 // (o_W and o_Omega over disjoint W and Omega, each with its local max) and
 // Eq. 4-5 (o_t = g1 o_W + g2 o_Omega).
 //
-// One thread-block cluster of NC CTAs (NC = 8, 4, 2 or 1, chosen at launch
-// so that all clusters are resident at once, one CTA per SM) per (sequence,
-// query head):
+// One thread-block cluster of NC CTAs (NC = 8, 4 or 2, chosen at launch so
+// that all clusters are resident at once, one CTA per SM; with more heads one
+// CTA per head) per (sequence, query head):
 //   0. the threshold bin b* is the largest bin whose suffix count of the
 //      head's emitted pairs reaches K: from the scan's fine histogram (16 key
 //      bits; every CTA reads it, no exchange), or -- a first call, an
@@ -34,15 +34,16 @@
 //      logit key, then ~position, so ties go to the smaller position);
 //   3. the selected rows (window, above-b* pairs, selected candidates) are
 //      split evenly over the cluster; each warp gathers V for its rows with
-//      half-warp 16-byte loads, keeping (max, sum, o) per set in base 2;
+//      half-warp 16-byte loads, a spill-free batch of rows at a time,
+//      keeping (max, sum, o) per set in base 2;
 //      every CTA pushes its partials into rank 0's shared memory, and rank
 //      0 applies Eq. 4-5 and stores the next call's emission key (the K-th
 //      logit minus a margin).
 // ReTopK steps use the same kernel: a reuse head has no pair list; each CTA
 // rescores its share of the head's candidates A_t (exact logits e_i on the
-// key rows) and all of them compete in the radix (no bins, no emission key); no
-// head has a window, and rank 0 pushes (qbar_t, S_t) into the query-support
-// FIFO.
+// key rows), stores the keys into every CTA of the cluster, and all of them
+// compete in the radix (no bins, no emission key); no head has a window, and
+// rank 0 pushes (qbar_t, S_t) into the query-support FIFO.
 // Launched as a programmatic dependent of the kernel that wrote the lists.
 #include "tsa_internal.cuh"
 #include "tsa_kernels.h"
