@@ -151,6 +151,15 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
     a.seq_ws[b] = sq;
   }
   if (tid < kD) a.qbar_new[(int64_t)bh * kD + tid] = qs[tid];
+  // the fresh entry's support size and first kSelectorThreads entries,
+  // requested with its query: the newest query is usually the most similar,
+  // and its support is then part of the union
+  int fsn = 0;
+  int32_t fsup0 = -1;
+  if (fresh >= 0) {
+    fsn = cache_sup_n[(int64_t)h * a.C + fresh];
+    if (tid < a.K) fsup0 = cache_sup[((int64_t)h * a.C + fresh) * a.K + tid];
+  }
   if (fresh >= 0) cosine(true);
   __syncthreads();
 
@@ -208,11 +217,9 @@ __global__ void __launch_bounds__(kSelectorThreads) retopk_selector_kernel(Retop
     const int r = j / a.K, i = j - r * a.K;  // past the prefetched entries
     if (i < stab_n[r]) mark(cache_sup[((int64_t)h * a.C + stab[r]) * a.K + i]);
   }
-  if (fin) {
-    const int nf = cache_sup_n[(int64_t)h * a.C + fresh];
-    for (int i = tid; i < nf && i < a.K; i += kSelectorThreads)
-      mark(cache_sup[((int64_t)h * a.C + fresh) * a.K + i]);
-  }
+  if (fin)
+    for (int i = tid; i < fsn && i < a.K; i += kSelectorThreads)
+      mark(i == tid ? fsup0 : cache_sup[((int64_t)h * a.C + fresh) * a.K + i]);
   const int64_t lo = L - a.W > 0 ? L - a.W : 0;
   for (int64_t p = lo + tid; p < L; p += kSelectorThreads) mark((int32_t)p);
   __syncthreads();
